@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the virtual-rank AllReduce algorithms on one GB300.
+
+Workload (the AllReduce algorithm sweep): N = 8 virtual ranks, fp32 sum,
+inputs uniform[-1, 1).  One step = one AllReduce of 256 MiB per rank with each
+of Ring, Recursive Halving-Doubling, Double Binary Tree and the fused one-pass
+kernel (out of place, each algorithm into its own output buffers).
+
+value = busbw of the step: sum over the four AllReduces of
+M * 2(N-1)/N, divided by the step time (GB/s, 1e9 B/s).  Inputs (2 GiB per
+buffer set) are larger than the 129 MB L2, so no flush is needed between
+steps.  The JSON line also carries per-algorithm busbw and HBM fractions at
+256 MiB, the busbw-vs-message-size sweep (1 KiB .. 256 MiB per rank), the
+roofline of the dominant kernel from the library's live launch trace, sampled
+clocks, an end-to-end number through host buffers, and the oracle's CPU time.
+
+Multi-GPU: replicas only (every GPU runs the same workload on its own
+buffers; nothing crosses GPUs); value = all ranks' bytes / the slowest rank.
+
+``--impl reference`` times the CPU oracle (oracle/) on the host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "busbw GB/s vs message size per algo (N virtual ranks); % of HBM roofline"
+WORKLOAD = "allreduce_sweep_n8_f32"
+NVR = 8
+BYTES_PER_RANK = 256 << 20
+ALGOS = ["ring", "rhd", "dbt", "fused"]
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ----------------------------------------------------------------------------
+# helpers shared by both arms (and by the multi-rank tests)
+# ----------------------------------------------------------------------------
+
+def busbw_factor(N: int) -> float:
+    return 2.0 * (N - 1) / N
+
+
+def step_bus_bytes(bytes_per_rank: int, nalgos: int = len(ALGOS), N: int = NVR) -> float:
+    return nalgos * bytes_per_rank * busbw_factor(N)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max over ranks (one scalar, host-side timing only)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "collective_communication_algorithms_virtual_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary is absent or was taken on different kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.path = None
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="vc_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        self.out = open(self.path, "w")
+        self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(self.NAMES, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host: CPU baseline and reference arm
+# ----------------------------------------------------------------------------
+
+def oracle_step(xs) -> None:
+    from oracle import schedules
+
+    for algo in ALGOS:
+        schedules.allreduce(xs, algo, "f32")
+
+
+def oracle_inputs(mib_per_rank: float):
+    from synthetic_inputs import uniform_pm1_f32
+
+    count = max(4, int(mib_per_rank * (1 << 20)) // 4)
+    return [uniform_pm1_f32(2, r, count) for r in range(NVR)], count * 4
+
+
+def time_oracle(target_s: float = 15.0, mib: float | None = None) -> dict:
+    """The oracle, as it stands, on a bounded sample of the workload."""
+    if mib is None:
+        xs, _ = oracle_inputs(1)
+        t0 = time.perf_counter()
+        oracle_step(xs)
+        t1 = time.perf_counter() - t0
+        mib = max(1, min(64, int(target_s / 3 / max(t1, 1e-3))))
+    xs, nbytes = oracle_inputs(mib)
+    reps, total, t_start = 0, 0.0, time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle_step(xs)
+        total += time.perf_counter() - t0
+        reps += 1
+        if time.perf_counter() - t_start >= target_s or reps >= 50:
+            break
+    busbw = step_bus_bytes(nbytes) * reps / total / 1e9
+    return {"value": busbw, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"N={NVR} fp32 AllReduce ring+rhd+dbt+fused at {nbytes >> 20} MiB per rank, "
+                       f"{reps} step(s), {total:.1f} s, single-threaded numpy on a host with "
+                       f"{os.cpu_count()} cores")}
+
+
+def run_reference(args) -> int:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    steps, warm = args.steps, args.warmup
+    mib = args.ref_mib
+    if mib is None:
+        xs, _ = oracle_inputs(1)
+        t0 = time.perf_counter()
+        oracle_step(xs)
+        t1 = time.perf_counter() - t0
+        budget = 120.0 / max(1, steps + warm)
+        mib = max(1, min(256, int(budget / max(t1, 1e-3))))
+    xs, nbytes = oracle_inputs(mib)
+    for _ in range(warm):
+        oracle_step(xs)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(xs)
+    el = time.perf_counter() - t0
+    value = step_bus_bytes(nbytes) * steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(nbytes),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{nbytes >> 20} MiB per rank (bench workload at 256 MiB), {steps} steps"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(bytes_per_rank: int) -> dict:
+    return {"workload": WORKLOAD, "virtual_ranks": NVR, "dtype": "f32", "op": "sum",
+            "bytes_per_rank": bytes_per_rank, "algos": ALGOS,
+            "step": "one out-of-place AllReduce per algorithm",
+            "inputs": "uniform[-1,1) fp32, seed 2, PCG64 per (seed, rank)",
+            "l2": "inputs larger than L2 (2 GiB per buffer set), no flush",
+            "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args) -> int:
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import collective_communication_algorithms_virtual_gb300 as vc
+    from synthetic_inputs import uniform_pm1_f32
+
+    N, M = NVR, BYTES_PER_RANK
+    count = M // 4
+    host = [uniform_pm1_f32(2, r, count) for r in range(N)]
+    send = [torch.from_numpy(h).to(dev) for h in host]
+    recv = {a: [torch.empty_like(send[0]) for _ in range(N)] for a in ALGOS}
+    stream = torch.cuda.current_stream(dev)
+
+    def step(sz=None):
+        for a in ALGOS:
+            if sz is None:
+                vc.vc_allreduce(send, recv[a], algo=a)
+            else:
+                vc.vc_allreduce([s[:sz] for s in send], [r[:sz] for r in recv[a]], algo=a)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    vc.vc_trace_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    trace = vc.vc_trace_read(1 << 22)
+    vc.vc_trace_enable(False)
+    clocks = sampler.stop()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1)
+    ms_max = reduce_max(ms_local, world, dev)
+    ms_per_step = ms_max / args.steps
+    value = step_bus_bytes(M) * world / (ms_per_step * 1e-3) / 1e9
+
+    peaks = measured_peaks()
+    # roofline of the dominant kernel, from the traced launches of the timed region
+    by_kernel = {}
+    for r in trace:
+        k = by_kernel.setdefault(r["kernel"], {"launches": 0, "ms": 0.0, "bytes": 0})
+        k["launches"] += 1
+        k["ms"] += r["ms"]
+        k["bytes"] += r["bytes"]
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    d = by_kernel[dom]
+    achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+    traffic = committed_traffic(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                "traffic": traffic, "algorithmic_bytes_per_launch": d["bytes"] / d["launches"],
+                "launches": d["launches"], "avg_launch_ms": d["ms"] / d["launches"],
+                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "kernels": {k: {"launches": v["launches"], "share": v["ms"] / sum(x["ms"] for x in by_kernel.values()),
+                                "gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9} for k, v in by_kernel.items()}}
+
+    out = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": config_block(M), "roofline": roofline, "gpu_launches": len(trace),
+           "clocks": clocks}
+
+    # per-algorithm figures at 256 MiB and the message-size sweep (rank 0 only)
+    if rank == 0:
+        out["per_algo"] = per_algo(vc, send, recv, stream, M, peaks)
+        if not args.no_sweep:
+            out["sweep"] = sweep(vc, send, recv, stream)
+
+    # end to end: pinned host inputs -> device -> four AllReduces -> all outputs back
+    if not args.no_e2e:
+        out["e2e"] = e2e(vc, host, send, recv, stream, args, world, dev, M)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = time_oracle(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    barrier(world)
+    return 0
+
+
+def time_calls(fn, stream, min_ms=20.0, max_reps=2000):
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    torch.cuda.synchronize()
+    reps = 1
+    while True:
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if ms >= min_ms or reps >= max_reps:
+            return ms / reps
+        reps = min(max_reps, reps * max(2, int(min_ms / max(ms, 1e-3))))
+
+
+def plan_bytes(vc, algo: str, N: int, count: int) -> int:
+    """Algorithmic bytes of one AllReduce: every operand of every operation of
+    the library's plan read or written once."""
+    entries, _, _ = vc.vc_plan_describe("allreduce", algo, N, count, "f32")
+    return sum(e.n * e.nb * 4 for e in entries)
+
+
+def per_algo(vc, send, recv, stream, M, peaks):
+    N = len(send)
+    alg_bytes = {a: plan_bytes(vc, a, N, M // 4) for a in ALGOS}
+    res = {}
+    for a in ALGOS:
+        ms = time_calls(lambda: vc.vc_allreduce(send, recv[a], algo=a), stream, min_ms=50.0)
+        hbm = alg_bytes[a] / (ms * 1e-3) / 1e9
+        res[a] = {"ms": ms, "algbw": M / (ms * 1e-3) / 1e9, "busbw": M * busbw_factor(N) / (ms * 1e-3) / 1e9,
+                  "hbm_gbs": hbm, "algorithmic_bytes": alg_bytes[a],
+                  "frac_of_measured": hbm / peaks["hbm_gbs"], "frac_of_nominal_8TBs": hbm / NOMINAL_HBM_GBS}
+    return res
+
+
+def sweep(vc, send, recv, stream):
+    N = len(send)
+    res = {a: [] for a in ALGOS}
+    for lg in range(10, 29):
+        nbytes = 1 << lg
+        sz = nbytes // 4
+        for a in ALGOS:
+            ms = time_calls(lambda: vc.vc_allreduce([s[:sz] for s in send], [r[:sz] for r in recv[a]], algo=a),
+                            stream, min_ms=10.0)
+            res[a].append({"bytes_per_rank": nbytes, "us": ms * 1e3,
+                           "busbw": nbytes * busbw_factor(N) / (ms * 1e-3) / 1e9,
+                           "l2_resident": 2 * N * nbytes <= (129 << 20)})
+    return res
+
+
+def e2e(vc, host, send, recv, stream, args, world, dev, M):
+    import torch
+
+    N = len(send)
+    pin_in = [torch.from_numpy(h).pin_memory() for h in host]
+    pin_out = {a: [torch.empty(M // 4, dtype=torch.float32).pin_memory() for _ in range(N)] for a in ALGOS}
+
+    def step():
+        for r in range(N):
+            send[r].copy_(pin_in[r], non_blocking=True)
+        for a in ALGOS:
+            vc.vc_allreduce(send, recv[a], algo=a)
+        for a in ALGOS:
+            for r in range(N):
+                pin_out[a][r].copy_(recv[a][r], non_blocking=True)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world, dev) / steps
+    return {"value": step_bus_bytes(M) * world / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": N * M, "d2h_bytes_per_step": len(ALGOS) * N * M,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--ref-mib", type=float, default=None,
+                    help="reference arm: MiB per rank of the oracle's sample (default: sized to ~2 min)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,30 @@
+"""Virtual-rank collectives on one GB300.
+
+N logical ranks are N buffers in one GPU's HBM.  The collectives and schedules
+(Ring / Recursive Halving-Doubling / Double Binary Tree AllReduce, Ring
+ReduceScatter and AllGather, binomial Broadcast and Scatter, Pairwise and
+Bruck AllToAll, and a fused one-pass form of each) run in hand-written sm_103a
+CUDA kernels behind the C ABI of ``include/vc.h``; this package is the thin
+Python binding over it.
+"""
+from .binding import (  # noqa: F401
+    ALGOS,
+    COLLS,
+    DTYPES,
+    LIB_PATH,
+    VCError,
+    lib,
+    vc_allgather,
+    vc_allreduce,
+    vc_alltoall,
+    vc_broadcast,
+    vc_busbw_factor,
+    vc_last_error,
+    vc_plan_describe,
+    vc_reduce_scatter,
+    vc_scatter,
+    vc_status_string,
+    vc_trace_enable,
+    vc_trace_read,
+    vc_version,
+)

@@ -1,0 +1,230 @@
+"""Thin ctypes binding over the C ABI of include/vc.h.
+
+Argument marshalling only: tensors become device pointers, counts and enum
+codes; every step of every collective runs in libvcoll.so.  The functions
+keep the C names.  There is no fallback: if the library is not built, or a
+call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvcoll.so")
+
+VC_SUCCESS, VC_ERR_INVALID_ARG, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_NOMEM, VC_ERR_TIMEOUT = range(6)
+DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
+OPS = {"sum": 0, "max": 1, "min": 2}
+ALGOS = {"fused": 0, "ring": 1, "rhd": 2, "dbt": 3, "binomial": 4, "scatter_allgather": 5,
+         "pairwise": 6, "bruck": 7}
+COLLS = {"allreduce": 0, "reduce_scatter": 1, "allgather": 2, "broadcast": 3, "scatter": 4,
+         "alltoall": 5}
+
+
+class VCError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("coll", ctypes.c_int32), ("algo", ctypes.c_int32), ("step", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("bytes", ctypes.c_int64), ("nops", ctypes.c_int32),
+                ("ms", ctypes.c_float)]
+
+
+KERNEL_NAMES = {0: "copy", 1: "sum_f32", 2: "sum_i32", 3: "sum_bf16"}
+
+
+def kernel_name(code: int) -> str:
+    return KERNEL_NAMES[code & 3] + ("_large" if code & 4 else "")
+
+
+class PlanEntry(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int32), ("op", ctypes.c_int32), ("role", ctypes.c_int32),
+                ("pos", ctypes.c_int32), ("buf", ctypes.c_int32), ("owner", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("reduce", ctypes.c_int32), ("byte_off", ctypes.c_int64),
+                ("n", ctypes.c_int64), ("nb", ctypes.c_int64), ("stride_bytes", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded once); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z, V = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+        PP = ctypes.POINTER(ctypes.c_void_p)
+        for name, args in {
+            "vc_allreduce": [PP, PP, I, Z, I, I, I, V],
+            "vc_reduce_scatter": [PP, PP, I, Z, I, I, I, V],
+            "vc_allgather": [PP, PP, I, Z, I, I, V],
+            "vc_broadcast": [P, PP, I, Z, I, I, I, V],
+            "vc_scatter": [P, PP, I, Z, I, I, I, V],
+            "vc_alltoall": [PP, PP, I, Z, I, I, V],
+        }.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = I
+        L.vc_status_string.argtypes = [I]
+        L.vc_status_string.restype = ctypes.c_char_p
+        L.vc_last_error.argtypes = []
+        L.vc_last_error.restype = ctypes.c_char_p
+        L.vc_busbw_factor.argtypes = [I, I]
+        L.vc_busbw_factor.restype = ctypes.c_double
+        L.vc_plan_describe.argtypes = [I, I, I, Z, I, I, I, ctypes.POINTER(PlanEntry), Z,
+                                       ctypes.POINTER(Z), ctypes.POINTER(Z), ctypes.POINTER(I)]
+        L.vc_plan_describe.restype = I
+        L.vc_trace_enable.argtypes = [I]
+        L.vc_trace_enable.restype = I
+        L.vc_trace_read.argtypes = [ctypes.POINTER(TraceRecord), Z, ctypes.POINTER(Z)]
+        L.vc_trace_read.restype = I
+        L.vc_version.argtypes = []
+        L.vc_version.restype = I
+        _lib = L
+    return _lib
+
+
+def check(status: int) -> None:
+    if status != VC_SUCCESS:
+        L = lib()
+        raise VCError(status, f"{L.vc_status_string(status).decode()}: {L.vc_last_error().decode()}")
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr_array(ptrs: Sequence[int]):
+    return (ctypes.c_void_p * len(ptrs))(*[ctypes.c_void_p(int(p)) for p in ptrs])
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    m = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
+    if t.dtype not in m:
+        raise VCError(VC_ERR_INVALID_ARG, f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _stream_handle(stream, like) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(like.device)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _ptrs(ts) -> list[int]:
+    return [t.data_ptr() for t in ts]
+
+
+def _code(table: dict, key) -> int:
+    return table[key] if isinstance(key, str) else int(key)
+
+
+# ---------------------------------------------------------------------------
+# collectives (tensor arguments; one tensor per virtual rank)
+# ---------------------------------------------------------------------------
+
+def vc_allreduce(send, recv, algo="fused", op="sum", stream=None) -> None:
+    """recv[r] = sum over ranks of send[q]; ``send[r] is recv[r]`` allowed."""
+    N = len(send)
+    check(lib().vc_allreduce(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, send[0].numel(),
+                             _dtype_code(send[0]), _code(OPS, op), _code(ALGOS, algo),
+                             _stream_handle(stream, send[0])))
+
+
+def vc_reduce_scatter(send, recv, algo="fused", op="sum", stream=None) -> None:
+    """recv[r] = block r of the sum; send[q] holds N blocks of recv[r].numel()."""
+    N = len(send)
+    check(lib().vc_reduce_scatter(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, recv[0].numel(),
+                                  _dtype_code(send[0]), _code(OPS, op), _code(ALGOS, algo),
+                                  _stream_handle(stream, send[0])))
+
+
+def vc_allgather(send, recv, algo="fused", stream=None) -> None:
+    """recv[r] = concatenation of send[0..N-1]."""
+    N = len(send)
+    check(lib().vc_allgather(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, send[0].numel(),
+                             _dtype_code(send[0]), _code(ALGOS, algo), _stream_handle(stream, send[0])))
+
+
+def vc_broadcast(send_root, recv, root=0, algo="fused", stream=None) -> None:
+    """recv[r] = send_root for every rank; ``send_root is recv[root]`` allowed."""
+    N = len(recv)
+    check(lib().vc_broadcast(ctypes.c_void_p(send_root.data_ptr()), _ptr_array(_ptrs(recv)), N,
+                             recv[0].numel(), _dtype_code(send_root), int(root), _code(ALGOS, algo),
+                             _stream_handle(stream, send_root)))
+
+
+def vc_scatter(send_root, recv, root=0, algo="fused", stream=None) -> None:
+    """recv[r] = block r of send_root."""
+    N = len(recv)
+    check(lib().vc_scatter(ctypes.c_void_p(send_root.data_ptr()), _ptr_array(_ptrs(recv)), N,
+                           recv[0].numel(), _dtype_code(send_root), int(root), _code(ALGOS, algo),
+                           _stream_handle(stream, send_root)))
+
+
+def vc_alltoall(send, recv, algo="fused", stream=None) -> None:
+    """recv[j] block i = send[i] block j; every buffer holds N blocks."""
+    N = len(send)
+    check(lib().vc_alltoall(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, send[0].numel() // N,
+                            _dtype_code(send[0]), _code(ALGOS, algo), _stream_handle(stream, send[0])))
+
+
+def vc_busbw_factor(coll, nranks: int) -> float:
+    return lib().vc_busbw_factor(_code(COLLS, coll), int(nranks))
+
+
+def vc_status_string(status: int) -> str:
+    return lib().vc_status_string(int(status)).decode()
+
+
+def vc_last_error() -> str:
+    return lib().vc_last_error().decode()
+
+
+def vc_version() -> int:
+    return lib().vc_version()
+
+
+def vc_trace_enable(on: bool = True) -> None:
+    """Start (clearing old records) or stop the launch trace."""
+    check(lib().vc_trace_enable(int(bool(on))))
+
+
+def vc_trace_read(capacity: int = 1 << 20) -> list:
+    """Wait for the traced launches and return their records (dicts)."""
+    buf = (TraceRecord * capacity)()
+    n = ctypes.c_size_t(0)
+    check(lib().vc_trace_read(buf, capacity, ctypes.byref(n)))
+    out = []
+    for r in buf[:n.value]:
+        out.append({"coll": r.coll, "algo": r.algo, "step": r.step, "kernel": kernel_name(r.kernel),
+                    "bytes": r.bytes, "nops": r.nops, "ms": r.ms})
+    return out
+
+
+def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False):
+    """The step plan the library would run, as (entries, scratch_bytes, n_steps);
+    host only, needs no GPU."""
+    L = lib()
+    need, scratch = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    steps = ctypes.c_int(0)
+    args = (_code(COLLS, coll), _code(ALGOS, algo), int(nranks), int(count), _code(DTYPES, dtype),
+            int(root), int(bool(inplace)))
+    check(L.vc_plan_describe(*args, None, 0, ctypes.byref(need), ctypes.byref(scratch), ctypes.byref(steps)))
+    buf = (PlanEntry * max(1, need.value))()
+    check(L.vc_plan_describe(*args, buf, need.value, ctypes.byref(need), ctypes.byref(scratch),
+                             ctypes.byref(steps)))
+    return list(buf[:need.value]), scratch.value, steps.value

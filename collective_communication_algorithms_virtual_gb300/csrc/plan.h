@@ -1,0 +1,66 @@
+// Step plans of the virtual-rank collectives (host C++, no CUDA).
+//
+// A plan is a list of steps; a step is a list of independent operations; an
+// operation reads its sources, adds them left to right (or copies its single
+// source) and writes every destination.  Steps run in order, one kernel
+// launch each; the operations of a step never write what another operation of
+// the same step reads or writes, so they run in any order or all at once.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+namespace vc {
+
+enum class Buf : uint8_t { Send = 0, Recv = 1, Scratch = 2 };
+enum class DT : uint8_t { F32 = 0, BF16 = 1, I32 = 2 };
+enum class Mode : uint8_t { Copy = 0, F32 = 1, I32 = 2, BF16 = 3 };
+
+enum class Coll : int { AllReduce = 0, ReduceScatter = 1, AllGather = 2, Broadcast = 3, Scatter = 4, AllToAll = 5 };
+enum class Algo : int { Fused = 0, Ring = 1, RHD = 2, DBT = 3, Binomial = 4, ScatterAllGather = 5, Pairwise = 6, Bruck = 7 };
+
+inline int esize(DT t) { return t == DT::BF16 ? 2 : 4; }
+
+struct Operand {
+  Buf buf;
+  int owner;         // rank holding the buffer (scratch: the rank it belongs to)
+  int64_t byte_off;  // from the rank's buffer start (scratch: from the scratch block start)
+  DT dt;             // storage type
+};
+
+struct Op {
+  std::vector<Operand> src;
+  std::vector<Operand> dst;
+  int64_t n = 0;        // elements per run
+  int64_t nb = 1;       // runs
+  int64_t sstride = 0;  // bytes between runs, every source
+  int64_t dstride = 0;  // bytes between runs, every destination
+};
+
+struct Step {
+  Mode mode;
+  std::vector<Op> ops;
+};
+
+struct Plan {
+  std::vector<Step> steps;
+  int64_t scratch_bytes = 0;
+};
+
+struct PlanArgs {
+  Coll coll;
+  Algo algo;
+  int nranks;
+  int64_t count;  // per the collective's convention (see vc.h)
+  DT dt;
+  int root = 0;
+  bool inplace = false;
+};
+
+enum class PlanStatus { Ok, Invalid, Unsupported };
+
+// Builds the plan; on failure `why` says what is wrong.
+PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why);
+
+}  // namespace vc

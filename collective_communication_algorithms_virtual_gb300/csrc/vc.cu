@@ -1,0 +1,979 @@
+// Kernels, launcher and C-ABI of the virtual-rank collectives (sm_103a).
+//
+// Every schedule is executed as its plan (plan.h): one launch per step, each
+// launch running all independent operations of that step.  One kernel
+// template does every step: a persistent grid walks "tiles" (a fixed number
+// of 16-byte groups of one run of one operation); each thread loads its
+// groups from every source with 128-bit loads, adds them in the order the
+// plan lists them (fp32 registers; bf16 widened exactly; int32 wrapping), and
+// stores the result to every destination with 128-bit stores.  Copy steps
+// move raw 16-byte groups.  Distinct elements are the only thing split across
+// threads, so each element's association is exactly the plan's.
+//
+// Nothing here is a dense contraction: the kernels are HBM-streaming and use
+// no tensor cores.  Kernels never wait on each other or on flags: ordering
+// between steps is stream order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "plan.h"
+#include "vc.h"
+
+#define VC_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace vc {
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+namespace {
+thread_local std::string g_last_error;
+
+vc_status_t fail(vc_status_t s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+vc_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(VC_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("VC_LOG");
+    return v && v[0] && std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// device code
+// ---------------------------------------------------------------------------
+namespace dev {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;           // 16-byte groups per thread per tile (vector path)
+constexpr int kScalarPerThread = 4;  // elements per thread per tile (element path)
+constexpr int kTileGroups = kThreads * kUnroll;
+constexpr int kTileElems = kThreads * kScalarPerThread;
+
+enum : int { kCopy = 0, kF32 = 1, kI32 = 2, kBF16 = 3 };
+
+struct __align__(16) OpDesc {
+  int64_t n;        // elements per run (copy: elements of esz bytes)
+  int64_t nb;       // runs
+  int64_t sstride;  // bytes between runs, sources
+  int64_t dstride;  // bytes between runs, destinations
+  int64_t groups;   // vector path: 16-byte groups per run (fp32 bf16-mode operands: 32 bytes)
+  uint64_t smask;   // bf16 mode: bit s set -> source s is stored as fp32
+  uint64_t dmask;   // bf16 mode: bit d set -> destination d is stored as fp32
+  uint32_t tile0;   // first tile of this operation within the launch
+  uint32_t tpr;     // tiles per run
+  uint16_t p0;      // first pointer (sources, then destinations)
+  uint8_t ns, nd;
+  uint8_t vec;      // 1: vector path
+  uint8_t esz;      // copy: element size in bytes
+};
+
+template <int OPS, int PTRS>
+struct __align__(16) LaunchParams {
+  uint32_t nops;
+  uint32_t ntiles;
+  uint32_t pad[2];
+  OpDesc op[OPS];
+  const void* ptr[PTRS];
+};
+using SmallParams = LaunchParams<16, 64>;
+using LargeParams = LaunchParams<128, 512>;
+
+// -- memory access helpers (sources are never written within a launch) -------
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even, lo in the low half
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void widen8(uint4 v, float* f) {
+  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// -- vector path -------------------------------------------------------------
+template <int MODE>
+__device__ __forceinline__ void tile_vec(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr);
+
+template <>
+__device__ __forceinline__ void tile_vec<kCopy>(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+  const int64_t g0 = tr * kTileGroups + threadIdx.x;
+  const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
+  uint4 v[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t g = g0 + u * kThreads;
+    if (g < o.groups) v[u] = ld16(s + g * 16);
+  }
+  for (int d = 0; d < o.nd; ++d) {
+    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = g0 + u * kThreads;
+      if (g < o.groups) st16(dp + g * 16, v[u]);
+    }
+  }
+}
+
+// fp32 and int32: 4 elements per 16-byte group.
+template <int MODE>
+__device__ __forceinline__ void tile_vec_4b(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+  const int64_t g0 = tr * kTileGroups + threadIdx.x;
+  uint4 acc[kUnroll];
+  {
+    const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = g0 + u * kThreads;
+      if (g < o.groups) acc[u] = ld16(s + g * 16);
+    }
+  }
+  for (int k = 1; k < o.ns; ++k) {
+    const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = g0 + u * kThreads;
+      if (g < o.groups) {
+        const uint4 v = ld16(s + g * 16);
+        if (MODE == kF32) {
+          acc[u].x = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].x), __uint_as_float(v.x)));
+          acc[u].y = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].y), __uint_as_float(v.y)));
+          acc[u].z = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].z), __uint_as_float(v.z)));
+          acc[u].w = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].w), __uint_as_float(v.w)));
+        } else {
+          acc[u].x += v.x; acc[u].y += v.y; acc[u].z += v.z; acc[u].w += v.w;
+        }
+      }
+    }
+  }
+  for (int d = 0; d < o.nd; ++d) {
+    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t g = g0 + u * kThreads;
+      if (g < o.groups) st16(dp + g * 16, acc[u]);
+    }
+  }
+}
+template <>
+__device__ __forceinline__ void tile_vec<kF32>(const OpDesc& o, const void* const* p, int64_t r, int64_t t) {
+  tile_vec_4b<kF32>(o, p, r, t);
+}
+template <>
+__device__ __forceinline__ void tile_vec<kI32>(const OpDesc& o, const void* const* p, int64_t r, int64_t t) {
+  tile_vec_4b<kI32>(o, p, r, t);
+}
+
+// bf16 mode: 8 elements per group; a bf16 operand moves 16 bytes, an fp32 one 32.
+constexpr int kUnrollBF = 2;
+template <>
+__device__ __forceinline__ void tile_vec<kBF16>(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+  // A tile covers kTileGroups groups in kUnroll/kUnrollBF passes of kUnrollBF groups per thread.
+#pragma unroll 1
+  for (int pass = 0; pass < kUnroll / kUnrollBF; ++pass) {
+    const int64_t g0 = tr * kTileGroups + pass * kUnrollBF * kThreads + threadIdx.x;
+    float acc[kUnrollBF][8];
+    for (int k = 0; k < o.ns; ++k) {
+      const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
+      const bool f32 = (o.smask >> k) & 1;
+#pragma unroll
+      for (int u = 0; u < kUnrollBF; ++u) {
+        const int64_t g = g0 + u * kThreads;
+        if (g < o.groups) {
+          float f[8];
+          if (f32) {
+            const uint4 a = ld16(s + g * 32), b = ld16(s + g * 32 + 16);
+            f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+            f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+          } else {
+            widen8(ld16(s + g * 16), f);
+          }
+          if (k == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[u][i] = f[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], f[i]);
+          }
+        }
+      }
+    }
+    for (int d = 0; d < o.nd; ++d) {
+      char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
+      const bool f32 = (o.dmask >> d) & 1;
+#pragma unroll
+      for (int u = 0; u < kUnrollBF; ++u) {
+        const int64_t g = g0 + u * kThreads;
+        if (g < o.groups) {
+          if (f32) {
+            st16(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
+                                         __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
+            st16(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
+                                              __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
+          } else {
+            st16(dp + g * 16, make_uint4(pack_bf16(acc[u][0], acc[u][1]), pack_bf16(acc[u][2], acc[u][3]),
+                                         pack_bf16(acc[u][4], acc[u][5]), pack_bf16(acc[u][6], acc[u][7])));
+          }
+        }
+      }
+    }
+  }
+}
+
+// -- element path (unaligned operands and the tails of vector runs) ---------
+template <int MODE>
+__device__ __forceinline__ void elem(const OpDesc& o, const void* const* ptr, int64_t soff, int64_t doff, int64_t e) {
+  if (MODE == kCopy) {
+    const char* s = static_cast<const char*>(ptr[0]) + soff + e * o.esz;
+    if (o.esz == 2) {
+      const uint16_t v = *reinterpret_cast<const uint16_t*>(s);
+      for (int d = 0; d < o.nd; ++d)
+        *reinterpret_cast<uint16_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 2) = v;
+    } else {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(s);
+      for (int d = 0; d < o.nd; ++d)
+        *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = v;
+    }
+  } else if (MODE == kF32) {
+    float acc = *reinterpret_cast<const float*>(static_cast<const char*>(ptr[0]) + soff + e * 4);
+    for (int k = 1; k < o.ns; ++k)
+      acc = __fadd_rn(acc, *reinterpret_cast<const float*>(static_cast<const char*>(ptr[k]) + soff + e * 4));
+    for (int d = 0; d < o.nd; ++d)
+      *reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
+  } else if (MODE == kI32) {
+    uint32_t acc = *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[0]) + soff + e * 4);
+    for (int k = 1; k < o.ns; ++k)
+      acc += *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[k]) + soff + e * 4);
+    for (int d = 0; d < o.nd; ++d)
+      *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
+  } else {
+    float acc = 0.f;
+    for (int k = 0; k < o.ns; ++k) {
+      const char* s = static_cast<const char*>(ptr[k]) + soff;
+      const float v = ((o.smask >> k) & 1) ? *reinterpret_cast<const float*>(s + e * 4)
+                                           : bf16lo(*reinterpret_cast<const uint16_t*>(s + e * 2));
+      acc = k == 0 ? v : __fadd_rn(acc, v);
+    }
+    for (int d = 0; d < o.nd; ++d) {
+      char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
+      if ((o.dmask >> d) & 1) {
+        *reinterpret_cast<float*>(dp + e * 4) = acc;
+      } else {
+        __nv_bfloat16 h = __float2bfloat16_rn(acc);
+        *reinterpret_cast<uint16_t*>(dp + e * 2) = *reinterpret_cast<uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ int64_t group_elems(const OpDesc& o) {
+  return MODE == kCopy ? 16 / o.esz : (MODE == kBF16 ? 8 : 4);
+}
+
+template <int MODE, class P>
+__global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
+  for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+    int lo = 0, hi = static_cast<int>(p.nops) - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.op[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+    }
+    const OpDesc& o = p.op[lo];
+    const void* const* ptr = p.ptr + o.p0;
+    const int64_t lt = t - o.tile0;
+    const int64_t run = lt / o.tpr;
+    const int64_t tr = lt - run * o.tpr;
+    const int64_t soff = run * o.sstride, doff = run * o.dstride;
+    if (o.vec) {
+      tile_vec<MODE>(o, ptr, run, tr);
+      if (tr == o.tpr - 1) {  // elements after the last whole group (single-run operations only)
+        for (int64_t e = o.groups * group_elems<MODE>(o) + threadIdx.x; e < o.n; e += kThreads)
+          elem<MODE>(o, ptr, soff, doff, e);
+      }
+    } else {
+      const int64_t e0 = tr * kTileElems;
+      const int64_t e1 = e0 + kTileElems < o.n ? e0 + kTileElems : o.n;
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) elem<MODE>(o, ptr, soff, doff, e);
+    }
+  }
+}
+
+}  // namespace dev
+
+// ---------------------------------------------------------------------------
+// per-device state: SM count, occupancy, scratch pool
+// ---------------------------------------------------------------------------
+namespace {
+
+struct DeviceState {
+  bool init = false;
+  int nsm = 0;
+  cudaMemPool_t pool = nullptr;
+  std::map<const void*, int> occupancy;
+};
+std::mutex g_mu;
+DeviceState g_dev[64];
+
+vc_status_t device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(VC_ERR_CUDA, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    e = cudaDeviceGetAttribute(&st.nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    st.init = true;
+  }
+  *out = &st;
+  *dev_out = dev;
+  return VC_SUCCESS;
+}
+
+vc_status_t scratch_pool(DeviceState* st, int dev, cudaMemPool_t* pool) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!st->pool) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaError_t e = cudaMemPoolCreate(&st->pool, &props);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = UINT64_MAX;  // keep freed scratch cached for the next call
+    e = cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+  }
+  *pool = st->pool;
+  return VC_SUCCESS;
+}
+
+template <class K>
+int blocks_per_sm(DeviceState* st, K kernel) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  const void* key = reinterpret_cast<const void*>(kernel);
+  auto it = st->occupancy.find(key);
+  if (it != st->occupancy.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, dev::kThreads, 0) != cudaSuccess || n < 1) n = 1;
+  st->occupancy[key] = n;
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// launch trace
+// ---------------------------------------------------------------------------
+struct TraceCtx {
+  int coll = 0, algo = 0, step = 0;
+};
+struct Pending {
+  vc_trace_record_t rec;
+  cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<Pending> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaError_t take_event(cudaEvent_t* ev) {
+  if (!g_event_pool.empty()) {
+    *ev = g_event_pool.back();
+    g_event_pool.pop_back();
+    return cudaSuccess;
+  }
+  return cudaEventCreate(ev);
+}
+
+int64_t launch_bytes(const Step& st, size_t i, size_t j) {
+  int64_t b = 0;
+  for (size_t k = i; k < j; ++k) {
+    const Op& op = st.ops[k];
+    int64_t per = 0;
+    for (const Operand& o : op.src) per += esize(o.dt);
+    for (const Operand& o : op.dst) per += esize(o.dt);
+    b += per * op.n * op.nb;
+  }
+  return b;
+}
+
+// ---------------------------------------------------------------------------
+// launching one step
+// ---------------------------------------------------------------------------
+struct Bases {
+  const void* const* send;  // per rank (broadcast/scatter: only the root's entry is used)
+  void* const* recv;
+  char* scratch;
+};
+
+const char* base_ptr(const Bases& b, const Operand& o) {
+  switch (o.buf) {
+    case Buf::Send: return static_cast<const char*>(b.send[o.owner]) + o.byte_off;
+    case Buf::Recv: return static_cast<const char*>(b.recv[o.owner]) + o.byte_off;
+    default: return b.scratch + o.byte_off;
+  }
+}
+
+template <class P>
+bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t* tiles_out) {
+  std::memset(&p, 0, sizeof(P));
+  const Mode mode = st.mode;
+  int64_t tiles = 0;
+  int np = 0;
+  for (size_t k = i; k < j; ++k) {
+    const Op& op = st.ops[k];
+    dev::OpDesc& d = p.op[k - i];
+    d.n = op.n;
+    d.nb = op.nb;
+    d.sstride = op.sstride;
+    d.dstride = op.dstride;
+    d.ns = static_cast<uint8_t>(op.src.size());
+    d.nd = static_cast<uint8_t>(op.dst.size());
+    d.p0 = static_cast<uint16_t>(np);
+    d.esz = static_cast<uint8_t>(esize(op.src[0].dt));
+    bool aligned = true;
+    for (size_t s = 0; s < op.src.size(); ++s) {
+      const char* ptr = base_ptr(b, op.src[s]);
+      p.ptr[np++] = ptr;
+      aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
+      if (op.src[s].dt == DT::F32) d.smask |= 1ull << s;
+    }
+    for (size_t s = 0; s < op.dst.size(); ++s) {
+      const char* ptr = base_ptr(b, op.dst[s]);
+      p.ptr[np++] = ptr;
+      aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
+      if (op.dst[s].dt == DT::F32) d.dmask |= 1ull << s;
+    }
+    int64_t gelems = mode == Mode::Copy ? 16 / d.esz : (mode == Mode::BF16 ? 8 : 4);
+    if (op.nb > 1) {
+      aligned &= (op.n % gelems) == 0 && (op.sstride % 16) == 0 && (op.dstride % 16) == 0;
+    }
+    d.vec = aligned ? 1 : 0;
+    int64_t tpr;
+    if (aligned) {
+      d.groups = op.n / gelems;
+      tpr = std::max<int64_t>(1, (d.groups + dev::kTileGroups - 1) / dev::kTileGroups);
+    } else {
+      d.groups = 0;
+      tpr = std::max<int64_t>(1, (op.n + dev::kTileElems - 1) / dev::kTileElems);
+    }
+    d.tpr = static_cast<uint32_t>(tpr);
+    d.tile0 = static_cast<uint32_t>(tiles);
+    tiles += tpr * op.nb;
+    if (tiles > 0xFFFFFFFFll || tpr > 0xFFFFFFFFll) return false;
+  }
+  p.nops = static_cast<uint32_t>(j - i);
+  p.ntiles = static_cast<uint32_t>(tiles);
+  *tiles_out = tiles;
+  return true;
+}
+
+template <int MODE, class P>
+vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
+                         const TraceCtx& tc) {
+  static thread_local P p;  // large: keep off the stack
+  int64_t tiles = 0;
+  if (!fill_params(p, s, i, j, b, &tiles)) return fail(VC_ERR_INVALID_ARG, "operation too large for one launch");
+  if (tiles == 0) return VC_SUCCESS;
+  auto kernel = dev::step_kernel<MODE, P>;
+  const int64_t cap = int64_t(st->nsm) * blocks_per_sm(st, kernel);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, cap));
+  std::unique_lock<std::mutex> lk(g_trace_mu);
+  const bool trace = g_trace_on;
+  if (!trace) lk.unlock();
+  Pending pend{};
+  if (trace) {
+    cudaError_t e = take_event(&pend.start);
+    if (e == cudaSuccess) e = take_event(&pend.stop);
+    if (e == cudaSuccess) e = cudaEventRecord(pend.start, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event");
+  }
+  kernel<<<grid, dev::kThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (trace) {
+    e = cudaEventRecord(pend.stop, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event");
+    pend.rec.coll = tc.coll;
+    pend.rec.algo = tc.algo;
+    pend.rec.step = tc.step;
+    pend.rec.kernel = MODE + (sizeof(P) == sizeof(dev::LargeParams) ? 4 : 0);
+    pend.rec.bytes = launch_bytes(s, i, j);
+    pend.rec.nops = static_cast<int32_t>(j - i);
+    g_trace.push_back(pend);
+  }
+  return VC_SUCCESS;
+}
+
+template <class P>
+vc_status_t launch_mode(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
+                        const TraceCtx& tc) {
+  switch (s.mode) {
+    case Mode::Copy: return launch_typed<dev::kCopy, P>(st, s, i, j, b, stream, tc);
+    case Mode::F32: return launch_typed<dev::kF32, P>(st, s, i, j, b, stream, tc);
+    case Mode::I32: return launch_typed<dev::kI32, P>(st, s, i, j, b, stream, tc);
+    default: return launch_typed<dev::kBF16, P>(st, s, i, j, b, stream, tc);
+  }
+}
+
+int op_ptrs(const Op& op) { return static_cast<int>(op.src.size() + op.dst.size()); }
+
+vc_status_t launch_step(DeviceState* st, const Step& s, const Bases& b, cudaStream_t stream, int* launches,
+                        const TraceCtx& tc) {
+  size_t i = 0;
+  while (i < s.ops.size()) {
+    // the largest prefix that fits the small parameter block, else the large one
+    size_t j = i;
+    int ptrs = 0;
+    while (j < s.ops.size() && j - i < 16 && ptrs + op_ptrs(s.ops[j]) <= 64) ptrs += op_ptrs(s.ops[j++]);
+    vc_status_t rc;
+    if (j == s.ops.size()) {
+      rc = launch_mode<dev::SmallParams>(st, s, i, j, b, stream, tc);
+    } else {
+      j = i;
+      ptrs = 0;
+      while (j < s.ops.size() && j - i < 128 && ptrs + op_ptrs(s.ops[j]) <= 512) ptrs += op_ptrs(s.ops[j++]);
+      if (j == i) return fail(VC_ERR_INVALID_ARG, "operation has too many operands");
+      rc = launch_mode<dev::LargeParams>(st, s, i, j, b, stream, tc);
+    }
+    if (rc != VC_SUCCESS) return rc;
+    ++*launches;
+    i = j;
+  }
+  return VC_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// argument checks shared by the entry points
+// ---------------------------------------------------------------------------
+const char* coll_name(Coll c) {
+  static const char* n[] = {"allreduce", "reduce_scatter", "allgather", "broadcast", "scatter", "alltoall"};
+  return n[static_cast<int>(c)];
+}
+const char* algo_name(Algo a) {
+  static const char* n[] = {"fused", "ring", "rhd", "dbt", "binomial", "scatter_allgather", "pairwise", "bruck"};
+  return n[static_cast<int>(a)];
+}
+
+struct Call {
+  Coll coll;
+  Algo algo;
+  int nranks;
+  int64_t count;
+  DT dt;
+  int root = 0;
+  const void* const* send = nullptr;  // per-rank inputs (AllReduce, ReduceScatter, AllGather, AllToAll)
+  const void* send_root = nullptr;    // Broadcast, Scatter
+  void* const* recv = nullptr;
+  cudaStream_t stream = nullptr;
+};
+
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+}
+
+vc_status_t plan_status(PlanStatus ps, const std::string& why) {
+  if (ps == PlanStatus::Invalid) return fail(VC_ERR_INVALID_ARG, why);
+  if (ps == PlanStatus::Unsupported) return fail(VC_ERR_UNSUPPORTED, why);
+  return VC_SUCCESS;
+}
+
+vc_status_t to_dt(vc_dtype_t d, DT* out) {
+  switch (d) {
+    case VC_FLOAT32: *out = DT::F32; return VC_SUCCESS;
+    case VC_BFLOAT16: *out = DT::BF16; return VC_SUCCESS;
+    case VC_INT32: *out = DT::I32; return VC_SUCCESS;
+  }
+  return fail(VC_ERR_INVALID_ARG, "unknown dtype");
+}
+
+vc_status_t to_algo(vc_algo_t a, Algo* out) {
+  if (static_cast<int>(a) < 0 || static_cast<int>(a) > 7) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
+  *out = static_cast<Algo>(static_cast<int>(a));
+  return VC_SUCCESS;
+}
+
+vc_status_t run(const Call& c) {
+  const int N = c.nranks;
+  if (N < 1 || N > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
+  if (!c.recv) return fail(VC_ERR_INVALID_ARG, "null recv array");
+  const bool rooted = c.coll == Coll::Broadcast || c.coll == Coll::Scatter;
+  if (rooted && (c.root < 0 || c.root >= N)) return fail(VC_ERR_INVALID_ARG, "root outside [0, nranks)");
+  if (!rooted && !c.send) return fail(VC_ERR_INVALID_ARG, "null send array");
+  if (c.count < 0) return fail(VC_ERR_INVALID_ARG, "count too large");
+  // algorithm / rank-count support is decided before looking at sizes
+  PlanArgs pa{c.coll, c.algo, N, c.count, c.dt, c.root, false};
+  {
+    Plan probe;
+    std::string why;
+    PlanArgs zero = pa;
+    zero.count = 0;
+    const PlanStatus ps = build_plan(zero, &probe, &why);
+    if (ps != PlanStatus::Ok) return plan_status(ps, why);
+  }
+  if (c.count == 0) return VC_SUCCESS;
+
+  // element counts of each send / recv buffer
+  const int64_t es = esize(c.dt);
+  int64_t send_elems = c.count, recv_elems = c.count;
+  if (c.coll == Coll::ReduceScatter || c.coll == Coll::Scatter) send_elems = c.count * N;
+  if (c.coll == Coll::AllGather) recv_elems = c.count * N;
+  if (c.coll == Coll::AllToAll) send_elems = recv_elems = c.count * N;
+  if (c.count > (INT64_MAX / 8) / N) return fail(VC_ERR_INVALID_ARG, "count too large");
+  const int64_t sbytes = send_elems * es, rbytes = recv_elems * es;
+
+  std::vector<const void*> sends;
+  if (rooted) {
+    if (!c.send_root) return fail(VC_ERR_INVALID_ARG, "null root send buffer");
+    sends.assign(N, nullptr);
+    sends[c.root] = c.send_root;
+  } else {
+    for (int r = 0; r < N; ++r) {
+      if (!c.send[r]) return fail(VC_ERR_INVALID_ARG, "null send buffer");
+      sends.push_back(c.send[r]);
+    }
+  }
+  for (int r = 0; r < N; ++r)
+    if (!c.recv[r]) return fail(VC_ERR_INVALID_ARG, "null recv buffer");
+
+  // outputs must not overlap each other or any input, except in place
+  bool inplace = false;
+  for (int i = 0; i < N; ++i) {
+    for (int j = i + 1; j < N; ++j)
+      if (overlap(c.recv[i], rbytes, c.recv[j], rbytes)) return fail(VC_ERR_INVALID_ARG, "receive buffers overlap");
+    for (int q = 0; q < N; ++q) {
+      if (!sends[q] || !overlap(c.recv[i], rbytes, sends[q], sbytes)) continue;
+      const bool same = sends[q] == c.recv[i] && q == i && sbytes == rbytes;
+      const bool allowed = same && (c.coll == Coll::AllReduce || (c.coll == Coll::Broadcast && i == c.root));
+      if (!allowed) return fail(VC_ERR_INVALID_ARG, "a receive buffer overlaps a send buffer");
+      inplace = true;
+    }
+  }
+  pa.inplace = c.coll == Coll::AllReduce ? (N == 1 && inplace) : inplace;
+
+  Plan plan;
+  std::string why;
+  const PlanStatus ps = build_plan(pa, &plan, &why);
+  if (ps != PlanStatus::Ok) return plan_status(ps, why);
+
+  DeviceState* st = nullptr;
+  int dev = 0;
+  vc_status_t rc = device_state(&st, &dev);
+  if (rc != VC_SUCCESS) return rc;
+
+  char* scratch = nullptr;
+  if (plan.scratch_bytes > 0) {
+    cudaMemPool_t pool;
+    rc = scratch_pool(st, dev, &pool);
+    if (rc != VC_SUCCESS) return rc;
+    cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), plan.scratch_bytes, pool, c.stream);
+    if (e == cudaErrorMemoryAllocation) {
+      cudaGetLastError();
+      return fail(VC_ERR_NOMEM, "scratch allocation of " + std::to_string(plan.scratch_bytes) + " bytes failed");
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
+  }
+  const Bases b{sends.data(), c.recv, scratch};
+  int launches = 0;
+  TraceCtx tc;
+  tc.coll = static_cast<int>(c.coll);
+  tc.algo = static_cast<int>(c.algo);
+  for (size_t si = 0; si < plan.steps.size(); ++si) {
+    tc.step = static_cast<int>(si);
+    rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
+    if (rc != VC_SUCCESS) break;
+  }
+  if (scratch) {
+    cudaError_t e = cudaFreeAsync(scratch, c.stream);
+    if (e != cudaSuccess && rc == VC_SUCCESS) rc = cuda_fail(e, "cudaFreeAsync");
+  }
+  if (log_enabled()) {
+    size_t ops = 0;
+    for (const Step& s : plan.steps) ops += s.ops.size();
+    std::fprintf(stderr, "[vc] %s algo=%s nranks=%d count=%lld dtype=%d root=%d steps=%zu ops=%zu launches=%d scratch=%lld\n",
+                 coll_name(c.coll), algo_name(c.algo), N, static_cast<long long>(c.count), static_cast<int>(c.dt),
+                 c.root, plan.steps.size(), ops, launches, static_cast<long long>(plan.scratch_bytes));
+  }
+  return rc;
+}
+
+template <class F>
+vc_status_t entry(F&& f) {
+  g_last_error.clear();
+  try {
+    return f();
+  } catch (const std::bad_alloc&) {
+    return fail(VC_ERR_NOMEM, "host allocation failed");
+  } catch (...) {
+    return fail(VC_ERR_INVALID_ARG, "internal error");
+  }
+}
+
+}  // namespace
+}  // namespace vc
+
+using namespace vc;
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+VC_EXPORT vc_status_t vc_allreduce(const void* const* send, void* const* recv, int nranks, size_t count,
+                                   vc_dtype_t dtype, vc_op_t op, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::AllReduce;
+    vc_status_t rc = to_algo(algo, &c.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(count);
+    c.send = send;
+    c.recv = recv;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_reduce_scatter(const void* const* send, void* const* recv, int nranks, size_t recvcount,
+                                        vc_dtype_t dtype, vc_op_t op, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::ReduceScatter;
+    vc_status_t rc = to_algo(algo, &c.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(recvcount);
+    c.send = send;
+    c.recv = recv;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_allgather(const void* const* send, void* const* recv, int nranks, size_t sendcount,
+                                   vc_dtype_t dtype, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::AllGather;
+    vc_status_t rc = to_algo(algo, &c.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(sendcount);
+    c.send = send;
+    c.recv = recv;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_broadcast(const void* send_root, void* const* recv, int nranks, size_t count,
+                                   vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::Broadcast;
+    vc_status_t rc = to_algo(algo, &c.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(count);
+    c.root = root;
+    c.send_root = send_root;
+    c.recv = recv;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_scatter(const void* send_root, void* const* recv, int nranks, size_t recvcount,
+                                 vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::Scatter;
+    vc_status_t rc = to_algo(algo, &c.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(recvcount);
+    c.root = root;
+    c.send_root = send_root;
+    c.recv = recv;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_alltoall(const void* const* send, void* const* recv, int nranks, size_t blockcount,
+                                  vc_dtype_t dtype, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::AllToAll;
+    vc_status_t rc = to_algo(algo, &c.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(blockcount);
+    c.send = send;
+    c.recv = recv;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT const char* vc_status_string(vc_status_t s) {
+  switch (s) {
+    case VC_SUCCESS: return "VC_SUCCESS";
+    case VC_ERR_INVALID_ARG: return "VC_ERR_INVALID_ARG";
+    case VC_ERR_UNSUPPORTED: return "VC_ERR_UNSUPPORTED";
+    case VC_ERR_CUDA: return "VC_ERR_CUDA";
+    case VC_ERR_NOMEM: return "VC_ERR_NOMEM";
+    case VC_ERR_TIMEOUT: return "VC_ERR_TIMEOUT";
+  }
+  return "VC_ERR_UNKNOWN";
+}
+
+VC_EXPORT const char* vc_last_error(void) { return g_last_error.c_str(); }
+
+VC_EXPORT double vc_busbw_factor(vc_coll_t coll, int nranks) {
+  if (nranks < 1) return 0.0;
+  const double N = nranks;
+  switch (coll) {
+    case VC_COLL_ALLREDUCE: return 2.0 * (N - 1) / N;
+    case VC_COLL_REDUCE_SCATTER:
+    case VC_COLL_ALLGATHER:
+    case VC_COLL_ALLTOALL:
+    case VC_COLL_SCATTER: return (N - 1) / N;
+    case VC_COLL_BROADCAST: return 1.0;
+  }
+  return 0.0;
+}
+
+VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
+                                       vc_dtype_t dtype, int root, int inplace, vc_plan_entry_t* entries,
+                                       size_t capacity, size_t* n_entries, size_t* scratch_bytes, int* n_steps) {
+  return entry([&]() -> vc_status_t {
+    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 5) return fail(VC_ERR_INVALID_ARG, "unknown collective");
+    PlanArgs pa;
+    pa.coll = static_cast<Coll>(static_cast<int>(coll));
+    vc_status_t rc = to_algo(algo, &pa.algo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &pa.dt);
+    if (rc != VC_SUCCESS) return rc;
+    pa.nranks = nranks;
+    pa.count = static_cast<int64_t>(count);
+    pa.root = root;
+    pa.inplace = inplace != 0;
+    Plan plan;
+    std::string why;
+    const PlanStatus ps = build_plan(pa, &plan, &why);
+    if (ps != PlanStatus::Ok) return plan_status(ps, why);
+    size_t need = 0;
+    for (const Step& s : plan.steps)
+      for (const Op& op : s.ops) need += op.src.size() + op.dst.size();
+    if (n_entries) *n_entries = need;
+    if (scratch_bytes) *scratch_bytes = static_cast<size_t>(plan.scratch_bytes);
+    if (n_steps) *n_steps = static_cast<int>(plan.steps.size());
+    if (!entries) return capacity == 0 ? VC_SUCCESS : fail(VC_ERR_INVALID_ARG, "null entries");
+    if (capacity < need) return fail(VC_ERR_INVALID_ARG, "capacity too small");
+    size_t k = 0;
+    for (size_t si = 0; si < plan.steps.size(); ++si) {
+      const Step& s = plan.steps[si];
+      for (size_t oi = 0; oi < s.ops.size(); ++oi) {
+        const Op& op = s.ops[oi];
+        for (int role = 0; role < 2; ++role) {
+          const auto& list = role == 0 ? op.src : op.dst;
+          for (size_t pos = 0; pos < list.size(); ++pos) {
+            vc_plan_entry_t& e = entries[k++];
+            e.step = static_cast<int32_t>(si);
+            e.op = static_cast<int32_t>(oi);
+            e.role = role;
+            e.pos = static_cast<int32_t>(pos);
+            e.buf = static_cast<int32_t>(list[pos].buf);
+            e.owner = list[pos].owner;
+            e.dtype = static_cast<int32_t>(list[pos].dt);
+            e.reduce = s.mode == Mode::Copy ? 0 : 1;
+            e.byte_off = list[pos].byte_off;
+            e.n = op.n;
+            e.nb = op.nb;
+            e.stride_bytes = role == 0 ? op.sstride : op.dstride;
+          }
+        }
+      }
+    }
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_trace_enable(int on) {
+  return entry([&]() -> vc_status_t {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (Pending& p : g_trace) {
+      g_event_pool.push_back(p.start);
+      g_event_pool.push_back(p.stop);
+    }
+    g_trace.clear();
+    g_trace_on = on != 0;
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n_records) {
+  return entry([&]() -> vc_status_t {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    size_t n = 0;
+    vc_status_t rc = VC_SUCCESS;
+    for (Pending& p : g_trace) {
+      if (records && n < capacity && rc == VC_SUCCESS) {
+        cudaError_t e = cudaEventSynchronize(p.stop);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, p.start, p.stop);
+        if (e != cudaSuccess) {
+          rc = cuda_fail(e, "trace event");
+        } else {
+          records[n] = p.rec;
+          records[n].ms = ms;
+          ++n;
+        }
+      }
+      g_event_pool.push_back(p.start);
+      g_event_pool.push_back(p.stop);
+    }
+    g_trace.clear();
+    if (n_records) *n_records = n;
+    return rc;
+  });
+}
+
+VC_EXPORT int vc_version(void) { return 100; }

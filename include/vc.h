@@ -1,0 +1,244 @@
+/*
+ * vc.h -- virtual-rank collectives on one GPU.
+ *
+ * N logical ranks are N buffers in one GPU's memory.  Each call reduces or
+ * redistributes those buffers with one of the schedules analysed on three
+ * pages: the Broadcast/Scatter page "一对多通信：Broadcast 与 Scatter"
+ * (one-to-many communication), the CSDN article on CANN hccl's AllReduce
+ * algorithms, and the latency-formula page "集合通信算法延迟公式" (alpha-beta
+ * latency formulas of collective algorithms).  The call shape follows the
+ * article's hccl_allreduce(sendbuf, recvbuf, count, dataType, op, comm,
+ * stream) (section "hccl_allreduce接口详解"); the communicator becomes an
+ * explicit rank count and one pointer per rank.
+ *
+ * Common rules for every collective below:
+ *
+ *  - Counts are in ELEMENTS, not bytes.
+ *  - `send` / `recv` are HOST arrays of `nranks` DEVICE pointers, one per
+ *    virtual rank, all on the current CUDA device.  The arrays are read
+ *    during the call only; the buffers belong to the caller and must stay
+ *    alive until the work enqueued on `stream` has finished.
+ *  - Every call only enqueues work on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns without waiting for it.  Scratch
+ *    memory, where a schedule needs it, comes from a memory pool owned by the
+ *    library, is allocated and freed in stream order, and stays cached in the
+ *    pool for later calls.
+ *  - Output buffers must not overlap each other or any input, except where a
+ *    function allows in-place operation.  Inputs may overlap each other.
+ *  - Any alignment is accepted.  When every pointer a step touches is 16-byte
+ *    aligned the vector path runs; otherwise a slower element-wise path.
+ *  - Errors are returned, never raised: VC_ERR_INVALID_ARG (null pointer,
+ *    nranks outside [1, VC_MAX_RANKS], root outside [0, nranks), overlapping
+ *    buffers, size overflow), VC_ERR_UNSUPPORTED (an algorithm that is not
+ *    defined for the collective or the rank count, an op other than VC_SUM),
+ *    VC_ERR_NOMEM (scratch allocation failed), VC_ERR_CUDA (a CUDA call or
+ *    launch failed; vc_last_error() has the text).  On any error nothing has
+ *    been enqueued, except for VC_ERR_CUDA from a launch after earlier steps.
+ *  - A count of 0 returns VC_SUCCESS without enqueuing anything.
+ *
+ * Reductions: VC_SUM on VC_FLOAT32 (fp32 adds), VC_BFLOAT16 (inputs widened to
+ * fp32, summed in fp32, rounded once to bf16, round to nearest even) and
+ * VC_INT32 (two's-complement wrap-around).  Every algorithm fixes the
+ * association of its adds per element, so results are reproducible bit for
+ * bit run to run; different algorithms may differ in the last bits.
+ */
+#ifndef VC_H_
+#define VC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that the header needs no CUDA headers. */
+typedef struct CUstream_st* vc_stream_t;
+
+#define VC_MAX_RANKS 64
+
+typedef enum {
+  VC_SUCCESS = 0,
+  VC_ERR_INVALID_ARG = 1,
+  VC_ERR_UNSUPPORTED = 2,
+  VC_ERR_CUDA = 3,
+  VC_ERR_NOMEM = 4,
+  VC_ERR_TIMEOUT = 5
+} vc_status_t;
+
+typedef enum { VC_FLOAT32 = 0, VC_BFLOAT16 = 1, VC_INT32 = 2 } vc_dtype_t;
+
+/* The hccl article lists SUM / MAX / MIN; this version implements VC_SUM. */
+typedef enum { VC_SUM = 0, VC_MAX = 1, VC_MIN = 2 } vc_op_t;
+
+typedef enum {
+  VC_ALGO_FUSED = 0,             /* one pass over all ranks: every collective          */
+  VC_ALGO_RING = 1,              /* AllReduce, ReduceScatter, AllGather                */
+  VC_ALGO_RHD = 2,               /* AllReduce, nranks a power of 2                     */
+  VC_ALGO_DBT = 3,               /* AllReduce                                          */
+  VC_ALGO_BINOMIAL = 4,          /* Broadcast, Scatter                                 */
+  VC_ALGO_SCATTER_ALLGATHER = 5, /* Broadcast                                          */
+  VC_ALGO_PAIRWISE = 6,          /* AllToAll                                           */
+  VC_ALGO_BRUCK = 7              /* AllToAll                                           */
+} vc_algo_t;
+
+typedef enum {
+  VC_COLL_ALLREDUCE = 0,
+  VC_COLL_REDUCE_SCATTER = 1,
+  VC_COLL_ALLGATHER = 2,
+  VC_COLL_BROADCAST = 3,
+  VC_COLL_SCATTER = 4,
+  VC_COLL_ALLTOALL = 5
+} vc_coll_t;
+
+/*
+ * AllReduce: recv[r][i] = sum over q of send[q][i], for every rank r and
+ * element i < count.  Latency-formula page, sections "Ring AllReduce",
+ * "Recursive Halving-Doubling" and "Double Binary Tree" (eqs.
+ * model-algo-ring-ar, model-algo-rhd-ar, model-algo-dbt-ar); hccl article,
+ * sections "Ring算法", "Tree算法".
+ *   send[r], recv[r]: `count` elements each.  send[r] == recv[r] (in place)
+ *   is allowed, as hccl_allreduce allows sendbuf == recvbuf.
+ *   algo: FUSED (rank-order sum in one pass), RING (ReduceScatter + AllGather
+ *   in 2(N-1) steps), RHD (2 log2 N rounds; VC_ERR_UNSUPPORTED unless nranks
+ *   is a power of 2), DBT (two mirrored heap trees, 2 floor(log2 N) levels).
+ */
+vc_status_t vc_allreduce(const void* const* send, void* const* recv, int nranks, size_t count,
+                         vc_dtype_t dtype, vc_op_t op, vc_algo_t algo, vc_stream_t stream);
+
+/*
+ * ReduceScatter: recv[r][j] = sum over q of send[q][r*recvcount + j].
+ * Latency-formula page, section "Ring ReduceScatter" (eq.
+ * model-algo-ring-reducescatter).
+ *   send[q]: nranks*recvcount elements; recv[r]: recvcount elements.  No in-place.
+ *   algo: FUSED or RING (N-1 steps; rank r's chain ends on rank r).
+ */
+vc_status_t vc_reduce_scatter(const void* const* send, void* const* recv, int nranks,
+                              size_t recvcount, vc_dtype_t dtype, vc_op_t op, vc_algo_t algo,
+                              vc_stream_t stream);
+
+/*
+ * AllGather: recv[r][q*sendcount + j] = send[q][j].  Latency-formula page,
+ * section "Ring AllGather" (eq. model-algo-ring-allgather).
+ *   send[q]: sendcount elements; recv[r]: nranks*sendcount elements.  No in-place.
+ *   algo: FUSED or RING (a local copy, then N-1 ring steps).
+ */
+vc_status_t vc_allgather(const void* const* send, void* const* recv, int nranks, size_t sendcount,
+                         vc_dtype_t dtype, vc_algo_t algo, vc_stream_t stream);
+
+/*
+ * Broadcast: recv[r][i] = send_root[i] for every rank r.  Broadcast/Scatter
+ * page, section "Broadcast" (eq. onetoall-bcast-semantic) and its algorithm
+ * sections.
+ *   send_root, recv[r]: `count` elements.  send_root == recv[root] is allowed.
+ *   algo: FUSED (one read, N writes), BINOMIAL (ceil(log2 N) steps),
+ *   SCATTER_ALLGATHER (binomial Scatter of N chunks, then a Ring AllGather).
+ */
+vc_status_t vc_broadcast(const void* send_root, void* const* recv, int nranks, size_t count,
+                         vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream);
+
+/*
+ * Scatter: recv[r][j] = send_root[r*recvcount + j].  Broadcast/Scatter page,
+ * section "Scatter" (eq. onetoall-scatter-semantic) and "二叉树 Scatter".
+ *   send_root: nranks*recvcount elements; recv[r]: recvcount elements.  No in-place.
+ *   algo: FUSED or BINOMIAL (ceil(log2 N) steps, halving sizes).
+ */
+vc_status_t vc_scatter(const void* send_root, void* const* recv, int nranks, size_t recvcount,
+                       vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream);
+
+/*
+ * AllToAll: recv[j][i*blockcount + e] = send[i][j*blockcount + e].
+ * Latency-formula page, section "AllToAll 算法怎么选" (eqs.
+ * model-algo-a2a-pairwise, model-algo-a2a-bruck).
+ *   send[i], recv[j]: nranks*blockcount elements.  No in-place.
+ *   algo: FUSED (one pass), PAIRWISE (N-1 exchange rounds plus the local
+ *   block), BRUCK (ceil(log2 N) rounds through two library scratch buffers).
+ */
+vc_status_t vc_alltoall(const void* const* send, void* const* recv, int nranks, size_t blockcount,
+                        vc_dtype_t dtype, vc_algo_t algo, vc_stream_t stream);
+
+/* Name of a status code (static string). */
+const char* vc_status_string(vc_status_t status);
+
+/* Text of the last error on the calling thread ("" if none). */
+const char* vc_last_error(void);
+
+/*
+ * busbw = algbw * factor: AllReduce 2(N-1)/N; AllGather, ReduceScatter,
+ * AllToAll (N-1)/N; Broadcast 1 (latency-formula page, table
+ * tbl-model-algo-busbw-coef).  Scatter is not in that table and gets (N-1)/N.
+ * Returns 0 for an unknown collective or nranks < 1.
+ */
+double vc_busbw_factor(vc_coll_t coll, int nranks);
+
+/*
+ * Schedule introspection (host only; no CUDA call, usable without a GPU).
+ *
+ * Builds the step plan a call with these arguments would execute and writes
+ * one entry per operand of every operation.  An operation reads its sources
+ * in the listed order (`pos`), adds them left to right (reduction steps) or
+ * copies its single source (copy steps), and writes the result to each of its
+ * destinations; it covers `nb` runs of `n` elements, run b starting
+ * b*stride_bytes after run 0.  All operations of one step are independent and
+ * run in one launch; steps run in order.
+ *   buf: 0 send, 1 recv, 2 library scratch; owner: the rank that holds it;
+ *   byte_off: from the start of that rank's buffer (scratch: of the scratch
+ *   block); dtype: storage type of the operand.
+ * Returns VC_ERR_INVALID_ARG if `capacity` is too small (with *n_entries set
+ * to the size needed).  *scratch_bytes receives the scratch the call needs,
+ * *n_steps the number of steps.
+ */
+typedef struct {
+  int32_t step;
+  int32_t op;     /* operation index within the step */
+  int32_t role;   /* 0 source, 1 destination */
+  int32_t pos;    /* position within the sources or destinations */
+  int32_t buf;    /* 0 send, 1 recv, 2 scratch */
+  int32_t owner;  /* rank */
+  int32_t dtype;  /* vc_dtype_t of the operand */
+  int32_t reduce; /* 1 for a reduction operation, 0 for a copy */
+  int64_t byte_off;
+  int64_t n;
+  int64_t nb;
+  int64_t stride_bytes;
+} vc_plan_entry_t;
+
+vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
+                             vc_dtype_t dtype, int root, int inplace, vc_plan_entry_t* entries,
+                             size_t capacity, size_t* n_entries, size_t* scratch_bytes,
+                             int* n_steps);
+
+/*
+ * Launch trace (off by default; host bookkeeping plus two CUDA events per
+ * launch while on).  While enabled, every kernel launch the library makes is
+ * bracketed by CUDA events recorded on the caller's stream, and a record
+ * keeps the collective, algorithm, step, kernel variant and the launch's
+ * algorithmic bytes (every operand of every operation read or written once,
+ * at its storage size).  vc_trace_enable(1) clears old records;
+ * vc_trace_read waits for the recorded events, writes up to `capacity`
+ * records with their event-timed durations and clears them.
+ *   kernel: 0 copy, 1 fp32 sum, 2 int32 sum, 3 bf16 sum; +4 when the
+ *   launch used the large parameter block (more than 16 operations or 64
+ *   operand pointers).
+ */
+typedef struct {
+  int32_t coll;   /* vc_coll_t */
+  int32_t algo;   /* vc_algo_t */
+  int32_t step;
+  int32_t kernel;
+  int64_t bytes;
+  int32_t nops;
+  float ms;
+} vc_trace_record_t;
+
+vc_status_t vc_trace_enable(int on);
+vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n_records);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int vc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VC_H_ */

@@ -1,0 +1,228 @@
+"""GPU path against the oracle, element by element, through the C ABI.
+
+Every collective, algorithm and dtype at sizes that span several tiles and
+ragged tails, odd rank counts, every root, in place, misaligned pointers, and
+the page-derived order witnesses.  Reductions are compared bit for bit with
+the oracle's simulation of the same schedule (same association); data
+movement and int32 sums are bit-exact by definition.  Canary bands around
+every device buffer catch stray writes.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_algorithms_virtual_gb300 as vc
+from oracle import schedules
+from synthetic_inputs import int32_bits, rank_buffers
+
+from .conftest import read_golden
+from .gpu_util import Guarded, first_diff, same_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from collective_communication_algorithms_virtual_gb300 import build
+
+    build.build()
+    vc.lib()
+    yield
+
+
+def _inputs(dtype, seed, N, n):
+    kind = {"f32": "uniform_f32", "bf16": "normal_bf16", "i32": "int32_bits"}[dtype]
+    return rank_buffers(kind, seed, N, n)
+
+
+def _run_allreduce(xs, algo, dtype, shift=0, inplace=False):
+    N, count = len(xs), len(xs[0])
+    sends = [Guarded(count, dtype, shift, fill=x) for x in xs]
+    recvs = sends if inplace else [Guarded(count, dtype, shift) for _ in range(N)]
+    vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo)
+    torch.cuda.synchronize()
+    assert all(g.guards_intact() for g in sends + recvs)
+    return [g.host() for g in recvs]
+
+
+def test_native_library_is_loaded():
+    x = [torch.ones(16, device="cuda") for _ in range(2)]
+    y = [torch.empty(16, device="cuda") for _ in range(2)]
+    vc.vc_allreduce(x, y, algo="ring")
+    torch.cuda.synchronize()
+    assert torch.equal(y[0], torch.full((16,), 2.0, device="cuda"))
+    maps = open("/proc/self/maps").read()
+    assert "libvcoll.so" in maps
+
+
+ALGOS_AR = schedules.ALGOS["allreduce"]
+AR_N = [1, 2, 3, 4, 5, 8, 16]
+AR_COUNTS = [1, 13, 4096, 65536 + 37, 1 << 20]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("N", AR_N)
+def test_allreduce_matches_oracle(N, dtype):
+    for count in AR_COUNTS:
+        xs = _inputs(dtype, 1000 + N + count, N, count)
+        for algo in ALGOS_AR:
+            if algo == "rhd" and N & (N - 1):
+                with pytest.raises(vc.VCError):
+                    _run_allreduce(xs, algo, dtype)
+                continue
+            want = schedules.allreduce(xs, algo, dtype).outputs
+            got = _run_allreduce(xs, algo, dtype)
+            for r in range(N):
+                assert same_bits(got[r], want[r]), (algo, N, count, dtype, r, first_diff(got[r], want[r]))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [3, 8])
+def test_allreduce_inplace_and_misaligned(N, dtype):
+    count = 4097 * 3
+    xs = _inputs(dtype, 77 + N, N, count)
+    for algo in ALGOS_AR:
+        if algo == "rhd" and N & (N - 1):
+            continue
+        want = schedules.allreduce(xs, algo, dtype).outputs
+        for shift, inplace in ((0, True), (1, False), (1, True), (3, False)):
+            got = _run_allreduce(xs, algo, dtype, shift=shift, inplace=inplace)
+            for r in range(N):
+                assert same_bits(got[r], want[r]), (algo, shift, inplace, r, first_diff(got[r], want[r]))
+
+
+def test_order_witnesses_on_gpu():
+    """The page-derived association of each schedule, checked on the device."""
+    for row in read_golden("order_witness_n4.txt"):
+        vals = [float(v) for v in row[1:5]]
+        algo = row[5]
+        want = np.repeat(np.array([float(v) for v in row[6:10]], dtype=np.float32), 4)
+        xs = [np.full(16, v, dtype=np.float32) for v in vals]
+        if algo.startswith("rs_"):
+            sends = [to_dev(x) for x in xs]
+            recvs = [torch.empty(4, device="cuda") for _ in range(4)]
+            vc.vc_reduce_scatter(sends, recvs, algo=algo[3:])
+            got = torch.cat(recvs).cpu().numpy()
+        else:
+            got = _run_allreduce(xs, algo, "f32")
+            for o in got:
+                assert same_bits(o, got[0])
+            got = got[0]
+        assert np.array_equal(got, want), (row[0], algo, got)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16])
+def test_reduce_scatter_allgather_match_oracle(N, dtype):
+    for rc in (1, 5, 4096, 40000 + 3):
+        xs = _inputs(dtype, 2000 + N + rc, N, N * rc)
+        for algo in schedules.ALGOS["reduce_scatter"]:
+            want = schedules.reduce_scatter(xs, algo, dtype).outputs
+            sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
+            recvs = [Guarded(rc, dtype) for _ in range(N)]
+            vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo=algo)
+            torch.cuda.synchronize()
+            assert all(g.guards_intact() for g in sends + recvs)
+            for r in range(N):
+                got = recvs[r].host()
+                assert same_bits(got, want[r]), ("rs", algo, N, rc, r, first_diff(got, want[r]))
+        ins = _inputs(dtype, 3000 + N + rc, N, rc)
+        for algo in schedules.ALGOS["allgather"]:
+            want = schedules.allgather(ins, algo, dtype).outputs
+            sends = [Guarded(rc, dtype, fill=x) for x in ins]
+            recvs = [Guarded(N * rc, dtype) for _ in range(N)]
+            vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo)
+            torch.cuda.synchronize()
+            assert all(g.guards_intact() for g in sends + recvs)
+            for r in range(N):
+                assert same_bits(recvs[r].host(), want[r]), ("ag", algo, N, rc, r)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 11, 16])
+def test_broadcast_scatter_match_oracle(N):
+    dtype = "i32"
+    for root in sorted({0, 1 % N, N - 1}):
+        for count in (1, 7, 4096 + 5, 300001):
+            A = int32_bits(4000 + root, N, count)
+            for algo in schedules.ALGOS["broadcast"]:
+                for inplace in (False, True):
+                    want = schedules.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
+                    recvs = [Guarded(count, dtype) for _ in range(N)]
+                    if inplace:
+                        recvs[root].t.copy_(to_dev(A))
+                        src = recvs[root].t
+                    else:
+                        src_g = Guarded(count, dtype, fill=A)
+                        src = src_g.t
+                    vc.vc_broadcast(src, [g.t for g in recvs], root=root, algo=algo)
+                    torch.cuda.synchronize()
+                    assert all(g.guards_intact() for g in recvs)
+                    for r in range(N):
+                        assert same_bits(recvs[r].host(), want[r]), ("bcast", algo, N, root, count, inplace, r)
+        for rc in (1, 3, 4096, 65537):
+            A = int32_bits(5000 + root, N, N * rc)
+            for algo in schedules.ALGOS["scatter"]:
+                want = schedules.scatter(A, N, root, algo, dtype).outputs
+                src_g = Guarded(N * rc, dtype, fill=A)
+                recvs = [Guarded(rc, dtype) for _ in range(N)]
+                vc.vc_scatter(src_g.t, [g.t for g in recvs], root=root, algo=algo)
+                torch.cuda.synchronize()
+                assert src_g.guards_intact() and all(g.guards_intact() for g in recvs)
+                for r in range(N):
+                    assert same_bits(recvs[r].host(), want[r]), ("scatter", algo, N, root, rc, r)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "i32"])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6, 7, 8, 16])
+def test_alltoall_matches_oracle(N, dtype):
+    for B in (1, 3, 1024, 20001):
+        xs = _inputs(dtype, 6000 + N + B, N, N * B)
+        for algo in schedules.ALGOS["alltoall"]:
+            want = schedules.alltoall(xs, algo, dtype).outputs
+            for shift in (0, 1):
+                sends = [Guarded(N * B, dtype, shift, fill=x) for x in xs]
+                recvs = [Guarded(N * B, dtype, shift) for _ in range(N)]
+                vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo=algo)
+                torch.cuda.synchronize()
+                assert all(g.guards_intact() for g in sends + recvs)
+                for j in range(N):
+                    assert same_bits(recvs[j].host(), want[j]), (algo, N, B, shift, j)
+
+
+def test_repeated_calls_reuse_scratch_and_agree():
+    """Scratch comes from the library's pool; back-to-back calls on one stream
+    (and on a second stream) give identical results."""
+    N, count = 8, (1 << 18) + 7
+    xs = _inputs("bf16", 9, N, count)
+    want = schedules.allreduce(xs, "ring", "bf16").outputs
+    sends = [to_dev(x) for x in xs]
+    outs = [[torch.empty_like(s) for s in sends] for _ in range(3)]
+    s2 = torch.cuda.Stream()
+    for i in range(3):
+        if i == 2:
+            with torch.cuda.stream(s2):
+                vc.vc_allreduce(sends, outs[i], algo="ring")
+        else:
+            vc.vc_allreduce(sends, outs[i], algo="ring")
+    torch.cuda.synchronize()
+    for i in range(3):
+        for r in range(N):
+            got = outs[i][r].cpu().view(torch.int16).numpy().view(np.uint16)
+            assert same_bits(got, want[r])
+
+
+def test_errors_leave_outputs_untouched():
+    N = 4
+    xs = [torch.ones(64, device="cuda") for _ in range(N)]
+    ys = [torch.zeros(64, device="cuda") for _ in range(N)]
+    with pytest.raises(vc.VCError) as e:
+        vc.vc_allreduce(xs, ys, algo="rhd", op="max")
+    assert e.value.status == 2
+    with pytest.raises(vc.VCError):
+        vc.vc_allreduce(xs, [ys[0]] * N, algo="ring")
+    torch.cuda.synchronize()
+    assert all(torch.count_nonzero(y).item() == 0 for y in ys)
