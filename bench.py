@@ -356,7 +356,7 @@ def run_ours(args) -> int:
            "clocks": clocks}
 
     # per-algorithm figures at 256 MiB and the message-size sweep (rank 0 only)
-    if rank == 0:
+    if rank == 0 and not args.no_per_algo:
         out["per_algo"] = per_algo(vc, send, recv, stream, M, peaks)
         if not args.no_sweep:
             out["sweep"] = sweep(vc, send, recv, stream)
@@ -467,6 +467,7 @@ def main(argv=None) -> int:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-per-algo", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
