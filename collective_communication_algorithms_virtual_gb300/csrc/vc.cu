@@ -976,4 +976,93 @@ VC_EXPORT vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity,
   });
 }
 
+// ---------------------------------------------------------------------------
+// Ring ReduceScatter without device allocation
+// ---------------------------------------------------------------------------
+// For callers that cannot allocate device memory during the call (see vc.h).
+// The partial sums use this fixed array instead of the library's pool.  Host
+// code may not use the array's name as a device address: it is looked up once
+// per device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[VC_NOALLOC_SCRATCH_BYTES];
+
+namespace vc {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+vc_status_t noalloc_scratch(int dev, char** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = static_cast<char*>(g_noalloc_ptr[dev]);
+  return VC_SUCCESS;
+}
+
+vc_status_t run_reduce_scatter_noalloc(const void* const* send, void* const* recv, int N, int64_t rc, DT dt,
+                                       cudaStream_t stream) {
+  if (N < 1 || N > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
+  if (!send || !recv) return fail(VC_ERR_INVALID_ARG, "null send or recv array");
+  if (rc < 0) return fail(VC_ERR_INVALID_ARG, "count too large");
+  if (rc == 0) return VC_SUCCESS;
+  if (rc > (INT64_MAX / 8) / N) return fail(VC_ERR_INVALID_ARG, "count too large");
+  const int64_t es = esize(dt);
+  const int64_t sbytes = rc * N * es, rbytes = rc * es;
+  for (int r = 0; r < N; ++r)
+    if (!send[r] || !recv[r]) return fail(VC_ERR_INVALID_ARG, "null send or recv buffer");
+  for (int i = 0; i < N; ++i) {
+    for (int j = i + 1; j < N; ++j)
+      if (overlap(recv[i], rbytes, recv[j], rbytes)) return fail(VC_ERR_INVALID_ARG, "receive buffers overlap");
+    for (int q = 0; q < N; ++q)
+      if (overlap(recv[i], rbytes, send[q], sbytes))
+        return fail(VC_ERR_INVALID_ARG, "a receive buffer overlaps a send buffer");
+  }
+  PlanArgs pa{Coll::ReduceScatter, Algo::Ring, N, rc, dt, 0, false};
+  Plan plan;
+  std::string why;
+  const PlanStatus ps = build_plan(pa, &plan, &why);
+  if (ps != PlanStatus::Ok) return plan_status(ps, why);
+  if (plan.scratch_bytes > static_cast<int64_t>(VC_NOALLOC_SCRATCH_BYTES))
+    return fail(VC_ERR_INVALID_ARG, "vc_reduce_scatter_noalloc needs " + std::to_string(plan.scratch_bytes) +
+                                        " bytes of scratch; the fixed array holds " +
+                                        std::to_string(VC_NOALLOC_SCRATCH_BYTES) +
+                                        " (2 * nranks * recvcount * 4 must not exceed it)");
+  DeviceState* st = nullptr;
+  int dev = 0;
+  vc_status_t rc_ = device_state(&st, &dev);
+  if (rc_ != VC_SUCCESS) return rc_;
+  char* scratch = nullptr;
+  rc_ = noalloc_scratch(dev, &scratch);
+  if (rc_ != VC_SUCCESS) return rc_;
+  const Bases b{send, recv, scratch};
+  int launches = 0;
+  TraceCtx tc;
+  tc.coll = static_cast<int>(Coll::ReduceScatter);
+  tc.algo = static_cast<int>(Algo::Ring);
+  for (size_t si = 0; si < plan.steps.size(); ++si) {
+    tc.step = static_cast<int>(si);
+    rc_ = launch_step(st, plan.steps[si], b, stream, &launches, tc);
+    if (rc_ != VC_SUCCESS) return rc_;
+  }
+  return VC_SUCCESS;
+}
+}  // namespace
+}  // namespace vc
+
+VC_EXPORT vc_status_t vc_reduce_scatter_noalloc(const void* const* send, void* const* recv, int nranks,
+                                                size_t recvcount, vc_dtype_t dtype, vc_op_t op,
+                                                vc_stream_t stream) {
+  return entry([&]() -> vc_status_t {
+    DT dt;
+    vc_status_t rc = to_dt(dtype, &dt);
+    if (rc != VC_SUCCESS) return rc;
+    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    return run_reduce_scatter_noalloc(send, recv, nranks, static_cast<int64_t>(recvcount), dt,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  });
+}
+
 VC_EXPORT int vc_version(void) { return 100; }

@@ -234,6 +234,35 @@ typedef struct {
 vc_status_t vc_trace_enable(int on);
 vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n_records);
 
+/*
+ * Ring ReduceScatter that allocates no device memory.
+ *
+ * The source pages have no counterpart to this call: it exists for callers
+ * that cannot allocate device memory while they run -- code inside a custom
+ * allocator or an out-of-memory handler, real-time loops that forbid
+ * cudaMalloc and pool growth, or hosts whose memory budget is fixed ahead of
+ * time.  It computes exactly what vc_reduce_scatter(..., VC_ALGO_RING, ...)
+ * computes (same schedule, same results bit for bit), but its partial sums
+ * live in one fixed array that the library reserves in every GPU's memory
+ * when the library is loaded on it, instead of in the library's pool.
+ *
+ *   send[q]: nranks*recvcount elements; recv[r]: recvcount elements; no in-place.
+ *   Scratch needed: 2 * nranks * recvcount * 4 bytes (fp32 and bf16 partials
+ *   are fp32, int32 partials int32), at most VC_NOALLOC_SCRATCH_BYTES
+ *   (16 MiB); larger calls return VC_ERR_INVALID_ARG and enqueue nothing.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array and leaves its last contents behind (no
+ *   part of it needs to start at zero: every partial sum is written before
+ *   it is read).  Calls whose work overlaps on the GPU -- on two streams, or
+ *   from two threads -- race on the array: serialise them.
+ */
+#define VC_NOALLOC_SCRATCH_BYTES (16u << 20)
+vc_status_t vc_reduce_scatter_noalloc(const void* const* send, void* const* recv, int nranks,
+                                      size_t recvcount, vc_dtype_t dtype, vc_op_t op,
+                                      vc_stream_t stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int vc_version(void);
 
