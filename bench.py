@@ -52,8 +52,8 @@ def busbw_factor(N: int) -> float:
     return 2.0 * (N - 1) / N
 
 
-def step_bus_bytes(bytes_per_rank: int, nalgos: int = len(ALGOS), N: int = NVR) -> float:
-    return nalgos * bytes_per_rank * busbw_factor(N)
+def step_bus_bytes(bytes_per_rank: int, nalgos: int | None = None, N: int = NVR) -> float:
+    return (len(ALGOS) if nalgos is None else nalgos) * bytes_per_rank * busbw_factor(N)
 
 
 def dist_env():
@@ -264,7 +264,8 @@ def config_block(bytes_per_rank: int) -> dict:
             "bytes_per_rank": bytes_per_rank, "algos": ALGOS,
             "step": "one out-of-place AllReduce per algorithm",
             "inputs": "uniform[-1,1) fp32, seed 2, PCG64 per (seed, rank)",
-            "l2": "inputs larger than L2 (2 GiB per buffer set), no flush",
+            "l2": (f"inputs larger than L2 ({NVR * bytes_per_rank >> 20} MiB per buffer set), no flush"
+                   if NVR * bytes_per_rank > (129 << 20) else "inputs fit in L2"),
             "parallelism": "replicas"}
 
 
@@ -286,7 +287,9 @@ def run_ours(args) -> int:
     import collective_communication_algorithms_virtual_gb300 as vc
     from synthetic_inputs import uniform_pm1_f32
 
-    N, M = NVR, BYTES_PER_RANK
+    global ALGOS
+    ALGOS = [a for a in args.algos.split(",") if a]
+    N, M = NVR, int(args.mib_per_rank * (1 << 20)) // 16 * 16
     count = M // 4
     host = [uniform_pm1_f32(2, r, count) for r in range(N)]
     send = [torch.from_numpy(h).to(dev) for h in host]
@@ -360,6 +363,9 @@ def run_ours(args) -> int:
         out["per_algo"] = per_algo(vc, send, recv, stream, M, peaks)
         if not args.no_sweep:
             out["sweep"] = sweep(vc, send, recv, stream)
+            out["alpha_beta"] = alpha_beta_fit(out["sweep"])
+        if not args.no_configs:
+            out["configs"] = other_configs(vc, dev, peaks)
 
     # end to end: pinned host inputs -> device -> four AllReduces -> all outputs back
     if not args.no_e2e:
@@ -412,18 +418,170 @@ def per_algo(vc, send, recv, stream, M, peaks):
     return res
 
 
+def time_graph(fn, stream, target_ms=3.0, max_reps=512):
+    """Per-call time with the calls captured in a CUDA graph: GPU time only,
+    no Python or launch-submission cost between calls."""
+    import torch
+
+    per = time_calls(fn, stream, min_ms=2.0, max_reps=64)
+    reps = int(max(1, min(max_reps, target_ms / max(per, 1e-4))))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(torch.cuda.current_stream())
+    for _ in range(3):
+        g.replay()
+    e1.record(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / (3 * reps)
+
+
+def plan_shape(vc, coll, algo, N, count, dtype="f32", root=0):
+    """(algorithmic bytes, launched steps) of one call, from the library's plan."""
+    entries, _, _ = vc.vc_plan_describe(coll, algo, N, count, dtype, root)
+    return sum(e.n * e.nb * (2 if e.dtype == 1 else 4) for e in entries), len({e.step for e in entries})
+
+
 def sweep(vc, send, recv, stream):
     N = len(send)
     res = {a: [] for a in ALGOS}
-    for lg in range(10, 29):
+    top = (send[0].numel() * 4).bit_length() - 1
+    for lg in range(10, top + 1):
         nbytes = 1 << lg
         sz = nbytes // 4
         for a in ALGOS:
-            ms = time_calls(lambda: vc.vc_allreduce([s[:sz] for s in send], [r[:sz] for r in recv[a]], algo=a),
-                            stream, min_ms=10.0)
-            res[a].append({"bytes_per_rank": nbytes, "us": ms * 1e3,
+            ins, outs = [s[:sz] for s in send], [r[:sz] for r in recv[a]]
+            fn = lambda: vc.vc_allreduce(ins, outs, algo=a)
+            ms_eager = time_calls(fn, stream, min_ms=5.0)
+            ms = time_graph(fn, stream)
+            hbm, steps = plan_shape(vc, "allreduce", a, N, sz)
+            res[a].append({"bytes_per_rank": nbytes, "us": ms * 1e3, "us_eager": ms_eager * 1e3,
                            "busbw": nbytes * busbw_factor(N) / (ms * 1e-3) / 1e9,
+                           "busbw_eager": nbytes * busbw_factor(N) / (ms_eager * 1e-3) / 1e9,
+                           "steps": steps, "algorithmic_bytes": hbm,
                            "l2_resident": 2 * N * nbytes <= (129 << 20)})
+    return res
+
+
+def alpha_beta_fit(sw: dict, min_bytes: int = 0) -> dict:
+    """Least-squares fit of T = steps * alpha + bytes / beta over the graph-timed
+    sweep of every algorithm: alpha is the cost of one dependent step (launch)
+    on this GPU, beta the HBM rate; the pages' model with a launch for a link
+    start-up and HBM for the link.  Reports the fit and, per pair of
+    algorithms, the crossover message size the fit predicts next to the one
+    measured."""
+    import numpy as np
+
+    rows, ts = [], []
+    for a, pts in sw.items():
+        for p in pts:
+            if p["bytes_per_rank"] >= min_bytes:
+                rows.append([p["steps"], p["algorithmic_bytes"]])
+                ts.append(p["us"] * 1e-6)
+    A, t = np.array(rows, dtype=np.float64), np.array(ts)
+    w = 1.0 / t  # relative error
+    coef, *_ = np.linalg.lstsq(A * w[:, None], t * w, rcond=None)
+    alpha, inv_beta = float(coef[0]), float(coef[1])
+    pred = A @ coef
+    out = {"alpha_us": alpha * 1e6, "beta_gbs": 1.0 / inv_beta / 1e9 if inv_beta > 0 else None,
+           "median_rel_err": float(np.median(np.abs(pred - t) / t)), "crossovers": {}}
+    algos = list(sw)
+    for i, a in enumerate(algos):
+        for b in algos[i + 1:]:
+            meas = None
+            for pa, pb in zip(sw[a], sw[b]):
+                if meas is None and (pa["us"] < pb["us"]) != (sw[a][0]["us"] < sw[b][0]["us"]):
+                    meas = pa["bytes_per_rank"]
+            def model(p):
+                return p["steps"] * alpha + p["algorithmic_bytes"] * inv_beta
+            predm = None
+            for pa, pb in zip(sw[a], sw[b]):
+                if predm is None and (model(pa) < model(pb)) != (model(sw[a][0]) < model(sw[b][0])):
+                    predm = pa["bytes_per_rank"]
+            out["crossovers"][f"{a}/{b}"] = {"measured_bytes_per_rank": meas, "predicted_bytes_per_rank": predm}
+    return out
+
+
+def other_configs(vc, dev, peaks):
+    """The other four workload configurations, timed (parity for them is in
+    tests/test_gpu_configs.py).  Device-side seeded torch inputs: the values
+    do not change the time of a copy or a sum."""
+    import torch
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+
+    def entry(coll, algo, N, count, dtype, fn, bytes_moved_per_rank, factor, root=0):
+        ms = time_calls(fn, stream, min_ms=50.0)
+        hbm, steps = plan_shape(vc, coll, algo, N, count, dtype, root)
+        return {"ms": ms, "busbw": bytes_moved_per_rank * factor / (ms * 1e-3) / 1e9,
+                "hbm_gbs": hbm / (ms * 1e-3) / 1e9, "frac_of_measured": hbm / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "frac_of_nominal_8TBs": hbm / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, "steps": steps,
+                "algorithmic_bytes": hbm}
+
+    # 1. Ring AllReduce, N=4, 4096 fp32 (latency-bound)
+    x = [torch.rand(4096, device=dev, generator=gen) * 2 - 1 for _ in range(4)]
+    y = [torch.empty_like(t) for t in x]
+    r = {}
+    for a in ("ring", "rhd", "dbt", "fused"):
+        fn = lambda a=a: vc.vc_allreduce(x, y, algo=a)
+        r[a] = {"us": time_graph(fn, stream) * 1e3, "us_eager": time_calls(fn, stream, min_ms=5.0) * 1e3}
+    res["ring_allreduce_n4_4096_f32"] = r
+    del x, y
+    # 3. bf16 gradient bucket, N=8, 64M elements: AllReduce, ReduceScatter, AllGather
+    N, cnt = 8, 64 << 20
+    xb = [(torch.randn(cnt, device=dev, generator=gen) * 1e-3).to(torch.bfloat16) for _ in range(N)]
+    yb = [torch.empty_like(t) for t in xb]
+    r = {}
+    for a in ("ring", "fused", "rhd", "dbt"):
+        r["allreduce_" + a] = entry("allreduce", a, N, cnt, "bf16", lambda a=a: vc.vc_allreduce(xb, yb, algo=a),
+                                    cnt * 2, 2 * (N - 1) / N)
+    rs_out = [t[: cnt // N] for t in yb]
+    for a in ("ring", "fused"):
+        r["reduce_scatter_" + a] = entry("reduce_scatter", a, N, cnt // N, "bf16",
+                                         lambda a=a: vc.vc_reduce_scatter(xb, rs_out, algo=a), cnt * 2, (N - 1) / N)
+    ag_in = [t[: cnt // N] for t in xb]
+    for a in ("ring", "fused"):
+        r["allgather_" + a] = entry("allgather", a, N, cnt // N, "bf16",
+                                    lambda a=a: vc.vc_allgather(ag_in, yb, algo=a), cnt * 2, (N - 1) / N)
+    res["bf16_bucket_n8_64M"] = r
+    del xb, yb, rs_out, ag_in
+    torch.cuda.empty_cache()
+    # 4. MoE AllToAll, N=8, 8192 x 4096 bf16 per rank in 8 blocks
+    cnt = 8192 * 4096
+    xa = [torch.randn(cnt, device=dev, generator=gen).to(torch.bfloat16) for _ in range(N)]
+    ya = [torch.empty_like(t) for t in xa]
+    r = {}
+    for a in ("pairwise", "bruck", "fused"):
+        r[a] = entry("alltoall", a, N, cnt // N, "bf16", lambda a=a: vc.vc_alltoall(xa, ya, algo=a),
+                     cnt * 2, (N - 1) / N)
+    res["moe_alltoall_n8_8192x4096_bf16"] = r
+    del xa, ya
+    torch.cuda.empty_cache()
+    # 5. Broadcast and Scatter, root 0, int32, 1 GiB total, N = 8 and 16
+    cnt = (1 << 30) // 4
+    src = torch.randint(-2**31, 2**31 - 1, (cnt,), dtype=torch.int32, device=dev, generator=gen)
+    r = {}
+    for N in (8, 16):
+        outs = [torch.empty_like(src) for _ in range(N)]
+        for a in ("binomial", "scatter_allgather", "fused"):
+            r[f"broadcast_n{N}_{a}"] = entry("broadcast", a, N, cnt, "i32",
+                                             lambda a=a: vc.vc_broadcast(src, outs, root=0, algo=a), cnt * 4, 1.0)
+        del outs
+        sc = [torch.empty(cnt // N, dtype=torch.int32, device=dev) for _ in range(N)]
+        for a in ("binomial", "fused"):
+            r[f"scatter_n{N}_{a}"] = entry("scatter", a, N, cnt // N, "i32",
+                                           lambda a=a: vc.vc_scatter(src, sc, root=0, algo=a), cnt * 4, (N - 1) / N)
+        del sc
+        torch.cuda.empty_cache()
+    res["bcast_scatter_int32_1GiB"] = r
     return res
 
 
@@ -466,8 +624,13 @@ def main(argv=None) -> int:
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algos", default="ring,rhd,dbt,fused",
+                    help="AllReduce algorithms in one step (profiling a single kernel uses one)")
+    ap.add_argument("--mib-per-rank", type=float, default=BYTES_PER_RANK / (1 << 20),
+                    help="message per rank (the workload is 256; smaller only for profiling captures)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-per-algo", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the other workload configurations")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
