@@ -35,11 +35,11 @@ class TraceRecord(ctypes.Structure):
                 ("ms", ctypes.c_float)]
 
 
-KERNEL_NAMES = {0: "copy", 1: "sum_f32", 2: "sum_i32", 3: "sum_bf16"}
+KERNEL_NAMES = {0: "copy", 1: "sum_f32", 2: "sum_i32", 3: "sum_bf16", 4: "sum_bf16_pure"}
 
 
 def kernel_name(code: int) -> str:
-    return KERNEL_NAMES[code & 3] + ("_large" if code & 4 else "")
+    return KERNEL_NAMES[code & 7] + ("_large" if code & 8 else "")
 
 
 class PlanEntry(ctypes.Structure):

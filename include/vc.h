@@ -217,9 +217,9 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  * at its storage size).  vc_trace_enable(1) clears old records;
  * vc_trace_read waits for the recorded events, writes up to `capacity`
  * records with their event-timed durations and clears them.
- *   kernel: 0 copy, 1 fp32 sum, 2 int32 sum, 3 bf16 sum; +4 when the
- *   launch used the large parameter block (more than 16 operations or 64
- *   operand pointers).
+ *   kernel: 0 copy, 1 fp32 sum, 2 int32 sum, 3 bf16 sum (bf16 and fp32
+ *   sources), 4 bf16 sum (bf16 sources only); +8 when the launch used the
+ *   large parameter block (more than 16 operations or 64 operand pointers).
  */
 typedef struct {
   int32_t coll;   /* vc_coll_t */
