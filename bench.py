@@ -488,8 +488,14 @@ def alpha_beta_fit(sw: dict, min_bytes: int = 0) -> dict:
     coef, *_ = np.linalg.lstsq(A * w[:, None], t * w, rcond=None)
     alpha, inv_beta = float(coef[0]), float(coef[1])
     pred = A @ coef
+    N = NVR
+    lg = np.log2(N)
     out = {"alpha_us": alpha * 1e6, "beta_gbs": 1.0 / inv_beta / 1e9 if inv_beta > 0 else None,
-           "median_rel_err": float(np.median(np.abs(pred - t) / t)), "crossovers": {}}
+           "median_rel_err": float(np.median(np.abs(pred - t) / t)), "crossovers": {},
+           # the latency-formula page's Ring/DBT crossover (link model) with these constants;
+           # on one GPU DBT moves fewer HBM bytes than Ring, so no crossover is measured
+           "page_ring_dbt_crossover_bytes": (2 * alpha * (1.0 / inv_beta) * ((N - 1) - lg) /
+                                             (lg - 2 * (N - 1) / N)) if inv_beta > 0 else None}
     algos = list(sw)
     for i, a in enumerate(algos):
         for b in algos[i + 1:]:

@@ -23,6 +23,9 @@ from .binding import (  # noqa: F401
     vc_plan_describe,
     vc_reduce_scatter,
     vc_scatter,
+    vc_select_algo,
+    vc_set_cost_model,
+    vc_get_cost_model,
     vc_status_string,
     vc_trace_enable,
     vc_trace_read,

@@ -18,7 +18,9 @@ VC_SUCCESS, VC_ERR_INVALID_ARG, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_NOMEM, V
 DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
 OPS = {"sum": 0, "max": 1, "min": 2}
 ALGOS = {"fused": 0, "ring": 1, "rhd": 2, "dbt": 3, "binomial": 4, "scatter_allgather": 5,
-         "pairwise": 6, "bruck": 7}
+         "pairwise": 6, "bruck": 7, "auto": 8}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
+COST_POLICIES = {"hbm": 0, "link": 1}
 COLLS = {"allreduce": 0, "reduce_scatter": 1, "allgather": 2, "broadcast": 3, "scatter": 4,
          "alltoall": 5}
 
@@ -85,6 +87,12 @@ def lib() -> ctypes.CDLL:
         L.vc_trace_enable.restype = I
         L.vc_trace_read.argtypes = [ctypes.POINTER(TraceRecord), Z, ctypes.POINTER(Z)]
         L.vc_trace_read.restype = I
+        L.vc_set_cost_model.argtypes = [I, ctypes.c_double, ctypes.c_double]
+        L.vc_set_cost_model.restype = I
+        L.vc_get_cost_model.argtypes = [ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        L.vc_get_cost_model.restype = I
+        L.vc_select_algo.argtypes = [I, I, Z, I, I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
+        L.vc_select_algo.restype = I
         L.vc_version.argtypes = []
         L.vc_version.restype = I
         _lib = L
@@ -196,6 +204,25 @@ def vc_last_error() -> str:
 
 def vc_version() -> int:
     return lib().vc_version()
+
+
+def vc_set_cost_model(policy="hbm", alpha_s: float = 0.0, beta_bytes_per_s: float = 0.0) -> None:
+    """Cost model behind algo="auto" (0 keeps the policy's default constant)."""
+    check(lib().vc_set_cost_model(_code(COST_POLICIES, policy), float(alpha_s), float(beta_bytes_per_s)))
+
+
+def vc_get_cost_model():
+    p, a, b = ctypes.c_int(0), ctypes.c_double(0), ctypes.c_double(0)
+    check(lib().vc_get_cost_model(ctypes.byref(p), ctypes.byref(a), ctypes.byref(b)))
+    return {0: "hbm", 1: "link"}[p.value], a.value, b.value
+
+
+def vc_select_algo(coll, nranks: int, count: int, dtype="f32", root: int = 0):
+    """(algorithm name, predicted seconds) that algo="auto" would use."""
+    a, t = ctypes.c_int(0), ctypes.c_double(0)
+    check(lib().vc_select_algo(_code(COLLS, coll), int(nranks), int(count), _code(DTYPES, dtype), int(root),
+                               ctypes.byref(a), ctypes.byref(t)))
+    return ALGO_NAMES[a.value], t.value
 
 
 def vc_trace_enable(on: bool = True) -> None:

@@ -24,6 +24,7 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <cmath>
 #include <functional>
 
 namespace vc {
@@ -553,6 +554,109 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   Builder b(a);
   b.build();
   *out = b.take();
+  return PlanStatus::Ok;
+}
+
+int64_t plan_bytes(const Plan& p) {
+  int64_t b = 0;
+  for (const Step& s : p.steps)
+    for (const Op& op : s.ops) {
+      int64_t per = 0;
+      for (const Operand& o : op.src) per += esize(o.dt);
+      for (const Operand& o : op.dst) per += esize(o.dt);
+      b += per * op.n * op.nb;
+    }
+  return b;
+}
+
+int plan_launch_steps(const Plan& p) {
+  int n = 0;
+  for (const Step& s : p.steps) n += s.ops.empty() ? 0 : 1;
+  return n;
+}
+
+namespace {
+
+// The pages' alpha-beta formulas with M the per-rank message in bytes
+// (latency-formula page: eqs. model-algo-ring-ar, -rhd-ar, -dbt-ar,
+// -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck;
+// Broadcast/Scatter page: eqs. binomial-bcast, binomial-scatter).
+double link_time(Coll c, Algo a, int N, double M, double al, double be) {
+  const double n = N, lg = std::log2(n), cl = ceil_log2(N);
+  switch (c) {
+    case Coll::AllReduce:
+      if (a == Algo::Ring) return 2 * (n - 1) * al + 2 * (n - 1) / n * M / be;
+      if (a == Algo::RHD) return 2 * lg * al + 2 * (n - 1) / n * M / be;
+      return 2 * lg * al + lg * M / be;  // DBT
+    case Coll::ReduceScatter:
+    case Coll::AllGather: return (n - 1) * al + (n - 1) / n * M / be;
+    case Coll::Broadcast:
+      if (a == Algo::Binomial) return cl * (al + M / be);
+      return cl * al + (n - 1) * M / (n * be) + (n - 1) * al + (n - 1) / n * M / be;  // scatter + ring AG
+    case Coll::Scatter: return cl * al + (n - 1) * M / (n * be);
+    case Coll::AllToAll:
+      if (a == Algo::Pairwise) return (n - 1) * (al + M / (n * be));
+      return cl * al + (n - 1) / n * M / be;  // Bruck
+  }
+  return 0;
+}
+
+}  // namespace
+
+PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double* predicted_s, std::string* why) {
+  std::vector<Algo> cand;
+  const bool link = cm.policy == CostPolicy::Link;
+  switch (a.coll) {
+    case Coll::AllReduce:
+      cand = link ? std::vector<Algo>{Algo::Ring, Algo::RHD, Algo::DBT}
+                  : std::vector<Algo>{Algo::Fused, Algo::Ring, Algo::RHD, Algo::DBT};
+      break;
+    case Coll::ReduceScatter:
+    case Coll::AllGather:
+      cand = link ? std::vector<Algo>{Algo::Ring} : std::vector<Algo>{Algo::Fused, Algo::Ring};
+      break;
+    case Coll::Broadcast:
+      cand = link ? std::vector<Algo>{Algo::Binomial, Algo::ScatterAllGather}
+                  : std::vector<Algo>{Algo::Fused, Algo::Binomial, Algo::ScatterAllGather};
+      break;
+    case Coll::Scatter:
+      cand = link ? std::vector<Algo>{Algo::Binomial} : std::vector<Algo>{Algo::Fused, Algo::Binomial};
+      break;
+    case Coll::AllToAll:
+      cand = link ? std::vector<Algo>{Algo::Pairwise, Algo::Bruck}
+                  : std::vector<Algo>{Algo::Fused, Algo::Pairwise, Algo::Bruck};
+      break;
+  }
+  const int64_t es = esize(a.dt);
+  const double M = (a.coll == Coll::AllReduce || a.coll == Coll::Broadcast) ? double(a.count * es)
+                                                                             : double(a.count * es * a.nranks);
+  bool found = false;
+  double best = 0;
+  PlanStatus last = PlanStatus::Unsupported;
+  for (Algo al : cand) {
+    PlanArgs pa = a;
+    pa.algo = al;
+    Plan p;
+    std::string w;
+    last = build_plan(pa, &p, &w);
+    if (last == PlanStatus::Invalid) {
+      if (why) *why = w;
+      return last;
+    }
+    if (last != PlanStatus::Ok) continue;
+    const double t = link ? link_time(a.coll, al, a.nranks, M, cm.alpha, cm.beta)
+                          : plan_launch_steps(p) * cm.alpha + double(plan_bytes(p)) / cm.beta;
+    if (!found || t < best) {
+      found = true;
+      best = t;
+      *out = al;
+    }
+  }
+  if (!found) {
+    if (why) *why = "no algorithm is defined for these arguments";
+    return PlanStatus::Unsupported;
+  }
+  if (predicted_s) *predicted_s = best;
   return PlanStatus::Ok;
 }
 

@@ -63,4 +63,20 @@ enum class PlanStatus { Ok, Invalid, Unsupported };
 // Builds the plan; on failure `why` says what is wrong.
 PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why);
 
+// Algorithmic bytes of a plan (every operand read or written once) and the
+// number of steps that launch work.
+int64_t plan_bytes(const Plan& p);
+int plan_launch_steps(const Plan& p);
+
+// Cost models for choosing an algorithm (see vc.h, vc_set_cost_model).
+enum class CostPolicy : int { Hbm = 0, Link = 1 };
+struct CostModel {
+  CostPolicy policy = CostPolicy::Hbm;
+  double alpha = 0;  // seconds per step
+  double beta = 0;   // bytes per second
+};
+
+// Picks the cheapest algorithm for a.coll under the model (a.algo is ignored).
+PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double* predicted_s, std::string* why);
+
 }  // namespace vc

@@ -679,6 +679,7 @@ const char* algo_name(Algo a) {
 struct Call {
   Coll coll;
   Algo algo;
+  bool autoalgo = false;  // VC_ALGO_AUTO: pick algo from the cost model
   int nranks;
   int64_t count;
   DT dt;
@@ -709,9 +710,38 @@ vc_status_t to_dt(vc_dtype_t d, DT* out) {
   return fail(VC_ERR_INVALID_ARG, "unknown dtype");
 }
 
-vc_status_t to_algo(vc_algo_t a, Algo* out) {
-  if (static_cast<int>(a) < 0 || static_cast<int>(a) > 7) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
-  *out = static_cast<Algo>(static_cast<int>(a));
+// Cost model of VC_ALGO_AUTO.
+std::mutex g_cost_mu;
+CostModel g_cost{CostPolicy::Hbm, 1.9e-6, 6.6e12};
+
+CostModel default_cost(CostPolicy p) {
+  return p == CostPolicy::Hbm ? CostModel{p, 1.9e-6, 6.6e12} : CostModel{p, 5e-6, 450e9};
+}
+CostModel current_cost() {
+  std::lock_guard<std::mutex> lk(g_cost_mu);
+  return g_cost;
+}
+
+// VC_ALGO_AUTO is returned as Algo::Fused with *is_auto set; the caller resolves it.
+vc_status_t to_algo(vc_algo_t a, Algo* out, bool* is_auto = nullptr) {
+  const int v = static_cast<int>(a);
+  if (v == VC_ALGO_AUTO && is_auto) {
+    *is_auto = true;
+    *out = Algo::Fused;
+    return VC_SUCCESS;
+  }
+  if (v < 0 || v > 7) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
+  if (is_auto) *is_auto = false;
+  *out = static_cast<Algo>(v);
+  return VC_SUCCESS;
+}
+
+vc_status_t resolve_auto(PlanArgs* pa) {
+  Algo chosen;
+  std::string why;
+  const PlanStatus ps = select_algo(*pa, current_cost(), &chosen, nullptr, &why);
+  if (ps != PlanStatus::Ok) return plan_status(ps, why);
+  pa->algo = chosen;
   return VC_SUCCESS;
 }
 
@@ -725,6 +755,10 @@ vc_status_t run(const Call& c) {
   if (c.count < 0) return fail(VC_ERR_INVALID_ARG, "count too large");
   // algorithm / rank-count support is decided before looking at sizes
   PlanArgs pa{c.coll, c.algo, N, c.count, c.dt, c.root, false};
+  if (c.autoalgo) {
+    const vc_status_t rs = resolve_auto(&pa);
+    if (rs != VC_SUCCESS) return rs;
+  }
   {
     Plan probe;
     std::string why;
@@ -799,7 +833,7 @@ vc_status_t run(const Call& c) {
   int launches = 0;
   TraceCtx tc;
   tc.coll = static_cast<int>(c.coll);
-  tc.algo = static_cast<int>(c.algo);
+  tc.algo = static_cast<int>(pa.algo);
   for (size_t si = 0; si < plan.steps.size(); ++si) {
     tc.step = static_cast<int>(si);
     rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
@@ -813,7 +847,7 @@ vc_status_t run(const Call& c) {
     size_t ops = 0;
     for (const Step& s : plan.steps) ops += s.ops.size();
     std::fprintf(stderr, "[vc] %s algo=%s nranks=%d count=%lld dtype=%d root=%d steps=%zu ops=%zu launches=%d scratch=%lld\n",
-                 coll_name(c.coll), algo_name(c.algo), N, static_cast<long long>(c.count), static_cast<int>(c.dt),
+                 coll_name(c.coll), algo_name(pa.algo), N, static_cast<long long>(c.count), static_cast<int>(c.dt),
                  c.root, plan.steps.size(), ops, launches, static_cast<long long>(plan.scratch_bytes));
   }
   return rc;
@@ -844,7 +878,7 @@ VC_EXPORT vc_status_t vc_allreduce(const void* const* send, void* const* recv, i
   return entry([&] {
     Call c;
     c.coll = Coll::AllReduce;
-    vc_status_t rc = to_algo(algo, &c.algo);
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
     if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
@@ -862,7 +896,7 @@ VC_EXPORT vc_status_t vc_reduce_scatter(const void* const* send, void* const* re
   return entry([&] {
     Call c;
     c.coll = Coll::ReduceScatter;
-    vc_status_t rc = to_algo(algo, &c.algo);
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
     if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
@@ -880,7 +914,7 @@ VC_EXPORT vc_status_t vc_allgather(const void* const* send, void* const* recv, i
   return entry([&] {
     Call c;
     c.coll = Coll::AllGather;
-    vc_status_t rc = to_algo(algo, &c.algo);
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
@@ -897,7 +931,7 @@ VC_EXPORT vc_status_t vc_broadcast(const void* send_root, void* const* recv, int
   return entry([&] {
     Call c;
     c.coll = Coll::Broadcast;
-    vc_status_t rc = to_algo(algo, &c.algo);
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
@@ -915,7 +949,7 @@ VC_EXPORT vc_status_t vc_scatter(const void* send_root, void* const* recv, int n
   return entry([&] {
     Call c;
     c.coll = Coll::Scatter;
-    vc_status_t rc = to_algo(algo, &c.algo);
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
@@ -933,7 +967,7 @@ VC_EXPORT vc_status_t vc_alltoall(const void* const* send, void* const* recv, in
   return entry([&] {
     Call c;
     c.coll = Coll::AllToAll;
-    vc_status_t rc = to_algo(algo, &c.algo);
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
@@ -959,6 +993,49 @@ VC_EXPORT const char* vc_status_string(vc_status_t s) {
 
 VC_EXPORT const char* vc_last_error(void) { return g_last_error.c_str(); }
 
+VC_EXPORT vc_status_t vc_set_cost_model(vc_cost_policy_t policy, double alpha_s, double beta_bytes_per_s) {
+  return entry([&]() -> vc_status_t {
+    if (policy != VC_COST_HBM && policy != VC_COST_LINK) return fail(VC_ERR_INVALID_ARG, "unknown cost policy");
+    CostModel m = default_cost(static_cast<CostPolicy>(static_cast<int>(policy)));
+    if (alpha_s > 0) m.alpha = alpha_s;
+    if (beta_bytes_per_s > 0) m.beta = beta_bytes_per_s;
+    std::lock_guard<std::mutex> lk(g_cost_mu);
+    g_cost = m;
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_get_cost_model(vc_cost_policy_t* policy, double* alpha_s, double* beta_bytes_per_s) {
+  return entry([&]() -> vc_status_t {
+    const CostModel m = current_cost();
+    if (policy) *policy = static_cast<vc_cost_policy_t>(static_cast<int>(m.policy));
+    if (alpha_s) *alpha_s = m.alpha;
+    if (beta_bytes_per_s) *beta_bytes_per_s = m.beta;
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_select_algo(vc_coll_t coll, int nranks, size_t count, vc_dtype_t dtype, int root,
+                                     vc_algo_t* algo, double* predicted_s) {
+  return entry([&]() -> vc_status_t {
+    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 5) return fail(VC_ERR_INVALID_ARG, "unknown collective");
+    if (!algo) return fail(VC_ERR_INVALID_ARG, "null algo");
+    PlanArgs pa;
+    pa.coll = static_cast<Coll>(static_cast<int>(coll));
+    vc_status_t rc = to_dt(dtype, &pa.dt);
+    if (rc != VC_SUCCESS) return rc;
+    pa.nranks = nranks;
+    pa.count = static_cast<int64_t>(count);
+    pa.root = root;
+    Algo chosen;
+    std::string why;
+    const PlanStatus ps = select_algo(pa, current_cost(), &chosen, predicted_s, &why);
+    if (ps != PlanStatus::Ok) return plan_status(ps, why);
+    *algo = static_cast<vc_algo_t>(static_cast<int>(chosen));
+    return VC_SUCCESS;
+  });
+}
+
 VC_EXPORT double vc_busbw_factor(vc_coll_t coll, int nranks) {
   if (nranks < 1) return 0.0;
   const double N = nranks;
@@ -980,13 +1057,18 @@ VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nrank
     if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 5) return fail(VC_ERR_INVALID_ARG, "unknown collective");
     PlanArgs pa;
     pa.coll = static_cast<Coll>(static_cast<int>(coll));
-    vc_status_t rc = to_algo(algo, &pa.algo);
+    bool is_auto = false;
+    vc_status_t rc = to_algo(algo, &pa.algo, &is_auto);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &pa.dt);
     if (rc != VC_SUCCESS) return rc;
     pa.nranks = nranks;
     pa.count = static_cast<int64_t>(count);
     pa.root = root;
     pa.inplace = inplace != 0;
+    if (is_auto) {
+      rc = resolve_auto(&pa);
+      if (rc != VC_SUCCESS) return rc;
+    }
     Plan plan;
     std::string why;
     const PlanStatus ps = build_plan(pa, &plan, &why);

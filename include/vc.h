@@ -79,7 +79,8 @@ typedef enum {
   VC_ALGO_BINOMIAL = 4,          /* Broadcast, Scatter                                 */
   VC_ALGO_SCATTER_ALLGATHER = 5, /* Broadcast                                          */
   VC_ALGO_PAIRWISE = 6,          /* AllToAll                                           */
-  VC_ALGO_BRUCK = 7              /* AllToAll                                           */
+  VC_ALGO_BRUCK = 7,             /* AllToAll                                           */
+  VC_ALGO_AUTO = 8               /* any collective: cheapest under the cost model      */
 } vc_algo_t;
 
 typedef enum {
@@ -156,6 +157,41 @@ vc_status_t vc_scatter(const void* send_root, void* const* recv, int nranks, siz
  */
 vc_status_t vc_alltoall(const void* const* send, void* const* recv, int nranks, size_t blockcount,
                         vc_dtype_t dtype, vc_algo_t algo, vc_stream_t stream);
+
+/*
+ * Cost model behind VC_ALGO_AUTO (process-wide, thread-safe).  The model is
+ * the latency-formula page's alpha-beta (Hockney) model, T = alpha terms +
+ * data terms.
+ *
+ *   VC_COST_HBM (default): the model on one GPU, where every virtual rank
+ *     lives in the same HBM: T = (steps that launch work) * alpha +
+ *     (algorithmic bytes the call reads and writes) / beta, both taken from
+ *     the call's plan.  Candidates: every algorithm of the collective, the
+ *     fused one included.  Defaults: alpha = 1.9e-6 s (one dependent step on
+ *     a GB300 with programmatic dependent launch, fitted to the message-size
+ *     sweep), beta = 6.6e12 B/s (measured HBM copy rate).
+ *   VC_COST_LINK: the pages' own formulas with M the per-rank message and
+ *     beta a link bandwidth (eqs. model-algo-ring-ar, -rhd-ar, -dbt-ar,
+ *     -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck;
+ *     Broadcast/Scatter page eqs. binomial-bcast, binomial-scatter).
+ *     Candidates: the pages' algorithms only (no fused).  Defaults: alpha =
+ *     5e-6 s, beta = 450e9 B/s, the page's NVLink example.
+ *
+ * alpha <= 0 or beta <= 0 selects the policy's default.  Ties go to the
+ * first candidate in enum order.
+ */
+typedef enum { VC_COST_HBM = 0, VC_COST_LINK = 1 } vc_cost_policy_t;
+
+vc_status_t vc_set_cost_model(vc_cost_policy_t policy, double alpha_s, double beta_bytes_per_s);
+vc_status_t vc_get_cost_model(vc_cost_policy_t* policy, double* alpha_s, double* beta_bytes_per_s);
+
+/*
+ * The algorithm VC_ALGO_AUTO would run for these arguments and the time the
+ * model predicts for it (host only, no CUDA call).  `count` follows the
+ * collective's convention; `root` is used by Broadcast and Scatter.
+ */
+vc_status_t vc_select_algo(vc_coll_t coll, int nranks, size_t count, vc_dtype_t dtype, int root,
+                           vc_algo_t* algo, double* predicted_s);
 
 /* Name of a status code (static string). */
 const char* vc_status_string(vc_status_t status);

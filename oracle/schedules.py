@@ -56,11 +56,19 @@ class Result:
     outputs: list
     log: TransferLog
     hbm_bytes: int
+    local_steps: int = 0  # steps that only copy within a rank (no message)
 
     @property
     def nsteps(self) -> int:
         """Steps that carry messages: the coefficient of alpha."""
         return len(self.log.steps())
+
+    @property
+    def launch_steps(self) -> int:
+        """Steps that move any data on one device (messages or local copies)."""
+        if self.nsteps == 0:
+            return 1 if self.hbm_bytes > 0 else 0
+        return self.nsteps + self.local_steps
 
 
 @dataclass
@@ -697,7 +705,7 @@ def _alltoall_pairwise(inputs, dtype, B):
                              src_off=j * B, dst_off=i * B))
             bm.rw(B, bm.e_in, bm.e_out)
         _run_step(log, k, msgs)
-    return Result(out, log, bm.total)
+    return Result(out, log, bm.total, local_steps=1 if N > 1 else 0)
 
 
 def _alltoall_bruck(inputs, dtype, B):

@@ -40,8 +40,9 @@ class TransferLog:
         self.records.append(Transfer(**kw))
 
     def steps(self) -> list[int]:
-        """Distinct step indices that carry at least one message, in order."""
-        return sorted({t.step for t in self.records})
+        """Distinct step indices that carry data (a message of at least one
+        element), in order."""
+        return sorted({t.step for t in self.records if t.n > 0})
 
     def bytes_sent_by(self, rank: int) -> int:
         return sum(t.nbytes for t in self.records if t.src == rank)

@@ -292,3 +292,22 @@ np.save(sys.argv[1], np.stack(out))
             subprocess.run([sys.executable, "-c", code, path], cwd=root, env=env, check=True)
             outs.append(np.load(path))
         assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_auto_runs_the_selected_algorithm():
+    N, count = 8, 200003
+    xs = _inputs("f32", 21, N, count)
+    sends = [to_dev(x) for x in xs]
+    try:
+        for policy in ("hbm", "link"):
+            vc.vc_set_cost_model(policy)
+            chosen, _ = vc.vc_select_algo("allreduce", N, count, "f32")
+            got = [torch.empty_like(s) for s in sends]
+            vc.vc_allreduce(sends, got, algo="auto")
+            want = [torch.empty_like(s) for s in sends]
+            vc.vc_allreduce(sends, want, algo=chosen)
+            torch.cuda.synchronize()
+            for r in range(N):
+                assert torch.equal(got[r], want[r]), (policy, chosen, r)
+    finally:
+        vc.vc_set_cost_model("hbm")
