@@ -527,6 +527,8 @@ def other_configs(vc, dev, peaks):
     def entry(coll, algo, N, count, dtype, fn, bytes_moved_per_rank, factor, root=0):
         ms = time_calls(fn, stream, min_ms=50.0)
         hbm, steps = plan_shape(vc, coll, algo, N, count, dtype, root)
+        if algo.startswith("pipe_"):
+            steps = (steps, "chunks from the cost model")
         return {"ms": ms, "busbw": bytes_moved_per_rank * factor / (ms * 1e-3) / 1e9,
                 "hbm_gbs": hbm / (ms * 1e-3) / 1e9, "frac_of_measured": hbm / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "frac_of_nominal_8TBs": hbm / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, "steps": steps,
@@ -577,7 +579,7 @@ def other_configs(vc, dev, peaks):
     r = {}
     for N in (8, 16):
         outs = [torch.empty_like(src) for _ in range(N)]
-        for a in ("binomial", "scatter_allgather", "fused"):
+        for a in ("binomial", "scatter_allgather", "fused", "pipe_chain", "pipe_tree"):
             r[f"broadcast_n{N}_{a}"] = entry("broadcast", a, N, cnt, "i32",
                                              lambda a=a: vc.vc_broadcast(src, outs, root=0, algo=a), cnt * 4, 1.0)
         del outs

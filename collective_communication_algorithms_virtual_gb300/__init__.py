@@ -18,6 +18,9 @@ from .binding import (  # noqa: F401
     vc_allreduce,
     vc_alltoall,
     vc_broadcast,
+    vc_broadcast_pipelined,
+    vc_gather,
+    vc_reduce,
     vc_busbw_factor,
     vc_last_error,
     vc_plan_describe,

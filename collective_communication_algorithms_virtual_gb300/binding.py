@@ -18,11 +18,11 @@ VC_SUCCESS, VC_ERR_INVALID_ARG, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_NOMEM, V
 DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
 OPS = {"sum": 0, "max": 1, "min": 2}
 ALGOS = {"fused": 0, "ring": 1, "rhd": 2, "dbt": 3, "binomial": 4, "scatter_allgather": 5,
-         "pairwise": 6, "bruck": 7, "auto": 8}
+         "pairwise": 6, "bruck": 7, "auto": 8, "pipe_chain": 9, "pipe_tree": 10}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 COST_POLICIES = {"hbm": 0, "link": 1}
 COLLS = {"allreduce": 0, "reduce_scatter": 1, "allgather": 2, "broadcast": 3, "scatter": 4,
-         "alltoall": 5}
+         "alltoall": 5, "gather": 6, "reduce": 7}
 
 
 class VCError(RuntimeError):
@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
             "vc_broadcast": [P, PP, I, Z, I, I, I, V],
             "vc_scatter": [P, PP, I, Z, I, I, I, V],
             "vc_alltoall": [PP, PP, I, Z, I, I, V],
+            "vc_broadcast_pipelined": [P, PP, I, Z, I, I, I, I, V],
+            "vc_gather": [PP, P, I, Z, I, I, I, V],
+            "vc_reduce": [PP, P, I, Z, I, I, I, I, V],
         }.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -80,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.vc_last_error.restype = ctypes.c_char_p
         L.vc_busbw_factor.argtypes = [I, I]
         L.vc_busbw_factor.restype = ctypes.c_double
-        L.vc_plan_describe.argtypes = [I, I, I, Z, I, I, I, ctypes.POINTER(PlanEntry), Z,
+        L.vc_plan_describe.argtypes = [I, I, I, Z, I, I, I, I, ctypes.POINTER(PlanEntry), Z,
                                        ctypes.POINTER(Z), ctypes.POINTER(Z), ctypes.POINTER(I)]
         L.vc_plan_describe.restype = I
         L.vc_trace_enable.argtypes = [I]
@@ -190,6 +193,29 @@ def vc_alltoall(send, recv, algo="fused", stream=None) -> None:
                             _dtype_code(send[0]), _code(ALGOS, algo), _stream_handle(stream, send[0])))
 
 
+def vc_broadcast_pipelined(send_root, recv, root=0, algo="pipe_tree", nchunks=0, stream=None) -> None:
+    """Chunked Broadcast; nchunks=0 takes the cost model's optimum."""
+    N = len(recv)
+    check(lib().vc_broadcast_pipelined(ctypes.c_void_p(send_root.data_ptr()), _ptr_array(_ptrs(recv)), N,
+                                       recv[0].numel(), _dtype_code(send_root), int(root), _code(ALGOS, algo),
+                                       int(nchunks), _stream_handle(stream, send_root)))
+
+
+def vc_gather(send, recv_root, root=0, algo="fused", stream=None) -> None:
+    """recv_root = concatenation of send[0..N-1] (on the root only)."""
+    N = len(send)
+    check(lib().vc_gather(_ptr_array(_ptrs(send)), ctypes.c_void_p(recv_root.data_ptr()), N, send[0].numel(),
+                          _dtype_code(send[0]), int(root), _code(ALGOS, algo), _stream_handle(stream, send[0])))
+
+
+def vc_reduce(send, recv_root, root=0, algo="fused", op="sum", stream=None) -> None:
+    """recv_root = sum over ranks of send[q]; ``recv_root is send[root]`` allowed."""
+    N = len(send)
+    check(lib().vc_reduce(_ptr_array(_ptrs(send)), ctypes.c_void_p(recv_root.data_ptr()), N, send[0].numel(),
+                          _dtype_code(send[0]), _code(OPS, op), int(root), _code(ALGOS, algo),
+                          _stream_handle(stream, send[0])))
+
+
 def vc_busbw_factor(coll, nranks: int) -> float:
     return lib().vc_busbw_factor(_code(COLLS, coll), int(nranks))
 
@@ -242,14 +268,15 @@ def vc_trace_read(capacity: int = 1 << 20) -> list:
     return out
 
 
-def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False):
+def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,
+                     nchunks: int = 0):
     """The step plan the library would run, as (entries, scratch_bytes, n_steps);
     host only, needs no GPU."""
     L = lib()
     need, scratch = ctypes.c_size_t(0), ctypes.c_size_t(0)
     steps = ctypes.c_int(0)
     args = (_code(COLLS, coll), _code(ALGOS, algo), int(nranks), int(count), _code(DTYPES, dtype),
-            int(root), int(bool(inplace)))
+            int(root), int(bool(inplace)), int(nchunks))
     check(L.vc_plan_describe(*args, None, 0, ctypes.byref(need), ctypes.byref(scratch), ctypes.byref(steps)))
     buf = (PlanEntry * max(1, need.value))()
     check(L.vc_plan_describe(*args, buf, need.value, ctypes.byref(need), ctypes.byref(scratch),

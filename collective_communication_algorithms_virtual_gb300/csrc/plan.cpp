@@ -77,6 +77,8 @@ class Builder {
       case Coll::Broadcast: broadcast(); break;
       case Coll::Scatter: scatter(); break;
       case Coll::AllToAll: alltoall(); break;
+      case Coll::Gather: gather(); break;
+      case Coll::Reduce: reduce(); break;
     }
   }
 
@@ -349,6 +351,10 @@ class Builder {
       if (!dst.empty()) add(new_step(Mode::Copy), {S(root, 0)}, dst, count);
       return;
     }
+    if (a_.algo == Algo::PipeChain || a_.algo == Algo::PipeTree) {
+      broadcast_pipelined();
+      return;
+    }
     if (a_.algo == Algo::Binomial) {
       // At distance d = 2^(L-1-s), every relative rank v with v mod 2d == 0
       // and v + d < N sends the whole message to v + d.
@@ -377,6 +383,122 @@ class Builder {
       for (int r = 0; r < N_; ++r) {
         const int c = md(r - s - 1, N_);
         copy(st, R(md(r - 1, N_), ch.lo(c)), R(r, ch.lo(c)), ch.len(c));
+      }
+    }
+  }
+
+  // Chunked Broadcasts (Broadcast/Scatter page, sections "分块链式流水线" and
+  // "分块二叉树流水线"): the message is cut into k chunks and chunk j follows
+  // the unpipelined route delayed by j steps -- along the chain, relative rank
+  // v forwards chunk j to v+1 at step v+j (N+k-2 steps); down the binomial
+  // tree, chunk j takes binomial step s at step j+s (ceil(log2 N)+k-1 steps).
+  // The pages give the step counts and chunk sizes; following the unpipelined
+  // route with a delay per chunk is the reading taken.  In any one step a rank
+  // receives one chunk and forwards other, earlier chunks.
+  void broadcast_pipelined() {
+    const int k = std::max(1, a_.nchunks);
+    const Chunks ch(a_.count, k, es_);
+    const int root = a_.root;
+    const bool chain = a_.algo == Algo::PipeChain;
+    const int L = ceil_log2(N_);
+    const int nsteps = chain ? N_ + k - 2 : L + k - 1;
+    for (int t = 0; t < nsteps; ++t) {
+      const size_t st = new_step(Mode::Copy);
+      if (t == 0 && !a_.inplace) copy(st, S(root, 0), R(root, 0), count_all());
+      for (int j = 0; j < k; ++j) {
+        const int s = t - j;
+        if (chain) {
+          if (s < 0 || s >= N_ - 1) continue;
+          const int v = s;
+          copy(st, v == 0 ? S(root, ch.lo(j)) : R(absr(v), ch.lo(j)), R(absr(v + 1), ch.lo(j)), ch.len(j));
+        } else {
+          if (s < 0 || s >= L) continue;
+          const int d = 1 << (L - 1 - s);
+          for (int v = 0; v + d < N_; v += 2 * d)
+            copy(st, v == 0 ? S(root, ch.lo(j)) : R(absr(v), ch.lo(j)), R(absr(v + d), ch.lo(j)), ch.len(j));
+        }
+      }
+    }
+  }
+  int64_t count_all() const { return a_.count; }
+
+  // Gather: the Scatter run backwards (Broadcast/Scatter page, section
+  // "对偶性：Scatter 与 Gather").  Distances 1, 2, 4, ...: relative rank v with
+  // v mod 2d == d hands the chunks of relative ranks [v, min(v+d, N)) -- its
+  // own input and what its subtree gave it, kept in its staging scratch -- to
+  // v - d; the root places them straight into its receive buffer.
+  void gather() {
+    const int64_t rc = a_.count;
+    if (rc == 0) return;
+    const int root = a_.root;
+    if (a_.algo == Algo::Fused || N_ == 1) {
+      const size_t st = new_step(Mode::Copy);
+      for (int q = 0; q < N_; ++q) copy(st, S(q, 0), R(root, q * rc), rc);
+      return;
+    }
+    const int L = ceil_log2(N_);
+    std::vector<int64_t> stage(N_, 0);
+    for (int v = 1; v < N_; ++v) {
+      const int cap = std::min(lowbit(v), N_ - v) - 1;
+      if (cap > 0) stage[v] = alloc(cap * rc * es_);
+    }
+    auto stage_op = [&](int v, int q) { return Sc(absr(v), stage[v] + (q - v - 1) * rc * es_, a_.dt); };
+    for (int s = 0; s < L; ++s) {
+      const int d = 1 << s;
+      const size_t st = new_step(Mode::Copy);
+      if (s == 0) copy(st, S(root, 0), R(root, root * rc), rc);
+      for (int u = 0; u + d < N_; u += 2 * d) {
+        const int v = u + d, end = std::min(v + d, N_);
+        auto dst = [&](int q) { return u == 0 ? R(root, absr(q) * rc) : stage_op(u, q); };
+        copy(st, S(absr(v), 0), dst(v), rc);
+        int q = v + 1;
+        while (q < end) {  // runs contiguous at both ends (the root's buffer wraps past rank N-1)
+          int q2 = q + 1;
+          while (q2 < end && !(u == 0 && absr(q2) == 0)) ++q2;
+          copy(st, stage_op(v, q), dst(q), int64_t(q2 - q) * rc);
+          q = q2;
+        }
+      }
+    }
+  }
+
+  // Reduce to the root: the binomial Broadcast run backwards with adds
+  // (latency-formula page, section "Broadcast / Reduce 怎么用 Tree 算法").
+  // Distances 1, 2, 4, ...: relative rank u with u mod 2d == 0 adds the value
+  // of u + d (its partial sum, or its input if it has none yet) to its own.
+  // Partial sums live in scratch (fp32 for bf16); the root's last step writes
+  // the (rounded) result into its receive buffer, which may be its input.
+  void reduce() {
+    const int64_t count = a_.count;
+    if (count == 0) return;
+    const int root = a_.root;
+    if (N_ == 1) {
+      if (!a_.inplace) copy(new_step(Mode::Copy), S(0, 0), R(0, 0), count);
+      return;
+    }
+    if (a_.algo == Algo::Fused) {
+      std::vector<Operand> src;
+      for (int q = 0; q < N_; ++q) src.push_back(S(q, 0));
+      add(new_step(reduce_mode()), src, {R(root, 0)}, count);
+      return;
+    }
+    const int L = ceil_log2(N_);
+    const DT adt = acc_dt();
+    std::vector<int64_t> base(N_, -1);
+    for (int u = 0; u + 1 < N_; u += 2)
+      if (u != 0 || bf16()) base[u] = alloc(count * esize(adt));
+    auto P = [&](int u) { return base[u] >= 0 ? Sc(absr(u), base[u], adt) : R(root, 0); };
+    std::vector<bool> partial(N_, false);
+    for (int s = 0; s < L; ++s) {
+      const int d = 1 << s;
+      const size_t st = new_step(reduce_mode());
+      for (int u = 0; u + d < N_; u += 2 * d) {
+        const int v = u + d;
+        const Operand own = partial[u] ? P(u) : S(absr(u), 0);
+        const Operand other = partial[v] ? P(v) : S(absr(v), 0);
+        const bool last = u == 0 && s == L - 1;
+        add(st, {own, other}, {last ? R(root, 0) : P(u)}, count);
+        partial[u] = true;
       }
     }
   }
@@ -533,8 +655,10 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   };
   if (a.nranks < 1 || a.nranks > 64) return bad(PlanStatus::Invalid, "nranks must be in [1, 64]");
   if (a.count < 0) return bad(PlanStatus::Invalid, "negative count");
-  const bool rooted = a.coll == Coll::Broadcast || a.coll == Coll::Scatter;
+  const bool rooted = a.coll == Coll::Broadcast || a.coll == Coll::Scatter || a.coll == Coll::Gather ||
+                      a.coll == Coll::Reduce;
   if (rooted && (a.root < 0 || a.root >= a.nranks)) return bad(PlanStatus::Invalid, "root outside [0, nranks)");
+  if (a.nchunks < 1 || a.nchunks > 1024) return bad(PlanStatus::Invalid, "nchunks must be in [1, 1024]");
   bool ok = false;
   switch (a.coll) {
     case Coll::AllReduce:
@@ -547,7 +671,10 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
       break;
     case Coll::Scatter: ok = a.algo == Algo::Fused || a.algo == Algo::Binomial; break;
     case Coll::AllToAll: ok = a.algo == Algo::Fused || a.algo == Algo::Pairwise || a.algo == Algo::Bruck; break;
+    case Coll::Gather:
+    case Coll::Reduce: ok = a.algo == Algo::Fused || a.algo == Algo::Binomial; break;
   }
+  if (a.coll == Coll::Broadcast && (a.algo == Algo::PipeChain || a.algo == Algo::PipeTree)) ok = true;
   if (!ok) return bad(PlanStatus::Unsupported, "algorithm not defined for this collective");
   if (a.coll == Coll::AllReduce && a.algo == Algo::RHD && !is_pow2(a.nranks))
     return bad(PlanStatus::Unsupported, "recursive halving-doubling needs nranks a power of 2");
@@ -581,7 +708,7 @@ namespace {
 // (latency-formula page: eqs. model-algo-ring-ar, -rhd-ar, -dbt-ar,
 // -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck;
 // Broadcast/Scatter page: eqs. binomial-bcast, binomial-scatter).
-double link_time(Coll c, Algo a, int N, double M, double al, double be) {
+double link_time(Coll c, Algo a, int N, double M, double al, double be, double k) {
   const double n = N, lg = std::log2(n), cl = ceil_log2(N);
   switch (c) {
     case Coll::AllReduce:
@@ -592,8 +719,12 @@ double link_time(Coll c, Algo a, int N, double M, double al, double be) {
     case Coll::AllGather: return (n - 1) * al + (n - 1) / n * M / be;
     case Coll::Broadcast:
       if (a == Algo::Binomial) return cl * (al + M / be);
+      if (a == Algo::PipeChain) return (n + k - 2) * (al + M / (k * be));
+      if (a == Algo::PipeTree) return (cl + k - 1) * (al + M / (k * be));
       return cl * al + (n - 1) * M / (n * be) + (n - 1) * al + (n - 1) / n * M / be;  // scatter + ring AG
-    case Coll::Scatter: return cl * al + (n - 1) * M / (n * be);
+    case Coll::Scatter:
+    case Coll::Gather: return cl * al + (n - 1) * M / (n * be);
+    case Coll::Reduce: return lg * (al + M / be);
     case Coll::AllToAll:
       if (a == Algo::Pairwise) return (n - 1) * (al + M / (n * be));
       return cl * al + (n - 1) / n * M / be;  // Bruck
@@ -602,6 +733,15 @@ double link_time(Coll c, Algo a, int N, double M, double al, double be) {
 }
 
 }  // namespace
+
+int default_chunks(Algo a, int nranks, int64_t count, DT dt, const CostModel& cm) {
+  const double h = a == Algo::PipeChain ? nranks - 2 : ceil_log2(nranks) - 1;
+  const double M = double(count) * esize(dt);
+  int64_t k = 1;
+  if (h > 0 && M > 0 && cm.alpha > 0 && cm.beta > 0) k = static_cast<int64_t>(std::floor(std::sqrt(h * M / (cm.alpha * cm.beta)) + 0.5));
+  const int64_t groups = std::max<int64_t>(1, count * esize(dt) / 16);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({k, 256, groups})));
+}
 
 PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double* predicted_s, std::string* why) {
   std::vector<Algo> cand;
@@ -626,16 +766,25 @@ PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double
       cand = link ? std::vector<Algo>{Algo::Pairwise, Algo::Bruck}
                   : std::vector<Algo>{Algo::Fused, Algo::Pairwise, Algo::Bruck};
       break;
+    case Coll::Gather:
+    case Coll::Reduce:
+      cand = link ? std::vector<Algo>{Algo::Binomial} : std::vector<Algo>{Algo::Fused, Algo::Binomial};
+      break;
+  }
+  if (a.coll == Coll::Broadcast) {
+    cand.push_back(Algo::PipeChain);
+    cand.push_back(Algo::PipeTree);
   }
   const int64_t es = esize(a.dt);
-  const double M = (a.coll == Coll::AllReduce || a.coll == Coll::Broadcast) ? double(a.count * es)
-                                                                             : double(a.count * es * a.nranks);
+  const bool per_rank = a.coll == Coll::AllReduce || a.coll == Coll::Broadcast || a.coll == Coll::Reduce;
+  const double M = per_rank ? double(a.count * es) : double(a.count * es * a.nranks);
   bool found = false;
   double best = 0;
   PlanStatus last = PlanStatus::Unsupported;
   for (Algo al : cand) {
     PlanArgs pa = a;
     pa.algo = al;
+    pa.nchunks = (al == Algo::PipeChain || al == Algo::PipeTree) ? default_chunks(al, a.nranks, a.count, a.dt, cm) : 1;
     Plan p;
     std::string w;
     last = build_plan(pa, &p, &w);
@@ -644,7 +793,7 @@ PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double
       return last;
     }
     if (last != PlanStatus::Ok) continue;
-    const double t = link ? link_time(a.coll, al, a.nranks, M, cm.alpha, cm.beta)
+    const double t = link ? link_time(a.coll, al, a.nranks, M, cm.alpha, cm.beta, pa.nchunks)
                           : plan_launch_steps(p) * cm.alpha + double(plan_bytes(p)) / cm.beta;
     if (!found || t < best) {
       found = true;

@@ -17,8 +17,13 @@ enum class Buf : uint8_t { Send = 0, Recv = 1, Scratch = 2 };
 enum class DT : uint8_t { F32 = 0, BF16 = 1, I32 = 2 };
 enum class Mode : uint8_t { Copy = 0, F32 = 1, I32 = 2, BF16 = 3 };
 
-enum class Coll : int { AllReduce = 0, ReduceScatter = 1, AllGather = 2, Broadcast = 3, Scatter = 4, AllToAll = 5 };
-enum class Algo : int { Fused = 0, Ring = 1, RHD = 2, DBT = 3, Binomial = 4, ScatterAllGather = 5, Pairwise = 6, Bruck = 7 };
+enum class Coll : int {
+  AllReduce = 0, ReduceScatter = 1, AllGather = 2, Broadcast = 3, Scatter = 4, AllToAll = 5, Gather = 6, Reduce = 7
+};
+enum class Algo : int {
+  Fused = 0, Ring = 1, RHD = 2, DBT = 3, Binomial = 4, ScatterAllGather = 5, Pairwise = 6, Bruck = 7,
+  PipeChain = 9, PipeTree = 10
+};
 
 inline int esize(DT t) { return t == DT::BF16 ? 2 : 4; }
 
@@ -56,6 +61,7 @@ struct PlanArgs {
   DT dt;
   int root = 0;
   bool inplace = false;
+  int nchunks = 1;  // pipelined Broadcasts: chunks of the message (>= 1)
 };
 
 enum class PlanStatus { Ok, Invalid, Unsupported };
@@ -75,6 +81,12 @@ struct CostModel {
   double alpha = 0;  // seconds per step
   double beta = 0;   // bytes per second
 };
+
+// Chunks of a pipelined Broadcast when the caller does not choose: the
+// optimum of the page's pipelined formula, k* = sqrt(h M / (alpha beta)) with
+// h = N-2 (chain) or ceil(log2 N)-1 (tree), rounded, within [1, 256] and at
+// most one chunk per 16 bytes.
+int default_chunks(Algo a, int nranks, int64_t count, DT dt, const CostModel& cm);
 
 // Picks the cheapest algorithm for a.coll under the model (a.algo is ignored).
 PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double* predicted_s, std::string* why);

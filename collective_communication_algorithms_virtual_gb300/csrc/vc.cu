@@ -668,11 +668,13 @@ vc_status_t launch_step(DeviceState* st, const Step& s, const Bases& b, cudaStre
 // argument checks shared by the entry points
 // ---------------------------------------------------------------------------
 const char* coll_name(Coll c) {
-  static const char* n[] = {"allreduce", "reduce_scatter", "allgather", "broadcast", "scatter", "alltoall"};
+  static const char* n[] = {"allreduce", "reduce_scatter", "allgather", "broadcast", "scatter", "alltoall",
+                            "gather", "reduce"};
   return n[static_cast<int>(c)];
 }
 const char* algo_name(Algo a) {
-  static const char* n[] = {"fused", "ring", "rhd", "dbt", "binomial", "scatter_allgather", "pairwise", "bruck"};
+  static const char* n[] = {"fused", "ring", "rhd", "dbt", "binomial", "scatter_allgather", "pairwise", "bruck",
+                            "auto", "pipe_chain", "pipe_tree"};
   return n[static_cast<int>(a)];
 }
 
@@ -687,6 +689,8 @@ struct Call {
   const void* const* send = nullptr;  // per-rank inputs (AllReduce, ReduceScatter, AllGather, AllToAll)
   const void* send_root = nullptr;    // Broadcast, Scatter
   void* const* recv = nullptr;
+  void* recv_root = nullptr;          // Gather, Reduce
+  int nchunks = 0;                    // pipelined Broadcast (0: from the cost model)
   cudaStream_t stream = nullptr;
 };
 
@@ -730,7 +734,7 @@ vc_status_t to_algo(vc_algo_t a, Algo* out, bool* is_auto = nullptr) {
     *out = Algo::Fused;
     return VC_SUCCESS;
   }
-  if (v < 0 || v > 7) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
+  if (v < 0 || v > 10 || v == VC_ALGO_AUTO) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
   if (is_auto) *is_auto = false;
   *out = static_cast<Algo>(v);
   return VC_SUCCESS;
@@ -748,10 +752,12 @@ vc_status_t resolve_auto(PlanArgs* pa) {
 vc_status_t run(const Call& c) {
   const int N = c.nranks;
   if (N < 1 || N > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
-  if (!c.recv) return fail(VC_ERR_INVALID_ARG, "null recv array");
-  const bool rooted = c.coll == Coll::Broadcast || c.coll == Coll::Scatter;
+  const bool root_send = c.coll == Coll::Broadcast || c.coll == Coll::Scatter;  // one input: the root's
+  const bool root_recv = c.coll == Coll::Gather || c.coll == Coll::Reduce;      // one output: the root's
+  const bool rooted = root_send || root_recv;
+  if (!root_recv && !c.recv) return fail(VC_ERR_INVALID_ARG, "null recv array");
   if (rooted && (c.root < 0 || c.root >= N)) return fail(VC_ERR_INVALID_ARG, "root outside [0, nranks)");
-  if (!rooted && !c.send) return fail(VC_ERR_INVALID_ARG, "null send array");
+  if (!root_send && !c.send) return fail(VC_ERR_INVALID_ARG, "null send array");
   if (c.count < 0) return fail(VC_ERR_INVALID_ARG, "count too large");
   // algorithm / rank-count support is decided before looking at sizes
   PlanArgs pa{c.coll, c.algo, N, c.count, c.dt, c.root, false};
@@ -759,6 +765,9 @@ vc_status_t run(const Call& c) {
     const vc_status_t rs = resolve_auto(&pa);
     if (rs != VC_SUCCESS) return rs;
   }
+  pa.nchunks = 1;
+  if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
+    pa.nchunks = c.nchunks > 0 ? c.nchunks : default_chunks(pa.algo, N, c.count, c.dt, current_cost());
   {
     Plan probe;
     std::string why;
@@ -773,13 +782,13 @@ vc_status_t run(const Call& c) {
   const int64_t es = esize(c.dt);
   int64_t send_elems = c.count, recv_elems = c.count;
   if (c.coll == Coll::ReduceScatter || c.coll == Coll::Scatter) send_elems = c.count * N;
-  if (c.coll == Coll::AllGather) recv_elems = c.count * N;
+  if (c.coll == Coll::AllGather || c.coll == Coll::Gather) recv_elems = c.count * N;
   if (c.coll == Coll::AllToAll) send_elems = recv_elems = c.count * N;
   if (c.count > (INT64_MAX / 8) / N) return fail(VC_ERR_INVALID_ARG, "count too large");
   const int64_t sbytes = send_elems * es, rbytes = recv_elems * es;
 
   std::vector<const void*> sends;
-  if (rooted) {
+  if (root_send) {
     if (!c.send_root) return fail(VC_ERR_INVALID_ARG, "null root send buffer");
     sends.assign(N, nullptr);
     sends[c.root] = c.send_root;
@@ -789,18 +798,28 @@ vc_status_t run(const Call& c) {
       sends.push_back(c.send[r]);
     }
   }
-  for (int r = 0; r < N; ++r)
-    if (!c.recv[r]) return fail(VC_ERR_INVALID_ARG, "null recv buffer");
+  std::vector<void*> recvs(N, nullptr);
+  if (root_recv) {
+    if (!c.recv_root) return fail(VC_ERR_INVALID_ARG, "null root recv buffer");
+    recvs[c.root] = c.recv_root;
+  } else {
+    for (int r = 0; r < N; ++r) {
+      if (!c.recv[r]) return fail(VC_ERR_INVALID_ARG, "null recv buffer");
+      recvs[r] = c.recv[r];
+    }
+  }
 
   // outputs must not overlap each other or any input, except in place
   bool inplace = false;
   for (int i = 0; i < N; ++i) {
+    if (!recvs[i]) continue;
     for (int j = i + 1; j < N; ++j)
-      if (overlap(c.recv[i], rbytes, c.recv[j], rbytes)) return fail(VC_ERR_INVALID_ARG, "receive buffers overlap");
+      if (recvs[j] && overlap(recvs[i], rbytes, recvs[j], rbytes)) return fail(VC_ERR_INVALID_ARG, "receive buffers overlap");
     for (int q = 0; q < N; ++q) {
-      if (!sends[q] || !overlap(c.recv[i], rbytes, sends[q], sbytes)) continue;
-      const bool same = sends[q] == c.recv[i] && q == i && sbytes == rbytes;
-      const bool allowed = same && (c.coll == Coll::AllReduce || (c.coll == Coll::Broadcast && i == c.root));
+      if (!sends[q] || !overlap(recvs[i], rbytes, sends[q], sbytes)) continue;
+      const bool same = sends[q] == recvs[i] && q == i && sbytes == rbytes;
+      const bool allowed = same && (c.coll == Coll::AllReduce ||
+                                    ((c.coll == Coll::Broadcast || c.coll == Coll::Reduce) && i == c.root));
       if (!allowed) return fail(VC_ERR_INVALID_ARG, "a receive buffer overlaps a send buffer");
       inplace = true;
     }
@@ -829,7 +848,7 @@ vc_status_t run(const Call& c) {
     }
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
   }
-  const Bases b{sends.data(), c.recv, scratch};
+  const Bases b{sends.data(), recvs.data(), scratch};
   int launches = 0;
   TraceCtx tc;
   tc.coll = static_cast<int>(c.coll);
@@ -979,6 +998,64 @@ VC_EXPORT vc_status_t vc_alltoall(const void* const* send, void* const* recv, in
   });
 }
 
+VC_EXPORT vc_status_t vc_broadcast_pipelined(const void* send_root, void* const* recv, int nranks, size_t count,
+                                             vc_dtype_t dtype, int root, vc_algo_t algo, int nchunks,
+                                             vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::Broadcast;
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    if (nchunks < 0 || nchunks > 1024) return fail(VC_ERR_INVALID_ARG, "nchunks must be in [0, 1024]");
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(count);
+    c.root = root;
+    c.send_root = send_root;
+    c.recv = recv;
+    c.nchunks = nchunks;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_gather(const void* const* send, void* recv_root, int nranks, size_t sendcount,
+                                vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::Gather;
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(sendcount);
+    c.root = root;
+    c.send = send;
+    c.recv_root = recv_root;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
+VC_EXPORT vc_status_t vc_reduce(const void* const* send, void* recv_root, int nranks, size_t count,
+                                vc_dtype_t dtype, vc_op_t op, int root, vc_algo_t algo, vc_stream_t stream) {
+  return entry([&] {
+    Call c;
+    c.coll = Coll::Reduce;
+    vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
+    if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
+    if (rc != VC_SUCCESS) return rc;
+    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    c.nranks = nranks;
+    c.count = static_cast<int64_t>(count);
+    c.root = root;
+    c.send = send;
+    c.recv_root = recv_root;
+    c.stream = reinterpret_cast<cudaStream_t>(stream);
+    return run(c);
+  });
+}
+
 VC_EXPORT const char* vc_status_string(vc_status_t s) {
   switch (s) {
     case VC_SUCCESS: return "VC_SUCCESS";
@@ -1018,7 +1095,7 @@ VC_EXPORT vc_status_t vc_get_cost_model(vc_cost_policy_t* policy, double* alpha_
 VC_EXPORT vc_status_t vc_select_algo(vc_coll_t coll, int nranks, size_t count, vc_dtype_t dtype, int root,
                                      vc_algo_t* algo, double* predicted_s) {
   return entry([&]() -> vc_status_t {
-    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 5) return fail(VC_ERR_INVALID_ARG, "unknown collective");
+    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
     if (!algo) return fail(VC_ERR_INVALID_ARG, "null algo");
     PlanArgs pa;
     pa.coll = static_cast<Coll>(static_cast<int>(coll));
@@ -1044,17 +1121,19 @@ VC_EXPORT double vc_busbw_factor(vc_coll_t coll, int nranks) {
     case VC_COLL_REDUCE_SCATTER:
     case VC_COLL_ALLGATHER:
     case VC_COLL_ALLTOALL:
-    case VC_COLL_SCATTER: return (N - 1) / N;
-    case VC_COLL_BROADCAST: return 1.0;
+    case VC_COLL_SCATTER:
+    case VC_COLL_GATHER: return (N - 1) / N;
+    case VC_COLL_BROADCAST:
+    case VC_COLL_REDUCE: return 1.0;
   }
   return 0.0;
 }
 
 VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
-                                       vc_dtype_t dtype, int root, int inplace, vc_plan_entry_t* entries,
+                                       vc_dtype_t dtype, int root, int inplace, int nchunks, vc_plan_entry_t* entries,
                                        size_t capacity, size_t* n_entries, size_t* scratch_bytes, int* n_steps) {
   return entry([&]() -> vc_status_t {
-    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 5) return fail(VC_ERR_INVALID_ARG, "unknown collective");
+    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
     PlanArgs pa;
     pa.coll = static_cast<Coll>(static_cast<int>(coll));
     bool is_auto = false;
@@ -1069,6 +1148,8 @@ VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nrank
       rc = resolve_auto(&pa);
       if (rc != VC_SUCCESS) return rc;
     }
+    if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
+      pa.nchunks = nchunks > 0 ? nchunks : default_chunks(pa.algo, nranks, pa.count, pa.dt, current_cost());
     Plan plan;
     std::string why;
     const PlanStatus ps = build_plan(pa, &plan, &why);

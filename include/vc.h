@@ -80,7 +80,9 @@ typedef enum {
   VC_ALGO_SCATTER_ALLGATHER = 5, /* Broadcast                                          */
   VC_ALGO_PAIRWISE = 6,          /* AllToAll                                           */
   VC_ALGO_BRUCK = 7,             /* AllToAll                                           */
-  VC_ALGO_AUTO = 8               /* any collective: cheapest under the cost model      */
+  VC_ALGO_AUTO = 8,              /* any collective: cheapest under the cost model      */
+  VC_ALGO_PIPE_CHAIN = 9,        /* Broadcast, message cut into chunks along a chain   */
+  VC_ALGO_PIPE_TREE = 10         /* Broadcast, chunks down the binomial tree           */
 } vc_algo_t;
 
 typedef enum {
@@ -89,7 +91,9 @@ typedef enum {
   VC_COLL_ALLGATHER = 2,
   VC_COLL_BROADCAST = 3,
   VC_COLL_SCATTER = 4,
-  VC_COLL_ALLTOALL = 5
+  VC_COLL_ALLTOALL = 5,
+  VC_COLL_GATHER = 6,
+  VC_COLL_REDUCE = 7
 } vc_coll_t;
 
 /*
@@ -193,6 +197,45 @@ vc_status_t vc_get_cost_model(vc_cost_policy_t* policy, double* alpha_s, double*
 vc_status_t vc_select_algo(vc_coll_t coll, int nranks, size_t count, vc_dtype_t dtype, int root,
                            vc_algo_t* algo, double* predicted_s);
 
+/*
+ * Broadcast with the message cut into `nchunks` chunks that travel one
+ * behind another (Broadcast/Scatter page, sections "分块链式流水线", eq.
+ * pipe-chain-bcast: N+k-2 steps, and "分块二叉树流水线", eq. pipe-tree-bcast:
+ * ceil(log2 N)+k-1 steps).  Chunk j follows the chain (PIPE_CHAIN) or the
+ * binomial tree (PIPE_TREE) delayed by j steps.  nchunks = 0 takes the
+ * optimum of the page's formula under the current cost model,
+ * k* = sqrt(h M / (alpha beta)) with h = N-2 (chain) or ceil(log2 N)-1
+ * (tree), within [1, 256] and at most one chunk per 16 bytes; otherwise
+ * nchunks must be in [1, 1024].  vc_broadcast with a PIPE algorithm uses
+ * nchunks = 0.  Other algorithms ignore nchunks.  Buffers as vc_broadcast.
+ */
+vc_status_t vc_broadcast_pipelined(const void* send_root, void* const* recv, int nranks, size_t count,
+                                   vc_dtype_t dtype, int root, vc_algo_t algo, int nchunks,
+                                   vc_stream_t stream);
+
+/*
+ * Gather: recv_root[q*sendcount + j] = send[q][j] -- Scatter's dual
+ * (Broadcast/Scatter page, section "对偶性：Scatter 与 Gather", eq.
+ * onetoall-gather-scatter-duality: its data flow reversed, same cost).
+ *   send[q]: sendcount elements; recv_root (a single device pointer, the
+ *   root's buffer): nranks*sendcount elements.  No in-place.
+ *   algo: FUSED or BINOMIAL (distances 1, 2, 4, ...: each subtree hands
+ *   everything it holds to its parent).
+ */
+vc_status_t vc_gather(const void* const* send, void* recv_root, int nranks, size_t sendcount,
+                      vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream);
+
+/*
+ * Reduce: recv_root[i] = sum over q of send[q][i] (latency-formula page,
+ * section "Broadcast / Reduce 怎么用 Tree 算法", eq. model-algo-reduce-tree).
+ *   send[q], recv_root: `count` elements.  recv_root == send[root] is allowed.
+ *   algo: FUSED (rank-order sum) or BINOMIAL (the binomial Broadcast run
+ *   backwards with adds: distances 1, 2, 4, ...; the sum is the balanced
+ *   tree over adjacent ranks counted from the root).
+ */
+vc_status_t vc_reduce(const void* const* send, void* recv_root, int nranks, size_t count, vc_dtype_t dtype,
+                      vc_op_t op, int root, vc_algo_t algo, vc_stream_t stream);
+
 /* Name of a status code (static string). */
 const char* vc_status_string(vc_status_t status);
 
@@ -201,8 +244,9 @@ const char* vc_last_error(void);
 
 /*
  * busbw = algbw * factor: AllReduce 2(N-1)/N; AllGather, ReduceScatter,
- * AllToAll (N-1)/N; Broadcast 1 (latency-formula page, table
- * tbl-model-algo-busbw-coef).  Scatter is not in that table and gets (N-1)/N.
+ * AllToAll (N-1)/N; Broadcast, Reduce 1 (latency-formula page, table
+ * tbl-model-algo-busbw-coef).  Scatter and Gather are not in that table and
+ * get (N-1)/N.
  * Returns 0 for an unknown collective or nranks < 1.
  */
 double vc_busbw_factor(vc_coll_t coll, int nranks);
@@ -210,7 +254,8 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
 /*
  * Schedule introspection (host only; no CUDA call, usable without a GPU).
  *
- * Builds the step plan a call with these arguments would execute and writes
+ * Builds the step plan a call with these arguments would execute (nchunks:
+ * as vc_broadcast_pipelined; ignored by other algorithms) and writes
  * one entry per operand of every operation.  An operation reads its sources
  * in the listed order (`pos`), adds them left to right (reduction steps) or
  * copies its single source (copy steps), and writes the result to each of its
@@ -240,7 +285,7 @@ typedef struct {
 } vc_plan_entry_t;
 
 vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
-                             vc_dtype_t dtype, int root, int inplace, vc_plan_entry_t* entries,
+                             vc_dtype_t dtype, int root, int inplace, int nchunks, vc_plan_entry_t* entries,
                              size_t capacity, size_t* n_entries, size_t* scratch_bytes,
                              int* n_steps);
 

@@ -751,3 +751,170 @@ def _alltoall_bruck(inputs, dtype, B):
         blocks = [W[j][(j - i) % N] for i in range(N)]
         out.append(np.concatenate(blocks))
     return Result(out, log, bm.total)
+
+
+# --------------------------------------------------------------------------
+# Pipelined Broadcasts, Gather, Tree Reduce
+# --------------------------------------------------------------------------
+
+ALGOS_EXTRA = {
+    "broadcast": ("pipe_chain", "pipe_tree"),
+    "gather": ("fused", "binomial"),
+    "reduce": ("fused", "binomial"),
+}
+
+
+def broadcast_pipelined(root_input, N: int, root: int, algo: str, dtype: str, k: int,
+                        inplace: bool = False) -> Result:
+    """Chunked (pipelined) Broadcasts of the [Bcast/Scatter page]: the message
+    is cut into k chunks (``oracle.partition``) and chunk j runs the
+    unpipelined schedule delayed by j steps.
+
+    * pipe_chain (section "分块链式流水线", eq. pipe-chain-bcast): relative
+      rank v forwards chunk j to v + 1 at step v + j; N + k - 2 steps.
+    * pipe_tree (section "分块二叉树流水线", eq. pipe-tree-bcast): chunk j
+      takes binomial step s at step j + s; ceil(log2 N) + k - 1 steps.
+
+    That each chunk follows the unpipelined route shifted by its index is the
+    reading taken; the pages give only the step counts and chunk sizes."""
+    _check_same([root_input], dtype)
+    assert 0 <= root < N and k >= 1
+    count = len(root_input)
+    e = ESIZE[dtype]
+    bm = _Bytes(dtype)
+    log = TransferLog()
+    have = {r: {} for r in range(N)}
+    have[root] = {j: root_input[slice(*chunk_range(j, count, k, e))].copy() for j in range(k)}
+    if not inplace:
+        bm.rw(count, bm.e_in, bm.e_out)
+    if algo == "pipe_chain":
+        nsteps = N + k - 2 if N > 1 else 0
+        route = [[(v, v + 1) for v in range(N - 1)]]  # one hop per step
+        hops = lambda t, j: [route[0][t - j]] if 0 <= t - j < N - 1 else []
+    elif algo == "pipe_tree":
+        rounds = binomial_rounds(N)
+        nsteps = len(rounds) + k - 1 if N > 1 else 0
+
+        def hops(t, j):
+            s = t - j
+            if not 0 <= s < len(rounds):
+                return []
+            d = rounds[s]
+            return [(v, v + d) for v in range(0, N, 2 * d) if v + d < N]
+    else:
+        raise Unsupported(f"broadcast/{algo}")
+    for t in range(nsteps):
+        msgs = []
+        for j in range(k):
+            lo, hi = chunk_range(j, count, k, e)
+            for v, w in hops(t, j):
+                src, dst = (v + root) % N, (w + root) % N
+
+                def deliver(p, dst=dst, j=j):
+                    have[dst][j] = p
+                msgs.append(_Msg(src=src, dst=dst, n=hi - lo, reduce=False, esize=bm.e_in,
+                                 payload=have[src][j].copy(), deliver=deliver, phase=algo,
+                                 src_off=lo, dst_off=lo, chunks=(j,)))
+                bm.rw(hi - lo, bm.e_out, bm.e_out)
+        _run_step(log, t, msgs)
+    outs = []
+    for r in range(N):
+        outs.append(np.concatenate([have[r][j] for j in range(k)]) if k else np.array(root_input[:0]))
+    return Result(outs, log, bm.total)
+
+
+def gather(inputs, root: int, algo: str, dtype: str) -> Result:
+    """The dual of Scatter: the root ends with [A_0, ..., A_{N-1}], A_i being
+    rank i's input ([Bcast/Scatter page] section "对偶性：Scatter 与 Gather",
+    eq. onetoall-gather-scatter-duality: reverse the Scatter's data flow).
+
+    binomial: distances 1, 2, 4, ...; at distance d relative rank v with
+    v mod 2d == d hands everything it holds -- the chunks of relative ranks
+    [v, min(v+d, N)) -- to v - d."""
+    N, rc = _check_same(inputs, dtype)
+    assert 0 <= root < N
+    bm = _Bytes(dtype)
+    log = TransferLog()
+    if algo == "fused":
+        out = np.concatenate([np.array(x, copy=True) for x in inputs]) if N else None
+        for r in range(N):
+            if r != root:
+                log.add(step=0, phase="fused", src=r, dst=root, n=rc, reduce=False, esize=bm.e_in,
+                        src_off=0, dst_off=r * rc, chunks=(r,))
+        bm.rw(rc * N, bm.e_in, bm.e_out)
+        return Result([out], log, bm.total)
+    if algo != "binomial":
+        raise Unsupported(f"gather/{algo}")
+    holdings = {r: {r: np.array(inputs[r], copy=True)} for r in range(N)}
+    bm.rw(rc, bm.e_in, bm.e_out)  # the root's own block
+    L = _ceil_log2(N)
+    for s in range(L):
+        d = 1 << s
+        msgs = []
+        for u in range(0, N, 2 * d):
+            v = u + d
+            if v >= N:
+                continue
+            src, dst = (v + root) % N, (u + root) % N
+            chunks = tuple((q + root) % N for q in range(v, min(v + d, N)))
+            payload = {c: holdings[src][c].copy() for c in chunks}
+
+            def deliver(p, dst=dst):
+                holdings[dst].update(p)
+            msgs.append(_Msg(src=src, dst=dst, n=rc * len(chunks), reduce=False, esize=bm.e_in,
+                             payload=payload, deliver=deliver, phase="gather", chunks=chunks))
+            bm.rw(rc * len(chunks), bm.e_in, bm.e_out)
+        _run_step(log, s, msgs)
+    out = np.concatenate([holdings[root][c] for c in range(N)])
+    return Result([out], log, bm.total)
+
+
+def reduce(inputs, root: int, algo: str, dtype: str, inplace: bool = False) -> Result:
+    """Reduce to one root: out_root = elementwise sum of every rank's input
+    ([Latency-formula page] section "Broadcast / Reduce 怎么用 Tree 算法", eq.
+    model-algo-reduce-tree: the Tree Broadcast run backwards, same cost).
+
+    binomial: distances 1, 2, 4, ...; at distance d relative rank u with
+    u mod 2d == 0 adds the partial sum of u + d to its own.  The association
+    is the balanced tree over adjacent relative ranks, ((x0+x1)+(x2+x3)) + ...
+    fused: rank order ((x_0 + x_1) + x_2) + ..., as the fused AllReduce."""
+    N, count = _check_same(inputs, dtype)
+    assert 0 <= root < N
+    bm = _Bytes(dtype)
+    log = TransferLog()
+    if algo not in ALGOS_EXTRA["reduce"]:
+        raise Unsupported(f"reduce/{algo}")
+    if N == 1:  # one rank: the result is its input (copied unless in place)
+        if not inplace:
+            bm.rw(count, bm.e_in, bm.e_out)
+        return Result([np.array(inputs[0], copy=True)], log, bm.total)
+    if algo == "fused":
+        acc = widen(inputs[0], dtype)
+        for q in range(1, N):
+            acc = add(acc, widen(inputs[q], dtype))
+        for q in range(N):
+            if q != root:
+                log.add(step=0, phase="fused", src=q, dst=root, n=count, reduce=True, esize=bm.e_in,
+                        src_off=0, dst_off=0)
+        bm.rw(count, *([bm.e_in] * N), bm.e_out)
+        return Result([narrow(acc, dtype)], log, bm.total)
+    acc = [widen(x, dtype) for x in inputs]
+    partial = [False] * N  # relative rank holds a partial sum (not its raw input)
+    L = _ceil_log2(N)
+    for s in range(L):
+        d = 1 << s
+        msgs = []
+        for u in range(0, N, 2 * d):
+            v = u + d
+            if v >= N:
+                continue
+            src, dst = (v + root) % N, (u + root) % N
+            wire = bm.e_acc if partial[v] else bm.e_in
+            msgs.append(_Msg(src=src, dst=dst, n=count, reduce=True, esize=wire,
+                             payload=acc[src].copy(), deliver=_reduce_into(acc[dst], 0, count),
+                             phase="reduce", src_off=0, dst_off=0))
+            last = u == 0 and s == L - 1
+            bm.rw(count, bm.e_acc if partial[u] else bm.e_in, wire, bm.e_out if last else bm.e_acc)
+            partial[u] = True
+        _run_step(log, s, msgs)
+    return Result([narrow(acc[root], dtype)], log, bm.total)

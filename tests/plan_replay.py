@@ -22,8 +22,8 @@ ESZ = {0: 4, 1: 2, 2: 4}
 DT = {"f32": 0, "bf16": 1, "i32": 2}
 
 
-def get_plan(coll, algo, N, count, dtype, root=0, inplace=False):
-    entries, scratch, nsteps = vc_plan_describe(coll, algo, N, count, dtype, root, inplace)
+def get_plan(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0):
+    entries, scratch, nsteps = vc_plan_describe(coll, algo, N, count, dtype, root, inplace, nchunks)
     steps = [dict() for _ in range(nsteps)]
     for e in entries:
         op = steps[e.step].setdefault(e.op, {"reduce": bool(e.reduce), "n": e.n, "nb": e.nb,
