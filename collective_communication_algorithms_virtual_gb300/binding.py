@@ -15,10 +15,10 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libvcoll.so")
 
 VC_SUCCESS, VC_ERR_INVALID_ARG, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_NOMEM, VC_ERR_TIMEOUT = range(6)
-DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
+DTYPES = {"f32": 0, "bf16": 1, "i32": 2, "f16": 3}
 OPS = {"sum": 0, "max": 1, "min": 2}
 ALGOS = {"fused": 0, "ring": 1, "rhd": 2, "dbt": 3, "binomial": 4, "scatter_allgather": 5,
-         "pairwise": 6, "bruck": 7, "auto": 8, "pipe_chain": 9, "pipe_tree": 10}
+         "pairwise": 6, "bruck": 7, "auto": 8, "pipe_chain": 9, "pipe_tree": 10, "mesh": 11}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 COST_POLICIES = {"hbm": 0, "link": 1}
 COLLS = {"allreduce": 0, "reduce_scatter": 1, "allgather": 2, "broadcast": 3, "scatter": 4,
@@ -37,11 +37,14 @@ class TraceRecord(ctypes.Structure):
                 ("ms", ctypes.c_float)]
 
 
-KERNEL_NAMES = {0: "copy", 1: "sum_f32", 2: "sum_i32", 3: "sum_bf16", 4: "sum_bf16_pure"}
+KERNEL_MODES = {0: "copy", 1: "f32", 2: "i32", 3: "bf16", 4: "bf16_pure", 5: "f16", 6: "f16_pure"}
+KERNEL_OPS = {0: "sum", 1: "max", 2: "min"}
 
 
 def kernel_name(code: int) -> str:
-    return KERNEL_NAMES[code & 7] + ("_large" if code & 8 else "")
+    mode = KERNEL_MODES[code & 7]
+    name = mode if mode == "copy" else f"{KERNEL_OPS[(code >> 3) & 3]}_{mode}"
+    return name + ("_large" if code & 32 else "")
 
 
 class PlanEntry(ctypes.Structure):
@@ -83,7 +86,7 @@ def lib() -> ctypes.CDLL:
         L.vc_last_error.restype = ctypes.c_char_p
         L.vc_busbw_factor.argtypes = [I, I]
         L.vc_busbw_factor.restype = ctypes.c_double
-        L.vc_plan_describe.argtypes = [I, I, I, Z, I, I, I, I, ctypes.POINTER(PlanEntry), Z,
+        L.vc_plan_describe.argtypes = [I, I, I, Z, I, I, I, I, I, ctypes.POINTER(PlanEntry), Z,
                                        ctypes.POINTER(Z), ctypes.POINTER(Z), ctypes.POINTER(I)]
         L.vc_plan_describe.restype = I
         L.vc_trace_enable.argtypes = [I]
@@ -119,7 +122,7 @@ def _ptr_array(ptrs: Sequence[int]):
 def _dtype_code(t) -> int:
     import torch
 
-    m = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
+    m = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2, torch.float16: 3}
     if t.dtype not in m:
         raise VCError(VC_ERR_INVALID_ARG, f"unsupported dtype {t.dtype}")
     return m[t.dtype]
@@ -269,14 +272,14 @@ def vc_trace_read(capacity: int = 1 << 20) -> list:
 
 
 def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,
-                     nchunks: int = 0):
+                     nchunks: int = 0, op="sum"):
     """The step plan the library would run, as (entries, scratch_bytes, n_steps);
     host only, needs no GPU."""
     L = lib()
     need, scratch = ctypes.c_size_t(0), ctypes.c_size_t(0)
     steps = ctypes.c_int(0)
     args = (_code(COLLS, coll), _code(ALGOS, algo), int(nranks), int(count), _code(DTYPES, dtype),
-            int(root), int(bool(inplace)), int(nchunks))
+            _code(OPS, op), int(root), int(bool(inplace)), int(nchunks))
     check(L.vc_plan_describe(*args, None, 0, ctypes.byref(need), ctypes.byref(scratch), ctypes.byref(steps)))
     buf = (PlanEntry * max(1, need.value))()
     check(L.vc_plan_describe(*args, buf, need.value, ctypes.byref(need), ctypes.byref(scratch),

@@ -100,14 +100,22 @@ class Builder {
   }
 
   Mode reduce_mode() const {
-    return a_.dt == DT::F32 ? Mode::F32 : a_.dt == DT::I32 ? Mode::I32 : Mode::BF16;
+    switch (a_.dt) {
+      case DT::F32: return Mode::F32;
+      case DT::I32: return Mode::I32;
+      case DT::BF16: return Mode::BF16;
+      default: return Mode::F16;
+    }
   }
-  // Partial sums are stored as fp32 when the data is bf16, else in the data type.
-  DT acc_dt() const { return a_.dt == DT::BF16 ? DT::F32 : a_.dt; }
-  bool bf16() const { return a_.dt == DT::BF16; }
+  // Partial results are stored as fp32 when the data is 16-bit, else in the data type.
+  DT acc_dt() const { return bf16() ? DT::F32 : a_.dt; }
+  // 16-bit floating point data (bf16 or fp16): partials go to fp32 scratch.
+  bool bf16() const { return a_.dt == DT::BF16 || a_.dt == DT::F16; }
 
   size_t new_step(Mode m) {
-    plan_.steps.push_back(Step{m, {}});
+    Step st{m, {}};
+    if (m != Mode::Copy) st.red = a_.op;
+    plan_.steps.push_back(std::move(st));
     return plan_.steps.size() - 1;
   }
   void add(size_t st, std::vector<Operand> src, std::vector<Operand> dst, int64_t n) {
@@ -132,8 +140,31 @@ class Builder {
       case Algo::Ring: allreduce_ring(); break;
       case Algo::RHD: allreduce_rhd(); break;
       case Algo::DBT: allreduce_dbt(); break;
+      case Algo::Mesh: allreduce_mesh(); break;
       default: break;
     }
+  }
+
+  // Mesh AllReduce (hccl article, section "Mesh算法：全连接广播"), step for
+  // step from its code: the root folds every other rank's buffer into its own
+  // in rank order, one rank per step, then sends the result to every other
+  // rank in rank order, one per step.  The article's call takes a root; an
+  // AllReduce here has none and rank 0 is the root.  The root's running
+  // result lives in its receive buffer (fp32 scratch for 16-bit data).
+  void allreduce_mesh() {
+    const int root = 0;
+    const int64_t count = a_.count;
+    const int64_t part = bf16() ? alloc(count * 4) : -1;
+    auto acc = [&]() { return part >= 0 ? Sc(root, part, DT::F32) : R(root, 0); };
+    int t = 0;
+    for (int i = 0; i < N_; ++i) {
+      if (i == root) continue;
+      const bool last = t == N_ - 2;
+      add(new_step(reduce_mode()), {t == 0 ? S(root, 0) : acc(), S(i, 0)}, {last ? R(root, 0) : acc()}, count);
+      ++t;
+    }
+    for (int i = 0; i < N_; ++i)
+      if (i != root) copy(new_step(Mode::Copy), R(root, 0), R(i, 0), count);
   }
 
   // One pass: every output element is ((x0 + x1) + x2) + ... in rank order,
@@ -594,6 +625,41 @@ class Builder {
     }
   }
 
+  // Ring AllToAll (latency-formula page, eq. model-algo-a2a-ring), store and
+  // forward: in round k rank i receives from rank i-1 the blocks that left
+  // rank s = i-k k rounds ago and are addressed to ranks i, i+1, ..., s-1;
+  // it keeps the one for itself (block s of its output) and stages the rest,
+  // indexed by destination, in one of two forwarding buffers (round k writes
+  // buffer k%2 while rank i+1 reads rank i's buffer (k-1)%2).  Round 0 is the
+  // local block.
+  void alltoall_ring(int64_t B) {
+    const int64_t fbytes = int64_t(N_) * B * es_;
+    int64_t F[2] = {0, 0};
+    if (N_ > 2) {
+      F[0] = alloc(int64_t(N_) * fbytes);
+      F[1] = alloc(int64_t(N_) * fbytes);
+    }
+    auto fwd = [&](int which, int rank, int d) { return Sc(rank, F[which] + rank * fbytes + d * B * es_, a_.dt); };
+    {
+      const size_t st = new_step(Mode::Copy);
+      for (int i = 0; i < N_; ++i) copy(st, S(i, i * B), R(i, i * B), B);
+    }
+    for (int k = 1; k < N_; ++k) {
+      const size_t st = new_step(Mode::Copy);
+      for (int i = 0; i < N_; ++i) {
+        const int from = md(i - 1, N_), src = md(i - k, N_);
+        auto held = [&](int d) { return k == 1 ? S(from, int64_t(d) * B) : fwd((k - 1) & 1, from, d); };
+        copy(st, held(i), R(i, int64_t(src) * B), B);
+        std::vector<BlockCopy> rest;
+        for (int h = 1; h < N_ - k; ++h) {  // destinations i+1 .. s-1, in ring order
+          const int d = (i + h) % N_;
+          rest.push_back({held(d), fwd(k & 1, i, d)});
+        }
+        emit_runs(st, rest, B);
+      }
+    }
+  }
+
   void alltoall() {
     const int64_t B = a_.count;
     if (B == 0) return;
@@ -613,6 +679,10 @@ class Builder {
           copy(st, S(i, j * B), R(j, i * B), B);
         }
       }
+      return;
+    }
+    if (a_.algo == Algo::Ring) {
+      alltoall_ring(B);
       return;
     }
     // Bruck (Bruck et al. 1997, cited by the latency-formula page): position p
@@ -662,7 +732,8 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   bool ok = false;
   switch (a.coll) {
     case Coll::AllReduce:
-      ok = a.algo == Algo::Fused || a.algo == Algo::Ring || a.algo == Algo::RHD || a.algo == Algo::DBT;
+      ok = a.algo == Algo::Fused || a.algo == Algo::Ring || a.algo == Algo::RHD || a.algo == Algo::DBT ||
+           a.algo == Algo::Mesh;
       break;
     case Coll::ReduceScatter:
     case Coll::AllGather: ok = a.algo == Algo::Fused || a.algo == Algo::Ring; break;
@@ -670,7 +741,9 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
       ok = a.algo == Algo::Fused || a.algo == Algo::Binomial || a.algo == Algo::ScatterAllGather;
       break;
     case Coll::Scatter: ok = a.algo == Algo::Fused || a.algo == Algo::Binomial; break;
-    case Coll::AllToAll: ok = a.algo == Algo::Fused || a.algo == Algo::Pairwise || a.algo == Algo::Bruck; break;
+    case Coll::AllToAll:
+      ok = a.algo == Algo::Fused || a.algo == Algo::Pairwise || a.algo == Algo::Bruck || a.algo == Algo::Ring;
+      break;
     case Coll::Gather:
     case Coll::Reduce: ok = a.algo == Algo::Fused || a.algo == Algo::Binomial; break;
   }
@@ -727,6 +800,7 @@ double link_time(Coll c, Algo a, int N, double M, double al, double be, double k
     case Coll::Reduce: return lg * (al + M / be);
     case Coll::AllToAll:
       if (a == Algo::Pairwise) return (n - 1) * (al + M / (n * be));
+      if (a == Algo::Ring) return (n - 1) * al + (n - 1) / n * M / be;  // as printed (see the oracle)
       return cl * al + (n - 1) / n * M / be;  // Bruck
   }
   return 0;
@@ -749,7 +823,7 @@ PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double
   switch (a.coll) {
     case Coll::AllReduce:
       cand = link ? std::vector<Algo>{Algo::Ring, Algo::RHD, Algo::DBT}
-                  : std::vector<Algo>{Algo::Fused, Algo::Ring, Algo::RHD, Algo::DBT};
+                  : std::vector<Algo>{Algo::Fused, Algo::Ring, Algo::RHD, Algo::DBT, Algo::Mesh};
       break;
     case Coll::ReduceScatter:
     case Coll::AllGather:
@@ -763,8 +837,8 @@ PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double
       cand = link ? std::vector<Algo>{Algo::Binomial} : std::vector<Algo>{Algo::Fused, Algo::Binomial};
       break;
     case Coll::AllToAll:
-      cand = link ? std::vector<Algo>{Algo::Pairwise, Algo::Bruck}
-                  : std::vector<Algo>{Algo::Fused, Algo::Pairwise, Algo::Bruck};
+      cand = link ? std::vector<Algo>{Algo::Pairwise, Algo::Bruck, Algo::Ring}
+                  : std::vector<Algo>{Algo::Fused, Algo::Pairwise, Algo::Bruck, Algo::Ring};
       break;
     case Coll::Gather:
     case Coll::Reduce:

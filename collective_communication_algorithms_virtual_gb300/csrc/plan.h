@@ -14,18 +14,19 @@
 namespace vc {
 
 enum class Buf : uint8_t { Send = 0, Recv = 1, Scratch = 2 };
-enum class DT : uint8_t { F32 = 0, BF16 = 1, I32 = 2 };
-enum class Mode : uint8_t { Copy = 0, F32 = 1, I32 = 2, BF16 = 3 };
+enum class DT : uint8_t { F32 = 0, BF16 = 1, I32 = 2, F16 = 3 };
+enum class Mode : uint8_t { Copy = 0, F32 = 1, I32 = 2, BF16 = 3, F16 = 4 };
+enum class RedOp : uint8_t { Sum = 0, Max = 1, Min = 2 };
 
 enum class Coll : int {
   AllReduce = 0, ReduceScatter = 1, AllGather = 2, Broadcast = 3, Scatter = 4, AllToAll = 5, Gather = 6, Reduce = 7
 };
 enum class Algo : int {
   Fused = 0, Ring = 1, RHD = 2, DBT = 3, Binomial = 4, ScatterAllGather = 5, Pairwise = 6, Bruck = 7,
-  PipeChain = 9, PipeTree = 10
+  PipeChain = 9, PipeTree = 10, Mesh = 11
 };
 
-inline int esize(DT t) { return t == DT::BF16 ? 2 : 4; }
+inline int esize(DT t) { return (t == DT::BF16 || t == DT::F16) ? 2 : 4; }
 
 struct Operand {
   Buf buf;
@@ -46,6 +47,7 @@ struct Op {
 struct Step {
   Mode mode;
   std::vector<Op> ops;
+  RedOp red = RedOp::Sum;  // how a reduction step combines its sources
 };
 
 struct Plan {
@@ -62,6 +64,7 @@ struct PlanArgs {
   int root = 0;
   bool inplace = false;
   int nchunks = 1;  // pipelined Broadcasts: chunks of the message (>= 1)
+  RedOp op = RedOp::Sum;
 };
 
 enum class PlanStatus { Ok, Invalid, Unsupported };

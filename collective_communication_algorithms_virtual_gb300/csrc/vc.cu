@@ -14,6 +14,7 @@
 // no tensor cores.  Kernels never wait on each other or on flags: ordering
 // between steps is stream order.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -74,7 +75,14 @@ constexpr int kScalarPerThread = 4;  // elements per thread per tile (element pa
 constexpr int kTileGroups = kThreads * kUnroll;
 constexpr int kTileElems = kThreads * kScalarPerThread;
 
-enum : int { kCopy = 0, kF32 = 1, kI32 = 2, kBF16 = 3, kBF16P = 4 };
+// Kernel modes: copy; fp32 / int32 reductions; 16-bit float reductions whose
+// sources mix the data type with fp32 partial sums, or are all of the data
+// type ("P": pure), for bf16 and fp16.
+enum : int { kCopy = 0, kF32 = 1, kI32 = 2, kBF16 = 3, kBF16P = 4, kF16 = 5, kF16P = 6 };
+// Reduction ops.  max / min keep the first operand unless the second is
+// larger / smaller or the first is NaN (so NaN is passed over while a number
+// is present and of +0 / -0 the first seen is kept); int32 compares signed.
+enum : int { kSum = 0, kMax = 1, kMin = 2 };
 
 struct __align__(16) OpDesc {
   int64_t n;        // elements per run (copy: elements of esz bytes)
@@ -118,23 +126,61 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even, lo in the low half
-  return *reinterpret_cast<uint32_t*>(&h);
+template <int OP>
+__device__ __forceinline__ float cmb(float a, float b) {
+  if constexpr (OP == kSum) return __fadd_rn(a, b);
+  else if constexpr (OP == kMax) return (b > a || a != a) ? b : a;
+  else return (b < a || a != a) ? b : a;
 }
+template <int OP>
+__device__ __forceinline__ uint32_t cmbi(uint32_t a, uint32_t b) {
+  if constexpr (OP == kSum) return a + b;  // two's-complement wrap-around
+  else if constexpr (OP == kMax) return static_cast<int32_t>(b) > static_cast<int32_t>(a) ? b : a;
+  else return static_cast<int32_t>(b) < static_cast<int32_t>(a) ? b : a;
+}
+
+// 16-bit float formats: widening is exact; narrowing rounds to nearest even.
+template <bool F16>
+__device__ __forceinline__ float widen1(uint16_t h) {
+  if constexpr (F16) return __half2float(__ushort_as_half(h));
+  else return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+template <bool F16>
+__device__ __forceinline__ uint16_t narrow1(float x) {
+  if constexpr (F16) return __half_as_ushort(__float2half_rn(x));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <bool F16>
+__device__ __forceinline__ void widen2(uint32_t w, float* f) {
+  if constexpr (F16) {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    f[0] = v.x;
+    f[1] = v.y;
+  } else {
+    f[0] = __uint_as_float(w << 16);
+    f[1] = __uint_as_float(w & 0xffff0000u);
+  }
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {  // lo in the low half
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+template <bool F16>
 __device__ __forceinline__ void widen8(uint4 v, float* f) {
-  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  widen2<F16>(v.x, f);
+  widen2<F16>(v.y, f + 2);
+  widen2<F16>(v.z, f + 4);
+  widen2<F16>(v.w, f + 6);
 }
 
 // -- vector path -------------------------------------------------------------
-template <int MODE>
-__device__ __forceinline__ void tile_vec(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr);
-
-template <>
-__device__ __forceinline__ void tile_vec<kCopy>(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+__device__ __forceinline__ void tile_copy(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
   const int64_t g0 = tr * kTileGroups + threadIdx.x;
   const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
   uint4 v[kUnroll];
@@ -154,8 +200,8 @@ __device__ __forceinline__ void tile_vec<kCopy>(const OpDesc& o, const void* con
 }
 
 // fp32 and int32: 4 elements per 16-byte group.
-template <int MODE>
-__device__ __forceinline__ void tile_vec_4b(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+template <bool FLOAT, int OP>
+__device__ __forceinline__ void tile_4b(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
   const int64_t g0 = tr * kTileGroups + threadIdx.x;
   uint4 acc[kUnroll];
   {
@@ -173,13 +219,16 @@ __device__ __forceinline__ void tile_vec_4b(const OpDesc& o, const void* const* 
       const int64_t g = g0 + u * kThreads;
       if (g < o.groups) {
         const uint4 v = ld16(s + g * 16);
-        if (MODE == kF32) {
-          acc[u].x = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].x), __uint_as_float(v.x)));
-          acc[u].y = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].y), __uint_as_float(v.y)));
-          acc[u].z = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].z), __uint_as_float(v.z)));
-          acc[u].w = __float_as_uint(__fadd_rn(__uint_as_float(acc[u].w), __uint_as_float(v.w)));
+        if constexpr (FLOAT) {
+          acc[u].x = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].x), __uint_as_float(v.x)));
+          acc[u].y = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].y), __uint_as_float(v.y)));
+          acc[u].z = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].z), __uint_as_float(v.z)));
+          acc[u].w = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].w), __uint_as_float(v.w)));
         } else {
-          acc[u].x += v.x; acc[u].y += v.y; acc[u].z += v.z; acc[u].w += v.w;
+          acc[u].x = cmbi<OP>(acc[u].x, v.x);
+          acc[u].y = cmbi<OP>(acc[u].y, v.y);
+          acc[u].z = cmbi<OP>(acc[u].z, v.z);
+          acc[u].w = cmbi<OP>(acc[u].w, v.w);
         }
       }
     }
@@ -193,31 +242,21 @@ __device__ __forceinline__ void tile_vec_4b(const OpDesc& o, const void* const* 
     }
   }
 }
-template <>
-__device__ __forceinline__ void tile_vec<kF32>(const OpDesc& o, const void* const* p, int64_t r, int64_t t) {
-  tile_vec_4b<kF32>(o, p, r, t);
-}
-template <>
-__device__ __forceinline__ void tile_vec<kI32>(const OpDesc& o, const void* const* p, int64_t r, int64_t t) {
-  tile_vec_4b<kI32>(o, p, r, t);
-}
-
-// bf16 mode: 8 elements per group; a bf16 operand moves 16 bytes, an fp32 one 32.
-constexpr int kUnrollBF = 2;  // groups per thread per pass, mixed bf16 / fp32 sources
 
 // Adds one loaded group of 8 values to the accumulator (or starts it).
+template <int OP>
 __device__ __forceinline__ void accumulate8(float* acc, const float* f, bool first) {
   if (first) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = f[i];
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+    for (int i = 0; i < 8; ++i) acc[i] = cmb<OP>(acc[i], f[i]);
   }
 }
 
-template <int U>
-__device__ __forceinline__ void store_bf16_mode(const OpDesc& o, const void* const* ptr, int64_t run, int64_t g0,
+template <bool F16, int U>
+__device__ __forceinline__ void store_half_mode(const OpDesc& o, const void* const* ptr, int64_t run, int64_t g0,
                                                 float (&acc)[U][8]) {
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
@@ -232,17 +271,18 @@ __device__ __forceinline__ void store_bf16_mode(const OpDesc& o, const void* con
           st16(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
                                             __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
         } else {
-          st16(dp + g * 16, make_uint4(pack_bf16(acc[u][0], acc[u][1]), pack_bf16(acc[u][2], acc[u][3]),
-                                       pack_bf16(acc[u][4], acc[u][5]), pack_bf16(acc[u][6], acc[u][7])));
+          st16(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
+                                       pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
         }
       }
     }
   }
 }
 
-// Sources of either storage type (bf16 data, fp32 partial sums), one at a time.
-template <>
-__device__ __forceinline__ void tile_vec<kBF16>(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+// 16-bit data with fp32 partial sums among the sources, one source at a time.
+constexpr int kUnrollBF = 2;  // groups per thread per pass
+template <bool F16, int OP>
+__device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
   // A tile covers kTileGroups groups in kUnroll/kUnrollBF passes of kUnrollBF groups per thread.
 #pragma unroll 1
   for (int pass = 0; pass < kUnroll / kUnrollBF; ++pass) {
@@ -261,25 +301,26 @@ __device__ __forceinline__ void tile_vec<kBF16>(const OpDesc& o, const void* con
             f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
             f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
           } else {
-            widen8(ld16(s + g * 16), f);
+            widen8<F16>(ld16(s + g * 16), f);
           }
-          accumulate8(acc[u], f, k == 0);
+          accumulate8<OP>(acc[u], f, k == 0);
         }
       }
     }
-    store_bf16_mode<kUnrollBF>(o, ptr, run, g0, acc);
+    store_half_mode<F16, kUnrollBF>(o, ptr, run, g0, acc);
   }
 }
 
-// Every source stored as bf16 (fused AllReduce / ReduceScatter, first ring and
-// halving steps): kBatchBP sources' loads are in flight together before they
-// are added, still one after another in source order.  Measured on the fused
-// bf16 AllReduce at 8 x 128 MiB: 5811 -> 6516 GB/s; kept apart from the mixed
-// kernel because its extra registers lower that kernel's occupancy.
+// Every source stored in the 16-bit type (fused AllReduce / ReduceScatter,
+// first ring and halving steps): kBatchBP sources' loads are in flight
+// together before they are combined, still one after another in source
+// order.  Measured on the fused bf16 AllReduce at 8 x 128 MiB: 5811 -> 6516
+// GB/s; kept apart from the mixed kernel because its extra registers lower
+// that kernel's occupancy.
 constexpr int kUnrollBP = 4;
 constexpr int kBatchBP = 2;
-template <>
-__device__ __forceinline__ void tile_vec<kBF16P>(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+template <bool F16, int OP>
+__device__ __forceinline__ void tile_half_pure(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
 #pragma unroll 1
   for (int pass = 0; pass < kUnroll / kUnrollBP; ++pass) {
     const int64_t g0 = tr * kTileGroups + pass * kUnrollBP * kThreads + threadIdx.x;
@@ -305,21 +346,32 @@ __device__ __forceinline__ void tile_vec<kBF16P>(const OpDesc& o, const void* co
             const int64_t g = g0 + u * kThreads;
             if (g < o.groups) {
               float f[8];
-              widen8(raw[j][u], f);
-              accumulate8(acc[u], f, k + j == 0);
+              widen8<F16>(raw[j][u], f);
+              accumulate8<OP>(acc[u], f, k + j == 0);
             }
           }
         }
       }
     }
-    store_bf16_mode<kUnrollBP>(o, ptr, run, g0, acc);
+    store_half_mode<F16, kUnrollBP>(o, ptr, run, g0, acc);
   }
 }
 
+template <int MODE, int OP>
+__device__ __forceinline__ void tile_vec(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+  if constexpr (MODE == kCopy) tile_copy(o, ptr, run, tr);
+  else if constexpr (MODE == kF32) tile_4b<true, OP>(o, ptr, run, tr);
+  else if constexpr (MODE == kI32) tile_4b<false, OP>(o, ptr, run, tr);
+  else if constexpr (MODE == kBF16) tile_half_mixed<false, OP>(o, ptr, run, tr);
+  else if constexpr (MODE == kF16) tile_half_mixed<true, OP>(o, ptr, run, tr);
+  else if constexpr (MODE == kBF16P) tile_half_pure<false, OP>(o, ptr, run, tr);
+  else tile_half_pure<true, OP>(o, ptr, run, tr);
+}
+
 // -- element path (unaligned operands and the tails of vector runs) ---------
-template <int MODE>
+template <int MODE, int OP>
 __device__ __forceinline__ void elem(const OpDesc& o, const void* const* ptr, int64_t soff, int64_t doff, int64_t e) {
-  if (MODE == kCopy) {
+  if constexpr (MODE == kCopy) {
     const char* s = static_cast<const char*>(ptr[0]) + soff + e * o.esz;
     if (o.esz == 2) {
       const uint16_t v = *reinterpret_cast<const uint16_t*>(s);
@@ -330,44 +382,41 @@ __device__ __forceinline__ void elem(const OpDesc& o, const void* const* ptr, in
       for (int d = 0; d < o.nd; ++d)
         *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = v;
     }
-  } else if (MODE == kF32) {
+  } else if constexpr (MODE == kF32) {
     float acc = *reinterpret_cast<const float*>(static_cast<const char*>(ptr[0]) + soff + e * 4);
     for (int k = 1; k < o.ns; ++k)
-      acc = __fadd_rn(acc, *reinterpret_cast<const float*>(static_cast<const char*>(ptr[k]) + soff + e * 4));
+      acc = cmb<OP>(acc, *reinterpret_cast<const float*>(static_cast<const char*>(ptr[k]) + soff + e * 4));
     for (int d = 0; d < o.nd; ++d)
       *reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
-  } else if (MODE == kI32) {
+  } else if constexpr (MODE == kI32) {
     uint32_t acc = *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[0]) + soff + e * 4);
     for (int k = 1; k < o.ns; ++k)
-      acc += *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[k]) + soff + e * 4);
+      acc = cmbi<OP>(acc, *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[k]) + soff + e * 4));
     for (int d = 0; d < o.nd; ++d)
       *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
   } else {
+    constexpr bool F16 = MODE == kF16 || MODE == kF16P;
     float acc = 0.f;
     for (int k = 0; k < o.ns; ++k) {
       const char* s = static_cast<const char*>(ptr[k]) + soff;
       const float v = ((o.smask >> k) & 1) ? *reinterpret_cast<const float*>(s + e * 4)
-                                           : bf16lo(*reinterpret_cast<const uint16_t*>(s + e * 2));
-      acc = k == 0 ? v : __fadd_rn(acc, v);
+                                           : widen1<F16>(*reinterpret_cast<const uint16_t*>(s + e * 2));
+      acc = k == 0 ? v : cmb<OP>(acc, v);
     }
     for (int d = 0; d < o.nd; ++d) {
       char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
-      if ((o.dmask >> d) & 1) {
-        *reinterpret_cast<float*>(dp + e * 4) = acc;
-      } else {
-        __nv_bfloat16 h = __float2bfloat16_rn(acc);
-        *reinterpret_cast<uint16_t*>(dp + e * 2) = *reinterpret_cast<uint16_t*>(&h);
-      }
+      if ((o.dmask >> d) & 1) *reinterpret_cast<float*>(dp + e * 4) = acc;
+      else *reinterpret_cast<uint16_t*>(dp + e * 2) = narrow1<F16>(acc);
     }
   }
 }
 
 template <int MODE>
 __device__ __forceinline__ int64_t group_elems(const OpDesc& o) {
-  return MODE == kCopy ? 16 / o.esz : ((MODE == kBF16 || MODE == kBF16P) ? 8 : 4);
+  return MODE == kCopy ? 16 / o.esz : (MODE == kF32 || MODE == kI32 ? 4 : 8);
 }
 
-template <int MODE, class P>
+template <int MODE, int OP, class P>
 __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
   // Programmatic dependent launch: this grid may be scheduled while the
   // previous step's grid drains; it lets the next step be scheduled the same
@@ -389,15 +438,15 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     const int64_t tr = lt - run * o.tpr;
     const int64_t soff = run * o.sstride, doff = run * o.dstride;
     if (o.vec) {
-      tile_vec<MODE>(o, ptr, run, tr);
+      tile_vec<MODE, OP>(o, ptr, run, tr);
       if (tr == o.tpr - 1) {  // elements after the last whole group (single-run operations only)
         for (int64_t e = o.groups * group_elems<MODE>(o) + threadIdx.x; e < o.n; e += kThreads)
-          elem<MODE>(o, ptr, soff, doff, e);
+          elem<MODE, OP>(o, ptr, soff, doff, e);
       }
     } else {
       const int64_t e0 = tr * kTileElems;
       const int64_t e1 = e0 + kTileElems < o.n ? e0 + kTileElems : o.n;
-      for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) elem<MODE>(o, ptr, soff, doff, e);
+      for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) elem<MODE, OP>(o, ptr, soff, doff, e);
     }
   }
 }
@@ -519,6 +568,20 @@ const char* base_ptr(const Bases& b, const Operand& o) {
   }
 }
 
+// Elements in one vector group of a step's kernel (must match the device's
+// group_elems): 16 bytes of the copied type; 4 fp32 / int32 values; 8 values
+// of a 16-bit type (fp32 partial sums among them move 32 bytes).
+int64_t group_elements(Mode mode, int esz) {
+  switch (mode) {
+    case Mode::Copy: return 16 / esz;
+    case Mode::F32:
+    case Mode::I32: return 4;
+    case Mode::BF16:
+    case Mode::F16: return 8;
+  }
+  return 0;
+}
+
 template <class P>
 bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t* tiles_out) {
   std::memset(&p, 0, sizeof(P));
@@ -549,7 +612,7 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
       aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
       if (op.dst[s].dt == DT::F32) d.dmask |= 1ull << s;
     }
-    int64_t gelems = mode == Mode::Copy ? 16 / d.esz : (mode == Mode::BF16 ? 8 : 4);
+    const int64_t gelems = group_elements(mode, d.esz);
     if (op.nb > 1) {
       aligned &= (op.n % gelems) == 0 && (op.sstride % 16) == 0 && (op.dstride % 16) == 0;
     }
@@ -573,14 +636,14 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
   return true;
 }
 
-template <int MODE, class P>
+template <int MODE, int OP, class P>
 vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
                          const TraceCtx& tc) {
   static thread_local P p;  // large: keep off the stack
   int64_t tiles = 0;
   if (!fill_params(p, s, i, j, b, &tiles)) return fail(VC_ERR_INVALID_ARG, "operation too large for one launch");
   if (tiles == 0) return VC_SUCCESS;
-  auto kernel = dev::step_kernel<MODE, P>;
+  auto kernel = dev::step_kernel<MODE, OP, P>;
   const int64_t cap = int64_t(st->nsm) * blocks_per_sm(st, kernel);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, cap));
   std::unique_lock<std::mutex> lk(g_trace_mu);
@@ -612,7 +675,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
     pend.rec.coll = tc.coll;
     pend.rec.algo = tc.algo;
     pend.rec.step = tc.step;
-    pend.rec.kernel = MODE + (sizeof(P) == sizeof(dev::LargeParams) ? 8 : 0);
+    pend.rec.kernel = MODE | (OP << 3) | (sizeof(P) == sizeof(dev::LargeParams) ? 32 : 0);
     pend.rec.bytes = launch_bytes(s, i, j);
     pend.rec.nops = static_cast<int32_t>(j - i);
     g_trace.push_back(pend);
@@ -620,20 +683,36 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   return VC_SUCCESS;
 }
 
+template <int MODE, class P>
+vc_status_t launch_op(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
+                      const TraceCtx& tc) {
+  switch (s.red) {
+    case RedOp::Max: return launch_typed<MODE, dev::kMax, P>(st, s, i, j, b, stream, tc);
+    case RedOp::Min: return launch_typed<MODE, dev::kMin, P>(st, s, i, j, b, stream, tc);
+    default: return launch_typed<MODE, dev::kSum, P>(st, s, i, j, b, stream, tc);
+  }
+}
+
 template <class P>
 vc_status_t launch_mode(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
                         const TraceCtx& tc) {
+  // 16-bit steps whose sources are all of the data type take the batched kernel
+  auto pure = [&](DT want) {
+    for (size_t k = i; k < j; ++k)
+      for (const Operand& o : s.ops[k].src)
+        if (o.dt != want) return false;
+    return true;
+  };
   switch (s.mode) {
-    case Mode::Copy: return launch_typed<dev::kCopy, P>(st, s, i, j, b, stream, tc);
-    case Mode::F32: return launch_typed<dev::kF32, P>(st, s, i, j, b, stream, tc);
-    case Mode::I32: return launch_typed<dev::kI32, P>(st, s, i, j, b, stream, tc);
-    default: {
-      bool pure = true;  // every source of every operation in this launch is bf16
-      for (size_t k = i; k < j && pure; ++k)
-        for (const Operand& o : s.ops[k].src) pure &= o.dt == DT::BF16;
-      return pure ? launch_typed<dev::kBF16P, P>(st, s, i, j, b, stream, tc)
-                  : launch_typed<dev::kBF16, P>(st, s, i, j, b, stream, tc);
-    }
+    case Mode::Copy: return launch_typed<dev::kCopy, dev::kSum, P>(st, s, i, j, b, stream, tc);
+    case Mode::F32: return launch_op<dev::kF32, P>(st, s, i, j, b, stream, tc);
+    case Mode::I32: return launch_op<dev::kI32, P>(st, s, i, j, b, stream, tc);
+    case Mode::BF16:
+      return pure(DT::BF16) ? launch_op<dev::kBF16P, P>(st, s, i, j, b, stream, tc)
+                            : launch_op<dev::kBF16, P>(st, s, i, j, b, stream, tc);
+    default:
+      return pure(DT::F16) ? launch_op<dev::kF16P, P>(st, s, i, j, b, stream, tc)
+                           : launch_op<dev::kF16, P>(st, s, i, j, b, stream, tc);
   }
 }
 
@@ -674,7 +753,7 @@ const char* coll_name(Coll c) {
 }
 const char* algo_name(Algo a) {
   static const char* n[] = {"fused", "ring", "rhd", "dbt", "binomial", "scatter_allgather", "pairwise", "bruck",
-                            "auto", "pipe_chain", "pipe_tree"};
+                            "auto", "pipe_chain", "pipe_tree", "mesh"};
   return n[static_cast<int>(a)];
 }
 
@@ -691,6 +770,7 @@ struct Call {
   void* const* recv = nullptr;
   void* recv_root = nullptr;          // Gather, Reduce
   int nchunks = 0;                    // pipelined Broadcast (0: from the cost model)
+  RedOp red = RedOp::Sum;
   cudaStream_t stream = nullptr;
 };
 
@@ -705,11 +785,21 @@ vc_status_t plan_status(PlanStatus ps, const std::string& why) {
   return VC_SUCCESS;
 }
 
+vc_status_t to_op(vc_op_t op, RedOp* out) {
+  switch (op) {
+    case VC_SUM: *out = RedOp::Sum; return VC_SUCCESS;
+    case VC_MAX: *out = RedOp::Max; return VC_SUCCESS;
+    case VC_MIN: *out = RedOp::Min; return VC_SUCCESS;
+  }
+  return fail(VC_ERR_INVALID_ARG, "unknown reduction op");
+}
+
 vc_status_t to_dt(vc_dtype_t d, DT* out) {
   switch (d) {
     case VC_FLOAT32: *out = DT::F32; return VC_SUCCESS;
     case VC_BFLOAT16: *out = DT::BF16; return VC_SUCCESS;
     case VC_INT32: *out = DT::I32; return VC_SUCCESS;
+    case VC_FLOAT16: *out = DT::F16; return VC_SUCCESS;
   }
   return fail(VC_ERR_INVALID_ARG, "unknown dtype");
 }
@@ -734,7 +824,7 @@ vc_status_t to_algo(vc_algo_t a, Algo* out, bool* is_auto = nullptr) {
     *out = Algo::Fused;
     return VC_SUCCESS;
   }
-  if (v < 0 || v > 10 || v == VC_ALGO_AUTO) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
+  if (v < 0 || v > 11 || v == VC_ALGO_AUTO) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
   if (is_auto) *is_auto = false;
   *out = static_cast<Algo>(v);
   return VC_SUCCESS;
@@ -761,6 +851,7 @@ vc_status_t run(const Call& c) {
   if (c.count < 0) return fail(VC_ERR_INVALID_ARG, "count too large");
   // algorithm / rank-count support is decided before looking at sizes
   PlanArgs pa{c.coll, c.algo, N, c.count, c.dt, c.root, false};
+  pa.op = c.red;
   if (c.autoalgo) {
     const vc_status_t rs = resolve_auto(&pa);
     if (rs != VC_SUCCESS) return rs;
@@ -900,7 +991,8 @@ VC_EXPORT vc_status_t vc_allreduce(const void* const* send, void* const* recv, i
     vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
-    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    rc = to_op(op, &c.red);
+    if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
     c.count = static_cast<int64_t>(count);
     c.send = send;
@@ -918,7 +1010,8 @@ VC_EXPORT vc_status_t vc_reduce_scatter(const void* const* send, void* const* re
     vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
-    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    rc = to_op(op, &c.red);
+    if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
     c.count = static_cast<int64_t>(recvcount);
     c.send = send;
@@ -1045,7 +1138,8 @@ VC_EXPORT vc_status_t vc_reduce(const void* const* send, void* recv_root, int nr
     vc_status_t rc = to_algo(algo, &c.algo, &c.autoalgo);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &c.dt);
     if (rc != VC_SUCCESS) return rc;
-    if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
+    rc = to_op(op, &c.red);
+    if (rc != VC_SUCCESS) return rc;
     c.nranks = nranks;
     c.count = static_cast<int64_t>(count);
     c.root = root;
@@ -1130,7 +1224,8 @@ VC_EXPORT double vc_busbw_factor(vc_coll_t coll, int nranks) {
 }
 
 VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
-                                       vc_dtype_t dtype, int root, int inplace, int nchunks, vc_plan_entry_t* entries,
+                                       vc_dtype_t dtype, vc_op_t op, int root, int inplace, int nchunks,
+                                       vc_plan_entry_t* entries,
                                        size_t capacity, size_t* n_entries, size_t* scratch_bytes, int* n_steps) {
   return entry([&]() -> vc_status_t {
     if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
@@ -1139,6 +1234,7 @@ VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nrank
     bool is_auto = false;
     vc_status_t rc = to_algo(algo, &pa.algo, &is_auto);
     if (rc == VC_SUCCESS) rc = to_dt(dtype, &pa.dt);
+    if (rc == VC_SUCCESS) rc = to_op(op, &pa.op);
     if (rc != VC_SUCCESS) return rc;
     pa.nranks = nranks;
     pa.count = static_cast<int64_t>(count);
@@ -1178,7 +1274,7 @@ VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nrank
             e.buf = static_cast<int32_t>(list[pos].buf);
             e.owner = list[pos].owner;
             e.dtype = static_cast<int32_t>(list[pos].dt);
-            e.reduce = s.mode == Mode::Copy ? 0 : 1;
+            e.reduce = s.mode == Mode::Copy ? 0 : 1 + static_cast<int32_t>(s.red);
             e.byte_off = list[pos].byte_off;
             e.n = op.n;
             e.nb = op.nb;

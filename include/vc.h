@@ -30,17 +30,18 @@
  *  - Errors are returned, never raised: VC_ERR_INVALID_ARG (null pointer,
  *    nranks outside [1, VC_MAX_RANKS], root outside [0, nranks), overlapping
  *    buffers, size overflow), VC_ERR_UNSUPPORTED (an algorithm that is not
- *    defined for the collective or the rank count, an op other than VC_SUM),
+ *    defined for the collective or the rank count),
  *    VC_ERR_NOMEM (scratch allocation failed), VC_ERR_CUDA (a CUDA call or
  *    launch failed; vc_last_error() has the text).  On any error nothing has
  *    been enqueued, except for VC_ERR_CUDA from a launch after earlier steps.
  *  - A count of 0 returns VC_SUCCESS without enqueuing anything.
  *
- * Reductions: VC_SUM on VC_FLOAT32 (fp32 adds), VC_BFLOAT16 (inputs widened to
- * fp32, summed in fp32, rounded once to bf16, round to nearest even) and
- * VC_INT32 (two's-complement wrap-around).  Every algorithm fixes the
- * association of its adds per element, so results are reproducible bit for
- * bit run to run; different algorithms may differ in the last bits.
+ * Reductions (VC_SUM, VC_MAX, VC_MIN) on VC_FLOAT32 (in fp32), VC_BFLOAT16
+ * and VC_FLOAT16 (inputs widened exactly to fp32, combined in fp32, rounded
+ * once to the 16-bit type, round to nearest even) and VC_INT32 (sums wrap
+ * around).  Every algorithm fixes the association per element, so results
+ * are reproducible bit for bit run to run; different algorithms may differ
+ * in the last bits of a sum.
  */
 #ifndef VC_H_
 #define VC_H_
@@ -66,9 +67,15 @@ typedef enum {
   VC_ERR_TIMEOUT = 5
 } vc_status_t;
 
-typedef enum { VC_FLOAT32 = 0, VC_BFLOAT16 = 1, VC_INT32 = 2 } vc_dtype_t;
+typedef enum { VC_FLOAT32 = 0, VC_BFLOAT16 = 1, VC_INT32 = 2, VC_FLOAT16 = 3 } vc_dtype_t;
 
-/* The hccl article lists SUM / MAX / MIN; this version implements VC_SUM. */
+/*
+ * Reduction ops, as the hccl article lists them (SUM / MAX / MIN).  MAX and
+ * MIN keep the first operand unless the second is larger (smaller) or the
+ * first is NaN: a NaN is passed over while a number is present, and of +0
+ * and -0 the one met first in the algorithm's fixed association is kept.
+ * int32 compares signed.  16-bit floats are compared after exact widening.
+ */
 typedef enum { VC_SUM = 0, VC_MAX = 1, VC_MIN = 2 } vc_op_t;
 
 typedef enum {
@@ -82,7 +89,8 @@ typedef enum {
   VC_ALGO_BRUCK = 7,             /* AllToAll                                           */
   VC_ALGO_AUTO = 8,              /* any collective: cheapest under the cost model      */
   VC_ALGO_PIPE_CHAIN = 9,        /* Broadcast, message cut into chunks along a chain   */
-  VC_ALGO_PIPE_TREE = 10         /* Broadcast, chunks down the binomial tree           */
+  VC_ALGO_PIPE_TREE = 10,        /* Broadcast, chunks down the binomial tree           */
+  VC_ALGO_MESH = 11              /* AllReduce: root 0 folds every rank, then sends     */
 } vc_algo_t;
 
 typedef enum {
@@ -106,7 +114,10 @@ typedef enum {
  *   is allowed, as hccl_allreduce allows sendbuf == recvbuf.
  *   algo: FUSED (rank-order sum in one pass), RING (ReduceScatter + AllGather
  *   in 2(N-1) steps), RHD (2 log2 N rounds; VC_ERR_UNSUPPORTED unless nranks
- *   is a power of 2), DBT (two mirrored heap trees, 2 floor(log2 N) levels).
+ *   is a power of 2), DBT (two mirrored heap trees, 2 floor(log2 N) levels),
+ *   MESH (hccl article, section "Mesh算法：全连接广播": rank 0 folds the other
+ *   ranks in rank order, one per step, then sends the result to each, one
+ *   per step; 2(N-1) steps).
  */
 vc_status_t vc_allreduce(const void* const* send, void* const* recv, int nranks, size_t count,
                          vc_dtype_t dtype, vc_op_t op, vc_algo_t algo, vc_stream_t stream);
@@ -157,7 +168,9 @@ vc_status_t vc_scatter(const void* send_root, void* const* recv, int nranks, siz
  * model-algo-a2a-pairwise, model-algo-a2a-bruck).
  *   send[i], recv[j]: nranks*blockcount elements.  No in-place.
  *   algo: FUSED (one pass), PAIRWISE (N-1 exchange rounds plus the local
- *   block), BRUCK (ceil(log2 N) rounds through two library scratch buffers).
+ *   block), BRUCK (ceil(log2 N) rounds through two library scratch buffers),
+ *   RING (eq. model-algo-a2a-ring: N-1 rounds of store and forward to the
+ *   right-hand neighbour, through two library forwarding buffers).
  */
 vc_status_t vc_alltoall(const void* const* send, void* const* recv, int nranks, size_t blockcount,
                         vc_dtype_t dtype, vc_algo_t algo, vc_stream_t stream);
@@ -257,8 +270,9 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
  * Builds the step plan a call with these arguments would execute (nchunks:
  * as vc_broadcast_pipelined; ignored by other algorithms) and writes
  * one entry per operand of every operation.  An operation reads its sources
- * in the listed order (`pos`), adds them left to right (reduction steps) or
- * copies its single source (copy steps), and writes the result to each of its
+ * in the listed order (`pos`), combines them left to right with the step's
+ * op (reduction steps) or copies its single source (copy steps), and writes
+ * the result to each of its
  * destinations; it covers `nb` runs of `n` elements, run b starting
  * b*stride_bytes after run 0.  All operations of one step are independent and
  * run in one launch; steps run in order.
@@ -277,7 +291,7 @@ typedef struct {
   int32_t buf;    /* 0 send, 1 recv, 2 scratch */
   int32_t owner;  /* rank */
   int32_t dtype;  /* vc_dtype_t of the operand */
-  int32_t reduce; /* 1 for a reduction operation, 0 for a copy */
+  int32_t reduce; /* 0 copy; reduction: 1 sum, 2 max, 3 min */
   int64_t byte_off;
   int64_t n;
   int64_t nb;
@@ -285,7 +299,8 @@ typedef struct {
 } vc_plan_entry_t;
 
 vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
-                             vc_dtype_t dtype, int root, int inplace, int nchunks, vc_plan_entry_t* entries,
+                             vc_dtype_t dtype, vc_op_t op, int root, int inplace, int nchunks,
+                             vc_plan_entry_t* entries,
                              size_t capacity, size_t* n_entries, size_t* scratch_bytes,
                              int* n_steps);
 
@@ -298,9 +313,11 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  * at its storage size).  vc_trace_enable(1) clears old records;
  * vc_trace_read waits for the recorded events, writes up to `capacity`
  * records with their event-timed durations and clears them.
- *   kernel: 0 copy, 1 fp32 sum, 2 int32 sum, 3 bf16 sum (bf16 and fp32
- *   sources), 4 bf16 sum (bf16 sources only); +8 when the launch used the
- *   large parameter block (more than 16 operations or 64 operand pointers).
+ *   kernel: bits 0-2 the mode (0 copy, 1 fp32, 2 int32, 3 bf16 with fp32
+ *   partials among the sources, 4 bf16 only, 5 fp16 with fp32 partials, 6
+ *   fp16 only), bits 3-4 the op (0 sum, 1 max, 2 min), bit 5 set when the
+ *   launch used the large parameter block (more than 16 operations or 64
+ *   operand pointers).
  */
 typedef struct {
   int32_t coll;   /* vc_coll_t */

@@ -18,13 +18,14 @@ from __future__ import annotations
 
 import numpy as np
 
-DTYPES = ("f32", "bf16", "i32")
-ESIZE = {"f32": 4, "bf16": 2, "i32": 4}  # bytes per stored element
-ACC_ESIZE = {"f32": 4, "bf16": 4, "i32": 4}  # bytes per accumulated element
+DTYPES = ("f32", "bf16", "i32", "f16")
+ESIZE = {"f32": 4, "bf16": 2, "i32": 4, "f16": 2}  # bytes per stored element
+ACC_ESIZE = {"f32": 4, "bf16": 4, "i32": 4, "f16": 4}  # bytes per accumulated element
+OPS = ("sum", "max", "min")
 
 
 def storage_dtype(dtype: str):
-    return {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}[dtype]
+    return {"f32": np.float32, "bf16": np.uint16, "i32": np.int32, "f16": np.float16}[dtype]
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -54,9 +55,12 @@ def f32_to_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def widen(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Stored values -> accumulation lane type (a fresh array)."""
+    """Stored values -> accumulation lane type (a fresh array).  fp16 is
+    widened by numpy's binary16 -> binary32 conversion (exact)."""
     if dtype == "f32":
         return np.array(x, dtype=np.float32, copy=True)
+    if dtype == "f16":
+        return np.asarray(x, dtype=np.float16).astype(np.float32)
     if dtype == "bf16":
         return bf16_to_f32(x).copy()
     if dtype == "i32":
@@ -65,9 +69,14 @@ def widen(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def narrow(acc: np.ndarray, dtype: str) -> np.ndarray:
-    """Accumulation lane type -> stored values (one rounding for bf16)."""
+    """Accumulation lane type -> stored values (one rounding for bf16 and
+    fp16; fp16 by numpy's binary32 -> binary16 conversion, round to nearest
+    even)."""
     if dtype == "f32":
         return np.array(acc, dtype=np.float32, copy=True)
+    if dtype == "f16":
+        with np.errstate(over="ignore"):
+            return np.asarray(acc, dtype=np.float32).astype(np.float16)
     if dtype == "bf16":
         return f32_to_bf16(acc)
     if dtype == "i32":
@@ -80,6 +89,28 @@ def add(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     assert a.dtype == b.dtype and a.dtype in (np.float32, np.uint32), (a.dtype, b.dtype)
     with np.errstate(over="ignore", invalid="ignore"):
         return a + b
+
+
+def combine(a: np.ndarray, b: np.ndarray, op: str) -> np.ndarray:
+    """One reduction step a (+) b in the lane type.
+
+    sum: ``add``.  max / min (the hccl article lists SUM, MAX and MIN; it does
+    not say how NaN or signed zeros behave): the reading taken is
+    max(a, b) = b if b > a or a is NaN, else a (and min with b < a).  A NaN
+    operand is passed over while a number is present, and of two equal
+    values (+0 and -0) the first is kept, so the result depends on the
+    association only through the sign of zero and NaN payloads.  int32
+    compares as signed."""
+    if op == "sum":
+        return add(a, b)
+    assert a.dtype == b.dtype
+    if a.dtype == np.uint32:
+        ai, bi = a.view(np.int32), b.view(np.int32)
+        take_b = bi > ai if op == "max" else bi < ai
+    else:
+        with np.errstate(invalid="ignore"):
+            take_b = ((b > a) if op == "max" else (b < a)) | np.isnan(a)
+    return np.where(take_b, b, a)
 
 
 def same_bits(a: np.ndarray, b: np.ndarray) -> bool:

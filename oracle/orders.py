@@ -9,8 +9,8 @@ inputs.  Large buffers are checked element by element through this module.
 
 AllReduce, element e (chunks cut by ``oracle.partition``):
 
-* fused:  ((x0 + x1) + x2) + ... + x_{N-1}  -- rank order, the fold of the
-  [hccl article]'s Mesh root (section "Mesh算法：全连接广播").
+* fused, mesh:  ((x0 + x1) + x2) + ... + x_{N-1}  -- rank order, the fold
+  of the [hccl article]'s Mesh root (section "Mesh算法：全连接广播").
 * ring:   chunk c = chunk of e; ((x_c + x_{c+1}) + x_{c+2}) + ... + x_{c+N-1},
   indices mod N ([hccl article] section "Ring算法": at step 0 rank c sends
   chunk c, each later hop adds its own copy).
@@ -34,7 +34,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .numerics import ESIZE, add, narrow, widen
+from .numerics import ESIZE, combine, narrow, widen
 from .partition import chunk_of, chunk_range
 from .schedules import dbt_trees
 
@@ -64,7 +64,7 @@ def heap_tree(i: int, N: int, rank_of):
 def allreduce_tree(algo: str, N: int, count: int, dtype: str, e: int):
     """Association tree (nested pairs of rank indices) for element e."""
     esz = ESIZE[dtype]
-    if algo == "fused":
+    if algo in ("fused", "mesh"):
         return left_fold(list(range(N)))
     if algo == "ring":
         c = chunk_of(e, count, N, esz)
@@ -88,12 +88,12 @@ def reduce_scatter_tree(algo: str, N: int, rc: int, e: int):
     raise ValueError(algo)
 
 
-def evaluate(tree, cols: dict):
+def evaluate(tree, cols: dict, op: str = "sum"):
     """Evaluate a tree on lane-type columns (one array per rank)."""
     if isinstance(tree, int):
         return cols[tree]
     a, b = tree
-    return add(evaluate(a, cols), evaluate(b, cols))
+    return combine(evaluate(a, cols, op), evaluate(b, cols, op), op)
 
 
 def _group_key_allreduce(algo, N, count, dtype, e):
@@ -105,7 +105,7 @@ def _group_key_allreduce(algo, N, count, dtype, e):
     return 0
 
 
-def allreduce_at(values_at, algo: str, count: int, dtype: str, idx) -> np.ndarray:
+def allreduce_at(values_at, algo: str, count: int, dtype: str, idx, op: str = "sum") -> np.ndarray:
     """Expected AllReduce output at element indices ``idx``.
 
     ``values_at[r]`` holds rank r's stored input values at ``idx``.  Returns
@@ -118,14 +118,14 @@ def allreduce_at(values_at, algo: str, count: int, dtype: str, idx) -> np.ndarra
         sel = np.nonzero(keys == key)[0]
         tree = allreduce_tree(algo, N, count, dtype, int(idx[sel[0]]))
         cols = {r: widen(np.asarray(values_at[r])[sel], dtype) for r in range(N)}
-        res = narrow(evaluate(tree, cols), dtype)
+        res = narrow(evaluate(tree, cols, op), dtype)
         if out is None:
             out = np.empty(len(idx), dtype=res.dtype)
         out[sel] = res
     return out
 
 
-def reduce_scatter_at(values_at, algo: str, rc: int, dtype: str, idx) -> np.ndarray:
+def reduce_scatter_at(values_at, algo: str, rc: int, dtype: str, idx, op: str = "sum") -> np.ndarray:
     """Expected ReduceScatter result for input-space element indices ``idx``
     (element e lands on rank e // rc at offset e % rc)."""
     N = len(values_at)
@@ -136,7 +136,7 @@ def reduce_scatter_at(values_at, algo: str, rc: int, dtype: str, idx) -> np.ndar
         sel = np.nonzero(keys == key)[0]
         tree = reduce_scatter_tree(algo, N, rc, int(idx[sel[0]]))
         cols = {r: widen(np.asarray(values_at[r])[sel], dtype) for r in range(N)}
-        res = narrow(evaluate(tree, cols), dtype)
+        res = narrow(evaluate(tree, cols, op), dtype)
         if out is None:
             out = np.empty(len(idx), dtype=res.dtype)
         out[sel] = res

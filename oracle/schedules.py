@@ -29,17 +29,17 @@ from typing import Callable
 
 import numpy as np
 
-from .numerics import ACC_ESIZE, ESIZE, add, narrow, storage_dtype, widen
+from .numerics import ACC_ESIZE, ESIZE, combine, narrow, storage_dtype, widen
 from .partition import chunk_range
 from .translog import TransferLog
 
 ALGOS = {
-    "allreduce": ("fused", "ring", "rhd", "dbt"),
+    "allreduce": ("fused", "ring", "rhd", "dbt", "mesh"),
     "reduce_scatter": ("fused", "ring"),
     "allgather": ("fused", "ring"),
     "broadcast": ("fused", "binomial", "scatter_allgather"),
     "scatter": ("fused", "binomial"),
-    "alltoall": ("fused", "pairwise", "bruck"),
+    "alltoall": ("fused", "pairwise", "bruck", "ring"),
 }
 
 # Test-only fault injection: {"drop_step": s} loses every message of step s,
@@ -97,9 +97,9 @@ def _run_step(log: TransferLog, step: int, msgs: list) -> None:
             m.deliver(m.payload)
 
 
-def _reduce_into(buf: np.ndarray, lo: int, hi: int):
+def _reduce_into(buf: np.ndarray, lo: int, hi: int, op: str = "sum"):
     def f(p):
-        buf[lo:hi] = add(buf[lo:hi], p)
+        buf[lo:hi] = combine(buf[lo:hi], p, op)
     return f
 
 
@@ -145,19 +145,21 @@ def _check_same(inputs, dtype):
 # AllReduce
 # --------------------------------------------------------------------------
 
-def allreduce(inputs, algo: str, dtype: str, inplace: bool = False) -> Result:
+def allreduce(inputs, algo: str, dtype: str, inplace: bool = False, op: str = "sum") -> Result:
     """out_r = elementwise sum of all ranks' inputs, on every rank
     ([Latency-formula page], section "Ring AllReduce"; [hccl article] section
     "集合通信vs点对点" -- every rank ends with the same reduced data)."""
     N, count = _check_same(inputs, dtype)
     if algo == "fused":
-        return _allreduce_fused(inputs, dtype)
+        return _allreduce_fused(inputs, dtype, op)
     if algo == "ring":
-        return _allreduce_ring(inputs, dtype)
+        return _allreduce_ring(inputs, dtype, op)
     if algo == "rhd":
-        return _allreduce_rhd(inputs, dtype)
+        return _allreduce_rhd(inputs, dtype, op)
     if algo == "dbt":
-        return _allreduce_dbt(inputs, dtype)
+        return _allreduce_dbt(inputs, dtype, op)
+    if algo == "mesh":
+        return _allreduce_mesh(inputs, dtype, op)
     raise Unsupported(f"allreduce/{algo}")
 
 
@@ -166,7 +168,7 @@ def _self_copy_result(inputs, dtype, bm: _Bytes):
     return [np.array(x, copy=True) for x in inputs]
 
 
-def _allreduce_fused(inputs, dtype):
+def _allreduce_fused(inputs, dtype, op="sum"):
     """One pass: every rank's element e is read once and summed in rank order,
     ((x0 + x1) + x2) + ... -- the order in which the Mesh root of the
     [hccl article] (section "Mesh算法：全连接广播") folds ranks 0..N-1 into its
@@ -177,7 +179,7 @@ def _allreduce_fused(inputs, dtype):
     log = TransferLog()
     acc = widen(inputs[0], dtype)
     for q in range(1, N):
-        acc = add(acc, widen(inputs[q], dtype))
+        acc = combine(acc, widen(inputs[q], dtype), op)
     if N > 1:
         for q in range(N):
             for r in range(N):
@@ -189,7 +191,39 @@ def _allreduce_fused(inputs, dtype):
     return Result([out.copy() for _ in range(N)], log, bm.total)
 
 
-def _allreduce_ring(inputs, dtype):
+def _allreduce_mesh(inputs, dtype, op="sum"):
+    """Mesh AllReduce of the [hccl article] (section "Mesh算法：全连接广播"),
+    taken step for step from its code: the root receives every other rank's
+    buffer in rank order and folds each into its own (N-1 steps of one
+    message), then sends the result to every other rank in rank order (N-1
+    steps).  The article's AllReduce has a root argument; an AllReduce call
+    here has none, and the reading taken is root 0.  The fold is the rank
+    order ((x0 + x1) + x2) + ..., the fused kernel's."""
+    N, count = len(inputs), len(inputs[0])
+    bm = _Bytes(dtype)
+    log = TransferLog()
+    if N == 1:
+        return Result(_self_copy_result(inputs, dtype, bm), log, bm.total)
+    acc = [widen(x, dtype) for x in inputs]
+    root, step = 0, 0
+    others = [i for i in range(N) if i != root]
+    for t, i in enumerate(others):
+        wire_own = bm.e_in if t == 0 else bm.e_acc
+        _run_step(log, step, [_Msg(src=i, dst=root, n=count, reduce=True, esize=bm.e_in,
+                                   payload=acc[i].copy(), deliver=_reduce_into(acc[root], 0, count, op),
+                                   phase="mesh_reduce", src_off=0, dst_off=0)])
+        bm.rw(count, wire_own, bm.e_in, bm.e_out if t == N - 2 else bm.e_acc)
+        step += 1
+    for i in others:
+        _run_step(log, step, [_Msg(src=root, dst=i, n=count, reduce=False, esize=bm.e_out,
+                                   payload=acc[root].copy(), deliver=_store_into(acc[i], 0, count),
+                                   phase="mesh_bcast", src_off=0, dst_off=0)])
+        bm.rw(count, bm.e_out, bm.e_out)
+        step += 1
+    return Result([narrow(a, dtype) for a in acc], log, bm.total)
+
+
+def _allreduce_ring(inputs, dtype, op="sum"):
     """Ring AllReduce = Ring ReduceScatter (N-1 steps) then Ring AllGather
     (N-1 steps) ([hccl article] section "Ring算法：环形流水线传输";
     [Latency-formula page] eqs. model-algo-ring-rs, -ag, -ar).
@@ -224,7 +258,7 @@ def _allreduce_ring(inputs, dtype):
             dst = (r + 1) % N
             wire = bm.e_in if s == 0 else bm.e_acc
             msgs.append(_Msg(src=r, dst=dst, n=hi - lo, reduce=True, esize=wire,
-                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[dst], lo, hi),
+                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[dst], lo, hi, op),
                              phase="rs", src_off=lo, dst_off=lo, chunks=(c,)))
             bm.rw(hi - lo, bm.e_in, wire, bm.e_out if s == N - 2 else bm.e_acc)
         _run_step(log, step, msgs)
@@ -244,7 +278,7 @@ def _allreduce_ring(inputs, dtype):
     return Result([narrow(a, dtype) for a in acc], log, bm.total)
 
 
-def _allreduce_rhd(inputs, dtype):
+def _allreduce_rhd(inputs, dtype, op="sum"):
     """Recursive Halving-Doubling (Rabenseifner) AllReduce, N a power of 2
     ([Latency-formula page] section "Recursive Halving-Doubling", eqs.
     model-algo-rhd-rs, -ag, -ar).
@@ -291,7 +325,7 @@ def _allreduce_rhd(inputs, dtype):
             lo, hi = elems(*give)
             wire = bm.e_in if k == 0 else bm.e_acc
             msgs.append(_Msg(src=r, dst=p, n=hi - lo, reduce=True, esize=wire,
-                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[p], lo, hi),
+                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[p], lo, hi, op),
                              phase="halving", src_off=lo, dst_off=lo,
                              chunks=tuple(range(*give))))
             bm.rw(hi - lo, bm.e_in if k == 0 else bm.e_acc, wire,
@@ -338,7 +372,7 @@ def heap_depth(i: int) -> int:
     return (i + 1).bit_length() - 1
 
 
-def _allreduce_dbt(inputs, dtype):
+def _allreduce_dbt(inputs, dtype, op="sum"):
     """Double Binary Tree AllReduce ([Latency-formula page] section "Double
     Binary Tree", eq. model-algo-dbt-ar): each tree reduces its half up to the
     root (one tree level per step, deepest first) and broadcasts it back down
@@ -376,7 +410,7 @@ def _allreduce_dbt(inputs, dtype):
                     reads.append(wire)
                     u = rank_of(c)
                     msgs.append(_Msg(src=u, dst=v, n=hi - lo, reduce=True, esize=wire,
-                                     payload=acc[u][lo:hi].copy(), deliver=_reduce_into(acc[v], lo, hi),
+                                     payload=acc[u][lo:hi].copy(), deliver=_reduce_into(acc[v], lo, hi, op),
                                      phase="reduce" + name, src_off=lo, dst_off=lo))
                 bm.rw(hi - lo, *reads, bm.e_out if i == 0 else bm.e_acc)
         _run_step(log, step, msgs)
@@ -402,7 +436,7 @@ def _allreduce_dbt(inputs, dtype):
 # ReduceScatter and AllGather alone
 # --------------------------------------------------------------------------
 
-def reduce_scatter(inputs, algo: str, dtype: str) -> Result:
+def reduce_scatter(inputs, algo: str, dtype: str, op: str = "sum") -> Result:
     """Each input holds N blocks of rc elements; rank r ends with block r of
     the elementwise sum ([Latency-formula page] section "Ring ReduceScatter",
     eq. model-algo-ring-reducescatter: every node ends with 1/N of the reduced
@@ -418,7 +452,7 @@ def reduce_scatter(inputs, algo: str, dtype: str) -> Result:
         for r in range(N):
             acc = widen(inputs[0][r * rc:(r + 1) * rc], dtype)
             for q in range(1, N):
-                acc = add(acc, widen(inputs[q][r * rc:(r + 1) * rc], dtype))
+                acc = combine(acc, widen(inputs[q][r * rc:(r + 1) * rc], dtype), op)
             for q in range(N):
                 if q != r:
                     log.add(step=0, phase="fused", src=q, dst=r, n=rc, reduce=True, esize=e,
@@ -444,7 +478,7 @@ def reduce_scatter(inputs, algo: str, dtype: str) -> Result:
             dst = (r + 1) % N
             wire = bm.e_in if s == 0 else bm.e_acc
             msgs.append(_Msg(src=r, dst=dst, n=rc, reduce=True, esize=wire,
-                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[dst], lo, hi),
+                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[dst], lo, hi, op),
                              phase="rs", src_off=lo, dst_off=lo, chunks=(c,)))
             bm.rw(rc, bm.e_in, wire, bm.e_out if s == N - 2 else bm.e_acc)
         _run_step(log, s, msgs)
@@ -681,6 +715,8 @@ def alltoall(inputs, algo: str, dtype: str) -> Result:
         return _alltoall_pairwise(inputs, dtype, B)
     if algo == "bruck":
         return _alltoall_bruck(inputs, dtype, B)
+    if algo == "ring":
+        return _alltoall_ring(inputs, dtype, B)
     raise Unsupported(f"alltoall/{algo}")
 
 
@@ -705,6 +741,46 @@ def _alltoall_pairwise(inputs, dtype, B):
                              src_off=j * B, dst_off=i * B))
             bm.rw(B, bm.e_in, bm.e_out)
         _run_step(log, k, msgs)
+    return Result(out, log, bm.total, local_steps=1 if N > 1 else 0)
+
+
+def _alltoall_ring(inputs, dtype, B):
+    """Ring AllToAll ([Latency-formula page] eq. model-algo-a2a-ring: N-1
+    rounds, each rank talking only to its ring neighbours).  Reading: store
+    and forward -- in round k every rank passes to rank i+1 every block it
+    holds that is not addressed to itself, and keeps the one that is; a block
+    from rank s for rank d travels (d - s) mod N hops.  Round 0 is the local
+    block.  Round k carries N-k blocks per rank, so a rank sends
+    (N-1)/2 * M in all, not the (N-1)/N * M the page's formula charges (it
+    writes Pairwise's bandwidth term for the ring as well)."""
+    N = len(inputs)
+    bm = _Bytes(dtype)
+    log = TransferLog()
+    out = [np.zeros(N * B, dtype=storage_dtype(dtype)) for _ in range(N)]
+    for i in range(N):
+        out[i][i * B:(i + 1) * B] = inputs[i][i * B:(i + 1) * B]
+        bm.rw(B, bm.e_in, bm.e_out)
+    # in transit at rank i: {(source, destination): block}
+    transit = {i: {(i, d): inputs[i][d * B:(d + 1) * B].copy() for d in range(N) if d != i} for i in range(N)}
+    for k in range(1, N):
+        msgs = []
+        nxt = {i: {} for i in range(N)}
+        for i in range(N):
+            dst = (i + 1) % N
+            keys = sorted(transit[i], key=lambda sd: (sd[1] - dst) % N)
+            payload = {key: transit[i][key] for key in keys}
+
+            def deliver(p, dst=dst):
+                for (src, d), blk in p.items():
+                    if d == dst:
+                        out[dst][src * B:(src + 1) * B] = blk
+                    else:
+                        nxt[dst][(src, d)] = blk
+            msgs.append(_Msg(src=i, dst=dst, n=len(keys) * B, reduce=False, esize=bm.e_in,
+                             payload=payload, deliver=deliver, phase="ring", chunks=tuple(keys)))
+            bm.rw(len(keys) * B, bm.e_in, bm.e_out)
+        _run_step(log, k, msgs)
+        transit = nxt
     return Result(out, log, bm.total, local_steps=1 if N > 1 else 0)
 
 
@@ -869,7 +945,7 @@ def gather(inputs, root: int, algo: str, dtype: str) -> Result:
     return Result([out], log, bm.total)
 
 
-def reduce(inputs, root: int, algo: str, dtype: str, inplace: bool = False) -> Result:
+def reduce(inputs, root: int, algo: str, dtype: str, inplace: bool = False, op: str = "sum") -> Result:
     """Reduce to one root: out_root = elementwise sum of every rank's input
     ([Latency-formula page] section "Broadcast / Reduce 怎么用 Tree 算法", eq.
     model-algo-reduce-tree: the Tree Broadcast run backwards, same cost).
@@ -891,7 +967,7 @@ def reduce(inputs, root: int, algo: str, dtype: str, inplace: bool = False) -> R
     if algo == "fused":
         acc = widen(inputs[0], dtype)
         for q in range(1, N):
-            acc = add(acc, widen(inputs[q], dtype))
+            acc = combine(acc, widen(inputs[q], dtype), op)
         for q in range(N):
             if q != root:
                 log.add(step=0, phase="fused", src=q, dst=root, n=count, reduce=True, esize=bm.e_in,
@@ -911,7 +987,7 @@ def reduce(inputs, root: int, algo: str, dtype: str, inplace: bool = False) -> R
             src, dst = (v + root) % N, (u + root) % N
             wire = bm.e_acc if partial[v] else bm.e_in
             msgs.append(_Msg(src=src, dst=dst, n=count, reduce=True, esize=wire,
-                             payload=acc[src].copy(), deliver=_reduce_into(acc[dst], 0, count),
+                             payload=acc[src].copy(), deliver=_reduce_into(acc[dst], 0, count, op),
                              phase="reduce", src_off=0, dst_off=0))
             last = u == 0 and s == L - 1
             bm.rw(count, bm.e_acc if partial[u] else bm.e_in, wire, bm.e_out if last else bm.e_acc)

@@ -82,7 +82,7 @@ def link_candidates(coll: str, N: int) -> dict:
     if coll == "reduce":
         return {"binomial": cm.t_reduce_tree}
     if coll == "alltoall":
-        return {"pairwise": cm.t_a2a_pairwise, "bruck": cm.t_a2a_bruck}
+        return {"pairwise": cm.t_a2a_pairwise, "bruck": cm.t_a2a_bruck, "ring": cm.t_a2a_ring}
     raise ValueError(coll)
 
 

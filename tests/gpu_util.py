@@ -8,13 +8,14 @@ import torch
 GUARD_BYTES = 256
 CANARY = 0x5A
 
-TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32}
-NP_DT = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}
-ESZ = {"f32": 4, "bf16": 2, "i32": 4}
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "i32": torch.int32, "f16": torch.float16}
+NP_DT = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32, "f16": np.float16}
+ESZ = {"f32": 4, "bf16": 2, "i32": 4, "f16": 2}
 
 
 def dtype_of(x: np.ndarray) -> str:
-    return {np.dtype(np.float32): "f32", np.dtype(np.uint16): "bf16", np.dtype(np.int32): "i32"}[x.dtype]
+    return {np.dtype(np.float32): "f32", np.dtype(np.uint16): "bf16", np.dtype(np.int32): "i32",
+            np.dtype(np.float16): "f16"}[x.dtype]
 
 
 class Guarded:

@@ -17,17 +17,17 @@ import torch
 from collective_communication_algorithms_virtual_gb300 import vc_plan_describe
 
 SEND, RECV, SCRATCH = 0, 1, 2
-NPT = {0: np.float32, 1: np.uint16, 2: np.int32}
-ESZ = {0: 4, 1: 2, 2: 4}
-DT = {"f32": 0, "bf16": 1, "i32": 2}
+NPT = {0: np.float32, 1: np.uint16, 2: np.int32, 3: np.float16}
+ESZ = {0: 4, 1: 2, 2: 4, 3: 2}
+DT = {"f32": 0, "bf16": 1, "i32": 2, "f16": 3}
 
 
-def get_plan(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0):
-    entries, scratch, nsteps = vc_plan_describe(coll, algo, N, count, dtype, root, inplace, nchunks)
+def get_plan(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0, op="sum"):
+    entries, scratch, nsteps = vc_plan_describe(coll, algo, N, count, dtype, root, inplace, nchunks, op)
     steps = [dict() for _ in range(nsteps)]
     for e in entries:
-        op = steps[e.step].setdefault(e.op, {"reduce": bool(e.reduce), "n": e.n, "nb": e.nb,
-                                             "src": [], "dst": []})
+        op = steps[e.step].setdefault(e.op, {"reduce": bool(e.reduce), "red": e.reduce, "n": e.n,
+                                             "nb": e.nb, "src": [], "dst": []})
         (op["src"] if e.role == 0 else op["dst"]).append(
             (e.pos, e.buf, e.owner, e.dtype, e.byte_off, e.stride_bytes))
     out = []
@@ -77,6 +77,8 @@ class Memory:
 def _widen(raw, dt):
     if dt == 0:
         return raw.view(np.float32).copy()
+    if dt == 3:
+        return raw.view(np.float16).astype(np.float32)
     if dt == 1:
         return (raw.view(np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
     return raw.view(np.int32).view(np.uint32).copy()
@@ -85,10 +87,24 @@ def _widen(raw, dt):
 def _narrow(acc, dt):
     if dt == 0:
         return acc.astype(np.float32).view(np.uint8)
+    if dt == 3:
+        with np.errstate(over="ignore"):
+            return acc.astype(np.float32).astype(np.float16).view(np.uint8)
     if dt == 1:
         t = torch.from_numpy(acc.astype(np.float32)).to(torch.bfloat16)
         return t.view(torch.int16).numpy().view(np.uint8)
     return acc.astype(np.uint32).view(np.uint8)
+
+
+def _combine(a, b, red):
+    """1 sum, 2 max, 3 min (max/min: take b if it is larger/smaller or a is NaN)."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        if red == 1:
+            return a + b
+        if a.dtype == np.uint32:
+            ai, bi = a.view(np.int32), b.view(np.int32)
+            return np.where(bi > ai if red == 2 else bi < ai, b, a)
+        return np.where(((b > a) if red == 2 else (b < a)) | (a != a), b, a)
 
 
 def run_plan(plan, mem: Memory) -> None:
@@ -100,8 +116,7 @@ def run_plan(plan, mem: Memory) -> None:
                 if op["reduce"]:
                     acc = _widen(srcs[0], op["src"][0][2])
                     for s, (k, o, dt, off, stride) in zip(srcs[1:], op["src"][1:]):
-                        with np.errstate(over="ignore", invalid="ignore"):
-                            acc = acc + _widen(s, dt)
+                        acc = _combine(acc, _widen(s, dt), op["red"])
                 for (k, o, dt, off, stride) in op["dst"]:
                     dstv = mem.view(k, o, dt, off + b * stride, n)
                     dstv[:] = _narrow(acc, dt) if op["reduce"] else srcs[0]

@@ -220,8 +220,11 @@ def test_errors_leave_outputs_untouched():
     xs = [torch.ones(64, device="cuda") for _ in range(N)]
     ys = [torch.zeros(64, device="cuda") for _ in range(N)]
     with pytest.raises(vc.VCError) as e:
-        vc.vc_allreduce(xs, ys, algo="rhd", op="max")
+        vc.vc_allreduce(xs[:3], ys[:3], algo="rhd")
     assert e.value.status == 2
+    with pytest.raises(vc.VCError) as e:
+        vc.vc_allreduce(xs, ys, algo="ring", op=7)
+    assert e.value.status == 1
     with pytest.raises(vc.VCError):
         vc.vc_allreduce(xs, [ys[0]] * N, algo="ring")
     torch.cuda.synchronize()

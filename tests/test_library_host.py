@@ -79,13 +79,14 @@ def test_invalid_arguments_rejected_on_host():
     assert L.vc_allreduce(good, outs, 0, 16, F32, SUM, RING, None) == vc.binding.VC_ERR_INVALID_ARG
     assert L.vc_allreduce(good, outs, 65, 16, F32, SUM, RING, None) == vc.binding.VC_ERR_INVALID_ARG
     assert L.vc_allreduce(good, outs, 4, 16, 7, SUM, RING, None) == vc.binding.VC_ERR_INVALID_ARG
-    assert L.vc_allreduce(good, outs, 4, 16, F32, 1, RING, None) == vc.binding.VC_ERR_UNSUPPORTED
+    assert L.vc_allreduce(good, outs, 4, 16, F32, 7, RING, None) == vc.binding.VC_ERR_INVALID_ARG
     assert L.vc_allreduce(good, outs, 4, 16, F32, SUM, 99, None) == vc.binding.VC_ERR_INVALID_ARG
     # RHD needs a power of 2; DBT is not a ReduceScatter
     assert L.vc_allreduce(good, outs, 3, 16, F32, SUM, 2, None) == vc.binding.VC_ERR_UNSUPPORTED
     assert "power of 2" in vc.vc_last_error()
     assert L.vc_reduce_scatter(good, outs, 4, 16, F32, SUM, 3, None) == vc.binding.VC_ERR_UNSUPPORTED
-    assert L.vc_alltoall(good, outs, 4, 16, F32, RING, None) == vc.binding.VC_ERR_UNSUPPORTED
+    assert L.vc_alltoall(good, outs, 4, 16, F32, 3, None) == vc.binding.VC_ERR_UNSUPPORTED  # DBT
+    assert L.vc_allgather(good, outs, 4, 16, F32, 11, None) == vc.binding.VC_ERR_UNSUPPORTED  # MESH
     # roots
     assert L.vc_broadcast(ctypes.c_void_p(0x10000), outs, 4, 16, F32, 4, FUSED, None) == vc.binding.VC_ERR_INVALID_ARG
     assert L.vc_scatter(ctypes.c_void_p(0x10000), outs, 4, 16, F32, -1, FUSED, None) == vc.binding.VC_ERR_INVALID_ARG
