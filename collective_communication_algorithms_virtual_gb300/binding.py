@@ -18,7 +18,7 @@ VC_SUCCESS, VC_ERR_INVALID_ARG, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_NOMEM, V
 DTYPES = {"f32": 0, "bf16": 1, "i32": 2, "f16": 3}
 OPS = {"sum": 0, "max": 1, "min": 2}
 ALGOS = {"fused": 0, "ring": 1, "rhd": 2, "dbt": 3, "binomial": 4, "scatter_allgather": 5,
-         "pairwise": 6, "bruck": 7, "auto": 8, "pipe_chain": 9, "pipe_tree": 10, "mesh": 11}
+         "pairwise": 6, "bruck": 7, "auto": 8, "pipe_chain": 9, "pipe_tree": 10, "mesh": 11, "ring_hop": 12}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 COST_POLICIES = {"hbm": 0, "link": 1}
 COLLS = {"allreduce": 0, "reduce_scatter": 1, "allgather": 2, "broadcast": 3, "scatter": 4,

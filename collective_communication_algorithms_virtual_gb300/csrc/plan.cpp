@@ -137,7 +137,8 @@ class Builder {
     }
     switch (a_.algo) {
       case Algo::Fused: allreduce_fused(); break;
-      case Algo::Ring: allreduce_ring(); break;
+      case Algo::Ring:
+      case Algo::RingHop: allreduce_ring(); break;
       case Algo::RHD: allreduce_rhd(); break;
       case Algo::DBT: allreduce_dbt(); break;
       case Algo::Mesh: allreduce_mesh(); break;
@@ -186,10 +187,13 @@ class Builder {
   // slots per rank used alternately (step s writes slot s%2 while rank r+1
   // reads rank r's slot (s-1)%2).  The last ReduceScatter step writes the
   // final (rounded) chunk into the receive buffer.
+  // RingHop: the same schedule with the partial sums kept in the data type,
+  // rounded on every hop (no scratch); for fp32 / int32 it is the ring.
   void allreduce_ring() {
     const Chunks ch(a_.count, N_, es_);
+    const bool wide = bf16() && a_.algo != Algo::RingHop;  // fp32 partials in scratch
     std::vector<int64_t> slot0(N_, 0);
-    if (bf16())
+    if (wide)
       for (int r = 0; r < N_; ++r) slot0[r] = alloc(2 * ch.ce * 4);
     auto part = [&](int r, int s) { return Sc(r, slot0[r] + (s & 1) * ch.ce * 4, DT::F32); };
     for (int s = 0; s < N_ - 1; ++s) {
@@ -198,8 +202,8 @@ class Builder {
         const int c = md(r - s - 1, N_), left = md(r - 1, N_);
         const int64_t lo = ch.lo(c);
         const Operand own = S(r, lo);
-        const Operand in = s == 0 ? S(left, lo) : (bf16() ? part(left, s - 1) : R(left, lo));
-        const Operand out = s == N_ - 2 ? R(r, lo) : (bf16() ? part(r, s) : R(r, lo));
+        const Operand in = s == 0 ? S(left, lo) : (wide ? part(left, s - 1) : R(left, lo));
+        const Operand out = s == N_ - 2 ? R(r, lo) : (wide ? part(r, s) : R(r, lo));
         add(st, {own, in}, {out}, ch.len(c));
       }
     }
@@ -220,25 +224,44 @@ class Builder {
   // for bf16); a rank writes only the half it keeps while its partner reads
   // the other half, so no round overwrites what another op of it reads.
   void allreduce_rhd() {
-    const Chunks ch(a_.count, N_, es_);
-    const int L = ceil_log2(N_);
+    // N not a power of 2 (the pages require one; Rabenseifner's fold-in is the
+    // reading taken): with P the largest power of 2 below N and r = N - P,
+    // rank 2i+1 first hands its buffer to rank 2i (i < r), RHD runs on the P
+    // virtual ranks v (real rank 2v for v < r, v + r after), and rank 2i
+    // finally copies the result to 2i+1.
+    int P = 1;
+    while (P * 2 <= N_) P *= 2;
+    const int rr = N_ - P;
+    std::vector<int> real(P);
+    for (int v = 0; v < P; ++v) real[v] = v < rr ? 2 * v : v + rr;
+    const Chunks ch(a_.count, P, es_);
+    const int L = ceil_log2(P);
     std::vector<int64_t> base(N_, 0);
     if (bf16())
-      for (int r = 0; r < N_; ++r) base[r] = alloc(a_.count * 4);
+      for (int v = 0; v < P; ++v) base[real[v]] = alloc(a_.count * 4);
     auto X = [&](int r, int64_t lo) { return bf16() ? Sc(r, base[r] + lo * 4, DT::F32) : R(r, lo); };
-    std::vector<std::pair<int, int>> seg(N_, {0, N_});
+    std::vector<bool> folded(N_, false);
+    if (rr > 0) {
+      const size_t st = new_step(reduce_mode());
+      for (int i = 0; i < rr; ++i) {
+        add(st, {S(2 * i, 0), S(2 * i + 1, 0)}, {X(2 * i, 0)}, a_.count);
+        folded[2 * i] = true;
+      }
+    }
+    std::vector<std::pair<int, int>> seg(P, {0, P});
     for (int k = 0; k < L; ++k) {
       const size_t st = new_step(reduce_mode());
       auto next = seg;
-      for (int r = 0; r < N_; ++r) {
-        const int p = r ^ (1 << k);
-        const int c0 = seg[r].first, c1 = seg[r].second, h = (c1 - c0) / 2;
-        const std::pair<int, int> keep = ((r >> k) & 1) ? std::make_pair(c0 + h, c1) : std::make_pair(c0, c0 + h);
-        next[r] = keep;
+      for (int v = 0; v < P; ++v) {
+        const int w = v ^ (1 << k);
+        const int c0 = seg[v].first, c1 = seg[v].second, h = (c1 - c0) / 2;
+        const std::pair<int, int> keep = ((v >> k) & 1) ? std::make_pair(c0 + h, c1) : std::make_pair(c0, c0 + h);
+        next[v] = keep;
         const int64_t lo = ch.lo(keep.first), hi = ch.hi(keep.second - 1);
-        const Operand own = k == 0 ? S(r, lo) : X(r, lo);
-        const Operand partner = k == 0 ? S(p, lo) : X(p, lo);
-        const Operand out = k == L - 1 ? R(r, lo) : X(r, lo);
+        const int rv = real[v], rw = real[w];
+        const Operand own = (k == 0 && !folded[rv]) ? S(rv, lo) : X(rv, lo);
+        const Operand partner = (k == 0 && !folded[rw]) ? S(rw, lo) : X(rw, lo);
+        const Operand out = k == L - 1 ? R(rv, lo) : X(rv, lo);
         add(st, {own, partner}, {out}, hi - lo);
       }
       seg = next;
@@ -247,13 +270,17 @@ class Builder {
       const int d = 1 << (L - 1 - j);
       const size_t st = new_step(Mode::Copy);
       auto next = seg;
-      for (int r = 0; r < N_; ++r) {
-        const int p = r ^ d;
-        const int64_t lo = ch.lo(seg[p].first), hi = ch.hi(seg[p].second - 1);
-        copy(st, R(p, lo), R(r, lo), hi - lo);
-        next[r] = {std::min(seg[r].first, seg[p].first), std::max(seg[r].second, seg[p].second)};
+      for (int v = 0; v < P; ++v) {
+        const int w = v ^ d;
+        const int64_t lo = ch.lo(seg[w].first), hi = ch.hi(seg[w].second - 1);
+        copy(st, R(real[w], lo), R(real[v], lo), hi - lo);
+        next[v] = {std::min(seg[v].first, seg[w].first), std::max(seg[v].second, seg[w].second)};
       }
       seg = next;
+    }
+    if (rr > 0) {
+      const size_t st = new_step(Mode::Copy);
+      for (int i = 0; i < rr; ++i) copy(st, R(2 * i, 0), R(2 * i + 1, 0), a_.count);
     }
   }
 
@@ -733,7 +760,7 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   switch (a.coll) {
     case Coll::AllReduce:
       ok = a.algo == Algo::Fused || a.algo == Algo::Ring || a.algo == Algo::RHD || a.algo == Algo::DBT ||
-           a.algo == Algo::Mesh;
+           a.algo == Algo::Mesh || a.algo == Algo::RingHop;
       break;
     case Coll::ReduceScatter:
     case Coll::AllGather: ok = a.algo == Algo::Fused || a.algo == Algo::Ring; break;
@@ -749,8 +776,6 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   }
   if (a.coll == Coll::Broadcast && (a.algo == Algo::PipeChain || a.algo == Algo::PipeTree)) ok = true;
   if (!ok) return bad(PlanStatus::Unsupported, "algorithm not defined for this collective");
-  if (a.coll == Coll::AllReduce && a.algo == Algo::RHD && !is_pow2(a.nranks))
-    return bad(PlanStatus::Unsupported, "recursive halving-doubling needs nranks a power of 2");
   Builder b(a);
   b.build();
   *out = b.take();
@@ -823,7 +848,8 @@ PlanStatus select_algo(const PlanArgs& a, const CostModel& cm, Algo* out, double
   switch (a.coll) {
     case Coll::AllReduce:
       cand = link ? std::vector<Algo>{Algo::Ring, Algo::RHD, Algo::DBT}
-                  : std::vector<Algo>{Algo::Fused, Algo::Ring, Algo::RHD, Algo::DBT, Algo::Mesh};
+                  : std::vector<Algo>{Algo::Fused, Algo::Ring, Algo::RHD, Algo::DBT, Algo::Mesh, Algo::RingHop};
+      if (link && !is_pow2(a.nranks)) cand.erase(cand.begin() + 1);  // the page's RHD formula needs 2^k
       break;
     case Coll::ReduceScatter:
     case Coll::AllGather:

@@ -23,7 +23,7 @@ enum class Coll : int {
 };
 enum class Algo : int {
   Fused = 0, Ring = 1, RHD = 2, DBT = 3, Binomial = 4, ScatterAllGather = 5, Pairwise = 6, Bruck = 7,
-  PipeChain = 9, PipeTree = 10, Mesh = 11
+  PipeChain = 9, PipeTree = 10, Mesh = 11, RingHop = 12
 };
 
 inline int esize(DT t) { return (t == DT::BF16 || t == DT::F16) ? 2 : 4; }

@@ -753,7 +753,7 @@ const char* coll_name(Coll c) {
 }
 const char* algo_name(Algo a) {
   static const char* n[] = {"fused", "ring", "rhd", "dbt", "binomial", "scatter_allgather", "pairwise", "bruck",
-                            "auto", "pipe_chain", "pipe_tree", "mesh"};
+                            "auto", "pipe_chain", "pipe_tree", "mesh", "ring_hop"};
   return n[static_cast<int>(a)];
 }
 
@@ -824,7 +824,7 @@ vc_status_t to_algo(vc_algo_t a, Algo* out, bool* is_auto = nullptr) {
     *out = Algo::Fused;
     return VC_SUCCESS;
   }
-  if (v < 0 || v > 11 || v == VC_ALGO_AUTO) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
+  if (v < 0 || v > 12 || v == VC_ALGO_AUTO) return fail(VC_ERR_INVALID_ARG, "unknown algorithm");
   if (is_auto) *is_auto = false;
   *out = static_cast<Algo>(v);
   return VC_SUCCESS;

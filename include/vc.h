@@ -90,7 +90,8 @@ typedef enum {
   VC_ALGO_AUTO = 8,              /* any collective: cheapest under the cost model      */
   VC_ALGO_PIPE_CHAIN = 9,        /* Broadcast, message cut into chunks along a chain   */
   VC_ALGO_PIPE_TREE = 10,        /* Broadcast, chunks down the binomial tree           */
-  VC_ALGO_MESH = 11              /* AllReduce: root 0 folds every rank, then sends     */
+  VC_ALGO_MESH = 11,             /* AllReduce: root 0 folds every rank, then sends     */
+  VC_ALGO_RING_HOP = 12          /* AllReduce: ring, partials rounded on every hop     */
 } vc_algo_t;
 
 typedef enum {
@@ -113,8 +114,12 @@ typedef enum {
  *   send[r], recv[r]: `count` elements each.  send[r] == recv[r] (in place)
  *   is allowed, as hccl_allreduce allows sendbuf == recvbuf.
  *   algo: FUSED (rank-order sum in one pass), RING (ReduceScatter + AllGather
- *   in 2(N-1) steps), RHD (2 log2 N rounds; VC_ERR_UNSUPPORTED unless nranks
- *   is a power of 2), DBT (two mirrored heap trees, 2 floor(log2 N) levels),
+ *   in 2(N-1) steps; 16-bit data keeps fp32 partial sums in library scratch),
+ *   RING_HOP (the same ring with the partial sums kept in the data type and
+ *   rounded on every hop; equals RING for fp32 and int32), RHD (2 log2 N
+ *   rounds for N a power of 2; otherwise the first 2(N-P) ranks, P the
+ *   largest power of 2 below N, fold in pairwise before and get the result
+ *   back after), DBT (two mirrored heap trees, 2 floor(log2 N) levels),
  *   MESH (hccl article, section "Mesh算法：全连接广播": rank 0 folds the other
  *   ranks in rank order, one per step, then sends the result to each, one
  *   per step; 2(N-1) steps).

@@ -13,10 +13,13 @@ AllReduce, element e (chunks cut by ``oracle.partition``):
   of the [hccl article]'s Mesh root (section "Mesh算法：全连接广播").
 * ring:   chunk c = chunk of e; ((x_c + x_{c+1}) + x_{c+2}) + ... + x_{c+N-1},
   indices mod N ([hccl article] section "Ring算法": at step 0 rank c sends
-  chunk c, each later hop adds its own copy).
+  chunk c, each later hop adds its own copy).  ring_hop: the same tree with
+  every partial sum rounded to the data type.
 * rhd:    balanced tree over adjacent rank pairs, ((x0+x1)+(x2+x3)) + ...
   ([Latency-formula page] section "Recursive Halving-Doubling": round k pairs
-  ranks at distance 2**k, starting at distance 1).
+  ranks at distance 2**k, starting at distance 1); for N not a power of 2
+  the leaves are the folded pairs (x_{2i} + x_{2i+1}), i < N - P, and then
+  the ranks 2r .. N-1.
 * dbt:    S(i) = (x_i + S(2i+1)) + S(2i+2) on the heap of the tree holding e
   (tree A: rank i; tree B: rank N-1-i) ([hccl article] section "Tree算法").
 
@@ -36,7 +39,7 @@ import numpy as np
 
 from .numerics import ESIZE, combine, narrow, widen
 from .partition import chunk_of, chunk_range
-from .schedules import dbt_trees
+from .schedules import dbt_trees, rhd_virtual_ranks
 
 
 def left_fold(ranks):
@@ -48,7 +51,7 @@ def left_fold(ranks):
 
 def balanced_pairs(ranks):
     if len(ranks) == 1:
-        return ranks[0]
+        return ranks[0]  # a rank, or an already built subtree
     mid = len(ranks) // 2
     return (balanced_pairs(ranks[:mid]), balanced_pairs(ranks[mid:]))
 
@@ -66,11 +69,13 @@ def allreduce_tree(algo: str, N: int, count: int, dtype: str, e: int):
     esz = ESIZE[dtype]
     if algo in ("fused", "mesh"):
         return left_fold(list(range(N)))
-    if algo == "ring":
+    if algo in ("ring", "ring_hop"):
         c = chunk_of(e, count, N, esz)
         return left_fold([(c + j) % N for j in range(N)])
     if algo == "rhd":
-        return balanced_pairs(list(range(N)))
+        P, r, real = rhd_virtual_ranks(N)
+        leaves = [(2 * v, 2 * v + 1) if v < r else real[v] for v in range(P)]
+        return balanced_pairs(leaves)
     if algo == "dbt":
         for _, rank_of, (lo, hi) in dbt_trees(N, count, esz):
             if lo <= e < hi:
@@ -88,17 +93,20 @@ def reduce_scatter_tree(algo: str, N: int, rc: int, e: int):
     raise ValueError(algo)
 
 
-def evaluate(tree, cols: dict, op: str = "sum"):
-    """Evaluate a tree on lane-type columns (one array per rank)."""
+def evaluate(tree, cols: dict, op: str = "sum", round_to: str | None = None):
+    """Evaluate a tree on lane-type columns (one array per rank).  With
+    ``round_to`` every inner node's value is rounded to that storage type (a
+    schedule that stores its partial results in the data type)."""
     if isinstance(tree, int):
         return cols[tree]
     a, b = tree
-    return combine(evaluate(a, cols, op), evaluate(b, cols, op), op)
+    v = combine(evaluate(a, cols, op, round_to), evaluate(b, cols, op, round_to), op)
+    return widen(narrow(v, round_to), round_to) if round_to else v
 
 
 def _group_key_allreduce(algo, N, count, dtype, e):
     esz = ESIZE[dtype]
-    if algo == "ring":
+    if algo in ("ring", "ring_hop"):
         return chunk_of(e, count, N, esz)
     if algo == "dbt":
         return 0 if e < chunk_range(0, count, 2, esz)[1] else 1
@@ -118,7 +126,7 @@ def allreduce_at(values_at, algo: str, count: int, dtype: str, idx, op: str = "s
         sel = np.nonzero(keys == key)[0]
         tree = allreduce_tree(algo, N, count, dtype, int(idx[sel[0]]))
         cols = {r: widen(np.asarray(values_at[r])[sel], dtype) for r in range(N)}
-        res = narrow(evaluate(tree, cols, op), dtype)
+        res = narrow(evaluate(tree, cols, op, dtype if algo == "ring_hop" else None), dtype)
         if out is None:
             out = np.empty(len(idx), dtype=res.dtype)
         out[sel] = res

@@ -34,7 +34,7 @@ from .partition import chunk_range
 from .translog import TransferLog
 
 ALGOS = {
-    "allreduce": ("fused", "ring", "rhd", "dbt", "mesh"),
+    "allreduce": ("fused", "ring", "rhd", "dbt", "mesh", "ring_hop"),
     "reduce_scatter": ("fused", "ring"),
     "allgather": ("fused", "ring"),
     "broadcast": ("fused", "binomial", "scatter_allgather"),
@@ -160,6 +160,8 @@ def allreduce(inputs, algo: str, dtype: str, inplace: bool = False, op: str = "s
         return _allreduce_dbt(inputs, dtype, op)
     if algo == "mesh":
         return _allreduce_mesh(inputs, dtype, op)
+    if algo == "ring_hop":
+        return _allreduce_ring(inputs, dtype, op, round_each_hop=True)
     raise Unsupported(f"allreduce/{algo}")
 
 
@@ -223,7 +225,7 @@ def _allreduce_mesh(inputs, dtype, op="sum"):
     return Result([narrow(a, dtype) for a in acc], log, bm.total)
 
 
-def _allreduce_ring(inputs, dtype, op="sum"):
+def _allreduce_ring(inputs, dtype, op="sum", round_each_hop=False):
     """Ring AllReduce = Ring ReduceScatter (N-1 steps) then Ring AllGather
     (N-1 steps) ([hccl article] section "Ring算法：环形流水线传输";
     [Latency-formula page] eqs. model-algo-ring-rs, -ag, -ar).
@@ -240,8 +242,12 @@ def _allreduce_ring(inputs, dtype, op="sum"):
     chunks not yet received and never deliver chunk r - 1.  The reading taken
     is the forwarding the article's prose and the formula page describe.)
 
-    bf16: partial sums travel and are stored as fp32; the last ReduceScatter
-    step writes the rounded result, which the AllGather copies."""
+    bf16 / fp16: partial sums travel and are stored as fp32; the last
+    ReduceScatter step writes the rounded result, which the AllGather copies.
+    ``round_each_hop`` (algorithm "ring_hop"): every hop instead rounds the
+    partial sum to the data type and stores it there, as a ring that sends
+    its partials in the data type would -- half the partial traffic of
+    16-bit data, one rounding per hop; for fp32 and int32 nothing changes."""
     N, count = len(inputs), len(inputs[0])
     e = ESIZE[dtype]
     bm = _Bytes(dtype)
@@ -249,6 +255,18 @@ def _allreduce_ring(inputs, dtype, op="sum"):
     if N == 1:
         return Result(_self_copy_result(inputs, dtype, bm), log, bm.total)
     acc = [widen(x, dtype) for x in inputs]
+    e_part = bm.e_in if round_each_hop else bm.e_acc
+
+    def reduce_and_round(buf, lo, hi):
+        plain = _reduce_into(buf, lo, hi, op)
+        if not round_each_hop:
+            return plain
+
+        def f(p):
+            plain(p)
+            buf[lo:hi] = widen(narrow(buf[lo:hi], dtype), dtype)
+        return f
+
     step = 0
     for s in range(N - 1):
         msgs = []
@@ -256,11 +274,11 @@ def _allreduce_ring(inputs, dtype, op="sum"):
             c = (r - s) % N
             lo, hi = chunk_range(c, count, N, e)
             dst = (r + 1) % N
-            wire = bm.e_in if s == 0 else bm.e_acc
+            wire = bm.e_in if s == 0 else e_part
             msgs.append(_Msg(src=r, dst=dst, n=hi - lo, reduce=True, esize=wire,
-                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[dst], lo, hi, op),
+                             payload=acc[r][lo:hi].copy(), deliver=reduce_and_round(acc[dst], lo, hi),
                              phase="rs", src_off=lo, dst_off=lo, chunks=(c,)))
-            bm.rw(hi - lo, bm.e_in, wire, bm.e_out if s == N - 2 else bm.e_acc)
+            bm.rw(hi - lo, bm.e_in, wire, bm.e_out if s == N - 2 else e_part)
         _run_step(log, step, msgs)
         step += 1
     for s in range(N - 1):
@@ -278,58 +296,82 @@ def _allreduce_ring(inputs, dtype, op="sum"):
     return Result([narrow(a, dtype) for a in acc], log, bm.total)
 
 
+def rhd_virtual_ranks(N: int):
+    """(P, r, real): RHD runs on P = 2**floor(log2 N) virtual ranks; the first
+    2r real ranks (r = N - P) fold in pairwise beforehand, virtual rank v < r
+    being real rank 2v and v >= r real rank v + r."""
+    P = 1 << (N.bit_length() - 1)
+    r = N - P
+    return P, r, [2 * v if v < r else v + r for v in range(P)]
+
+
 def _allreduce_rhd(inputs, dtype, op="sum"):
-    """Recursive Halving-Doubling (Rabenseifner) AllReduce, N a power of 2
-    ([Latency-formula page] section "Recursive Halving-Doubling", eqs.
-    model-algo-rhd-rs, -ag, -ar).
+    """Recursive Halving-Doubling (Rabenseifner) AllReduce ([Latency-formula
+    page] section "Recursive Halving-Doubling", eqs. model-algo-rhd-rs, -ag,
+    -ar, which ask for N a power of 2).
 
-    Halving round k = 0 .. log2(N)-1: rank r pairs with r XOR 2**k; both hold
-    the same segment (a run of chunks); the rank whose bit k is 0 keeps the
-    lower half, the other the upper half; each sends the half it gives up and
-    adds the half it keeps.  Round k moves M / 2**(k+1).  Afterwards rank r
-    holds chunk bitreverse(r) fully reduced; every element was summed as the
-    balanced tree over adjacent rank pairs, ((x0+x1)+(x2+x3)) + ....
+    Halving round k = 0 .. log2(P)-1: virtual rank v pairs with v XOR 2**k;
+    both hold the same segment (a run of chunks); the one whose bit k is 0
+    keeps the lower half, the other the upper half; each sends the half it
+    gives up and adds the half it keeps.  Round k moves M / 2**(k+1).
+    Afterwards rank v holds chunk bitreverse(v) fully reduced; every element
+    was summed as the balanced tree over adjacent rank pairs,
+    ((x0+x1)+(x2+x3)) + ....  Doubling: the reverse process; round j pairs v
+    with v XOR 2**(log2P-1-j), each sends its whole segment (M * 2**j / P) and
+    stores the partner's.  Which half is kept and the order of the doubling
+    distances are readings; the reduced values do not depend on them.
 
-    Doubling: the reverse process; round j pairs r with r XOR 2**(log2N-1-j),
-    each sends its whole segment (M * 2**j / N) and stores the partner's.
-    Which half is kept and the order of the doubling distances are readings;
-    the reduced values do not depend on them."""
+    N not a power of 2 (the page leaves it out; the reading taken is
+    Rabenseifner's own fold-in): with P the largest power of 2 below N and
+    r = N - P, odd rank 2i+1 first hands its whole buffer to rank 2i (i < r),
+    which adds it; RHD runs on the P remaining ranks; rank 2i finally hands
+    the whole result back to 2i+1.  For N a power of 2 there is no such step."""
     N, count = len(inputs), len(inputs[0])
-    if not _is_pow2(N):
-        raise Unsupported("recursive halving-doubling needs N a power of 2")
     e = ESIZE[dtype]
     bm = _Bytes(dtype)
     log = TransferLog()
     if N == 1:
         return Result(_self_copy_result(inputs, dtype, bm), log, bm.total)
-    L = N.bit_length() - 1
+    P, rr, real = rhd_virtual_ranks(N)
+    L = P.bit_length() - 1
     acc = [widen(x, dtype) for x in inputs]
-    seg = [(0, N)] * N  # chunk index range [c0, c1) each rank is responsible for
+    folded = set()  # real ranks holding a partial sum before the halving
+    step = 0
+    if rr:
+        msgs = []
+        for i in range(rr):
+            msgs.append(_Msg(src=2 * i + 1, dst=2 * i, n=count, reduce=True, esize=bm.e_in,
+                             payload=acc[2 * i + 1].copy(), deliver=_reduce_into(acc[2 * i], 0, count, op),
+                             phase="fold", src_off=0, dst_off=0))
+            bm.rw(count, bm.e_in, bm.e_in, bm.e_acc)
+            folded.add(2 * i)
+        _run_step(log, step, msgs)
+        step += 1
+    seg = [(0, P)] * P  # chunk index range [c0, c1) each virtual rank is responsible for
 
     def elems(c0, c1):
-        return chunk_range(c0, count, N, e)[0], chunk_range(c1 - 1, count, N, e)[1]
+        return chunk_range(c0, count, P, e)[0], chunk_range(c1 - 1, count, P, e)[1]
 
-    step = 0
     for k in range(L):
         msgs = []
         new_seg = list(seg)
-        for r in range(N):
-            p = r ^ (1 << k)
-            c0, c1 = seg[r]
+        for v in range(P):
+            w = v ^ (1 << k)
+            c0, c1 = seg[v]
             h = (c1 - c0) // 2
-            if (r >> k) & 1 == 0:
+            if (v >> k) & 1 == 0:
                 keep, give = (c0, c0 + h), (c0 + h, c1)
             else:
                 keep, give = (c0 + h, c1), (c0, c0 + h)
-            new_seg[r] = keep
+            new_seg[v] = keep
             lo, hi = elems(*give)
-            wire = bm.e_in if k == 0 else bm.e_acc
-            msgs.append(_Msg(src=r, dst=p, n=hi - lo, reduce=True, esize=wire,
-                             payload=acc[r][lo:hi].copy(), deliver=_reduce_into(acc[p], lo, hi, op),
+            wire = bm.e_acc if (k > 0 or real[v] in folded) else bm.e_in
+            msgs.append(_Msg(src=real[v], dst=real[w], n=hi - lo, reduce=True, esize=wire,
+                             payload=acc[real[v]][lo:hi].copy(), deliver=_reduce_into(acc[real[w]], lo, hi, op),
                              phase="halving", src_off=lo, dst_off=lo,
                              chunks=tuple(range(*give))))
-            bm.rw(hi - lo, bm.e_in if k == 0 else bm.e_acc, wire,
-                  bm.e_out if k == L - 1 else bm.e_acc)
+            own = bm.e_acc if (k > 0 or real[w] in folded) else bm.e_in
+            bm.rw(hi - lo, own, wire, bm.e_out if k == L - 1 else bm.e_acc)
         _run_step(log, step, msgs)
         seg = new_seg
         step += 1
@@ -337,20 +379,28 @@ def _allreduce_rhd(inputs, dtype, op="sum"):
         d = 1 << (L - 1 - j)
         msgs = []
         new_seg = list(seg)
-        for r in range(N):
-            p = r ^ d
-            c0, c1 = seg[r]
+        for v in range(P):
+            w = v ^ d
+            c0, c1 = seg[v]
             lo, hi = elems(c0, c1)
-            msgs.append(_Msg(src=r, dst=p, n=hi - lo, reduce=False, esize=bm.e_out,
-                             payload=acc[r][lo:hi].copy(), deliver=_store_into(acc[p], lo, hi),
+            msgs.append(_Msg(src=real[v], dst=real[w], n=hi - lo, reduce=False, esize=bm.e_out,
+                             payload=acc[real[v]][lo:hi].copy(), deliver=_store_into(acc[real[w]], lo, hi),
                              phase="doubling", src_off=lo, dst_off=lo,
                              chunks=tuple(range(c0, c1))))
             bm.rw(hi - lo, bm.e_out, bm.e_out)
-            pc0, pc1 = seg[p]
-            new_seg[r] = (min(c0, pc0), max(c1, pc1))
+            pc0, pc1 = seg[w]
+            new_seg[v] = (min(c0, pc0), max(c1, pc1))
         _run_step(log, step, msgs)
         seg = new_seg
         step += 1
+    if rr:
+        msgs = []
+        for i in range(rr):
+            msgs.append(_Msg(src=2 * i, dst=2 * i + 1, n=count, reduce=False, esize=bm.e_out,
+                             payload=acc[2 * i].copy(), deliver=_store_into(acc[2 * i + 1], 0, count),
+                             phase="unfold", src_off=0, dst_off=0))
+            bm.rw(count, bm.e_out, bm.e_out)
+        _run_step(log, step, msgs)
     return Result([narrow(a, dtype) for a in acc], log, bm.total)
 
 

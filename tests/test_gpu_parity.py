@@ -70,10 +70,6 @@ def test_allreduce_matches_oracle(N, dtype):
     for count in AR_COUNTS:
         xs = _inputs(dtype, 1000 + N + count, N, count)
         for algo in ALGOS_AR:
-            if algo == "rhd" and N & (N - 1):
-                with pytest.raises(vc.VCError):
-                    _run_allreduce(xs, algo, dtype)
-                continue
             want = schedules.allreduce(xs, algo, dtype).outputs
             got = _run_allreduce(xs, algo, dtype)
             for r in range(N):
@@ -86,8 +82,6 @@ def test_allreduce_inplace_and_misaligned(N, dtype):
     count = 4097 * 3
     xs = _inputs(dtype, 77 + N, N, count)
     for algo in ALGOS_AR:
-        if algo == "rhd" and N & (N - 1):
-            continue
         want = schedules.allreduce(xs, algo, dtype).outputs
         for shift, inplace in ((0, True), (1, False), (1, True), (3, False)):
             got = _run_allreduce(xs, algo, dtype, shift=shift, inplace=inplace)
@@ -220,7 +214,7 @@ def test_errors_leave_outputs_untouched():
     xs = [torch.ones(64, device="cuda") for _ in range(N)]
     ys = [torch.zeros(64, device="cuda") for _ in range(N)]
     with pytest.raises(vc.VCError) as e:
-        vc.vc_allreduce(xs[:3], ys[:3], algo="rhd")
+        vc.vc_reduce_scatter(xs, [y[:16] for y in ys], algo="dbt")
     assert e.value.status == 2
     with pytest.raises(vc.VCError) as e:
         vc.vc_allreduce(xs, ys, algo="ring", op=7)

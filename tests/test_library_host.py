@@ -81,9 +81,9 @@ def test_invalid_arguments_rejected_on_host():
     assert L.vc_allreduce(good, outs, 4, 16, 7, SUM, RING, None) == vc.binding.VC_ERR_INVALID_ARG
     assert L.vc_allreduce(good, outs, 4, 16, F32, 7, RING, None) == vc.binding.VC_ERR_INVALID_ARG
     assert L.vc_allreduce(good, outs, 4, 16, F32, SUM, 99, None) == vc.binding.VC_ERR_INVALID_ARG
-    # RHD needs a power of 2; DBT is not a ReduceScatter
-    assert L.vc_allreduce(good, outs, 3, 16, F32, SUM, 2, None) == vc.binding.VC_ERR_UNSUPPORTED
-    assert "power of 2" in vc.vc_last_error()
+    # RHD and DBT are not ReduceScatters
+    assert L.vc_reduce_scatter(good, outs, 4, 16, F32, SUM, 2, None) == vc.binding.VC_ERR_UNSUPPORTED
+    assert "not defined" in vc.vc_last_error()
     assert L.vc_reduce_scatter(good, outs, 4, 16, F32, SUM, 3, None) == vc.binding.VC_ERR_UNSUPPORTED
     assert L.vc_alltoall(good, outs, 4, 16, F32, 3, None) == vc.binding.VC_ERR_UNSUPPORTED  # DBT
     assert L.vc_allgather(good, outs, 4, 16, F32, 11, None) == vc.binding.VC_ERR_UNSUPPORTED  # MESH
@@ -132,8 +132,6 @@ AR_CASES = [(N, c) for N in (1, 2, 3, 4, 5, 8) for c in (0, 1, 13, 64, 203)] + [
 def test_allreduce_plans_replay_to_oracle(N, count, dtype):
     xs = _inputs(dtype, 100 + N, N, count)
     for algo in schedules.ALGOS["allreduce"]:
-        if algo == "rhd" and N & (N - 1):
-            continue
         res = schedules.allreduce(xs, algo, dtype)
         for inplace in (False, True):
             plan, scratch = get_plan("allreduce", algo, N, count, dtype, inplace=inplace and N == 1)
@@ -241,8 +239,6 @@ def test_plan_bytes_equal_oracle_algorithmic_bytes(dtype):
         count = N * 1000 + 8
         xs = _inputs(dtype, 3, N, count)
         for algo in schedules.ALGOS["allreduce"]:
-            if algo == "rhd" and N & (N - 1):
-                continue
             assert plan_bytes("allreduce", algo, N, count) == schedules.allreduce(xs, algo, dtype).hbm_bytes
         rc = 100
         xr = _inputs(dtype, 4, N, N * rc)

@@ -42,8 +42,6 @@ def test_max_min_equal_library_max_min(N, dtype):
         want = f(lanes, axis=0)
         want = numerics.narrow(want.view(np.uint32) if dtype == "i32" else want, dtype)
         for algo in schedules.ALGOS["allreduce"]:
-            if algo == "rhd" and N & (N - 1):
-                continue
             out = schedules.allreduce(xs, algo, dtype, op=op).outputs
             for o in out:
                 assert numerics.same_bits(o, want), (op, algo, N, dtype)
@@ -129,8 +127,6 @@ def test_op_and_fp16_plans_replay(N, op, dtype):
     xs = _inputs(dtype, 20 + N, N, count)
     es = ESZ[DT[dtype]]
     for algo in schedules.ALGOS["allreduce"]:
-        if algo == "rhd" and N & (N - 1):
-            continue
         res = schedules.allreduce(xs, algo, dtype, op=op)
         plan, scratch = get_plan("allreduce", algo, N, count, dtype, op=op)
         mem = Memory(xs, [count * es] * N, scratch)
@@ -154,3 +150,19 @@ def test_op_and_fp16_plans_replay(N, op, dtype):
         mem = Memory(xs, [count * es if r == N // 2 else 0 for r in range(N)], scratch)
         run_plan(plan, mem)
         assert numerics.same_bits(mem.recv[N // 2].view(NPT[DT[dtype]]), res.outputs[0]), (algo, op, dtype)
+
+
+def test_rhd_fold_in_for_n_not_a_power_of_2():
+    """N = 6: P = 4, r = 2.  Step 0: 1->0 and 3->2 fold in (whole buffer);
+    then halving / doubling among real ranks 0, 2, 4, 5 (2 log2 4 steps);
+    last step 0->1 and 2->3 hand the result back: 2 + 2 log2 P steps."""
+    N, count = 6, 64
+    res = schedules.allreduce(rank_buffers("small_ints_f32", 7, N, count), "rhd", "f32")
+    table = res.log.table()
+    assert [t for t in table if t[0] == 0] == [(0, 1, 0), (0, 3, 2)]
+    assert [t for t in table if t[0] == 5] == [(5, 0, 1), (5, 2, 3)]
+    mid = {t[1] for t in table if 1 <= t[0] <= 4} | {t[2] for t in table if 1 <= t[0] <= 4}
+    assert mid == {0, 2, 4, 5}
+    assert res.nsteps == 2 + 2 * 2
+    for o in res.outputs:
+        assert numerics.same_bits(o, res.outputs[0])
