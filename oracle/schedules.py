@@ -150,6 +150,10 @@ def allreduce(inputs, algo: str, dtype: str, inplace: bool = False, op: str = "s
     ([Latency-formula page], section "Ring AllReduce"; [hccl article] section
     "集合通信vs点对点" -- every rank ends with the same reduced data)."""
     N, count = _check_same(inputs, dtype)
+    if algo not in ALGOS["allreduce"]:
+        raise Unsupported(f"allreduce/{algo}")
+    if N == 1 and inplace:  # one rank, in place: the result is already there
+        return Result([np.array(inputs[0], copy=True)], TransferLog(), 0)
     if algo == "fused":
         return _allreduce_fused(inputs, dtype, op)
     if algo == "ring":
@@ -605,7 +609,9 @@ def broadcast(root_input, N: int, root: int, algo: str, dtype: str, inplace: boo
             if r != root:
                 log.add(step=0, phase="fused", src=root, dst=r, n=count, reduce=False,
                         esize=e, src_off=0, dst_off=0)
-        bm.rw(count, bm.e_in, *([bm.e_out] * (N - 1 if inplace else N)))
+        ndst = N - 1 if inplace else N
+        if ndst:  # read once, written to every destination (none: nothing moves)
+            bm.rw(count, bm.e_in, *([bm.e_out] * ndst))
         return Result(out, log, bm.total)
     if algo == "binomial":
         return _broadcast_binomial(root_input, N, root, dtype, inplace)

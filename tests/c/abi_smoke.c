@@ -1,0 +1,32 @@
+/* Plain C99 use of include/vc.h: the header compiles as C, the library links,
+ * and the host-only entry points answer without a GPU. */
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "vc.h"
+
+int main(void) {
+  if (strcmp(vc_status_string(VC_ERR_UNSUPPORTED), "VC_ERR_UNSUPPORTED") != 0) return 1;
+  if (vc_busbw_factor(VC_COLL_ALLREDUCE, 8) != 1.75) return 2;
+  size_t n = 0, scratch = 0;
+  int steps = 0;
+  /* Ring AllReduce over 8 ranks: 14 steps, no scratch for fp32 */
+  if (vc_plan_describe(VC_COLL_ALLREDUCE, VC_ALGO_RING, 8, 1 << 20, VC_FLOAT32, VC_SUM, 0, 0, 0, NULL, 0, &n,
+                       &scratch, &steps) != VC_SUCCESS)
+    return 3;
+  if (steps != 14 || scratch != 0 || n == 0) return 4;
+  vc_plan_entry_t* e = (vc_plan_entry_t*)malloc(n * sizeof(vc_plan_entry_t));
+  if (vc_plan_describe(VC_COLL_ALLREDUCE, VC_ALGO_RING, 8, 1 << 20, VC_FLOAT32, VC_SUM, 0, 0, 0, e, n, &n,
+                       &scratch, &steps) != VC_SUCCESS)
+    return 5;
+  if (e[0].step != 0 || e[0].reduce != 1) return 6;
+  free(e);
+  /* bad arguments are refused before any CUDA call */
+  if (vc_allreduce(NULL, NULL, 8, 16, VC_FLOAT32, VC_SUM, VC_ALGO_RING, NULL) != VC_ERR_INVALID_ARG) return 7;
+  vc_algo_t a;
+  double t = 0;
+  if (vc_select_algo(VC_COLL_ALLREDUCE, 8, 1 << 20, VC_FLOAT32, 0, &a, &t) != VC_SUCCESS || a != VC_ALGO_FUSED) return 8;
+  printf("ok %d\n", vc_version());
+  return 0;
+}
