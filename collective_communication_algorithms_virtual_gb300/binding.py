@@ -44,7 +44,7 @@ KERNEL_OPS = {0: "sum", 1: "max", 2: "min"}
 def kernel_name(code: int) -> str:
     mode = KERNEL_MODES[code & 7]
     name = mode if mode == "copy" else f"{KERNEL_OPS[(code >> 3) & 3]}_{mode}"
-    return name + ("_large" if code & 32 else "")
+    return name + ("_large" if code & 32 else "") + ("_batched" if code & 64 else "")
 
 
 class PlanEntry(ctypes.Structure):

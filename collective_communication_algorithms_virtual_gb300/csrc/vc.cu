@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -101,25 +102,45 @@ struct __align__(16) OpDesc {
   uint8_t ns, nd;
   uint8_t vec;      // 1: vector path
   uint8_t esz;      // copy: element size in bytes
+  uint8_t upt;      // vector path: groups per thread in one tile (1, 2 or 4)
 };
 
 template <int OPS, int PTRS>
 struct __align__(16) LaunchParams {
-  uint32_t nops;
-  uint32_t ntiles;
-  uint32_t pad[2];
+  uint32_t nops;    // operations in use
+  uint32_t ntiles;  // tiles of the launch
+  uint32_t nptrs;   // pointers in use
+  uint32_t pad;
   OpDesc op[OPS];
   const void* ptr[PTRS];
+  static constexpr uint32_t kHeaderBytes = 16;
+  static constexpr uint32_t kPtrOffset = 16 + OPS * sizeof(OpDesc);
 };
 using SmallParams = LaunchParams<16, 64>;
 using LargeParams = LaunchParams<128, 512>;
+static_assert(sizeof(OpDesc) % 16 == 0, "parameter blocks are copied in 16-byte words");
+static_assert(offsetof(SmallParams, ptr) == SmallParams::kPtrOffset, "pointer table offset");
+static_assert(offsetof(LargeParams, ptr) == LargeParams::kPtrOffset, "pointer table offset");
 
-// -- memory access helpers (sources are never written within a launch) -------
+// -- memory access --------------------------------------------------------------
+// Per-step launches (COH = false): the sources of a launch are never written
+// during it, so loads take the non-coherent path and skip L1; stores are
+// streaming (evict-first in L2).  One-launch plans (COH = true) read in a step
+// what other blocks of the cluster wrote in an earlier one: loads go to L2
+// (.cg, never a stale L1 line) after the step barrier, stores are plain.
 __device__ __forceinline__ uint4 ld16(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld16_cg(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
   return v;
 }
 // Streaming store (evict-first in L2): measured 2-3% faster than a plain
@@ -129,6 +150,21 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ void st16_wb(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+template <bool COH>
+__device__ __forceinline__ uint4 ldv(const void* p) {
+  if constexpr (COH) return ld16_cg(p);
+  else return ld16(p);
+}
+template <bool COH>
+__device__ __forceinline__ void stv(void* p, uint4 v) {
+  if constexpr (COH) st16_wb(p, v);
+  else st16(p, v);
+}
+
 template <int OP>
 __device__ __forceinline__ float cmb(float a, float b) {
   if constexpr (OP == kSum) return __fadd_rn(a, b);
@@ -183,26 +219,38 @@ __device__ __forceinline__ void widen8(uint4 v, float* f) {
 }
 
 // -- vector path -------------------------------------------------------------
+// A tile is the groups [gbeg, gend) of one run of one operation; thread i
+// takes groups gbeg + i, gbeg + i + kThreads, ...  `ptr` is the operation's
+// pointer table (sources, then destinations): an array of addresses, or a
+// table that forms them from buffer bases.
+//
 // Fan-out copies (one source, several destinations: fused AllGather and
-// Broadcast): the tile is loaded once into shared memory and thread 0 issues
-// one bulk asynchronous store per destination (cp.async.bulk, the TMA engine),
+// Broadcast): the tile is loaded into shared memory and thread 0 issues one
+// bulk asynchronous store per destination (cp.async.bulk, the TMA engine),
 // which writes it out in 16 KB bursts.  Measured 3-4.5% faster than eight
 // 128-bit stores per thread on the fused Broadcast and AllGather at 8 x 256
-// MiB; single-destination copies keep the plain path (no gain there).  Before
-// the buffer is refilled the previous tile's bulk stores must have read it
-// (wait_group.read); the kernel waits for their completion before it exits.
-__device__ __forceinline__ void tile_copy_fanout(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+// MiB; single-destination copies keep the plain path (no gain there).  The
+// next tile's loads are issued before waiting until the previous tile's bulk
+// stores have read the buffer (wait_group.read), so the two overlap; the
+// kernel waits for the stores' completion before it exits.
+template <class PT>
+__device__ __forceinline__ void tile_copy_fanout(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
+                                                 int64_t gend) {
   __shared__ alignas(128) uint4 stage[kTileGroups];
-  const int64_t gbeg = tr * kTileGroups;
-  const int64_t gend = gbeg + kTileGroups < o.groups ? gbeg + kTileGroups : o.groups;
   const int ng = static_cast<int>(gend - gbeg);
-  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  __syncthreads();
   const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
+  uint4 v[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int64_t g = gbeg + u * kThreads + threadIdx.x;
-    if (g < gend) stage[g - gbeg] = ld16(s + g * 16);
+    if (g < gend) v[u] = ld16(s + g * 16);
+  }
+  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int64_t g = gbeg + u * kThreads + threadIdx.x;
+    if (g < gend) stage[g - gbeg] = v[u];
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make the tile visible to the bulk copies
   __syncthreads();
@@ -217,70 +265,92 @@ __device__ __forceinline__ void tile_copy_fanout(const OpDesc& o, const void* co
   }
 }
 
-__device__ __forceinline__ void tile_copy(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
-  if (o.nd > 1) {
-    tile_copy_fanout(o, ptr, run, tr);
-    return;
+template <bool COH, class PT>
+__device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
+  if constexpr (!COH) {
+    if (o.nd > 1) {
+      tile_copy_fanout(o, ptr, run, gbeg, gend);
+      return;
+    }
   }
-  const int64_t g0 = tr * kTileGroups + threadIdx.x;
-  const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
+  // slot u of this thread is group gbeg + threadIdx.x + u * kThreads; it
+  // exists while u * kThreads < lim
+  const int lim = static_cast<int>(gend - gbeg) - static_cast<int>(threadIdx.x);
+  const int64_t off = (gbeg + threadIdx.x) * 16;
+  const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride + off;
   uint4 v[kUnroll];
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int64_t g = g0 + u * kThreads;
-    if (g < o.groups) v[u] = ld16(s + g * 16);
-  }
+  for (int u = 0; u < kUnroll; ++u)
+    if (u * kThreads < lim) v[u] = ldv<COH>(s + u * kThreads * 16);
   for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
+    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + off;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t g = g0 + u * kThreads;
-      if (g < o.groups) st16(dp + g * 16, v[u]);
-    }
+    for (int u = 0; u < kUnroll; ++u)
+      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, v[u]);
   }
 }
 
-// fp32 and int32: 4 elements per 16-byte group.
-template <bool FLOAT, int OP>
-__device__ __forceinline__ void tile_4b(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
-  const int64_t g0 = tr * kTileGroups + threadIdx.x;
+// fp32 and int32: 4 elements per 16-byte group.  The loads of SB sources are
+// issued together, then combined one after another in source order, so an
+// operation with many sources waits for ceil(ns / SB) memory round trips
+// rather than ns.  SB = 1 (fewest registers, most resident blocks) for
+// launches that fill the GPU; SB = 4 for small launches of many-source
+// operations, where the round trips are the time: measured on 8 ranks, the
+// fused AllReduce of 1 MiB per rank takes 3.6 instead of 5.6 us, while at
+// 256 MiB per rank SB = 4 is 2% slower than SB = 1.
+template <bool FLOAT, int OP, bool COH, int SB, class PT>
+__device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
+  const int lim = static_cast<int>(gend - gbeg) - static_cast<int>(threadIdx.x);  // slots as in tile_copy
+  const int64_t soff = run * o.sstride + (gbeg + threadIdx.x) * 16;
+  // The first source loads straight into the accumulator (a register copy of
+  // a pending load would stall until it arrives, holding back the next loads).
   uint4 acc[kUnroll];
   {
-    const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
+    const char* s = static_cast<const char*>(ptr[0]) + soff;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t g = g0 + u * kThreads;
-      if (g < o.groups) acc[u] = ld16(s + g * 16);
-    }
+    for (int u = 0; u < kUnroll; ++u)
+      if (u * kThreads < lim) acc[u] = ldv<COH>(s + u * kThreads * 16);
   }
-  for (int k = 1; k < o.ns; ++k) {
-    const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
+  for (int k0 = 1; k0 < o.ns; k0 += SB) {
+    uint4 v[SB][kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t g = g0 + u * kThreads;
-      if (g < o.groups) {
-        const uint4 v = ld16(s + g * 16);
-        if constexpr (FLOAT) {
-          acc[u].x = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].x), __uint_as_float(v.x)));
-          acc[u].y = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].y), __uint_as_float(v.y)));
-          acc[u].z = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].z), __uint_as_float(v.z)));
-          acc[u].w = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].w), __uint_as_float(v.w)));
-        } else {
-          acc[u].x = cmbi<OP>(acc[u].x, v.x);
-          acc[u].y = cmbi<OP>(acc[u].y, v.y);
-          acc[u].z = cmbi<OP>(acc[u].z, v.z);
-          acc[u].w = cmbi<OP>(acc[u].w, v.w);
+    for (int j = 0; j < SB; ++j) {
+      if (k0 + j < o.ns) {
+        const char* s = static_cast<const char*>(ptr[k0 + j]) + soff;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (u * kThreads < lim) v[j][u] = ldv<COH>(s + u * kThreads * 16);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      if (k0 + j < o.ns) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          if (u * kThreads < lim) {
+            const uint4 w = v[j][u];
+            if constexpr (FLOAT) {
+              acc[u].x = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].x), __uint_as_float(w.x)));
+              acc[u].y = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].y), __uint_as_float(w.y)));
+              acc[u].z = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].z), __uint_as_float(w.z)));
+              acc[u].w = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].w), __uint_as_float(w.w)));
+            } else {
+              acc[u].x = cmbi<OP>(acc[u].x, w.x);
+              acc[u].y = cmbi<OP>(acc[u].y, w.y);
+              acc[u].z = cmbi<OP>(acc[u].z, w.z);
+              acc[u].w = cmbi<OP>(acc[u].w, w.w);
+            }
+          }
         }
       }
     }
   }
+  const int64_t doff = run * o.dstride + (gbeg + threadIdx.x) * 16;
   for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
+    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t g = g0 + u * kThreads;
-      if (g < o.groups) st16(dp + g * 16, acc[u]);
-    }
+    for (int u = 0; u < kUnroll; ++u)
+      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, acc[u]);
   }
 }
 
@@ -296,8 +366,8 @@ __device__ __forceinline__ void accumulate8(float* acc, const float* f, bool fir
   }
 }
 
-template <bool F16, int U>
-__device__ __forceinline__ void store_half_mode(const OpDesc& o, const void* const* ptr, int64_t run, int64_t g0,
+template <bool F16, int U, bool COH, class PT>
+__device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, int64_t run, int64_t g0, int64_t gend,
                                                 float (&acc)[U][8]) {
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
@@ -305,15 +375,15 @@ __device__ __forceinline__ void store_half_mode(const OpDesc& o, const void* con
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = g0 + u * kThreads;
-      if (g < o.groups) {
+      if (g < gend) {
         if (f32) {
-          st16(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
-                                       __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
-          st16(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
-                                            __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
+          stv<COH>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
+                                           __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
+          stv<COH>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
+                                                __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
         } else {
-          st16(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
-                                       pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
+          stv<COH>(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
+                                           pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
         }
       }
     }
@@ -322,12 +392,15 @@ __device__ __forceinline__ void store_half_mode(const OpDesc& o, const void* con
 
 // 16-bit data with fp32 partial sums among the sources, one source at a time.
 constexpr int kUnrollBF = 2;  // groups per thread per pass
-template <bool F16, int OP>
-__device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
-  // A tile covers kTileGroups groups in kUnroll/kUnrollBF passes of kUnrollBF groups per thread.
+template <bool F16, int OP, bool COH, class PT>
+__device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
+                                                int64_t gend) {
+  // A tile is covered in passes of kUnrollBF groups per thread.
 #pragma unroll 1
   for (int pass = 0; pass < kUnroll / kUnrollBF; ++pass) {
-    const int64_t g0 = tr * kTileGroups + pass * kUnrollBF * kThreads + threadIdx.x;
+    const int64_t pbeg = gbeg + pass * kUnrollBF * kThreads;
+    if (pbeg >= gend) break;
+    const int64_t g0 = pbeg + threadIdx.x;
     float acc[kUnrollBF][8];
     for (int k = 0; k < o.ns; ++k) {
       const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
@@ -335,20 +408,20 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const void* con
 #pragma unroll
       for (int u = 0; u < kUnrollBF; ++u) {
         const int64_t g = g0 + u * kThreads;
-        if (g < o.groups) {
+        if (g < gend) {
           float f[8];
           if (f32) {
-            const uint4 a = ld16(s + g * 32), b = ld16(s + g * 32 + 16);
+            const uint4 a = ldv<COH>(s + g * 32), b = ldv<COH>(s + g * 32 + 16);
             f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
             f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
           } else {
-            widen8<F16>(ld16(s + g * 16), f);
+            widen8<F16>(ldv<COH>(s + g * 16), f);
           }
           accumulate8<OP>(acc[u], f, k == 0);
         }
       }
     }
-    store_half_mode<F16, kUnrollBF>(o, ptr, run, g0, acc);
+    store_half_mode<F16, kUnrollBF, COH>(o, ptr, run, g0, gend, acc);
   }
 }
 
@@ -360,11 +433,14 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const void* con
 // that kernel's occupancy.
 constexpr int kUnrollBP = 4;
 constexpr int kBatchBP = 2;
-template <bool F16, int OP>
-__device__ __forceinline__ void tile_half_pure(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
+template <bool F16, int OP, bool COH, class PT>
+__device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
+                                               int64_t gend) {
 #pragma unroll 1
   for (int pass = 0; pass < kUnroll / kUnrollBP; ++pass) {
-    const int64_t g0 = tr * kTileGroups + pass * kUnrollBP * kThreads + threadIdx.x;
+    const int64_t pbeg = gbeg + pass * kUnrollBP * kThreads;
+    if (pbeg >= gend) break;
+    const int64_t g0 = pbeg + threadIdx.x;
     float acc[kUnrollBP][8];
     for (int k = 0; k < o.ns; k += kBatchBP) {
       uint4 raw[kBatchBP][kUnrollBP];
@@ -375,7 +451,7 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const void* cons
 #pragma unroll
           for (int u = 0; u < kUnrollBP; ++u) {
             const int64_t g = g0 + u * kThreads;
-            if (g < o.groups) raw[j][u] = ld16(s + g * 16);
+            if (g < gend) raw[j][u] = ldv<COH>(s + g * 16);
           }
         }
       }
@@ -385,7 +461,7 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const void* cons
 #pragma unroll
           for (int u = 0; u < kUnrollBP; ++u) {
             const int64_t g = g0 + u * kThreads;
-            if (g < o.groups) {
+            if (g < gend) {
               float f[8];
               widen8<F16>(raw[j][u], f);
               accumulate8<OP>(acc[u], f, k + j == 0);
@@ -394,24 +470,24 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const void* cons
         }
       }
     }
-    store_half_mode<F16, kUnrollBP>(o, ptr, run, g0, acc);
+    store_half_mode<F16, kUnrollBP, COH>(o, ptr, run, g0, gend, acc);
   }
 }
 
-template <int MODE, int OP>
-__device__ __forceinline__ void tile_vec(const OpDesc& o, const void* const* ptr, int64_t run, int64_t tr) {
-  if constexpr (MODE == kCopy) tile_copy(o, ptr, run, tr);
-  else if constexpr (MODE == kF32) tile_4b<true, OP>(o, ptr, run, tr);
-  else if constexpr (MODE == kI32) tile_4b<false, OP>(o, ptr, run, tr);
-  else if constexpr (MODE == kBF16) tile_half_mixed<false, OP>(o, ptr, run, tr);
-  else if constexpr (MODE == kF16) tile_half_mixed<true, OP>(o, ptr, run, tr);
-  else if constexpr (MODE == kBF16P) tile_half_pure<false, OP>(o, ptr, run, tr);
-  else tile_half_pure<true, OP>(o, ptr, run, tr);
+template <int MODE, int OP, bool COH, int SB, class PT>
+__device__ __forceinline__ void tile_vec(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
+  if constexpr (MODE == kCopy) tile_copy<COH>(o, ptr, run, gbeg, gend);
+  else if constexpr (MODE == kF32) tile_4b<true, OP, COH, SB>(o, ptr, run, gbeg, gend);
+  else if constexpr (MODE == kI32) tile_4b<false, OP, COH, SB>(o, ptr, run, gbeg, gend);
+  else if constexpr (MODE == kBF16) tile_half_mixed<false, OP, COH>(o, ptr, run, gbeg, gend);
+  else if constexpr (MODE == kF16) tile_half_mixed<true, OP, COH>(o, ptr, run, gbeg, gend);
+  else if constexpr (MODE == kBF16P) tile_half_pure<false, OP, COH>(o, ptr, run, gbeg, gend);
+  else tile_half_pure<true, OP, COH>(o, ptr, run, gbeg, gend);
 }
 
 // -- element path (unaligned operands and the tails of vector runs) ---------
-template <int MODE, int OP>
-__device__ __forceinline__ void elem(const OpDesc& o, const void* const* ptr, int64_t soff, int64_t doff, int64_t e) {
+template <int MODE, int OP, class PT>
+__device__ __forceinline__ void elem(const OpDesc& o, const PT& ptr, int64_t soff, int64_t doff, int64_t e) {
   if constexpr (MODE == kCopy) {
     const char* s = static_cast<const char*>(ptr[0]) + soff + e * o.esz;
     if (o.esz == 2) {
@@ -457,29 +533,25 @@ __device__ __forceinline__ int64_t group_elems(const OpDesc& o) {
   return MODE == kCopy ? 16 / o.esz : (MODE == kF32 || MODE == kI32 ? 4 : 8);
 }
 
-template <int MODE, int OP, class P>
-__global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
-  // Programmatic dependent launch: this grid may be scheduled while the
-  // previous step's grid drains; it lets the next step be scheduled the same
-  // way, then waits until the previous grid has completed and its writes are
-  // visible before touching memory.  Without the launch attribute both are
-  // no-ops and plain stream order applies.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-    int lo = 0, hi = static_cast<int>(p.nops) - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.op[mid].tile0 <= t) lo = mid; else hi = mid - 1;
-    }
-    const OpDesc& o = p.op[lo];
-    const void* const* ptr = p.ptr + o.p0;
-    const int64_t lt = t - o.tile0;
-    const int64_t run = lt / o.tpr;
-    const int64_t tr = lt - run * o.tpr;
+// Tile lt of operation o (tiles of one operation are numbered run by run).
+// ELEM: the launch has operations that take the element path (unaligned, or
+// a tail after the last whole group).  Launches without them use the kernel
+// compiled without that path: inlined, its registers count against the
+// vector path (58 instead of 46 for fp32), costing a resident block per SM.
+template <int MODE, int OP, bool COH, int SB, bool ELEM, class PT>
+__device__ __forceinline__ void run_tile(const OpDesc& o, const PT& ptr, uint32_t lt) {
+  const uint32_t run32 = lt / o.tpr;  // tiles of a launch number below 2^32
+  const int64_t run = run32;
+  const int64_t tr = lt - run32 * o.tpr;
+  if (!ELEM || o.vec) {
+    const int64_t tg = static_cast<int64_t>(o.upt) * kThreads;
+    const int64_t gbeg = tr * tg;
+    const int64_t gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
+    tile_vec<MODE, OP, COH, SB>(o, ptr, run, gbeg, gend);
+  }
+  if constexpr (ELEM) {
     const int64_t soff = run * o.sstride, doff = run * o.dstride;
     if (o.vec) {
-      tile_vec<MODE, OP>(o, ptr, run, tr);
       if (tr == o.tpr - 1) {  // elements after the last whole group (single-run operations only)
         for (int64_t e = o.groups * group_elems<MODE>(o) + threadIdx.x; e < o.n; e += kThreads)
           elem<MODE, OP>(o, ptr, soff, doff, e);
@@ -489,6 +561,47 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
       const int64_t e1 = e0 + kTileElems < o.n ? e0 + kTileElems : o.n;
       for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) elem<MODE, OP>(o, ptr, soff, doff, e);
     }
+  }
+}
+
+// The operation holding tile t: the last of op[0, nops) whose tile0 <= t.
+__device__ __forceinline__ int find_op(const OpDesc* op, int nops, uint32_t t) {
+  int lo = 0, hi = nops - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (op[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int MODE, int OP, class P, int SB, bool ELEM>
+__global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
+  // The parameter block is copied to shared memory first, all of it at once
+  // (operation lookups then cost shared-memory reads instead of a chain of
+  // dependent constant-cache misses).  Programmatic dependent launch: this
+  // grid may be scheduled while the previous step's grid drains; it lets the
+  // next step be scheduled the same way, copies its parameters (which do not
+  // depend on the previous step), then waits until the previous grid has
+  // completed and its writes are visible before touching the buffers.
+  // Without the launch attribute both are no-ops and stream order applies.
+  __shared__ P sp;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(&p);
+    uint4* dst = reinterpret_cast<uint4*>(&sp);
+    const uint32_t w0 = (P::kHeaderBytes + p.nops * sizeof(OpDesc)) / 16;
+    for (uint32_t i = threadIdx.x; i < w0; i += kThreads) dst[i] = src[i];
+    constexpr uint32_t pw = P::kPtrOffset / 16;
+    const uint32_t w1 = (p.nptrs * 8 + 15) / 16;
+    for (uint32_t i = threadIdx.x; i < w1; i += kThreads) dst[pw + i] = src[pw + i];
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int nops = static_cast<int>(sp.nops);
+  for (uint32_t t = blockIdx.x; t < sp.ntiles; t += gridDim.x) {
+    const OpDesc& o = sp.op[find_op(sp.op, nops, t)];
+    const void* const* ptr = sp.ptr + o.p0;
+    run_tile<MODE, OP, false, SB, ELEM>(o, ptr, t - o.tile0);
   }
   // outstanding bulk stores of fan-out copies finish before the block exits
   if (MODE == kCopy && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -501,11 +614,19 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------
 namespace {
 
+// Blocks of one kernel resident per SM, and the dynamic shared memory each
+// launch requests to hold it there (0: the kernel's own limit applies).
+struct Residency {
+  int blocks = 1;
+  int dyn_smem = 0;
+};
 struct DeviceState {
   bool init = false;
   int nsm = 0;
+  int smem_per_sm = 0;     // shared memory per SM
+  int smem_reserved = 0;   // reserved by the system per block
   cudaMemPool_t pool = nullptr;
-  std::map<const void*, int> occupancy;
+  std::map<const void*, Residency> occupancy;
 };
 std::mutex g_mu;
 DeviceState g_dev[64];
@@ -519,6 +640,10 @@ vc_status_t device_state(DeviceState** out, int* dev_out) {
   DeviceState& st = g_dev[dev];
   if (!st.init) {
     e = cudaDeviceGetAttribute(&st.nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaDeviceGetAttribute(&st.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     st.init = true;
   }
@@ -546,16 +671,46 @@ vc_status_t scratch_pool(DeviceState* st, int dev, cudaMemPool_t* pool) {
   return VC_SUCCESS;
 }
 
+// VC_BLOCKS_PER_SM=k holds every kernel at k resident blocks per SM (tuning;
+// 0 or unset: each kernel's own limit).
+int blocks_env() {
+  static const int k = [] {
+    const char* v = std::getenv("VC_BLOCKS_PER_SM");
+    return v ? std::atoi(v) : 0;
+  }();
+  return k;
+}
+
+// Residency of a kernel: its occupancy limit, or `want` blocks per SM when
+// that is lower.  A lower count is enforced, not just asked for: each block
+// requests enough dynamic shared memory that no more than `want` fit on an
+// SM, so the grid (SMs x blocks) lands evenly instead of five blocks on some
+// SMs and three on others.
 template <class K>
-int blocks_per_sm(DeviceState* st, K kernel) {
+Residency residency(DeviceState* st, K kernel, int want = 0) {
   std::lock_guard<std::mutex> lk(g_mu);
   const void* key = reinterpret_cast<const void*>(kernel);
   auto it = st->occupancy.find(key);
   if (it != st->occupancy.end()) return it->second;
+  Residency r;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, dev::kThreads, 0) != cudaSuccess || n < 1) n = 1;
-  st->occupancy[key] = n;
-  return n;
+  r.blocks = n;
+  if (blocks_env() > 0) want = blocks_env();
+  cudaFuncAttributes fa{};
+  if (want > 0 && want < n && cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
+    const int per_block = st->smem_per_sm / want - st->smem_reserved - static_cast<int>(fa.sharedSizeBytes);
+    const int dyn = (per_block - 128) / 128 * 128;
+    int m = 0;
+    if (dyn > 0 && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m, kernel, dev::kThreads, dyn) == cudaSuccess && m == want) {
+      r.blocks = want;
+      r.dyn_smem = dyn;
+    }
+    cudaGetLastError();
+  }
+  st->occupancy[key] = r;
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -625,11 +780,14 @@ int64_t group_elements(Mode mode, int esz) {
   return 0;
 }
 
+// Fills the parameter block of operations [i, j) of a step.  Tiles: the
+// largest number of groups per thread (4, 2 or 1) that still gives the launch
+// `cap` tiles (one per resident block), so a small step is spread over many
+// blocks instead of a few doing all of it.
 template <class P>
-bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t* tiles_out) {
+bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t cap, int64_t* tiles_out) {
   std::memset(&p, 0, sizeof(P));
   const Mode mode = st.mode;
-  int64_t tiles = 0;
   int np = 0;
   for (size_t k = i; k < j; ++k) {
     const Op& op = st.ops[k];
@@ -660,21 +818,33 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
       aligned &= (op.n % gelems) == 0 && (op.sstride % 16) == 0 && (op.dstride % 16) == 0;
     }
     d.vec = aligned ? 1 : 0;
-    int64_t tpr;
-    if (aligned) {
-      d.groups = op.n / gelems;
-      tpr = std::max<int64_t>(1, (d.groups + dev::kTileGroups - 1) / dev::kTileGroups);
-    } else {
-      d.groups = 0;
-      tpr = std::max<int64_t>(1, (op.n + dev::kTileElems - 1) / dev::kTileElems);
-    }
+    d.groups = aligned ? op.n / gelems : 0;
+  }
+  auto tiles_per_run = [](const dev::OpDesc& d, int upt) {
+    const int64_t per = d.vec ? int64_t(upt) * dev::kThreads : dev::kTileElems;
+    const int64_t units = d.vec ? d.groups : d.n;
+    return std::max<int64_t>(1, (units + per - 1) / per);
+  };
+  auto count_tiles = [&](int upt) {
+    int64_t total = 0;
+    for (size_t k = i; k < j; ++k) total += tiles_per_run(p.op[k - i], upt) * p.op[k - i].nb;
+    return total;
+  };
+  int upt = dev::kUnroll;
+  while (upt > 1 && count_tiles(upt) < cap) upt /= 2;
+  int64_t tiles = 0;
+  for (size_t k = i; k < j; ++k) {
+    dev::OpDesc& d = p.op[k - i];
+    d.upt = static_cast<uint8_t>(upt);
+    const int64_t tpr = tiles_per_run(d, upt);
     d.tpr = static_cast<uint32_t>(tpr);
     d.tile0 = static_cast<uint32_t>(tiles);
-    tiles += tpr * op.nb;
+    tiles += tpr * d.nb;
     if (tiles > 0xFFFFFFFFll || tpr > 0xFFFFFFFFll) return false;
   }
   p.nops = static_cast<uint32_t>(j - i);
   p.ntiles = static_cast<uint32_t>(tiles);
+  p.nptrs = static_cast<uint32_t>(np);
   *tiles_out = tiles;
   return true;
 }
@@ -683,11 +853,32 @@ template <int MODE, int OP, class P>
 vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
                          const TraceCtx& tc) {
   static thread_local P p;  // large: keep off the stack
+  // tiles are sized against the vector-only kernel's residency
+  auto kernel = dev::step_kernel<MODE, OP, P, 1, false>;
+  Residency res = residency(st, kernel);
+  int64_t cap = int64_t(st->nsm) * res.blocks;
   int64_t tiles = 0;
-  if (!fill_params(p, s, i, j, b, &tiles)) return fail(VC_ERR_INVALID_ARG, "operation too large for one launch");
+  if (!fill_params(p, s, i, j, b, cap, &tiles)) return fail(VC_ERR_INVALID_ARG, "operation too large for one launch");
   if (tiles == 0) return VC_SUCCESS;
-  auto kernel = dev::step_kernel<MODE, OP, P>;
-  const int64_t cap = int64_t(st->nsm) * blocks_per_sm(st, kernel);
+  bool elem = false;
+  int maxns = 0;
+  for (uint32_t k = 0; k < p.nops; ++k) {
+    const dev::OpDesc& d = p.op[k];
+    elem |= !d.vec || d.groups * group_elements(s.mode, d.esz) < d.n;
+    maxns = std::max<int>(maxns, d.ns);
+  }
+  // fp32 / int32: a launch that does not fill the GPU (tiles were shrunk)
+  // with a many-source operation loads four sources at a time
+  bool batched = false;
+  if constexpr (MODE == dev::kF32 || MODE == dev::kI32) {
+    batched = p.op[0].upt < dev::kUnroll && maxns > 2;
+    if (batched) kernel = elem ? dev::step_kernel<MODE, OP, P, 4, true> : dev::step_kernel<MODE, OP, P, 4, false>;
+  }
+  if (!batched && elem) kernel = dev::step_kernel<MODE, OP, P, 1, true>;
+  if (batched || elem) {
+    res = residency(st, kernel);
+    cap = int64_t(st->nsm) * res.blocks;
+  }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, cap));
   std::unique_lock<std::mutex> lk(g_trace_mu);
   const bool trace = g_trace_on;
@@ -702,7 +893,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(dev::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(res.dyn_smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -718,7 +909,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
     pend.rec.coll = tc.coll;
     pend.rec.algo = tc.algo;
     pend.rec.step = tc.step;
-    pend.rec.kernel = MODE | (OP << 3) | (sizeof(P) == sizeof(dev::LargeParams) ? 32 : 0);
+    pend.rec.kernel = MODE | (OP << 3) | (sizeof(P) == sizeof(dev::LargeParams) ? 32 : 0) | (batched ? 64 : 0);
     pend.rec.bytes = launch_bytes(s, i, j);
     pend.rec.nops = static_cast<int32_t>(j - i);
     g_trace.push_back(pend);

@@ -322,7 +322,8 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  *   partials among the sources, 4 bf16 only, 5 fp16 with fp32 partials, 6
  *   fp16 only), bits 3-4 the op (0 sum, 1 max, 2 min), bit 5 set when the
  *   launch used the large parameter block (more than 16 operations or 64
- *   operand pointers).
+ *   operand pointers), bit 6 set when an fp32 / int32 launch too small to
+ *   fill the GPU took the kernel that loads four sources at a time.
  */
 typedef struct {
   int32_t coll;   /* vc_coll_t */
