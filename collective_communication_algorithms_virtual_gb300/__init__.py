@@ -28,6 +28,9 @@ from .binding import (  # noqa: F401
     vc_scatter,
     vc_select_algo,
     vc_set_cost_model,
+    vc_set_single_launch,
+    vc_get_single_launch,
+    SINGLE_LAUNCH_ALWAYS,
     vc_get_cost_model,
     vc_status_string,
     vc_trace_enable,

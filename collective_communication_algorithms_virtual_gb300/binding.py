@@ -44,7 +44,8 @@ KERNEL_OPS = {0: "sum", 1: "max", 2: "min"}
 def kernel_name(code: int) -> str:
     mode = KERNEL_MODES[code & 7]
     name = mode if mode == "copy" else f"{KERNEL_OPS[(code >> 3) & 3]}_{mode}"
-    return name + ("_large" if code & 32 else "") + ("_batched" if code & 64 else "")
+    return (name + ("_large" if code & 32 else "") + ("_batched" if code & 64 else "")
+            + ("_single_launch" if code & 128 else ""))
 
 
 class PlanEntry(ctypes.Structure):
@@ -99,6 +100,10 @@ def lib() -> ctypes.CDLL:
         L.vc_get_cost_model.restype = I
         L.vc_select_algo.argtypes = [I, I, Z, I, I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
         L.vc_select_algo.restype = I
+        L.vc_set_single_launch.argtypes = [Z]
+        L.vc_set_single_launch.restype = I
+        L.vc_get_single_launch.argtypes = [ctypes.POINTER(Z)]
+        L.vc_get_single_launch.restype = I
         L.vc_version.argtypes = []
         L.vc_version.restype = I
         _lib = L
@@ -252,6 +257,21 @@ def vc_select_algo(coll, nranks: int, count: int, dtype="f32", root: int = 0):
     check(lib().vc_select_algo(_code(COLLS, coll), int(nranks), int(count), _code(DTYPES, dtype), int(root),
                                ctypes.byref(a), ctypes.byref(t)))
     return ALGO_NAMES[a.value], t.value
+
+
+def vc_set_single_launch(max_step_bytes: int) -> None:
+    """Run schedules whose steps each move at most this many bytes in one
+    launch (0: never; SINGLE_LAUNCH_ALWAYS: whenever eligible)."""
+    check(lib().vc_set_single_launch(int(max_step_bytes)))
+
+
+def vc_get_single_launch() -> int:
+    v = ctypes.c_size_t(0)
+    check(lib().vc_get_single_launch(ctypes.byref(v)))
+    return v.value
+
+
+SINGLE_LAUNCH_ALWAYS = (1 << 64) - 1
 
 
 def vc_trace_enable(on: bool = True) -> None:

@@ -78,6 +78,9 @@ constexpr int kUnroll = 4;           // 16-byte groups per thread per tile (vect
 constexpr int kScalarPerThread = 4;  // elements per thread per tile (element path)
 constexpr int kTileGroups = kThreads * kUnroll;
 constexpr int kTileElems = kThreads * kScalarPerThread;
+// A tile is worked by kThreads threads: a whole block of the per-step kernel,
+// or one of the sub-blocks of a one-launch plan's larger blocks.
+__device__ __forceinline__ int lane() { return static_cast<int>(threadIdx.x) & (kThreads - 1); }
 
 // Kernel modes: copy; fp32 / int32 reductions; 16-bit float reductions whose
 // sources mix the data type with fp32 partial sums, or are all of the data
@@ -273,10 +276,10 @@ __device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_
       return;
     }
   }
-  // slot u of this thread is group gbeg + threadIdx.x + u * kThreads; it
+  // slot u of this thread is group gbeg + lane() + u * kThreads; it
   // exists while u * kThreads < lim
-  const int lim = static_cast<int>(gend - gbeg) - static_cast<int>(threadIdx.x);
-  const int64_t off = (gbeg + threadIdx.x) * 16;
+  const int lim = static_cast<int>(gend - gbeg) - lane();
+  const int64_t off = (gbeg + lane()) * 16;
   const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride + off;
   uint4 v[kUnroll];
 #pragma unroll
@@ -300,8 +303,8 @@ __device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_
 // 256 MiB per rank SB = 4 is 2% slower than SB = 1.
 template <bool FLOAT, int OP, bool COH, int SB, class PT>
 __device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
-  const int lim = static_cast<int>(gend - gbeg) - static_cast<int>(threadIdx.x);  // slots as in tile_copy
-  const int64_t soff = run * o.sstride + (gbeg + threadIdx.x) * 16;
+  const int lim = static_cast<int>(gend - gbeg) - lane();  // slots as in tile_copy
+  const int64_t soff = run * o.sstride + (gbeg + lane()) * 16;
   // The first source loads straight into the accumulator (a register copy of
   // a pending load would stall until it arrives, holding back the next loads).
   uint4 acc[kUnroll];
@@ -345,7 +348,7 @@ __device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t 
       }
     }
   }
-  const int64_t doff = run * o.dstride + (gbeg + threadIdx.x) * 16;
+  const int64_t doff = run * o.dstride + (gbeg + lane()) * 16;
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
 #pragma unroll
@@ -400,7 +403,7 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, 
   for (int pass = 0; pass < kUnroll / kUnrollBF; ++pass) {
     const int64_t pbeg = gbeg + pass * kUnrollBF * kThreads;
     if (pbeg >= gend) break;
-    const int64_t g0 = pbeg + threadIdx.x;
+    const int64_t g0 = pbeg + lane();
     float acc[kUnrollBF][8];
     for (int k = 0; k < o.ns; ++k) {
       const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
@@ -440,7 +443,7 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, i
   for (int pass = 0; pass < kUnroll / kUnrollBP; ++pass) {
     const int64_t pbeg = gbeg + pass * kUnrollBP * kThreads;
     if (pbeg >= gend) break;
-    const int64_t g0 = pbeg + threadIdx.x;
+    const int64_t g0 = pbeg + lane();
     float acc[kUnrollBP][8];
     for (int k = 0; k < o.ns; k += kBatchBP) {
       uint4 raw[kBatchBP][kUnrollBP];
@@ -486,29 +489,50 @@ __device__ __forceinline__ void tile_vec(const OpDesc& o, const PT& ptr, int64_t
 }
 
 // -- element path (unaligned operands and the tails of vector runs) ---------
-template <int MODE, int OP, class PT>
+// Scalar loads: plain, or through L2 (.cg) for one-launch plans (see ldv).
+template <bool COH>
+__device__ __forceinline__ uint32_t ld32(const void* p) {
+  if constexpr (COH) {
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+  } else {
+    return *static_cast<const uint32_t*>(p);
+  }
+}
+template <bool COH>
+__device__ __forceinline__ uint16_t ld16b(const void* p) {
+  if constexpr (COH) {
+    uint16_t v;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return v;
+  } else {
+    return *static_cast<const uint16_t*>(p);
+  }
+}
+
+template <int MODE, int OP, bool COH, class PT>
 __device__ __forceinline__ void elem(const OpDesc& o, const PT& ptr, int64_t soff, int64_t doff, int64_t e) {
   if constexpr (MODE == kCopy) {
     const char* s = static_cast<const char*>(ptr[0]) + soff + e * o.esz;
     if (o.esz == 2) {
-      const uint16_t v = *reinterpret_cast<const uint16_t*>(s);
+      const uint16_t v = ld16b<COH>(s);
       for (int d = 0; d < o.nd; ++d)
         *reinterpret_cast<uint16_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 2) = v;
     } else {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(s);
+      const uint32_t v = ld32<COH>(s);
       for (int d = 0; d < o.nd; ++d)
         *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = v;
     }
   } else if constexpr (MODE == kF32) {
-    float acc = *reinterpret_cast<const float*>(static_cast<const char*>(ptr[0]) + soff + e * 4);
+    float acc = __uint_as_float(ld32<COH>(static_cast<const char*>(ptr[0]) + soff + e * 4));
     for (int k = 1; k < o.ns; ++k)
-      acc = cmb<OP>(acc, *reinterpret_cast<const float*>(static_cast<const char*>(ptr[k]) + soff + e * 4));
+      acc = cmb<OP>(acc, __uint_as_float(ld32<COH>(static_cast<const char*>(ptr[k]) + soff + e * 4)));
     for (int d = 0; d < o.nd; ++d)
       *reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
   } else if constexpr (MODE == kI32) {
-    uint32_t acc = *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[0]) + soff + e * 4);
-    for (int k = 1; k < o.ns; ++k)
-      acc = cmbi<OP>(acc, *reinterpret_cast<const uint32_t*>(static_cast<const char*>(ptr[k]) + soff + e * 4));
+    uint32_t acc = ld32<COH>(static_cast<const char*>(ptr[0]) + soff + e * 4);
+    for (int k = 1; k < o.ns; ++k) acc = cmbi<OP>(acc, ld32<COH>(static_cast<const char*>(ptr[k]) + soff + e * 4));
     for (int d = 0; d < o.nd; ++d)
       *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
   } else {
@@ -516,8 +540,7 @@ __device__ __forceinline__ void elem(const OpDesc& o, const PT& ptr, int64_t sof
     float acc = 0.f;
     for (int k = 0; k < o.ns; ++k) {
       const char* s = static_cast<const char*>(ptr[k]) + soff;
-      const float v = ((o.smask >> k) & 1) ? *reinterpret_cast<const float*>(s + e * 4)
-                                           : widen1<F16>(*reinterpret_cast<const uint16_t*>(s + e * 2));
+      const float v = ((o.smask >> k) & 1) ? __uint_as_float(ld32<COH>(s + e * 4)) : widen1<F16>(ld16b<COH>(s + e * 2));
       acc = k == 0 ? v : cmb<OP>(acc, v);
     }
     for (int d = 0; d < o.nd; ++d) {
@@ -553,13 +576,13 @@ __device__ __forceinline__ void run_tile(const OpDesc& o, const PT& ptr, uint32_
     const int64_t soff = run * o.sstride, doff = run * o.dstride;
     if (o.vec) {
       if (tr == o.tpr - 1) {  // elements after the last whole group (single-run operations only)
-        for (int64_t e = o.groups * group_elems<MODE>(o) + threadIdx.x; e < o.n; e += kThreads)
-          elem<MODE, OP>(o, ptr, soff, doff, e);
+        for (int64_t e = o.groups * group_elems<MODE>(o) + lane(); e < o.n; e += kThreads)
+          elem<MODE, OP, COH>(o, ptr, soff, doff, e);
       }
     } else {
       const int64_t e0 = tr * kTileElems;
       const int64_t e1 = e0 + kTileElems < o.n ? e0 + kTileElems : o.n;
-      for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) elem<MODE, OP>(o, ptr, soff, doff, e);
+      for (int64_t e = e0 + lane(); e < e1; e += kThreads) elem<MODE, OP, COH>(o, ptr, soff, doff, e);
     }
   }
 }
@@ -605,6 +628,86 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
   }
   // outstanding bulk stores of fan-out copies finish before the block exits
   if (MODE == kCopy && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// -- one-launch plans ------------------------------------------------------------
+// A plan can run as one launch of one thread-block cluster: the blocks walk
+// the tiles of step 0, meet at a cluster barrier (release / acquire: every
+// write of the step is visible to every block before any block starts the
+// next), walk step 1, and so on.  The operations, their order and each
+// element's association are those of the per-step launches; only the launch
+// and grid drain between steps are gone.  The plan's description lives in
+// device memory (written once per plan shape): a header, the steps, the
+// operations (tile numbers relative to their step, pointer indices into the
+// operand table) and the operand table, whose entries name a buffer base
+// (send r, recv r, scratch) and a byte offset.  The call passes only the
+// bases.  Every block copies the description and the bases to shared memory
+// before waiting on the previous grid, so the lookups of the step walk are
+// shared-memory reads.
+struct __align__(16) PlanHeader {
+  uint32_t nsteps, nops, nrefs, pad;
+};
+struct __align__(16) PlanStep {
+  uint32_t op0;     // first operation of the step
+  uint32_t nops;    // its operations
+  uint32_t ntiles;  // its tiles
+  uint32_t mode;    // kCopy or the plan's reduction mode
+};
+struct __align__(16) OperandRef {
+  uint32_t base;  // index into the bases: send r = r, recv r = N + r, scratch = 2N
+  uint32_t pad;
+  int64_t off;    // bytes from the base
+};
+struct RefPtrs {
+  const OperandRef* ref;
+  const void* const* base;
+  __device__ __forceinline__ const void* operator[](int k) const {
+    return static_cast<const char*>(base[ref[k].base]) + ref[k].off;
+  }
+};
+struct __align__(16) PlanParams {
+  const uint4* plan;  // the description, 16-byte words
+  uint32_t words;
+  uint32_t nbases;
+  const void* base[2 * VC_MAX_RANKS + 1];
+};
+
+// Blocks of kPlanSubs sub-blocks of kThreads threads; each sub-block walks
+// its own tiles (tile functions index by lane()).  Measured on 8 ranks: two
+// sub-blocks double the bandwidth of mid-size plans (16 MB per rank ring:
+// 962 -> 599 us) but add about 0.2 us per step to small ones (1 KB ring:
+// 18.0 -> 20.9 us), and single launches are only chosen for small ones.
+constexpr int kPlanSubs = 1;
+constexpr int kPlanThreads = kThreads * kPlanSubs;
+
+template <int RMODE, int OP>
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
+  extern __shared__ uint4 sm[];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (uint32_t i = threadIdx.x; i < p.words; i += kPlanThreads) sm[i] = ld16(p.plan + i);
+  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
+  for (uint32_t i = threadIdx.x; i < p.nbases; i += kPlanThreads) sbase[i] = p.base[i];
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
+  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
+  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
+  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
+  // Every block runs every iteration of this loop (the step count is the
+  // same for all), so each meets each barrier exactly once.
+  for (uint32_t s = 0; s < h.nsteps; ++s) {
+    const PlanStep st = steps[s];
+    const OpDesc* sop = ops + st.op0;
+    const uint32_t first = blockIdx.x * kPlanSubs + threadIdx.x / kThreads, stride = gridDim.x * kPlanSubs;
+    for (uint32_t t = first; t < st.ntiles; t += stride) {
+      const OpDesc& o = sop[find_op(sop, static_cast<int>(st.nops), t)];
+      const RefPtrs ptr{refs + o.p0, sbase};
+      if (st.mode == kCopy) run_tile<kCopy, OP, true, 1, true>(o, ptr, t - o.tile0);
+      else run_tile<RMODE, OP, true, 4, true>(o, ptr, t - o.tile0);
+    }
+    if (s + 1 < h.nsteps)
+      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
 }
 
 }  // namespace dev
@@ -780,68 +883,81 @@ int64_t group_elements(Mode mode, int esz) {
   return 0;
 }
 
-// Fills the parameter block of operations [i, j) of a step.  Tiles: the
-// largest number of groups per thread (4, 2 or 1) that still gives the launch
-// `cap` tiles (one per resident block), so a small step is spread over many
-// blocks instead of a few doing all of it.
-template <class P>
-bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t cap, int64_t* tiles_out) {
-  std::memset(&p, 0, sizeof(P));
-  const Mode mode = st.mode;
-  int np = 0;
-  for (size_t k = i; k < j; ++k) {
-    const Op& op = st.ops[k];
-    dev::OpDesc& d = p.op[k - i];
-    d.n = op.n;
-    d.nb = op.nb;
-    d.sstride = op.sstride;
-    d.dstride = op.dstride;
-    d.ns = static_cast<uint8_t>(op.src.size());
-    d.nd = static_cast<uint8_t>(op.dst.size());
-    d.p0 = static_cast<uint16_t>(np);
-    d.esz = static_cast<uint8_t>(esize(op.src[0].dt));
-    bool aligned = true;
-    for (size_t s = 0; s < op.src.size(); ++s) {
-      const char* ptr = base_ptr(b, op.src[s]);
-      p.ptr[np++] = ptr;
-      aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
-      if (op.src[s].dt == DT::F32) d.smask |= 1ull << s;
-    }
-    for (size_t s = 0; s < op.dst.size(); ++s) {
-      const char* ptr = base_ptr(b, op.dst[s]);
-      p.ptr[np++] = ptr;
-      aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
-      if (op.dst[s].dt == DT::F32) d.dmask |= 1ull << s;
-    }
-    const int64_t gelems = group_elements(mode, d.esz);
-    if (op.nb > 1) {
-      aligned &= (op.n % gelems) == 0 && (op.sstride % 16) == 0 && (op.dstride % 16) == 0;
-    }
-    d.vec = aligned ? 1 : 0;
-    d.groups = aligned ? op.n / gelems : 0;
-  }
-  auto tiles_per_run = [](const dev::OpDesc& d, int upt) {
-    const int64_t per = d.vec ? int64_t(upt) * dev::kThreads : dev::kTileElems;
-    const int64_t units = d.vec ? d.groups : d.n;
+// Descriptor of one operation, except its tiling and pointer index.
+// `ptrs_aligned`: every operand address is 16-byte aligned.
+void describe_op(dev::OpDesc& d, const Op& op, Mode mode, bool ptrs_aligned) {
+  d.n = op.n;
+  d.nb = op.nb;
+  d.sstride = op.sstride;
+  d.dstride = op.dstride;
+  d.ns = static_cast<uint8_t>(op.src.size());
+  d.nd = static_cast<uint8_t>(op.dst.size());
+  d.esz = static_cast<uint8_t>(esize(op.src[0].dt));
+  d.smask = d.dmask = 0;
+  for (size_t s = 0; s < op.src.size(); ++s)
+    if (op.src[s].dt == DT::F32) d.smask |= 1ull << s;
+  for (size_t s = 0; s < op.dst.size(); ++s)
+    if (op.dst[s].dt == DT::F32) d.dmask |= 1ull << s;
+  const int64_t gelems = group_elements(mode, d.esz);
+  bool aligned = ptrs_aligned;
+  if (op.nb > 1) aligned &= (op.n % gelems) == 0 && (op.sstride % 16) == 0 && (op.dstride % 16) == 0;
+  d.vec = aligned ? 1 : 0;
+  d.groups = aligned ? op.n / gelems : 0;
+}
+
+// Tiles operations d[0, n): the largest number of groups per thread (4, 2 or
+// 1) that still gives `cap` tiles (one per resident block), so a small step
+// is spread over many blocks instead of a few doing all of it.  Returns the
+// tile count, or -1 if it does not fit the 32-bit tile numbers.
+int64_t assign_tiles(dev::OpDesc* d, size_t n, int64_t cap) {
+  auto tiles_per_run = [](const dev::OpDesc& o, int upt) {
+    const int64_t per = o.vec ? int64_t(upt) * dev::kThreads : dev::kTileElems;
+    const int64_t units = o.vec ? o.groups : o.n;
     return std::max<int64_t>(1, (units + per - 1) / per);
   };
   auto count_tiles = [&](int upt) {
     int64_t total = 0;
-    for (size_t k = i; k < j; ++k) total += tiles_per_run(p.op[k - i], upt) * p.op[k - i].nb;
+    for (size_t k = 0; k < n; ++k) total += tiles_per_run(d[k], upt) * d[k].nb;
     return total;
   };
   int upt = dev::kUnroll;
   while (upt > 1 && count_tiles(upt) < cap) upt /= 2;
   int64_t tiles = 0;
-  for (size_t k = i; k < j; ++k) {
-    dev::OpDesc& d = p.op[k - i];
-    d.upt = static_cast<uint8_t>(upt);
-    const int64_t tpr = tiles_per_run(d, upt);
-    d.tpr = static_cast<uint32_t>(tpr);
-    d.tile0 = static_cast<uint32_t>(tiles);
-    tiles += tpr * d.nb;
-    if (tiles > 0xFFFFFFFFll || tpr > 0xFFFFFFFFll) return false;
+  for (size_t k = 0; k < n; ++k) {
+    d[k].upt = static_cast<uint8_t>(upt);
+    const int64_t tpr = tiles_per_run(d[k], upt);
+    d[k].tpr = static_cast<uint32_t>(tpr);
+    d[k].tile0 = static_cast<uint32_t>(tiles);
+    tiles += tpr * d[k].nb;
+    if (tiles > 0xFFFFFFFFll || tpr > 0xFFFFFFFFll) return -1;
   }
+  return tiles;
+}
+
+// Fills the parameter block of operations [i, j) of a step.
+template <class P>
+bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t cap, int64_t* tiles_out) {
+  std::memset(&p, 0, sizeof(P));
+  int np = 0;
+  for (size_t k = i; k < j; ++k) {
+    const Op& op = st.ops[k];
+    bool aligned = true;
+    const int p0 = np;
+    for (const Operand& o : op.src) {
+      const char* ptr = base_ptr(b, o);
+      p.ptr[np++] = ptr;
+      aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
+    }
+    for (const Operand& o : op.dst) {
+      const char* ptr = base_ptr(b, o);
+      p.ptr[np++] = ptr;
+      aligned &= (reinterpret_cast<uintptr_t>(ptr) & 15) == 0;
+    }
+    describe_op(p.op[k - i], op, st.mode, aligned);
+    p.op[k - i].p0 = static_cast<uint16_t>(p0);
+  }
+  const int64_t tiles = assign_tiles(p.op, j - i, cap);
+  if (tiles < 0) return false;
   p.nops = static_cast<uint32_t>(j - i);
   p.ntiles = static_cast<uint32_t>(tiles);
   p.nptrs = static_cast<uint32_t>(np);
@@ -1095,9 +1211,13 @@ struct PlanKeyHash {
 std::mutex g_plan_mu;
 std::unordered_map<PlanKey, std::shared_ptr<const Plan>, PlanKeyHash> g_plans;
 
+PlanKey plan_key(const PlanArgs& pa) {
+  return PlanKey{static_cast<int>(pa.coll), static_cast<int>(pa.algo), pa.nranks, static_cast<int>(pa.dt),
+                 pa.root, pa.inplace ? 1 : 0, pa.nchunks, static_cast<int>(pa.op), pa.count};
+}
+
 PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std::string* why) {
-  const PlanKey key{static_cast<int>(pa.coll), static_cast<int>(pa.algo), pa.nranks, static_cast<int>(pa.dt),
-                    pa.root, pa.inplace ? 1 : 0, pa.nchunks, static_cast<int>(pa.op), pa.count};
+  const PlanKey key = plan_key(pa);
   {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     auto it = g_plans.find(key);
@@ -1114,6 +1234,292 @@ PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std
   g_plans.emplace(key, plan);
   *out = plan;
   return PlanStatus::Ok;
+}
+
+// ---------------------------------------------------------------------------
+// one-launch plans (host side)
+// ---------------------------------------------------------------------------
+std::mutex g_sl_mu;
+size_t g_sl_limit = VC_SINGLE_LAUNCH_DEFAULT;
+constexpr int kPlanSmemMax = 96 << 10;            // description + bases in shared memory
+constexpr size_t kPlanArenaChunk = 4u << 20;      // device memory for descriptions, per allocation
+constexpr size_t kPlanArenaMax = 64u << 20;       // and in total, per device
+
+size_t single_launch_limit() {
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  return g_sl_limit;
+}
+
+struct DevPlan {
+  bool eligible = false;
+  const char* why = "";          // when not eligible
+  const uint4* dptr = nullptr;   // description in device memory
+  uint32_t words = 0;
+  int rmode = dev::kCopy;        // kernel mode of the reduction steps
+  RedOp red = RedOp::Sum;
+  int64_t max_step_bytes = 0;
+  int64_t bytes = 0;
+  int nops = 0;
+};
+struct PlanStore {
+  std::unordered_map<PlanKey, DevPlan, PlanKeyHash> plans;
+  std::vector<void*> chunks;
+  size_t chunk_used = kPlanArenaChunk;  // forces the first allocation
+  size_t total = 0;
+  cudaStream_t upload = nullptr;
+  int cluster = 0;  // blocks per cluster (0: not yet chosen)
+};
+PlanStore g_store[64];
+
+int kernel_mode(Mode m) {
+  switch (m) {
+    case Mode::Copy: return dev::kCopy;
+    case Mode::F32: return dev::kF32;
+    case Mode::I32: return dev::kI32;
+    case Mode::BF16: return dev::kBF16;
+    case Mode::F16: return dev::kF16;
+  }
+  return dev::kCopy;
+}
+
+using PlanKernel = void (*)(dev::PlanParams);
+template <int RMODE>
+PlanKernel plan_kernel_op(RedOp r) {
+  switch (r) {
+    case RedOp::Max: return dev::plan_kernel<RMODE, dev::kMax>;
+    case RedOp::Min: return dev::plan_kernel<RMODE, dev::kMin>;
+    default: return dev::plan_kernel<RMODE, dev::kSum>;
+  }
+}
+PlanKernel plan_kernel_for(int rmode, RedOp r) {
+  switch (rmode) {
+    case dev::kF32: return plan_kernel_op<dev::kF32>(r);
+    case dev::kI32: return plan_kernel_op<dev::kI32>(r);
+    case dev::kBF16: return plan_kernel_op<dev::kBF16>(r);
+    case dev::kF16: return plan_kernel_op<dev::kF16>(r);
+    default: return dev::plan_kernel<dev::kCopy, dev::kSum>;
+  }
+}
+
+// Blocks per cluster: 16 (non-portable size) where the device can place such
+// a cluster with the largest description, else 8.
+int plan_cluster(PlanStore& ps) {
+  if (ps.cluster) return ps.cluster;
+  PlanKernel k = dev::plan_kernel<dev::kF32, dev::kSum>;
+  int best = 8;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax) == cudaSuccess &&
+      cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(dev::kPlanThreads);
+    cfg.dynamicSmemBytes = kPlanSmemMax;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 16;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n >= 1) best = 16;
+  }
+  cudaGetLastError();
+  ps.cluster = best;
+  return best;
+}
+
+// Builds the description of `plan` for N ranks tiled for `workers` tile
+// walkers (sub-blocks of the cluster), assuming every buffer base is 16-byte
+// aligned (checked at each call).
+void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, DevPlan* dp) {
+  dp->eligible = false;
+  const size_t S = plan.steps.size();
+  if (S < 2) { dp->why = "single step"; return; }
+  bool have_red = false;
+  size_t nops = 0, nrefs = 0;
+  for (const Step& s : plan.steps) {
+    nops += s.ops.size();
+    for (const Op& op : s.ops) nrefs += op.src.size() + op.dst.size();
+    if (s.mode == Mode::Copy) continue;
+    if (have_red && (kernel_mode(s.mode) != dp->rmode || s.red != dp->red)) { dp->why = "mixed reductions"; return; }
+    have_red = true;
+    dp->rmode = kernel_mode(s.mode);
+    dp->red = s.red;
+  }
+  if (nrefs > 0xFFFF) { dp->why = "too many operands"; return; }
+  const size_t words = 1 + S + nops * (sizeof(dev::OpDesc) / 16) + nrefs;
+  if (words * 16 + (2 * N + 1) * sizeof(void*) > static_cast<size_t>(kPlanSmemMax)) { dp->why = "too large"; return; }
+  img->assign(words, make_uint4(0, 0, 0, 0));
+  auto* hdr = reinterpret_cast<dev::PlanHeader*>(img->data());
+  auto* steps = reinterpret_cast<dev::PlanStep*>(img->data() + 1);
+  auto* ops = reinterpret_cast<dev::OpDesc*>(img->data() + 1 + S);
+  auto* refs = reinterpret_cast<dev::OperandRef*>(ops + nops);
+  hdr->nsteps = static_cast<uint32_t>(S);
+  hdr->nops = static_cast<uint32_t>(nops);
+  hdr->nrefs = static_cast<uint32_t>(nrefs);
+  auto ref_of = [&](const Operand& o) {
+    dev::OperandRef r{};
+    r.base = o.buf == Buf::Send ? o.owner : o.buf == Buf::Recv ? N + o.owner : 2 * N;
+    r.off = o.byte_off;
+    return r;
+  };
+  size_t oi = 0, ri = 0;
+  for (size_t si = 0; si < S; ++si) {
+    const Step& s = plan.steps[si];
+    steps[si].op0 = static_cast<uint32_t>(oi);
+    steps[si].nops = static_cast<uint32_t>(s.ops.size());
+    steps[si].mode = static_cast<uint32_t>(s.mode == Mode::Copy ? dev::kCopy : dp->rmode);
+    int64_t step_bytes = 0;
+    for (const Op& op : s.ops) {
+      bool aligned = true;
+      dev::OpDesc& d = ops[oi++];
+      d.p0 = static_cast<uint16_t>(ri);
+      for (const Operand& o : op.src) {
+        refs[ri++] = ref_of(o);
+        aligned &= (o.byte_off & 15) == 0;
+        step_bytes += esize(o.dt) * op.n * op.nb;
+      }
+      for (const Operand& o : op.dst) {
+        refs[ri++] = ref_of(o);
+        aligned &= (o.byte_off & 15) == 0;
+        step_bytes += esize(o.dt) * op.n * op.nb;
+      }
+      describe_op(d, op, s.mode, aligned);
+    }
+    const int64_t tiles = assign_tiles(ops + steps[si].op0, s.ops.size(), workers);
+    if (tiles < 0) { dp->why = "too many tiles"; return; }
+    steps[si].ntiles = static_cast<uint32_t>(tiles);
+    dp->max_step_bytes = std::max(dp->max_step_bytes, step_bytes);
+    dp->bytes += step_bytes;
+  }
+  dp->words = static_cast<uint32_t>(words);
+  dp->nops = static_cast<int>(nops);
+  dp->eligible = true;
+}
+
+// The resident description of a plan shape, uploading it at the first call
+// that may (not while `stream` is being captured).  nullptr: not available
+// for this call.
+const DevPlan* resident_plan(int dev, const PlanKey& key, const Plan& plan, int N, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  PlanStore& ps = g_store[dev];
+  auto it = ps.plans.find(key);
+  if (it != ps.plans.end()) return &it->second;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  DevPlan dp;
+  std::vector<uint4> img;
+  build_image(plan, N, plan_cluster(ps) * dev::kPlanSubs, &img, &dp);
+  if (dp.eligible) {
+    const size_t bytes = (img.size() * 16 + 255) / 256 * 256;
+    // another thread's capture in global mode must not see these calls
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    cudaError_t e = cudaSuccess;
+    if (ps.chunk_used + bytes > kPlanArenaChunk) {
+      if (ps.total + kPlanArenaChunk > kPlanArenaMax) {
+        e = cudaErrorMemoryAllocation;
+      } else {
+        void* chunk = nullptr;
+        e = cudaMalloc(&chunk, kPlanArenaChunk);
+        if (e == cudaSuccess) {
+          ps.chunks.push_back(chunk);
+          ps.total += kPlanArenaChunk;
+          ps.chunk_used = 0;
+        }
+      }
+    }
+    if (e == cudaSuccess && !ps.upload) e = cudaStreamCreateWithFlags(&ps.upload, cudaStreamNonBlocking);
+    char* dst = nullptr;
+    if (e == cudaSuccess) {
+      dst = static_cast<char*>(ps.chunks.back()) + ps.chunk_used;
+      e = cudaMemcpyAsync(dst, img.data(), img.size() * 16, cudaMemcpyHostToDevice, ps.upload);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(ps.upload);
+    }
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e == cudaSuccess) {
+      ps.chunk_used += bytes;
+      dp.dptr = reinterpret_cast<const uint4*>(dst);
+    } else {
+      cudaGetLastError();
+      dp.eligible = false;
+      dp.why = "no device memory for the description";
+    }
+  }
+  return &ps.plans.emplace(key, dp).first->second;
+}
+
+vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<const void*>& sends,
+                        const std::vector<void*>& recvs, char* scratch, cudaStream_t stream, const TraceCtx& tc) {
+  dev::PlanParams prm{};
+  prm.plan = dp.dptr;
+  prm.words = dp.words;
+  prm.nbases = static_cast<uint32_t>(2 * N + 1);
+  for (int r = 0; r < N; ++r) {
+    prm.base[r] = sends[r];
+    prm.base[N + r] = recvs[r];
+  }
+  prm.base[2 * N] = scratch;
+  const PlanKernel kernel = plan_kernel_for(dp.rmode, dp.red);
+  int cluster;
+  {
+    std::lock_guard<std::mutex> lk(g_sl_mu);
+    cluster = g_store[dev].cluster;
+  }
+  static std::mutex attr_mu;
+  static std::map<std::pair<int, const void*>, bool> attr_done;
+  {
+    std::lock_guard<std::mutex> lk(attr_mu);
+    auto key = std::make_pair(dev, reinterpret_cast<const void*>(kernel));
+    if (!attr_done[key]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
+      if (e == cudaSuccess && cluster > 8) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+      attr_done[key] = true;
+    }
+  }
+  std::unique_lock<std::mutex> lk(g_trace_mu);
+  const bool trace = g_trace_on;
+  if (!trace) lk.unlock();
+  Pending pend{};
+  if (trace) {
+    cudaError_t e = take_event(&pend.start);
+    if (e == cudaSuccess) e = take_event(&pend.stop);
+    if (e == cudaSuccess) e = cudaEventRecord(pend.start, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event");
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(dev::kPlanThreads);
+  cfg.dynamicSmemBytes = dp.words * 16 + prm.nbases * sizeof(void*);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (trace) {
+    e = cudaEventRecord(pend.stop, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event");
+    pend.rec.coll = tc.coll;
+    pend.rec.algo = tc.algo;
+    pend.rec.step = -1;
+    pend.rec.kernel = dp.rmode | (static_cast<int>(dp.red) << 3) | 128;
+    pend.rec.bytes = dp.bytes;
+    pend.rec.nops = dp.nops;
+    g_trace.push_back(pend);
+  }
+  return VC_SUCCESS;
 }
 
 vc_status_t run(const Call& c) {
@@ -1222,10 +1628,28 @@ vc_status_t run(const Call& c) {
   TraceCtx tc;
   tc.coll = static_cast<int>(c.coll);
   tc.algo = static_cast<int>(pa.algo);
-  for (size_t si = 0; si < plan.steps.size(); ++si) {
-    tc.step = static_cast<int>(si);
-    rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
-    if (rc != VC_SUCCESS) break;
+  // one launch for the whole plan when it is small enough and eligible
+  const DevPlan* dp = nullptr;
+  const size_t limit = single_launch_limit();
+  if (limit > 0 && plan.steps.size() >= 2 && plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
+    bool aligned = (reinterpret_cast<uintptr_t>(scratch) & 15) == 0;
+    for (int r = 0; r < N; ++r)
+      aligned &= (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0 && (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0;
+    if (aligned) {
+      dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
+      if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > limit)) dp = nullptr;
+    }
+  }
+  if (dp) {
+    tc.step = -1;
+    rc = launch_plan(*dp, dev, N, sends, recvs, scratch, c.stream, tc);
+    if (rc == VC_SUCCESS) launches = 1;
+  } else {
+    for (size_t si = 0; si < plan.steps.size(); ++si) {
+      tc.step = static_cast<int>(si);
+      rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
+      if (rc != VC_SUCCESS) break;
+    }
   }
   if (scratch) {
     cudaError_t e = cudaFreeAsync(scratch, c.stream);
@@ -1234,9 +1658,10 @@ vc_status_t run(const Call& c) {
   if (log_enabled()) {
     size_t ops = 0;
     for (const Step& s : plan.steps) ops += s.ops.size();
-    std::fprintf(stderr, "[vc] %s algo=%s nranks=%d count=%lld dtype=%d root=%d steps=%zu ops=%zu launches=%d scratch=%lld\n",
+    std::fprintf(stderr, "[vc] %s algo=%s nranks=%d count=%lld dtype=%d root=%d steps=%zu ops=%zu launches=%d%s scratch=%lld\n",
                  coll_name(c.coll), algo_name(pa.algo), N, static_cast<long long>(c.count), static_cast<int>(c.dt),
-                 c.root, plan.steps.size(), ops, launches, static_cast<long long>(plan.scratch_bytes));
+                 c.root, plan.steps.size(), ops, launches, dp ? " (single launch)" : "",
+                 static_cast<long long>(plan.scratch_bytes));
   }
   return rc;
 }
@@ -1692,6 +2117,19 @@ VC_EXPORT vc_status_t vc_reduce_scatter_noalloc(const void* const* send, void* c
     return run_reduce_scatter_noalloc(send, recv, nranks, static_cast<int64_t>(recvcount), dt,
                                       reinterpret_cast<cudaStream_t>(stream));
   });
+}
+
+VC_EXPORT vc_status_t vc_set_single_launch(size_t max_step_bytes) {
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  g_sl_limit = max_step_bytes;
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_get_single_launch(size_t* max_step_bytes) {
+  if (!max_step_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  *max_step_bytes = g_sl_limit;
+  return VC_SUCCESS;
 }
 
 VC_EXPORT int vc_version(void) { return 100; }

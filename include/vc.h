@@ -323,7 +323,10 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  *   fp16 only), bits 3-4 the op (0 sum, 1 max, 2 min), bit 5 set when the
  *   launch used the large parameter block (more than 16 operations or 64
  *   operand pointers), bit 6 set when an fp32 / int32 launch too small to
- *   fill the GPU took the kernel that loads four sources at a time.
+ *   fill the GPU took the kernel that loads four sources at a time, bit 7
+ *   set for a single-launch plan (vc_set_single_launch: one record for the
+ *   whole call, step -1, bytes and nops of all steps; bits 0-2 then give the
+ *   mode of the plan's reduction steps).
  */
 typedef struct {
   int32_t coll;   /* vc_coll_t */
@@ -337,6 +340,40 @@ typedef struct {
 
 vc_status_t vc_trace_enable(int on);
 vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n_records);
+
+/*
+ * Single-launch execution.
+ *
+ * By default every step of a schedule is one kernel launch and stream order
+ * is the barrier between steps.  A call whose schedule has two or more steps,
+ * each moving at most `max_step_bytes` (algorithmic bytes: every operand of
+ * every operation read or written once), instead runs ALL its steps in one
+ * launch: a single thread-block cluster (16 blocks where the device allows,
+ * else 8) executes the steps in order with a cluster-wide barrier between
+ * consecutive steps.  The operations, their order and every element's
+ * association are unchanged, so results are identical bit for bit; what goes
+ * away is one launch and one grid drain per step, which dominate small
+ * messages.  It applies when, in addition,
+ *   - the schedule's reduction steps share one data type and op (true of
+ *     every schedule of this library),
+ *   - its description fits the kernel's shared memory (96 KB; e.g. the ring
+ *     AllReduce up to about 24 ranks),
+ *   - every buffer pointer of the call is 16-byte aligned,
+ *   - the description is resident on the device.  It is uploaded once per
+ *     call shape (collective, algorithm, ranks, count, type, op, root, in
+ *     place), at the first call that is not being captured into a CUDA graph
+ *     (a capture of a shape not seen before takes the per-step path), into
+ *     at most 64 MB of device memory per device that is kept until the
+ *     process exits; shapes beyond that take the per-step path.
+ *  max_step_bytes: 0 disables single-launch execution, SIZE_MAX applies it
+ *  to every eligible call.  Default VC_SINGLE_LAUNCH_DEFAULT, the measured
+ *  crossover on a GB300 (8 ranks, fp32): at steps of 768 KB or less one
+ *  cluster beats a launch per step over the whole GPU, above it the full
+ *  GPU's bandwidth wins.  Process-wide.
+ */
+#define VC_SINGLE_LAUNCH_DEFAULT ((size_t)768 << 10)
+vc_status_t vc_set_single_launch(size_t max_step_bytes);
+vc_status_t vc_get_single_launch(size_t* max_step_bytes);
 
 /*
  * Ring ReduceScatter that allocates no device memory.

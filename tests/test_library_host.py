@@ -54,6 +54,18 @@ def test_status_strings_and_version():
     assert vc.vc_version() >= 100
 
 
+def test_single_launch_limit_is_settable_without_a_gpu():
+    old = vc.vc_get_single_launch()
+    try:
+        assert old == 768 << 10  # VC_SINGLE_LAUNCH_DEFAULT
+        for v in (0, 1, 4096, vc.SINGLE_LAUNCH_ALWAYS):
+            vc.vc_set_single_launch(v)
+            assert vc.vc_get_single_launch() == v
+        assert vc.lib().vc_get_single_launch(None) == 1  # VC_ERR_INVALID_ARG
+    finally:
+        vc.vc_set_single_launch(old)
+
+
 def test_busbw_factors_match_cost_model():
     for coll in ("allreduce", "reduce_scatter", "allgather", "alltoall", "broadcast", "scatter"):
         for N in (1, 2, 8, 16, 64):
