@@ -112,18 +112,13 @@ template <int OPS, int PTRS>
 struct __align__(16) LaunchParams {
   uint32_t nops;    // operations in use
   uint32_t ntiles;  // tiles of the launch
-  uint32_t nptrs;   // pointers in use
-  uint32_t pad;
+  uint32_t pad[2];
   OpDesc op[OPS];
   const void* ptr[PTRS];
-  static constexpr uint32_t kHeaderBytes = 16;
-  static constexpr uint32_t kPtrOffset = 16 + OPS * sizeof(OpDesc);
 };
 using SmallParams = LaunchParams<16, 64>;
 using LargeParams = LaunchParams<128, 512>;
-static_assert(sizeof(OpDesc) % 16 == 0, "parameter blocks are copied in 16-byte words");
-static_assert(offsetof(SmallParams, ptr) == SmallParams::kPtrOffset, "pointer table offset");
-static_assert(offsetof(LargeParams, ptr) == LargeParams::kPtrOffset, "pointer table offset");
+static_assert(sizeof(OpDesc) % 16 == 0, "plan descriptions are copied in 16-byte words");
 
 // -- memory access --------------------------------------------------------------
 // Per-step launches (COH = false): the sources of a launch are never written
@@ -268,9 +263,12 @@ __device__ __forceinline__ void tile_copy_fanout(const OpDesc& o, const PT& ptr,
   }
 }
 
-template <bool COH, class PT>
+// FAN: the kernel has the bulk-store fan-out path compiled in (launches with
+// a multi-destination copy); without it the copy kernel needs 32 registers
+// instead of 44 and keeps 8 blocks per SM resident instead of 5.
+template <bool COH, bool FAN, class PT>
 __device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
-  if constexpr (!COH) {
+  if constexpr (FAN && !COH) {
     if (o.nd > 1) {
       tile_copy_fanout(o, ptr, run, gbeg, gend);
       return;
@@ -477,9 +475,9 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, i
   }
 }
 
-template <int MODE, int OP, bool COH, int SB, class PT>
+template <int MODE, int OP, bool COH, int SB, bool FAN, class PT>
 __device__ __forceinline__ void tile_vec(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
-  if constexpr (MODE == kCopy) tile_copy<COH>(o, ptr, run, gbeg, gend);
+  if constexpr (MODE == kCopy) tile_copy<COH, FAN>(o, ptr, run, gbeg, gend);
   else if constexpr (MODE == kF32) tile_4b<true, OP, COH, SB>(o, ptr, run, gbeg, gend);
   else if constexpr (MODE == kI32) tile_4b<false, OP, COH, SB>(o, ptr, run, gbeg, gend);
   else if constexpr (MODE == kBF16) tile_half_mixed<false, OP, COH>(o, ptr, run, gbeg, gend);
@@ -561,7 +559,7 @@ __device__ __forceinline__ int64_t group_elems(const OpDesc& o) {
 // a tail after the last whole group).  Launches without them use the kernel
 // compiled without that path: inlined, its registers count against the
 // vector path (58 instead of 46 for fp32), costing a resident block per SM.
-template <int MODE, int OP, bool COH, int SB, bool ELEM, class PT>
+template <int MODE, int OP, bool COH, int SB, bool ELEM, bool FAN, class PT>
 __device__ __forceinline__ void run_tile(const OpDesc& o, const PT& ptr, uint32_t lt) {
   const uint32_t run32 = lt / o.tpr;  // tiles of a launch number below 2^32
   const int64_t run = run32;
@@ -570,7 +568,7 @@ __device__ __forceinline__ void run_tile(const OpDesc& o, const PT& ptr, uint32_
     const int64_t tg = static_cast<int64_t>(o.upt) * kThreads;
     const int64_t gbeg = tr * tg;
     const int64_t gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
-    tile_vec<MODE, OP, COH, SB>(o, ptr, run, gbeg, gend);
+    tile_vec<MODE, OP, COH, SB, FAN>(o, ptr, run, gbeg, gend);
   }
   if constexpr (ELEM) {
     const int64_t soff = run * o.sstride, doff = run * o.dstride;
@@ -597,37 +595,37 @@ __device__ __forceinline__ int find_op(const OpDesc* op, int nops, uint32_t t) {
   return lo;
 }
 
-template <int MODE, int OP, class P, int SB, bool ELEM>
+// One launch of one step.  The operation lookup (a binary search on each
+// operation's first tile) reads a shared-memory copy of the first-tile
+// column, made before waiting on the previous grid; the operations' fields
+// and pointers are read from the parameter block in the constant bank (a
+// shared-memory copy of those measured 5-9% slower on the bf16 ring steps:
+// the per-source loops then wait on a shared-memory load for each source's
+// pointer).  Programmatic dependent launch: this grid may be scheduled while
+// the previous step's grid drains; it lets the next step be scheduled the
+// same way, then waits until the previous grid has completed and its writes
+// are visible before touching the buffers.  Without the launch attribute
+// both are no-ops and stream order applies.
+template <int MODE, int OP, class P, int SB, bool ELEM, bool FAN>
 __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
-  // The parameter block is copied to shared memory first, all of it at once
-  // (operation lookups then cost shared-memory reads instead of a chain of
-  // dependent constant-cache misses).  Programmatic dependent launch: this
-  // grid may be scheduled while the previous step's grid drains; it lets the
-  // next step be scheduled the same way, copies its parameters (which do not
-  // depend on the previous step), then waits until the previous grid has
-  // completed and its writes are visible before touching the buffers.
-  // Without the launch attribute both are no-ops and stream order applies.
-  __shared__ P sp;
+  __shared__ uint32_t s_tile0[sizeof(P::op) / sizeof(OpDesc)];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(&p);
-    uint4* dst = reinterpret_cast<uint4*>(&sp);
-    const uint32_t w0 = (P::kHeaderBytes + p.nops * sizeof(OpDesc)) / 16;
-    for (uint32_t i = threadIdx.x; i < w0; i += kThreads) dst[i] = src[i];
-    constexpr uint32_t pw = P::kPtrOffset / 16;
-    const uint32_t w1 = (p.nptrs * 8 + 15) / 16;
-    for (uint32_t i = threadIdx.x; i < w1; i += kThreads) dst[pw + i] = src[pw + i];
-  }
+  const int nops = static_cast<int>(p.nops);
+  for (int i = threadIdx.x; i < nops; i += kThreads) s_tile0[i] = p.op[i].tile0;
   __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int nops = static_cast<int>(sp.nops);
-  for (uint32_t t = blockIdx.x; t < sp.ntiles; t += gridDim.x) {
-    const OpDesc& o = sp.op[find_op(sp.op, nops, t)];
-    const void* const* ptr = sp.ptr + o.p0;
-    run_tile<MODE, OP, false, SB, ELEM>(o, ptr, t - o.tile0);
+  for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+    int lo = 0, hi = nops - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tile0[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const OpDesc& o = p.op[lo];
+    const void* const* ptr = p.ptr + o.p0;
+    run_tile<MODE, OP, false, SB, ELEM, FAN>(o, ptr, t - o.tile0);
   }
   // outstanding bulk stores of fan-out copies finish before the block exits
-  if (MODE == kCopy && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (FAN && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // -- one-launch plans ------------------------------------------------------------
@@ -702,8 +700,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     for (uint32_t t = first; t < st.ntiles; t += stride) {
       const OpDesc& o = sop[find_op(sop, static_cast<int>(st.nops), t)];
       const RefPtrs ptr{refs + o.p0, sbase};
-      if (st.mode == kCopy) run_tile<kCopy, OP, true, 1, true>(o, ptr, t - o.tile0);
-      else run_tile<RMODE, OP, true, 4, true>(o, ptr, t - o.tile0);
+      if (st.mode == kCopy) run_tile<kCopy, OP, true, 1, true, false>(o, ptr, t - o.tile0);
+      else run_tile<RMODE, OP, true, 4, true, false>(o, ptr, t - o.tile0);
     }
     if (s + 1 < h.nsteps)
       asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -960,7 +958,6 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
   if (tiles < 0) return false;
   p.nops = static_cast<uint32_t>(j - i);
   p.ntiles = static_cast<uint32_t>(tiles);
-  p.nptrs = static_cast<uint32_t>(np);
   *tiles_out = tiles;
   return true;
 }
@@ -970,17 +967,18 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
                          const TraceCtx& tc) {
   static thread_local P p;  // large: keep off the stack
   // tiles are sized against the vector-only kernel's residency
-  auto kernel = dev::step_kernel<MODE, OP, P, 1, false>;
+  auto kernel = dev::step_kernel<MODE, OP, P, 1, false, false>;
   Residency res = residency(st, kernel);
   int64_t cap = int64_t(st->nsm) * res.blocks;
   int64_t tiles = 0;
   if (!fill_params(p, s, i, j, b, cap, &tiles)) return fail(VC_ERR_INVALID_ARG, "operation too large for one launch");
   if (tiles == 0) return VC_SUCCESS;
-  bool elem = false;
+  bool elem = false, fan = false;
   int maxns = 0;
   for (uint32_t k = 0; k < p.nops; ++k) {
     const dev::OpDesc& d = p.op[k];
     elem |= !d.vec || d.groups * group_elements(s.mode, d.esz) < d.n;
+    fan |= MODE == dev::kCopy && d.nd > 1;  // only copies have a fan-out kernel
     maxns = std::max<int>(maxns, d.ns);
   }
   // fp32 / int32: a launch that does not fill the GPU (tiles were shrunk)
@@ -988,10 +986,14 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   bool batched = false;
   if constexpr (MODE == dev::kF32 || MODE == dev::kI32) {
     batched = p.op[0].upt < dev::kUnroll && maxns > 2;
-    if (batched) kernel = elem ? dev::step_kernel<MODE, OP, P, 4, true> : dev::step_kernel<MODE, OP, P, 4, false>;
+    if (batched)
+      kernel = elem ? dev::step_kernel<MODE, OP, P, 4, true, false> : dev::step_kernel<MODE, OP, P, 4, false, false>;
   }
-  if (!batched && elem) kernel = dev::step_kernel<MODE, OP, P, 1, true>;
-  if (batched || elem) {
+  if constexpr (MODE == dev::kCopy) {
+    if (fan) kernel = elem ? dev::step_kernel<MODE, OP, P, 1, true, true> : dev::step_kernel<MODE, OP, P, 1, false, true>;
+  }
+  if (!batched && !fan && elem) kernel = dev::step_kernel<MODE, OP, P, 1, true, false>;
+  if (batched || elem || fan) {
     res = residency(st, kernel);
     cap = int64_t(st->nsm) * res.blocks;
   }
