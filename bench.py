@@ -431,14 +431,17 @@ def time_graph(fn, stream, target_ms=3.0, max_reps=512):
             fn()
     g.replay()
     torch.cuda.synchronize()
+    # median of 7 separately timed replays: one stall on a shared host does not move it
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(torch.cuda.current_stream())
-    for _ in range(3):
+    times = []
+    for _ in range(7):
+        e0.record(torch.cuda.current_stream())
         g.replay()
-    e1.record(torch.cuda.current_stream())
-    torch.cuda.synchronize()
+        e1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / reps)
     del g
-    return e0.elapsed_time(e1) / (3 * reps)
+    return sorted(times)[3]
 
 
 def plan_shape(vc, coll, algo, N, count, dtype="f32", root=0):
