@@ -1524,6 +1524,27 @@ vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<con
   return VC_SUCCESS;
 }
 
+std::mutex g_support_mu;
+std::unordered_map<PlanKey, std::pair<PlanStatus, std::string>, PlanKeyHash> g_support;
+
+PlanStatus supported(const PlanArgs& zero, std::string* why) {
+  const PlanKey key = plan_key(zero);
+  {
+    std::lock_guard<std::mutex> lk(g_support_mu);
+    auto it = g_support.find(key);
+    if (it != g_support.end()) {
+      *why = it->second.second;
+      return it->second.first;
+    }
+  }
+  Plan probe;
+  const PlanStatus ps = build_plan(zero, &probe, why);
+  std::lock_guard<std::mutex> lk(g_support_mu);
+  if (g_support.size() >= 4096) g_support.clear();
+  g_support.emplace(key, std::make_pair(ps, *why));
+  return ps;
+}
+
 vc_status_t run(const Call& c) {
   const int N = c.nranks;
   if (N < 1 || N > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
@@ -1545,11 +1566,12 @@ vc_status_t run(const Call& c) {
   if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
     pa.nchunks = c.nchunks > 0 ? c.nchunks : default_chunks(pa.algo, N, c.count, c.dt, current_cost());
   {
-    Plan probe;
-    std::string why;
+    // support of the algorithm for this collective and rank count, decided
+    // on a zero-size plan (cached: it does not depend on the size)
     PlanArgs zero = pa;
     zero.count = 0;
-    const PlanStatus ps = build_plan(zero, &probe, &why);
+    std::string why;
+    const PlanStatus ps = supported(zero, &why);
     if (ps != PlanStatus::Ok) return plan_status(ps, why);
   }
   if (c.count == 0) return VC_SUCCESS;
