@@ -1,19 +1,12 @@
-// Kernels, launcher and C-ABI of the virtual-rank collectives (sm_103a).
+// Launcher and C ABI of the virtual-rank collectives (host side).
 //
-// Every schedule is executed as its plan (plan.h): one launch per step, each
-// launch running all independent operations of that step.  One kernel
-// template does every step: a persistent grid walks "tiles" (a fixed number
-// of 16-byte groups of one run of one operation); each thread loads its
-// groups from every source with 128-bit loads, adds them in the order the
-// plan lists them (fp32 registers; bf16 widened exactly; int32 wrapping), and
-// stores the result to every destination with 128-bit stores.  Copy steps
-// move raw 16-byte groups; a copy to several destinations stages the tile in
-// shared memory and writes it out with bulk asynchronous (TMA) stores.  Distinct elements are the only thing split across
-// threads, so each element's association is exactly the plan's.
-//
-// Nothing here is a dense contraction: the kernels are HBM-streaming and use
-// no tensor cores.  Kernels never wait on each other or on flags: ordering
-// between steps is stream order.
+// A call becomes a plan (plan.h, cached per call shape).  Its steps run one
+// launch each on the caller's stream (kernels.cuh step_kernel), with the
+// parameter block filled here from the plan and the call's pointers; or, for
+// a small plan, all in one cluster launch of the plan kernel, whose
+// description is uploaded to device memory once per call shape.  Also here:
+// argument checks, the scratch pool, the cost-model selection of
+// VC_ALGO_AUTO, the launch trace, and the C entry points of vc.h.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -31,6 +24,7 @@
 #include <string>
 #include <vector>
 
+#include "kernels.cuh"
 #include "plan.h"
 #include "vc.h"
 
@@ -68,647 +62,7 @@ bool log_enabled() {
 }
 }  // namespace
 
-// ---------------------------------------------------------------------------
-// device code
-// ---------------------------------------------------------------------------
-namespace dev {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 4;           // 16-byte groups per thread per tile (vector path)
-constexpr int kScalarPerThread = 4;  // elements per thread per tile (element path)
-constexpr int kTileGroups = kThreads * kUnroll;
-constexpr int kTileElems = kThreads * kScalarPerThread;
-// A tile is worked by kThreads threads: a whole block of the per-step kernel,
-// or one of the sub-blocks of a one-launch plan's larger blocks.
-__device__ __forceinline__ int lane() { return static_cast<int>(threadIdx.x) & (kThreads - 1); }
-
-// Kernel modes: copy; fp32 / int32 reductions; 16-bit float reductions whose
-// sources mix the data type with fp32 partial sums, or are all of the data
-// type ("P": pure), for bf16 and fp16.
-enum : int { kCopy = 0, kF32 = 1, kI32 = 2, kBF16 = 3, kBF16P = 4, kF16 = 5, kF16P = 6 };
-// Reduction ops.  max / min keep the first operand unless the second is
-// larger / smaller or the first is NaN (so NaN is passed over while a number
-// is present and of +0 / -0 the first seen is kept); int32 compares signed.
-enum : int { kSum = 0, kMax = 1, kMin = 2 };
-
-struct __align__(16) OpDesc {
-  int64_t n;        // elements per run (copy: elements of esz bytes)
-  int64_t nb;       // runs
-  int64_t sstride;  // bytes between runs, sources
-  int64_t dstride;  // bytes between runs, destinations
-  int64_t groups;   // vector path: 16-byte groups per run (fp32 bf16-mode operands: 32 bytes)
-  uint64_t smask;   // bf16 mode: bit s set -> source s is stored as fp32
-  uint64_t dmask;   // bf16 mode: bit d set -> destination d is stored as fp32
-  uint32_t tile0;   // first tile of this operation within the launch
-  uint32_t tpr;     // tiles per run
-  uint16_t p0;      // first pointer (sources, then destinations)
-  uint8_t ns, nd;
-  uint8_t vec;      // 1: vector path
-  uint8_t esz;      // copy: element size in bytes
-  uint8_t upt;      // vector path: groups per thread in one tile (1, 2 or 4)
-};
-
-template <int OPS, int PTRS>
-struct __align__(16) LaunchParams {
-  uint32_t nops;    // operations in use
-  uint32_t ntiles;  // tiles of the launch
-  uint32_t pad[2];
-  OpDesc op[OPS];
-  const void* ptr[PTRS];
-};
-using SmallParams = LaunchParams<16, 64>;
-using LargeParams = LaunchParams<128, 512>;
-static_assert(sizeof(OpDesc) % 16 == 0, "plan descriptions are copied in 16-byte words");
-
-// -- memory access --------------------------------------------------------------
-// Per-step launches (COH = false): the sources of a launch are never written
-// during it, so loads take the non-coherent path and skip L1; stores are
-// streaming (evict-first in L2).  One-launch plans (COH = true) read in a step
-// what other blocks of the cluster wrote in an earlier one: loads go to L2
-// (.cg, never a stale L1 line) after the step barrier, stores are plain.
-__device__ __forceinline__ uint4 ld16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint4 ld16_cg(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
-// Streaming store (evict-first in L2): measured 2-3% faster than a plain
-// store on the write-heavy steps (fused AllReduce / AllToAll, tree levels)
-// and neutral on the ring steps whose outputs the next step reads.
-__device__ __forceinline__ void st16(void* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void st16_wb(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-template <bool COH>
-__device__ __forceinline__ uint4 ldv(const void* p) {
-  if constexpr (COH) return ld16_cg(p);
-  else return ld16(p);
-}
-template <bool COH>
-__device__ __forceinline__ void stv(void* p, uint4 v) {
-  if constexpr (COH) st16_wb(p, v);
-  else st16(p, v);
-}
-
-template <int OP>
-__device__ __forceinline__ float cmb(float a, float b) {
-  if constexpr (OP == kSum) return __fadd_rn(a, b);
-  else if constexpr (OP == kMax) return (b > a || a != a) ? b : a;
-  else return (b < a || a != a) ? b : a;
-}
-template <int OP>
-__device__ __forceinline__ uint32_t cmbi(uint32_t a, uint32_t b) {
-  if constexpr (OP == kSum) return a + b;  // two's-complement wrap-around
-  else if constexpr (OP == kMax) return static_cast<int32_t>(b) > static_cast<int32_t>(a) ? b : a;
-  else return static_cast<int32_t>(b) < static_cast<int32_t>(a) ? b : a;
-}
-
-// 16-bit float formats: widening is exact; narrowing rounds to nearest even.
-template <bool F16>
-__device__ __forceinline__ float widen1(uint16_t h) {
-  if constexpr (F16) return __half2float(__ushort_as_half(h));
-  else return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-template <bool F16>
-__device__ __forceinline__ uint16_t narrow1(float x) {
-  if constexpr (F16) return __half_as_ushort(__float2half_rn(x));
-  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-template <bool F16>
-__device__ __forceinline__ void widen2(uint32_t w, float* f) {
-  if constexpr (F16) {
-    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w));
-    f[0] = v.x;
-    f[1] = v.y;
-  } else {
-    f[0] = __uint_as_float(w << 16);
-    f[1] = __uint_as_float(w & 0xffff0000u);
-  }
-}
-template <bool F16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {  // lo in the low half
-  if constexpr (F16) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  } else {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-}
-template <bool F16>
-__device__ __forceinline__ void widen8(uint4 v, float* f) {
-  widen2<F16>(v.x, f);
-  widen2<F16>(v.y, f + 2);
-  widen2<F16>(v.z, f + 4);
-  widen2<F16>(v.w, f + 6);
-}
-
-// -- vector path -------------------------------------------------------------
-// A tile is the groups [gbeg, gend) of one run of one operation; thread i
-// takes groups gbeg + i, gbeg + i + kThreads, ...  `ptr` is the operation's
-// pointer table (sources, then destinations): an array of addresses, or a
-// table that forms them from buffer bases.
-//
-// Fan-out copies (one source, several destinations: fused AllGather and
-// Broadcast): the tile is loaded into shared memory and thread 0 issues one
-// bulk asynchronous store per destination (cp.async.bulk, the TMA engine),
-// which writes it out in 16 KB bursts.  Measured 3-4.5% faster than eight
-// 128-bit stores per thread on the fused Broadcast and AllGather at 8 x 256
-// MiB; single-destination copies keep the plain path (no gain there).  The
-// next tile's loads are issued before waiting until the previous tile's bulk
-// stores have read the buffer (wait_group.read), so the two overlap; the
-// kernel waits for the stores' completion before it exits.
-template <class PT>
-__device__ __forceinline__ void tile_copy_fanout(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
-                                                 int64_t gend) {
-  __shared__ alignas(128) uint4 stage[kTileGroups];
-  const int ng = static_cast<int>(gend - gbeg);
-  const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride;
-  uint4 v[kUnroll];
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int64_t g = gbeg + u * kThreads + threadIdx.x;
-    if (g < gend) v[u] = ld16(s + g * 16);
-  }
-  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  __syncthreads();
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int64_t g = gbeg + u * kThreads + threadIdx.x;
-    if (g < gend) stage[g - gbeg] = v[u];
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make the tile visible to the bulk copies
-  __syncthreads();
-  if (threadIdx.x == 0 && ng > 0) {
-    const uint32_t saddr = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
-    for (int d = 0; d < o.nd; ++d) {
-      char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + gbeg * 16;
-      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dp), "r"(saddr), "r"(ng * 16)
-                   : "memory");
-    }
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  }
-}
-
-// FAN: the kernel has the bulk-store fan-out path compiled in (launches with
-// a multi-destination copy); without it the copy kernel needs 32 registers
-// instead of 44 and keeps 8 blocks per SM resident instead of 5.
-template <bool COH, bool FAN, class PT>
-__device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
-  if constexpr (FAN && !COH) {
-    if (o.nd > 1) {
-      tile_copy_fanout(o, ptr, run, gbeg, gend);
-      return;
-    }
-  }
-  // slot u of this thread is group gbeg + lane() + u * kThreads; it
-  // exists while u * kThreads < lim
-  const int lim = static_cast<int>(gend - gbeg) - lane();
-  const int64_t off = (gbeg + lane()) * 16;
-  const char* s = static_cast<const char*>(ptr[0]) + run * o.sstride + off;
-  uint4 v[kUnroll];
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u)
-    if (u * kThreads < lim) v[u] = ldv<COH>(s + u * kThreads * 16);
-  for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + off;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, v[u]);
-  }
-}
-
-// fp32 and int32: 4 elements per 16-byte group.  The loads of SB sources are
-// issued together, then combined one after another in source order, so an
-// operation with many sources waits for ceil(ns / SB) memory round trips
-// rather than ns.  SB = 1 (fewest registers, most resident blocks) for
-// launches that fill the GPU; SB = 4 for small launches of many-source
-// operations, where the round trips are the time: measured on 8 ranks, the
-// fused AllReduce of 1 MiB per rank takes 3.6 instead of 5.6 us, while at
-// 256 MiB per rank SB = 4 is 2% slower than SB = 1.
-template <bool FLOAT, int OP, bool COH, int SB, class PT>
-__device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
-  const int lim = static_cast<int>(gend - gbeg) - lane();  // slots as in tile_copy
-  const int64_t soff = run * o.sstride + (gbeg + lane()) * 16;
-  // The first source loads straight into the accumulator (a register copy of
-  // a pending load would stall until it arrives, holding back the next loads).
-  uint4 acc[kUnroll];
-  {
-    const char* s = static_cast<const char*>(ptr[0]) + soff;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) acc[u] = ldv<COH>(s + u * kThreads * 16);
-  }
-  for (int k0 = 1; k0 < o.ns; k0 += SB) {
-    uint4 v[SB][kUnroll];
-#pragma unroll
-    for (int j = 0; j < SB; ++j) {
-      if (k0 + j < o.ns) {
-        const char* s = static_cast<const char*>(ptr[k0 + j]) + soff;
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (u * kThreads < lim) v[j][u] = ldv<COH>(s + u * kThreads * 16);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < SB; ++j) {
-      if (k0 + j < o.ns) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          if (u * kThreads < lim) {
-            const uint4 w = v[j][u];
-            if constexpr (FLOAT) {
-              acc[u].x = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].x), __uint_as_float(w.x)));
-              acc[u].y = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].y), __uint_as_float(w.y)));
-              acc[u].z = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].z), __uint_as_float(w.z)));
-              acc[u].w = __float_as_uint(cmb<OP>(__uint_as_float(acc[u].w), __uint_as_float(w.w)));
-            } else {
-              acc[u].x = cmbi<OP>(acc[u].x, w.x);
-              acc[u].y = cmbi<OP>(acc[u].y, w.y);
-              acc[u].z = cmbi<OP>(acc[u].z, w.z);
-              acc[u].w = cmbi<OP>(acc[u].w, w.w);
-            }
-          }
-        }
-      }
-    }
-  }
-  const int64_t doff = run * o.dstride + (gbeg + lane()) * 16;
-  for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, acc[u]);
-  }
-}
-
-// Adds one loaded group of 8 values to the accumulator (or starts it).
-template <int OP>
-__device__ __forceinline__ void accumulate8(float* acc, const float* f, bool first) {
-  if (first) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = f[i];
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = cmb<OP>(acc[i], f[i]);
-  }
-}
-
-template <bool F16, int U, bool COH, class PT>
-__device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, int64_t run, int64_t g0, int64_t gend,
-                                                float (&acc)[U][8]) {
-  for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
-    const bool f32 = (o.dmask >> d) & 1;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t g = g0 + u * kThreads;
-      if (g < gend) {
-        if (f32) {
-          stv<COH>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
-                                           __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
-          stv<COH>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
-                                                __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
-        } else {
-          stv<COH>(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
-                                           pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
-        }
-      }
-    }
-  }
-}
-
-// 16-bit data with fp32 partial sums among the sources, one source at a time.
-constexpr int kUnrollBF = 2;  // groups per thread per pass
-template <bool F16, int OP, bool COH, class PT>
-__device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
-                                                int64_t gend) {
-  // A tile is covered in passes of kUnrollBF groups per thread.
-#pragma unroll 1
-  for (int pass = 0; pass < kUnroll / kUnrollBF; ++pass) {
-    const int64_t pbeg = gbeg + pass * kUnrollBF * kThreads;
-    if (pbeg >= gend) break;
-    const int64_t g0 = pbeg + lane();
-    float acc[kUnrollBF][8];
-    for (int k = 0; k < o.ns; ++k) {
-      const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
-      const bool f32 = (o.smask >> k) & 1;
-#pragma unroll
-      for (int u = 0; u < kUnrollBF; ++u) {
-        const int64_t g = g0 + u * kThreads;
-        if (g < gend) {
-          float f[8];
-          if (f32) {
-            const uint4 a = ldv<COH>(s + g * 32), b = ldv<COH>(s + g * 32 + 16);
-            f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
-            f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
-          } else {
-            widen8<F16>(ldv<COH>(s + g * 16), f);
-          }
-          accumulate8<OP>(acc[u], f, k == 0);
-        }
-      }
-    }
-    store_half_mode<F16, kUnrollBF, COH>(o, ptr, run, g0, gend, acc);
-  }
-}
-
-// Every source stored in the 16-bit type (fused AllReduce / ReduceScatter,
-// first ring and halving steps): kBatchBP sources' loads are in flight
-// together before they are combined, still one after another in source
-// order.  Measured on the fused bf16 AllReduce at 8 x 128 MiB: 5811 -> 6516
-// GB/s; kept apart from the mixed kernel because its extra registers lower
-// that kernel's occupancy.
-constexpr int kUnrollBP = 4;
-constexpr int kBatchBP = 2;
-template <bool F16, int OP, bool COH, class PT>
-__device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
-                                               int64_t gend) {
-#pragma unroll 1
-  for (int pass = 0; pass < kUnroll / kUnrollBP; ++pass) {
-    const int64_t pbeg = gbeg + pass * kUnrollBP * kThreads;
-    if (pbeg >= gend) break;
-    const int64_t g0 = pbeg + lane();
-    float acc[kUnrollBP][8];
-    for (int k = 0; k < o.ns; k += kBatchBP) {
-      uint4 raw[kBatchBP][kUnrollBP];
-#pragma unroll
-      for (int j = 0; j < kBatchBP; ++j) {
-        if (k + j < o.ns) {
-          const char* s = static_cast<const char*>(ptr[k + j]) + run * o.sstride;
-#pragma unroll
-          for (int u = 0; u < kUnrollBP; ++u) {
-            const int64_t g = g0 + u * kThreads;
-            if (g < gend) raw[j][u] = ldv<COH>(s + g * 16);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kBatchBP; ++j) {
-        if (k + j < o.ns) {
-#pragma unroll
-          for (int u = 0; u < kUnrollBP; ++u) {
-            const int64_t g = g0 + u * kThreads;
-            if (g < gend) {
-              float f[8];
-              widen8<F16>(raw[j][u], f);
-              accumulate8<OP>(acc[u], f, k + j == 0);
-            }
-          }
-        }
-      }
-    }
-    store_half_mode<F16, kUnrollBP, COH>(o, ptr, run, g0, gend, acc);
-  }
-}
-
-template <int MODE, int OP, bool COH, int SB, bool FAN, class PT>
-__device__ __forceinline__ void tile_vec(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
-  if constexpr (MODE == kCopy) tile_copy<COH, FAN>(o, ptr, run, gbeg, gend);
-  else if constexpr (MODE == kF32) tile_4b<true, OP, COH, SB>(o, ptr, run, gbeg, gend);
-  else if constexpr (MODE == kI32) tile_4b<false, OP, COH, SB>(o, ptr, run, gbeg, gend);
-  else if constexpr (MODE == kBF16) tile_half_mixed<false, OP, COH>(o, ptr, run, gbeg, gend);
-  else if constexpr (MODE == kF16) tile_half_mixed<true, OP, COH>(o, ptr, run, gbeg, gend);
-  else if constexpr (MODE == kBF16P) tile_half_pure<false, OP, COH>(o, ptr, run, gbeg, gend);
-  else tile_half_pure<true, OP, COH>(o, ptr, run, gbeg, gend);
-}
-
-// -- element path (unaligned operands and the tails of vector runs) ---------
-// Scalar loads: plain, or through L2 (.cg) for one-launch plans (see ldv).
-template <bool COH>
-__device__ __forceinline__ uint32_t ld32(const void* p) {
-  if constexpr (COH) {
-    uint32_t v;
-    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-  } else {
-    return *static_cast<const uint32_t*>(p);
-  }
-}
-template <bool COH>
-__device__ __forceinline__ uint16_t ld16b(const void* p) {
-  if constexpr (COH) {
-    uint16_t v;
-    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
-    return v;
-  } else {
-    return *static_cast<const uint16_t*>(p);
-  }
-}
-
-template <int MODE, int OP, bool COH, class PT>
-__device__ __forceinline__ void elem(const OpDesc& o, const PT& ptr, int64_t soff, int64_t doff, int64_t e) {
-  if constexpr (MODE == kCopy) {
-    const char* s = static_cast<const char*>(ptr[0]) + soff + e * o.esz;
-    if (o.esz == 2) {
-      const uint16_t v = ld16b<COH>(s);
-      for (int d = 0; d < o.nd; ++d)
-        *reinterpret_cast<uint16_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 2) = v;
-    } else {
-      const uint32_t v = ld32<COH>(s);
-      for (int d = 0; d < o.nd; ++d)
-        *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = v;
-    }
-  } else if constexpr (MODE == kF32) {
-    float acc = __uint_as_float(ld32<COH>(static_cast<const char*>(ptr[0]) + soff + e * 4));
-    for (int k = 1; k < o.ns; ++k)
-      acc = cmb<OP>(acc, __uint_as_float(ld32<COH>(static_cast<const char*>(ptr[k]) + soff + e * 4)));
-    for (int d = 0; d < o.nd; ++d)
-      *reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
-  } else if constexpr (MODE == kI32) {
-    uint32_t acc = ld32<COH>(static_cast<const char*>(ptr[0]) + soff + e * 4);
-    for (int k = 1; k < o.ns; ++k) acc = cmbi<OP>(acc, ld32<COH>(static_cast<const char*>(ptr[k]) + soff + e * 4));
-    for (int d = 0; d < o.nd; ++d)
-      *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff + e * 4) = acc;
-  } else {
-    constexpr bool F16 = MODE == kF16 || MODE == kF16P;
-    float acc = 0.f;
-    for (int k = 0; k < o.ns; ++k) {
-      const char* s = static_cast<const char*>(ptr[k]) + soff;
-      const float v = ((o.smask >> k) & 1) ? __uint_as_float(ld32<COH>(s + e * 4)) : widen1<F16>(ld16b<COH>(s + e * 2));
-      acc = k == 0 ? v : cmb<OP>(acc, v);
-    }
-    for (int d = 0; d < o.nd; ++d) {
-      char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
-      if ((o.dmask >> d) & 1) *reinterpret_cast<float*>(dp + e * 4) = acc;
-      else *reinterpret_cast<uint16_t*>(dp + e * 2) = narrow1<F16>(acc);
-    }
-  }
-}
-
-template <int MODE>
-__device__ __forceinline__ int64_t group_elems(const OpDesc& o) {
-  return MODE == kCopy ? 16 / o.esz : (MODE == kF32 || MODE == kI32 ? 4 : 8);
-}
-
-// Tile lt of operation o (tiles of one operation are numbered run by run).
-// ELEM: the launch has operations that take the element path (unaligned, or
-// a tail after the last whole group).  Launches without them use the kernel
-// compiled without that path: inlined, its registers count against the
-// vector path (58 instead of 46 for fp32), costing a resident block per SM.
-template <int MODE, int OP, bool COH, int SB, bool ELEM, bool FAN, class PT>
-__device__ __forceinline__ void run_tile(const OpDesc& o, const PT& ptr, uint32_t lt) {
-  const uint32_t run32 = lt / o.tpr;  // tiles of a launch number below 2^32
-  const int64_t run = run32;
-  const int64_t tr = lt - run32 * o.tpr;
-  if (!ELEM || o.vec) {
-    const int64_t tg = static_cast<int64_t>(o.upt) * kThreads;
-    const int64_t gbeg = tr * tg;
-    const int64_t gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
-    tile_vec<MODE, OP, COH, SB, FAN>(o, ptr, run, gbeg, gend);
-  }
-  if constexpr (ELEM) {
-    const int64_t soff = run * o.sstride, doff = run * o.dstride;
-    if (o.vec) {
-      if (tr == o.tpr - 1) {  // elements after the last whole group (single-run operations only)
-        for (int64_t e = o.groups * group_elems<MODE>(o) + lane(); e < o.n; e += kThreads)
-          elem<MODE, OP, COH>(o, ptr, soff, doff, e);
-      }
-    } else {
-      const int64_t e0 = tr * kTileElems;
-      const int64_t e1 = e0 + kTileElems < o.n ? e0 + kTileElems : o.n;
-      for (int64_t e = e0 + lane(); e < e1; e += kThreads) elem<MODE, OP, COH>(o, ptr, soff, doff, e);
-    }
-  }
-}
-
-// The operation holding tile t: the last of op[0, nops) whose tile0 <= t.
-__device__ __forceinline__ int find_op(const OpDesc* op, int nops, uint32_t t) {
-  int lo = 0, hi = nops - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (op[mid].tile0 <= t) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-// One launch of one step.  The operation lookup (a binary search on each
-// operation's first tile) reads a shared-memory copy of the first-tile
-// column, made before waiting on the previous grid; the operations' fields
-// and pointers are read from the parameter block in the constant bank (a
-// shared-memory copy of those measured 5-9% slower on the bf16 ring steps:
-// the per-source loops then wait on a shared-memory load for each source's
-// pointer).  Programmatic dependent launch: this grid may be scheduled while
-// the previous step's grid drains; it lets the next step be scheduled the
-// same way, then waits until the previous grid has completed and its writes
-// are visible before touching the buffers.  Without the launch attribute
-// both are no-ops and stream order applies.
-template <int MODE, int OP, class P, int SB, bool ELEM, bool FAN>
-__global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
-  __shared__ uint32_t s_tile0[sizeof(P::op) / sizeof(OpDesc)];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int nops = static_cast<int>(p.nops);
-  for (int i = threadIdx.x; i < nops; i += kThreads) s_tile0[i] = p.op[i].tile0;
-  __syncthreads();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-    int lo = 0, hi = nops - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_tile0[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const OpDesc& o = p.op[lo];
-    const void* const* ptr = p.ptr + o.p0;
-    run_tile<MODE, OP, false, SB, ELEM, FAN>(o, ptr, t - o.tile0);
-  }
-  // outstanding bulk stores of fan-out copies finish before the block exits
-  if (FAN && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// -- one-launch plans ------------------------------------------------------------
-// A plan can run as one launch of one thread-block cluster: the blocks walk
-// the tiles of step 0, meet at a cluster barrier (release / acquire: every
-// write of the step is visible to every block before any block starts the
-// next), walk step 1, and so on.  The operations, their order and each
-// element's association are those of the per-step launches; only the launch
-// and grid drain between steps are gone.  The plan's description lives in
-// device memory (written once per plan shape): a header, the steps, the
-// operations (tile numbers relative to their step, pointer indices into the
-// operand table) and the operand table, whose entries name a buffer base
-// (send r, recv r, scratch) and a byte offset.  The call passes only the
-// bases.  Every block copies the description and the bases to shared memory
-// before waiting on the previous grid, so the lookups of the step walk are
-// shared-memory reads.
-struct __align__(16) PlanHeader {
-  uint32_t nsteps, nops, nrefs, pad;
-};
-struct __align__(16) PlanStep {
-  uint32_t op0;     // first operation of the step
-  uint32_t nops;    // its operations
-  uint32_t ntiles;  // its tiles
-  uint32_t mode;    // kCopy or the plan's reduction mode
-};
-struct __align__(16) OperandRef {
-  uint32_t base;  // index into the bases: send r = r, recv r = N + r, scratch = 2N
-  uint32_t pad;
-  int64_t off;    // bytes from the base
-};
-struct RefPtrs {
-  const OperandRef* ref;
-  const void* const* base;
-  __device__ __forceinline__ const void* operator[](int k) const {
-    return static_cast<const char*>(base[ref[k].base]) + ref[k].off;
-  }
-};
-struct __align__(16) PlanParams {
-  const uint4* plan;  // the description, 16-byte words
-  uint32_t words;
-  uint32_t nbases;
-  const void* base[2 * VC_MAX_RANKS + 1];
-};
-
-// Blocks of kPlanSubs sub-blocks of kThreads threads; each sub-block walks
-// its own tiles (tile functions index by lane()).  Measured on 8 ranks: two
-// sub-blocks double the bandwidth of mid-size plans (16 MB per rank ring:
-// 962 -> 599 us) but add about 0.2 us per step to small ones (1 KB ring:
-// 18.0 -> 20.9 us), and single launches are only chosen for small ones.
-constexpr int kPlanSubs = 1;
-constexpr int kPlanThreads = kThreads * kPlanSubs;
-
-template <int RMODE, int OP>
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
-  extern __shared__ uint4 sm[];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (uint32_t i = threadIdx.x; i < p.words; i += kPlanThreads) sm[i] = ld16(p.plan + i);
-  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
-  for (uint32_t i = threadIdx.x; i < p.nbases; i += kPlanThreads) sbase[i] = p.base[i];
-  __syncthreads();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
-  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
-  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
-  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
-  // Every block runs every iteration of this loop (the step count is the
-  // same for all), so each meets each barrier exactly once.
-  for (uint32_t s = 0; s < h.nsteps; ++s) {
-    const PlanStep st = steps[s];
-    const OpDesc* sop = ops + st.op0;
-    const uint32_t first = blockIdx.x * kPlanSubs + threadIdx.x / kThreads, stride = gridDim.x * kPlanSubs;
-    for (uint32_t t = first; t < st.ntiles; t += stride) {
-      const OpDesc& o = sop[find_op(sop, static_cast<int>(st.nops), t)];
-      const RefPtrs ptr{refs + o.p0, sbase};
-      if (st.mode == kCopy) run_tile<kCopy, OP, true, 1, true, false>(o, ptr, t - o.tile0);
-      else run_tile<RMODE, OP, true, 4, true, false>(o, ptr, t - o.tile0);
-    }
-    if (s + 1 < h.nsteps)
-      asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-  }
-}
-
-}  // namespace dev
 
 // ---------------------------------------------------------------------------
 // per-device state: SM count, occupancy, scratch pool
