@@ -69,17 +69,13 @@ bool log_enabled() {
 // ---------------------------------------------------------------------------
 namespace {
 
-// Blocks of one kernel resident per SM, and the dynamic shared memory each
-// launch requests to hold it there (0: the kernel's own limit applies).
+// Blocks of one kernel resident per SM.
 struct Residency {
   int blocks = 1;
-  int dyn_smem = 0;
 };
 struct DeviceState {
   bool init = false;
   int nsm = 0;
-  int smem_per_sm = 0;     // shared memory per SM
-  int smem_reserved = 0;   // reserved by the system per block
   cudaMemPool_t pool = nullptr;
   std::map<const void*, Residency> occupancy;
 };
@@ -95,10 +91,6 @@ vc_status_t device_state(DeviceState** out, int* dev_out) {
   DeviceState& st = g_dev[dev];
   if (!st.init) {
     e = cudaDeviceGetAttribute(&st.nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = cudaDeviceGetAttribute(&st.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     st.init = true;
   }
@@ -126,23 +118,9 @@ vc_status_t scratch_pool(DeviceState* st, int dev, cudaMemPool_t* pool) {
   return VC_SUCCESS;
 }
 
-// VC_BLOCKS_PER_SM=k holds every kernel at k resident blocks per SM (tuning;
-// 0 or unset: each kernel's own limit).
-int blocks_env() {
-  static const int k = [] {
-    const char* v = std::getenv("VC_BLOCKS_PER_SM");
-    return v ? std::atoi(v) : 0;
-  }();
-  return k;
-}
-
-// Residency of a kernel: its occupancy limit, or `want` blocks per SM when
-// that is lower.  A lower count is enforced, not just asked for: each block
-// requests enough dynamic shared memory that no more than `want` fit on an
-// SM, so the grid (SMs x blocks) lands evenly instead of five blocks on some
-// SMs and three on others.
+// Resident blocks per SM of a kernel (its occupancy limit), queried once.
 template <class K>
-Residency residency(DeviceState* st, K kernel, int want = 0) {
+Residency residency(DeviceState* st, K kernel) {
   std::lock_guard<std::mutex> lk(g_mu);
   const void* key = reinterpret_cast<const void*>(kernel);
   auto it = st->occupancy.find(key);
@@ -151,19 +129,6 @@ Residency residency(DeviceState* st, K kernel, int want = 0) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, dev::kThreads, 0) != cudaSuccess || n < 1) n = 1;
   r.blocks = n;
-  if (blocks_env() > 0) want = blocks_env();
-  cudaFuncAttributes fa{};
-  if (want > 0 && want < n && cudaFuncGetAttributes(&fa, kernel) == cudaSuccess) {
-    const int per_block = st->smem_per_sm / want - st->smem_reserved - static_cast<int>(fa.sharedSizeBytes);
-    const int dyn = (per_block - 128) / 128 * 128;
-    int m = 0;
-    if (dyn > 0 && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m, kernel, dev::kThreads, dyn) == cudaSuccess && m == want) {
-      r.blocks = want;
-      r.dyn_smem = dyn;
-    }
-    cudaGetLastError();
-  }
   st->occupancy[key] = r;
   return r;
 }
@@ -365,7 +330,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(dev::kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(res.dyn_smem);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
