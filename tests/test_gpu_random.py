@@ -1,0 +1,149 @@
+"""Randomised GPU parity sweep through the C ABI.
+
+1000 calls drawn from one seeded generator: collective, schedule, rank count
+(1-16), element count (log-uniform 1..5000, so odd sizes and ragged tails;
+one in ten 5000..100000 for several tiles per operation),
+data type, reduction op, root, in place or not, 16-byte aligned or not, and
+the execution form (default, forced single launch, one launch per step).
+Each must equal the oracle's simulation of the same schedule bit for bit,
+with the canary bands around every buffer intact.  Shapes a schedule does
+not define (the library and the oracle both refuse them) are skipped.
+"""
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_algorithms_virtual_gb300 as vc
+from oracle import schedules
+from synthetic_inputs import int32_bits, rank_buffers
+
+from .gpu_util import Guarded, first_diff, same_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+REDUCTIONS = ("allreduce", "reduce_scatter", "reduce")
+COLLS = ("allreduce", "reduce_scatter", "allgather", "broadcast", "scatter", "alltoall", "gather", "reduce",
+         "pipelined")
+ALGOS = dict(schedules.ALGOS, gather=schedules.ALGOS_EXTRA["gather"], reduce=schedules.ALGOS_EXTRA["reduce"],
+             pipelined=("pipe_chain", "pipe_tree"))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from collective_communication_algorithms_virtual_gb300 import build
+
+    build.build()
+    vc.lib()
+    old = vc.vc_get_single_launch()
+    yield
+    vc.vc_set_single_launch(old)
+
+
+def _inputs(dtype, seed, N, n):
+    if dtype == "f16":
+        return [(x * 4).astype(np.float16) for x in rank_buffers("uniform_f32", seed, N, n)]
+    if dtype == "i32":
+        return [int32_bits(seed, r, n) for r in range(N)]
+    return rank_buffers({"f32": "uniform_f32", "bf16": "normal_bf16"}[dtype], seed, N, n)
+
+
+def _case(rng):
+    coll = COLLS[rng.integers(len(COLLS))]
+    algo = ALGOS[coll][rng.integers(len(ALGOS[coll]))]
+    N = int(rng.integers(1, 17))
+    if rng.uniform() < 0.1:  # several tiles per operation, per-step launches by default
+        count = int(rng.integers(5000, 100000))
+        if coll in ("reduce_scatter", "alltoall", "scatter", "allgather", "gather"):
+            count = max(1, count // N)
+    else:
+        count = int(np.exp(rng.uniform(0, np.log(5000))))
+    dtype = ("f32", "bf16", "i32", "f16")[rng.integers(4)]
+    op = ("sum", "max", "min")[rng.integers(3)] if coll in REDUCTIONS else "sum"
+    root = int(rng.integers(N))
+    inplace = bool(rng.integers(2)) and coll in ("allreduce", "broadcast", "reduce")
+    shift = int(rng.integers(2))
+    form = ("default", "single", "per_step")[rng.integers(3)]
+    nchunks = int(rng.integers(1, 6))
+    return coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks
+
+
+def _run(i, coll, algo, N, count, dtype, op, root, inplace, shift, nchunks):
+    """Runs the call on the GPU; returns (got, want) lists of host arrays."""
+    seed = 9000 + i
+    G = lambda n, fill=None: Guarded(n, dtype, shift, fill=fill)
+    guards = []
+    if coll in ("allreduce", "reduce_scatter", "allgather", "alltoall", "gather", "reduce"):
+        n_in = count * N if coll in ("reduce_scatter", "alltoall") else count
+        xs = _inputs(dtype, seed, N, n_in)
+        sends = [G(n_in, x) for x in xs]
+        guards += sends
+        if coll == "allreduce":
+            want = schedules.allreduce(xs, algo, dtype, inplace=inplace, op=op).outputs
+            recvs = sends if inplace else [G(count) for _ in range(N)]
+            vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo, op=op)
+        elif coll == "reduce_scatter":
+            want = schedules.reduce_scatter(xs, algo, dtype, op=op).outputs
+            recvs = [G(count) for _ in range(N)]
+            vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo=algo, op=op)
+        elif coll == "allgather":
+            want = schedules.allgather(xs, algo, dtype).outputs
+            recvs = [G(count * N) for _ in range(N)]
+            vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo)
+        elif coll == "alltoall":
+            want = schedules.alltoall(xs, algo, dtype).outputs
+            recvs = [G(count * N) for _ in range(N)]
+            vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo=algo)
+        elif coll == "gather":
+            want = [schedules.gather(xs, root, algo, dtype).outputs[0]]
+            recvs = [G(count * N)]
+            vc.vc_gather([g.t for g in sends], recvs[0].t, root=root, algo=algo)
+        else:
+            want = [schedules.reduce(xs, root, algo, dtype, inplace=inplace, op=op).outputs[0]]
+            recvs = [sends[root]] if inplace else [G(count)]
+            vc.vc_reduce([g.t for g in sends], recvs[0].t, root=root, algo=algo, op=op)
+    else:
+        n_in = count * N if coll == "scatter" else count
+        A = _inputs(dtype, seed, 1, n_in)[0]
+        recvs = [G(count) for _ in range(N)]
+        if inplace:
+            recvs[root].t.copy_(to_dev(A))
+            src = recvs[root]
+        else:
+            src = G(n_in, A)
+            guards.append(src)
+        if coll == "broadcast":
+            want = schedules.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
+            vc.vc_broadcast(src.t, [g.t for g in recvs], root=root, algo=algo)
+        elif coll == "scatter":
+            want = schedules.scatter(A, N, root, algo, dtype).outputs
+            vc.vc_scatter(src.t, [g.t for g in recvs], root=root, algo=algo)
+        else:
+            want = schedules.broadcast_pipelined(A, N, root, algo, dtype, nchunks, inplace=inplace).outputs
+            vc.vc_broadcast_pipelined(src.t, [g.t for g in recvs], root=root, algo=algo, nchunks=nchunks)
+    torch.cuda.synchronize()
+    assert all(g.guards_intact() for g in guards + recvs), "canary band overwritten"
+    return [g.host() for g in recvs], want
+
+
+def test_random_calls_match_oracle():
+    rng = np.random.default_rng(20261202)
+    ran = 0
+    for i in range(1000):
+        coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks = _case(rng)
+        vc.vc_set_single_launch({"default": 768 << 10, "single": vc.SINGLE_LAUNCH_ALWAYS, "per_step": 0}[form])
+        what = (i, coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks)
+        try:
+            got, want = _run(i, coll, algo, N, count, dtype, op, root, inplace, shift, nchunks)
+        except schedules.Unsupported:
+            # the oracle runs first: a shape it does not define is not sent to the
+            # library, which must refuse it as well
+            with pytest.raises(vc.VCError):
+                vc.vc_plan_describe("broadcast" if coll == "pipelined" else coll, algo, N, count, dtype, root,
+                                    nchunks=nchunks, op=op)
+            continue
+        ran += 1
+        for r in range(len(want)):
+            assert same_bits(got[r], want[r]), (what, r, first_diff(got[r], want[r]))
+    assert ran >= 900, ran
