@@ -297,7 +297,8 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   for (uint32_t k = 0; k < p.nops; ++k) {
     const dev::OpDesc& d = p.op[k];
     elem |= !d.vec || d.groups * group_elements(s.mode, d.esz) < d.n;
-    fan |= MODE == dev::kCopy && d.nd > 1;  // only copies have a fan-out kernel
+    // multi-destination operations: bulk-store kernels for copies and fp32 / int32 sums
+    fan |= (MODE == dev::kCopy || MODE == dev::kF32 || MODE == dev::kI32) && d.nd > 1;
     maxns = std::max<int>(maxns, d.ns);
   }
   // fp32 / int32: a launch that does not fill the GPU (tiles were shrunk)
@@ -308,8 +309,9 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
     if (batched)
       kernel = elem ? dev::step_kernel<MODE, OP, P, 4, true, false> : dev::step_kernel<MODE, OP, P, 4, false, false>;
   }
-  if constexpr (MODE == dev::kCopy) {
-    if (fan) kernel = elem ? dev::step_kernel<MODE, OP, P, 1, true, true> : dev::step_kernel<MODE, OP, P, 1, false, true>;
+  if constexpr (MODE == dev::kCopy || MODE == dev::kF32 || MODE == dev::kI32) {
+    if (fan && !batched)
+      kernel = elem ? dev::step_kernel<MODE, OP, P, 1, true, true> : dev::step_kernel<MODE, OP, P, 1, false, true>;
   }
   if (!batched && !fan && elem) kernel = dev::step_kernel<MODE, OP, P, 1, true, false>;
   if (batched || elem || fan) {
