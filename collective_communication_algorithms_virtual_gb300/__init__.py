@@ -24,7 +24,6 @@ from .binding import (  # noqa: F401
     vc_busbw_factor,
     vc_last_error,
     vc_plan_describe,
-    vc_flow_describe,
     vc_reduce_scatter,
     vc_scatter,
     vc_select_algo,

@@ -55,12 +55,6 @@ class PlanEntry(ctypes.Structure):
                 ("n", ctypes.c_int64), ("nb", ctypes.c_int64), ("stride_bytes", ctypes.c_int64)]
 
 
-class FlowTile(ctypes.Structure):
-    _fields_ = [("step", ctypes.c_int32), ("op", ctypes.c_int32), ("run", ctypes.c_int64),
-                ("e0", ctypes.c_int64), ("e1", ctypes.c_int64), ("dep_begin", ctypes.c_uint32),
-                ("dep_end", ctypes.c_uint32)]
-
-
 _lib = None
 
 
@@ -106,9 +100,6 @@ def lib() -> ctypes.CDLL:
         L.vc_get_cost_model.restype = I
         L.vc_select_algo.argtypes = [I, I, Z, I, I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
         L.vc_select_algo.restype = I
-        L.vc_flow_describe.argtypes = [I, I, I, Z, I, I, I, I, I, I, ctypes.POINTER(FlowTile), Z,
-                                       ctypes.POINTER(Z), ctypes.POINTER(ctypes.c_uint32), Z, ctypes.POINTER(Z)]
-        L.vc_flow_describe.restype = I
         L.vc_set_single_launch.argtypes = [Z]
         L.vc_set_single_launch.restype = I
         L.vc_get_single_launch.argtypes = [ctypes.POINTER(Z)]
@@ -320,21 +311,6 @@ def vc_trace_read(capacity: int = 1 << 20) -> list:
         out.append({"coll": r.coll, "algo": r.algo, "step": r.step, "kernel": kernel_name(r.kernel),
                     "bytes": r.bytes, "nops": r.nops, "ms": r.ms})
     return out
-
-
-def vc_flow_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,
-                     nchunks: int = 0, op="sum", workers: int = 760):
-    """The call's tiles and the earlier tiles each must follow, as (tiles, deps);
-    host only, needs no GPU."""
-    L = lib()
-    nt, nd = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    args = (_code(COLLS, coll), _code(ALGOS, algo), int(nranks), int(count), _code(DTYPES, dtype),
-            _code(OPS, op), int(root), int(bool(inplace)), int(nchunks), int(workers))
-    check(L.vc_flow_describe(*args, None, 0, ctypes.byref(nt), None, 0, ctypes.byref(nd)))
-    tiles = (FlowTile * max(1, nt.value))()
-    deps = (ctypes.c_uint32 * max(1, nd.value))()
-    check(L.vc_flow_describe(*args, tiles, nt.value, ctypes.byref(nt), deps, nd.value, ctypes.byref(nd)))
-    return list(tiles[:nt.value]), list(deps[:nd.value])
 
 
 def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,

@@ -845,197 +845,6 @@ vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<con
   return VC_SUCCESS;
 }
 
-// ---------------------------------------------------------------------------
-// dataflow plans (host side): every tile of every step, with the tiles of
-// earlier steps it must wait for
-// ---------------------------------------------------------------------------
-// A tile depends on an earlier tile when they touch the same bytes and one of
-// them writes: it reads what the other wrote (read after write), writes what
-// the other read (write after read) or writes what the other wrote (write
-// after write).  Tracked per buffer (send r, recv r, scratch; a receive
-// buffer that is its rank's send buffer, in place, is the same buffer) and
-// byte range: the last tile that wrote the range and the tiles that read it
-// since.  Tiles of one step never conflict (the plans' contract), so each
-// step's dependencies are taken against the state after the previous step.
-class RangeState {
- public:
-  void deps_read(int64_t lo, int64_t hi, std::vector<uint32_t>* out) const {
-    visit(lo, hi, [&](const Seg& s) {
-      if (s.writer >= 0) out->push_back(static_cast<uint32_t>(s.writer));
-    });
-  }
-  void deps_write(int64_t lo, int64_t hi, std::vector<uint32_t>* out) const {
-    visit(lo, hi, [&](const Seg& s) {
-      if (s.writer >= 0) out->push_back(static_cast<uint32_t>(s.writer));
-      out->insert(out->end(), s.readers.begin(), s.readers.end());
-    });
-  }
-  void record_read(int64_t lo, int64_t hi, uint32_t t) {
-    span(lo, hi, [&](Seg& s) { s.readers.push_back(t); });
-  }
-  void record_write(int64_t lo, int64_t hi, uint32_t t) {
-    span(lo, hi, [&](Seg& s) {
-      s.writer = static_cast<int32_t>(t);
-      s.readers.clear();
-    });
-  }
-
- private:
-  struct Seg {
-    int64_t end = 0;
-    int32_t writer = -1;
-    std::vector<uint32_t> readers;
-  };
-  std::map<int64_t, Seg> m_;  // start -> segment; segments do not overlap
-
-  template <class F>
-  void visit(int64_t lo, int64_t hi, F f) const {
-    if (lo >= hi) return;
-    auto it = m_.upper_bound(lo);
-    if (it != m_.begin()) --it;
-    for (; it != m_.end() && it->first < hi; ++it)
-      if (it->second.end > lo) f(it->second);
-  }
-  // the segment boundary at pos exists (no segment straddles it)
-  void cut(int64_t pos) {
-    auto it = m_.upper_bound(pos);
-    if (it == m_.begin()) return;
-    --it;
-    if (it->first < pos && pos < it->second.end) {
-      Seg right = it->second;
-      it->second.end = pos;
-      m_.emplace(pos, std::move(right));
-    }
-  }
-  // applies f to segments exactly covering [lo, hi), creating empty ones in gaps
-  template <class F>
-  void span(int64_t lo, int64_t hi, F f) {
-    if (lo >= hi) return;
-    cut(lo);
-    cut(hi);
-    int64_t pos = lo;
-    auto it = m_.lower_bound(lo);
-    while (pos < hi) {
-      if (it == m_.end() || it->first > pos) {
-        const int64_t gap_end = it == m_.end() ? hi : std::min(hi, it->first);
-        Seg s;
-        s.end = gap_end;
-        it = m_.emplace_hint(it, pos, std::move(s));
-      }
-      f(it->second);
-      pos = it->second.end;
-      ++it;
-    }
-  }
-};
-
-struct FlowTile {
-  uint32_t step, op;  // op: index within the step
-  int64_t run, e0, e1;  // elements [e0, e1) of run `run` of the operation
-};
-struct FlowGraph {
-  bool ok = false;
-  const char* why = "";
-  std::vector<dev::OpDesc> ops;        // every step's operations; tile0 relative to the step
-  std::vector<uint32_t> step_op0;      // first operation of each step
-  std::vector<uint32_t> step_tile0;    // first global tile of each step (nsteps + 1 entries)
-  std::vector<FlowTile> tiles;
-  std::vector<uint32_t> dep_off, dep;  // dependencies of tile t: dep[dep_off[t] .. dep_off[t + 1])
-};
-constexpr int64_t kFlowMaxTiles = 1 << 16;
-
-// `alias`: bit r set when rank r's receive buffer is its send buffer (in
-// place).  Tiles are sized for `workers` concurrent tile walkers, as for a
-// per-step launch of that many blocks.
-void build_flow(const Plan& plan, int N, uint64_t alias, int64_t workers, FlowGraph* g) {
-  g->ok = false;
-  const int nbase = 2 * N + 1;
-  auto base_of = [&](const Operand& o) {
-    if (o.buf == Buf::Send) return o.owner;
-    if (o.buf == Buf::Recv) return ((alias >> o.owner) & 1) ? o.owner : N + o.owner;
-    return 2 * N;
-  };
-  // operations and tiling, step by step
-  uint32_t tile_base = 0;
-  for (const Step& s : plan.steps) {
-    g->step_op0.push_back(static_cast<uint32_t>(g->ops.size()));
-    g->step_tile0.push_back(tile_base);
-    const size_t first = g->ops.size();
-    for (const Op& op : s.ops) {
-      bool aligned = true;
-      for (const Operand& o : op.src) aligned &= (o.byte_off & 15) == 0;
-      for (const Operand& o : op.dst) aligned &= (o.byte_off & 15) == 0;
-      dev::OpDesc d{};
-      describe_op(d, op, s.mode, aligned);
-      g->ops.push_back(d);
-    }
-    const int64_t tiles = assign_tiles(g->ops.data() + first, s.ops.size(), workers);
-    if (tiles < 0 || tile_base + tiles > kFlowMaxTiles) {
-      g->why = "too many tiles";
-      return;
-    }
-    tile_base += static_cast<uint32_t>(tiles);
-  }
-  g->step_tile0.push_back(tile_base);
-  // tiles and dependencies
-  std::vector<RangeState> state(nbase);
-  g->dep_off.push_back(0);
-  struct Touch {
-    int base;
-    int64_t lo, hi;
-    bool write;
-  };
-  for (size_t si = 0; si < plan.steps.size(); ++si) {
-    const Step& s = plan.steps[si];
-    std::vector<std::vector<Touch>> touched;
-    for (size_t oi = 0; oi < s.ops.size(); ++oi) {
-      const Op& op = s.ops[oi];
-      const dev::OpDesc& d = g->ops[g->step_op0[si] + oi];
-      const int64_t gelems = group_elements(s.mode, d.esz);
-      for (int64_t lt = 0; lt < int64_t(d.tpr) * d.nb; ++lt) {
-        FlowTile ft{static_cast<uint32_t>(si), static_cast<uint32_t>(oi), lt / d.tpr, 0, 0};
-        const int64_t tr = lt % d.tpr;
-        if (d.vec) {
-          const int64_t tg = int64_t(d.upt) * dev::kThreads;
-          ft.e0 = tr * tg * gelems;
-          ft.e1 = tr == int64_t(d.tpr) - 1 ? d.n : std::min((tr + 1) * tg, d.groups) * gelems;
-        } else {
-          ft.e0 = tr * dev::kTileElems;
-          ft.e1 = std::min(ft.e0 + dev::kTileElems, d.n);
-        }
-        std::vector<Touch> tv;
-        for (const Operand& o : op.src) {
-          const int64_t b = o.byte_off + ft.run * op.sstride;
-          tv.push_back({base_of(o), b + ft.e0 * esize(o.dt), b + ft.e1 * esize(o.dt), false});
-        }
-        for (const Operand& o : op.dst) {
-          const int64_t b = o.byte_off + ft.run * op.dstride;
-          tv.push_back({base_of(o), b + ft.e0 * esize(o.dt), b + ft.e1 * esize(o.dt), true});
-        }
-        std::vector<uint32_t> deps;
-        for (const Touch& x : tv) {
-          if (x.write) state[x.base].deps_write(x.lo, x.hi, &deps);
-          else state[x.base].deps_read(x.lo, x.hi, &deps);
-        }
-        std::sort(deps.begin(), deps.end());
-        deps.erase(std::unique(deps.begin(), deps.end()), deps.end());
-        g->dep.insert(g->dep.end(), deps.begin(), deps.end());
-        g->dep_off.push_back(static_cast<uint32_t>(g->dep.size()));
-        g->tiles.push_back(ft);
-        touched.push_back(std::move(tv));
-      }
-    }
-    // the step's own reads and writes become the state for the next step
-    const uint32_t t0 = g->step_tile0[si];
-    for (size_t k = 0; k < touched.size(); ++k)
-      for (const Touch& x : touched[k]) {
-        if (x.write) state[x.base].record_write(x.lo, x.hi, t0 + static_cast<uint32_t>(k));
-        else state[x.base].record_read(x.lo, x.hi, t0 + static_cast<uint32_t>(k));
-      }
-  }
-  g->ok = true;
-}
-
 std::mutex g_support_mu;
 std::unordered_map<PlanKey, std::pair<PlanStatus, std::string>, PlanKeyHash> g_support;
 
@@ -1652,65 +1461,6 @@ VC_EXPORT vc_status_t vc_reduce_scatter_noalloc(const void* const* send, void* c
     if (op != VC_SUM) return fail(op == VC_MAX || op == VC_MIN ? VC_ERR_UNSUPPORTED : VC_ERR_INVALID_ARG, "only VC_SUM is implemented");
     return run_reduce_scatter_noalloc(send, recv, nranks, static_cast<int64_t>(recvcount), dt,
                                       reinterpret_cast<cudaStream_t>(stream));
-  });
-}
-
-VC_EXPORT vc_status_t vc_flow_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
-                                       vc_dtype_t dtype, vc_op_t op, int root, int inplace, int nchunks,
-                                       int workers, vc_flow_tile_t* tiles, size_t tile_capacity,
-                                       size_t* n_tiles, uint32_t* deps, size_t dep_capacity, size_t* n_deps) {
-  return entry([&]() -> vc_status_t {
-    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
-    if (nranks < 1 || nranks > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
-    if (workers < 1) return fail(VC_ERR_INVALID_ARG, "workers must be positive");
-    PlanArgs pa;
-    pa.coll = static_cast<Coll>(static_cast<int>(coll));
-    bool is_auto = false;
-    vc_status_t rc = to_algo(algo, &pa.algo, &is_auto);
-    if (rc == VC_SUCCESS) rc = to_dt(dtype, &pa.dt);
-    if (rc == VC_SUCCESS) rc = to_op(op, &pa.op);
-    if (rc != VC_SUCCESS) return rc;
-    pa.nranks = nranks;
-    pa.count = static_cast<int64_t>(count);
-    pa.root = root;
-    // the plan a call makes: an in-place AllReduce keeps the out-of-place plan (N > 1)
-    pa.inplace = inplace != 0 && (pa.coll != Coll::AllReduce || nranks == 1);
-    if (is_auto) {
-      rc = resolve_auto(&pa);
-      if (rc != VC_SUCCESS) return rc;
-    }
-    if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
-      pa.nchunks = nchunks > 0 ? nchunks : default_chunks(pa.algo, nranks, pa.count, pa.dt, current_cost());
-    Plan plan;
-    std::string why;
-    const PlanStatus ps = build_plan(pa, &plan, &why);
-    if (ps != PlanStatus::Ok) return plan_status(ps, why);
-    // in place: AllReduce every rank; Broadcast and Reduce the root
-    uint64_t alias = 0;
-    if (inplace) {
-      if (pa.coll == Coll::AllReduce) alias = nranks == 64 ? ~0ull : (1ull << nranks) - 1;
-      else if (pa.coll == Coll::Broadcast || pa.coll == Coll::Reduce) alias = 1ull << root;
-    }
-    FlowGraph g;
-    build_flow(plan, nranks, alias, workers, &g);
-    if (!g.ok) return fail(VC_ERR_UNSUPPORTED, g.why);
-    if (n_tiles) *n_tiles = g.tiles.size();
-    if (n_deps) *n_deps = g.dep.size();
-    if (!tiles && !deps) return VC_SUCCESS;
-    if (!tiles || !deps || tile_capacity < g.tiles.size() || dep_capacity < g.dep.size())
-      return fail(VC_ERR_INVALID_ARG, "capacity too small");
-    for (size_t k = 0; k < g.tiles.size(); ++k) {
-      vc_flow_tile_t& o = tiles[k];
-      o.step = static_cast<int32_t>(g.tiles[k].step);
-      o.op = static_cast<int32_t>(g.tiles[k].op);
-      o.run = g.tiles[k].run;
-      o.e0 = g.tiles[k].e0;
-      o.e1 = g.tiles[k].e1;
-      o.dep_begin = g.dep_off[k];
-      o.dep_end = g.dep_off[k + 1];
-    }
-    std::copy(g.dep.begin(), g.dep.end(), deps);
-    return VC_SUCCESS;
   });
 }
 

@@ -376,33 +376,6 @@ vc_status_t vc_set_single_launch(size_t max_step_bytes);
 vc_status_t vc_get_single_launch(size_t* max_step_bytes);
 
 /*
- * Tiles of a plan and the order between them (host only, needs no GPU).
- *
- * The work of a call, cut into the tiles a launch over `workers` blocks
- * would use: tile k does elements [e0, e1) of run `run` of operation `op` of
- * step `step` (as vc_plan_describe numbers them).  A tile must come after
- * every tile listed in deps[dep_begin .. dep_end): the tiles of earlier
- * steps whose bytes it reads after they wrote them, writes after they read
- * them, or writes after they wrote them (inplace: as the call would alias
- * the buffers).  Running the tiles in any order that respects these lists
- * gives the same result as running the steps in order.  With tiles and deps
- * both null, returns only the counts; VC_ERR_UNSUPPORTED when the plan has
- * more than 65536 tiles.
- */
-typedef struct {
-  int32_t step;
-  int32_t op;
-  int64_t run;
-  int64_t e0, e1;
-  uint32_t dep_begin, dep_end;
-} vc_flow_tile_t;
-
-vc_status_t vc_flow_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype,
-                             vc_op_t op, int root, int inplace, int nchunks, int workers,
-                             vc_flow_tile_t* tiles, size_t tile_capacity, size_t* n_tiles,
-                             uint32_t* deps, size_t dep_capacity, size_t* n_deps);
-
-/*
  * Ring ReduceScatter that allocates no device memory.
  *
  * The source pages have no counterpart to this call: it exists for callers

@@ -170,59 +170,3 @@ def oracle_transfers(log) -> Counter:
         if t.n:
             tot[(t.step, t.src, t.dst, t.reduce)] += t.n
     return tot
-
-
-def run_tile(plan, tile, mem: Memory) -> None:
-    """One tile of a dataflow plan: elements [e0, e1) of run `run` of one operation."""
-    op = plan[tile.step][tile.op]
-    n = tile.e1 - tile.e0
-    if n <= 0:
-        return
-    b = tile.run
-    srcs = [mem.view(k, o, dt, off + b * stride + tile.e0 * ESZ[dt], n) for (k, o, dt, off, stride) in op["src"]]
-    if op["reduce"]:
-        acc = _widen(srcs[0], op["src"][0][2])
-        for s, (k, o, dt, off, stride) in zip(srcs[1:], op["src"][1:]):
-            acc = _combine(acc, _widen(s, dt), op["red"])
-    for (k, o, dt, off, stride) in op["dst"]:
-        dstv = mem.view(k, o, dt, off + b * stride + tile.e0 * ESZ[dt], n)
-        dstv[:] = _narrow(acc, dt) if op["reduce"] else srcs[0]
-
-
-def tile_order(tiles, deps, rng=None):
-    """An order of the tiles that respects their dependency lists: random among
-    the ready tiles (rng), or, without rng, always the ready tile of the latest
-    step (steps interleaved as far as the dependencies allow)."""
-    children = [[] for _ in tiles]
-    indeg = [0] * len(tiles)
-    for t, tile in enumerate(tiles):
-        for d in deps[tile.dep_begin:tile.dep_end]:
-            assert tiles[d].step < tile.step, (t, d)
-            children[d].append(t)
-            indeg[t] += 1
-    ready = [t for t in range(len(tiles)) if indeg[t] == 0]
-    order = []
-    while ready:
-        if rng is not None:
-            i = int(rng.integers(len(ready)))
-        else:
-            i = max(range(len(ready)), key=lambda j: (tiles[ready[j]].step, -ready[j]))
-        t = ready.pop(i)
-        order.append(t)
-        for c in children[t]:
-            indeg[c] -= 1
-            if indeg[c] == 0:
-                ready.append(c)
-    assert len(order) == len(tiles)
-    return order
-
-
-def tile_touches(plan, tile, mem: Memory):
-    """(buffer identity, lo, hi, writes) of every operand of a tile."""
-    op = plan[tile.step][tile.op]
-    out = []
-    for role, lst, in ((False, op["src"]), (True, op["dst"])):
-        for (k, o, dt, off, stride) in lst:
-            lo = off + tile.run * stride + tile.e0 * ESZ[dt]
-            out.append((mem.ident(k, o), lo, lo + (tile.e1 - tile.e0) * ESZ[dt], role))
-    return out
