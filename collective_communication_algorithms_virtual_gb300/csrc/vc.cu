@@ -145,7 +145,18 @@ struct Pending {
 };
 std::mutex g_trace_mu;
 bool g_trace_on = false;
+size_t g_trace_dropped = 0;
+constexpr size_t kTraceMax = 1u << 20;  // records kept until vc_trace_read
+
 std::vector<Pending> g_trace;
+// With g_trace_mu held: whether this launch is traced (tracing on and room
+// left; launches past the cap are counted, not recorded).
+bool trace_slot() {
+  if (!g_trace_on) return false;
+  if (g_trace.size() < kTraceMax) return true;
+  ++g_trace_dropped;
+  return false;
+}
 std::vector<cudaEvent_t> g_event_pool;
 
 cudaError_t take_event(cudaEvent_t* ev) {
@@ -320,7 +331,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, cap));
   std::unique_lock<std::mutex> lk(g_trace_mu);
-  const bool trace = g_trace_on;
+  const bool trace = trace_slot();
   if (!trace) lk.unlock();
   Pending pend{};
   if (trace) {
@@ -805,7 +816,7 @@ vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<con
     }
   }
   std::unique_lock<std::mutex> lk(g_trace_mu);
-  const bool trace = g_trace_on;
+  const bool trace = trace_slot();
   if (!trace) lk.unlock();
   Pending pend{};
   if (trace) {
@@ -1343,6 +1354,7 @@ VC_EXPORT vc_status_t vc_trace_enable(int on) {
       g_event_pool.push_back(p.stop);
     }
     g_trace.clear();
+    g_trace_dropped = 0;
     g_trace_on = on != 0;
     return VC_SUCCESS;
   });

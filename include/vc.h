@@ -315,7 +315,8 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  * bracketed by CUDA events recorded on the caller's stream, and a record
  * keeps the collective, algorithm, step, kernel variant and the launch's
  * algorithmic bytes (every operand of every operation read or written once,
- * at its storage size).  vc_trace_enable(1) clears old records;
+ * at its storage size); at most 2^20 records are kept between reads (later
+ * launches run untraced).  vc_trace_enable(1) clears old records;
  * vc_trace_read waits for the recorded events, writes up to `capacity`
  * records with their event-timed durations and clears them.
  *   kernel: bits 0-2 the mode (0 copy, 1 fp32, 2 int32, 3 bf16 with fp32
