@@ -30,7 +30,12 @@ from .binding import (  # noqa: F401
     vc_set_cost_model,
     vc_set_single_launch,
     vc_get_single_launch,
+    vc_device_errors,
+    vc_copy_selftest,
     SINGLE_LAUNCH_ALWAYS,
+    vc_set_copy_pipeline,
+    vc_get_copy_pipeline,
+    COPY_PIPELINE_NEVER,
     vc_get_cost_model,
     vc_status_string,
     vc_trace_enable,

@@ -44,8 +44,10 @@ KERNEL_OPS = {0: "sum", 1: "max", 2: "min"}
 def kernel_name(code: int) -> str:
     mode = KERNEL_MODES[code & 7]
     name = mode if mode == "copy" else f"{KERNEL_OPS[(code >> 3) & 3]}_{mode}"
-    return (name + ("_large" if code & 32 else "") + ("_batched" if code & 64 else "")
-            + ("_single_launch" if code & 128 else ""))
+    if code & 128:  # one cluster launch for the whole plan
+        return name + "_single_launch"
+    extra = ("_tma" if mode == "copy" else "_batched") if code & 64 else ""
+    return name + ("_large" if code & 32 else "") + extra
 
 
 class PlanEntry(ctypes.Structure):
@@ -100,10 +102,18 @@ def lib() -> ctypes.CDLL:
         L.vc_get_cost_model.restype = I
         L.vc_select_algo.argtypes = [I, I, Z, I, I, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]
         L.vc_select_algo.restype = I
+        L.vc_device_errors.argtypes = [V, ctypes.POINTER(ctypes.c_uint32)]
+        L.vc_device_errors.restype = I
+        L.vc_copy_selftest.argtypes = [V, ctypes.POINTER(ctypes.c_uint32)]
+        L.vc_copy_selftest.restype = I
         L.vc_set_single_launch.argtypes = [Z]
         L.vc_set_single_launch.restype = I
         L.vc_get_single_launch.argtypes = [ctypes.POINTER(Z)]
         L.vc_get_single_launch.restype = I
+        L.vc_set_copy_pipeline.argtypes = [Z]
+        L.vc_set_copy_pipeline.restype = I
+        L.vc_get_copy_pipeline.argtypes = [ctypes.POINTER(Z)]
+        L.vc_get_copy_pipeline.restype = I
         L.vc_version.argtypes = []
         L.vc_version.restype = I
         _lib = L
@@ -294,6 +304,37 @@ def vc_get_single_launch() -> int:
 
 
 SINGLE_LAUNCH_ALWAYS = (1 << 64) - 1
+
+
+def vc_set_copy_pipeline(min_bytes: int) -> None:
+    """Copy launches of whole 16-byte groups that write at least this many
+    bytes take the bulk-copy pipeline (0: every one; COPY_PIPELINE_NEVER: none)."""
+    check(lib().vc_set_copy_pipeline(int(min_bytes)))
+
+
+def vc_get_copy_pipeline() -> int:
+    v = ctypes.c_size_t(0)
+    check(lib().vc_get_copy_pipeline(ctypes.byref(v)))
+    return v.value
+
+
+COPY_PIPELINE_NEVER = (1 << 64) - 1
+
+
+def vc_device_errors(stream=None) -> int:
+    """Waits for the stream, then reads and clears the device error word."""
+    v = ctypes.c_uint32(0)
+    s = None if stream is None else (stream if isinstance(stream, int) else int(stream.cuda_stream))
+    check(lib().vc_device_errors(s, ctypes.byref(v)))
+    return v.value
+
+
+def vc_copy_selftest(stream=None) -> int:
+    """Error word left by a bulk-copy launch whose first wait is made to run out."""
+    v = ctypes.c_uint32(0)
+    s = None if stream is None else (stream if isinstance(stream, int) else int(stream.cuda_stream))
+    check(lib().vc_copy_selftest(s, ctypes.byref(v)))
+    return v.value
 
 
 def vc_trace_enable(on: bool = True) -> None:

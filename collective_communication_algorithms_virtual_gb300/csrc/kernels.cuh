@@ -64,7 +64,7 @@ struct __align__(16) OpDesc {
   uint8_t ns, nd;
   uint8_t vec;      // 1: vector path
   uint8_t esz;      // copy: element size in bytes
-  uint8_t upt;      // vector path: groups per thread in one tile (1, 2 or 4)
+  uint8_t upt;      // vector path: groups per thread in one tile (1, 2, 4; 8 in the bulk-copy pipeline)
 };
 
 template <int OPS, int PTRS>
@@ -626,6 +626,128 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
   }
   // outstanding bulk stores of fan-out copies finish before the block exits
   if (FAN && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// -- bulk-copy (TMA) kernel ------------------------------------------------------
+// Copy steps whose operations are all 16-byte aligned with no element tail run
+// as a pipeline of bulk asynchronous copies: in each block one thread loads a
+// tile of up to 32 KB global -> shared (cp.async.bulk with mbarrier
+// completion), keeping kCopyStages tiles in flight, and writes each landed
+// tile to every destination with bulk stores (cp.async.bulk shared -> global);
+// a stage is refilled once the stores of the tile it held have read it.  One
+// block per SM.  Measured on a 1 GiB copy: 6835 GB/s against 6385 for 128-bit
+// loads and stores through registers (8 blocks per SM); 256 MiB: 6517 vs 6206.
+// The host takes it for launches that write at least 256 MiB; smaller ones keep
+// the register kernel.
+// Waits on an mbarrier are bounded: one that gives up sets the device error
+// word, stops issuing, waits (bounded) for the loads it issued and returns.
+constexpr int kCopyStages = 3;
+constexpr int kCopyTileBytes = 32 << 10;  // largest tile: 2048 groups (tile groups = upt * kThreads, upt <= 8)
+constexpr int kCopyThreads = 32;
+constexpr uint32_t kMbarWaitLimit = 1u << 21;
+
+__device__ uint32_t g_device_error;  // bit 1: a bulk-copy wait gave up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// Polls the mbarrier phase with test_wait (never blocks: try_wait may suspend
+// the thread for a system-dependent time per call, which would leave the
+// total unbounded), backing off with a short sleep after the first polls:
+// at most kMbarWaitLimit polls of at most ~0.1 us sleep each, well under a
+// second, while a tile's load lands in a few microseconds.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kMbarWaitLimit; ++it) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+    if (it >= 32) __nanosleep(64);
+  }
+  return false;
+}
+
+template <class P, bool DRILL = false>
+__global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_constant__ P p) {
+  extern __shared__ __align__(128) unsigned char stage[];  // kCopyStages * kCopyTileBytes, then the mbarriers
+  __shared__ uint32_t s_tile0[sizeof(P::op) / sizeof(OpDesc)];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kCopyStages * kCopyTileBytes);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int nops = static_cast<int>(p.nops);
+  for (int i = threadIdx.x; i < nops; i += kCopyThreads) s_tile0[i] = p.op[i].tile0;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kCopyStages; ++k)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bars + k)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x != 0) return;
+  // tile i of this block is global tile blockIdx.x + i * gridDim.x
+  const int64_t n = p.ntiles > blockIdx.x ? (p.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  struct Tile {
+    const OpDesc* o;
+    int64_t run, gbeg;
+    uint32_t bytes;
+  };
+  auto tile = [&](int64_t i) {
+    const uint32_t t = static_cast<uint32_t>(blockIdx.x + i * gridDim.x);
+    int lo = 0, hi = nops - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tile0[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const OpDesc& o = p.op[lo];
+    const uint32_t lt = t - o.tile0, run = lt / o.tpr, tr = lt - run * o.tpr;
+    const int64_t tg = int64_t(o.upt) * kThreads;
+    const int64_t gbeg = tr * tg, gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
+    return Tile{&o, run, gbeg, static_cast<uint32_t>((gend - gbeg) * 16)};
+  };
+  auto load = [&](int64_t i) {
+    const int k = static_cast<int>(i % kCopyStages);
+    const Tile x = tile(i);
+    const char* src = static_cast<const char*>(p.ptr[x.o->p0]) + x.run * x.o->sstride + x.gbeg * 16;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bars + k)), "r"(x.bytes)
+                 : "memory");
+    if (DRILL && i == 0) return;
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(stage + k * kCopyTileBytes)),
+                 "l"(src), "r"(x.bytes), "r"(smem_addr(bars + k))
+                 : "memory");
+  };
+  uint64_t policy;  // stores are written once: evict first in L2, as the streaming stores of the other paths
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  int64_t issued = 0;
+  for (; issued < n && issued < kCopyStages; ++issued) load(issued);
+  int64_t i = 0;
+  bool ok = true;
+  for (; i < n; ++i) {
+    const int k = static_cast<int>(i % kCopyStages);
+    if (!mbar_wait(smem_addr(bars + k), static_cast<uint32_t>((i / kCopyStages) & 1))) {
+      ok = false;
+      break;
+    }
+    const Tile x = tile(i);
+    for (int d = 0; d < x.o->nd; ++d) {
+      char* dst = static_cast<char*>(const_cast<void*>(p.ptr[x.o->p0 + x.o->ns + d])) + x.run * x.o->dstride + x.gbeg * 16;
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                   "r"(smem_addr(stage + k * kCopyTileBytes)), "r"(x.bytes), "l"(policy)
+                   : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    if (i >= 1 && issued < n) {  // refill the stage of tile i - 1 once its stores have read it
+      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      load(issued++);
+    }
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (!ok) {
+    atomicOr(&g_device_error, 2u);
+    // loads issued and not consumed land before the block's shared memory is released
+    for (int64_t j = i; j < issued; ++j)
+      mbar_wait(smem_addr(bars + j % kCopyStages), static_cast<uint32_t>((j / kCopyStages) & 1));
+  }
 }
 
 // -- one-launch plans ------------------------------------------------------------

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cstdio>
@@ -53,6 +54,9 @@ bool pdl_enabled() {
   }();
   return on;
 }
+// Copy launches writing at least this many bytes take the bulk-copy pipeline
+// (vc_set_copy_pipeline).
+std::atomic<size_t> g_copy_pipeline{VC_COPY_PIPELINE_DEFAULT};
 bool log_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("VC_LOG");
@@ -136,8 +140,11 @@ Residency residency(DeviceState* st, K kernel) {
 // ---------------------------------------------------------------------------
 // launch trace
 // ---------------------------------------------------------------------------
-struct TraceCtx {
+// What a step launch knows of its call: collective, algorithm and step (for
+// the trace), and whether its copies may take the bulk-copy pipeline.
+struct LaunchCtx {
   int coll = 0, algo = 0, step = 0;
+  bool pipeline = true;
 };
 struct Pending {
   vc_trace_record_t rec;
@@ -237,7 +244,7 @@ void describe_op(dev::OpDesc& d, const Op& op, Mode mode, bool ptrs_aligned) {
 // 1) that still gives `cap` tiles (one per resident block), so a small step
 // is spread over many blocks instead of a few doing all of it.  Returns the
 // tile count, or -1 if it does not fit the 32-bit tile numbers.
-int64_t assign_tiles(dev::OpDesc* d, size_t n, int64_t cap) {
+int64_t assign_tiles(dev::OpDesc* d, size_t n, int64_t cap, int max_upt = dev::kUnroll) {
   auto tiles_per_run = [](const dev::OpDesc& o, int upt) {
     const int64_t per = o.vec ? int64_t(upt) * dev::kThreads : dev::kTileElems;
     const int64_t units = o.vec ? o.groups : o.n;
@@ -248,7 +255,7 @@ int64_t assign_tiles(dev::OpDesc* d, size_t n, int64_t cap) {
     for (size_t k = 0; k < n; ++k) total += tiles_per_run(d[k], upt) * d[k].nb;
     return total;
   };
-  int upt = dev::kUnroll;
+  int upt = max_upt;
   while (upt > 1 && count_tiles(upt) < cap) upt /= 2;
   int64_t tiles = 0;
   for (size_t k = 0; k < n; ++k) {
@@ -264,7 +271,8 @@ int64_t assign_tiles(dev::OpDesc* d, size_t n, int64_t cap) {
 
 // Fills the parameter block of operations [i, j) of a step.
 template <class P>
-bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t cap, int64_t* tiles_out) {
+bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64_t cap, int64_t* tiles_out,
+                 int max_upt = dev::kUnroll) {
   std::memset(&p, 0, sizeof(P));
   int np = 0;
   for (size_t k = i; k < j; ++k) {
@@ -284,7 +292,7 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
     describe_op(p.op[k - i], op, st.mode, aligned);
     p.op[k - i].p0 = static_cast<uint16_t>(p0);
   }
-  const int64_t tiles = assign_tiles(p.op, j - i, cap);
+  const int64_t tiles = assign_tiles(p.op, j - i, cap, max_upt);
   if (tiles < 0) return false;
   p.nops = static_cast<uint32_t>(j - i);
   p.ntiles = static_cast<uint32_t>(tiles);
@@ -294,7 +302,7 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
 
 template <int MODE, int OP, class P>
 vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
-                         const TraceCtx& tc) {
+                         const LaunchCtx& tc) {
   static thread_local P p;  // large: keep off the stack
   // tiles are sized against the vector-only kernel's residency
   auto kernel = dev::step_kernel<MODE, OP, P, 1, false, false>;
@@ -329,6 +337,37 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
     res = residency(st, kernel);
     cap = int64_t(st->nsm) * res.blocks;
   }
+  // copies of aligned whole groups: the bulk-copy pipeline, one block per SM, tiles of up to 32 KB
+  unsigned block = dev::kThreads;
+  size_t dyn_smem = 0;
+  bool tma = false;
+  if constexpr (MODE == dev::kCopy) {
+    // Only for launches that write at least the set minimum (128 MiB by
+    // default) in calls without 16-bit reductions: the pipeline wants most of
+    // an SM's shared memory while the other step kernels run with a large L1,
+    // so the SMs are reconfigured at each switch, and a reduction kernel that
+    // starts early behind the pipeline runs in its configuration; smaller
+    // copies, and the 16-bit reductions (the most sensitive to L1), lose more
+    // there than the pipeline gains.
+    int64_t groups = 0;  // 16-byte groups the launch writes
+    for (uint32_t k = 0; k < p.nops; ++k) groups += p.op[k].groups * p.op[k].nb * p.op[k].nd;
+    const size_t min_bytes = g_copy_pipeline.load(std::memory_order_relaxed);
+    if (!elem && tc.pipeline && min_bytes != SIZE_MAX && static_cast<size_t>(groups) * 16 >= min_bytes) {
+      cap = st->nsm;
+      if (!fill_params(p, s, i, j, b, cap, &tiles, dev::kCopyTileBytes / (dev::kThreads * 16)))
+        return fail(VC_ERR_INVALID_ARG, "operation too large for one launch");
+      kernel = dev::tma_copy_kernel<P>;
+      block = dev::kCopyThreads;
+      dyn_smem = dev::kCopyStages * dev::kCopyTileBytes + dev::kCopyStages * sizeof(uint64_t);
+      tma = true;
+      static std::once_flag once[64];  // per device
+      cudaError_t ea = cudaSuccess;
+      std::call_once(once[st - g_dev], [&] {
+        ea = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn_smem));
+      });
+      if (ea != cudaSuccess) return cuda_fail(ea, "cudaFuncSetAttribute");
+    }
+  }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, cap));
   std::unique_lock<std::mutex> lk(g_trace_mu);
   const bool trace = trace_slot();
@@ -342,8 +381,8 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(dev::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -359,7 +398,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
     pend.rec.coll = tc.coll;
     pend.rec.algo = tc.algo;
     pend.rec.step = tc.step;
-    pend.rec.kernel = MODE | (OP << 3) | (sizeof(P) == sizeof(dev::LargeParams) ? 32 : 0) | (batched ? 64 : 0);
+    pend.rec.kernel = MODE | (OP << 3) | (sizeof(P) == sizeof(dev::LargeParams) ? 32 : 0) | (batched || tma ? 64 : 0);
     pend.rec.bytes = launch_bytes(s, i, j);
     pend.rec.nops = static_cast<int32_t>(j - i);
     g_trace.push_back(pend);
@@ -369,7 +408,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
 
 template <int MODE, class P>
 vc_status_t launch_op(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
-                      const TraceCtx& tc) {
+                      const LaunchCtx& tc) {
   switch (s.red) {
     case RedOp::Max: return launch_typed<MODE, dev::kMax, P>(st, s, i, j, b, stream, tc);
     case RedOp::Min: return launch_typed<MODE, dev::kMin, P>(st, s, i, j, b, stream, tc);
@@ -379,7 +418,7 @@ vc_status_t launch_op(DeviceState* st, const Step& s, size_t i, size_t j, const 
 
 template <class P>
 vc_status_t launch_mode(DeviceState* st, const Step& s, size_t i, size_t j, const Bases& b, cudaStream_t stream,
-                        const TraceCtx& tc) {
+                        const LaunchCtx& tc) {
   // 16-bit steps whose sources are all of the data type take the batched kernel
   auto pure = [&](DT want) {
     for (size_t k = i; k < j; ++k)
@@ -403,7 +442,7 @@ vc_status_t launch_mode(DeviceState* st, const Step& s, size_t i, size_t j, cons
 int op_ptrs(const Op& op) { return static_cast<int>(op.src.size() + op.dst.size()); }
 
 vc_status_t launch_step(DeviceState* st, const Step& s, const Bases& b, cudaStream_t stream, int* launches,
-                        const TraceCtx& tc) {
+                        const LaunchCtx& tc) {
   size_t i = 0;
   while (i < s.ops.size()) {
     // the largest prefix that fits the small parameter block, else the large one
@@ -787,7 +826,7 @@ const DevPlan* resident_plan(int dev, const PlanKey& key, const Plan& plan, int 
 }
 
 vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<const void*>& sends,
-                        const std::vector<void*>& recvs, char* scratch, cudaStream_t stream, const TraceCtx& tc) {
+                        const std::vector<void*>& recvs, char* scratch, cudaStream_t stream, const LaunchCtx& tc) {
   dev::PlanParams prm{};
   prm.plan = dp.dptr;
   prm.words = dp.words;
@@ -981,9 +1020,10 @@ vc_status_t run(const Call& c) {
   }
   const Bases b{sends.data(), recvs.data(), scratch};
   int launches = 0;
-  TraceCtx tc;
+  LaunchCtx tc;
   tc.coll = static_cast<int>(c.coll);
   tc.algo = static_cast<int>(pa.algo);
+  for (const Step& s : plan.steps) tc.pipeline &= s.mode != Mode::BF16 && s.mode != Mode::F16;
   // one launch for the whole plan when it is small enough and eligible
   const DevPlan* dp = nullptr;
   const size_t limit = single_launch_limit();
@@ -1450,7 +1490,7 @@ vc_status_t run_reduce_scatter_noalloc(const void* const* send, void* const* rec
   if (rc_ != VC_SUCCESS) return rc_;
   const Bases b{send, recv, scratch};
   int launches = 0;
-  TraceCtx tc;
+  LaunchCtx tc;
   tc.coll = static_cast<int>(Coll::ReduceScatter);
   tc.algo = static_cast<int>(Algo::Ring);
   for (size_t si = 0; si < plan.steps.size(); ++si) {
@@ -1476,6 +1516,71 @@ VC_EXPORT vc_status_t vc_reduce_scatter_noalloc(const void* const* send, void* c
   });
 }
 
+VC_EXPORT vc_status_t vc_device_errors(vc_stream_t stream, uint32_t* flags) {
+  return entry([&]() -> vc_status_t {
+    if (!flags) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+    *flags = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint32_t zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flags, dev::g_device_error, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(dev::g_device_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_copy_selftest(vc_stream_t stream, uint32_t* flags) {
+  return entry([&]() -> vc_status_t {
+    if (!flags) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+    DeviceState* st = nullptr;
+    int dev = 0;
+    vc_status_t rc = device_state(&st, &dev);
+    if (rc != VC_SUCCESS) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // one copy of 64 KB (two 32 KB tiles) from a zeroed buffer to another
+    char* mem = nullptr;
+    cudaError_t e = cudaMalloc(&mem, 2 << 16);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    Step step;
+    step.mode = Mode::Copy;
+    Op op;
+    op.src.push_back(Operand{Buf::Send, 0, 0, DT::I32});
+    op.dst.push_back(Operand{Buf::Recv, 0, 0, DT::I32});
+    op.n = (1 << 16) / 4;
+    step.ops.push_back(op);
+    const void* send[1] = {mem};
+    void* recv[1] = {mem + (1 << 16)};
+    const Bases b{send, recv, nullptr};
+    static thread_local dev::SmallParams p;
+    int64_t tiles = 0;
+    fill_params(p, step, 0, 1, b, 1, &tiles, dev::kCopyTileBytes / (dev::kThreads * 16));
+    auto kernel = dev::tma_copy_kernel<dev::SmallParams, true>;
+    const size_t smem = dev::kCopyStages * dev::kCopyTileBytes + dev::kCopyStages * sizeof(uint64_t);
+    const uint32_t zero = 0;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess) e = cudaMemsetAsync(mem, 0, 2 << 16, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyToSymbolAsync(dev::g_device_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1);
+      cfg.blockDim = dim3(dev::kCopyThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = s;
+      e = cudaLaunchKernelEx(&cfg, kernel, p);
+    }
+    if (e == cudaSuccess)
+      e = cudaMemcpyFromSymbolAsync(flags, dev::g_device_error, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyToSymbolAsync(dev::g_device_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(mem);
+    if (e != cudaSuccess) return cuda_fail(e, "copy self-test");
+    return VC_SUCCESS;
+  });
+}
+
 VC_EXPORT vc_status_t vc_set_single_launch(size_t max_step_bytes) {
   std::lock_guard<std::mutex> lk(g_sl_mu);
   g_sl_limit = max_step_bytes;
@@ -1486,6 +1591,17 @@ VC_EXPORT vc_status_t vc_get_single_launch(size_t* max_step_bytes) {
   if (!max_step_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
   std::lock_guard<std::mutex> lk(g_sl_mu);
   *max_step_bytes = g_sl_limit;
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_set_copy_pipeline(size_t min_bytes) {
+  g_copy_pipeline.store(min_bytes, std::memory_order_relaxed);
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_get_copy_pipeline(size_t* min_bytes) {
+  if (!min_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+  *min_bytes = g_copy_pipeline.load(std::memory_order_relaxed);
   return VC_SUCCESS;
 }
 

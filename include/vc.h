@@ -324,7 +324,8 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  *   fp16 only), bits 3-4 the op (0 sum, 1 max, 2 min), bit 5 set when the
  *   launch used the large parameter block (more than 16 operations or 64
  *   operand pointers), bit 6 set when an fp32 / int32 launch too small to
- *   fill the GPU took the kernel that loads four sources at a time, bit 7
+ *   fill the GPU took the kernel that loads four sources at a time or a copy
+ *   launch took the bulk-copy (TMA) pipeline, bit 7
  *   set for a single-launch plan (vc_set_single_launch: one record for the
  *   whole call, step -1, bytes and nops of all steps; bits 0-2 then give the
  *   mode of the plan's reduction steps).
@@ -375,6 +376,43 @@ vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n
 #define VC_SINGLE_LAUNCH_DEFAULT ((size_t)768 << 10)
 vc_status_t vc_set_single_launch(size_t max_step_bytes);
 vc_status_t vc_get_single_launch(size_t* max_step_bytes);
+
+/*
+ * Bulk-copy pipeline for large copy steps (no counterpart on the source
+ * pages: an execution choice that leaves every result unchanged, bit for
+ * bit).  A per-step copy launch whose operations move whole 16-byte groups
+ * and that writes at least min_bytes in total, in a call with no bf16 / fp16
+ * reduction step, runs as a pipeline of bulk (TMA) loads into shared memory,
+ * three 32 KB stages per SM, each landed tile written to every destination
+ * with bulk stores; other copy launches load and store through registers.
+ * The pipeline holds most of an SM's shared memory while the reduction
+ * kernels run best with a large L1 (the 16-bit ones most), so each switch
+ * between the two reconfigures the SMs; the default, VC_COPY_PIPELINE_DEFAULT,
+ * is where the pipeline's higher copy bandwidth pays for that on a GB300
+ * (8 ranks: AllGather 4-6% faster from 128 MiB per step, fp32 ring and
+ * halving-doubling AllReduce 2-4% at 256 MiB per rank; slower below).  0
+ * takes it for every eligible copy launch, SIZE_MAX for none.  Process-wide.
+ */
+#define VC_COPY_PIPELINE_DEFAULT ((size_t)128 << 20)
+vc_status_t vc_set_copy_pipeline(size_t min_bytes);
+vc_status_t vc_get_copy_pipeline(size_t* min_bytes);
+
+/*
+ * Device error word.  Waits for `stream` (after the work enqueued so far),
+ * then reads and clears the word: bit 1 set when a bulk-copy pipeline's wait
+ * for a tile's load gave up (the launch then stopped issuing copies and
+ * returned; its outputs are incomplete).  Never set in correct operation;
+ * the waits are bounded so that a fault elsewhere cannot hang a launch.
+ */
+vc_status_t vc_device_errors(vc_stream_t stream, uint32_t* flags);
+
+/* Exercises that bounded wait (no counterpart on the source pages): runs the
+ * bulk-copy pipeline on a 64 KB copy whose first tile's load is announced but
+ * never issued, so the wait for it gives up (within about a second) and
+ * the launch returns.  *flags receives the error word that launch left
+ * (bit 1 set); the word is cleared before and after.  Allocates and frees
+ * 128 KB of device memory and waits for `stream`. */
+vc_status_t vc_copy_selftest(vc_stream_t stream, uint32_t* flags);
 
 /*
  * Ring ReduceScatter that allocates no device memory.

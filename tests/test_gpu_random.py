@@ -4,7 +4,9 @@
 (1-16), element count (log-uniform 1..5000, so odd sizes and ragged tails;
 one in ten 5000..100000 for several tiles per operation),
 data type, reduction op, root, in place or not, 16-byte aligned or not, and
-the execution form (default, forced single launch, one launch per step).
+the execution form (default, forced single launch, one launch per step;
+the last with the bulk-copy pipeline taken by every aligned copy launch on
+odd-numbered calls and by none on even ones).
 Each must equal the oracle's simulation of the same schedule bit for bit,
 with the canary bands around every buffer intact.  Shapes a schedule does
 not define (the library and the oracle both refuse them) are skipped.
@@ -37,8 +39,11 @@ def _lib():
     build.build()
     vc.lib()
     old = vc.vc_get_single_launch()
+    old_cp = vc.vc_get_copy_pipeline()
     yield
     vc.vc_set_single_launch(old)
+    vc.vc_set_copy_pipeline(old_cp)
+    assert vc.vc_device_errors() == 0
 
 
 def _inputs(dtype, seed, N, n):
@@ -133,6 +138,10 @@ def test_random_calls_match_oracle():
     for i in range(1000):
         coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks = _case(rng)
         vc.vc_set_single_launch({"default": 768 << 10, "single": vc.SINGLE_LAUNCH_ALWAYS, "per_step": 0}[form])
+        if form == "per_step":
+            vc.vc_set_copy_pipeline(0 if i % 2 else vc.COPY_PIPELINE_NEVER)
+        else:
+            vc.vc_set_copy_pipeline(256 << 20)
         what = (i, coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks)
         try:
             got, want = _run(i, coll, algo, N, count, dtype, op, root, inplace, shift, nchunks)
