@@ -111,6 +111,43 @@ __device__ __forceinline__ void st16_wb(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+// 32-byte accesses (one fp32 partial group: 8 floats) as single 256-bit
+// loads and stores, so that a warp's access is one contiguous kilobyte.  As
+// two 16-byte accesses 32 bytes apart, each instruction used half of every
+// sector it touched and the second fetched the same sectors from L2 again.
+// A 256-bit access must be 32-byte aligned; the vector path only guarantees
+// 16, so callers check the operand's base (group offsets are multiples of
+// 32) and otherwise take two 16-byte accesses.
+struct __align__(32) W8 {
+  uint32_t w[8];
+};
+template <bool COH>
+__device__ __forceinline__ W8 ldv32(const void* p) {
+  W8 v;
+  if constexpr (COH)
+    asm volatile("ld.global.cg.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                   "=r"(v.w[7])
+                 : "l"(p)
+                 : "memory");
+  else
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                   "=r"(v.w[7])
+                 : "l"(p));
+  return v;
+}
+template <bool COH>
+__device__ __forceinline__ void stv32(void* p, const W8& v) {
+  if constexpr (COH)
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                 "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+  else
+    asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                 "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+}
 template <bool COH>
 __device__ __forceinline__ uint4 ldv(const void* p) {
   if constexpr (COH) return ld16_cg(p);
@@ -373,15 +410,23 @@ __device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, 
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
     const bool f32 = (o.dmask >> d) & 1;
+    const bool a32 = (reinterpret_cast<uintptr_t>(dp) & 31) == 0;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = g0 + u * kThreads;
       if (g < gend) {
         if (f32) {
-          stv<COH>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
-                                           __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
-          stv<COH>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
-                                                __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
+          if (a32) {
+            W8 v;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v.w[i] = __float_as_uint(acc[u][i]);
+            stv32<COH>(dp + g * 32, v);
+          } else {
+            stv<COH>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
+                                             __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
+            stv<COH>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
+                                                  __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
+          }
         } else {
           stv<COH>(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
                                            pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
@@ -391,8 +436,12 @@ __device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, 
   }
 }
 
-// 16-bit data with fp32 partial sums among the sources, one source at a time.
+// 16-bit data with fp32 partial sums among the sources: kBatchBF sources'
+// loads are in flight together before they are combined, one after another
+// in source order.  A group is 16 bytes of a 16-bit source or 32 of an fp32
+// one, loaded as one access either way.
 constexpr int kUnrollBF = 2;  // groups per thread per pass
+constexpr int kBatchBF = 2;
 template <bool F16, int OP, bool COH, class PT>
 __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
                                                 int64_t gend) {
@@ -403,22 +452,50 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, 
     if (pbeg >= gend) break;
     const int64_t g0 = pbeg + lane();
     float acc[kUnrollBF][8];
-    for (int k = 0; k < o.ns; ++k) {
-      const char* s = static_cast<const char*>(ptr[k]) + run * o.sstride;
-      const bool f32 = (o.smask >> k) & 1;
+    for (int k = 0; k < o.ns; k += kBatchBF) {
+      W8 raw[kBatchBF][kUnrollBF];
 #pragma unroll
-      for (int u = 0; u < kUnrollBF; ++u) {
-        const int64_t g = g0 + u * kThreads;
-        if (g < gend) {
-          float f[8];
-          if (f32) {
-            const uint4 a = ldv<COH>(s + g * 32), b = ldv<COH>(s + g * 32 + 16);
-            f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
-            f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
-          } else {
-            widen8<F16>(ldv<COH>(s + g * 16), f);
+      for (int j = 0; j < kBatchBF; ++j) {
+        if (k + j < o.ns) {
+          const char* s = static_cast<const char*>(ptr[k + j]) + run * o.sstride;
+          const bool f32 = (o.smask >> (k + j)) & 1;
+          const bool a32 = (reinterpret_cast<uintptr_t>(s) & 31) == 0;
+#pragma unroll
+          for (int u = 0; u < kUnrollBF; ++u) {
+            const int64_t g = g0 + u * kThreads;
+            if (g < gend) {
+              if (f32 && a32) {
+                raw[j][u] = ldv32<COH>(s + g * 32);
+              } else if (f32) {
+                const uint4 a = ldv<COH>(s + g * 32), b = ldv<COH>(s + g * 32 + 16);
+                raw[j][u].w[0] = a.x; raw[j][u].w[1] = a.y; raw[j][u].w[2] = a.z; raw[j][u].w[3] = a.w;
+                raw[j][u].w[4] = b.x; raw[j][u].w[5] = b.y; raw[j][u].w[6] = b.z; raw[j][u].w[7] = b.w;
+              } else {
+                const uint4 v = ldv<COH>(s + g * 16);
+                raw[j][u].w[0] = v.x; raw[j][u].w[1] = v.y; raw[j][u].w[2] = v.z; raw[j][u].w[3] = v.w;
+              }
+            }
           }
-          accumulate8<OP>(acc[u], f, k == 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatchBF; ++j) {
+        if (k + j < o.ns) {
+          const bool f32 = (o.smask >> (k + j)) & 1;
+#pragma unroll
+          for (int u = 0; u < kUnrollBF; ++u) {
+            const int64_t g = g0 + u * kThreads;
+            if (g < gend) {
+              float f[8];
+              if (f32) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(raw[j][u].w[i]);
+              } else {
+                widen8<F16>(make_uint4(raw[j][u].w[0], raw[j][u].w[1], raw[j][u].w[2], raw[j][u].w[3]), f);
+              }
+              accumulate8<OP>(acc[u], f, k + j == 0);
+            }
+          }
         }
       }
     }

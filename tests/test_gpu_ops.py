@@ -99,3 +99,31 @@ def test_fp16_data_movement(N):
         want = schedules.allgather([x[:rc] for x in xs], algo, "f16").outputs
         for r in range(N):
             assert same_bits(to_host(outs[r]), want[r])
+
+
+@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_fp32_partials_at_offsets_that_are_16_but_not_32_byte_aligned(dtype, single):
+    # 16-bit reductions keep fp32 partial sums in scratch.  With 100 or 1004
+    # elements per rank a rank's scratch region starts 16 bytes past a
+    # 32-byte boundary: the vector path takes it (16-byte aligned) and must
+    # not use a 32-byte access there.  Checked in per-step and one-launch form.
+    old = vc.vc_get_single_launch()
+    vc.vc_set_single_launch(vc.SINGLE_LAUNCH_ALWAYS if single else 0)
+    try:
+        for N, rc in ((4, 100), (5, 1004), (8, 1004)):
+            entries, _, _ = vc.vc_plan_describe("reduce_scatter", "ring", N, rc, dtype)
+            f32 = [e for e in entries if e.dtype == 0]
+            assert any(e.byte_off % 32 == 16 for e in f32), (N, rc)
+            xr = _inputs(dtype, 70 + N + rc, N, N * rc)
+            want = schedules.reduce_scatter(xr, "ring", dtype).outputs
+            sends = [Guarded(N * rc, dtype, fill=x) for x in xr]
+            recvs = [Guarded(rc, dtype) for _ in range(N)]
+            vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo="ring")
+            torch.cuda.synchronize()
+            assert all(g.guards_intact() for g in sends + recvs)
+            for r in range(N):
+                got = recvs[r].host()
+                assert same_bits(got, want[r]), (dtype, single, N, rc, r, first_diff(got, want[r]))
+    finally:
+        vc.vc_set_single_launch(old)
