@@ -714,8 +714,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
 // a stage is refilled once the stores of the tile it held have read it.  One
 // block per SM.  Measured on a 1 GiB copy: 6835 GB/s against 6385 for 128-bit
 // loads and stores through registers (8 blocks per SM); 256 MiB: 6517 vs 6206.
-// The host takes it for launches that write at least 256 MiB; smaller ones keep
-// the register kernel.
+// The host takes it for launches that write at least 128 MiB in calls without
+// 16-bit reduction steps; other copy launches keep the register kernel.
 // Waits on an mbarrier are bounded: one that gives up sets the device error
 // word, stops issuing, waits (bounded) for the loads it issued and returns.
 constexpr int kCopyStages = 3;
