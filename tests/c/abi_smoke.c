@@ -27,6 +27,14 @@ int main(void) {
   vc_algo_t a;
   double t = 0;
   if (vc_select_algo(VC_COLL_ALLREDUCE, 8, 1 << 20, VC_FLOAT32, 0, &a, &t) != VC_SUCCESS || a != VC_ALGO_FUSED) return 8;
+  /* execution-form settings: defaults, set, read back, restore */
+  size_t v = 0;
+  if (vc_get_copy_pipeline(&v) != VC_SUCCESS || v != VC_COPY_PIPELINE_DEFAULT) return 9;
+  if (vc_set_copy_pipeline((size_t)-1) != VC_SUCCESS || vc_get_copy_pipeline(&v) != VC_SUCCESS || v != (size_t)-1)
+    return 10;
+  vc_set_copy_pipeline(VC_COPY_PIPELINE_DEFAULT);
+  if (vc_get_single_launch(&v) != VC_SUCCESS || v != VC_SINGLE_LAUNCH_DEFAULT) return 11;
+  if (vc_get_copy_pipeline(NULL) != VC_ERR_INVALID_ARG) return 12;
   printf("ok %d\n", vc_version());
   return 0;
 }
