@@ -65,6 +65,8 @@ struct __align__(16) OpDesc {
   uint8_t vec;      // 1: vector path
   uint8_t esz;      // copy: element size in bytes
   uint8_t upt;      // vector path: groups per thread in one tile (1, 2, 4; 8 in the bulk-copy pipeline)
+  uint8_t rev;      // per-step kernels: walk this operation's tiles last to first
+  uint8_t keep;     // the next step reads the results: store them with the default L2 policy
 };
 
 template <int OPS, int PTRS>
@@ -138,25 +140,33 @@ __device__ __forceinline__ W8 ldv32(const void* p) {
   return v;
 }
 template <bool COH>
-__device__ __forceinline__ void stv32(void* p, const W8& v) {
-  if constexpr (COH)
-    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
-                 "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
-                 : "memory");
-  else
-    asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
-                 "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
-                 : "memory");
+__device__ __forceinline__ void stv32(void* p, const W8& v, bool keep = false) {
+  // plain (default L2 policy) when coherent or kept, else streaming; one store under a predicate
+  asm volatile("{\n\t.reg .pred k;\n\tsetp.ne.u32 k, %9, 0;\n\t"
+               "@k st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+               "@!k st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t}" ::"l"(p),
+               "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7]),
+               "r"(static_cast<uint32_t>(COH || keep))
+               : "memory");
 }
 template <bool COH>
 __device__ __forceinline__ uint4 ldv(const void* p) {
   if constexpr (COH) return ld16_cg(p);
   else return ld16(p);
 }
+// keep: results the next step reads take the default L2 policy instead of
+// streaming (evict-first), so that they can still be in L2 when it does.
+__device__ __forceinline__ void st16_sel(void* p, uint4 v, bool keep) {
+  asm volatile("{\n\t.reg .pred k;\n\tsetp.ne.u32 k, %5, 0;\n\t"
+               "@k st.global.v4.u32 [%0], {%1,%2,%3,%4};\n\t"
+               "@!k st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};\n\t}" ::"l"(p),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(static_cast<uint32_t>(keep))
+               : "memory");
+}
 template <bool COH>
-__device__ __forceinline__ void stv(void* p, uint4 v) {
+__device__ __forceinline__ void stv(void* p, uint4 v, bool keep = false) {
   if constexpr (COH) st16_wb(p, v);
-  else st16(p, v);
+  else st16_sel(p, v, keep);
 }
 
 template <int OP>
@@ -265,6 +275,7 @@ __device__ __forceinline__ void tile_copy_fanout(const OpDesc& o, const PT& ptr,
 // resident instead of 5.
 template <bool COH, bool FAN, class PT>
 __device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
+  const bool keep = o.keep;  // read before the loads (see tile_4b)
   if constexpr (FAN && !COH) {
     if (o.nd > 1) {
       tile_copy_fanout(o, ptr, run, gbeg, gend);
@@ -284,7 +295,7 @@ __device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + off;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, v[u]);
+      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, v[u], keep);
   }
 }
 
@@ -320,7 +331,8 @@ __device__ __forceinline__ void store_tile_bulk(const OpDesc& o, const PT& ptr, 
   if (threadIdx.x == 0 && ng > 0) {
     const uint32_t saddr = static_cast<uint32_t>(__cvta_generic_to_shared(rstage));
     uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    if (o.keep) asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     for (int d = 0; d < o.nd; ++d) {
       char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + gbeg * 16;
       asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dp), "r"(saddr), "r"(ng * 16), "l"(pol)
@@ -332,6 +344,11 @@ __device__ __forceinline__ void store_tile_bulk(const OpDesc& o, const PT& ptr, 
 
 template <bool FLOAT, int OP, bool COH, int SB, bool FAN, class PT>
 __device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg, int64_t gend) {
+  // The store policy is read before the loads: read at the stores, it kept the
+  // operation's parameter address live across them (44 -> 56 registers).  The
+  // kernel with the bulk-store path reads it at the stores (hoisted there, it
+  // reshaped that kernel's schedule and the fused AllReduce measured 1.4% slower).
+  [[maybe_unused]] const bool keep_early = FAN ? false : static_cast<bool>(o.keep);
   const int lim = static_cast<int>(gend - gbeg) - lane();  // slots as in tile_copy
   const int64_t soff = run * o.sstride + (gbeg + lane()) * 16;
   // The first source loads straight into the accumulator (a register copy of
@@ -383,12 +400,13 @@ __device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t 
       return;
     }
   }
+  const bool keep = FAN ? static_cast<bool>(o.keep) : keep_early;
   const int64_t doff = run * o.dstride + (gbeg + lane()) * 16;
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, acc[u]);
+      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, acc[u], keep);
   }
 }
 
@@ -406,7 +424,7 @@ __device__ __forceinline__ void accumulate8(float* acc, const float* f, bool fir
 
 template <bool F16, int U, bool COH, class PT>
 __device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, int64_t run, int64_t g0, int64_t gend,
-                                                float (&acc)[U][8]) {
+                                                float (&acc)[U][8], bool keep) {
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
     const bool f32 = (o.dmask >> d) & 1;
@@ -420,16 +438,16 @@ __device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, 
             W8 v;
 #pragma unroll
             for (int i = 0; i < 8; ++i) v.w[i] = __float_as_uint(acc[u][i]);
-            stv32<COH>(dp + g * 32, v);
+            stv32<COH>(dp + g * 32, v, keep);
           } else {
             stv<COH>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
-                                             __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
+                                             __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])), keep);
             stv<COH>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
-                                                  __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
+                                                  __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])), keep);
           }
         } else {
           stv<COH>(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
-                                           pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
+                                           pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])), keep);
         }
       }
     }
@@ -445,6 +463,7 @@ constexpr int kBatchBF = 2;
 template <bool F16, int OP, bool COH, class PT>
 __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
                                                 int64_t gend) {
+  const bool keep = o.keep;  // read before the loads (see tile_4b)
   // A tile is covered in passes of kUnrollBF groups per thread.
 #pragma unroll 1
   for (int pass = 0; pass < kUnroll / kUnrollBF; ++pass) {
@@ -499,7 +518,7 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, 
         }
       }
     }
-    store_half_mode<F16, kUnrollBF, COH>(o, ptr, run, g0, gend, acc);
+    store_half_mode<F16, kUnrollBF, COH>(o, ptr, run, g0, gend, acc, keep);
   }
 }
 
@@ -514,6 +533,7 @@ constexpr int kBatchBP = 2;
 template <bool F16, int OP, bool COH, class PT>
 __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, int64_t run, int64_t gbeg,
                                                int64_t gend) {
+  const bool keep = o.keep;  // read before the loads (see tile_4b)
 #pragma unroll 1
   for (int pass = 0; pass < kUnroll / kUnrollBP; ++pass) {
     const int64_t pbeg = gbeg + pass * kUnrollBP * kThreads;
@@ -548,7 +568,7 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, i
         }
       }
     }
-    store_half_mode<F16, kUnrollBP, COH>(o, ptr, run, g0, gend, acc);
+    store_half_mode<F16, kUnrollBP, COH>(o, ptr, run, g0, gend, acc, keep);
   }
 }
 
@@ -699,7 +719,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
     }
     const OpDesc& o = p.op[lo];
     const void* const* ptr = p.ptr + o.p0;
-    run_tile<MODE, OP, false, SB, ELEM, FAN>(o, ptr, t - o.tile0);
+    const uint32_t lt = t - o.tile0;
+    run_tile<MODE, OP, false, SB, ELEM, FAN>(o, ptr, o.rev ? static_cast<uint32_t>(o.tpr * o.nb) - 1 - lt : lt);
   }
   // outstanding bulk stores of fan-out copies finish before the block exits
   if (FAN && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -776,7 +797,9 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
       if (s_tile0[mid] <= t) lo = mid; else hi = mid - 1;
     }
     const OpDesc& o = p.op[lo];
-    const uint32_t lt = t - o.tile0, run = lt / o.tpr, tr = lt - run * o.tpr;
+    const uint32_t lt0 = t - o.tile0;
+    const uint32_t lt = o.rev ? static_cast<uint32_t>(o.tpr * o.nb) - 1 - lt0 : lt0;
+    const uint32_t run = lt / o.tpr, tr = lt - run * o.tpr;
     const int64_t tg = int64_t(o.upt) * kThreads;
     const int64_t gbeg = tr * tg, gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
     return Tile{&o, run, gbeg, static_cast<uint32_t>((gend - gbeg) * 16)};
@@ -793,8 +816,11 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
                  "l"(src), "r"(x.bytes), "r"(smem_addr(bars + k))
                  : "memory");
   };
-  uint64_t policy;  // stores are written once: evict first in L2, as the streaming stores of the other paths
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  // stores: evict first in L2, as the streaming stores of the other paths,
+  // unless the next step reads them (keep)
+  uint64_t evict_first, evict_normal;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(evict_normal));
   int64_t issued = 0;
   for (; issued < n && issued < kCopyStages; ++issued) load(issued);
   int64_t i = 0;
@@ -806,6 +832,7 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
       break;
     }
     const Tile x = tile(i);
+    const uint64_t policy = x.o->keep ? evict_normal : evict_first;
     for (int d = 0; d < x.o->nd; ++d) {
       char* dst = static_cast<char*>(const_cast<void*>(p.ptr[x.o->p0 + x.o->ns + d])) + x.run * x.o->dstride + x.gbeg * 16;
       asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),

@@ -42,6 +42,8 @@ struct Op {
   int64_t nb = 1;       // runs
   int64_t sstride = 0;  // bytes between runs, every source
   int64_t dstride = 0;  // bytes between runs, every destination
+  bool reverse = false; // execution order only: walk the operation's tiles from the last one
+  bool keep = false;    // execution only: the next step reads the results (keep them in L2)
 };
 
 struct Step {

@@ -238,6 +238,8 @@ void describe_op(dev::OpDesc& d, const Op& op, Mode mode, bool ptrs_aligned) {
   if (op.nb > 1) aligned &= (op.n % gelems) == 0 && (op.sstride % 16) == 0 && (op.dstride % 16) == 0;
   d.vec = aligned ? 1 : 0;
   d.groups = aligned ? op.n / gelems : 0;
+  d.rev = op.reverse ? 1 : 0;
+  d.keep = op.keep ? 1 : 0;
 }
 
 // Tiles operations d[0, n): the largest number of groups per thread (4, 2 or
@@ -589,6 +591,69 @@ PlanKey plan_key(const PlanArgs& pa) {
                  pa.root, pa.inplace ? 1 : 0, pa.nchunks, static_cast<int>(pa.op), pa.count};
 }
 
+// Orders each step's operations for reuse of what the previous step wrote
+// while it is still in L2: an operation whose sources the previous step wrote
+// later runs earlier, and walks its tiles against the direction they were
+// written, so that it starts on the most recent lines; and marks the
+// operations whose results the next step reads, which are then stored with
+// the default L2 policy instead of streaming.  Operations of a step are
+// independent, and neither their order, a tile's order nor a cache policy
+// changes any element's association.
+void order_for_reuse(Plan* plan) {
+  struct Span {
+    Buf buf;
+    int owner;
+    int64_t lo, hi;
+  };
+  auto span = [](const Operand& o, const Op& op, int64_t stride) {
+    const int64_t last = o.byte_off + (op.nb - 1) * stride;
+    return Span{o.buf, o.buf == Buf::Scratch ? -1 : o.owner, std::min(o.byte_off, last),
+                std::max(o.byte_off, last) + op.n * esize(o.dt)};
+  };
+  for (size_t s = 0; s + 1 < plan->steps.size(); ++s) {
+    const Step& next = plan->steps[s + 1];
+    std::vector<Span> reads;
+    for (const Op& op : next.ops)
+      for (const Operand& src : op.src) reads.push_back(span(src, op, op.sstride));
+    for (Op& op : plan->steps[s].ops)
+      for (const Operand& d : op.dst) {
+        const Span w = span(d, op, op.dstride);
+        for (const Span& r : reads)
+          if (r.buf == w.buf && r.owner == w.owner && r.lo < w.hi && w.lo < r.hi) op.keep = true;
+      }
+  }
+  for (size_t s = 1; s < plan->steps.size(); ++s) {
+    const Step& prev = plan->steps[s - 1];
+    Step& cur = plan->steps[s];
+    std::vector<std::pair<Span, int>> writes;
+    for (size_t j = 0; j < prev.ops.size(); ++j)
+      for (const Operand& d : prev.ops[j].dst) writes.push_back({span(d, prev.ops[j], prev.ops[j].dstride), static_cast<int>(j)});
+    const size_t n = cur.ops.size();
+    std::vector<int> when(n, -1);
+    std::vector<char> rev(n, 0);
+    for (size_t i = 0; i < n; ++i)
+      for (const Operand& src : cur.ops[i].src) {
+        const Span sp = span(src, cur.ops[i], cur.ops[i].sstride);
+        for (const auto& w : writes)
+          if (w.first.buf == sp.buf && w.first.owner == sp.owner && w.first.lo < sp.hi && sp.lo < w.first.hi &&
+              w.second > when[i]) {
+            when[i] = w.second;
+            rev[i] = !prev.ops[w.second].reverse;
+          }
+      }
+    std::vector<size_t> idx(n);
+    for (size_t i = 0; i < n; ++i) idx[i] = i;
+    std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return when[a] > when[b]; });
+    std::vector<Op> ops;
+    ops.reserve(n);
+    for (size_t i : idx) {
+      ops.push_back(cur.ops[i]);
+      ops.back().reverse = when[i] >= 0 && rev[i];
+    }
+    cur.ops = std::move(ops);
+  }
+}
+
 PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std::string* why) {
   const PlanKey key = plan_key(pa);
   {
@@ -602,6 +667,7 @@ PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std
   auto plan = std::make_shared<Plan>();
   const PlanStatus ps = build_plan(pa, plan.get(), why);
   if (ps != PlanStatus::Ok) return ps;
+  order_for_reuse(plan.get());
   std::lock_guard<std::mutex> lk(g_plan_mu);
   if (g_plans.size() >= 256) g_plans.clear();
   g_plans.emplace(key, plan);
