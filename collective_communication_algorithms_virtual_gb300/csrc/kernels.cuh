@@ -154,6 +154,33 @@ __device__ __forceinline__ uint4 ldv(const void* p) {
   if constexpr (COH) return ld16_cg(p);
   else return ld16(p);
 }
+// Loads whose lines are not read again (the mixed 16-bit kernel's sources:
+// each partial is consumed once) marked evict-first in L2, leaving room for
+// the results a step keeps for the next one.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+template <bool COH>
+__device__ __forceinline__ uint4 ldv_once(const void* p) {
+  if constexpr (COH) return ld16_cg(p);
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(l2_evict_first()));
+  return v;
+}
+template <bool COH>
+__device__ __forceinline__ W8 ldv32_once(const void* p) {
+  if constexpr (COH) return ldv32<COH>(p);
+  W8 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]),
+                 "=r"(v.w[7])
+               : "l"(p), "l"(l2_evict_first()));
+  return v;
+}
 // keep: results the next step reads take the default L2 policy instead of
 // streaming (evict-first), so that they can still be in L2 when it does.
 __device__ __forceinline__ void st16_sel(void* p, uint4 v, bool keep) {
@@ -484,13 +511,13 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, 
             const int64_t g = g0 + u * kThreads;
             if (g < gend) {
               if (f32 && a32) {
-                raw[j][u] = ldv32<COH>(s + g * 32);
+                raw[j][u] = ldv32_once<COH>(s + g * 32);
               } else if (f32) {
-                const uint4 a = ldv<COH>(s + g * 32), b = ldv<COH>(s + g * 32 + 16);
+                const uint4 a = ldv_once<COH>(s + g * 32), b = ldv_once<COH>(s + g * 32 + 16);
                 raw[j][u].w[0] = a.x; raw[j][u].w[1] = a.y; raw[j][u].w[2] = a.z; raw[j][u].w[3] = a.w;
                 raw[j][u].w[4] = b.x; raw[j][u].w[5] = b.y; raw[j][u].w[6] = b.z; raw[j][u].w[7] = b.w;
               } else {
-                const uint4 v = ldv<COH>(s + g * 16);
+                const uint4 v = ldv_once<COH>(s + g * 16);
                 raw[j][u].w[0] = v.x; raw[j][u].w[1] = v.y; raw[j][u].w[2] = v.z; raw[j][u].w[3] = v.w;
               }
             }
