@@ -831,6 +831,11 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
     const int64_t gbeg = tr * tg, gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
     return Tile{&o, run, gbeg, static_cast<uint32_t>((gend - gbeg) * 16)};
   };
+  // stores: evict first in L2, as the streaming stores of the other paths,
+  // unless the next step reads them (keep); loads: read once, evict first
+  uint64_t evict_first, evict_normal;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(evict_normal));
   auto load = [&](int64_t i) {
     const int k = static_cast<int>(i % kCopyStages);
     const Tile x = tile(i);
@@ -838,16 +843,12 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bars + k)), "r"(x.bytes)
                  : "memory");
     if (DRILL && i == 0) return;
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
                      smem_addr(stage + k * kCopyTileBytes)),
-                 "l"(src), "r"(x.bytes), "r"(smem_addr(bars + k))
+                 "l"(src), "r"(x.bytes), "r"(smem_addr(bars + k)), "l"(evict_first)
                  : "memory");
   };
-  // stores: evict first in L2, as the streaming stores of the other paths,
-  // unless the next step reads them (keep)
-  uint64_t evict_first, evict_normal;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(evict_normal));
+
   int64_t issued = 0;
   for (; issued < n && issued < kCopyStages; ++issued) load(issued);
   int64_t i = 0;
