@@ -25,6 +25,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 #include "vc.h"
 
@@ -65,7 +66,6 @@ struct __align__(16) OpDesc {
   uint8_t vec;      // 1: vector path
   uint8_t esz;      // copy: element size in bytes
   uint8_t upt;      // vector path: groups per thread in one tile (1, 2, 4; 8 in the bulk-copy pipeline)
-  uint8_t rev;      // per-step kernels: walk this operation's tiles last to first
   uint8_t keep;     // the next step reads the results: store them with the default L2 policy
 };
 
@@ -73,7 +73,8 @@ template <int OPS, int PTRS>
 struct __align__(16) LaunchParams {
   uint32_t nops;    // operations in use
   uint32_t ntiles;  // tiles of the launch
-  uint32_t pad[2];
+  uint32_t rev;     // walk the launch's tiles last to first (the previous step's latest writes first)
+  uint32_t pad;
   OpDesc op[OPS];
   const void* ptr[PTRS];
 };
@@ -139,15 +140,16 @@ __device__ __forceinline__ W8 ldv32(const void* p) {
                  : "l"(p));
   return v;
 }
-template <bool COH>
-__device__ __forceinline__ void stv32(void* p, const W8& v, bool keep = false) {
-  // plain (default L2 policy) when coherent or kept, else streaming; one store under a predicate
-  asm volatile("{\n\t.reg .pred k;\n\tsetp.ne.u32 k, %9, 0;\n\t"
-               "@k st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
-               "@!k st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t}" ::"l"(p),
-               "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7]),
-               "r"(static_cast<uint32_t>(COH || keep))
-               : "memory");
+template <bool COH, bool KEEP = false>
+__device__ __forceinline__ void stv32(void* p, const W8& v) {
+  if constexpr (COH || KEEP)
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                 "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+  else
+    asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                 "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
 }
 template <bool COH>
 __device__ __forceinline__ uint4 ldv(const void* p) {
@@ -181,19 +183,26 @@ __device__ __forceinline__ W8 ldv32_once(const void* p) {
                : "l"(p), "l"(l2_evict_first()));
   return v;
 }
-// keep: results the next step reads take the default L2 policy instead of
+// KEEP: results the next step reads take the default L2 policy instead of
 // streaming (evict-first), so that they can still be in L2 when it does.
-__device__ __forceinline__ void st16_sel(void* p, uint4 v, bool keep) {
-  asm volatile("{\n\t.reg .pred k;\n\tsetp.ne.u32 k, %5, 0;\n\t"
-               "@k st.global.v4.u32 [%0], {%1,%2,%3,%4};\n\t"
-               "@!k st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};\n\t}" ::"l"(p),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(static_cast<uint32_t>(keep))
-               : "memory");
+template <bool COH, bool KEEP = false>
+__device__ __forceinline__ void stv(void* p, uint4 v) {
+  if constexpr (COH || KEEP) st16_wb(p, v);
+  else st16(p, v);
 }
-template <bool COH>
-__device__ __forceinline__ void stv(void* p, uint4 v, bool keep = false) {
-  if constexpr (COH) st16_wb(p, v);
-  else st16_sel(p, v, keep);
+// Runs f with the store policy as a compile-time flag, chosen once per tile
+// (a uniform branch).  Chosen per store, as a store pair under a predicate,
+// each store took two issue slots: the fused AllReduce (eight destinations)
+// measured 0.5 us slower at 1 KiB per rank and 12% at 4 MiB.  Coherent
+// kernels have one form.
+// FAN: kernels with the bulk-store path run the fused one-step calls, whose
+// results nothing reads again: one streaming form (with both, that kernel's
+// schedule changed and the fused AllReduce measured 2% slower).
+template <bool COH, bool FAN = false, class F>
+__device__ __forceinline__ void keep_stores(bool keep, F&& f) {
+  if constexpr (COH || FAN) f(std::false_type{});
+  else if (keep) f(std::true_type{});
+  else f(std::false_type{});
 }
 
 template <int OP>
@@ -318,12 +327,14 @@ __device__ __forceinline__ void tile_copy(const OpDesc& o, const PT& ptr, int64_
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u)
     if (u * kThreads < lim) v[u] = ldv<COH>(s + u * kThreads * 16);
-  for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + off;
+  keep_stores<COH, FAN>(keep, [&](auto k) {
+    for (int d = 0; d < o.nd; ++d) {
+      char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride + off;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, v[u], keep);
-  }
+      for (int u = 0; u < kUnroll; ++u)
+        if (u * kThreads < lim) stv<COH, decltype(k)::value>(dp + u * kThreads * 16, v[u]);
+    }
+  });
 }
 
 // fp32 and int32: 4 elements per 16-byte group.  The loads of SB sources are
@@ -429,12 +440,14 @@ __device__ __forceinline__ void tile_4b(const OpDesc& o, const PT& ptr, int64_t 
   }
   const bool keep = FAN ? static_cast<bool>(o.keep) : keep_early;
   const int64_t doff = run * o.dstride + (gbeg + lane()) * 16;
-  for (int d = 0; d < o.nd; ++d) {
-    char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
+  keep_stores<COH, FAN>(keep, [&](auto k) {
+    for (int d = 0; d < o.nd; ++d) {
+      char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + doff;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (u * kThreads < lim) stv<COH>(dp + u * kThreads * 16, acc[u], keep);
-  }
+      for (int u = 0; u < kUnroll; ++u)
+        if (u * kThreads < lim) stv<COH, decltype(k)::value>(dp + u * kThreads * 16, acc[u]);
+    }
+  });
 }
 
 // Adds one loaded group of 8 values to the accumulator (or starts it).
@@ -449,9 +462,9 @@ __device__ __forceinline__ void accumulate8(float* acc, const float* f, bool fir
   }
 }
 
-template <bool F16, int U, bool COH, class PT>
+template <bool F16, int U, bool COH, bool KEEP, class PT>
 __device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, int64_t run, int64_t g0, int64_t gend,
-                                                float (&acc)[U][8], bool keep) {
+                                                float (&acc)[U][8]) {
   for (int d = 0; d < o.nd; ++d) {
     char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + run * o.dstride;
     const bool f32 = (o.dmask >> d) & 1;
@@ -465,16 +478,16 @@ __device__ __forceinline__ void store_half_mode(const OpDesc& o, const PT& ptr, 
             W8 v;
 #pragma unroll
             for (int i = 0; i < 8; ++i) v.w[i] = __float_as_uint(acc[u][i]);
-            stv32<COH>(dp + g * 32, v, keep);
+            stv32<COH, KEEP>(dp + g * 32, v);
           } else {
-            stv<COH>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
-                                             __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])), keep);
-            stv<COH>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
-                                                  __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])), keep);
+            stv<COH, KEEP>(dp + g * 32, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
+                                                   __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
+            stv<COH, KEEP>(dp + g * 32 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
+                                                        __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
           }
         } else {
-          stv<COH>(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
-                                           pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])), keep);
+          stv<COH, KEEP>(dp + g * 16, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
+                                                 pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
         }
       }
     }
@@ -545,7 +558,7 @@ __device__ __forceinline__ void tile_half_mixed(const OpDesc& o, const PT& ptr, 
         }
       }
     }
-    store_half_mode<F16, kUnrollBF, COH>(o, ptr, run, g0, gend, acc, keep);
+    keep_stores<COH>(keep, [&](auto k) { store_half_mode<F16, kUnrollBF, COH, decltype(k)::value>(o, ptr, run, g0, gend, acc); });
   }
 }
 
@@ -595,7 +608,7 @@ __device__ __forceinline__ void tile_half_pure(const OpDesc& o, const PT& ptr, i
         }
       }
     }
-    store_half_mode<F16, kUnrollBP, COH>(o, ptr, run, g0, gend, acc, keep);
+    keep_stores<COH>(keep, [&](auto k) { store_half_mode<F16, kUnrollBP, COH, decltype(k)::value>(o, ptr, run, g0, gend, acc); });
   }
 }
 
@@ -738,16 +751,19 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ 
   for (int i = threadIdx.x; i < nops; i += kThreads) s_tile0[i] = p.op[i].tile0;
   __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+  // (kernels with the bulk-store path, which serve fused and fan-out
+  // operations, keep the forward walk: their code stays as it was, and the
+  // fused AllReduce measured 2% slower with the direction select in it)
+  const bool rev = !FAN && p.rev != 0;
+  for (uint32_t t0 = blockIdx.x; t0 < p.ntiles; t0 += gridDim.x) {
+    const uint32_t t = rev ? p.ntiles - 1 - t0 : t0;
     int lo = 0, hi = nops - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_tile0[mid] <= t) lo = mid; else hi = mid - 1;
     }
     const OpDesc& o = p.op[lo];
-    const void* const* ptr = p.ptr + o.p0;
-    const uint32_t lt = t - o.tile0;
-    run_tile<MODE, OP, false, SB, ELEM, FAN>(o, ptr, o.rev ? static_cast<uint32_t>(o.tpr * o.nb) - 1 - lt : lt);
+    run_tile<MODE, OP, false, SB, ELEM, FAN>(o, p.ptr + o.p0, t - o.tile0);
   }
   // outstanding bulk stores of fan-out copies finish before the block exits
   if (FAN && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -817,16 +833,15 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
     uint32_t bytes;
   };
   auto tile = [&](int64_t i) {
-    const uint32_t t = static_cast<uint32_t>(blockIdx.x + i * gridDim.x);
+    const uint32_t t0 = static_cast<uint32_t>(blockIdx.x + i * gridDim.x);
+    const uint32_t t = p.rev ? p.ntiles - 1 - t0 : t0;
     int lo = 0, hi = nops - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_tile0[mid] <= t) lo = mid; else hi = mid - 1;
     }
     const OpDesc& o = p.op[lo];
-    const uint32_t lt0 = t - o.tile0;
-    const uint32_t lt = o.rev ? static_cast<uint32_t>(o.tpr * o.nb) - 1 - lt0 : lt0;
-    const uint32_t run = lt / o.tpr, tr = lt - run * o.tpr;
+    const uint32_t lt = t - o.tile0, run = lt / o.tpr, tr = lt - run * o.tpr;
     const int64_t tg = int64_t(o.upt) * kThreads;
     const int64_t gbeg = tr * tg, gend = gbeg + tg < o.groups ? gbeg + tg : o.groups;
     return Tile{&o, run, gbeg, static_cast<uint32_t>((gend - gbeg) * 16)};

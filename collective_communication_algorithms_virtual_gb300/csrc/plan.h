@@ -42,7 +42,6 @@ struct Op {
   int64_t nb = 1;       // runs
   int64_t sstride = 0;  // bytes between runs, every source
   int64_t dstride = 0;  // bytes between runs, every destination
-  bool reverse = false; // execution order only: walk the operation's tiles from the last one
   bool keep = false;    // execution only: the next step reads the results (keep them in L2)
 };
 
@@ -50,6 +49,7 @@ struct Step {
   Mode mode;
   std::vector<Op> ops;
   RedOp red = RedOp::Sum;  // how a reduction step combines its sources
+  bool reverse = false;    // execution order only: walk the step's tiles from the last one
 };
 
 struct Plan {
