@@ -33,6 +33,9 @@ from .binding import (  # noqa: F401
     vc_device_errors,
     vc_copy_selftest,
     SINGLE_LAUNCH_ALWAYS,
+    vc_set_reuse_order,
+    vc_get_reuse_order,
+    REUSE_ORDER_NEVER,
     vc_set_copy_pipeline,
     vc_get_copy_pipeline,
     COPY_PIPELINE_NEVER,

@@ -110,6 +110,10 @@ def lib() -> ctypes.CDLL:
         L.vc_set_single_launch.restype = I
         L.vc_get_single_launch.argtypes = [ctypes.POINTER(Z)]
         L.vc_get_single_launch.restype = I
+        L.vc_set_reuse_order.argtypes = [Z]
+        L.vc_set_reuse_order.restype = I
+        L.vc_get_reuse_order.argtypes = [ctypes.POINTER(Z)]
+        L.vc_get_reuse_order.restype = I
         L.vc_set_copy_pipeline.argtypes = [Z]
         L.vc_set_copy_pipeline.restype = I
         L.vc_get_copy_pipeline.argtypes = [ctypes.POINTER(Z)]
@@ -304,6 +308,21 @@ def vc_get_single_launch() -> int:
 
 
 SINGLE_LAUNCH_ALWAYS = (1 << 64) - 1
+
+
+def vc_set_reuse_order(min_step_bytes: int) -> None:
+    """Steps after one writing at least this many bytes are ordered for L2 reuse
+    (0: every step; REUSE_ORDER_NEVER: none).  Clears the plan cache."""
+    check(lib().vc_set_reuse_order(int(min_step_bytes)))
+
+
+def vc_get_reuse_order() -> int:
+    v = ctypes.c_size_t(0)
+    check(lib().vc_get_reuse_order(ctypes.byref(v)))
+    return v.value
+
+
+REUSE_ORDER_NEVER = (1 << 64) - 1
 
 
 def vc_set_copy_pipeline(min_bytes: int) -> None:

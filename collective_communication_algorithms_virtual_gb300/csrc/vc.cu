@@ -57,6 +57,9 @@ bool pdl_enabled() {
 // Copy launches writing at least this many bytes take the bulk-copy pipeline
 // (vc_set_copy_pipeline).
 std::atomic<size_t> g_copy_pipeline{VC_COPY_PIPELINE_DEFAULT};
+// Steps after one that writes at least this many bytes are ordered for L2
+// reuse (vc_set_reuse_order); read when a plan is built.
+std::atomic<size_t> g_reuse_min{VC_REUSE_ORDER_DEFAULT};
 bool log_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("VC_LOG");
@@ -597,13 +600,12 @@ PlanKey plan_key(const PlanArgs& pa) {
 // walked that way, the one whose sources the previous step wrote last comes
 // first: every step starts on the most recent lines.  Operations whose results
 // the next step reads are marked keep and stored with the default L2 policy
-// instead of streaming.  Only where a step writes at least kReuseMinBytes:
+// instead of streaming.  Only where a step writes at least the set minimum:
 // below that everything stays in L2 anyway, and the reordered walks and plain
 // stores measured 3-7% slower (ring, 8 ranks, 1-8 MiB per rank), while from
 // 16 MiB per step on they win.  Operations of a step are independent, and
 // neither their order, a tile's order nor a cache policy changes any
 // element's association.
-constexpr int64_t kReuseMinBytes = int64_t(16) << 20;
 int64_t step_written_bytes(const Step& s) {
   int64_t b = 0;
   for (const Op& op : s.ops)
@@ -611,6 +613,9 @@ int64_t step_written_bytes(const Step& s) {
   return b;
 }
 void order_for_reuse(Plan* plan) {
+  const size_t min_bytes = g_reuse_min.load(std::memory_order_relaxed);
+  if (min_bytes == SIZE_MAX) return;
+  auto small = [&](const Step& s) { return static_cast<size_t>(step_written_bytes(s)) < min_bytes; };
   struct Span {
     Buf buf;
     int owner;
@@ -625,7 +630,7 @@ void order_for_reuse(Plan* plan) {
     return a.buf == b.buf && a.owner == b.owner && a.lo < b.hi && b.lo < a.hi;
   };
   for (size_t s = 0; s + 1 < plan->steps.size(); ++s) {
-    if (step_written_bytes(plan->steps[s]) < kReuseMinBytes) continue;
+    if (small(plan->steps[s])) continue;
     std::vector<Span> reads;
     for (const Op& op : plan->steps[s + 1].ops)
       for (const Operand& src : op.src) reads.push_back(span(src, op, op.sstride));
@@ -637,7 +642,7 @@ void order_for_reuse(Plan* plan) {
   }
   for (size_t s = 1; s < plan->steps.size(); ++s) {
     const Step& prev = plan->steps[s - 1];
-    if (step_written_bytes(prev) < kReuseMinBytes) continue;
+    if (small(prev)) continue;
     Step& cur = plan->steps[s];
     // when each of the previous step's operations ran: its place in the list,
     // counted from the end if that step walked backwards
@@ -1669,6 +1674,19 @@ VC_EXPORT vc_status_t vc_get_single_launch(size_t* max_step_bytes) {
   if (!max_step_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
   std::lock_guard<std::mutex> lk(g_sl_mu);
   *max_step_bytes = g_sl_limit;
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_set_reuse_order(size_t min_step_bytes) {
+  g_reuse_min.store(min_step_bytes, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_plan_mu);  // cached plans carry the order they were built with
+  g_plans.clear();
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_get_reuse_order(size_t* min_step_bytes) {
+  if (!min_step_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+  *min_step_bytes = g_reuse_min.load(std::memory_order_relaxed);
   return VC_SUCCESS;
 }
 

@@ -398,6 +398,22 @@ vc_status_t vc_set_copy_pipeline(size_t min_bytes);
 vc_status_t vc_get_copy_pipeline(size_t* min_bytes);
 
 /*
+ * L2 reuse order (no counterpart on the source pages: an execution choice
+ * that leaves every result unchanged, bit for bit).  A step that follows one
+ * writing at least min_step_bytes walks its tiles in the direction opposite
+ * to that step, with its (independent) operations listed so that the one
+ * whose inputs were written last comes first; results the next step reads
+ * are stored with the default L2 policy instead of streaming.  The step then
+ * starts on lines still in L2.  Below the default, VC_REUSE_ORDER_DEFAULT,
+ * the data stay in L2 anyway and the reordering measured slower on a GB300.
+ * 0 orders every step, SIZE_MAX none.  Process-wide; applies to plans built
+ * after the call (the plan cache is cleared).
+ */
+#define VC_REUSE_ORDER_DEFAULT ((size_t)16 << 20)
+vc_status_t vc_set_reuse_order(size_t min_step_bytes);
+vc_status_t vc_get_reuse_order(size_t* min_step_bytes);
+
+/*
  * Device error word.  Waits for `stream` (after the work enqueued so far),
  * then reads and clears the word: bit 1 set when a bulk-copy pipeline's wait
  * for a tile's load gave up (the launch then stopped issuing copies and

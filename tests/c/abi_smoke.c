@@ -35,6 +35,9 @@ int main(void) {
   vc_set_copy_pipeline(VC_COPY_PIPELINE_DEFAULT);
   if (vc_get_single_launch(&v) != VC_SUCCESS || v != VC_SINGLE_LAUNCH_DEFAULT) return 11;
   if (vc_get_copy_pipeline(NULL) != VC_ERR_INVALID_ARG) return 12;
+  if (vc_get_reuse_order(&v) != VC_SUCCESS || v != VC_REUSE_ORDER_DEFAULT) return 13;
+  if (vc_set_reuse_order(0) != VC_SUCCESS || vc_get_reuse_order(&v) != VC_SUCCESS || v != 0) return 14;
+  vc_set_reuse_order(VC_REUSE_ORDER_DEFAULT);
   printf("ok %d\n", vc_version());
   return 0;
 }

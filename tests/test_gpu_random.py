@@ -6,7 +6,8 @@ one in ten 5000..100000 for several tiles per operation),
 data type, reduction op, root, in place or not, 16-byte aligned or not, and
 the execution form (default, forced single launch, one launch per step;
 the last with the bulk-copy pipeline taken by every aligned copy launch on
-odd-numbered calls and by none on even ones).
+odd-numbered calls and by none on even ones, and with the L2 reuse order
+forced onto every step on calls numbered 1 mod 4).
 Each must equal the oracle's simulation of the same schedule bit for bit,
 with the canary bands around every buffer intact.  Shapes a schedule does
 not define (the library and the oracle both refuse them) are skipped.
@@ -40,9 +41,11 @@ def _lib():
     vc.lib()
     old = vc.vc_get_single_launch()
     old_cp = vc.vc_get_copy_pipeline()
+    old_ro = vc.vc_get_reuse_order()
     yield
     vc.vc_set_single_launch(old)
     vc.vc_set_copy_pipeline(old_cp)
+    vc.vc_set_reuse_order(old_ro)
     assert vc.vc_device_errors() == 0
 
 
@@ -140,6 +143,9 @@ def test_random_calls_match_oracle():
         vc.vc_set_single_launch({"default": 768 << 10, "single": vc.SINGLE_LAUNCH_ALWAYS, "per_step": 0}[form])
         if form == "per_step":
             vc.vc_set_copy_pipeline(0 if i % 2 else vc.COPY_PIPELINE_NEVER)
+            want_reuse = 0 if i % 4 == 1 else 16 << 20  # the reuse order forced on a quarter of them
+            if vc.vc_get_reuse_order() != want_reuse:
+                vc.vc_set_reuse_order(want_reuse)
         else:
             vc.vc_set_copy_pipeline(256 << 20)
         what = (i, coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks)
