@@ -92,6 +92,10 @@ def lib() -> ctypes.CDLL:
         L.vc_plan_describe.argtypes = [I, I, I, Z, I, I, I, I, I, ctypes.POINTER(PlanEntry), Z,
                                        ctypes.POINTER(Z), ctypes.POINTER(Z), ctypes.POINTER(I)]
         L.vc_plan_describe.restype = I
+        U32P, U8P = ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint8)
+        L.vc_plan_exec_order.argtypes = [I, I, I, Z, I, I, I, I, I, U32P, U8P, Z, U8P, Z, ctypes.POINTER(Z),
+                                         ctypes.POINTER(I)]
+        L.vc_plan_exec_order.restype = I
         L.vc_trace_enable.argtypes = [I]
         L.vc_trace_enable.restype = I
         L.vc_trace_read.argtypes = [ctypes.POINTER(TraceRecord), Z, ctypes.POINTER(Z)]
@@ -387,3 +391,32 @@ def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int
     check(L.vc_plan_describe(*args, buf, need.value, ctypes.byref(need), ctypes.byref(scratch),
                              ctypes.byref(steps)))
     return list(buf[:need.value]), scratch.value, steps.value
+
+
+def vc_plan_exec_order(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,
+                       nchunks: int = 0, op="sum"):
+    """The order the library executes the plan in (the L2 reuse order): per
+    step, the operations' indices as vc_plan_describe numbers them, their keep
+    flags, and whether the step walks its tiles backwards.  Returns
+    (order, keep, reverse) with order and keep lists of lists per step; host
+    only, needs no GPU."""
+    L = lib()
+    nops, steps = ctypes.c_size_t(0), ctypes.c_int(0)
+    args = (_code(COLLS, coll), _code(ALGOS, algo), int(nranks), int(count), _code(DTYPES, dtype),
+            _code(OPS, op), int(root), int(bool(inplace)), int(nchunks))
+    check(L.vc_plan_exec_order(*args, None, None, 0, None, 0, ctypes.byref(nops), ctypes.byref(steps)))
+    order = (ctypes.c_uint32 * max(1, nops.value))()
+    keep = (ctypes.c_uint8 * max(1, nops.value))()
+    rev = (ctypes.c_uint8 * max(1, steps.value))()
+    check(L.vc_plan_exec_order(*args, order, keep, nops.value, rev, steps.value, ctypes.byref(nops),
+                               ctypes.byref(steps)))
+    entries, _, _ = vc_plan_describe(coll, algo, nranks, count, dtype, root, inplace, nchunks, op)
+    per_step = [0] * steps.value
+    for e in entries:
+        per_step[e.step] = max(per_step[e.step], e.op + 1)
+    out_order, out_keep, k = [], [], 0
+    for n in per_step:
+        out_order.append(list(order[k:k + n]))
+        out_keep.append(list(keep[k:k + n]))
+        k += n
+    return out_order, out_keep, list(rev[:steps.value])

@@ -43,6 +43,7 @@ struct Op {
   int64_t sstride = 0;  // bytes between runs, every source
   int64_t dstride = 0;  // bytes between runs, every destination
   bool keep = false;    // execution only: the next step reads the results (keep them in L2)
+  uint32_t built = 0;   // introspection: the operation's index in its step as built
 };
 
 struct Step {

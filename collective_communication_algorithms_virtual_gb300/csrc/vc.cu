@@ -613,6 +613,8 @@ int64_t step_written_bytes(const Step& s) {
   return b;
 }
 void order_for_reuse(Plan* plan) {
+  for (Step& s : plan->steps)
+    for (size_t i = 0; i < s.ops.size(); ++i) s.ops[i].built = static_cast<uint32_t>(i);
   const size_t min_bytes = g_reuse_min.load(std::memory_order_relaxed);
   if (min_bytes == SIZE_MAX) return;
   auto small = [&](const Step& s) { return static_cast<size_t>(step_written_bytes(s)) < min_bytes; };
@@ -1405,33 +1407,41 @@ VC_EXPORT double vc_busbw_factor(vc_coll_t coll, int nranks) {
   return 0.0;
 }
 
+// The plan of a host-only description call (vc_plan_describe, vc_plan_exec_order).
+vc_status_t describe_plan(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype, vc_op_t op,
+                          int root, int inplace, int nchunks, Plan* plan) {
+  if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
+  PlanArgs pa;
+  pa.coll = static_cast<Coll>(static_cast<int>(coll));
+  bool is_auto = false;
+  vc_status_t rc = to_algo(algo, &pa.algo, &is_auto);
+  if (rc == VC_SUCCESS) rc = to_dt(dtype, &pa.dt);
+  if (rc == VC_SUCCESS) rc = to_op(op, &pa.op);
+  if (rc != VC_SUCCESS) return rc;
+  pa.nranks = nranks;
+  pa.count = static_cast<int64_t>(count);
+  pa.root = root;
+  pa.inplace = inplace != 0;
+  if (is_auto) {
+    rc = resolve_auto(&pa);
+    if (rc != VC_SUCCESS) return rc;
+  }
+  if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
+    pa.nchunks = nchunks > 0 ? nchunks : default_chunks(pa.algo, nranks, pa.count, pa.dt, current_cost());
+  std::string why;
+  const PlanStatus ps = build_plan(pa, plan, &why);
+  if (ps != PlanStatus::Ok) return plan_status(ps, why);
+  return VC_SUCCESS;
+}
+
 VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
                                        vc_dtype_t dtype, vc_op_t op, int root, int inplace, int nchunks,
                                        vc_plan_entry_t* entries,
                                        size_t capacity, size_t* n_entries, size_t* scratch_bytes, int* n_steps) {
   return entry([&]() -> vc_status_t {
-    if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
-    PlanArgs pa;
-    pa.coll = static_cast<Coll>(static_cast<int>(coll));
-    bool is_auto = false;
-    vc_status_t rc = to_algo(algo, &pa.algo, &is_auto);
-    if (rc == VC_SUCCESS) rc = to_dt(dtype, &pa.dt);
-    if (rc == VC_SUCCESS) rc = to_op(op, &pa.op);
-    if (rc != VC_SUCCESS) return rc;
-    pa.nranks = nranks;
-    pa.count = static_cast<int64_t>(count);
-    pa.root = root;
-    pa.inplace = inplace != 0;
-    if (is_auto) {
-      rc = resolve_auto(&pa);
-      if (rc != VC_SUCCESS) return rc;
-    }
-    if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
-      pa.nchunks = nchunks > 0 ? nchunks : default_chunks(pa.algo, nranks, pa.count, pa.dt, current_cost());
     Plan plan;
-    std::string why;
-    const PlanStatus ps = build_plan(pa, &plan, &why);
-    if (ps != PlanStatus::Ok) return plan_status(ps, why);
+    const vc_status_t rc = describe_plan(coll, algo, nranks, count, dtype, op, root, inplace, nchunks, &plan);
+    if (rc != VC_SUCCESS) return rc;
     size_t need = 0;
     for (const Step& s : plan.steps)
       for (const Op& op : s.ops) need += op.src.size() + op.dst.size();
@@ -1463,6 +1473,35 @@ VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nrank
             e.stride_bytes = role == 0 ? op.sstride : op.dstride;
           }
         }
+      }
+    }
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_plan_exec_order(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype,
+                                         vc_op_t op, int root, int inplace, int nchunks, uint32_t* order,
+                                         uint8_t* keep, size_t op_capacity, uint8_t* reverse, size_t step_capacity,
+                                         size_t* n_ops, int* n_steps) {
+  return entry([&]() -> vc_status_t {
+    Plan plan;
+    const vc_status_t rc = describe_plan(coll, algo, nranks, count, dtype, op, root, inplace, nchunks, &plan);
+    if (rc != VC_SUCCESS) return rc;
+    order_for_reuse(&plan);
+    size_t nops = 0;
+    for (const Step& s : plan.steps) nops += s.ops.size();
+    if (n_ops) *n_ops = nops;
+    if (n_steps) *n_steps = static_cast<int>(plan.steps.size());
+    if (!order && !keep && !reverse && op_capacity == 0 && step_capacity == 0) return VC_SUCCESS;
+    if (!order || !keep || !reverse) return fail(VC_ERR_INVALID_ARG, "null output array");
+    if (op_capacity < nops || step_capacity < plan.steps.size()) return fail(VC_ERR_INVALID_ARG, "capacity too small");
+    size_t k = 0;
+    for (size_t si = 0; si < plan.steps.size(); ++si) {
+      reverse[si] = plan.steps[si].reverse ? 1 : 0;
+      for (const Op& o : plan.steps[si].ops) {
+        order[k] = o.built;
+        keep[k] = o.keep ? 1 : 0;
+        ++k;
       }
     }
     return VC_SUCCESS;

@@ -310,6 +310,24 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
                              int* n_steps);
 
 /*
+ * Host-only introspection of the L2 reuse order (vc_set_reuse_order, read at
+ * the call): the plan vc_plan_describe returns, in the order the library
+ * executes it (no counterpart on the source pages).  For the k-th operation
+ * executed (steps in order, a step's operations consecutive):
+ *   order[k]: its index within its step as vc_plan_describe numbers it;
+ *   keep[k]: 1 if its results are stored with the default L2 policy (the
+ *            next step reads them), else 0 (streaming);
+ * reverse[s]: 1 if step s walks its tiles last to first.
+ * *n_ops and *n_steps receive the sizes; null arrays with both capacities 0
+ * ask for the sizes only.  VC_ERR_INVALID_ARG if a capacity is too small.
+ * Needs no GPU.
+ */
+vc_status_t vc_plan_exec_order(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype,
+                               vc_op_t op, int root, int inplace, int nchunks, uint32_t* order, uint8_t* keep,
+                               size_t op_capacity, uint8_t* reverse, size_t step_capacity, size_t* n_ops,
+                               int* n_steps);
+
+/*
  * Launch trace (off by default; host bookkeeping plus two CUDA events per
  * launch while on).  While enabled, every kernel launch the library makes is
  * bracketed by CUDA events recorded on the caller's stream, and a record
