@@ -318,6 +318,10 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  *   keep[k]: 1 if its results are stored with the default L2 policy (the
  *            next step reads them), else 0 (streaming);
  * reverse[s]: 1 if step s walks its tiles last to first.
+ * This is the order of per-step launches; a one-launch plan (vc_set_single_
+ * launch) runs the same operation order with every step walked forward and
+ * plain stores, and launches of multi-destination (fused) operations walk
+ * forward with streaming stores.
  * *n_ops and *n_steps receive the sizes; null arrays with both capacities 0
  * ask for the sizes only.  VC_ERR_INVALID_ARG if a capacity is too small.
  * Needs no GPU.
