@@ -388,9 +388,76 @@ def run_ours(args) -> int:
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = time_oracle(args.cpu_seconds)
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        emit(out, args.details_out)
     barrier(world)
     return 0
+
+
+DETAIL_KEYS = ("per_algo", "sweep", "alpha_beta", "configs")
+FINAL_LINE_MAX = 2048
+
+
+def _r(x, nd=4):
+    """Round floats for the final line (keeps it short); other values pass."""
+    if isinstance(x, float):
+        return float(f"{x:.{nd}g}")
+    if isinstance(x, dict):
+        return {k: _r(v, nd) for k, v in x.items()}
+    if isinstance(x, list):
+        return [_r(v, nd) for v in x]
+    return x
+
+
+def final_line(out: dict) -> dict:
+    """The headline JSON line: the contract's keys, a compact roofline of the
+    dominant kernel, clocks, e2e and the CPU baseline, plus one busbw figure per
+    algorithm.  The detail sections (per-algorithm figures, the message-size
+    sweep, the alpha-beta fit, the other workload configurations) are printed
+    on earlier lines; this one stays under FINAL_LINE_MAX bytes."""
+    line = {k: out[k] for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config")
+            if k in out}
+    line["value"] = _r(out["value"], 6)
+    line["ms_per_step"] = _r(out["ms_per_step"], 6)
+    cfg = dict(out["config"])
+    cfg.pop("inputs", None)
+    line["config"] = cfg
+    rf = out.get("roofline")
+    if rf:
+        line["roofline"] = _r({k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "kernel",
+                                                   "launches", "avg_launch_ms", "algorithmic_bytes_per_launch",
+                                                   "peak_source") if k in rf}, 6)
+    for k in ("gpu_launches", "clocks"):
+        if k in out:
+            line[k] = _r(out[k])
+    if "e2e" in out:
+        line["e2e"] = _r({k: out["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step",
+                                                     "ms_per_step") if k in out["e2e"]})
+    if "cpu_baseline" in out:
+        cb = dict(out["cpu_baseline"])
+        cb["sample"] = cb.get("sample", "")[:200]
+        line["cpu_baseline"] = _r(cb)
+    if "per_algo" in out:
+        line["busbw_256MiB"] = {a: round(v["busbw"], 1) for a, v in out["per_algo"].items()}
+        line["frac_of_measured_256MiB"] = {a: round(v["frac_of_measured"], 3) for a, v in out["per_algo"].items()}
+    line["details"] = "earlier stdout lines, one JSON object per section: " + ",".join(
+        k for k in DETAIL_KEYS if k in out)
+    return line
+
+
+def emit(out: dict, details_out: str | None = None) -> str:
+    """Print every detail section on its own line, then the final line."""
+    for k in ("roofline",) + DETAIL_KEYS:
+        if k in out:
+            print(json.dumps({"detail": k, k: out[k]}), flush=True)
+    if details_out:
+        os.makedirs(os.path.dirname(os.path.abspath(details_out)), exist_ok=True)
+        with open(details_out, "w") as f:
+            json.dump(out, f)
+    s = json.dumps(final_line(out))
+    assert len(s) <= FINAL_LINE_MAX, len(s)
+    print(s, flush=True)
+    return s
 
 
 def time_calls(fn, stream, min_ms=20.0, max_reps=2000):
@@ -699,6 +766,7 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--details-out", default=None, help="also write every section as one JSON file here")
     ap.add_argument("--ref-mib", type=float, default=None,
                     help="reference arm: MiB per rank of the oracle's sample (default: sized to ~2 min)")
     args = ap.parse_args(argv)

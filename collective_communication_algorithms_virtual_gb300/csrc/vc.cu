@@ -1564,6 +1564,8 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64] = {};
 
 vc_status_t noalloc_scratch(int dev, char** out) {
+  if (dev < 0 || dev >= static_cast<int>(sizeof(g_noalloc_ptr) / sizeof(g_noalloc_ptr[0])))
+    return fail(VC_ERR_CUDA, "device index out of range for the fixed scratch table");
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
@@ -1593,16 +1595,18 @@ vc_status_t run_reduce_scatter_noalloc(const void* const* send, void* const* rec
       if (overlap(recv[i], rbytes, send[q], sbytes))
         return fail(VC_ERR_INVALID_ARG, "a receive buffer overlaps a send buffer");
   }
+  // the same cached plan, in the same execution order, as the allocating call
   PlanArgs pa{Coll::ReduceScatter, Algo::Ring, N, rc, dt, 0, false};
-  Plan plan;
+  std::shared_ptr<const Plan> plan_ptr;
   std::string why;
-  const PlanStatus ps = build_plan(pa, &plan, &why);
+  const PlanStatus ps = cached_plan(pa, &plan_ptr, &why);
   if (ps != PlanStatus::Ok) return plan_status(ps, why);
+  const Plan& plan = *plan_ptr;
   if (plan.scratch_bytes > static_cast<int64_t>(VC_NOALLOC_SCRATCH_BYTES))
     return fail(VC_ERR_INVALID_ARG, "vc_reduce_scatter_noalloc needs " + std::to_string(plan.scratch_bytes) +
                                         " bytes of scratch; the fixed array holds " +
                                         std::to_string(VC_NOALLOC_SCRATCH_BYTES) +
-                                        " (2 * nranks * recvcount * 4 must not exceed it)");
+                                        " (nranks * roundup(2 * recvcount * 4, 256) must not exceed it)");
   DeviceState* st = nullptr;
   int dev = 0;
   vc_status_t rc_ = device_state(&st, &dev);
@@ -1615,6 +1619,7 @@ vc_status_t run_reduce_scatter_noalloc(const void* const* send, void* const* rec
   LaunchCtx tc;
   tc.coll = static_cast<int>(Coll::ReduceScatter);
   tc.algo = static_cast<int>(Algo::Ring);
+  for (const Step& s : plan.steps) tc.pipeline &= s.mode != Mode::BF16 && s.mode != Mode::F16;
   for (size_t si = 0; si < plan.steps.size(); ++si) {
     tc.step = static_cast<int>(si);
     rc_ = launch_step(st, plan.steps[si], b, stream, &launches, tc);

@@ -460,17 +460,26 @@ vc_status_t vc_copy_selftest(vc_stream_t stream, uint32_t* flags);
  * allocator or an out-of-memory handler, real-time loops that forbid
  * cudaMalloc and pool growth, or hosts whose memory budget is fixed ahead of
  * time.  It computes exactly what vc_reduce_scatter(..., VC_ALGO_RING, ...)
- * computes (same schedule, same results bit for bit), but its partial sums
- * live in one fixed array that the library reserves in every GPU's memory
- * when the library is loaded on it, instead of in the library's pool.
+ * computes (same schedule and execution order, same results bit for bit),
+ * but its partial sums live in one fixed array that the library places in
+ * each GPU's memory when its device code is loaded there, instead of in the
+ * library's pool.
  *
+ *   op: VC_SUM only; VC_MAX and VC_MIN return VC_ERR_UNSUPPORTED.
+ *   dtype: VC_FLOAT32, VC_BFLOAT16, VC_FLOAT16 or VC_INT32.
  *   send[q]: nranks*recvcount elements; recv[r]: recvcount elements; no in-place.
- *   Scratch needed: 2 * nranks * recvcount * 4 bytes (fp32 and bf16 partials
- *   are fp32, int32 partials int32), at most VC_NOALLOC_SCRATCH_BYTES
- *   (16 MiB); larger calls return VC_ERR_INVALID_ARG and enqueue nothing.
+ *   Scratch needed: nranks * roundup(2 * recvcount * 4, 256) bytes (two
+ *   4-byte partial slots per rank -- 16-bit partials are kept in fp32 --
+ *   each rank's pair rounded up to 256 bytes), at most
+ *   VC_NOALLOC_SCRATCH_BYTES (16 MiB); larger calls return VC_ERR_INVALID_ARG
+ *   and enqueue nothing.
  *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress) with that device current.  With CUDA's lazy module
+ *   loading that lookup (or the first launch of any of this library's
+ *   kernels) is also when the device code, and with it the array, is loaded
+ *   onto the device, which takes device memory.  So make the first call of
+ *   this entry point on each device outside the code that must not allocate,
+ *   and before any stream capture; later calls allocate nothing.
  *   Every call shares the one array and leaves its last contents behind (no
  *   part of it needs to start at zero: every partial sum is written before
  *   it is read).  Calls whose work overlaps on the GPU -- on two streams, or

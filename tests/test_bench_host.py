@@ -70,3 +70,56 @@ def test_replica_timing_reductions_gloo():
         assert p.exitcode == 0
     for r, mx, sm in res:
         assert mx == 11.0 and sm == 3.0
+
+
+def _stub_result():
+    """A GPU-arm result as run_ours builds it, with full-size detail sections."""
+    algos = ["ring", "rhd", "dbt", "fused"]
+    pt = {"bytes_per_rank": 1 << 20, "us": 30.123456, "us_eager": 36.1, "busbw": 61.2345678, "busbw_eager": 50.1,
+          "steps": 14, "algorithmic_bytes": 36700160, "l2_resident": True}
+    return {
+        "metric": bench.METRIC, "value": 417.123456789, "unit": "GB/s", "n_gpus": 1, "steps": 200, "warmup": 5,
+        "ms_per_step": 4.50412345, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": bench.config_block(256 << 20),
+        "roofline": {"bound": "hbm", "kernel": "step_kernel<sum_f32>", "achieved": 6624.123456, "peak": 6659.6,
+                     "unit": "GB/s", "frac": 0.99465, "peak_source": "measured", "traffic": 1.34e9,
+                     "algorithmic_bytes_per_launch": 1.3997e9, "launches": 2800, "avg_launch_ms": 0.2113,
+                     "frac_of_nominal_8TBs": 0.82, "kernels": {f"k{i}": {"launches": 1, "share": 0.1, "gbs": 1.0}
+                                                               for i in range(12)},
+                     "measured": "x" * 300, "ms_per_step_traced": 4.68},
+        "gpu_launches": 12345,
+        "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 120},
+        "per_algo": {a: {"ms": 1.3, "algbw": 200.1, "busbw": 352.123, "hbm_gbs": 7031.2, "algorithmic_bytes": 1 << 33,
+                         "frac_of_measured": 1.0561, "frac_of_nominal_8TBs": 0.879} for a in algos},
+        "sweep": {a: [dict(pt) for _ in range(19)] for a in algos},
+        "alpha_beta": {"alpha_us": 1.48, "crossovers": {f"{a}/{b}": {"measured_bytes_per_rank": 1 << 25}
+                                                        for a in algos for b in algos}},
+        "configs": {f"cfg{i}": {"ms": 1.0, "busbw": 2.0, "steps": 3, "note": "y" * 200} for i in range(40)},
+        "e2e": {"value": 27.33, "unit": "GB/s", "h2d_bytes_per_step": 2147483648,
+                "d2h_bytes_per_step": 8589934592, "ms_per_step": 68.7, "steps": 8, "pipeline": "z" * 100},
+        "cpu_baseline": {"value": 0.4776, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "s" * 400},
+    }
+
+
+def test_final_line_is_short_and_last(tmp_path):
+    out = _stub_result()
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        s = bench.emit(out, str(tmp_path / "d.json"))
+    lines = [l for l in buf.getvalue().splitlines() if l.strip()]
+    assert lines[-1] == s
+    assert len(s.encode()) <= bench.FINAL_LINE_MAX
+    d = json.loads(s)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "clocks",
+                "gpu_launches"):
+        assert key in d, key
+    assert d["value"] > 0 and d["config"]["workload"] == bench.WORKLOAD
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in d["roofline"], key
+    assert d["e2e"]["h2d_bytes_per_step"] == 2147483648 and d["e2e"]["d2h_bytes_per_step"] == 8589934592
+    # every detail section is on an earlier line, whole
+    sections = {json.loads(l)["detail"] for l in lines[:-1]}
+    assert {"per_algo", "sweep", "alpha_beta", "configs", "roofline"} <= sections
+    with open(tmp_path / "d.json") as f:
+        assert json.load(f)["sweep"] == out["sweep"]
