@@ -1,7 +1,11 @@
 """Oracle for the virtual-rank collectives -- TEST INFRASTRUCTURE ONLY.
 
 A plain, slow, single-threaded CPU model of N ranks exchanging messages step by
-step, written from the three source pages:
+step, written twice from the three source pages: as a C++17 program
+(``sim.cpp``, loaded through ``cxx``), which the GPU tests and the benchmark's
+CPU baseline use, and in numpy (``schedules`` and ``orders``).  The two are
+independent restatements, cross-checked bit for bit on every collective, and
+the pins hold for both.  The pages are:
 
 * the Broadcast/Scatter page, "一对多通信：Broadcast 与 Scatter" (one-to-many
   communication: Broadcast and Scatter), cited below as [Bcast/Scatter page];
@@ -22,7 +26,9 @@ Modules:
 * ``numerics``   -- fp32 / int32 lane arithmetic and the bf16 <-> fp32 rules.
 * ``partition``  -- how a buffer is cut into N chunks.
 * ``translog``   -- the transfer log each schedule writes.
-* ``schedules``  -- every algorithm as a message-passing simulation.
+* ``cxx``        -- the C++ oracle: every schedule, the closed-form trees and
+                    the element conversions (``sim.cpp``, ``sim.h``).
+* ``schedules``  -- every algorithm as a message-passing simulation (numpy).
 * ``orders``     -- the per-element association tree each algorithm produces,
                     stated in closed form and evaluated for sampled elements.
 * ``cost_model`` -- the alpha-beta (Hockney) formulas and busbw factors.

@@ -33,3 +33,15 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+@pytest.fixture(params=["cxx", "numpy"])
+def sim(request):
+    """The oracle a pin runs against: the C++ simulation or the numpy one."""
+    if request.param == "cxx":
+        from oracle import cxx
+
+        return cxx
+    from oracle import schedules
+
+    return schedules

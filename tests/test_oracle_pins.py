@@ -3,8 +3,11 @@
 Pins: the printed tables (binomial Broadcast / Scatter, the N=8 AllReduce
 comparison, busbw factors, latency examples, the 14.4 MB crossover), closed
 forms, brute force on integer data (any association is exact), hand-derived
-order witnesses, library routines for data movement and for bf16 rounding,
-and a planted-fault check that the pins catch a broken schedule.
+order witnesses, library routines for data movement and for bf16 / fp16
+rounding, and a planted-fault check that the pins catch a broken schedule.
+
+Every pin on a schedule runs against both oracles (the ``sim`` fixture: the
+C++ simulation and the numpy one).
 """
 import math
 
@@ -13,7 +16,7 @@ import pytest
 import torch
 
 from oracle import cost_model as cm
-from oracle import numerics, orders, schedules
+from oracle import cxx, numerics, orders, schedules
 from oracle.partition import chunk_elems, chunk_range
 from synthetic_inputs import int32_bits, rank_buffers, small_ints_f32, uniform_pm1_f32
 
@@ -22,20 +25,20 @@ from synthetic_inputs import int32_bits, rank_buffers, small_ints_f32, uniform_p
 # printed tables
 # ----------------------------------------------------------------------------
 
-def test_binomial_broadcast_table_n8(golden):
+def test_binomial_broadcast_table_n8(golden, sim):
     want = sorted((int(s) - 1, int(a), int(b)) for s, a, b in golden("binomial_broadcast_n8.txt"))
     A = np.arange(64, dtype=np.int32)
-    res = schedules.broadcast(A, 8, 0, "binomial", "i32")
+    res = sim.broadcast(A, 8, 0, "binomial", "i32")
     assert res.log.table() == want
     assert res.nsteps == 3
 
 
-def test_binomial_scatter_table_n8(golden):
+def test_binomial_scatter_table_n8(golden, sim):
     rows = golden("binomial_scatter_n8.txt")
     rc = 16
     M = 8 * rc * 4
     A = np.arange(8 * rc, dtype=np.int32)
-    res = schedules.scatter(A, 8, 0, "binomial", "i32")
+    res = sim.scatter(A, 8, 0, "binomial", "i32")
     got = sorted((t.step, t.src, t.dst, tuple(sorted(t.chunks)), t.nbytes) for t in res.log.records)
     want = sorted((int(s) - 1, int(a), int(b), tuple(int(c) for c in ch.split(",")), M // int(den))
                   for s, a, b, ch, den in rows)
@@ -45,25 +48,25 @@ def test_binomial_scatter_table_n8(golden):
     assert res.log.bytes_sent_by(0) == (8 - 1) * M // 8
 
 
-def test_allreduce_compare_table_n8(golden):
+def test_allreduce_compare_table_n8(golden, sim):
     N, count = 8, 8 * 64
     M = count * 4
     xs = rank_buffers("small_ints_f32", 1, N, count)
     for algo, lat, bw in golden("allreduce_compare_n8.txt"):
-        res = schedules.allreduce(xs, algo, "f32")
+        res = sim.allreduce(xs, algo, "f32")
         assert res.nsteps == int(lat), algo
         assert res.log.bandwidth_bytes() / M == pytest.approx(float(bw), rel=0, abs=1e-12), algo
         assert cm.allreduce_latency_coeff(algo, N) == pytest.approx(float(lat))
         assert cm.allreduce_bandwidth_coeff(algo, N) == pytest.approx(float(bw))
 
 
-def test_latency_examples(golden):
+def test_latency_examples(golden, sim):
     for algo, N, lat in golden("latency_examples.txt"):
         assert cm.allreduce_latency_coeff(algo, int(N)) == pytest.approx(float(lat))
     # the schedules themselves at N = 64 (small buffers)
     xs = [np.full(64 * 4, r, dtype=np.int32) for r in range(64)]
-    assert schedules.allreduce(xs, "rhd", "i32").nsteps == 12
-    assert schedules.allreduce(xs, "ring", "i32").nsteps == 126
+    assert sim.allreduce(xs, "rhd", "i32").nsteps == 12
+    assert sim.allreduce(xs, "ring", "i32").nsteps == 126
 
 
 def test_ring_dbt_crossover(golden):
@@ -140,17 +143,17 @@ def test_bcast_lower_bounds():
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("N", [2, 3, 4, 5, 8, 16])
-def test_ring_and_rhd_bytes_sent(N):
+def test_ring_and_rhd_bytes_sent(N, sim):
     count = N * 32
     M = count * 4
     xs = rank_buffers("small_ints_f32", 2, N, count)
-    res = schedules.allreduce(xs, "ring", "f32")
+    res = sim.allreduce(xs, "ring", "f32")
     assert res.nsteps == 2 * (N - 1)
     for r in range(N):
         assert res.log.bytes_sent_by(r) == 2 * (N - 1) * M // N
     assert res.log.bandwidth_bytes() == 2 * (N - 1) * M // N
     if N & (N - 1) == 0:
-        res = schedules.allreduce(xs, "rhd", "f32")
+        res = sim.allreduce(xs, "rhd", "f32")
         L = N.bit_length() - 1
         assert res.nsteps == 2 * L
         for r in range(N):
@@ -162,11 +165,11 @@ def test_ring_and_rhd_bytes_sent(N):
 
 
 @pytest.mark.parametrize("N", [2, 4, 8, 16])
-def test_dbt_levels_and_bandwidth(N):
+def test_dbt_levels_and_bandwidth(N, sim):
     count = N * 32
     M = count * 4
     xs = rank_buffers("small_ints_f32", 3, N, count)
-    res = schedules.allreduce(xs, "dbt", "f32")
+    res = sim.allreduce(xs, "dbt", "f32")
     L = N.bit_length() - 1
     assert res.nsteps == 2 * L
     assert all(t.nbytes == M // 2 for t in res.log.records)
@@ -179,28 +182,28 @@ def test_dbt_levels_and_bandwidth(N):
     assert not (interior["A"] & interior["B"])
 
 
-def test_ring_rs_ag_pieces():
+def test_ring_rs_ag_pieces(sim):
     N, rc = 8, 16
     xs = rank_buffers("small_ints_f32", 4, N, N * rc)
-    rs = schedules.reduce_scatter(xs, "ring", "f32")
+    rs = sim.reduce_scatter(xs, "ring", "f32")
     M = N * rc * 4
     assert rs.nsteps == N - 1 and rs.log.bandwidth_bytes() == (N - 1) * M // N
-    ag = schedules.allgather([np.arange(rc, dtype=np.float32)] * N, "ring", "f32")
+    ag = sim.allgather([np.arange(rc, dtype=np.float32)] * N, "ring", "f32")
     assert ag.nsteps == N - 1 and ag.log.bandwidth_bytes() == (N - 1) * M // N
-    ar = schedules.allreduce(xs, "ring", "f32")
+    ar = sim.allreduce(xs, "ring", "f32")
     assert ar.nsteps == rs.nsteps + ag.nsteps
 
 
-def test_pairwise_and_bruck_rounds():
+def test_pairwise_and_bruck_rounds(sim):
     N, B = 8, 16
     M = N * B * 4
     xs = rank_buffers("uniform_f32", 5, N, N * B)
-    pw = schedules.alltoall(xs, "pairwise", "f32")
+    pw = sim.alltoall(xs, "pairwise", "f32")
     assert pw.nsteps == N - 1
     assert pw.log.bandwidth_bytes() == (N - 1) * M // N
     for i in range(N):
         assert pw.log.bytes_sent_by(i) == (N - 1) * M // N
-    br = schedules.alltoall(xs, "bruck", "f32")
+    br = sim.alltoall(xs, "bruck", "f32")
     assert br.nsteps == 3
     # the page quotes (N-1)/N * M for Bruck's bandwidth term; the rounds carry
     # the blocks with bit k set, 4 of 8 per round at N = 8: 1.5 M, not 0.875 M
@@ -210,39 +213,39 @@ def test_pairwise_and_bruck_rounds():
         assert t.dst == (t.src + (1 << t.step)) % N
 
 
-def test_binomial_bcast_bandwidth():
+def test_binomial_bcast_bandwidth(sim):
     for N in (2, 3, 5, 8, 16):
         A = np.arange(40, dtype=np.int32)
-        res = schedules.broadcast(A, N, 0, "binomial", "i32")
+        res = sim.broadcast(A, N, 0, "binomial", "i32")
         assert res.nsteps == cm.ceil_log2(N)
         assert res.log.bandwidth_bytes() == cm.ceil_log2(N) * 160
 
 
 @pytest.mark.parametrize("N", [8])
-def test_hbm_bytes_closed_forms(N):
+def test_hbm_bytes_closed_forms(N, sim):
     """Algorithmic bytes at N = 8, fp32, M per rank."""
     count = N * 64
     M = count * 4
     xs = rank_buffers("small_ints_f32", 6, N, count)
-    ar = {a: schedules.allreduce(xs, a, "f32").hbm_bytes for a in ("fused", "ring", "rhd", "dbt")}
+    ar = {a: sim.allreduce(xs, a, "f32").hbm_bytes for a in ("fused", "ring", "rhd", "dbt")}
     assert ar == {"fused": 2 * N * M, "ring": 5 * (N - 1) * M, "rhd": 5 * (N - 1) * M, "dbt": 29 * M}
-    assert schedules.reduce_scatter(xs, "fused", "f32").hbm_bytes == (N + 1) * M
-    assert schedules.reduce_scatter(xs, "ring", "f32").hbm_bytes == 3 * (N - 1) * M
+    assert sim.reduce_scatter(xs, "fused", "f32").hbm_bytes == (N + 1) * M
+    assert sim.reduce_scatter(xs, "ring", "f32").hbm_bytes == 3 * (N - 1) * M
     sc = [x[:count // N] for x in xs]
-    assert schedules.allgather(sc, "ring", "f32").hbm_bytes == 2 * N * M
-    assert schedules.allgather(sc, "fused", "f32").hbm_bytes == (N + 1) * M
-    assert schedules.alltoall(xs, "fused", "f32").hbm_bytes == 2 * N * M
-    assert schedules.alltoall(xs, "pairwise", "f32").hbm_bytes == 2 * N * M
-    assert schedules.alltoall(xs, "bruck", "f32").hbm_bytes == 2 * 3 * N * M
+    assert sim.allgather(sc, "ring", "f32").hbm_bytes == 2 * N * M
+    assert sim.allgather(sc, "fused", "f32").hbm_bytes == (N + 1) * M
+    assert sim.alltoall(xs, "fused", "f32").hbm_bytes == 2 * N * M
+    assert sim.alltoall(xs, "pairwise", "f32").hbm_bytes == 2 * N * M
+    assert sim.alltoall(xs, "bruck", "f32").hbm_bytes == 2 * 3 * N * M
     A = xs[0]
-    assert schedules.broadcast(A, N, 0, "fused", "f32").hbm_bytes == (N + 1) * M
-    assert schedules.broadcast(A, N, 0, "binomial", "f32").hbm_bytes == 2 * N * M
-    assert schedules.scatter(A, N, 0, "binomial", "f32").hbm_bytes == 3 * M + 2 * M // N
-    assert schedules.scatter(A, N, 0, "fused", "f32").hbm_bytes == 2 * M
+    assert sim.broadcast(A, N, 0, "fused", "f32").hbm_bytes == (N + 1) * M
+    assert sim.broadcast(A, N, 0, "binomial", "f32").hbm_bytes == 2 * N * M
+    assert sim.scatter(A, N, 0, "binomial", "f32").hbm_bytes == 3 * M + 2 * M // N
+    assert sim.scatter(A, N, 0, "fused", "f32").hbm_bytes == 2 * M
     # bf16 ring with fp32 partials (rounded once on the last ReduceScatter step)
     xb = rank_buffers("small_ints_bf16", 6, N, count)
     Mb = count * 2
-    assert schedules.allreduce(xb, "ring", "bf16").hbm_bytes == 47 * Mb
+    assert sim.allreduce(xb, "ring", "bf16").hbm_bytes == 47 * Mb
 
 
 # ----------------------------------------------------------------------------
@@ -254,7 +257,7 @@ def _exact_sum(xs):
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4])
-def test_bruteforce_allreduce(N):
+def test_bruteforce_allreduce(N, sim):
     for count in range(0, 68):
         xs = [small_ints_f32(7, r, count) for r in range(N)]
         want = _exact_sum(xs).astype(np.float32)
@@ -262,66 +265,66 @@ def test_bruteforce_allreduce(N):
         wantb = _exact_sum([numerics.bf16_to_f32(x) for x in xb]).astype(np.float32)
         xi = [int32_bits(9, r, count) for r in range(N)]
         wanti = (_exact_sum(xi) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
-        for algo in schedules.ALGOS["allreduce"]:
-            res = schedules.allreduce(xs, algo, "f32")
+        for algo in sim.ALGOS["allreduce"]:
+            res = sim.allreduce(xs, algo, "f32")
             for o in res.outputs:
                 assert np.array_equal(o, want), (algo, N, count)
-            res = schedules.allreduce(xb, algo, "bf16")
+            res = sim.allreduce(xb, algo, "bf16")
             for o in res.outputs:
                 assert np.array_equal(numerics.bf16_to_f32(o), wantb), (algo, N, count)
-            res = schedules.allreduce(xi, algo, "i32")
+            res = sim.allreduce(xi, algo, "i32")
             for o in res.outputs:
                 assert np.array_equal(o, wanti), (algo, N, count)
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4])
-def test_bruteforce_reduce_scatter_allgather(N):
+def test_bruteforce_reduce_scatter_allgather(N, sim):
     for rc in range(0, 18):
         xs = [small_ints_f32(10, r, N * rc) for r in range(N)]
         total = _exact_sum(xs).astype(np.float32)
-        for algo in schedules.ALGOS["reduce_scatter"]:
-            res = schedules.reduce_scatter(xs, algo, "f32")
+        for algo in sim.ALGOS["reduce_scatter"]:
+            res = sim.reduce_scatter(xs, algo, "f32")
             for r, o in enumerate(res.outputs):
                 assert np.array_equal(o, total[r * rc:(r + 1) * rc]), (algo, N, rc)
         ins = [int32_bits(11, r, rc) for r in range(N)]
-        for algo in schedules.ALGOS["allgather"]:
-            res = schedules.allgather(ins, algo, "i32")
+        for algo in sim.ALGOS["allgather"]:
+            res = sim.allgather(ins, algo, "i32")
             for o in res.outputs:
                 assert np.array_equal(o, np.concatenate(ins)), (algo, N, rc)
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 7, 8])
-def test_bruteforce_broadcast_scatter(N):
+def test_bruteforce_broadcast_scatter(N, sim):
     for root in range(N):
         for count in (0, 1, 5, 16, 37, 67):
             A = int32_bits(12, root, count)
-            for algo in schedules.ALGOS["broadcast"]:
+            for algo in sim.ALGOS["broadcast"]:
                 for inplace in (False, True):
-                    res = schedules.broadcast(A, N, root, algo, "i32", inplace=inplace)
+                    res = sim.broadcast(A, N, root, algo, "i32", inplace=inplace)
                     for o in res.outputs:
                         assert np.array_equal(o, A), (algo, N, root, count)
         for rc in (0, 1, 3, 8):
             A = int32_bits(13, root, N * rc)
             parts = np.split(A, N) if rc else [A[:0]] * N
-            for algo in schedules.ALGOS["scatter"]:
-                res = schedules.scatter(A, N, root, algo, "i32")
+            for algo in sim.ALGOS["scatter"]:
+                res = sim.scatter(A, N, root, algo, "i32")
                 for r in range(N):
                     assert np.array_equal(res.outputs[r], parts[r]), (algo, N, root, rc)
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6, 7, 8, 16])
-def test_alltoall_against_block_transpose(N):
+def test_alltoall_against_block_transpose(N, sim):
     for B in (0, 1, 3, 8):
         xs = [int32_bits(14, r, N * B) for r in range(N)]
         # library special case: out_j[block i] = in_i[block j] is a transpose of
         # the (source rank, destination block) grid
         grid = np.stack(xs).reshape(N, N, B)
         want = np.transpose(grid, (1, 0, 2)).reshape(N, N * B)
-        for algo in schedules.ALGOS["alltoall"]:
-            res = schedules.alltoall(xs, algo, "i32")
+        for algo in sim.ALGOS["alltoall"]:
+            res = sim.alltoall(xs, algo, "i32")
             for j in range(N):
                 assert np.array_equal(res.outputs[j], want[j]), (algo, N, B)
-            twice = schedules.alltoall(res.outputs, algo, "i32")
+            twice = sim.alltoall(res.outputs, algo, "i32")
             for j in range(N):
                 assert np.array_equal(twice.outputs[j], xs[j])
 
@@ -331,15 +334,15 @@ def test_alltoall_against_block_transpose(N):
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("N", [2, 4, 8, 16])
-def test_allreduce_within_recursive_summation_bound(N):
+def test_allreduce_within_recursive_summation_bound(N, sim):
     count = 997
     xs = rank_buffers("uniform_f32", 15, N, count)
     exact = np.sum(np.stack([x.astype(np.float64) for x in xs]), axis=0)
     absum = np.sum(np.stack([np.abs(x.astype(np.float64)) for x in xs]), axis=0)
     u = 2.0 ** -24
     gamma = (N - 1) * u / (1 - (N - 1) * u)
-    for algo in schedules.ALGOS["allreduce"]:
-        res = schedules.allreduce(xs, algo, "f32")
+    for algo in sim.ALGOS["allreduce"]:
+        res = sim.allreduce(xs, algo, "f32")
         for o in res.outputs[1:]:
             assert numerics.same_bits(o, res.outputs[0])
         err = np.abs(res.outputs[0].astype(np.float64) - exact)
@@ -350,17 +353,17 @@ def _witness_inputs(vals, count=16):
     return [np.full(count, v, dtype=np.float32) for v in vals]
 
 
-def test_order_witnesses_n4(golden):
+def test_order_witnesses_n4(golden, sim):
     for row in golden("order_witness_n4.txt"):
         vals = [float(v) for v in row[1:5]]
         algo = row[5]
         want = np.repeat(np.array([float(v) for v in row[6:10]], dtype=np.float32), 4)
         xs = _witness_inputs(vals)
         if algo.startswith("rs_"):
-            res = schedules.reduce_scatter(xs, algo[3:], "f32")
+            res = sim.reduce_scatter(xs, algo[3:], "f32")
             got = np.concatenate(res.outputs)
         else:
-            res = schedules.allreduce(xs, algo, "f32")
+            res = sim.allreduce(xs, algo, "f32")
             got = res.outputs[0]
             for o in res.outputs:
                 assert numerics.same_bits(o, got)
@@ -369,27 +372,29 @@ def test_order_witnesses_n4(golden):
 
 @pytest.mark.parametrize("N", [2, 3, 4, 5, 7, 8, 16])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_closed_form_trees_match_simulation(N, dtype):
+def test_closed_form_trees_match_simulation(N, dtype, sim):
     esz = numerics.ESIZE[dtype]
     for count in (N * 8 * 3 + 5, 203):
         kind = "uniform_f32" if dtype == "f32" else "uniform_bf16"
         xs = rank_buffers(kind, 16 + N, N, count)
         idx = np.arange(count)
-        for algo in schedules.ALGOS["allreduce"]:
-            res = schedules.allreduce(xs, algo, dtype)
-            want = orders.allreduce_at(xs, algo, count, dtype, idx)
-            assert numerics.same_bits(res.outputs[0], want), (algo, N, count)
+        for algo in sim.ALGOS["allreduce"]:
+            res = sim.allreduce(xs, algo, dtype)
+            for closed in (orders, cxx):  # both closed-form statements of the trees
+                want = closed.allreduce_at(xs, algo, count, dtype, idx)
+                assert numerics.same_bits(res.outputs[0], want), (algo, N, count, closed.__name__)
         rc = 13
         xr = rank_buffers(kind, 30 + N, N, N * rc)
-        for algo in schedules.ALGOS["reduce_scatter"]:
-            res = schedules.reduce_scatter(xr, algo, dtype)
-            want = orders.reduce_scatter_at(xr, algo, rc, dtype, np.arange(N * rc))
-            assert numerics.same_bits(np.concatenate(res.outputs), want), (algo, N)
+        for algo in sim.ALGOS["reduce_scatter"]:
+            res = sim.reduce_scatter(xr, algo, dtype)
+            for closed in (orders, cxx):
+                want = closed.reduce_scatter_at(xr, algo, rc, dtype, np.arange(N * rc))
+                assert numerics.same_bits(np.concatenate(res.outputs), want), (algo, N, closed.__name__)
     assert chunk_elems(0, N, esz) == 0
 
 
 @pytest.mark.parametrize("N", [3, 5, 8])
-def test_witnesses_distinguish_orders(N):
+def test_witnesses_distinguish_orders(N, sim):
     """Each schedule's tree differs from the rank-order fold on some witness,
     so bit-exact agreement with the oracle pins the association, not just the sum."""
     count = N * 4 * 2
@@ -405,8 +410,8 @@ def test_witnesses_distinguish_orders(N):
                     vals = [0.0] * N
                     vals[a], vals[b], vals[c] = 2.0 ** 24, -(2.0 ** 24), 1.0
                     xs = _witness_inputs(vals, count)
-                    r1 = schedules.allreduce(xs, algo, "f32").outputs[0]
-                    r0 = schedules.allreduce(xs, "fused", "f32").outputs[0]
+                    r1 = sim.allreduce(xs, algo, "f32").outputs[0]
+                    r0 = sim.allreduce(xs, "fused", "f32").outputs[0]
                     if not np.array_equal(r1, r0):
                         distinct = True
                         break
@@ -451,16 +456,62 @@ def test_bf16_rounding_matches_library():
     # exact ties: the dropped half is 0x8000
     u = rng.integers(0, 2 ** 31, 10000, dtype=np.uint64).astype(np.uint32) & np.uint32(0x7F7F0000)
     x = np.concatenate([x, (u | np.uint32(0x8000)).view(np.float32)])
-    ours = numerics.f32_to_bf16(x)
     lib = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    assert np.array_equal(ours, lib)
-    back = numerics.bf16_to_f32(ours)
-    assert np.array_equal(back, torch.from_numpy(ours.view(np.int16)).view(torch.bfloat16).float().numpy())
+    for impl in (numerics, cxx):
+        ours = impl.f32_to_bf16(x)
+        assert np.array_equal(ours, lib), impl.__name__
+        back = impl.bf16_to_f32(ours)
+        assert np.array_equal(back, torch.from_numpy(ours.view(np.int16)).view(torch.bfloat16).float().numpy())
+        nan = np.array([np.nan, -np.nan], dtype=np.float32)
+        assert np.all(np.isnan(impl.bf16_to_f32(impl.f32_to_bf16(nan))))
+    # every bf16 pattern widens exactly (NaNs stay NaN)
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    wide = torch.from_numpy(allb.view(np.int16)).view(torch.bfloat16).float().numpy()
+    got = cxx.bf16_to_f32(allb)
+    fin = ~np.isnan(wide)
+    assert np.array_equal(got[fin].view(np.uint32), wide[fin].view(np.uint32))
+    assert np.all(np.isnan(got[~fin]))
+
+
+def test_f16_conversions_of_the_cxx_oracle_match_library():
+    """The C++ oracle writes its binary16 conversions from the format; they
+    must equal numpy's (a library routine): every binary16 pattern widens
+    exactly, and narrowing rounds to nearest even, including ties, the
+    subnormal range, the underflow tie at 2^-25 and overflow at 65520."""
+    allh = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    lib_wide = allh.view(np.float16).astype(np.float32)
+    got = cxx.f16_bits_to_f32(allh)
+    fin = ~np.isnan(lib_wide)
+    assert np.array_equal(got[fin].view(np.uint32), lib_wide[fin].view(np.uint32))
+    assert np.all(np.isnan(got[~fin]))
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.standard_normal(200000).astype(np.float32) * np.float32(100.0),
+        (rng.uniform(-1, 1, 50000) * 7e-5).astype(np.float32),       # around the subnormal halves
+        (rng.uniform(-1, 1, 50000) * 7e4).astype(np.float32),        # around overflow
+        (rng.uniform(-1, 1, 20000) * 1e-7).astype(np.float32),       # below the smallest subnormal
+        np.array([0.0, -0.0, np.inf, -np.inf, 65504.0, 65519.996, 65520.0, -65520.0, 2.0 ** -24, 2.0 ** -25,
+                  -(2.0 ** -25), 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -25, 2.0 ** -14, 2.0 ** -14 - 2.0 ** -25],
+                 dtype=np.float32),
+    ])
+    # exact ties of the normal range: the 13 dropped bits are 0x1000
+    u = rng.integers(0x38800000, 0x477FE000, 20000, dtype=np.uint64).astype(np.uint32) & np.uint32(0xFFFFE000)
+    x = np.concatenate([x, (u | np.uint32(0x1000)).view(np.float32)])
+    # every representable half plus and minus a hair, and the midpoints between neighbours
+    fin_h = lib_wide[fin & np.isfinite(lib_wide)]
+    mids = ((fin_h[:-1].astype(np.float64) + fin_h[1:].astype(np.float64)) / 2).astype(np.float32)
+    x = np.concatenate([x, fin_h, np.nextafter(fin_h, np.float32(np.inf)), mids])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    got = cxx.f32_to_f16_bits(x)
+    assert np.array_equal(got, want), np.nonzero(got != want)[0][:5]
+    # NaN: quiet NaN, sign kept
     nan = np.array([np.nan, -np.nan], dtype=np.float32)
-    assert np.all(np.isnan(numerics.bf16_to_f32(numerics.f32_to_bf16(nan))))
+    h = cxx.f32_to_f16_bits(nan)
+    assert np.all((h & 0x7E00) == 0x7E00) and (h[1] & 0x8000) and not (h[0] & 0x8000)
 
 
-def test_bf16_allreduce_one_rounding():
+def test_bf16_allreduce_one_rounding(sim):
     """bf16: fp32 accumulation in the schedule's order, one rounding at the end:
     within 1 bf16 ulp of the rounded direct-order fp32 sum, bit-exact to it for
     the fused order."""
@@ -473,8 +524,8 @@ def test_bf16_allreduce_one_rounding():
     ref = numerics.f32_to_bf16(direct)
     exact = np.sum(np.stack([w.astype(np.float64) for w in wide]), axis=0)
     absum = np.sum(np.stack([np.abs(w.astype(np.float64)) for w in wide]), axis=0)
-    for algo in schedules.ALGOS["allreduce"]:
-        out = schedules.allreduce(xs, algo, "bf16").outputs[0]
+    for algo in sim.ALGOS["allreduce"]:
+        out = sim.allreduce(xs, algo, "bf16").outputs[0]
         if algo == "fused":
             assert np.array_equal(out, ref)
         if algo == "ring_hop":
@@ -493,18 +544,22 @@ def test_bf16_allreduce_one_rounding():
 @pytest.mark.parametrize("algo", ["ring", "rhd", "dbt"])
 def test_planted_schedule_fault_is_caught(monkeypatch, algo):
     """Losing any step's messages, or delivering a reduce step twice, breaks
-    the brute-force pin."""
+    the brute-force pin (both oracles)."""
     N, count = 4, 64
     xs = [small_ints_f32(18, r, count) for r in range(N)]
     want = _exact_sum(xs).astype(np.float32)
     clean = schedules.allreduce(xs, algo, "f32")
     for t in clean.log.steps():
-        kinds = [{"drop_step": t}]
+        kinds = [("drop_step", t)]
         if any(r.reduce for r in clean.log.records if r.step == t):
-            kinds.append({"dup_step": t})
-        for fault in kinds:
-            monkeypatch.setattr(schedules, "_FAULT", fault)
+            kinds.append(("dup_step", t))
+        for kind, step in kinds:
+            monkeypatch.setattr(schedules, "_FAULT", {kind: step})
             res = schedules.allreduce(xs, algo, "f32")
-            assert not all(np.array_equal(o, want) for o in res.outputs), (algo, fault)
-    monkeypatch.setattr(schedules, "_FAULT", None)
-    assert all(np.array_equal(o, want) for o in schedules.allreduce(xs, algo, "f32").outputs)
+            assert not all(np.array_equal(o, want) for o in res.outputs), (algo, kind, step)
+            monkeypatch.setattr(schedules, "_FAULT", None)
+            with cxx.fault(kind, step):
+                res = cxx.allreduce(xs, algo, "f32")
+            assert not all(np.array_equal(o, want) for o in res.outputs), ("cxx", algo, kind, step)
+    for impl in (schedules, cxx):
+        assert all(np.array_equal(o, want) for o in impl.allreduce(xs, algo, "f32").outputs)
