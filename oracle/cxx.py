@@ -131,7 +131,9 @@ def _as_storage(x, dtype):
 
 
 def _run(coll, algo, arrays, n_in, N, dtype, op="sum", root=0, inplace=False, nchunks=0, want_log=True,
-         want_outputs=True):
+         want_outputs=True, keep=None):
+    """Run one collective.  ``keep`` lists the outputs to copy back (None: all;
+    the others are returned as None), for full-size checks that need one."""
     L = lib()
     arrays = [_as_storage(a, dtype) for a in arrays]
     for a in arrays:
@@ -149,6 +151,9 @@ def _run(coll, algo, arrays, n_in, N, dtype, op="sum", root=0, inplace=False, nc
         if want_outputs:
             es = np.dtype(STORAGE[dtype]).itemsize
             for i in range(L.vo_noutputs(res)):
+                if keep is not None and i not in keep:
+                    outs.append(None)
+                    continue
                 nbytes = L.vo_output_elems(res, i)
                 o = np.empty(nbytes // es, dtype=STORAGE[dtype])
                 L.vo_output_copy(res, i, o.ctypes.data)

@@ -31,7 +31,9 @@ ReduceScatter, element e of the N*rc input (block c = e // rc):
 
 Parity status: the fused, ring and rhd trees follow from the pages' step
 descriptions; the dbt tree rests on the reading of how the two trees are
-built (see ``oracle.schedules.dbt_trees``).
+built.  Every tree is stated here on its own, with no helper shared with the
+simulation in ``oracle.schedules``; hand-derived order witnesses pin them at
+N = 4 and 8 (and the RHD fold-in at N = 5, 6, 7).
 """
 from __future__ import annotations
 
@@ -39,7 +41,6 @@ import numpy as np
 
 from .numerics import ESIZE, combine, narrow, widen
 from .partition import chunk_of, chunk_range
-from .schedules import dbt_trees, rhd_virtual_ranks
 
 
 def left_fold(ranks):
@@ -54,6 +55,20 @@ def balanced_pairs(ranks):
         return ranks[0]  # a rank, or an already built subtree
     mid = len(ranks) // 2
     return (balanced_pairs(ranks[:mid]), balanced_pairs(ranks[mid:]))
+
+
+def halving_leaves(N: int):
+    """The participants of the recursive halving, in order: with P the largest
+    power of 2 not above N and r = N - P, ranks 2i+1 fold into 2i (i < r)
+    first, so the first r leaves are the pairs (2i, 2i+1) and the rest are the
+    ranks 2r .. N-1 ([Latency-formula page] section "Recursive
+    Halving-Doubling" for N = 2^k; the fold-in is the reading taken for other
+    N).  Stated here from that description, apart from the simulation."""
+    P = 1
+    while 2 * P <= N:
+        P *= 2
+    extra = N - P
+    return [(2 * i, 2 * i + 1) for i in range(extra)] + list(range(2 * extra, N))
 
 
 def heap_tree(i: int, N: int, rank_of):
@@ -73,14 +88,14 @@ def allreduce_tree(algo: str, N: int, count: int, dtype: str, e: int):
         c = chunk_of(e, count, N, esz)
         return left_fold([(c + j) % N for j in range(N)])
     if algo == "rhd":
-        P, r, real = rhd_virtual_ranks(N)
-        leaves = [(2 * v, 2 * v + 1) if v < r else real[v] for v in range(P)]
-        return balanced_pairs(leaves)
+        return balanced_pairs(halving_leaves(N))
     if algo == "dbt":
-        for _, rank_of, (lo, hi) in dbt_trees(N, count, esz):
-            if lo <= e < hi:
-                return heap_tree(0, N, rank_of)
-        raise IndexError(e)
+        # the first part of a two-way split on tree A (heap on the ranks), the
+        # rest on tree B (heap node i on rank N-1-i)
+        lo, hi = chunk_range(0, count, 2, esz)
+        if not 0 <= e < count:
+            raise IndexError(e)
+        return heap_tree(0, N, (lambda i: i) if e < hi else (lambda i: N - 1 - i))
     raise ValueError(algo)
 
 

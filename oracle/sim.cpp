@@ -327,12 +327,20 @@ struct Sim {
     }
   }
 
+  // payload snapshots, kept from step to step so that their memory is reused
+  std::vector<std::vector<uint8_t>> pb;
+  std::vector<std::vector<Lane>> pl;
+
   // All payloads are read from their senders first, then delivered in order.
   void run_step(int step, std::vector<Msg>& msgs) {
     if (g_fault_kind == 1 && g_fault_step == step) return;
-    std::vector<std::vector<uint8_t>> pb(msgs.size());
-    std::vector<std::vector<Lane>> pl(msgs.size());
+    if (pb.size() < msgs.size()) {
+      pb.resize(msgs.size());
+      pl.resize(msgs.size());
+    }
     for (size_t i = 0; i < msgs.size(); ++i) {
+      pb[i].clear();
+      pl[i].clear();
       for (const Piece& p : msgs[i].pieces) {
         if (p.src->lanes)
           pl[i].insert(pl[i].end(), p.src->l.begin() + p.soff, p.src->l.begin() + p.soff + p.n);

@@ -1,15 +1,16 @@
 """The benchmark's five workloads at their full sizes, on the GPU.
 
 1. Ring AllReduce, N=4, fp32, 4096 elements, uniform[-1,1] seed 0: bit-exact
-   against the oracle's replay of the same schedule (and every other algorithm).
-2. AllReduce sweep, N=8, fp32, 1 KiB .. 256 MiB per rank: full bit-exact
-   comparison at small and medium sizes; at 256 MiB (the size the benchmark
-   times, in the same launch configuration) every rank's output is identical,
-   sampled elements (chunk and tree boundaries plus random ones) match the
-   oracle's association tree bit for bit, and every element is within the
-   recursive-summation bound of the exact sum.
-3. bf16 gradient bucket, N=8, 64M elements N(0, 1e-3): AllReduce sampled
-   bit-exact; ReduceScatter sampled bit-exact; AllGather exact.
+   against the C++ oracle's replay of the same schedule (and every other
+   algorithm).
+2. AllReduce sweep, N=8, fp32, 1 KiB .. 256 MiB per rank: every element of
+   every size compared bit for bit with the oracle; at 256 MiB (the size the
+   benchmark times, in the same launch configuration) every rank's output is
+   identical on the device, all 64M elements match the oracle's simulation,
+   and every element is within the recursive-summation bound of the exact sum.
+3. bf16 gradient bucket, N=8, 64M elements N(0, 1e-3): AllReduce (every
+   algorithm) and ReduceScatter compared with the oracle element by element;
+   AllGather exact.
 4. MoE AllToAll, N=8, 8192x4096 bf16 per rank in 8 blocks: exact, every algorithm.
 5. Broadcast and Scatter, N=8 and 16, int32, 1 GiB total: exact.
 """
@@ -18,8 +19,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import orders, schedules
-from oracle.partition import chunk_range
+from oracle import cxx
 from synthetic_inputs import int32_bits, normal_bf16, rank_buffers, uniform_pm1_f32
 
 from .gpu_util import first_diff, same_bits, to_dev, to_host
@@ -39,24 +39,11 @@ def _lib():
     torch.cuda.empty_cache()
 
 
-def _sample_indices(count, N, esize, seed=0, nrand=1 << 15):
-    idx = {0, count - 1}
-    for parts in (N, 2):
-        for c in range(parts + 1):
-            lo = chunk_range(min(c, parts - 1), count, parts, esize)[0] if c < parts else count
-            for d in (-2, -1, 0, 1):
-                if 0 <= lo + d < count:
-                    idx.add(lo + d)
-    rng = np.random.default_rng(seed)
-    idx.update(rng.integers(0, count, nrand).tolist())
-    return np.array(sorted(idx), dtype=np.int64)
-
-
 def test_config1_ring_n4_bitexact():
     N, count = 4, 4096
     xs = [uniform_pm1_f32(0, r, count) for r in range(N)]
-    for algo in schedules.ALGOS["allreduce"]:
-        want = schedules.allreduce(xs, algo, "f32").outputs
+    for algo in cxx.ALGOS["allreduce"]:
+        want = cxx.allreduce(xs, algo, "f32").outputs
         sends = [to_dev(x) for x in xs]
         recvs = [torch.empty_like(s) for s in sends]
         vc.vc_allreduce(sends, recvs, algo=algo)
@@ -66,28 +53,25 @@ def test_config1_ring_n4_bitexact():
             assert same_bits(got, want[r]), (algo, r, first_diff(got, want[r]))
 
 
-@pytest.mark.parametrize("log2_bytes", [10, 16, 22])
+@pytest.mark.parametrize("log2_bytes", [10, 16, 22, 25])
 def test_config2_sweep_full_bitexact(log2_bytes):
     N, count = 8, (1 << log2_bytes) // 4
     xs = rank_buffers("uniform_f32", 20 + log2_bytes, N, count)
     sends = [to_dev(x) for x in xs]
     recvs = [torch.empty_like(s) for s in sends]
-    for algo in schedules.ALGOS["allreduce"]:
-        want = schedules.allreduce(xs, algo, "f32").outputs
+    for algo in cxx.ALGOS["allreduce"]:
+        want = cxx.allreduce(xs, algo, "f32", want_log=False).outputs
         vc.vc_allreduce(sends, recvs, algo=algo)
         torch.cuda.synchronize()
         for r in range(N):
             assert same_bits(to_host(recvs[r]), want[r]), (algo, log2_bytes, r)
 
 
-def test_config2_256mib_sampled_and_bounded():
+def test_config2_256mib_every_element():
     N, count = 8, (256 << 20) // 4
     xs = rank_buffers("uniform_f32", 28, N, count)
     sends = [to_dev(x) for x in xs]
     recvs = [torch.empty_like(s) for s in sends]
-    idx = _sample_indices(count, N, 4)
-    idx_dev = torch.from_numpy(idx).cuda()
-    vals = [x[idx] for x in xs]
     exact = np.zeros(count, np.float64)
     absum = np.zeros(count, np.float64)
     for x in xs:
@@ -95,50 +79,48 @@ def test_config2_256mib_sampled_and_bounded():
         absum += np.abs(x)
     u = 2.0 ** -24
     gamma = (N - 1) * u / (1 - (N - 1) * u)
-    for algo in schedules.ALGOS["allreduce"]:
+    for algo in cxx.ALGOS["allreduce"]:
         vc.vc_allreduce(sends, recvs, algo=algo)
         torch.cuda.synchronize()
         for r in range(1, N):
             assert torch.equal(recvs[r], recvs[0]), (algo, r)
-        want = orders.allreduce_at(vals, algo, count, "f32", idx)
-        got = recvs[0].index_select(0, idx_dev).cpu().numpy()
+        got = to_host(recvs[0])
+        want = cxx.allreduce(xs, algo, "f32", want_log=False, keep=(0,)).outputs[0]
         assert same_bits(got, want), (algo, first_diff(got, want))
-        full = recvs[0].cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(full - exact) <= gamma * absum), algo
+        assert np.all(np.abs(got.astype(np.float64) - exact) <= gamma * absum), algo
+        del got, want
 
 
 def test_config3_bf16_bucket():
     N, count = 8, 64 << 20
     xs = [normal_bf16(3, r, count, sigma=1e-3) for r in range(N)]
     sends = [to_dev(x) for x in xs]
-    idx = _sample_indices(count, N, 2)
-    idx_dev = torch.from_numpy(idx).cuda()
-    vals = [x[idx] for x in xs]
     recvs = [torch.empty_like(s) for s in sends]
-    for algo in schedules.ALGOS["allreduce"]:
+    for algo in cxx.ALGOS["allreduce"]:
         vc.vc_allreduce(sends, recvs, algo=algo)
         torch.cuda.synchronize()
         for r in range(1, N):
             assert torch.equal(recvs[r], recvs[0]), (algo, r)
-        want = orders.allreduce_at(vals, algo, count, "bf16", idx)
-        got = to_host(recvs[0].index_select(0, idx_dev))
+        got = to_host(recvs[0])
+        want = cxx.allreduce(xs, algo, "bf16", want_log=False, keep=(0,)).outputs[0]
         assert same_bits(got, want), (algo, first_diff(got, want))
+        del got, want
     del recvs
-    # ReduceScatter alone: in 64M -> out 8M per rank
+    # ReduceScatter alone: in 64M -> out 8M per rank, every output element
     rc = count // N
     outs = [torch.empty(rc, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
-    for algo in schedules.ALGOS["reduce_scatter"]:
+    for algo in cxx.ALGOS["reduce_scatter"]:
         vc.vc_reduce_scatter(sends, outs, algo=algo)
         torch.cuda.synchronize()
-        want = orders.reduce_scatter_at(vals, algo, rc, "bf16", idx)
-        flat = torch.cat(outs)
-        got_all = to_host(flat.index_select(0, idx_dev))
-        assert same_bits(got_all, want), (algo, first_diff(got_all, want))
+        want = cxx.reduce_scatter(xs, algo, "bf16", want_log=False).outputs
+        for r in range(N):
+            got = to_host(outs[r])
+            assert same_bits(got, want[r]), (algo, r, first_diff(got, want[r]))
     del outs
     # AllGather alone: in 8M -> out 64M per rank
     ins = [s[:rc] for s in sends]
     outs = [torch.empty(count, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
-    for algo in schedules.ALGOS["allgather"]:
+    for algo in cxx.ALGOS["allgather"]:
         vc.vc_allgather(ins, outs, algo=algo)
         torch.cuda.synchronize()
         for r in range(N):
@@ -152,7 +134,7 @@ def test_config4_moe_alltoall():
     xs = rank_buffers("normal_bf16", 4, N, N * B)
     sends = [to_dev(x) for x in xs]
     recvs = [torch.empty_like(s) for s in sends]
-    for algo in schedules.ALGOS["alltoall"]:
+    for algo in cxx.ALGOS["alltoall"]:
         for r in recvs:
             r.zero_()
         vc.vc_alltoall(sends, recvs, algo=algo)
@@ -173,7 +155,7 @@ def test_config5_broadcast_scatter_1gib(N):
     A = int32_bits(5, 0, count)
     src = to_dev(A)
     recvs = [torch.empty(count, dtype=torch.int32, device="cuda") for _ in range(N)]
-    for algo in schedules.ALGOS["broadcast"]:
+    for algo in cxx.ALGOS["broadcast"]:
         for r in recvs:
             r.fill_(-1)
         vc.vc_broadcast(src, recvs, root=0, algo=algo)
@@ -184,7 +166,7 @@ def test_config5_broadcast_scatter_1gib(N):
     del recvs
     rc = count // N
     outs = [torch.empty(rc, dtype=torch.int32, device="cuda") for _ in range(N)]
-    for algo in schedules.ALGOS["scatter"]:
+    for algo in cxx.ALGOS["scatter"]:
         for o in outs:
             o.fill_(-1)
         vc.vc_scatter(src, outs, root=0, algo=algo)

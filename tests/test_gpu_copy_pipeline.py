@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import int32_bits, rank_buffers
 
 from .gpu_util import Guarded, same_bits
@@ -57,8 +57,8 @@ def test_copy_heavy_collectives_take_the_pipeline_and_match(N):
     for rc in (4096, 333 * 8, 1 << 18):  # aligned: whole 16-byte groups
         xs = rank_buffers("normal_bf16", 9100 + N + rc, N, N * rc)
         ins = [x[:rc] for x in xs]
-        for algo in schedules.ALGOS["allgather"]:
-            want = schedules.allgather(ins, algo, dtype).outputs
+        for algo in cxx.ALGOS["allgather"]:
+            want = cxx.allgather(ins, algo, dtype).outputs
             sends = [Guarded(rc, dtype, fill=x) for x in ins]
             recvs = [Guarded(N * rc, dtype) for _ in range(N)]
             recs = _traced(lambda: vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo))
@@ -66,8 +66,8 @@ def test_copy_heavy_collectives_take_the_pipeline_and_match(N):
             for r in range(N):
                 assert same_bits(recvs[r].host(), want[r]), ("ag", algo, N, rc, r)
             assert recs and all(r["kernel"].endswith("_tma") for r in recs), (algo, recs[:2])
-        for algo in schedules.ALGOS["alltoall"]:
-            want = schedules.alltoall(xs, algo, dtype).outputs
+        for algo in cxx.ALGOS["alltoall"]:
+            want = cxx.alltoall(xs, algo, dtype).outputs
             sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
             recvs = [Guarded(N * rc, dtype) for _ in range(N)]
             recs = _traced(lambda: vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo=algo))
@@ -77,11 +77,11 @@ def test_copy_heavy_collectives_take_the_pipeline_and_match(N):
             assert recs and all(r["kernel"].endswith("_tma") for r in recs), (algo, recs[:2])
     for count in (8192, 1 << 20):
         A = int32_bits(9200, N, count)
-        for algo in schedules.ALGOS["broadcast"] + ("pipe_chain", "pipe_tree"):
+        for algo in cxx.ALGOS["broadcast"] + ("pipe_chain", "pipe_tree"):
             if algo.startswith("pipe"):
-                want = schedules.broadcast_pipelined(A, N, 0, algo, "i32", 4).outputs
+                want = cxx.broadcast_pipelined(A, N, 0, algo, "i32", 4).outputs
             else:
-                want = schedules.broadcast(A, N, 0, algo, "i32").outputs
+                want = cxx.broadcast(A, N, 0, algo, "i32").outputs
             src = Guarded(count, "i32", fill=A)
             recvs = [Guarded(count, "i32") for _ in range(N)]
             if algo.startswith("pipe"):
@@ -98,7 +98,7 @@ def test_copy_heavy_collectives_take_the_pipeline_and_match(N):
 def test_unaligned_copies_take_the_register_kernel():
     N, rc = 4, 1001  # 1001 bf16 per block: blocks are not whole 16-byte groups
     xs = rank_buffers("normal_bf16", 9300, N, N * rc)
-    want = schedules.alltoall(xs, "pairwise", "bf16").outputs
+    want = cxx.alltoall(xs, "pairwise", "bf16").outputs
     sends = [Guarded(N * rc, "bf16", fill=x) for x in xs]
     recvs = [Guarded(N * rc, "bf16") for _ in range(N)]
     recs = _traced(lambda: vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo="pairwise"))
@@ -110,7 +110,7 @@ def test_unaligned_copies_take_the_register_kernel():
 def test_the_minimum_size_and_the_off_switch_keep_small_copies_on_the_register_kernel():
     N, rc = 4, 1 << 16  # aligned: the pipeline would take it at minimum 0
     xs = rank_buffers("normal_bf16", 9400, N, N * rc)
-    want = schedules.alltoall(xs, "pairwise", "bf16").outputs
+    want = cxx.alltoall(xs, "pairwise", "bf16").outputs
     try:
         for setting in (vc.COPY_PIPELINE_NEVER, 128 << 20, 0):
             vc.vc_set_copy_pipeline(setting)
@@ -131,7 +131,7 @@ def test_calls_with_16_bit_reductions_keep_their_copies_on_the_register_kernel()
         xs = rank_buffers({"bf16": "normal_bf16", "f16": "uniform_f32", "f32": "uniform_f32"}[dtype], 9500, N, count)
         if dtype == "f16":
             xs = [x.astype(np.float16) for x in xs]
-        want = schedules.allreduce(xs, "ring", dtype).outputs
+        want = cxx.allreduce(xs, "ring", dtype).outputs
         sends = [Guarded(count, dtype, fill=x) for x in xs]
         recvs = [Guarded(count, dtype) for _ in range(N)]
         recs = _traced(lambda: vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo="ring"))

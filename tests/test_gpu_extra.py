@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import int32_bits, rank_buffers
 
 from .gpu_util import Guarded, first_diff, same_bits, to_dev
@@ -31,7 +31,7 @@ def test_pipelined_broadcast_matches_oracle(N):
             for algo in ("pipe_chain", "pipe_tree"):
                 for k in (1, 4, 13):
                     for inplace in (False, True):
-                        want = schedules.broadcast_pipelined(A, N, root, algo, "i32", k, inplace=inplace).outputs
+                        want = cxx.broadcast_pipelined(A, N, root, algo, "i32", k, inplace=inplace).outputs
                         recvs = [Guarded(count, "i32") for _ in range(N)]
                         if inplace:
                             recvs[root].t.copy_(to_dev(A))
@@ -61,17 +61,17 @@ def test_gather_reduce_match_oracle(N, dtype):
     for root in sorted({0, N - 1, N // 2}):
         for rc in (1, 5, 4096, 70001):
             xs = rank_buffers(kind, 20 + root + rc, N, rc)
-            for algo in schedules.ALGOS_EXTRA["gather"]:
-                want = schedules.gather(xs, root, algo, dtype).outputs[0]
+            for algo in cxx.ALGOS_EXTRA["gather"]:
+                want = cxx.gather(xs, root, algo, dtype).outputs[0]
                 sends = [Guarded(rc, dtype, fill=x) for x in xs]
                 out = Guarded(N * rc, dtype)
                 vc.vc_gather([g.t for g in sends], out.t, root=root, algo=algo)
                 torch.cuda.synchronize()
                 assert out.guards_intact() and all(g.guards_intact() for g in sends)
                 assert same_bits(out.host(), want), ("gather", algo, N, root, rc)
-            for algo in schedules.ALGOS_EXTRA["reduce"]:
+            for algo in cxx.ALGOS_EXTRA["reduce"]:
                 for inplace in (False, True):
-                    want = schedules.reduce(xs, root, algo, dtype, inplace=inplace).outputs[0]
+                    want = cxx.reduce(xs, root, algo, dtype, inplace=inplace).outputs[0]
                     sends = [Guarded(rc, dtype, fill=x) for x in xs]
                     out = sends[root] if inplace else Guarded(rc, dtype)
                     vc.vc_reduce([g.t for g in sends], out.t, root=root, algo=algo)

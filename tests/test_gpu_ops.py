@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import rank_buffers
 
 from .gpu_util import Guarded, first_diff, same_bits, to_dev, to_host
@@ -37,8 +37,8 @@ def _inputs(dtype, seed, N, n):
 def test_reductions_with_ops_match_oracle(N, dtype, op):
     for count in (13, 4099 * 2, 300007):
         xs = _inputs(dtype, 50 + N + count, N, count)
-        for algo in schedules.ALGOS["allreduce"]:
-            want = schedules.allreduce(xs, algo, dtype, op=op).outputs
+        for algo in cxx.ALGOS["allreduce"]:
+            want = cxx.allreduce(xs, algo, dtype, op=op).outputs
             sends = [Guarded(count, dtype, fill=x) for x in xs]
             recvs = [Guarded(count, dtype) for _ in range(N)]
             vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo, op=op)
@@ -49,16 +49,16 @@ def test_reductions_with_ops_match_oracle(N, dtype, op):
                 assert same_bits(got, want[r]), ("ar", algo, op, dtype, N, count, r, first_diff(got, want[r]))
         rc = count // N + 1
         xr = _inputs(dtype, 60 + N + count, N, N * rc)
-        for algo in schedules.ALGOS["reduce_scatter"]:
-            want = schedules.reduce_scatter(xr, algo, dtype, op=op).outputs
+        for algo in cxx.ALGOS["reduce_scatter"]:
+            want = cxx.reduce_scatter(xr, algo, dtype, op=op).outputs
             sends = [to_dev(x) for x in xr]
             recvs = [torch.empty(rc, dtype=sends[0].dtype, device="cuda") for _ in range(N)]
             vc.vc_reduce_scatter(sends, recvs, algo=algo, op=op)
             torch.cuda.synchronize()
             for r in range(N):
                 assert same_bits(to_host(recvs[r]), want[r]), ("rs", algo, op, dtype, N, r)
-        for algo in schedules.ALGOS_EXTRA["reduce"]:
-            want = schedules.reduce(xs, N - 1, algo, dtype, op=op).outputs[0]
+        for algo in cxx.ALGOS_EXTRA["reduce"]:
+            want = cxx.reduce(xs, N - 1, algo, dtype, op=op).outputs[0]
             sends = [to_dev(x) for x in xs]
             out = torch.empty_like(sends[0])
             vc.vc_reduce(sends, out, root=N - 1, algo=algo, op=op)
@@ -83,20 +83,20 @@ def test_max_min_nan_and_signed_zero_on_gpu():
 def test_fp16_data_movement(N):
     rc = 4099
     xs = _inputs("f16", 70 + N, N, N * rc)
-    for algo in schedules.ALGOS["alltoall"]:
-        want = schedules.alltoall(xs, algo, "f16").outputs
+    for algo in cxx.ALGOS["alltoall"]:
+        want = cxx.alltoall(xs, algo, "f16").outputs
         sends = [to_dev(x) for x in xs]
         recvs = [torch.empty_like(s) for s in sends]
         vc.vc_alltoall(sends, recvs, algo=algo)
         torch.cuda.synchronize()
         for j in range(N):
             assert same_bits(to_host(recvs[j]), want[j]), (algo, j)
-    for algo in schedules.ALGOS["allgather"]:
+    for algo in cxx.ALGOS["allgather"]:
         ins = [to_dev(x[:rc]) for x in xs]
         outs = [torch.empty(N * rc, dtype=torch.float16, device="cuda") for _ in range(N)]
         vc.vc_allgather(ins, outs, algo=algo)
         torch.cuda.synchronize()
-        want = schedules.allgather([x[:rc] for x in xs], algo, "f16").outputs
+        want = cxx.allgather([x[:rc] for x in xs], algo, "f16").outputs
         for r in range(N):
             assert same_bits(to_host(outs[r]), want[r])
 
@@ -116,7 +116,7 @@ def test_fp32_partials_at_offsets_that_are_16_but_not_32_byte_aligned(dtype, sin
             f32 = [e for e in entries if e.dtype == 0]
             assert any(e.byte_off % 32 == 16 for e in f32), (N, rc)
             xr = _inputs(dtype, 70 + N + rc, N, N * rc)
-            want = schedules.reduce_scatter(xr, "ring", dtype).outputs
+            want = cxx.reduce_scatter(xr, "ring", dtype).outputs
             sends = [Guarded(N * rc, dtype, fill=x) for x in xr]
             recvs = [Guarded(rc, dtype) for _ in range(N)]
             vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo="ring")

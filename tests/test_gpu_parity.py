@@ -14,9 +14,10 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import int32_bits, rank_buffers
 
+from . import witness
 from .conftest import read_golden
 from .gpu_util import Guarded, first_diff, same_bits, to_dev
 
@@ -59,7 +60,7 @@ def test_native_library_is_loaded():
     assert "libvcoll.so" in maps
 
 
-ALGOS_AR = schedules.ALGOS["allreduce"]
+ALGOS_AR = cxx.ALGOS["allreduce"]
 AR_N = [1, 2, 3, 4, 5, 8, 16]
 AR_COUNTS = [1, 13, 4096, 65536 + 37, 1 << 20]
 
@@ -70,7 +71,7 @@ def test_allreduce_matches_oracle(N, dtype):
     for count in AR_COUNTS:
         xs = _inputs(dtype, 1000 + N + count, N, count)
         for algo in ALGOS_AR:
-            want = schedules.allreduce(xs, algo, dtype).outputs
+            want = cxx.allreduce(xs, algo, dtype).outputs
             got = _run_allreduce(xs, algo, dtype)
             for r in range(N):
                 assert same_bits(got[r], want[r]), (algo, N, count, dtype, r, first_diff(got[r], want[r]))
@@ -82,7 +83,7 @@ def test_allreduce_inplace_and_misaligned(N, dtype):
     count = 4097 * 3
     xs = _inputs(dtype, 77 + N, N, count)
     for algo in ALGOS_AR:
-        want = schedules.allreduce(xs, algo, dtype).outputs
+        want = cxx.allreduce(xs, algo, dtype).outputs
         for shift, inplace in ((0, True), (1, False), (1, True), (3, False)):
             got = _run_allreduce(xs, algo, dtype, shift=shift, inplace=inplace)
             for r in range(N):
@@ -109,13 +110,30 @@ def test_order_witnesses_on_gpu():
         assert np.array_equal(got, want), (row[0], algo, got)
 
 
+def test_order_witnesses_n8_and_foldin_on_gpu():
+    """The hand-derived N = 8 Ring, RHD and Double Binary Tree witnesses and
+    the RHD fold-in witnesses at N = 5, 6, 7, on the device (every rank)."""
+    for wid, N, algo, xs, want in witness.rows(read_golden):
+        if algo.startswith("rs_"):
+            n = len(xs[0])
+            sends = [to_dev(x) for x in xs]
+            recvs = [torch.empty(n // N, device="cuda") for _ in range(N)]
+            vc.vc_reduce_scatter(sends, recvs, algo=algo[3:])
+            torch.cuda.synchronize()
+            outs = [torch.cat(recvs).cpu().numpy()]
+        else:
+            outs = _run_allreduce(xs, algo, "f32")
+        for r, got in enumerate(outs):
+            assert np.array_equal(got, want), (wid, N, algo, r, got)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16])
 def test_reduce_scatter_allgather_match_oracle(N, dtype):
     for rc in (1, 5, 4096, 40000 + 3):
         xs = _inputs(dtype, 2000 + N + rc, N, N * rc)
-        for algo in schedules.ALGOS["reduce_scatter"]:
-            want = schedules.reduce_scatter(xs, algo, dtype).outputs
+        for algo in cxx.ALGOS["reduce_scatter"]:
+            want = cxx.reduce_scatter(xs, algo, dtype).outputs
             sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
             recvs = [Guarded(rc, dtype) for _ in range(N)]
             vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo=algo)
@@ -125,8 +143,8 @@ def test_reduce_scatter_allgather_match_oracle(N, dtype):
                 got = recvs[r].host()
                 assert same_bits(got, want[r]), ("rs", algo, N, rc, r, first_diff(got, want[r]))
         ins = _inputs(dtype, 3000 + N + rc, N, rc)
-        for algo in schedules.ALGOS["allgather"]:
-            want = schedules.allgather(ins, algo, dtype).outputs
+        for algo in cxx.ALGOS["allgather"]:
+            want = cxx.allgather(ins, algo, dtype).outputs
             sends = [Guarded(rc, dtype, fill=x) for x in ins]
             recvs = [Guarded(N * rc, dtype) for _ in range(N)]
             vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo)
@@ -142,9 +160,9 @@ def test_broadcast_scatter_match_oracle(N):
     for root in sorted({0, 1 % N, N - 1}):
         for count in (1, 7, 4096 + 5, 300001):
             A = int32_bits(4000 + root, N, count)
-            for algo in schedules.ALGOS["broadcast"]:
+            for algo in cxx.ALGOS["broadcast"]:
                 for inplace in (False, True):
-                    want = schedules.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
+                    want = cxx.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
                     recvs = [Guarded(count, dtype) for _ in range(N)]
                     if inplace:
                         recvs[root].t.copy_(to_dev(A))
@@ -159,8 +177,8 @@ def test_broadcast_scatter_match_oracle(N):
                         assert same_bits(recvs[r].host(), want[r]), ("bcast", algo, N, root, count, inplace, r)
         for rc in (1, 3, 4096, 65537):
             A = int32_bits(5000 + root, N, N * rc)
-            for algo in schedules.ALGOS["scatter"]:
-                want = schedules.scatter(A, N, root, algo, dtype).outputs
+            for algo in cxx.ALGOS["scatter"]:
+                want = cxx.scatter(A, N, root, algo, dtype).outputs
                 src_g = Guarded(N * rc, dtype, fill=A)
                 recvs = [Guarded(rc, dtype) for _ in range(N)]
                 vc.vc_scatter(src_g.t, [g.t for g in recvs], root=root, algo=algo)
@@ -175,8 +193,8 @@ def test_broadcast_scatter_match_oracle(N):
 def test_alltoall_matches_oracle(N, dtype):
     for B in (1, 3, 1024, 20001):
         xs = _inputs(dtype, 6000 + N + B, N, N * B)
-        for algo in schedules.ALGOS["alltoall"]:
-            want = schedules.alltoall(xs, algo, dtype).outputs
+        for algo in cxx.ALGOS["alltoall"]:
+            want = cxx.alltoall(xs, algo, dtype).outputs
             for shift in (0, 1):
                 sends = [Guarded(N * B, dtype, shift, fill=x) for x in xs]
                 recvs = [Guarded(N * B, dtype, shift) for _ in range(N)]
@@ -192,7 +210,7 @@ def test_repeated_calls_reuse_scratch_and_agree():
     (and on a second stream) give identical results."""
     N, count = 8, (1 << 18) + 7
     xs = _inputs("bf16", 9, N, count)
-    want = schedules.allreduce(xs, "ring", "bf16").outputs
+    want = cxx.allreduce(xs, "ring", "bf16").outputs
     sends = [to_dev(x) for x in xs]
     outs = [[torch.empty_like(s) for s in sends] for _ in range(3)]
     s2 = torch.cuda.Stream()

@@ -17,7 +17,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import int32_bits, rank_buffers
 
 from .gpu_util import Guarded, first_diff, same_bits, to_dev
@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 REDUCTIONS = ("allreduce", "reduce_scatter", "reduce")
 COLLS = ("allreduce", "reduce_scatter", "allgather", "broadcast", "scatter", "alltoall", "gather", "reduce",
          "pipelined")
-ALGOS = dict(schedules.ALGOS, gather=schedules.ALGOS_EXTRA["gather"], reduce=schedules.ALGOS_EXTRA["reduce"],
+ALGOS = dict(cxx.ALGOS, gather=cxx.ALGOS_EXTRA["gather"], reduce=cxx.ALGOS_EXTRA["reduce"],
              pipelined=("pipe_chain", "pipe_tree"))
 
 
@@ -88,27 +88,27 @@ def _run(i, coll, algo, N, count, dtype, op, root, inplace, shift, nchunks):
         sends = [G(n_in, x) for x in xs]
         guards += sends
         if coll == "allreduce":
-            want = schedules.allreduce(xs, algo, dtype, inplace=inplace, op=op).outputs
+            want = cxx.allreduce(xs, algo, dtype, inplace=inplace, op=op).outputs
             recvs = sends if inplace else [G(count) for _ in range(N)]
             vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo, op=op)
         elif coll == "reduce_scatter":
-            want = schedules.reduce_scatter(xs, algo, dtype, op=op).outputs
+            want = cxx.reduce_scatter(xs, algo, dtype, op=op).outputs
             recvs = [G(count) for _ in range(N)]
             vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo=algo, op=op)
         elif coll == "allgather":
-            want = schedules.allgather(xs, algo, dtype).outputs
+            want = cxx.allgather(xs, algo, dtype).outputs
             recvs = [G(count * N) for _ in range(N)]
             vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo)
         elif coll == "alltoall":
-            want = schedules.alltoall(xs, algo, dtype).outputs
+            want = cxx.alltoall(xs, algo, dtype).outputs
             recvs = [G(count * N) for _ in range(N)]
             vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo=algo)
         elif coll == "gather":
-            want = [schedules.gather(xs, root, algo, dtype).outputs[0]]
+            want = [cxx.gather(xs, root, algo, dtype).outputs[0]]
             recvs = [G(count * N)]
             vc.vc_gather([g.t for g in sends], recvs[0].t, root=root, algo=algo)
         else:
-            want = [schedules.reduce(xs, root, algo, dtype, inplace=inplace, op=op).outputs[0]]
+            want = [cxx.reduce(xs, root, algo, dtype, inplace=inplace, op=op).outputs[0]]
             recvs = [sends[root]] if inplace else [G(count)]
             vc.vc_reduce([g.t for g in sends], recvs[0].t, root=root, algo=algo, op=op)
     else:
@@ -122,13 +122,13 @@ def _run(i, coll, algo, N, count, dtype, op, root, inplace, shift, nchunks):
             src = G(n_in, A)
             guards.append(src)
         if coll == "broadcast":
-            want = schedules.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
+            want = cxx.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
             vc.vc_broadcast(src.t, [g.t for g in recvs], root=root, algo=algo)
         elif coll == "scatter":
-            want = schedules.scatter(A, N, root, algo, dtype).outputs
+            want = cxx.scatter(A, N, root, algo, dtype).outputs
             vc.vc_scatter(src.t, [g.t for g in recvs], root=root, algo=algo)
         else:
-            want = schedules.broadcast_pipelined(A, N, root, algo, dtype, nchunks, inplace=inplace).outputs
+            want = cxx.broadcast_pipelined(A, N, root, algo, dtype, nchunks, inplace=inplace).outputs
             vc.vc_broadcast_pipelined(src.t, [g.t for g in recvs], root=root, algo=algo, nchunks=nchunks)
     torch.cuda.synchronize()
     assert all(g.guards_intact() for g in guards + recvs), "canary band overwritten"
@@ -151,7 +151,7 @@ def test_random_calls_match_oracle():
         what = (i, coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks)
         try:
             got, want = _run(i, coll, algo, N, count, dtype, op, root, inplace, shift, nchunks)
-        except schedules.Unsupported:
+        except cxx.Unsupported:
             # the oracle runs first: a shape it does not define is not sent to the
             # library, which must refuse it as well
             with pytest.raises(vc.VCError):

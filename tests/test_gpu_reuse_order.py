@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import int32_bits, rank_buffers
 
 from .gpu_util import Guarded, first_diff, same_bits
@@ -57,8 +57,8 @@ def test_reduction_schedules_with_the_reuse_order(N, dtype, form):
     assert vc.vc_get_reuse_order() == 0
     for count in (1000, 65536 + 40):
         xs = _inputs(dtype, 9600 + N + count, N, count)
-        for algo in schedules.ALGOS["allreduce"]:
-            want = schedules.allreduce(xs, algo, dtype).outputs
+        for algo in cxx.ALGOS["allreduce"]:
+            want = cxx.allreduce(xs, algo, dtype).outputs
             sends = [Guarded(count, dtype, fill=x) for x in xs]
             recvs = [Guarded(count, dtype) for _ in range(N)]
             vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo)
@@ -69,8 +69,8 @@ def test_reduction_schedules_with_the_reuse_order(N, dtype, form):
                 assert same_bits(got, want[r]), ("ar", algo, N, count, dtype, form, r, first_diff(got, want[r]))
         rc = count // N + 1
         xr = _inputs(dtype, 9700 + N + count, N, N * rc)
-        for algo in schedules.ALGOS["reduce_scatter"]:
-            want = schedules.reduce_scatter(xr, algo, dtype).outputs
+        for algo in cxx.ALGOS["reduce_scatter"]:
+            want = cxx.reduce_scatter(xr, algo, dtype).outputs
             sends = [Guarded(N * rc, dtype, fill=x) for x in xr]
             recvs = [Guarded(rc, dtype) for _ in range(N)]
             vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo=algo)
@@ -89,8 +89,8 @@ def test_data_movement_schedules_with_the_reuse_order(N, form):
     for rc in (1024, 20000):  # whole 16-byte groups (the pipeline) and many tiles
         xs = _inputs(dtype, 9800 + N + rc, N, N * rc)
         ins = [x[:rc] for x in xs]
-        for algo in schedules.ALGOS["allgather"]:
-            want = schedules.allgather(ins, algo, dtype).outputs
+        for algo in cxx.ALGOS["allgather"]:
+            want = cxx.allgather(ins, algo, dtype).outputs
             sends = [Guarded(rc, dtype, fill=x) for x in ins]
             recvs = [Guarded(N * rc, dtype) for _ in range(N)]
             vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo)
@@ -98,8 +98,8 @@ def test_data_movement_schedules_with_the_reuse_order(N, form):
             assert all(g.guards_intact() for g in sends + recvs)
             for r in range(N):
                 assert same_bits(recvs[r].host(), want[r]), ("ag", algo, N, rc, form, r)
-        for algo in schedules.ALGOS["alltoall"]:
-            want = schedules.alltoall(xs, algo, dtype).outputs
+        for algo in cxx.ALGOS["alltoall"]:
+            want = cxx.alltoall(xs, algo, dtype).outputs
             sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
             recvs = [Guarded(N * rc, dtype) for _ in range(N)]
             vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo=algo)
@@ -109,8 +109,8 @@ def test_data_movement_schedules_with_the_reuse_order(N, form):
                 assert same_bits(recvs[r].host(), want[r]), ("a2a", algo, N, rc, form, r)
     count = 30000
     A = int32_bits(9900 + N, N, count)
-    for algo in schedules.ALGOS["broadcast"]:
-        want = schedules.broadcast(A, N, 1, algo, "i32").outputs
+    for algo in cxx.ALGOS["broadcast"]:
+        want = cxx.broadcast(A, N, 1, algo, "i32").outputs
         src = Guarded(count, "i32", fill=A)
         recvs = [Guarded(count, "i32") for _ in range(N)]
         vc.vc_broadcast(src.t, [g.t for g in recvs], root=1, algo=algo)

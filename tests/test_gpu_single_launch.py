@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import int32_bits, rank_buffers
 
 from .gpu_util import Guarded, first_diff, same_bits, to_dev
@@ -76,8 +76,8 @@ def _nsteps(coll, algo, N, count, dtype="f32", root=0, nchunks=0, op="sum"):
 def test_allreduce_single_launch(N, dtype, op):
     for count in (1, 13, 4096 + 5, 65536 + 37):
         xs = _inputs(dtype, 7000 + N + count, N, count)
-        for algo in schedules.ALGOS["allreduce"]:
-            want = schedules.allreduce(xs, algo, dtype, op=op).outputs
+        for algo in cxx.ALGOS["allreduce"]:
+            want = cxx.allreduce(xs, algo, dtype, op=op).outputs
             nsteps = _nsteps("allreduce", algo, N, count, dtype, op=op)
             for limit in (ALWAYS, 0):
                 vc.vc_set_single_launch(limit)
@@ -97,8 +97,8 @@ def test_allreduce_in_place_single_launch(N, dtype):
     vc.vc_set_single_launch(ALWAYS)
     for count in (7, 4096 + 5, 30001):
         xs = _inputs(dtype, 7100 + N + count, N, count)
-        for algo in schedules.ALGOS["allreduce"]:
-            want = schedules.allreduce(xs, algo, dtype).outputs
+        for algo in cxx.ALGOS["allreduce"]:
+            want = cxx.allreduce(xs, algo, dtype).outputs
             bufs = [Guarded(count, dtype, fill=x) for x in xs]
             recs = _traced(lambda: vc.vc_allreduce([g.t for g in bufs], [g.t for g in bufs], algo=algo))
             assert all(g.guards_intact() for g in bufs)
@@ -114,8 +114,8 @@ def test_reduce_scatter_allgather_alltoall_single_launch(N, dtype):
         vc.vc_set_single_launch(limit)
         for rc in (1, 3, 1024 + 3, 20001):
             xs = _inputs(dtype, 7200 + N + rc, N, N * rc)
-            for algo in schedules.ALGOS["reduce_scatter"]:
-                want = schedules.reduce_scatter(xs, algo, dtype).outputs
+            for algo in cxx.ALGOS["reduce_scatter"]:
+                want = cxx.reduce_scatter(xs, algo, dtype).outputs
                 sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
                 recvs = [Guarded(rc, dtype) for _ in range(N)]
                 recs = _traced(lambda: vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo=algo))
@@ -124,8 +124,8 @@ def test_reduce_scatter_allgather_alltoall_single_launch(N, dtype):
                     assert same_bits(recvs[r].host(), want[r]), ("rs", algo, N, rc, limit, r)
                 _check_launches(recs, limit, _nsteps("reduce_scatter", algo, N, rc, dtype), ("rs", algo))
             ins = [x[:rc] for x in xs]
-            for algo in schedules.ALGOS["allgather"]:
-                want = schedules.allgather(ins, algo, dtype).outputs
+            for algo in cxx.ALGOS["allgather"]:
+                want = cxx.allgather(ins, algo, dtype).outputs
                 sends = [Guarded(rc, dtype, fill=x) for x in ins]
                 recvs = [Guarded(N * rc, dtype) for _ in range(N)]
                 recs = _traced(lambda: vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo=algo))
@@ -133,8 +133,8 @@ def test_reduce_scatter_allgather_alltoall_single_launch(N, dtype):
                 for r in range(N):
                     assert same_bits(recvs[r].host(), want[r]), ("ag", algo, N, rc, limit, r)
                 _check_launches(recs, limit, _nsteps("allgather", algo, N, rc, dtype), ("ag", algo))
-            for algo in schedules.ALGOS["alltoall"]:
-                want = schedules.alltoall(xs, algo, dtype).outputs
+            for algo in cxx.ALGOS["alltoall"]:
+                want = cxx.alltoall(xs, algo, dtype).outputs
                 sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
                 recvs = [Guarded(N * rc, dtype) for _ in range(N)]
                 recs = _traced(lambda: vc.vc_alltoall([g.t for g in sends], [g.t for g in recvs], algo=algo))
@@ -152,9 +152,9 @@ def test_rooted_collectives_single_launch(N):
         for root in sorted({0, N - 1}):
             for count in (1, 7, 4096 + 5, 30001):
                 A = int32_bits(7300 + root, N, count)
-                for algo in schedules.ALGOS["broadcast"]:
+                for algo in cxx.ALGOS["broadcast"]:
                     for inplace in (False, True):
-                        want = schedules.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
+                        want = cxx.broadcast(A, N, root, algo, dtype, inplace=inplace).outputs
                         recvs = [Guarded(count, dtype) for _ in range(N)]
                         if inplace:
                             recvs[root].t.copy_(to_dev(A))
@@ -167,7 +167,7 @@ def test_rooted_collectives_single_launch(N):
                             assert same_bits(recvs[r].host(), want[r]), ("bcast", algo, N, root, count, inplace, r)
                         _check_launches(recs, limit, _nsteps("broadcast", algo, N, count, dtype, root), ("bcast", algo))
                 for algo in ("pipe_chain", "pipe_tree"):
-                    want = schedules.broadcast_pipelined(A, N, root, algo, dtype, 3).outputs
+                    want = cxx.broadcast_pipelined(A, N, root, algo, dtype, 3).outputs
                     recvs = [Guarded(count, dtype) for _ in range(N)]
                     src = Guarded(count, dtype, fill=A).t
                     recs = _traced(lambda: vc.vc_broadcast_pipelined(src, [g.t for g in recvs], root=root,
@@ -177,8 +177,8 @@ def test_rooted_collectives_single_launch(N):
                         assert same_bits(recvs[r].host(), want[r]), (algo, N, root, count, r)
                     _check_launches(recs, limit, _nsteps("broadcast", algo, N, count, dtype, root, nchunks=3), algo)
                 S = int32_bits(7400 + root, N, N * count)
-                for algo in schedules.ALGOS["scatter"]:
-                    want = schedules.scatter(S, N, root, algo, dtype).outputs
+                for algo in cxx.ALGOS["scatter"]:
+                    want = cxx.scatter(S, N, root, algo, dtype).outputs
                     src_g = Guarded(N * count, dtype, fill=S)
                     recvs = [Guarded(count, dtype) for _ in range(N)]
                     recs = _traced(lambda: vc.vc_scatter(src_g.t, [g.t for g in recvs], root=root, algo=algo))
@@ -187,16 +187,16 @@ def test_rooted_collectives_single_launch(N):
                         assert same_bits(recvs[r].host(), want[r]), ("scatter", algo, N, root, count, r)
                     _check_launches(recs, limit, _nsteps("scatter", algo, N, count, dtype, root), ("scatter", algo))
                 xs = _inputs("f32", 7500 + root + count, N, count)
-                for algo in schedules.ALGOS_EXTRA["gather"]:
-                    want = schedules.gather(xs, root, algo, "f32").outputs[0]
+                for algo in cxx.ALGOS_EXTRA["gather"]:
+                    want = cxx.gather(xs, root, algo, "f32").outputs[0]
                     sends = [Guarded(count, "f32", fill=x) for x in xs]
                     out = Guarded(N * count, "f32")
                     recs = _traced(lambda: vc.vc_gather([g.t for g in sends], out.t, root=root, algo=algo))
                     assert out.guards_intact() and same_bits(out.host(), want), ("gather", algo, N, root, count)
                     _check_launches(recs, limit, _nsteps("gather", algo, N, count, "f32", root), ("gather", algo))
-                for algo in schedules.ALGOS_EXTRA["reduce"]:
+                for algo in cxx.ALGOS_EXTRA["reduce"]:
                     for op in ("sum", "min"):
-                        want = schedules.reduce(xs, root, algo, "f32", op=op).outputs[0]
+                        want = cxx.reduce(xs, root, algo, "f32", op=op).outputs[0]
                         sends = [Guarded(count, "f32", fill=x) for x in xs]
                         out = Guarded(count, "f32")
                         recs = _traced(lambda: vc.vc_reduce([g.t for g in sends], out.t, root=root, algo=algo, op=op))
@@ -210,7 +210,7 @@ def test_unaligned_pointers_fall_back_to_per_step_launches():
     N, count = 4, 4096 + 3
     xs = _inputs("f32", 7600, N, count)
     for algo in ("ring", "rhd", "dbt"):
-        want = schedules.allreduce(xs, algo, "f32").outputs
+        want = cxx.allreduce(xs, algo, "f32").outputs
         sends = [Guarded(count, "f32", shift=1, fill=x) for x in xs]
         recvs = [Guarded(count, "f32", shift=1) for _ in range(N)]
         recs = _traced(lambda: vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo))
@@ -224,7 +224,7 @@ def test_description_too_large_falls_back_to_per_step_launches():
     vc.vc_set_single_launch(ALWAYS)
     N, count = 64, 640
     xs = _inputs("f32", 7700, N, count)
-    want = schedules.allreduce(xs, "ring", "f32").outputs
+    want = cxx.allreduce(xs, "ring", "f32").outputs
     sends = [Guarded(count, "f32", fill=x) for x in xs]
     recvs = [Guarded(count, "f32") for _ in range(N)]
     recs = _traced(lambda: vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo="ring"))
@@ -267,8 +267,8 @@ def test_single_launch_inside_a_cuda_graph():
             fresh[r].copy_(to_dev(ys[r]))
         g.replay()
         torch.cuda.synchronize()
-        want = schedules.allreduce(xs, "dbt", "f32").outputs
-        want2 = schedules.allreduce(ys, "rhd", "f32").outputs
+        want = cxx.allreduce(xs, "dbt", "f32").outputs
+        want2 = cxx.allreduce(ys, "rhd", "f32").outputs
         for r in range(N):
             assert same_bits(recvs[r].cpu().numpy(), want[r]), (seed, r)
             assert same_bits(fresh_out[r].cpu().numpy(), want2[r]), (seed, r)

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import rank_buffers
 
 from .gpu_util import same_bits, to_dev, to_host
@@ -49,7 +49,7 @@ def _worker(tid, errors):
                     recvs = [torch.empty_like(s) for s in sends]
                     vc.vc_allreduce(sends, recvs, algo=algo, stream=stream)
                     stream.synchronize()
-                    want = schedules.allreduce(xs, algo, dtype).outputs
+                    want = cxx.allreduce(xs, algo, dtype).outputs
                     for r in range(N):
                         if not same_bits(to_host(recvs[r]), want[r]):
                             errors.append((tid, rep, algo, N, count, dtype, r))

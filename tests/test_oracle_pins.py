@@ -20,6 +20,8 @@ from oracle import cxx, numerics, orders, schedules
 from oracle.partition import chunk_elems, chunk_range
 from synthetic_inputs import int32_bits, rank_buffers, small_ints_f32, uniform_pm1_f32
 
+from . import witness
+
 
 # ----------------------------------------------------------------------------
 # printed tables
@@ -368,6 +370,88 @@ def test_order_witnesses_n4(golden, sim):
             for o in res.outputs:
                 assert numerics.same_bits(o, got)
         assert np.array_equal(got, want), (row[0], algo, got)
+
+
+def _witness_results(sim, wid, N, algo, xs):
+    if algo.startswith("rs_"):
+        res = sim.reduce_scatter(xs, algo[3:], "f32")
+        return [np.concatenate(res.outputs)]
+    return sim.allreduce(xs, algo, "f32").outputs
+
+
+def test_order_witnesses_n8_and_foldin(golden, sim):
+    """Hand-derived witnesses: the N = 8 Ring, RHD and both Double Binary
+    Trees, and RHD's fold-in at N = 5, 6, 7 (every rank's output)."""
+    for wid, N, algo, xs, want in witness.rows(golden):
+        for r, got in enumerate(_witness_results(sim, wid, N, algo, xs)):
+            assert np.array_equal(got, want), (wid, N, algo, r, got)
+
+
+def test_order_witnesses_n8_and_foldin_closed_forms(golden):
+    """The same witnesses against both closed-form statements of the trees."""
+    for wid, N, algo, xs, want in witness.rows(golden):
+        count = len(xs[0])
+        for closed in (orders, cxx):
+            if algo.startswith("rs_"):
+                got = closed.reduce_scatter_at(xs, algo[3:], count // N, "f32", np.arange(count))
+            else:
+                got = closed.allreduce_at(xs, algo, count, "f32", np.arange(count))
+            assert np.array_equal(got, want), (wid, N, algo, closed.__name__, got)
+
+
+def test_planted_rhd_mapping_fault_is_caught(monkeypatch, golden):
+    """Placing virtual rank 1 on the wrong real rank (a plausible mistake in
+    the fold-in's mapping) turns a fold-in witness red."""
+    real = schedules.rhd_virtual_ranks
+
+    def swapped(N):
+        P, r, m = real(N)
+        m = list(m)
+        m[1], m[2] = m[2], m[1]
+        return P, r, m
+
+    monkeypatch.setattr(schedules, "rhd_virtual_ranks", swapped)
+    failed = [wid for wid, N, algo, xs, want in witness.rows(golden)
+              if algo == "rhd" and N in (5, 6, 7)
+              and not np.array_equal(schedules.allreduce(xs, "rhd", "f32").outputs[0], want)]
+    assert failed
+
+
+def test_planted_dbt_tree_fault_is_caught(monkeypatch, golden):
+    """Building tree B as a copy of tree A instead of its mirror, or summing a
+    node's children before adding its own value, turns an N = 8 witness red."""
+    real = schedules.dbt_trees
+
+    def unmirrored(N, count, esize):
+        (na, fa, ra), (nb, fb, rb) = real(N, count, esize)
+        return [(na, fa, ra), (nb, fa, rb)]
+
+    monkeypatch.setattr(schedules, "dbt_trees", unmirrored)
+    failed = [wid for wid, N, algo, xs, want in witness.rows(golden)
+              if algo == "dbt" and not np.array_equal(schedules.allreduce(xs, "dbt", "f32").outputs[0], want)]
+    assert failed
+    monkeypatch.undo()
+    # the right-hand association: children summed first, then the node's own value
+    def kids_first(tree):
+        if isinstance(tree, int):
+            return tree
+        a, b = tree
+        if isinstance(a, tuple) and isinstance(a[0], int):  # ((own, left), right)
+            return (a[0], (kids_first(a[1]), kids_first(b)))
+        return (kids_first(a), kids_first(b))
+
+    wrong = 0
+    for wid, N, algo, xs, want in witness.rows(golden):
+        if algo != "dbt":
+            continue
+        count = len(xs[0])
+        half = count // 2
+        for lo, hi in ((0, half), (half, count)):
+            t = kids_first(orders.allreduce_tree("dbt", N, count, "f32", lo))
+            cols = {r: xs[r][lo:hi] for r in range(N)}
+            if not np.array_equal(orders.evaluate(t, cols), want[lo:hi]):
+                wrong += 1
+    assert wrong
 
 
 @pytest.mark.parametrize("N", [2, 3, 4, 5, 7, 8, 16])

@@ -18,7 +18,7 @@ import pytest
 import torch
 
 import collective_communication_algorithms_virtual_gb300 as vc
-from oracle import schedules
+from oracle import cxx
 from synthetic_inputs import normal_f32, rank_buffers
 
 from .gpu_util import first_diff, same_bits, to_dev, to_host
@@ -66,7 +66,7 @@ def _check_two_calls(L, dtype, N, rc, seed0):
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):  # two calls in a row, different data
         xs = _inputs(dtype, seed0 + call, N, N * rc)
-        want = schedules.reduce_scatter(xs, "ring", dtype).outputs
+        want = cxx.reduce_scatter(xs, "ring", dtype).outputs
         send = [to_dev(x) for x in xs]
         alloc = [torch.empty(rc, dtype=TDT[dtype], device="cuda") for _ in range(N)]
         got = [torch.full((rc,), -7, dtype=TDT[dtype], device="cuda") for _ in range(N)]
