@@ -19,7 +19,8 @@ buffers, and the oracle's CPU time.
 Multi-GPU: replicas only (every GPU runs the same workload on its own
 buffers; nothing crosses GPUs); value = all ranks' bytes / the slowest rank.
 
-``--impl reference`` times the CPU oracle (oracle/) on the host instead.
+``--impl reference`` times the C++ oracle (oracle/sim.cpp, single-threaded) on
+the host instead, at the same 256 MiB per rank, one AllReduce per step.
 """
 from __future__ import annotations
 
@@ -188,11 +189,12 @@ class ClockSampler:
 # the oracle on the host: CPU baseline and reference arm
 # ----------------------------------------------------------------------------
 
-def oracle_step(xs) -> None:
-    from oracle import schedules
+def oracle_step(xs, algos=None) -> None:
+    """One step of the workload through the C++ oracle (single-threaded)."""
+    from oracle import cxx
 
-    for algo in ALGOS:
-        schedules.allreduce(xs, algo, "f32")
+    for algo in (algos or ALGOS):
+        cxx.allreduce(xs, algo, "f32", want_log=False, want_outputs=False)
 
 
 def oracle_inputs(mib_per_rank: float):
@@ -202,14 +204,23 @@ def oracle_inputs(mib_per_rank: float):
     return [uniform_pm1_f32(2, r, count) for r in range(NVR)], count * 4
 
 
+ORACLE_KIND = "C++ oracle (oracle/sim.cpp, g++ -O2), single-threaded"
+
+
 def time_oracle(target_s: float = 15.0, mib: float | None = None) -> dict:
-    """The oracle, as it stands, on a bounded sample of the workload."""
+    """The oracle, as it stands, on a bounded sample of the workload: whole
+    steps (every algorithm) at a message size sized to the target time."""
+    from oracle import cxx
+
+    cxx.build()
     if mib is None:
-        xs, _ = oracle_inputs(1)
+        xs, _ = oracle_inputs(16)
+        oracle_step(xs)  # first touch of the oracle's memory
         t0 = time.perf_counter()
         oracle_step(xs)
         t1 = time.perf_counter() - t0
-        mib = max(1, min(64, int(target_s / 3 / max(t1, 1e-3))))
+        mib = int(max(1, min(256, 16 * target_s / 2 / max(t1, 1e-3))))
+        del xs
     xs, nbytes = oracle_inputs(mib)
     reps, total, t_start = 0, 0.0, time.perf_counter()
     while True:
@@ -221,39 +232,41 @@ def time_oracle(target_s: float = 15.0, mib: float | None = None) -> dict:
             break
     busbw = step_bus_bytes(nbytes) * reps / total / 1e9
     return {"value": busbw, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"N={NVR} fp32 AllReduce ring+rhd+dbt+fused at {nbytes >> 20} MiB per rank, "
-                       f"{reps} step(s), {total:.1f} s, single-threaded numpy on a host with "
-                       f"{os.cpu_count()} cores")}
+            "sample": (f"{ORACLE_KIND}, 1 thread of nproc={os.cpu_count()}: N={NVR} fp32 AllReduce "
+                       f"ring+rhd+dbt+fused at {nbytes / (1 << 20):g} MiB per rank, {reps} step(s), {total:.1f} s")}
 
 
 def run_reference(args) -> int:
+    """The oracle timed on the host cores on the GPU arm's workload: N = 8,
+    fp32, 256 MiB per rank (--ref-mib changes it).  A step is one AllReduce
+    with one algorithm, the algorithms taken in turn (ring, rhd, dbt, fused,
+    ring, ...), so that K steps of the single-threaded oracle end within a few
+    minutes; busbw = the bus bytes of the K AllReduces / their time."""
+    from oracle import cxx
+
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    cxx.build()
     steps, warm = args.steps, args.warmup
-    mib = args.ref_mib
-    if mib is None:
-        xs, _ = oracle_inputs(1)
-        t0 = time.perf_counter()
-        oracle_step(xs)
-        t1 = time.perf_counter() - t0
-        budget = 120.0 / max(1, steps + warm)
-        mib = max(1, min(256, int(budget / max(t1, 1e-3))))
+    mib = args.ref_mib if args.ref_mib is not None else BYTES_PER_RANK / (1 << 20)
     xs, nbytes = oracle_inputs(mib)
-    for _ in range(warm):
-        oracle_step(xs)
+    for i in range(warm):
+        oracle_step(xs, [ALGOS[i % len(ALGOS)]])
     t0 = time.perf_counter()
-    for _ in range(steps):
-        oracle_step(xs)
+    for i in range(steps):
+        oracle_step(xs, [ALGOS[i % len(ALGOS)]])
     el = time.perf_counter() - t0
-    value = step_bus_bytes(nbytes) * steps / el / 1e9
+    value = step_bus_bytes(nbytes, nalgos=1) * steps / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_block(nbytes),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{nbytes >> 20} MiB per rank (bench workload at 256 MiB), {steps} steps"},
+                         "sample": (f"{ORACLE_KIND}, 1 thread of nproc={os.cpu_count()}: "
+                                    f"{nbytes / (1 << 20):g} MiB per rank, one AllReduce per step, "
+                                    f"algorithms in turn {','.join(ALGOS)}")},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -377,7 +390,8 @@ def run_ours(args) -> int:
         out["per_algo"] = per_algo(vc, send, recv, stream, M, peaks)
         if not args.no_sweep:
             out["sweep"] = sweep(vc, send, recv, stream)
-            out["alpha_beta"] = alpha_beta_fit(out["sweep"])
+            out["alpha_beta"] = alpha_beta_fit(
+                out["sweep"], auto=lambda M: vc.vc_select_algo("allreduce", N, M // 4, "f32")[0])
         if not args.no_configs:
             out["configs"] = other_configs(vc, dev, peaks)
 
@@ -552,13 +566,61 @@ def sweep(vc, send, recv, stream):
     return res
 
 
-def alpha_beta_fit(sw: dict, min_bytes: int = 0) -> dict:
+def _crossover(ta, tb, a: str, b: str, sizes=None):
+    """Where two cost lines T = s * alpha + k * M cross, as a record: the
+    message size per rank (bytes) or, when they never cross at a positive
+    size, which algorithm the model finds faster at every size."""
+    (sa, ka), (sb, kb) = ta, tb
+    if ka != kb:
+        m = (sb - sa) / (ka - kb)
+        if m > 0:
+            return {"bytes_per_rank": m, "below": a if sa < sb else b, "above": b if sa < sb else a}
+    faster = a if (sa, ka) <= (sb, kb) else b
+    if sa == sb and ka == kb:
+        return {"bytes_per_rank": None, "never": "equal cost at every size"}
+    return {"bytes_per_rank": None, "never": f"{faster} faster at every size"}
+
+
+def measured_crossover(pa: list, pb: list, a: str, b: str):
+    """Every swept size at which the faster of the two changes (graph-timed):
+    the first of them as ``bytes_per_rank``, all of them in ``switches``."""
+    first = pa[0]["us"] < pb[0]["us"]
+    cur, switches = first, []
+    for x, y in zip(pa, pb):
+        now = x["us"] < y["us"]
+        if now != cur:
+            switches.append({"bytes_per_rank": x["bytes_per_rank"], "faster_from_here": a if now else b})
+            cur = now
+    if not switches:
+        return {"bytes_per_rank": None, "never": f"{a if first else b} faster at every swept size"}
+    return {"bytes_per_rank": switches[0]["bytes_per_rank"], "below": a if first else b, "switches": switches}
+
+
+# The latency-formula page's AllReduce costs (eqs. model-algo-ring-ar, -rhd-ar,
+# -dbt-ar) as (alpha coefficient, coefficient of M / beta) at N ranks.
+def page_costs(N: int) -> dict:
+    import math
+
+    lg = math.log2(N)
+    return {"ring": (2 * (N - 1), 2 * (N - 1) / N), "rhd": (2 * lg, 2 * (N - 1) / N), "dbt": (2 * lg, lg)}
+
+
+def alpha_beta_fit(sw: dict, min_bytes: int = 0, auto=None) -> dict:
     """Least-squares fit of T = steps * alpha + bytes / beta over the graph-timed
-    sweep of every algorithm: alpha is the cost of one dependent step (launch)
-    on this GPU, beta the HBM rate; the pages' model with a launch for a link
-    start-up and HBM for the link.  Reports the fit and, per pair of
-    algorithms, the crossover message size the fit predicts next to the one
-    measured."""
+    sweep of every algorithm: alpha is the cost of one dependent step on this
+    GPU, beta the HBM rate -- the pages' model with a launch for a link
+    start-up and HBM for the link.
+
+    For every pair of algorithms it reports three crossover message sizes:
+    the one measured in the sweep; the one the fitted HBM model predicts
+    (each algorithm's steps and algorithmic bytes per byte of message, from
+    the library's plans); and the one the latency-formula page's link
+    formulas give with the fitted alpha and beta (eq.
+    model-algo-ring-dbt-crossover and its analogues; the fused kernel has no
+    formula on the pages).  Where two cost lines never cross the record says
+    which algorithm is faster at every size.  ``auto(bytes_per_rank)`` gives
+    the algorithm AUTO picks; the sizes where it is not the measured fastest
+    are listed."""
     import numpy as np
 
     rows, ts = [], []
@@ -573,27 +635,39 @@ def alpha_beta_fit(sw: dict, min_bytes: int = 0) -> dict:
     alpha, inv_beta = float(coef[0]), float(coef[1])
     pred = A @ coef
     N = NVR
-    lg = np.log2(N)
     out = {"alpha_us": alpha * 1e6, "beta_gbs": 1.0 / inv_beta / 1e9 if inv_beta > 0 else None,
-           "median_rel_err": float(np.median(np.abs(pred - t) / t)), "crossovers": {},
-           # the latency-formula page's Ring/DBT crossover (link model) with these constants;
-           # on one GPU DBT moves fewer HBM bytes than Ring, so no crossover is measured
-           "page_ring_dbt_crossover_bytes": (2 * alpha * (1.0 / inv_beta) * ((N - 1) - lg) /
-                                             (lg - 2 * (N - 1) / N)) if inv_beta > 0 else None}
+           "median_rel_err": float(np.median(np.abs(pred - t) / t)), "crossovers": {}}
+    # each algorithm's (steps, algorithmic bytes per message byte) at the largest swept size
+    shape = {a: (pts[-1]["steps"], pts[-1]["algorithmic_bytes"] / pts[-1]["bytes_per_rank"]) for a, pts in sw.items()}
+    pc = page_costs(N)
     algos = list(sw)
     for i, a in enumerate(algos):
         for b in algos[i + 1:]:
-            meas = None
-            for pa, pb in zip(sw[a], sw[b]):
-                if meas is None and (pa["us"] < pb["us"]) != (sw[a][0]["us"] < sw[b][0]["us"]):
-                    meas = pa["bytes_per_rank"]
-            def model(p):
-                return p["steps"] * alpha + p["algorithmic_bytes"] * inv_beta
-            predm = None
-            for pa, pb in zip(sw[a], sw[b]):
-                if predm is None and (model(pa) < model(pb)) != (model(sw[a][0]) < model(sw[b][0])):
-                    predm = pa["bytes_per_rank"]
-            out["crossovers"][f"{a}/{b}"] = {"measured_bytes_per_rank": meas, "predicted_bytes_per_rank": predm}
+            hbm = _crossover((shape[a][0] * alpha, shape[a][1] * inv_beta),
+                             (shape[b][0] * alpha, shape[b][1] * inv_beta), a, b)
+            if a in pc and b in pc:
+                link = _crossover((pc[a][0] * alpha, pc[a][1] * inv_beta), (pc[b][0] * alpha, pc[b][1] * inv_beta), a, b)
+            else:
+                link = {"bytes_per_rank": None, "never": "no formula for the fused kernel on the pages"}
+            out["crossovers"][f"{a}/{b}"] = {"measured": measured_crossover(sw[a], sw[b], a, b),
+                                             "predicted_hbm_model": hbm, "predicted_page_formula": link}
+    if auto is not None:
+        diffs, sched = [], [x for x in algos if x in pc]
+        for k, p in enumerate(sw[algos[0]]):
+            M = p["bytes_per_rank"]
+            fastest = min(algos, key=lambda x: sw[x][k]["us"])
+            fastest_sched = min(sched, key=lambda x: sw[x][k]["us"]) if sched else None
+            pick = auto(M)
+            if pick != fastest:
+                diffs.append({"bytes_per_rank": M, "auto": pick, "measured_fastest": fastest,
+                              "auto_us": sw[pick][k]["us"] if pick in sw else None, "fastest_us": sw[fastest][k]["us"]})
+            # among the schedules alone the HBM model always ranks by steps then bytes
+            model_sched = min(sched, key=lambda x: (shape[x][0] * alpha + shape[x][1] * inv_beta * M)) if sched else None
+            if model_sched != fastest_sched:
+                out.setdefault("schedule_model_vs_measured", []).append(
+                    {"bytes_per_rank": M, "model": model_sched, "measured_fastest": fastest_sched,
+                     "model_us": sw[model_sched][k]["us"], "fastest_us": sw[fastest_sched][k]["us"]})
+        out["auto_vs_measured"] = {"sizes": len(sw[algos[0]]), "differs_at": diffs}
     return out
 
 
@@ -768,7 +842,7 @@ def main(argv=None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--details-out", default=None, help="also write every section as one JSON file here")
     ap.add_argument("--ref-mib", type=float, default=None,
-                    help="reference arm: MiB per rank of the oracle's sample (default: sized to ~2 min)")
+                    help="reference arm: MiB per rank (default: the workload's 256)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -123,3 +123,34 @@ def test_final_line_is_short_and_last(tmp_path):
     assert {"per_algo", "sweep", "alpha_beta", "configs", "roofline"} <= sections
     with open(tmp_path / "d.json") as f:
         assert json.load(f)["sweep"] == out["sweep"]
+
+
+def test_alpha_beta_fit_predicts_every_pair():
+    """A sweep that follows T = steps * alpha + bytes / beta exactly, with the
+    latency-formula page's NVLink constants (alpha 5 us, beta 450 GB/s): the fit
+    recovers them, the page formula puts the Ring/DBT crossover at 14.4 MB
+    (eq. model-algo-ring-dbt-crossover), and every pair gets a prediction from
+    both models (a size, or which algorithm is faster at every size)."""
+    alpha, beta = 5e-6, 450e9
+    shape = {"ring": (14, 35), "rhd": (6, 35), "dbt": (6, 29), "fused": (1, 16)}
+    sw = {a: [] for a in shape}
+    for lg in range(10, 29):
+        M = 1 << lg
+        for a, (s, k) in shape.items():
+            t = s * alpha + k * M / beta
+            sw[a].append({"bytes_per_rank": M, "us": t * 1e6, "steps": s, "algorithmic_bytes": k * M})
+    r = bench.alpha_beta_fit(sw, auto=lambda M: "fused")
+    assert abs(r["alpha_us"] - 5.0) < 1e-6 and abs(r["beta_gbs"] - 450.0) < 1e-6
+    assert len(r["crossovers"]) == 6
+    for pair, c in r["crossovers"].items():
+        for key in ("predicted_hbm_model", "predicted_page_formula", "measured"):
+            v = c[key]
+            assert v["bytes_per_rank"] is not None or v.get("never"), (pair, key, v)
+    page = r["crossovers"]["ring/dbt"]["predicted_page_formula"]
+    assert abs(page["bytes_per_rank"] - 1.44e7) / 1.44e7 < 1e-9 and page["below"] == "dbt"
+    # in the HBM model DBT moves fewer bytes in fewer steps than Ring: no crossover
+    assert r["crossovers"]["ring/dbt"]["predicted_hbm_model"]["never"] == "dbt faster at every size"
+    # measured on this exact sweep: the same as the HBM model
+    assert r["crossovers"]["ring/dbt"]["measured"]["never"] == "dbt faster at every swept size"
+    assert r["auto_vs_measured"]["differs_at"] == []
+    assert "schedule_model_vs_measured" not in r
