@@ -34,6 +34,10 @@ from .binding import (  # noqa: F401
     vc_device_errors,
     vc_copy_selftest,
     SINGLE_LAUNCH_ALWAYS,
+    vc_set_slice_limit,
+    vc_get_slice_limit,
+    SLICE_ALWAYS,
+    VC_SLICE_DEFAULT,
     vc_set_reuse_order,
     vc_get_reuse_order,
     REUSE_ORDER_NEVER,

@@ -44,6 +44,8 @@ KERNEL_OPS = {0: "sum", 1: "max", 2: "min"}
 def kernel_name(code: int) -> str:
     mode = KERNEL_MODES[code & 7]
     name = mode if mode == "copy" else f"{KERNEL_OPS[(code >> 3) & 3]}_{mode}"
+    if code & 256:  # one launch over the whole GPU, each thread carrying its group through every step
+        return name + "_sliced"
     if code & 128:  # one cluster launch for the whole plan
         return name + "_single_launch"
     extra = ("_tma" if mode == "copy" else "_batched") if code & 64 else ""
@@ -114,6 +116,10 @@ def lib() -> ctypes.CDLL:
         L.vc_set_single_launch.restype = I
         L.vc_get_single_launch.argtypes = [ctypes.POINTER(Z)]
         L.vc_get_single_launch.restype = I
+        L.vc_set_slice_limit.argtypes = [Z]
+        L.vc_set_slice_limit.restype = I
+        L.vc_get_slice_limit.argtypes = [ctypes.POINTER(Z)]
+        L.vc_get_slice_limit.restype = I
         L.vc_set_reuse_order.argtypes = [Z]
         L.vc_set_reuse_order.restype = I
         L.vc_get_reuse_order.argtypes = [ctypes.POINTER(Z)]
@@ -312,6 +318,23 @@ def vc_get_single_launch() -> int:
 
 
 SINGLE_LAUNCH_ALWAYS = (1 << 64) - 1
+
+
+def vc_set_slice_limit(max_bytes_per_rank: int) -> None:
+    """Run eligible schedules (fp32 / int32 AllReduce and the like) whose
+    message per rank is at most this many bytes in the sliced form (0: never;
+    SLICE_ALWAYS: whenever eligible)."""
+    check(lib().vc_set_slice_limit(int(max_bytes_per_rank)))
+
+
+def vc_get_slice_limit() -> int:
+    v = ctypes.c_size_t(0)
+    check(lib().vc_get_slice_limit(ctypes.byref(v)))
+    return v.value
+
+
+SLICE_ALWAYS = (1 << 64) - 1
+VC_SLICE_DEFAULT = 16 << 20  # VC_SLICE_LIMIT_DEFAULT
 
 
 def vc_set_reuse_order(min_step_bytes: int) -> None:

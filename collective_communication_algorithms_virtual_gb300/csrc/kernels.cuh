@@ -936,6 +936,7 @@ struct __align__(16) PlanParams {
   const uint4* plan;  // the description, 16-byte words
   uint32_t words;
   uint32_t nbases;
+  int64_t groups;     // sliced plans: 16-byte groups per rank buffer that the plan covers
   const void* base[2 * VC_MAX_RANKS + 1];
 };
 
@@ -974,6 +975,90 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     }
     if (s + 1 < h.nsteps)
       asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
+}
+
+// -- element-sliced plans ---------------------------------------------------------
+// A plan whose every operation maps element e of each source to element e of
+// each destination, at the same byte offset in every rank buffer (the fp32 /
+// int32 AllReduce schedules: Ring, RHD, DBT, Mesh), can run with its step
+// barrier kept per element instead of per launch.  The buffers are cut into
+// slices of kThreads 16-byte groups; thread i of a block owns group i of its
+// slice -- the same bytes of every rank's send and receive buffer -- for the
+// whole launch.  The thread walks the plan's steps in order and, in each,
+// applies every operation that covers its group: sources combined in the
+// plan's order, the result stored to every destination.  Whatever a step
+// reads at a position was written there by an earlier step, by this same
+// thread, so program order is the step barrier and no thread reads what
+// another wrote (loads go to L2 with .cg; a thread's own earlier store to the
+// address is ordered before them).  Steps, operations, operands and every
+// element's association are the plan's; only positions far apart run out of
+// step with each other, as when a ring is pipelined in slices.  The
+// operation's first element is its operands' common offset / 4; the element
+// after its last group whole is handled by the owner of that group.
+template <int RMODE, int OP>
+__global__ void __launch_bounds__(kThreads) slice_kernel(const __grid_constant__ PlanParams p) {
+  static_assert(RMODE == kF32 || RMODE == kI32, "sliced plans are fp32 or int32");
+  extern __shared__ uint4 sm[];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (uint32_t i = threadIdx.x; i < p.words; i += kThreads) sm[i] = ld16(p.plan + i);
+  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
+  for (uint32_t i = threadIdx.x; i < p.nbases; i += kThreads) sbase[i] = p.base[i];
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
+  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
+  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
+  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
+  const int64_t nslices = (p.groups + kThreads - 1) / kThreads;
+  for (int64_t sl = blockIdx.x; sl < nslices; sl += gridDim.x) {
+    const int64_t g = sl * kThreads + threadIdx.x;  // this thread's group
+    if (g >= p.groups) break;
+    for (uint32_t s = 0; s < h.nsteps; ++s) {
+      const PlanStep st = steps[s];
+      for (uint32_t k = 0; k < st.nops; ++k) {
+        const OpDesc& o = ops[st.op0 + k];
+        const int64_t e0 = refs[o.p0].off >> 2;  // first element (a multiple of 4)
+        const int64_t e = g * 4;                 // first element of the group
+        if (e < e0 || e >= e0 + o.n) continue;
+        const RefPtrs ptr{refs + o.p0, sbase};
+        const int64_t off = (e - e0) * 4;        // bytes into every operand
+        if (e + 4 <= e0 + o.n) {
+          uint4 acc = ld16_cg(static_cast<const char*>(ptr[0]) + off);
+          if (st.mode != kCopy) {
+            for (int q = 1; q < o.ns; ++q) {
+              const uint4 w = ld16_cg(static_cast<const char*>(ptr[q]) + off);
+              if constexpr (RMODE == kF32) {
+                acc.x = __float_as_uint(cmb<OP>(__uint_as_float(acc.x), __uint_as_float(w.x)));
+                acc.y = __float_as_uint(cmb<OP>(__uint_as_float(acc.y), __uint_as_float(w.y)));
+                acc.z = __float_as_uint(cmb<OP>(__uint_as_float(acc.z), __uint_as_float(w.z)));
+                acc.w = __float_as_uint(cmb<OP>(__uint_as_float(acc.w), __uint_as_float(w.w)));
+              } else {
+                acc.x = cmbi<OP>(acc.x, w.x);
+                acc.y = cmbi<OP>(acc.y, w.y);
+                acc.z = cmbi<OP>(acc.z, w.z);
+                acc.w = cmbi<OP>(acc.w, w.w);
+              }
+            }
+          }
+          for (int d = 0; d < o.nd; ++d) st16_wb(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + off, acc);
+        } else {
+          // the operation ends inside this group: its last elements one by one
+          for (int64_t x = e; x < e0 + o.n; ++x) {
+            const int64_t xo = (x - e0) * 4;
+            uint32_t a = ld32<true>(static_cast<const char*>(ptr[0]) + xo);
+            if (st.mode != kCopy)
+              for (int q = 1; q < o.ns; ++q) {
+                const uint32_t w = ld32<true>(static_cast<const char*>(ptr[q]) + xo);
+                if constexpr (RMODE == kF32) a = __float_as_uint(cmb<OP>(__uint_as_float(a), __uint_as_float(w)));
+                else a = cmbi<OP>(a, w);
+              }
+            for (int d = 0; d < o.nd; ++d)
+              *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + xo) = a;
+          }
+        }
+      }
+    }
   }
 }
 

@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <tuple>
 #include <map>
 #include <memory>
 #include <unordered_map>
@@ -699,6 +700,7 @@ PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std
 // ---------------------------------------------------------------------------
 std::mutex g_sl_mu;
 size_t g_sl_limit = VC_SINGLE_LAUNCH_DEFAULT;
+size_t g_slice_limit = VC_SLICE_LIMIT_DEFAULT;
 constexpr int kPlanSmemMax = 96 << 10;            // description + bases in shared memory
 constexpr size_t kPlanArenaChunk = 4u << 20;      // device memory for descriptions, per allocation
 constexpr size_t kPlanArenaMax = 64u << 20;       // and in total, per device
@@ -706,6 +708,10 @@ constexpr size_t kPlanArenaMax = 64u << 20;       // and in total, per device
 size_t single_launch_limit() {
   std::lock_guard<std::mutex> lk(g_sl_mu);
   return g_sl_limit;
+}
+size_t slice_limit() {
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  return g_slice_limit;
 }
 
 struct DevPlan {
@@ -718,6 +724,7 @@ struct DevPlan {
   int64_t max_step_bytes = 0;
   int64_t bytes = 0;
   int nops = 0;
+  bool sliced = false;           // every operation keeps element positions: the sliced form applies
 };
 struct PlanStore {
   std::unordered_map<PlanKey, DevPlan, PlanKeyHash> plans;
@@ -853,6 +860,19 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
   dp->words = static_cast<uint32_t>(words);
   dp->nops = static_cast<int>(nops);
   dp->eligible = true;
+  // The sliced form (slice_kernel): fp32 / int32 steps and 4-byte copies
+  // whose operands all sit at one 16-byte aligned offset of a send or receive
+  // buffer, one run each, so that every operation maps element e to element e.
+  dp->sliced = dp->rmode == dev::kF32 || dp->rmode == dev::kI32;
+  for (const Step& st : plan.steps)
+    for (const Op& op : st.ops) {
+      if (!dp->sliced) break;
+      const int64_t off = op.dst.empty() ? -1 : op.dst[0].byte_off;
+      bool ok = op.nb == 1 && (off & 15) == 0 && (st.mode != Mode::Copy || op.src.size() == 1);
+      for (const Operand& o : op.src) ok &= o.buf != Buf::Scratch && o.byte_off == off && esize(o.dt) == 4;
+      for (const Operand& o : op.dst) ok &= o.buf != Buf::Scratch && o.byte_off == off && esize(o.dt) == 4;
+      dp->sliced = ok;
+    }
 }
 
 // The resident description of a plan shape, uploading it at the first call
@@ -910,17 +930,92 @@ const DevPlan* resident_plan(int dev, const PlanKey& key, const Plan& plan, int 
   return &ps.plans.emplace(key, dp).first->second;
 }
 
+using SliceKernel = void (*)(dev::PlanParams);
+template <int RMODE>
+SliceKernel slice_kernel_op(RedOp r) {
+  switch (r) {
+    case RedOp::Max: return dev::slice_kernel<RMODE, dev::kMax>;
+    case RedOp::Min: return dev::slice_kernel<RMODE, dev::kMin>;
+    default: return dev::slice_kernel<RMODE, dev::kSum>;
+  }
+}
+
+// A sliced plan (slice_kernel): one launch over the whole GPU, each thread
+// carrying its 16-byte group of every buffer through every step.
+vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanParams& prm, cudaStream_t stream,
+                          const LaunchCtx& tc) {
+  const SliceKernel kernel = dp.rmode == dev::kI32 ? slice_kernel_op<dev::kI32>(dp.red) : slice_kernel_op<dev::kF32>(dp.red);
+  const size_t smem = dp.words * 16 + prm.nbases * sizeof(void*);
+  int per_sm = 0;
+  {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, size_t, DeviceState*>, int> occ;
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), smem, st);
+    auto it = occ.find(key);
+    if (it == occ.end()) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, dev::kThreads, smem);
+      if (e != cudaSuccess) return cuda_fail(e, "sliced plan occupancy");
+      it = occ.emplace(key, std::max(1, per_sm)).first;
+    }
+    per_sm = it->second;
+  }
+  const int64_t slices = (prm.groups + dev::kThreads - 1) / dev::kThreads;
+  const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(slices, int64_t(st->nsm) * per_sm)));
+  std::unique_lock<std::mutex> lk(g_trace_mu);
+  const bool trace = trace_slot();
+  if (!trace) lk.unlock();
+  Pending pend{};
+  if (trace) {
+    cudaError_t e = take_event(&pend.start);
+    if (e == cudaSuccess) e = take_event(&pend.stop);
+    if (e == cudaSuccess) e = cudaEventRecord(pend.start, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event");
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(dev::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (trace) {
+    e = cudaEventRecord(pend.stop, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace event");
+    pend.rec.coll = tc.coll;
+    pend.rec.algo = tc.algo;
+    pend.rec.step = -1;
+    pend.rec.kernel = dp.rmode | (static_cast<int>(dp.red) << 3) | 128 | 256;
+    pend.rec.bytes = dp.bytes;
+    pend.rec.nops = dp.nops;
+    g_trace.push_back(pend);
+  }
+  return VC_SUCCESS;
+}
+
+// slice_groups > 0: run the plan in the sliced form over that many 16-byte
+// groups per buffer; otherwise as one cluster with a barrier between steps.
 vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<const void*>& sends,
-                        const std::vector<void*>& recvs, char* scratch, cudaStream_t stream, const LaunchCtx& tc) {
+                        const std::vector<void*>& recvs, char* scratch, cudaStream_t stream, const LaunchCtx& tc,
+                        DeviceState* st = nullptr, int64_t slice_groups = 0) {
   dev::PlanParams prm{};
   prm.plan = dp.dptr;
   prm.words = dp.words;
   prm.nbases = static_cast<uint32_t>(2 * N + 1);
+  prm.groups = slice_groups;
   for (int r = 0; r < N; ++r) {
     prm.base[r] = sends[r];
     prm.base[N + r] = recvs[r];
   }
   prm.base[2 * N] = scratch;
+  if (slice_groups > 0) return launch_sliced(dp, st, prm, stream, tc);
   const PlanKernel kernel = plan_kernel_for(dp.rmode, dp.red);
   int cluster;
   {
@@ -1109,21 +1204,30 @@ vc_status_t run(const Call& c) {
   tc.coll = static_cast<int>(c.coll);
   tc.algo = static_cast<int>(pa.algo);
   for (const Step& s : plan.steps) tc.pipeline &= s.mode != Mode::BF16 && s.mode != Mode::F16;
-  // one launch for the whole plan when it is small enough and eligible
+  // one launch for the whole plan when it is small enough and eligible: the
+  // sliced form where every operation keeps element positions, else one
+  // cluster with a barrier between steps
   const DevPlan* dp = nullptr;
+  int64_t slice_groups = 0;
+  bool aligned = (reinterpret_cast<uintptr_t>(scratch) & 15) == 0;
+  for (int r = 0; r < N; ++r)
+    aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
+               (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
+  const size_t slim = slice_limit();
+  if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 && es == 4 &&
+      static_cast<uint64_t>(c.count * es) <= std::min<uint64_t>(slim, INT64_MAX)) {
+    dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
+    if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;
+    else dp = nullptr;
+  }
   const size_t limit = single_launch_limit();
-  if (limit > 0 && plan.steps.size() >= 2 && plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
-    bool aligned = (reinterpret_cast<uintptr_t>(scratch) & 15) == 0;
-    for (int r = 0; r < N; ++r)
-      aligned &= (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0 && (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0;
-    if (aligned) {
-      dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
-      if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > limit)) dp = nullptr;
-    }
+  if (!dp && aligned && limit > 0 && plan.steps.size() >= 2 && plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
+    dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
+    if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > limit)) dp = nullptr;
   }
   if (dp) {
     tc.step = -1;
-    rc = launch_plan(*dp, dev, N, sends, recvs, scratch, c.stream, tc);
+    rc = launch_plan(*dp, dev, N, sends, recvs, scratch, c.stream, tc, st, slice_groups);
     if (rc == VC_SUCCESS) launches = 1;
   } else {
     for (size_t si = 0; si < plan.steps.size(); ++si) {
@@ -1718,6 +1822,19 @@ VC_EXPORT vc_status_t vc_get_single_launch(size_t* max_step_bytes) {
   if (!max_step_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
   std::lock_guard<std::mutex> lk(g_sl_mu);
   *max_step_bytes = g_sl_limit;
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank) {
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  g_slice_limit = max_bytes_per_rank;
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank) {
+  if (!max_bytes_per_rank) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+  std::lock_guard<std::mutex> lk(g_sl_mu);
+  *max_bytes_per_rank = g_slice_limit;
   return VC_SUCCESS;
 }
 

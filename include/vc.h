@@ -350,7 +350,8 @@ vc_status_t vc_plan_exec_order(vc_coll_t coll, vc_algo_t algo, int nranks, size_
  *   launch took the bulk-copy (TMA) pipeline, bit 7
  *   set for a single-launch plan (vc_set_single_launch: one record for the
  *   whole call, step -1, bytes and nops of all steps; bits 0-2 then give the
- *   mode of the plan's reduction steps).
+ *   mode of the plan's reduction steps), bit 8 set as well when that launch
+ *   ran the sliced form (vc_set_slice_limit).
  */
 typedef struct {
   int32_t coll;   /* vc_coll_t */
@@ -398,6 +399,31 @@ vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n
 #define VC_SINGLE_LAUNCH_DEFAULT ((size_t)768 << 10)
 vc_status_t vc_set_single_launch(size_t max_step_bytes);
 vc_status_t vc_get_single_launch(size_t* max_step_bytes);
+
+/*
+ * Sliced execution (a form of single-launch execution, tried before the
+ * cluster form).
+ *
+ * In the fp32 and int32 AllReduce schedules (Ring, RHD, DBT, Mesh,
+ * RING_HOP) every operation maps element e of each source to element e of
+ * each destination, at the same offset in every rank buffer.  An AllReduce
+ * call of such a schedule whose message per rank is at most
+ * `max_bytes_per_rank` runs all its steps in one launch over the whole GPU:
+ * each thread owns one 16-byte group -- the same bytes of every rank's send
+ * and receive buffer -- and carries it through every step of the plan in
+ * order, applying each operation that covers it.  What a step reads at a
+ * position was written there by an earlier step, by the same thread, so the
+ * thread's program order is the step barrier and no thread reads what another
+ * wrote.  The steps, operations, operands and every element's association
+ * are unchanged, so results are identical bit for bit; different positions
+ * merely run out of step with each other, as when a ring is pipelined in
+ * slices.  The conditions of single-launch execution on alignment and the
+ * resident description apply as well.  max_bytes_per_rank: 0 disables it,
+ * SIZE_MAX applies it to every eligible call.  Process-wide.
+ */
+#define VC_SLICE_LIMIT_DEFAULT ((size_t)16 << 20)
+vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank);
+vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank);
 
 /*
  * Bulk-copy pipeline for large copy steps (no counterpart on the source

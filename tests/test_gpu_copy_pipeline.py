@@ -34,10 +34,13 @@ def _lib():
     vc.lib()
     old_sl = vc.vc_get_single_launch()
     old_cp = vc.vc_get_copy_pipeline()
+    old_slice = vc.vc_get_slice_limit()
     vc.vc_set_single_launch(0)  # every step its own launch, so copy steps take the step kernels
+    vc.vc_set_slice_limit(0)
     vc.vc_set_copy_pipeline(0)
     yield
     vc.vc_set_single_launch(old_sl)
+    vc.vc_set_slice_limit(old_slice)
     vc.vc_set_copy_pipeline(old_cp)
 
 

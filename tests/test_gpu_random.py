@@ -4,8 +4,9 @@
 (1-16), element count (log-uniform 1..5000, so odd sizes and ragged tails;
 one in ten 5000..100000 for several tiles per operation),
 data type, reduction op, root, in place or not, 16-byte aligned or not, and
-the execution form (default, forced single launch, one launch per step;
-the last with the bulk-copy pipeline taken by every aligned copy launch on
+the execution form (default, forced single launch in one cluster, forced
+sliced form, one launch per step; the per-step form with the bulk-copy
+pipeline taken by every aligned copy launch on
 odd-numbered calls and by none on even ones, and with the L2 reuse order
 forced onto every step on calls numbered 1 mod 4).
 Each must equal the oracle's simulation of the same schedule bit for bit,
@@ -42,7 +43,9 @@ def _lib():
     old = vc.vc_get_single_launch()
     old_cp = vc.vc_get_copy_pipeline()
     old_ro = vc.vc_get_reuse_order()
+    old_slice = vc.vc_get_slice_limit()
     yield
+    vc.vc_set_slice_limit(old_slice)
     vc.vc_set_single_launch(old)
     vc.vc_set_copy_pipeline(old_cp)
     vc.vc_set_reuse_order(old_ro)
@@ -72,7 +75,7 @@ def _case(rng):
     root = int(rng.integers(N))
     inplace = bool(rng.integers(2)) and coll in ("allreduce", "broadcast", "reduce")
     shift = int(rng.integers(2))
-    form = ("default", "single", "per_step")[rng.integers(3)]
+    form = ("default", "single", "per_step", "sliced")[rng.integers(4)]
     nchunks = int(rng.integers(1, 6))
     return coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks
 
@@ -140,7 +143,10 @@ def test_random_calls_match_oracle():
     ran = 0
     for i in range(1000):
         coll, algo, N, count, dtype, op, root, inplace, shift, form, nchunks = _case(rng)
-        vc.vc_set_single_launch({"default": 768 << 10, "single": vc.SINGLE_LAUNCH_ALWAYS, "per_step": 0}[form])
+        vc.vc_set_single_launch({"default": 768 << 10, "single": vc.SINGLE_LAUNCH_ALWAYS, "per_step": 0,
+                                 "sliced": 768 << 10}[form])
+        vc.vc_set_slice_limit({"default": vc.VC_SLICE_DEFAULT, "single": 0, "per_step": 0,
+                               "sliced": vc.SLICE_ALWAYS}[form])
         if form == "per_step":
             vc.vc_set_copy_pipeline(0 if i % 2 else vc.COPY_PIPELINE_NEVER)
             want_reuse = 0 if i % 4 == 1 else 16 << 20  # the reuse order forced on a quarter of them

@@ -30,12 +30,14 @@ def _lib():
 
     build.build()
     vc.lib()
-    saved = (vc.vc_get_reuse_order(), vc.vc_get_single_launch(), vc.vc_get_copy_pipeline())
+    saved = (vc.vc_get_reuse_order(), vc.vc_get_single_launch(), vc.vc_get_copy_pipeline(), vc.vc_get_slice_limit())
     vc.vc_set_reuse_order(0)
+    vc.vc_set_slice_limit(0)  # the per-step and cluster forms are the ones ordered for reuse
     yield
     vc.vc_set_reuse_order(saved[0])
     vc.vc_set_single_launch(saved[1])
     vc.vc_set_copy_pipeline(saved[2])
+    vc.vc_set_slice_limit(saved[3])
     assert vc.vc_device_errors() == 0
 
 

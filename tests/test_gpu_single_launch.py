@@ -37,9 +37,11 @@ def _lib():
 
 @pytest.fixture(autouse=True)
 def _restore_limit():
-    old = vc.vc_get_single_launch()
+    old, old_slice = vc.vc_get_single_launch(), vc.vc_get_slice_limit()
+    vc.vc_set_slice_limit(0)  # the cluster form is the one under test here (the sliced form: test_gpu_sliced.py)
     yield
     vc.vc_set_single_launch(old)
+    vc.vc_set_slice_limit(old_slice)
 
 
 def _inputs(dtype, seed, N, n):

@@ -1,0 +1,146 @@
+"""The sliced form of fp32 / int32 AllReduce schedules, against the oracle.
+
+In the sliced form (vc_set_slice_limit) one launch over the whole GPU runs
+every step of the plan, each thread carrying its 16-byte group of every rank
+buffer through the steps in order.  Forced on for every eligible call here:
+Ring, RHD (any rank count, with the fold-in), DBT, Mesh and the per-hop ring
+on fp32 and int32 with every op, ragged counts whose last group is partial,
+sizes from one element to 64 MiB per rank, in place.  Every result must equal
+the C++ oracle's simulation of the same schedule bit for bit, and the launch
+trace must show one sliced launch for the call.  Also: calls that do not
+qualify (16-bit data, unaligned pointers, single-step plans, other
+collectives) take the other forms and stay exact; the default size limit;
+canary bands around every buffer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import collective_communication_algorithms_virtual_gb300 as vc
+from oracle import cxx
+from synthetic_inputs import rank_buffers
+
+from .gpu_util import Guarded, first_diff, same_bits, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+SLICED_ALGOS = ("ring", "rhd", "dbt", "mesh", "ring_hop")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from collective_communication_algorithms_virtual_gb300 import build
+
+    build.build()
+    vc.lib()
+    old = vc.vc_get_slice_limit()
+    yield
+    vc.vc_set_slice_limit(old)
+    assert vc.vc_device_errors() == 0
+
+
+def _inputs(dtype, seed, N, n):
+    return rank_buffers({"f32": "uniform_f32", "i32": "int32_bits", "bf16": "normal_bf16"}[dtype], seed, N, n)
+
+
+def _traced(fn):
+    vc.vc_trace_enable(True)
+    try:
+        fn()
+        torch.cuda.synchronize()
+        return vc.vc_trace_read()
+    finally:
+        vc.vc_trace_enable(False)
+
+
+def _run(xs, algo, dtype, op="sum", shift=0, inplace=False):
+    N, count = len(xs), len(xs[0])
+    sends = [Guarded(count, dtype, shift, fill=x) for x in xs]
+    recvs = sends if inplace else [Guarded(count, dtype, shift) for _ in range(N)]
+    recs = _traced(lambda: vc.vc_allreduce([g.t for g in sends], [g.t for g in recvs], algo=algo, op=op))
+    assert all(g.guards_intact() for g in sends + recvs)
+    return [g.host() for g in recvs], recs
+
+
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("N", [2, 3, 4, 5, 7, 8, 9, 16])
+def test_sliced_allreduce_matches_oracle(N, dtype, op):
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    for count in (1, 3, 4, 13, 1023, 4096 + 5, 65536 + 37) + ((300_001,) if op == "sum" else ()):
+        xs = _inputs(dtype, 8100 + N + count, N, count)
+        for algo in SLICED_ALGOS:
+            want = cxx.allreduce(xs, algo, dtype, op=op, want_log=False).outputs
+            got, recs = _run(xs, algo, dtype, op)
+            assert len(recs) == 1 and recs[0]["kernel"].endswith("_sliced"), (algo, N, count, recs)
+            for r in range(N):
+                assert same_bits(got[r], want[r]), (algo, N, dtype, op, count, r, first_diff(got[r], want[r]))
+
+
+@pytest.mark.parametrize("N", [4, 8])
+def test_sliced_in_place(N):
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    for count in (777, 100_000):
+        xs = _inputs("f32", 8200 + N + count, N, count)
+        for algo in SLICED_ALGOS:
+            want = cxx.allreduce(xs, algo, "f32", want_log=False).outputs
+            got, recs = _run(xs, algo, "f32", inplace=True)
+            assert recs[0]["kernel"].endswith("_sliced"), (algo, recs)
+            for r in range(N):
+                assert same_bits(got[r], want[r]), (algo, N, count, r)
+
+
+def test_sliced_large_messages():
+    """64 MiB per rank, 8 ranks: every element of rank 0 and every rank equal."""
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    N, count = 8, (64 << 20) // 4
+    xs = _inputs("f32", 8300, N, count)
+    sends = [to_dev(x) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    for algo in ("ring", "rhd", "dbt"):
+        recs = _traced(lambda: vc.vc_allreduce(sends, recvs, algo=algo))
+        assert recs[0]["kernel"].endswith("_sliced"), recs
+        for r in range(1, N):
+            assert torch.equal(recvs[r], recvs[0]), (algo, r)
+        want = cxx.allreduce(xs, algo, "f32", want_log=False, keep=(0,)).outputs[0]
+        got = to_host(recvs[0])
+        assert same_bits(got, want), (algo, first_diff(got, want))
+
+
+def test_calls_that_do_not_qualify_take_other_forms():
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    N, count = 8, 4096 + 3
+    # 16-bit data (fp32 partials in scratch), unaligned pointers, a single-step plan
+    xb = _inputs("bf16", 8400, N, count)
+    for algo in ("ring", "rhd", "dbt"):
+        want = cxx.allreduce(xb, algo, "bf16", want_log=False).outputs
+        got, recs = _run(xb, algo, "bf16")
+        assert not any(r["kernel"].endswith("_sliced") for r in recs), (algo, recs)
+        assert all(same_bits(got[r], want[r]) for r in range(N)), algo
+    xs = _inputs("f32", 8401, N, count)
+    for algo in ("ring", "fused"):
+        want = cxx.allreduce(xs, algo, "f32", want_log=False).outputs
+        got, recs = _run(xs, algo, "f32", shift=1 if algo == "ring" else 0)
+        assert not any(r["kernel"].endswith("_sliced") for r in recs), (algo, recs)
+        assert all(same_bits(got[r], want[r]) for r in range(N)), algo
+    # another collective with 4-byte data: a binomial Broadcast
+    A = np.arange(count, dtype=np.int32)
+    outs = [torch.empty(count, dtype=torch.int32, device="cuda") for _ in range(N)]
+    recs = _traced(lambda: vc.vc_broadcast(to_dev(A), outs, root=0, algo="binomial"))
+    assert not any(r["kernel"].endswith("_sliced") for r in recs), recs
+    assert all(np.array_equal(to_host(o), A) for o in outs)
+
+
+def test_default_limit():
+    vc.vc_set_slice_limit(vc.VC_SLICE_DEFAULT)
+    assert vc.vc_get_slice_limit() == vc.VC_SLICE_DEFAULT
+    N = 8
+    for nbytes, sliced in ((1 << 20, True), (vc.VC_SLICE_DEFAULT, True), (2 * vc.VC_SLICE_DEFAULT, False)):
+        count = nbytes // 4
+        x = [torch.rand(count, device="cuda") for _ in range(N)]
+        y = [torch.empty_like(t) for t in x]
+        recs = _traced(lambda: vc.vc_allreduce(x, y, algo="ring"))
+        assert any(r["kernel"].endswith("_sliced") for r in recs) == sliced, (nbytes, recs)
+        s = torch.stack(x).sum(0)
+        assert torch.allclose(y[0], s, atol=1e-5), nbytes
