@@ -997,8 +997,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 // operation's first element is its operands' common offset / 4; the element
 // after its last group whole is handled by the owner of that group.
 template <int RMODE, int OP>
-__global__ void __launch_bounds__(kThreads) slice_kernel(const __grid_constant__ PlanParams p) {
+__device__ __forceinline__ uint4 cmb4(uint4 a, uint4 w) {
+  if constexpr (RMODE == kF32) {
+    a.x = __float_as_uint(cmb<OP>(__uint_as_float(a.x), __uint_as_float(w.x)));
+    a.y = __float_as_uint(cmb<OP>(__uint_as_float(a.y), __uint_as_float(w.y)));
+    a.z = __float_as_uint(cmb<OP>(__uint_as_float(a.z), __uint_as_float(w.z)));
+    a.w = __float_as_uint(cmb<OP>(__uint_as_float(a.w), __uint_as_float(w.w)));
+  } else {
+    a.x = cmbi<OP>(a.x, w.x);
+    a.y = cmbi<OP>(a.y, w.y);
+    a.z = cmbi<OP>(a.z, w.z);
+    a.w = cmbi<OP>(a.w, w.w);
+  }
+  return a;
+}
+
+// BT threads a block; U groups a thread, BT apart (slices of U * BT groups);
+// the loads of a thread's groups in a step are issued together.
+template <int RMODE, int OP, int U, int BT>
+__global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanParams p) {
   static_assert(RMODE == kF32 || RMODE == kI32, "sliced plans are fp32 or int32");
+  constexpr int kThreads = BT;  // this kernel's block (shadows the step kernels' size)
   extern __shared__ uint4 sm[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (uint32_t i = threadIdx.x; i < p.words; i += kThreads) sm[i] = ld16(p.plan + i);
@@ -1010,41 +1029,50 @@ __global__ void __launch_bounds__(kThreads) slice_kernel(const __grid_constant__
   const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
   const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
   const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
-  const int64_t nslices = (p.groups + kThreads - 1) / kThreads;
+  constexpr int64_t kSlice = int64_t(U) * kThreads;
+  const int64_t nslices = (p.groups + kSlice - 1) / kSlice;
   for (int64_t sl = blockIdx.x; sl < nslices; sl += gridDim.x) {
-    const int64_t g = sl * kThreads + threadIdx.x;  // this thread's group
-    if (g >= p.groups) break;
+    const int64_t g0 = sl * kSlice + threadIdx.x;  // this thread's groups: g0 + u * kThreads
+    if (g0 >= p.groups) break;
     for (uint32_t s = 0; s < h.nsteps; ++s) {
       const PlanStep st = steps[s];
       for (uint32_t k = 0; k < st.nops; ++k) {
         const OpDesc& o = ops[st.op0 + k];
         const int64_t e0 = refs[o.p0].off >> 2;  // first element (a multiple of 4)
-        const int64_t e = g * 4;                 // first element of the group
-        if (e < e0 || e >= e0 + o.n) continue;
+        const int64_t e1 = e0 + o.n;
+        if (g0 * 4 >= e1 || (g0 + (U - 1) * kThreads) * 4 + 4 <= e0) continue;  // none of the groups
         const RefPtrs ptr{refs + o.p0, sbase};
-        const int64_t off = (e - e0) * 4;        // bytes into every operand
-        if (e + 4 <= e0 + o.n) {
-          uint4 acc = ld16_cg(static_cast<const char*>(ptr[0]) + off);
-          if (st.mode != kCopy) {
-            for (int q = 1; q < o.ns; ++q) {
-              const uint4 w = ld16_cg(static_cast<const char*>(ptr[q]) + off);
-              if constexpr (RMODE == kF32) {
-                acc.x = __float_as_uint(cmb<OP>(__uint_as_float(acc.x), __uint_as_float(w.x)));
-                acc.y = __float_as_uint(cmb<OP>(__uint_as_float(acc.y), __uint_as_float(w.y)));
-                acc.z = __float_as_uint(cmb<OP>(__uint_as_float(acc.z), __uint_as_float(w.z)));
-                acc.w = __float_as_uint(cmb<OP>(__uint_as_float(acc.w), __uint_as_float(w.w)));
-              } else {
-                acc.x = cmbi<OP>(acc.x, w.x);
-                acc.y = cmbi<OP>(acc.y, w.y);
-                acc.z = cmbi<OP>(acc.z, w.z);
-                acc.w = cmbi<OP>(acc.w, w.w);
-              }
-            }
+        bool whole[U];
+        uint4 acc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t e = (g0 + u * kThreads) * 4;
+          whole[u] = e >= e0 && e + 4 <= e1;
+          if (whole[u]) acc[u] = ld16_cg(static_cast<const char*>(ptr[0]) + (e - e0) * 4);
+        }
+        if (st.mode != kCopy) {
+          for (int q = 1; q < o.ns; ++q) {
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (whole[u]) w[u] = ld16_cg(static_cast<const char*>(ptr[q]) + ((g0 + u * kThreads) * 4 - e0) * 4);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (whole[u]) acc[u] = cmb4<RMODE, OP>(acc[u], w[u]);
           }
-          for (int d = 0; d < o.nd; ++d) st16_wb(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + off, acc);
-        } else {
-          // the operation ends inside this group: its last elements one by one
-          for (int64_t x = e; x < e0 + o.n; ++x) {
+        }
+        for (int d = 0; d < o.nd; ++d) {
+          char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d]));
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (whole[u]) st16_wb(dp + ((g0 + u * kThreads) * 4 - e0) * 4, acc[u]);
+        }
+        // the operation ends inside a group: its last elements one by one
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t e = (g0 + u * kThreads) * 4;
+          if (whole[u] || e < e0 || e >= e1) continue;
+          for (int64_t x = e; x < e1; ++x) {
             const int64_t xo = (x - e0) * 4;
             uint32_t a = ld32<true>(static_cast<const char*>(ptr[0]) + xo);
             if (st.mode != kCopy)

@@ -931,20 +931,38 @@ const DevPlan* resident_plan(int dev, const PlanKey& key, const Plan& plan, int 
 }
 
 using SliceKernel = void (*)(dev::PlanParams);
-template <int RMODE>
+template <int RMODE, int U, int BT>
 SliceKernel slice_kernel_op(RedOp r) {
   switch (r) {
-    case RedOp::Max: return dev::slice_kernel<RMODE, dev::kMax>;
-    case RedOp::Min: return dev::slice_kernel<RMODE, dev::kMin>;
-    default: return dev::slice_kernel<RMODE, dev::kSum>;
+    case RedOp::Max: return dev::slice_kernel<RMODE, dev::kMax, U, BT>;
+    case RedOp::Min: return dev::slice_kernel<RMODE, dev::kMin, U, BT>;
+    default: return dev::slice_kernel<RMODE, dev::kSum, U, BT>;
   }
 }
+template <int U, int BT>
+SliceKernel slice_kernel_for(int rmode, RedOp r) {
+  return rmode == dev::kI32 ? slice_kernel_op<dev::kI32, U, BT>(r) : slice_kernel_op<dev::kF32, U, BT>(r);
+}
+// The sliced form's launch shape, measured on 8 ranks (ring / DBT / RHD, 64 KiB
+// to 8 MiB per rank): 256-thread blocks, and at most 64 blocks until every
+// thread carries 8 groups (a thread issues its groups' loads of a step
+// together).  Grids of 128 or more blocks of one group a thread were up to
+// twice as slow in the 512 KiB - 2 MiB range, and 512- or 1024-thread blocks
+// slower at small sizes.
+constexpr int kSliceBlock = 256;
+constexpr int kSliceMaxBlocks = 64;
 
 // A sliced plan (slice_kernel): one launch over the whole GPU, each thread
 // carrying its 16-byte group of every buffer through every step.
 vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanParams& prm, cudaStream_t stream,
                           const LaunchCtx& tc) {
-  const SliceKernel kernel = dp.rmode == dev::kI32 ? slice_kernel_op<dev::kI32>(dp.red) : slice_kernel_op<dev::kF32>(dp.red);
+  const int64_t g = prm.groups, per_block = kSliceBlock;
+  int U = 1;
+  while (U < 8 && g > int64_t(kSliceMaxBlocks) * per_block * U) U *= 2;
+  const SliceKernel kernel = U == 1 ? slice_kernel_for<1, kSliceBlock>(dp.rmode, dp.red)
+                           : U == 2 ? slice_kernel_for<2, kSliceBlock>(dp.rmode, dp.red)
+                           : U == 4 ? slice_kernel_for<4, kSliceBlock>(dp.rmode, dp.red)
+                                    : slice_kernel_for<8, kSliceBlock>(dp.rmode, dp.red);
   const size_t smem = dp.words * 16 + prm.nbases * sizeof(void*);
   int per_sm = 0;
   {
@@ -955,13 +973,13 @@ vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanPar
     auto it = occ.find(key);
     if (it == occ.end()) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
-      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, dev::kThreads, smem);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kSliceBlock, smem);
       if (e != cudaSuccess) return cuda_fail(e, "sliced plan occupancy");
       it = occ.emplace(key, std::max(1, per_sm)).first;
     }
     per_sm = it->second;
   }
-  const int64_t slices = (prm.groups + dev::kThreads - 1) / dev::kThreads;
+  const int64_t slices = (prm.groups + int64_t(U) * kSliceBlock - 1) / (int64_t(U) * kSliceBlock);
   const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(slices, int64_t(st->nsm) * per_sm)));
   std::unique_lock<std::mutex> lk(g_trace_mu);
   const bool trace = trace_slot();
@@ -975,7 +993,7 @@ vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanPar
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(dev::kThreads);
+  cfg.blockDim = dim3(kSliceBlock);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1213,8 +1231,13 @@ vc_status_t run(const Call& c) {
   for (int r = 0; r < N; ++r)
     aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
                (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
+  // RHD applies several operations to each position per halving step (4 in
+  // the first with 8 ranks), which lengthens every thread's chain: measured
+  // slower sliced than in the other forms up to 4 MiB per rank, so it takes
+  // the sliced form only when the limit is SIZE_MAX.
   const size_t slim = slice_limit();
-  if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 && es == 4 &&
+  const bool slice_algo = pa.algo != Algo::RHD || slim == SIZE_MAX;
+  if (aligned && slim > 0 && slice_algo && c.coll == Coll::AllReduce && plan.steps.size() >= 2 && es == 4 &&
       static_cast<uint64_t>(c.count * es) <= std::min<uint64_t>(slim, INT64_MAX)) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;
