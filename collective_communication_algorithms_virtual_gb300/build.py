@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libvcoll.so")
 SOURCES = ["plan.cpp", "vc.cu"]
-HEADERS = ["plan.h", "kernels.cuh"]
+HEADERS = ["plan.h", "kernels.cuh", "slice.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

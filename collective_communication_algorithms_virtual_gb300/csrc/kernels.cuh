@@ -978,117 +978,5 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   }
 }
 
-// -- element-sliced plans ---------------------------------------------------------
-// A plan whose every operation maps element e of each source to element e of
-// each destination, at the same byte offset in every rank buffer (the fp32 /
-// int32 AllReduce schedules: Ring, RHD, DBT, Mesh), can run with its step
-// barrier kept per element instead of per launch.  The buffers are cut into
-// slices of kThreads 16-byte groups; thread i of a block owns group i of its
-// slice -- the same bytes of every rank's send and receive buffer -- for the
-// whole launch.  The thread walks the plan's steps in order and, in each,
-// applies every operation that covers its group: sources combined in the
-// plan's order, the result stored to every destination.  Whatever a step
-// reads at a position was written there by an earlier step, by this same
-// thread, so program order is the step barrier and no thread reads what
-// another wrote (loads go to L2 with .cg; a thread's own earlier store to the
-// address is ordered before them).  Steps, operations, operands and every
-// element's association are the plan's; only positions far apart run out of
-// step with each other, as when a ring is pipelined in slices.  The
-// operation's first element is its operands' common offset / 4; the element
-// after its last group whole is handled by the owner of that group.
-template <int RMODE, int OP>
-__device__ __forceinline__ uint4 cmb4(uint4 a, uint4 w) {
-  if constexpr (RMODE == kF32) {
-    a.x = __float_as_uint(cmb<OP>(__uint_as_float(a.x), __uint_as_float(w.x)));
-    a.y = __float_as_uint(cmb<OP>(__uint_as_float(a.y), __uint_as_float(w.y)));
-    a.z = __float_as_uint(cmb<OP>(__uint_as_float(a.z), __uint_as_float(w.z)));
-    a.w = __float_as_uint(cmb<OP>(__uint_as_float(a.w), __uint_as_float(w.w)));
-  } else {
-    a.x = cmbi<OP>(a.x, w.x);
-    a.y = cmbi<OP>(a.y, w.y);
-    a.z = cmbi<OP>(a.z, w.z);
-    a.w = cmbi<OP>(a.w, w.w);
-  }
-  return a;
-}
-
-// BT threads a block; U groups a thread, BT apart (slices of U * BT groups);
-// the loads of a thread's groups in a step are issued together.
-template <int RMODE, int OP, int U, int BT>
-__global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanParams p) {
-  static_assert(RMODE == kF32 || RMODE == kI32, "sliced plans are fp32 or int32");
-  constexpr int kThreads = BT;  // this kernel's block (shadows the step kernels' size)
-  extern __shared__ uint4 sm[];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (uint32_t i = threadIdx.x; i < p.words; i += kThreads) sm[i] = ld16(p.plan + i);
-  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
-  for (uint32_t i = threadIdx.x; i < p.nbases; i += kThreads) sbase[i] = p.base[i];
-  __syncthreads();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
-  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
-  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
-  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
-  constexpr int64_t kSlice = int64_t(U) * kThreads;
-  const int64_t nslices = (p.groups + kSlice - 1) / kSlice;
-  for (int64_t sl = blockIdx.x; sl < nslices; sl += gridDim.x) {
-    const int64_t g0 = sl * kSlice + threadIdx.x;  // this thread's groups: g0 + u * kThreads
-    if (g0 >= p.groups) break;
-    for (uint32_t s = 0; s < h.nsteps; ++s) {
-      const PlanStep st = steps[s];
-      for (uint32_t k = 0; k < st.nops; ++k) {
-        const OpDesc& o = ops[st.op0 + k];
-        const int64_t e0 = refs[o.p0].off >> 2;  // first element (a multiple of 4)
-        const int64_t e1 = e0 + o.n;
-        if (g0 * 4 >= e1 || (g0 + (U - 1) * kThreads) * 4 + 4 <= e0) continue;  // none of the groups
-        const RefPtrs ptr{refs + o.p0, sbase};
-        bool whole[U];
-        uint4 acc[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int64_t e = (g0 + u * kThreads) * 4;
-          whole[u] = e >= e0 && e + 4 <= e1;
-          if (whole[u]) acc[u] = ld16_cg(static_cast<const char*>(ptr[0]) + (e - e0) * 4);
-        }
-        if (st.mode != kCopy) {
-          for (int q = 1; q < o.ns; ++q) {
-            uint4 w[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-              if (whole[u]) w[u] = ld16_cg(static_cast<const char*>(ptr[q]) + ((g0 + u * kThreads) * 4 - e0) * 4);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-              if (whole[u]) acc[u] = cmb4<RMODE, OP>(acc[u], w[u]);
-          }
-        }
-        for (int d = 0; d < o.nd; ++d) {
-          char* dp = static_cast<char*>(const_cast<void*>(ptr[o.ns + d]));
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-            if (whole[u]) st16_wb(dp + ((g0 + u * kThreads) * 4 - e0) * 4, acc[u]);
-        }
-        // the operation ends inside a group: its last elements one by one
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int64_t e = (g0 + u * kThreads) * 4;
-          if (whole[u] || e < e0 || e >= e1) continue;
-          for (int64_t x = e; x < e1; ++x) {
-            const int64_t xo = (x - e0) * 4;
-            uint32_t a = ld32<true>(static_cast<const char*>(ptr[0]) + xo);
-            if (st.mode != kCopy)
-              for (int q = 1; q < o.ns; ++q) {
-                const uint32_t w = ld32<true>(static_cast<const char*>(ptr[q]) + xo);
-                if constexpr (RMODE == kF32) a = __float_as_uint(cmb<OP>(__uint_as_float(a), __uint_as_float(w)));
-                else a = cmbi<OP>(a, w);
-              }
-            for (int d = 0; d < o.nd; ++d)
-              *reinterpret_cast<uint32_t*>(static_cast<char*>(const_cast<void*>(ptr[o.ns + d])) + xo) = a;
-          }
-        }
-      }
-    }
-  }
-}
-
 }  // namespace dev
 }  // namespace vc

@@ -657,9 +657,8 @@ class Builder {
   // rank s = i-k k rounds ago and are addressed to ranks i, i+1, ..., s-1;
   // it keeps the one for itself (block s of its output) and stages the rest,
   // indexed by destination, in one of two forwarding buffers (round k writes
-  // buffer k%2 while rank i+1 reads rank i's buffer (k-1)%2).  The local
-  // block is copied in round 1's launch: it reads and writes nothing that
-  // round's messages touch.
+  // buffer k%2 while rank i+1 reads rank i's buffer (k-1)%2).  Round 0 is the
+  // local block.
   void alltoall_ring(int64_t B) {
     const int64_t fbytes = int64_t(N_) * B * es_;
     int64_t F[2] = {0, 0};
@@ -668,10 +667,12 @@ class Builder {
       F[1] = alloc(int64_t(N_) * fbytes);
     }
     auto fwd = [&](int which, int rank, int d) { return Sc(rank, F[which] + rank * fbytes + d * B * es_, a_.dt); };
+    {
+      const size_t st = new_step(Mode::Copy);
+      for (int i = 0; i < N_; ++i) copy(st, S(i, i * B), R(i, i * B), B);
+    }
     for (int k = 1; k < N_; ++k) {
       const size_t st = new_step(Mode::Copy);
-      if (k == 1)  // the local block, in the first round's launch (it is no message)
-        for (int i = 0; i < N_; ++i) copy(st, S(i, i * B), R(i, i * B), B);
       for (int i = 0; i < N_; ++i) {
         const int from = md(i - 1, N_), src = md(i - k, N_);
         auto held = [&](int d) { return k == 1 ? S(from, int64_t(d) * B) : fwd((k - 1) & 1, from, d); };
@@ -696,14 +697,11 @@ class Builder {
       return;
     }
     if (a_.algo == Algo::Pairwise) {
-      // In round k = 1 .. N-1 rank i writes its block for rank (i+k) mod N
-      // into block i of that rank's output.  The local block (k = 0) is
-      // copied in round 1's launch: it is no message, and it reads and writes
-      // nothing that round's messages touch.
-      for (int k = 1; k < N_; ++k) {
+      // Round 0 is the local block; in round k rank i writes its block for
+      // rank (i+k) mod N into block i of that rank's output.
+      for (int k = 0; k < N_; ++k) {
         const size_t st = new_step(Mode::Copy);
         for (int i = 0; i < N_; ++i) {
-          if (k == 1) copy(st, S(i, i * B), R(i, i * B), B);
           const int j = (i + k) % N_;
           copy(st, S(i, j * B), R(j, i * B), B);
         }

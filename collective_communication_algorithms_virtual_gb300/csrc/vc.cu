@@ -27,6 +27,7 @@
 #include <vector>
 
 #include "kernels.cuh"
+#include "slice.cuh"
 #include "plan.h"
 #include "vc.h"
 
@@ -725,6 +726,7 @@ struct DevPlan {
   int64_t bytes = 0;
   int nops = 0;
   bool sliced = false;           // every operation keeps element positions: the sliced form applies
+  uint32_t nrefs = 0;
 };
 struct PlanStore {
   std::unordered_map<PlanKey, DevPlan, PlanKeyHash> plans;
@@ -859,11 +861,14 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
   }
   dp->words = static_cast<uint32_t>(words);
   dp->nops = static_cast<int>(nops);
+  dp->nrefs = static_cast<uint32_t>(nrefs);
   dp->eligible = true;
   // The sliced form (slice_kernel): fp32 / int32 steps and 4-byte copies
   // whose operands all sit at one 16-byte aligned offset of a send or receive
   // buffer, one run each, so that every operation maps element e to element e.
-  dp->sliced = dp->rmode == dev::kF32 || dp->rmode == dev::kI32;
+  dp->sliced = (dp->rmode == dev::kF32 || dp->rmode == dev::kI32) &&
+               dev::slice_smem_bytes(dp->words, 2 * N + 1, static_cast<uint32_t>(nops), static_cast<uint32_t>(nrefs)) <=
+                   static_cast<size_t>(kPlanSmemMax);
   for (const Step& st : plan.steps)
     for (const Op& op : st.ops) {
       if (!dp->sliced) break;
@@ -943,14 +948,14 @@ template <int U, int BT>
 SliceKernel slice_kernel_for(int rmode, RedOp r) {
   return rmode == dev::kI32 ? slice_kernel_op<dev::kI32, U, BT>(r) : slice_kernel_op<dev::kF32, U, BT>(r);
 }
-// The sliced form's launch shape, measured on 8 ranks (ring / DBT / RHD, 64 KiB
-// to 8 MiB per rank): 256-thread blocks, and at most 64 blocks until every
-// thread carries 8 groups (a thread issues its groups' loads of a step
-// together).  Grids of 128 or more blocks of one group a thread were up to
-// twice as slow in the 512 KiB - 2 MiB range, and 512- or 1024-thread blocks
-// slower at small sizes.
+// The sliced form's launch shape, measured on 8 ranks (ring / DBT / RHD, 256 KiB
+// to 8 MiB per rank): 256-thread blocks; one group a thread while that takes
+// at most 64 blocks, else the fewest groups a thread (2, 4 or 8, whose loads
+// of a step a thread issues together) that take at most two blocks per SM.
+// Grids of more than 64 blocks of one group a thread were up to twice as
+// slow, and 512- or 1024-thread blocks slower at small sizes.
 constexpr int kSliceBlock = 256;
-constexpr int kSliceMaxBlocks = 64;
+constexpr int kSliceSmallGrid = 64;
 
 // A sliced plan (slice_kernel): one launch over the whole GPU, each thread
 // carrying its 16-byte group of every buffer through every step.
@@ -958,12 +963,15 @@ vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanPar
                           const LaunchCtx& tc) {
   const int64_t g = prm.groups, per_block = kSliceBlock;
   int U = 1;
-  while (U < 8 && g > int64_t(kSliceMaxBlocks) * per_block * U) U *= 2;
+  if (g > int64_t(kSliceSmallGrid) * per_block) {
+    U = 2;
+    while (U < 8 && g > int64_t(2) * st->nsm * per_block * U) U *= 2;
+  }
   const SliceKernel kernel = U == 1 ? slice_kernel_for<1, kSliceBlock>(dp.rmode, dp.red)
                            : U == 2 ? slice_kernel_for<2, kSliceBlock>(dp.rmode, dp.red)
                            : U == 4 ? slice_kernel_for<4, kSliceBlock>(dp.rmode, dp.red)
                                     : slice_kernel_for<8, kSliceBlock>(dp.rmode, dp.red);
-  const size_t smem = dp.words * 16 + prm.nbases * sizeof(void*);
+  const size_t smem = dev::slice_smem_bytes(dp.words, prm.nbases, dp.nops, dp.nrefs);
   int per_sm = 0;
   {
     static std::mutex mu;
@@ -1231,14 +1239,9 @@ vc_status_t run(const Call& c) {
   for (int r = 0; r < N; ++r)
     aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
                (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
-  // RHD applies several operations to each position per halving step (4 in
-  // the first with 8 ranks), which lengthens every thread's chain: measured
-  // slower sliced than in the other forms up to 4 MiB per rank, so it takes
-  // the sliced form only when the limit is SIZE_MAX.
   const size_t slim = slice_limit();
-  const bool slice_algo = pa.algo != Algo::RHD || slim == SIZE_MAX;
-  if (aligned && slim > 0 && slice_algo && c.coll == Coll::AllReduce && plan.steps.size() >= 2 && es == 4 &&
-      static_cast<uint64_t>(c.count * es) <= std::min<uint64_t>(slim, INT64_MAX)) {
+  if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 && es == 4 &&
+      c.count < (int64_t(1) << 29) && static_cast<uint64_t>(c.count * es) <= std::min<uint64_t>(slim, INT64_MAX)) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;
     else dp = nullptr;

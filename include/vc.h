@@ -418,13 +418,11 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * are unchanged, so results are identical bit for bit; different positions
  * merely run out of step with each other, as when a ring is pipelined in
  * slices.  The conditions of single-launch execution on alignment and the
- * resident description apply as well.  RHD applies several operations to a
- * position in each halving step, and measured slower in this form than in
- * the others; it takes the sliced form only when the limit is SIZE_MAX.
- * max_bytes_per_rank: 0 disables it, SIZE_MAX applies it to every eligible
- * call.  Default VC_SLICE_LIMIT_DEFAULT: up to 16 MiB per rank the form
- * measured faster than per-step launches (8 ranks, fp32, GB300; above, the
- * whole GPU's bandwidth per step wins).  Process-wide.
+ * resident description apply as well.  max_bytes_per_rank: 0 disables it,
+ * SIZE_MAX applies it to every eligible call.  Default
+ * VC_SLICE_LIMIT_DEFAULT: up to 16 MiB per rank the form measured faster
+ * than the cluster form and than per-step launches (8 ranks, fp32, GB300;
+ * above, the whole GPU's bandwidth per step wins).  Process-wide.
  */
 #define VC_SLICE_LIMIT_DEFAULT ((size_t)16 << 20)
 vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank);

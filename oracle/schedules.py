@@ -779,8 +779,7 @@ def alltoall(inputs, algo: str, dtype: str) -> Result:
 def _alltoall_pairwise(inputs, dtype, B):
     """Pairwise exchange ([Latency-formula page] eq. model-algo-a2a-pairwise):
     in round k = 1 .. N-1 rank i sends its block for rank (i + k) mod N there
-    (and so receives from (i - k) mod N).  The N-1 rounds are steps 0 .. N-2;
-    the local block is no message and is copied with the first round."""
+    (and so receives from (i - k) mod N).  Round 0 is the local block."""
     N = len(inputs)
     bm = _Bytes(dtype)
     log = TransferLog()
@@ -797,8 +796,8 @@ def _alltoall_pairwise(inputs, dtype, B):
                              deliver=_store_into(out[j], i * B, (i + 1) * B), phase="round",
                              src_off=j * B, dst_off=i * B))
             bm.rw(B, bm.e_in, bm.e_out)
-        _run_step(log, k - 1, msgs)
-    return Result(out, log, bm.total)
+        _run_step(log, k, msgs)
+    return Result(out, log, bm.total, local_steps=1 if N > 1 else 0)
 
 
 def _alltoall_ring(inputs, dtype, B):
@@ -809,8 +808,7 @@ def _alltoall_ring(inputs, dtype, B):
     from rank s for rank d travels (d - s) mod N hops.  Round 0 is the local
     block.  Round k carries N-k blocks per rank, so a rank sends
     (N-1)/2 * M in all, not the (N-1)/N * M the page's formula charges (it
-    writes Pairwise's bandwidth term for the ring as well).  The rounds are
-    steps 0 .. N-2; the local block is copied with the first."""
+    writes Pairwise's bandwidth term for the ring as well)."""
     N = len(inputs)
     bm = _Bytes(dtype)
     log = TransferLog()
@@ -837,9 +835,9 @@ def _alltoall_ring(inputs, dtype, B):
             msgs.append(_Msg(src=i, dst=dst, n=len(keys) * B, reduce=False, esize=bm.e_in,
                              payload=payload, deliver=deliver, phase="ring", chunks=tuple(keys)))
             bm.rw(len(keys) * B, bm.e_in, bm.e_out)
-        _run_step(log, k - 1, msgs)
+        _run_step(log, k, msgs)
         transit = nxt
-    return Result(out, log, bm.total)
+    return Result(out, log, bm.total, local_steps=1 if N > 1 else 0)
 
 
 def _alltoall_bruck(inputs, dtype, B):

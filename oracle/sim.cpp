@@ -1117,8 +1117,7 @@ void alltoall(Sim& sm, const In& in, int64_t total, const std::string& algo, Out
   if (algo == "pairwise") {
     // [Latency-formula page] eq. model-algo-a2a-pairwise: in round k = 1 ..
     // N-1 rank i sends its block for rank (i + k) mod N there (reading: and so
-    // receives from (i - k) mod N).  The rounds are steps 0 .. N-2; the local
-    // block is no message and is copied with the first.
+    // receives from (i - k) mod N).  Round 0 is the local block.
     std::vector<Buf> src, out;
     for (int i = 0; i < N; ++i) {
       src.push_back(byte_copy(in[i], total, es));
@@ -1135,8 +1134,9 @@ void alltoall(Sim& sm, const In& in, int64_t total, const std::string& algo, Out
         ms.push_back(std::move(m));
         sm.rw(B, {sm.e_in, sm.e_out});
       }
-      sm.run_step(k - 1, ms);
+      sm.run_step(k, ms);
     }
+    sm.local_steps = N > 1 ? 1 : 0;
     for (Buf& b : out) o.outputs.push_back(std::move(b.b));
     return;
   }
@@ -1145,7 +1145,6 @@ void alltoall(Sim& sm, const In& in, int64_t total, const std::string& algo, Out
     // neighbours.  Reading: store and forward -- in round k every rank passes
     // to i + 1 every block it holds that is not addressed to itself, nearest
     // destination first; a block from s for d travels (d - s) mod N hops.
-    // The rounds are steps 0 .. N-2; the local block is copied with the first.
     std::vector<Buf> out;
     for (int i = 0; i < N; ++i) {
       out.push_back(byte_buf(total, es));
@@ -1192,10 +1191,11 @@ void alltoall(Sim& sm, const In& in, int64_t total, const std::string& algo, Out
         ms.push_back(std::move(m));
         sm.rw(static_cast<int64_t>(keys.size()) * B, {sm.e_in, sm.e_out});
       }
-      sm.run_step(k - 1, ms);
+      sm.run_step(k, ms);
       std::swap(tr, nx);
       held = next;
     }
+    sm.local_steps = N > 1 ? 1 : 0;
     for (Buf& b : out) o.outputs.push_back(std::move(b.b));
     return;
   }

@@ -3,8 +3,8 @@
 In the sliced form (vc_set_slice_limit) one launch over the whole GPU runs
 every step of the plan, each thread carrying its 16-byte group of every rank
 buffer through the steps in order.  Forced on for every eligible call here:
-Ring, RHD (any rank count, with the fold-in; sliced only when forced), DBT,
-Mesh and the per-hop ring on fp32 and int32 with every op, ragged counts whose last group is partial,
+Ring, RHD (any rank count, with the fold-in), DBT, Mesh and the per-hop ring
+on fp32 and int32 with every op, ragged counts whose last group is partial,
 sizes from one element to 64 MiB per rank, in place.  Every result must equal
 the C++ oracle's simulation of the same schedule bit for bit, and the launch
 trace must show one sliced launch for the call.  Also: calls that do not
@@ -133,8 +133,7 @@ def test_calls_that_do_not_qualify_take_other_forms():
 
 
 def test_default_limit():
-    """Ring, DBT and Mesh take the sliced form up to the default limit; RHD
-    only when the limit is SIZE_MAX."""
+    """Every eligible schedule takes the sliced form up to the default limit."""
     vc.vc_set_slice_limit(vc.VC_SLICE_DEFAULT)
     assert vc.vc_get_slice_limit() == vc.VC_SLICE_DEFAULT
     N = 8
@@ -145,7 +144,7 @@ def test_default_limit():
         s = torch.stack(x).sum(0)
         for algo in ("ring", "dbt", "mesh", "rhd"):
             recs = _traced(lambda: vc.vc_allreduce(x, y, algo=algo))
-            want = sliced and algo != "rhd"
+            want = sliced
             assert any(r["kernel"].endswith("_sliced") for r in recs) == want, (algo, nbytes, recs)
             assert torch.allclose(y[0], s, atol=1e-5), (algo, nbytes)
         del x, y

@@ -111,7 +111,7 @@ def test_ring_alltoall_traffic_contradicts_the_printed_formula():
     res = schedules.alltoall(rank_buffers("uniform_f32", 5, N, N * B), "ring", "f32")
     assert res.nsteps == N - 1
     per = res.log.max_message_bytes_per_step()
-    assert [per[k - 1] for k in range(1, N)] == [(N - k) * B * 4 for k in range(1, N)]  # round k is step k-1
+    assert [per[k] for k in range(1, N)] == [(N - k) * B * 4 for k in range(1, N)]
     assert res.log.bandwidth_bytes() == (N - 1) * M // 2
     assert res.log.bandwidth_bytes() != (N - 1) * M // N
     for t in res.log.records:
