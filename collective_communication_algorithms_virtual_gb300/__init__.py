@@ -35,6 +35,8 @@ from .binding import (  # noqa: F401
     vc_copy_selftest,
     SINGLE_LAUNCH_ALWAYS,
     vc_set_slice_limit,
+    vc_set_merge_steps,
+    vc_get_merge_steps,
     vc_get_slice_limit,
     SLICE_ALWAYS,
     VC_SLICE_DEFAULT,

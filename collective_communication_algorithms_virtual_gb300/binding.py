@@ -116,6 +116,10 @@ def lib() -> ctypes.CDLL:
         L.vc_set_single_launch.restype = I
         L.vc_get_single_launch.argtypes = [ctypes.POINTER(Z)]
         L.vc_get_single_launch.restype = I
+        L.vc_set_merge_steps.argtypes = [I]
+        L.vc_set_merge_steps.restype = I
+        L.vc_get_merge_steps.argtypes = [ctypes.POINTER(I)]
+        L.vc_get_merge_steps.restype = I
         L.vc_set_slice_limit.argtypes = [Z]
         L.vc_set_slice_limit.restype = I
         L.vc_get_slice_limit.argtypes = [ctypes.POINTER(Z)]
@@ -331,6 +335,18 @@ def vc_get_slice_limit() -> int:
     v = ctypes.c_size_t(0)
     check(lib().vc_get_slice_limit(ctypes.byref(v)))
     return v.value
+
+
+def vc_set_merge_steps(on: bool) -> None:
+    """Run consecutive steps that depend on nothing among themselves as one
+    launch (default on).  Clears the plan cache."""
+    check(lib().vc_set_merge_steps(int(bool(on))))
+
+
+def vc_get_merge_steps() -> bool:
+    v = ctypes.c_int(0)
+    check(lib().vc_get_merge_steps(ctypes.byref(v)))
+    return bool(v.value)
 
 
 SLICE_ALWAYS = (1 << 64) - 1

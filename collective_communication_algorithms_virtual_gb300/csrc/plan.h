@@ -56,6 +56,10 @@ struct Step {
 struct Plan {
   std::vector<Step> steps;
   int64_t scratch_bytes = 0;
+  // Execution only (set by the library, not by build_plan): launch_end[s] >
+  // s + 1 when steps s .. launch_end[s]-1 depend on nothing among themselves
+  // and share one launch; empty when every step is its own launch.
+  std::vector<uint32_t> launch_end;
 };
 
 struct PlanArgs {

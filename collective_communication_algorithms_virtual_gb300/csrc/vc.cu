@@ -675,6 +675,68 @@ void order_for_reuse(Plan* plan) {
   }
 }
 
+// Steps that share a launch.  The stream order between launches is the step
+// barrier, and a barrier is needed only where a step reads what an earlier
+// one wrote or writes what an earlier one read or wrote.  A run of
+// consecutive steps of one kernel mode in which no step does either with
+// respect to the earlier steps of the run (Pairwise AllToAll's rounds: each
+// reads only the send buffers and writes its own output blocks) runs as one
+// launch: its steps' operations in step order, so each block still takes the
+// rounds in order, without a barrier between them.  Every operation's
+// operands and bytes are unchanged.
+std::atomic<int> g_merge_steps{1};
+void mark_independent_steps(Plan* plan) {
+  plan->launch_end.clear();
+  if (!g_merge_steps.load(std::memory_order_relaxed)) return;
+  struct Span {
+    Buf buf;
+    int owner;
+    int64_t lo, hi;
+  };
+  auto span = [](const Operand& o, const Op& op, int64_t stride) {
+    const int64_t last = o.byte_off + (op.nb - 1) * stride;
+    return Span{o.buf, o.buf == Buf::Scratch ? -1 : o.owner, std::min(o.byte_off, last),
+                std::max(o.byte_off, last) + op.n * esize(o.dt)};
+  };
+  auto hit = [](const std::vector<Span>& a, const Span& b) {
+    for (const Span& x : a)
+      if (x.buf == b.buf && x.owner == b.owner && x.lo < b.hi && b.lo < x.hi) return true;
+    return false;
+  };
+  const size_t n = plan->steps.size();
+  std::vector<uint32_t> end(n, 0);
+  bool any = false;
+  for (size_t s = 0; s < n;) {
+    std::vector<Span> reads, writes;
+    auto add = [&](const Step& st) {
+      for (const Op& op : st.ops) {
+        for (const Operand& o : op.src) reads.push_back(span(o, op, op.sstride));
+        for (const Operand& o : op.dst) writes.push_back(span(o, op, op.dstride));
+      }
+    };
+    add(plan->steps[s]);
+    size_t e = s + 1;
+    for (; e < n; ++e) {
+      const Step& st = plan->steps[e];
+      if (st.mode != plan->steps[s].mode || st.red != plan->steps[s].red) break;
+      bool dep = false;
+      for (const Op& op : st.ops) {
+        for (const Operand& o : op.src) dep = dep || hit(writes, span(o, op, op.sstride));
+        for (const Operand& o : op.dst) {
+          const Span w = span(o, op, op.dstride);
+          dep = dep || hit(writes, w) || hit(reads, w);
+        }
+      }
+      if (dep) break;
+      add(st);
+    }
+    any = any || e > s + 1;
+    for (size_t k = s; k < e; ++k) end[k] = static_cast<uint32_t>(e);
+    s = e;
+  }
+  if (any) plan->launch_end = std::move(end);
+}
+
 PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std::string* why) {
   const PlanKey key = plan_key(pa);
   {
@@ -689,6 +751,7 @@ PlanStatus cached_plan(const PlanArgs& pa, std::shared_ptr<const Plan>* out, std
   const PlanStatus ps = build_plan(pa, plan.get(), why);
   if (ps != PlanStatus::Ok) return ps;
   order_for_reuse(plan.get());
+  mark_independent_steps(plan.get());
   std::lock_guard<std::mutex> lk(g_plan_mu);
   if (g_plans.size() >= 256) g_plans.clear();
   g_plans.emplace(key, plan);
@@ -1256,10 +1319,19 @@ vc_status_t run(const Call& c) {
     rc = launch_plan(*dp, dev, N, sends, recvs, scratch, c.stream, tc, st, slice_groups);
     if (rc == VC_SUCCESS) launches = 1;
   } else {
-    for (size_t si = 0; si < plan.steps.size(); ++si) {
+    for (size_t si = 0; si < plan.steps.size();) {
       tc.step = static_cast<int>(si);
-      rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
+      const size_t se = plan.launch_end.empty() ? si + 1 : plan.launch_end[si];
+      if (se == si + 1) {
+        rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
+      } else {  // independent steps: one launch, their operations in step order
+        Step merged = plan.steps[si];
+        for (size_t k = si + 1; k < se; ++k)
+          merged.ops.insert(merged.ops.end(), plan.steps[k].ops.begin(), plan.steps[k].ops.end());
+        rc = launch_step(st, merged, b, c.stream, &launches, tc);
+      }
       if (rc != VC_SUCCESS) break;
+      si = se;
     }
   }
   if (scratch) {
@@ -1848,6 +1920,19 @@ VC_EXPORT vc_status_t vc_get_single_launch(size_t* max_step_bytes) {
   if (!max_step_bytes) return fail(VC_ERR_INVALID_ARG, "null output pointer");
   std::lock_guard<std::mutex> lk(g_sl_mu);
   *max_step_bytes = g_sl_limit;
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_set_merge_steps(int on) {
+  g_merge_steps.store(on ? 1 : 0, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_plan_mu);  // cached plans carry the grouping they were built with
+  g_plans.clear();
+  return VC_SUCCESS;
+}
+
+VC_EXPORT vc_status_t vc_get_merge_steps(int* on) {
+  if (!on) return fail(VC_ERR_INVALID_ARG, "null output pointer");
+  *on = g_merge_steps.load(std::memory_order_relaxed);
   return VC_SUCCESS;
 }
 

@@ -424,6 +424,23 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * than the cluster form and than per-step launches (8 ranks, fp32, GB300;
  * above, the whole GPU's bandwidth per step wins).  Process-wide.
  */
+/*
+ * Independent steps in one launch.
+ *
+ * With one launch per step, stream order is the barrier between steps; a
+ * barrier is needed only where a step reads what an earlier one wrote, or
+ * writes what an earlier one read or wrote.  When `on` (the default), a run of
+ * consecutive steps of one kind in which no step does either with respect to
+ * the earlier steps of the run -- Pairwise AllToAll's rounds, each reading
+ * only the send buffers and writing its own output blocks, and the Ring
+ * AllToAll's local copy with its first round -- runs as one launch, the steps'
+ * operations in step order (each block takes them in that order), without a
+ * barrier between them.  Every operation, operand and byte is unchanged;
+ * vc_plan_describe still reports the schedule's steps.  Process-wide.
+ */
+vc_status_t vc_set_merge_steps(int on);
+vc_status_t vc_get_merge_steps(int* on);
+
 #define VC_SLICE_LIMIT_DEFAULT ((size_t)16 << 20)
 vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank);
 vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank);

@@ -38,6 +38,16 @@ int main(void) {
   if (vc_get_reuse_order(&v) != VC_SUCCESS || v != VC_REUSE_ORDER_DEFAULT) return 13;
   if (vc_set_reuse_order(0) != VC_SUCCESS || vc_get_reuse_order(&v) != VC_SUCCESS || v != 0) return 14;
   vc_set_reuse_order(VC_REUSE_ORDER_DEFAULT);
+  if (vc_get_slice_limit(&v) != VC_SUCCESS || v != VC_SLICE_LIMIT_DEFAULT) return 15;
+  if (vc_set_slice_limit(0) != VC_SUCCESS || vc_get_slice_limit(&v) != VC_SUCCESS || v != 0) return 16;
+  vc_set_slice_limit(VC_SLICE_LIMIT_DEFAULT);
+  {
+    int m = 0;
+    if (vc_get_merge_steps(&m) != VC_SUCCESS || m != 1) return 17;
+    if (vc_set_merge_steps(0) != VC_SUCCESS || vc_get_merge_steps(&m) != VC_SUCCESS || m != 0) return 18;
+    vc_set_merge_steps(1);
+    if (vc_get_merge_steps(NULL) != VC_ERR_INVALID_ARG) return 19;
+  }
   printf("ok %d\n", vc_version());
   return 0;
 }
