@@ -748,6 +748,34 @@ def other_configs(vc, dev, peaks):
         del sc
         torch.cuda.empty_cache()
     res["bcast_scatter_int32_1GiB"] = r
+    res["pipelined_broadcast_chunks_n8_1GiB"] = chunk_sweep(vc, src, stream)
+    return res
+
+
+def chunk_sweep(vc, src, stream, N: int = 8):
+    """The pipelined Broadcasts' chunk count k measured: every k from 1 to 256
+    (powers of 2) next to the k the cost model picks, k* = sqrt(h M / (alpha
+    beta)) with h = N-2 (chain) or ceil(log2 N)-1 (tree) -- the
+    Bcast/Scatter page's eqs. pipe-chain-bcast and pipe-tree-bcast optimised
+    in k (the page prints N-1 for the chain; the derivative gives N-2)."""
+    import math
+    import torch
+
+    M = src.numel() * 4
+    alpha, beta = vc.vc_get_cost_model()[1:]
+    outs = [torch.empty_like(src) for _ in range(N)]
+    res = {"bytes": M, "cost_model": {"alpha_s": alpha, "beta_bytes_per_s": beta}}
+    for algo, h in (("pipe_chain", N - 2), ("pipe_tree", math.ceil(math.log2(N)) - 1)):
+        ks = [1 << i for i in range(9)]
+        ms = [time_calls(lambda k=k: vc.vc_broadcast_pipelined(src, outs, root=0, algo=algo, nchunks=k), stream,
+                         min_ms=30.0) for k in ks]
+        model_k = min(256, max(1, round(math.sqrt(h * M / (alpha * beta)))))
+        model_ms = time_calls(lambda: vc.vc_broadcast_pipelined(src, outs, root=0, algo=algo, nchunks=0), stream,
+                              min_ms=30.0)
+        best = min(range(len(ks)), key=lambda i: ms[i])
+        res[algo] = {"k": ks, "ms": ms, "measured_best_k": ks[best], "measured_best_ms": ms[best],
+                     "model_k": model_k, "model_ms": model_ms}
+    del outs
     return res
 
 

@@ -92,13 +92,20 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
       // operations (small chunks); searching first and applying after keeps
       // the warp together, so their loads go out at once instead of one
       // operation's chain after another.
+      // The step's operations are listed by position (ascending first
+      // element), so none after one that starts past this thread's groups
+      // can cover them.
       uint32_t k = st.op0;
       const uint32_t kend = st.op0 + st.nops;
       for (;;) {
         int2 r = make_int2(0, 0);
         for (; k < kend; ++k) {
           r = rng[k];
-          if (ea < r.y && eb > r.x) break;  // covers one of the groups
+          if (r.x >= eb) {
+            k = kend;
+            break;
+          }
+          if (ea < r.y) break;  // covers one of the groups
         }
         if (k >= kend) break;
         const OpDesc& o = ops[k++];

@@ -900,7 +900,18 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
     steps[si].nops = static_cast<uint32_t>(s.ops.size());
     steps[si].mode = static_cast<uint32_t>(s.mode == Mode::Copy ? dev::kCopy : dp->rmode);
     int64_t step_bytes = 0;
-    for (const Op& op : s.ops) {
+    // A step's operations are independent: they are listed here by the byte
+    // offset of their first destination, so that a sliced thread can stop
+    // looking once an operation starts past its groups.
+    std::vector<size_t> by_pos(s.ops.size());
+    for (size_t k = 0; k < by_pos.size(); ++k) by_pos[k] = k;
+    std::stable_sort(by_pos.begin(), by_pos.end(), [&](size_t x, size_t y) {
+      const int64_t ox = s.ops[x].dst.empty() ? 0 : s.ops[x].dst[0].byte_off;
+      const int64_t oy = s.ops[y].dst.empty() ? 0 : s.ops[y].dst[0].byte_off;
+      return ox < oy;
+    });
+    for (size_t k : by_pos) {
+      const Op& op = s.ops[k];
       bool aligned = true;
       dev::OpDesc& d = ops[oi++];
       d.p0 = static_cast<uint16_t>(ri);
