@@ -268,3 +268,18 @@ def test_plan_bytes_equal_oracle_algorithmic_bytes(dtype):
             for algo in schedules.ALGOS["scatter"]:
                 assert plan_bytes("scatter", algo, N, rc, root) == \
                     schedules.scatter(xr[0], N, root, algo, dtype).hbm_bytes
+
+
+def test_step_merging_keeps_the_described_steps():
+    """vc_set_merge_steps changes how independent steps are launched, never
+    the steps vc_plan_describe reports: Pairwise AllToAll keeps its local
+    round and N-1 rounds either way."""
+    old = vc.vc_get_merge_steps()
+    try:
+        for on in (True, False):
+            vc.vc_set_merge_steps(on)
+            assert vc.vc_get_merge_steps() == on
+            for N in (2, 5, 8):
+                assert vc.vc_plan_describe("alltoall", "pairwise", N, 64, "bf16")[2] == N
+    finally:
+        vc.vc_set_merge_steps(old)
