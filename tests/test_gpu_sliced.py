@@ -148,3 +148,34 @@ def test_default_limit():
             assert any(r["kernel"].endswith("_sliced") for r in recs) == want, (algo, nbytes, recs)
             assert torch.allclose(y[0], s, atol=1e-5), (algo, nbytes)
         del x, y
+
+
+def test_sliced_inside_a_cuda_graph():
+    """A shape seen before capture runs sliced inside the graph; a shape first
+    seen under capture takes the per-step path (its description is uploaded
+    only outside a capture).  Both replay exactly, twice, on new data."""
+    vc.vc_set_slice_limit(vc.VC_SLICE_DEFAULT)
+    N, count = 8, 65536 + 12
+    sends = [torch.empty(count, device="cuda") for _ in range(N)]
+    recvs = [torch.empty(count, device="cuda") for _ in range(N)]
+    fresh = [torch.empty(count + 16, device="cuda") for _ in range(N)]
+    fresh_out = [torch.empty(count + 16, device="cuda") for _ in range(N)]
+    recs = _traced(lambda: vc.vc_allreduce(sends, recvs, algo="ring"))  # resident before capture
+    assert recs[0]["kernel"].endswith("_sliced"), recs
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        vc.vc_allreduce(sends, recvs, algo="ring")
+        vc.vc_allreduce(fresh, fresh_out, algo="dbt")
+    for seed in (1, 2):
+        xs = _inputs("f32", 8500 + seed, N, count)
+        ys = _inputs("f32", 8600 + seed, N, count + 16)
+        for r in range(N):
+            sends[r].copy_(to_dev(xs[r]))
+            fresh[r].copy_(to_dev(ys[r]))
+        g.replay()
+        torch.cuda.synchronize()
+        want = cxx.allreduce(xs, "ring", "f32", want_log=False).outputs
+        want2 = cxx.allreduce(ys, "dbt", "f32", want_log=False).outputs
+        for r in range(N):
+            assert same_bits(to_host(recvs[r]), want[r]), (seed, r)
+            assert same_bits(to_host(fresh_out[r]), want2[r]), (seed, r)
