@@ -14,9 +14,9 @@ namespace dev {
 // each destination, at the same byte offset in every rank buffer (the fp32 /
 // int32 AllReduce schedules: Ring, RHD, DBT, Mesh), can run with its step
 // barrier kept per element instead of per launch.  The buffers are cut into
-// slices of kThreads 16-byte groups; thread i of a block owns group i of its
-// slice -- the same bytes of every rank's send and receive buffer -- for the
-// whole launch.  The thread walks the plan's steps in order and, in each,
+// slices of U * BT 16-byte groups; thread i of a block owns groups i, i + BT,
+// ... of its slice -- the same bytes of every rank's send and receive buffer
+// -- for the whole launch.  The thread walks the plan's steps in order and, in each,
 // applies every operation that covers its group: sources combined in the
 // plan's order, the result stored to every destination.  Whatever a step
 // reads at a position was written there by an earlier step, by this same
