@@ -56,7 +56,8 @@ class PlanEntry(ctypes.Structure):
     _fields_ = [("step", ctypes.c_int32), ("op", ctypes.c_int32), ("role", ctypes.c_int32),
                 ("pos", ctypes.c_int32), ("buf", ctypes.c_int32), ("owner", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("reduce", ctypes.c_int32), ("byte_off", ctypes.c_int64),
-                ("n", ctypes.c_int64), ("nb", ctypes.c_int64), ("stride_bytes", ctypes.c_int64)]
+                ("n", ctypes.c_int64), ("nb", ctypes.c_int64), ("stride_bytes", ctypes.c_int64),
+                ("elem0", ctypes.c_int64)]
 
 
 _lib = None

@@ -42,6 +42,10 @@ int heap_depth(int i) {
   return d;
 }
 int lowbit(int v) { return v & -v; }
+
+// 16-bit Ring AllReduce: while its fp32 partial sums take at most this many
+// bytes per rank, they keep one place per element (see allreduce_ring).
+constexpr int64_t kFlatPartialBytes = int64_t(16) << 20;
 int md(int a, int n) { return ((a % n) + n) % n; }
 bool is_pow2(int n) { return n >= 1 && (n & (n - 1)) == 0; }
 
@@ -118,21 +122,23 @@ class Builder {
     plan_.steps.push_back(std::move(st));
     return plan_.steps.size() - 1;
   }
-  void add(size_t st, std::vector<Operand> src, std::vector<Operand> dst, int64_t n) {
+  // pos0: the operation's first element position (AllReduce schedules), or -1.
+  void add(size_t st, std::vector<Operand> src, std::vector<Operand> dst, int64_t n, int64_t pos0 = -1) {
     if (n <= 0) return;
     Op op;
     op.src = std::move(src);
     op.dst = std::move(dst);
     op.n = n;
+    op.pos0 = pos0;
     plan_.steps[st].ops.push_back(std::move(op));
   }
-  void copy(size_t st, Operand src, Operand dst, int64_t n) { add(st, {src}, {dst}, n); }
+  void copy(size_t st, Operand src, Operand dst, int64_t n, int64_t pos0 = -1) { add(st, {src}, {dst}, n, pos0); }
 
   // ---- AllReduce ------------------------------------------------------------
   void allreduce() {
     if (a_.count == 0) return;
     if (N_ == 1) {
-      if (!a_.inplace) copy(new_step(Mode::Copy), S(0, 0), R(0, 0), a_.count);
+      if (!a_.inplace) copy(new_step(Mode::Copy), S(0, 0), R(0, 0), a_.count, 0);
       return;
     }
     switch (a_.algo) {
@@ -161,11 +167,11 @@ class Builder {
     for (int i = 0; i < N_; ++i) {
       if (i == root) continue;
       const bool last = t == N_ - 2;
-      add(new_step(reduce_mode()), {t == 0 ? S(root, 0) : acc(), S(i, 0)}, {last ? R(root, 0) : acc()}, count);
+      add(new_step(reduce_mode()), {t == 0 ? S(root, 0) : acc(), S(i, 0)}, {last ? R(root, 0) : acc()}, count, 0);
       ++t;
     }
     for (int i = 0; i < N_; ++i)
-      if (i != root) copy(new_step(Mode::Copy), R(root, 0), R(i, 0), count);
+      if (i != root) copy(new_step(Mode::Copy), R(root, 0), R(i, 0), count, 0);
   }
 
   // One pass: every output element is ((x0 + x1) + x2) + ... in rank order,
@@ -175,7 +181,7 @@ class Builder {
     std::vector<Operand> src, dst;
     for (int q = 0; q < N_; ++q) src.push_back(S(q, 0));
     for (int r = 0; r < N_; ++r) dst.push_back(R(r, 0));
-    add(st, src, dst, a_.count);
+    add(st, src, dst, a_.count, 0);
   }
 
   // ReduceScatter step s: rank r adds chunk (r-s-1) mod N, sent by rank r-1,
@@ -183,35 +189,42 @@ class Builder {
   // rank r-1, i.e. every rank forwards the chunk it obtained the step before.
   // (The article prints the AllGather indices as r+s+1 / r+s; those agree with
   // the forwarding only at s = 0 and would leave chunk r-1 undelivered.)
-  // Partial sums live in the receive buffers, or for bf16 in two fp32 chunk
-  // slots per rank used alternately (step s writes slot s%2 while rank r+1
-  // reads rank r's slot (s-1)%2).  The last ReduceScatter step writes the
-  // final (rounded) chunk into the receive buffer.
+  // Partial sums live in the receive buffers, or for bf16 in fp32 scratch:
+  // up to kFlatPartialBytes of partials per rank one fp32 buffer per rank,
+  // element e of chunk c at position e (every scratch byte then belongs to
+  // one element of the buffers, which the sliced form needs); above that, two
+  // fp32 chunk slots per rank used alternately (step s writes slot s%2 while
+  // rank r+1 reads rank r's slot (s-1)%2), a quarter of the memory at 8
+  // ranks.  The last ReduceScatter step writes the final (rounded) chunk into
+  // the receive buffer.
   // RingHop: the same schedule with the partial sums kept in the data type,
   // rounded on every hop (no scratch); for fp32 / int32 it is the ring.
   void allreduce_ring() {
     const Chunks ch(a_.count, N_, es_);
     const bool wide = bf16() && a_.algo != Algo::RingHop;  // fp32 partials in scratch
+    const bool flat = wide && a_.count * 4 <= kFlatPartialBytes;
     std::vector<int64_t> slot0(N_, 0);
     if (wide)
-      for (int r = 0; r < N_; ++r) slot0[r] = alloc(2 * ch.ce * 4);
-    auto part = [&](int r, int s) { return Sc(r, slot0[r] + (s & 1) * ch.ce * 4, DT::F32); };
+      for (int r = 0; r < N_; ++r) slot0[r] = alloc(flat ? a_.count * 4 : 2 * ch.ce * 4);
+    auto part = [&](int r, int s, int64_t lo) {
+      return Sc(r, flat ? slot0[r] + lo * 4 : slot0[r] + (s & 1) * ch.ce * 4, DT::F32);
+    };
     for (int s = 0; s < N_ - 1; ++s) {
       const size_t st = new_step(reduce_mode());
       for (int r = 0; r < N_; ++r) {
         const int c = md(r - s - 1, N_), left = md(r - 1, N_);
         const int64_t lo = ch.lo(c);
         const Operand own = S(r, lo);
-        const Operand in = s == 0 ? S(left, lo) : (wide ? part(left, s - 1) : R(left, lo));
-        const Operand out = s == N_ - 2 ? R(r, lo) : (wide ? part(r, s) : R(r, lo));
-        add(st, {own, in}, {out}, ch.len(c));
+        const Operand in = s == 0 ? S(left, lo) : (wide ? part(left, s - 1, lo) : R(left, lo));
+        const Operand out = s == N_ - 2 ? R(r, lo) : (wide ? part(r, s, lo) : R(r, lo));
+        add(st, {own, in}, {out}, ch.len(c), lo);
       }
     }
     for (int s = 0; s < N_ - 1; ++s) {
       const size_t st = new_step(Mode::Copy);
       for (int r = 0; r < N_; ++r) {
         const int c = md(r - s, N_);
-        copy(st, R(md(r - 1, N_), ch.lo(c)), R(r, ch.lo(c)), ch.len(c));
+        copy(st, R(md(r - 1, N_), ch.lo(c)), R(r, ch.lo(c)), ch.len(c), ch.lo(c));
       }
     }
   }
@@ -244,7 +257,7 @@ class Builder {
     if (rr > 0) {
       const size_t st = new_step(reduce_mode());
       for (int i = 0; i < rr; ++i) {
-        add(st, {S(2 * i, 0), S(2 * i + 1, 0)}, {X(2 * i, 0)}, a_.count);
+        add(st, {S(2 * i, 0), S(2 * i + 1, 0)}, {X(2 * i, 0)}, a_.count, 0);
         folded[2 * i] = true;
       }
     }
@@ -262,7 +275,7 @@ class Builder {
         const Operand own = (k == 0 && !folded[rv]) ? S(rv, lo) : X(rv, lo);
         const Operand partner = (k == 0 && !folded[rw]) ? S(rw, lo) : X(rw, lo);
         const Operand out = k == L - 1 ? R(rv, lo) : X(rv, lo);
-        add(st, {own, partner}, {out}, hi - lo);
+        add(st, {own, partner}, {out}, hi - lo, lo);
       }
       seg = next;
     }
@@ -273,14 +286,14 @@ class Builder {
       for (int v = 0; v < P; ++v) {
         const int w = v ^ d;
         const int64_t lo = ch.lo(seg[w].first), hi = ch.hi(seg[w].second - 1);
-        copy(st, R(real[w], lo), R(real[v], lo), hi - lo);
+        copy(st, R(real[w], lo), R(real[v], lo), hi - lo, lo);
         next[v] = {std::min(seg[v].first, seg[w].first), std::max(seg[v].second, seg[w].second)};
       }
       seg = next;
     }
     if (rr > 0) {
       const size_t st = new_step(Mode::Copy);
-      for (int i = 0; i < rr; ++i) copy(st, R(2 * i, 0), R(2 * i + 1, 0), a_.count);
+      for (int i = 0; i < rr; ++i) copy(st, R(2 * i, 0), R(2 * i + 1, 0), a_.count, 0);
     }
   }
 
@@ -318,7 +331,7 @@ class Builder {
             const bool leaf = 2 * c + 1 >= N_;
             src.push_back(leaf ? S(rank_of(tree, c), lo) : X(rank_of(tree, c), lo));
           }
-          add(st, src, {i == 0 ? R(v, lo) : X(v, lo)}, n);
+          add(st, src, {i == 0 ? R(v, lo) : X(v, lo)}, n, lo);
         }
       }
     }
@@ -328,7 +341,7 @@ class Builder {
       for (int tree = 0; tree < 2; ++tree) {
         const int64_t lo = halves.lo(tree), n = halves.len(tree);
         for (int i = 0; i < N_; ++i)
-          if (heap_depth(i) == depth) copy(st, R(rank_of(tree, (i - 1) / 2), lo), R(rank_of(tree, i), lo), n);
+          if (heap_depth(i) == depth) copy(st, R(rank_of(tree, (i - 1) / 2), lo), R(rank_of(tree, i), lo), n, lo);
       }
     }
   }

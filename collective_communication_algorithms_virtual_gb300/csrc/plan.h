@@ -44,6 +44,10 @@ struct Op {
   int64_t dstride = 0;  // bytes between runs, every destination
   bool keep = false;    // execution only: the next step reads the results (keep them in L2)
   uint32_t built = 0;   // introspection: the operation's index in its step as built
+  // Element position of the operation's first element, when every operand
+  // holds position i of the operation at element pos0 + i of the collective's
+  // buffers (the AllReduce schedules set it); -1 otherwise.
+  int64_t pos0 = -1;
 };
 
 struct Step {

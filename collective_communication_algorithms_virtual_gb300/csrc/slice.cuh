@@ -1,7 +1,7 @@
-// Device code of the sliced form (sm_103a): a whole fp32 / int32 AllReduce
-// plan in one launch over the GPU, each thread carrying its 16-byte group of
-// every rank buffer through every step.  Uses the plan description and the
-// helpers of kernels.cuh.
+// Device code of the sliced form (sm_103a): a whole AllReduce plan in one
+// launch over the GPU, each thread carrying its 16-byte group of every rank
+// buffer through every step.  Uses the plan description and the helpers of
+// kernels.cuh.
 #pragma once
 
 #include "kernels.cuh"
@@ -10,23 +10,27 @@ namespace vc {
 namespace dev {
 
 // -- element-sliced plans ---------------------------------------------------------
-// A plan whose every operation maps element e of each source to element e of
-// each destination, at the same byte offset in every rank buffer (the fp32 /
-// int32 AllReduce schedules: Ring, RHD, DBT, Mesh), can run with its step
-// barrier kept per element instead of per launch.  The buffers are cut into
-// slices of U * BT 16-byte groups; thread i of a block owns groups i, i + BT,
-// ... of its slice -- the same bytes of every rank's send and receive buffer
-// -- for the whole launch.  The thread walks the plan's steps in order and, in each,
-// applies every operation that covers its group: sources combined in the
-// plan's order, the result stored to every destination.  Whatever a step
+// A plan whose every operation maps element position e of each source to
+// position e of each destination, each buffer holding position e at one fixed
+// place (the AllReduce schedules: Ring, RHD, DBT, Mesh), can run with its
+// step barrier kept per element instead of per launch.  The buffers are cut
+// into slices of U * BT groups of 16 bytes of the data type (4 fp32 / int32
+// elements, 8 bf16 / fp16 ones); thread i of a block owns groups i, i + BT,
+// ... of its slice -- the same positions of every rank's send and receive
+// buffer, and of the fp32 partial sums that 16-bit plans keep in scratch --
+// for the whole launch.  The thread walks the plan's steps in order and, in
+// each, applies every operation that covers its group: sources combined in
+// the plan's order, the result stored to every destination.  Whatever a step
 // reads at a position was written there by an earlier step, by this same
 // thread, so program order is the step barrier and no thread reads what
 // another wrote (loads go to L2 with .cg; a thread's own earlier store to the
 // address is ordered before them).  Steps, operations, operands and every
 // element's association are the plan's; only positions far apart run out of
-// step with each other, as when a ring is pipelined in slices.  The
-// operation's first element is its operands' common offset / 4; the element
-// after its last group whole is handled by the owner of that group.
+// step with each other, as when a ring is pipelined in slices.  The host
+// lists each operation's element range [e0, e1) after the operand table and
+// checks that every position has one place in each buffer; the positions
+// after an operation's last whole group are handled, one by one, by the
+// owner of that group.
 template <int RMODE, int OP>
 __device__ __forceinline__ uint4 cmb4(uint4 a, uint4 w) {
   if constexpr (RMODE == kF32) {
@@ -43,40 +47,75 @@ __device__ __forceinline__ uint4 cmb4(uint4 a, uint4 w) {
   return a;
 }
 
-// Shared memory of a block: the plan description (16-byte words), the call's
-// buffer bases, then two tables the block derives once: each operation's
-// element range [e0, e1) and each operand's address (base + offset).  Every
+// Shared memory of a block: the plan description (16-byte words, ending with
+// the operations' element ranges), the call's buffer bases, then each
+// operand's address (base + offset), which the block derives once.  Every
 // buffer of a sliced call holds fewer than 2^29 elements (checked on the
 // host), so element and byte offsets within it fit 32 bits.
-__host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t nbases, uint32_t nops,
-                                                      uint32_t nrefs) {
-  return size_t(words) * 16 + size_t(nbases) * 8 + size_t(nops) * 8 + size_t(nrefs) * 8;
+__host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t nbases, uint32_t nrefs) {
+  return size_t(words) * 16 + size_t(nbases) * 8 + size_t(nrefs) * 8;
+}
+
+// The block's copy of the description and the operand addresses.
+struct SliceTables {
+  PlanHeader h;
+  const PlanStep* steps;
+  const OpDesc* ops;
+  const int2* rng;   // per operation: e0, e1
+  char* const* addr;  // per operand: its address
+};
+template <int BT>
+__device__ __forceinline__ SliceTables slice_prologue(const PlanParams& p, uint4* sm) {
+  for (uint32_t i = threadIdx.x; i < p.words; i += BT) sm[i] = ld16(p.plan + i);
+  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
+  for (uint32_t i = threadIdx.x; i < p.nbases; i += BT) sbase[i] = p.base[i];
+  __syncthreads();
+  SliceTables t;
+  t.h = *reinterpret_cast<const PlanHeader*>(sm);
+  t.steps = reinterpret_cast<const PlanStep*>(sm + 1);
+  t.ops = reinterpret_cast<const OpDesc*>(sm + 1 + t.h.nsteps);
+  const OperandRef* refs = reinterpret_cast<const OperandRef*>(t.ops + t.h.nops);
+  t.rng = reinterpret_cast<const int2*>(refs + t.h.nrefs);
+  char** addr = reinterpret_cast<char**>(const_cast<void**>(sbase + p.nbases));
+  for (uint32_t i = threadIdx.x; i < t.h.nrefs; i += BT)
+    addr[i] = static_cast<char*>(const_cast<void*>(sbase[refs[i].base])) + refs[i].off;
+  t.addr = addr;
+  __syncthreads();
+  return t;
+}
+
+// Each thread looks for the next operation of the step that covers one of
+// its groups (elements [ea, eb) span them), then applies it.  Threads of a
+// warp can be in different operations (small chunks); searching first and
+// applying after keeps the warp together, so their loads go out at once
+// instead of one operation's chain after another.
+// The step's operations are listed by position (ascending first element), so
+// none after one that starts past this thread's groups can cover them.
+// Stopping there measured faster where a thread carries 4 or more groups (4
+// MiB per rank fp32: ring 24.5 -> 20.4 us) and slower where it carries 1 or 2
+// (up to 2 MiB: ring 10.7 -> 13.4 us at 4 KiB), so only the former stop
+// early.  Returns the operation's index, or kend.
+template <int U>
+__device__ __forceinline__ uint32_t slice_next_op(const int2* rng, uint32_t k, uint32_t kend, int ea, int eb,
+                                                  int2* r) {
+  for (; k < kend; ++k) {
+    *r = rng[k];
+    if constexpr (U >= 4) {
+      if (r->x >= eb) return kend;
+    }
+    if (ea < r->y && eb > r->x) return k;  // covers one of the groups
+  }
+  return kend;
 }
 
 // BT threads a block; U groups a thread, BT apart (slices of U * BT groups);
 // the loads of a thread's groups in a step are issued together.
 template <int RMODE, int OP, int U, int BT>
 __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanParams p) {
-  static_assert(RMODE == kF32 || RMODE == kI32, "sliced plans are fp32 or int32");
+  static_assert(RMODE == kF32 || RMODE == kI32, "4-byte sliced plans are fp32 or int32");
   extern __shared__ uint4 sm[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (uint32_t i = threadIdx.x; i < p.words; i += BT) sm[i] = ld16(p.plan + i);
-  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
-  for (uint32_t i = threadIdx.x; i < p.nbases; i += BT) sbase[i] = p.base[i];
-  __syncthreads();
-  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
-  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
-  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
-  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
-  int2* rng = reinterpret_cast<int2*>(sbase + p.nbases);             // per operation: e0, e1
-  char** addr = reinterpret_cast<char**>(rng + h.nops);              // per operand: its address
-  for (uint32_t i = threadIdx.x; i < h.nops; i += BT) {
-    const int e0 = static_cast<int>(refs[ops[i].p0].off >> 2);
-    rng[i] = make_int2(e0, e0 + static_cast<int>(ops[i].n));
-  }
-  for (uint32_t i = threadIdx.x; i < h.nrefs; i += BT)
-    addr[i] = static_cast<char*>(const_cast<void*>(sbase[refs[i].base])) + refs[i].off;
-  __syncthreads();
+  const SliceTables t = slice_prologue<BT>(p, sm);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kSlice = U * BT;
   const int groups = static_cast<int>(p.groups);
@@ -85,36 +124,14 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
     const int g0 = sl * kSlice + static_cast<int>(threadIdx.x);  // this thread's groups: g0 + u * BT
     if (g0 >= groups) break;
     const int ea = g0 * 4, eb = (g0 + (U - 1) * BT) * 4 + 4;     // elements its groups span
-    for (uint32_t s = 0; s < h.nsteps; ++s) {
-      const PlanStep st = steps[s];
-      // Each thread looks for the next operation of the step that covers one
-      // of its groups, then applies it.  Threads of a warp can be in different
-      // operations (small chunks); searching first and applying after keeps
-      // the warp together, so their loads go out at once instead of one
-      // operation's chain after another.
-      // The step's operations are listed by position (ascending first
-      // element), so none after one that starts past this thread's groups
-      // can cover them.  Stopping there measured faster where a thread
-      // carries 4 or more groups (4 MiB per rank: ring 24.5 -> 20.4 us) and
-      // slower where it carries 1 or 2 (up to 2 MiB: ring 10.7 -> 13.4 us at
-      // 4 KiB), so only the former stop early.
-      uint32_t k = st.op0;
+    for (uint32_t s = 0; s < t.h.nsteps; ++s) {
+      const PlanStep st = t.steps[s];
       const uint32_t kend = st.op0 + st.nops;
-      for (;;) {
-        int2 r = make_int2(0, 0);
-        for (; k < kend; ++k) {
-          r = rng[k];
-          if constexpr (U >= 4) {
-            if (r.x >= eb) {
-              k = kend;
-              break;
-            }
-          }
-          if (ea < r.y && eb > r.x) break;  // covers one of the groups
-        }
-        if (k >= kend) break;
-        const OpDesc& o = ops[k++];
-        char* const* P = addr + o.p0;  // sources, then destinations
+      int2 r = make_int2(0, 0);
+      for (uint32_t k = slice_next_op<U>(t.rng, st.op0, kend, ea, eb, &r); k < kend;
+           k = slice_next_op<U>(t.rng, k + 1, kend, ea, eb, &r)) {
+        const OpDesc& o = t.ops[k];
+        char* const* P = t.addr + o.p0;  // sources, then destinations
         const int ns = o.ns, nd = o.nd;
         bool whole[U];
         int off[U];  // bytes into every operand
@@ -159,6 +176,135 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
                 else a = cmbi<OP>(a, w);
               }
             for (int d = 0; d < nd; ++d) *reinterpret_cast<uint32_t*>(P[ns + d] + xo) = a;
+          }
+        }
+      }
+    }
+  }
+}
+
+// bf16 / fp16 plans: a group is 8 elements, 16 bytes of a buffer in the data
+// type or 32 of an fp32 partial-sum buffer (smask / dmask bit set).  Every
+// source is widened to fp32 (exact) and combined in the plan's order; a
+// destination in the data type takes the fp32 result rounded to nearest even,
+// once, exactly as the per-step kernels do.  Copies move the data type.
+template <bool F16, int OP, int U, int BT>
+__global__ void __launch_bounds__(BT) slice16_kernel(const __grid_constant__ PlanParams p) {
+  extern __shared__ uint4 sm[];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const SliceTables t = slice_prologue<BT>(p, sm);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kSlice = U * BT;
+  const int groups = static_cast<int>(p.groups);
+  const int nslices = (groups + kSlice - 1) / kSlice;
+  for (int sl = blockIdx.x; sl < nslices; sl += gridDim.x) {
+    const int g0 = sl * kSlice + static_cast<int>(threadIdx.x);  // this thread's groups: g0 + u * BT
+    if (g0 >= groups) break;
+    const int ea = g0 * 8, eb = (g0 + (U - 1) * BT) * 8 + 8;     // elements its groups span
+    for (uint32_t s = 0; s < t.h.nsteps; ++s) {
+      const PlanStep st = t.steps[s];
+      const uint32_t kend = st.op0 + st.nops;
+      int2 r = make_int2(0, 0);
+      for (uint32_t k = slice_next_op<U>(t.rng, st.op0, kend, ea, eb, &r); k < kend;
+           k = slice_next_op<U>(t.rng, k + 1, kend, ea, eb, &r)) {
+        const OpDesc& o = t.ops[k];
+        char* const* P = t.addr + o.p0;  // sources, then destinations
+        const int ns = o.ns, nd = o.nd;
+        bool whole[U];
+        int rel[U];  // elements into every operand
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = (g0 + u * BT) * 8;
+          whole[u] = e >= r.x && e + 8 <= r.y;
+          rel[u] = e - r.x;
+        }
+        if (st.mode == kCopy) {
+          uint4 v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (whole[u]) v[u] = ld16_cg(P[0] + rel[u] * 2);
+          for (int d = 0; d < nd; ++d) {
+            char* dp = P[ns + d];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (whole[u]) st16_wb(dp + rel[u] * 2, v[u]);
+          }
+        } else {
+          float acc[U][8];
+          for (int q = 0; q < ns; ++q) {
+            const char* src = P[q];
+            if ((o.smask >> q) & 1) {
+              uint4 a[U], b[U];
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (whole[u]) {
+                  a[u] = ld16_cg(src + rel[u] * 4);
+                  b[u] = ld16_cg(src + rel[u] * 4 + 16);
+                }
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (whole[u]) {
+                  const float f[8] = {__uint_as_float(a[u].x), __uint_as_float(a[u].y), __uint_as_float(a[u].z),
+                                      __uint_as_float(a[u].w), __uint_as_float(b[u].x), __uint_as_float(b[u].y),
+                                      __uint_as_float(b[u].z), __uint_as_float(b[u].w)};
+                  accumulate8<OP>(acc[u], f, q == 0);
+                }
+            } else {
+              uint4 w[U];
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (whole[u]) w[u] = ld16_cg(src + rel[u] * 2);
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (whole[u]) {
+                  float f[8];
+                  widen8<F16>(w[u], f);
+                  accumulate8<OP>(acc[u], f, q == 0);
+                }
+            }
+          }
+          for (int d = 0; d < nd; ++d) {
+            char* dp = P[ns + d];
+            if ((o.dmask >> d) & 1) {
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (whole[u]) {
+                  st16_wb(dp + rel[u] * 4, make_uint4(__float_as_uint(acc[u][0]), __float_as_uint(acc[u][1]),
+                                                      __float_as_uint(acc[u][2]), __float_as_uint(acc[u][3])));
+                  st16_wb(dp + rel[u] * 4 + 16, make_uint4(__float_as_uint(acc[u][4]), __float_as_uint(acc[u][5]),
+                                                           __float_as_uint(acc[u][6]), __float_as_uint(acc[u][7])));
+                }
+            } else {
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (whole[u])
+                  st16_wb(dp + rel[u] * 2, make_uint4(pack2<F16>(acc[u][0], acc[u][1]), pack2<F16>(acc[u][2], acc[u][3]),
+                                                      pack2<F16>(acc[u][4], acc[u][5]), pack2<F16>(acc[u][6], acc[u][7])));
+            }
+          }
+        }
+        // the operation ends inside a group: its last elements one by one
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = (g0 + u * BT) * 8;
+          if (whole[u] || e < r.x || e >= r.y) continue;
+          for (int x = e; x < r.y; ++x) {
+            const int xr = x - r.x;
+            if (st.mode == kCopy) {
+              const uint16_t v = ld16b<true>(P[0] + xr * 2);
+              for (int d = 0; d < nd; ++d) *reinterpret_cast<uint16_t*>(P[ns + d] + xr * 2) = v;
+              continue;
+            }
+            float a = 0.f;
+            for (int q = 0; q < ns; ++q) {
+              const float v = ((o.smask >> q) & 1) ? __uint_as_float(ld32<true>(P[q] + xr * 4))
+                                                    : widen1<F16>(ld16b<true>(P[q] + xr * 2));
+              a = q == 0 ? v : cmb<OP>(a, v);
+            }
+            for (int d = 0; d < nd; ++d) {
+              if ((o.dmask >> d) & 1) *reinterpret_cast<float*>(P[ns + d] + xr * 4) = a;
+              else *reinterpret_cast<uint16_t*>(P[ns + d] + xr * 2) = narrow1<F16>(a);
+            }
           }
         }
       }

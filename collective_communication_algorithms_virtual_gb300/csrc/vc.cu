@@ -790,6 +790,7 @@ struct DevPlan {
   int nops = 0;
   bool sliced = false;           // every operation keeps element positions: the sliced form applies
   uint32_t nrefs = 0;
+  uint32_t slice_words = 0;      // sliced form: the description with the operations' element ranges
 };
 struct PlanStore {
   std::unordered_map<PlanKey, DevPlan, PlanKeyHash> plans;
@@ -858,6 +859,53 @@ int plan_cluster(PlanStore& ps) {
   return best;
 }
 
+// The sliced form (slice_kernel, slice16_kernel) applies to a plan whose
+// every operation keeps element positions: operation element i is position
+// pos0 + i of the collective's buffers, one run, a copy from one source.
+// Position e lives at byte e * size of a send or receive buffer (of the data
+// type), and at byte origin + 4 e of an fp32 partial-sum region of scratch
+// (16-bit data), where the regions whose bytes overlap share one origin.
+// Then each byte any operation touches belongs to one position, and with
+// groups and operations starting on 16-byte boundaries a thread that owns a
+// group of positions owns every byte of them.  Positions stay below 2^29
+// (checked per call), so the kernels' 32-bit element offsets hold.
+bool sliceable(const Plan& plan, int rmode) {
+  int es;
+  if (rmode == dev::kF32 || rmode == dev::kI32) es = 4;
+  else if (rmode == dev::kBF16 || rmode == dev::kF16) es = 2;
+  else return false;
+  const int64_t gelems = 16 / es;
+  struct Region {
+    int64_t lo, hi, origin;
+  };
+  std::vector<Region> regions;
+  for (const Step& st : plan.steps)
+    for (const Op& op : st.ops) {
+      if (op.pos0 < 0 || op.nb != 1 || op.pos0 % gelems != 0 || op.pos0 + op.n > (int64_t(1) << 29)) return false;
+      if (st.mode == Mode::Copy && op.src.size() != 1) return false;
+      auto fits = [&](const Operand& o) {
+        if (o.buf != Buf::Scratch) return esize(o.dt) == es && o.byte_off == op.pos0 * es;
+        if (es != 2 || o.dt != DT::F32 || st.mode == Mode::Copy) return false;
+        const int64_t origin = o.byte_off - op.pos0 * 4;
+        if (origin % 16 != 0) return false;
+        regions.push_back({o.byte_off, o.byte_off + op.n * 4, origin});
+        return true;
+      };
+      for (const Operand& o : op.src)
+        if (!fits(o)) return false;
+      for (const Operand& o : op.dst)
+        if (!fits(o)) return false;
+    }
+  std::sort(regions.begin(), regions.end(), [](const Region& a, const Region& b) { return a.lo < b.lo; });
+  int64_t reach = INT64_MIN, origin = 0;  // furthest byte of the regions so far, and their origin
+  for (const Region& g : regions) {
+    if (g.lo < reach && g.origin != origin) return false;
+    if (g.lo >= reach) origin = g.origin;
+    reach = std::max(reach, g.hi);
+  }
+  return true;
+}
+
 // Builds the description of `plan` for N ranks tiled for `workers` tile
 // walkers (sub-blocks of the cluster), assuming every buffer base is 16-byte
 // aligned (checked at each call).
@@ -894,23 +942,27 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
     return r;
   };
   size_t oi = 0, ri = 0;
+  std::vector<const Op*> order;  // the operations as listed
+  order.reserve(nops);
   for (size_t si = 0; si < S; ++si) {
     const Step& s = plan.steps[si];
     steps[si].op0 = static_cast<uint32_t>(oi);
     steps[si].nops = static_cast<uint32_t>(s.ops.size());
     steps[si].mode = static_cast<uint32_t>(s.mode == Mode::Copy ? dev::kCopy : dp->rmode);
     int64_t step_bytes = 0;
-    // A step's operations are independent: they are listed here by the byte
-    // offset of their first destination, so that a sliced thread can stop
-    // looking once an operation starts past its groups.
+    // A step's operations are independent: they are listed here by their
+    // first element position (else the byte offset of their first
+    // destination), so that a sliced thread can stop looking once an
+    // operation starts past its groups.
     std::vector<size_t> by_pos(s.ops.size());
     for (size_t k = 0; k < by_pos.size(); ++k) by_pos[k] = k;
-    std::stable_sort(by_pos.begin(), by_pos.end(), [&](size_t x, size_t y) {
-      const int64_t ox = s.ops[x].dst.empty() ? 0 : s.ops[x].dst[0].byte_off;
-      const int64_t oy = s.ops[y].dst.empty() ? 0 : s.ops[y].dst[0].byte_off;
-      return ox < oy;
-    });
+    auto position = [&](const Op& op) {
+      return op.pos0 >= 0 ? op.pos0 : op.dst.empty() ? 0 : op.dst[0].byte_off;
+    };
+    std::stable_sort(by_pos.begin(), by_pos.end(),
+                     [&](size_t x, size_t y) { return position(s.ops[x]) < position(s.ops[y]); });
     for (size_t k : by_pos) {
+      order.push_back(&s.ops[k]);
       const Op& op = s.ops[k];
       bool aligned = true;
       dev::OpDesc& d = ops[oi++];
@@ -937,21 +989,16 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
   dp->nops = static_cast<int>(nops);
   dp->nrefs = static_cast<uint32_t>(nrefs);
   dp->eligible = true;
-  // The sliced form (slice_kernel): fp32 / int32 steps and 4-byte copies
-  // whose operands all sit at one 16-byte aligned offset of a send or receive
-  // buffer, one run each, so that every operation maps element e to element e.
-  dp->sliced = (dp->rmode == dev::kF32 || dp->rmode == dev::kI32) &&
-               dev::slice_smem_bytes(dp->words, 2 * N + 1, static_cast<uint32_t>(nops), static_cast<uint32_t>(nrefs)) <=
-                   static_cast<size_t>(kPlanSmemMax);
-  for (const Step& st : plan.steps)
-    for (const Op& op : st.ops) {
-      if (!dp->sliced) break;
-      const int64_t off = op.dst.empty() ? -1 : op.dst[0].byte_off;
-      bool ok = op.nb == 1 && (off & 15) == 0 && (st.mode != Mode::Copy || op.src.size() == 1);
-      for (const Operand& o : op.src) ok &= o.buf != Buf::Scratch && o.byte_off == off && esize(o.dt) == 4;
-      for (const Operand& o : op.dst) ok &= o.buf != Buf::Scratch && o.byte_off == off && esize(o.dt) == 4;
-      dp->sliced = ok;
-    }
+  dp->sliced = sliceable(plan, dp->rmode) &&
+               dev::slice_smem_bytes(dp->words + static_cast<uint32_t>((nops + 1) / 2), 2 * N + 1,
+                                     static_cast<uint32_t>(nrefs)) <= static_cast<size_t>(kPlanSmemMax);
+  if (dp->sliced) {  // the operations' element ranges [e0, e1), in listed order, after the operand table
+    dp->slice_words = dp->words + static_cast<uint32_t>((nops + 1) / 2);
+    img->resize(dp->slice_words, make_uint4(0, 0, 0, 0));
+    auto* rng = reinterpret_cast<int2*>(img->data() + dp->words);
+    for (size_t k = 0; k < nops; ++k)
+      rng[k] = make_int2(static_cast<int>(order[k]->pos0), static_cast<int>(order[k]->pos0 + order[k]->n));
+  }
 }
 
 // The resident description of a plan shape, uploading it at the first call
@@ -1018,16 +1065,35 @@ SliceKernel slice_kernel_op(RedOp r) {
     default: return dev::slice_kernel<RMODE, dev::kSum, U, BT>;
   }
 }
+template <bool F16, int U, int BT>
+SliceKernel slice16_kernel_op(RedOp r) {
+  switch (r) {
+    case RedOp::Max: return dev::slice16_kernel<F16, dev::kMax, U, BT>;
+    case RedOp::Min: return dev::slice16_kernel<F16, dev::kMin, U, BT>;
+    default: return dev::slice16_kernel<F16, dev::kSum, U, BT>;
+  }
+}
 template <int U, int BT>
 SliceKernel slice_kernel_for(int rmode, RedOp r) {
-  return rmode == dev::kI32 ? slice_kernel_op<dev::kI32, U, BT>(r) : slice_kernel_op<dev::kF32, U, BT>(r);
+  switch (rmode) {
+    case dev::kI32: return slice_kernel_op<dev::kI32, U, BT>(r);
+    case dev::kBF16:
+      if constexpr (U <= 4) return slice16_kernel_op<false, U, BT>(r);
+      return nullptr;
+    case dev::kF16:
+      if constexpr (U <= 4) return slice16_kernel_op<true, U, BT>(r);
+      return nullptr;
+    default: return slice_kernel_op<dev::kF32, U, BT>(r);
+  }
 }
 // The sliced form's launch shape, measured on 8 ranks (ring / DBT / RHD, 256 KiB
 // to 8 MiB per rank): 256-thread blocks; one group a thread while that takes
 // at most 64 blocks, else the fewest groups a thread (2, 4 or 8, whose loads
 // of a step a thread issues together) that take at most two blocks per SM.
 // Grids of more than 64 blocks of one group a thread were up to twice as
-// slow, and 512- or 1024-thread blocks slower at small sizes.
+// slow, and 512- or 1024-thread blocks slower at small sizes.  16-bit plans
+// stop at 4 groups a thread (8 elements each, fp32 sums: 128 registers, two
+// blocks per SM; 8 groups take 240).
 constexpr int kSliceBlock = 256;
 constexpr int kSliceSmallGrid = 64;
 
@@ -1036,16 +1102,18 @@ constexpr int kSliceSmallGrid = 64;
 vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanParams& prm, cudaStream_t stream,
                           const LaunchCtx& tc) {
   const int64_t g = prm.groups, per_block = kSliceBlock;
+  const int umax = (dp.rmode == dev::kBF16 || dp.rmode == dev::kF16) ? 4 : 8;
   int U = 1;
   if (g > int64_t(kSliceSmallGrid) * per_block) {
     U = 2;
-    while (U < 8 && g > int64_t(2) * st->nsm * per_block * U) U *= 2;
+    while (U < umax && g > int64_t(2) * st->nsm * per_block * U) U *= 2;
   }
   const SliceKernel kernel = U == 1 ? slice_kernel_for<1, kSliceBlock>(dp.rmode, dp.red)
                            : U == 2 ? slice_kernel_for<2, kSliceBlock>(dp.rmode, dp.red)
                            : U == 4 ? slice_kernel_for<4, kSliceBlock>(dp.rmode, dp.red)
                                     : slice_kernel_for<8, kSliceBlock>(dp.rmode, dp.red);
-  const size_t smem = dev::slice_smem_bytes(dp.words, prm.nbases, dp.nops, dp.nrefs);
+  if (!kernel) return fail(VC_ERR_UNSUPPORTED, "no sliced kernel for this launch shape");
+  const size_t smem = dev::slice_smem_bytes(dp.slice_words, prm.nbases, dp.nrefs);
   int per_sm = 0;
   {
     static std::mutex mu;
@@ -1110,6 +1178,7 @@ vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<con
   prm.words = dp.words;
   prm.nbases = static_cast<uint32_t>(2 * N + 1);
   prm.groups = slice_groups;
+  if (slice_groups > 0) prm.words = dp.slice_words;
   for (int r = 0; r < N; ++r) {
     prm.base[r] = sends[r];
     prm.base[N + r] = recvs[r];
@@ -1314,8 +1383,10 @@ vc_status_t run(const Call& c) {
     aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
                (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
   const size_t slim = slice_limit();
-  if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 && es == 4 &&
-      c.count < (int64_t(1) << 29) && static_cast<uint64_t>(c.count * es) <= std::min<uint64_t>(slim, INT64_MAX)) {
+  // the sliced form's size: the 4 bytes a thread carries through the steps
+  // per element (fp32 / int32 data, or the fp32 partial sums of 16-bit data)
+  if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 &&
+      c.count < (int64_t(1) << 29) && static_cast<uint64_t>(c.count * 4) <= std::min<uint64_t>(slim, INT64_MAX)) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;
     else dp = nullptr;
@@ -1684,6 +1755,7 @@ VC_EXPORT vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nrank
             e.n = op.n;
             e.nb = op.nb;
             e.stride_bytes = role == 0 ? op.sstride : op.dstride;
+            e.elem0 = op.pos0;
           }
         }
       }

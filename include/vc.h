@@ -283,7 +283,10 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
  * run in one launch; steps run in order.
  *   buf: 0 send, 1 recv, 2 library scratch; owner: the rank that holds it;
  *   byte_off: from the start of that rank's buffer (scratch: of the scratch
- *   block); dtype: storage type of the operand.
+ *   block); dtype: storage type of the operand; elem0: for AllReduce, the
+ *   element position (index into the collective's buffers) of the
+ *   operation's first element -- its element i combines position elem0 + i
+ *   of every rank -- else -1.
  * Returns VC_ERR_INVALID_ARG if `capacity` is too small (with *n_entries set
  * to the size needed).  *scratch_bytes receives the scratch the call needs,
  * *n_steps the number of steps.
@@ -301,6 +304,7 @@ typedef struct {
   int64_t n;
   int64_t nb;
   int64_t stride_bytes;
+  int64_t elem0;  /* AllReduce: element position of the first element; else -1 */
 } vc_plan_entry_t;
 
 vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
@@ -404,26 +408,37 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * Sliced execution (a form of single-launch execution, tried before the
  * cluster form).
  *
- * In the fp32 and int32 AllReduce schedules (Ring, RHD, DBT, Mesh,
- * RING_HOP) every operation maps element e of each source to element e of
- * each destination, at the same offset in every rank buffer.  An AllReduce
- * call of such a schedule whose message per rank is at most
- * `max_bytes_per_rank` runs all its steps in one launch over the whole GPU:
- * each thread owns one 16-byte group -- the same bytes of every rank's send
- * and receive buffer -- and carries it through every step of the plan in
- * order, applying each operation that covers it.  What a step reads at a
- * position was written there by an earlier step, by the same thread, so the
- * thread's program order is the step barrier and no thread reads what another
- * wrote.  The steps, operations, operands and every element's association
- * are unchanged, so results are identical bit for bit; different positions
- * merely run out of step with each other, as when a ring is pipelined in
- * slices.  The conditions of single-launch execution on alignment and the
- * resident description apply as well.  max_bytes_per_rank: 0 disables it,
- * SIZE_MAX applies it to every eligible call.  Default
- * VC_SLICE_LIMIT_DEFAULT: up to 16 MiB per rank the form measured faster
- * than the cluster form and than per-step launches (8 ranks, fp32, GB300;
- * above, the whole GPU's bandwidth per step wins).  Process-wide.
+ * In the AllReduce schedules (Ring, RHD, DBT, Mesh, RING_HOP) every
+ * operation maps element position e of each source to position e of each
+ * destination, and each buffer holds position e at one place: element e of
+ * every rank's send and receive buffer and, for bf16 / fp16 data, element e
+ * of the fp32 partial sums the schedule keeps in scratch.  An AllReduce call
+ * of such a schedule whose fp32 / int32 data, or fp32 partial sums of 16-bit
+ * data, take at most `max_bytes_per_rank` per rank (4 bytes per element in
+ * either case) runs all its steps in one launch over the whole GPU: each
+ * thread owns one group of positions (16 bytes of the data type) of every
+ * buffer and carries it through every step of the plan in order, applying
+ * each operation that covers it.  What a step reads at a position was written
+ * there by an earlier step, by the same thread, so the thread's program order
+ * is the step barrier and no thread reads what another wrote.  The steps,
+ * operations, operands and every element's association (16-bit data:
+ * widened, combined in fp32, rounded once) are unchanged, so results are
+ * identical bit for bit; different positions merely run out of step with
+ * each other, as when a ring is pipelined in slices.  The 16-bit Ring keeps
+ * one fp32 partial per element while they take at most 16 MiB per rank;
+ * above that it alternates two chunk-sized slots per rank, which several
+ * positions share, and does not run sliced at 5 ranks or more.  The
+ * conditions of single-launch execution on alignment and the resident
+ * description apply as well.  max_bytes_per_rank: 0 disables it, SIZE_MAX
+ * applies it to every eligible call.  Default VC_SLICE_LIMIT_DEFAULT: up to
+ * 16 MiB per rank the form measured faster than the cluster form and than
+ * per-step launches (8 ranks, fp32 and bf16, GB300; above, the whole GPU's
+ * bandwidth per step wins).  Process-wide.
  */
+#define VC_SLICE_LIMIT_DEFAULT ((size_t)16 << 20)
+vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank);
+vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank);
+
 /*
  * Independent steps in one launch.
  *
@@ -440,10 +455,6 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  */
 vc_status_t vc_set_merge_steps(int on);
 vc_status_t vc_get_merge_steps(int* on);
-
-#define VC_SLICE_LIMIT_DEFAULT ((size_t)16 << 20)
-vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank);
-vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank);
 
 /*
  * Bulk-copy pipeline for large copy steps (no counterpart on the source

@@ -27,7 +27,7 @@ def get_plan(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0, op="
     steps = [dict() for _ in range(nsteps)]
     for e in entries:
         op = steps[e.step].setdefault(e.op, {"reduce": bool(e.reduce), "red": e.reduce, "n": e.n,
-                                             "nb": e.nb, "src": [], "dst": []})
+                                             "nb": e.nb, "elem0": e.elem0, "src": [], "dst": []})
         (op["src"] if e.role == 0 else op["dst"]).append(
             (e.pos, e.buf, e.owner, e.dtype, e.byte_off, e.stride_bytes))
     out = []
@@ -107,19 +107,86 @@ def _combine(a, b, red):
         return np.where(((b > a) if red == 2 else (b < a)) | (a != a), b, a)
 
 
+def _apply(op, mem: Memory, b: int, i0: int, i1: int) -> None:
+    """Elements [i0, i1) of run b of one operation."""
+    n = i1 - i0
+    srcs = [mem.view(k, o, dt, off + b * stride + i0 * ESZ[dt], n) for (k, o, dt, off, stride) in op["src"]]
+    if op["reduce"]:
+        acc = _widen(srcs[0], op["src"][0][2])
+        for s, (k, o, dt, off, stride) in zip(srcs[1:], op["src"][1:]):
+            acc = _combine(acc, _widen(s, dt), op["red"])
+    for (k, o, dt, off, stride) in op["dst"]:
+        dstv = mem.view(k, o, dt, off + b * stride + i0 * ESZ[dt], n)
+        dstv[:] = _narrow(acc, dt) if op["reduce"] else srcs[0]
+
+
 def run_plan(plan, mem: Memory) -> None:
     for ops in plan:
         for op in ops:
-            n = op["n"]
             for b in range(op["nb"]):
-                srcs = [mem.view(k, o, dt, off + b * stride, n) for (k, o, dt, off, stride) in op["src"]]
-                if op["reduce"]:
-                    acc = _widen(srcs[0], op["src"][0][2])
-                    for s, (k, o, dt, off, stride) in zip(srcs[1:], op["src"][1:]):
-                        acc = _combine(acc, _widen(s, dt), op["red"])
-                for (k, o, dt, off, stride) in op["dst"]:
-                    dstv = mem.view(k, o, dt, off + b * stride, n)
-                    dstv[:] = _narrow(acc, dt) if op["reduce"] else srcs[0]
+                _apply(op, mem, b, 0, op["n"])
+
+
+def position_places(plan, mem: Memory, group: int) -> list:
+    """The sliced form's precondition, checked on the described plan: every
+    operation names its first element position (elem0), a multiple of
+    `group`, covers one run, and every operand holds position elem0 + i at a
+    fixed place of its buffer -- byte off - elem0 * size + position * size,
+    with one origin (off - elem0 * size) for all operands whose bytes overlap.
+    Returns the violations (empty: each byte belongs to one position, so a
+    thread that owns a group of positions owns every byte of them)."""
+    bad = []
+    spans = defaultdict(list)  # buffer -> (lo, hi, origin, size)
+    for si, ops in enumerate(plan):
+        for oi, op in enumerate(ops):
+            e0 = op["elem0"]
+            if e0 < 0 or e0 % group or op["nb"] != 1:
+                bad.append((si, oi, "elem0", e0, op["nb"]))
+                continue
+            for (k, o, dt, off, stride) in op["src"] + op["dst"]:
+                z = ESZ[dt]
+                spans[mem.ident(k, o)].append((off, off + op["n"] * z, off - e0 * z, z, si, oi))
+    for key, lst in spans.items():
+        lst.sort()
+        reach, place = None, None
+        for (lo, hi, origin, z, si, oi) in lst:
+            if reach is not None and lo < reach and (origin, z) != place:
+                bad.append((si, oi, key, lo, origin, place))
+            if reach is None or lo >= reach:
+                place = (origin, z)
+            reach = hi if reach is None else max(reach, hi)
+    return bad
+
+
+def run_plan_sliced(plan, mem: Memory, count: int, group: int, schedule) -> None:
+    """The sliced form's execution with its owners interleaved as given: each
+    group of `group` element positions walks the steps in order, applying the
+    part of each operation that covers it; every entry of `schedule` (group
+    indices, each len(plan) times) advances that group by one step.  Equal to
+    run_plan for any schedule when the plan meets position_places."""
+    ranges = [[(op["elem0"], op["elem0"] + op["n"]) for op in ops] for ops in plan]
+    at = defaultdict(int)  # group -> next step
+    for g in schedule:
+        s = at[g]
+        at[g] = s + 1
+        a, z = g * group, min(count, (g + 1) * group)
+        for op, (lo, hi) in zip(plan[s], ranges[s]):
+            x, y = max(a, lo), min(z, hi)
+            if x < y:
+                _apply(op, mem, 0, x - lo, y - lo)
+
+
+def one_after_another(groups: int, steps: int, reverse: bool = True) -> list:
+    """Every group to the end before the next (last group first)."""
+    order = range(groups - 1, -1, -1) if reverse else range(groups)
+    return [g for g in order for _ in range(steps)]
+
+
+def shuffled(groups: int, steps: int, rng) -> list:
+    """A random interleaving of the groups' steps."""
+    sched = np.repeat(np.arange(groups), steps)
+    rng.shuffle(sched)
+    return sched.tolist()
 
 
 def hazards(plan, mem: Memory) -> list:

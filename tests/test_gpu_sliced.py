@@ -1,16 +1,18 @@
-"""The sliced form of fp32 / int32 AllReduce schedules, against the oracle.
+"""The sliced form of AllReduce schedules, against the oracle.
 
 In the sliced form (vc_set_slice_limit) one launch over the whole GPU runs
 every step of the plan, each thread carrying its 16-byte group of every rank
-buffer through the steps in order.  Forced on for every eligible call here:
-Ring, RHD (any rank count, with the fold-in), DBT, Mesh and the per-hop ring
-on fp32 and int32 with every op, ragged counts whose last group is partial,
+buffer (and, for bf16 / fp16, of the fp32 partial sums in scratch) through
+the steps in order.  Forced on for every eligible call here: Ring, RHD (any
+rank count, with the fold-in), DBT, Mesh and the per-hop ring on fp32, int32,
+bf16 and fp16 with every op, ragged counts whose last group is partial,
 sizes from one element to 64 MiB per rank, in place.  Every result must equal
 the C++ oracle's simulation of the same schedule bit for bit, and the launch
 trace must show one sliced launch for the call.  Also: calls that do not
-qualify (16-bit data, unaligned pointers, single-step plans, other
-collectives) take the other forms and stay exact; the default size limit;
-canary bands around every buffer.
+qualify (an 8-rank 16-bit Ring whose fp32 partial sums take more than 16
+MiB per rank and alternate between two chunk slots, unaligned pointers,
+single-step plans, other collectives) take the other forms and stay exact;
+the default size limit; canary bands around every buffer.
 """
 import numpy as np
 import pytest
@@ -41,6 +43,8 @@ def _lib():
 
 
 def _inputs(dtype, seed, N, n):
+    if dtype == "f16":
+        return [x.astype(np.float16) for x in rank_buffers("normal_f32", seed, N, n)]
     return rank_buffers({"f32": "uniform_f32", "i32": "int32_bits", "bf16": "normal_bf16"}[dtype], seed, N, n)
 
 
@@ -78,17 +82,36 @@ def test_sliced_allreduce_matches_oracle(N, dtype, op):
                 assert same_bits(got[r], want[r]), (algo, N, dtype, op, count, r, first_diff(got[r], want[r]))
 
 
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("N", [2, 3, 5, 8, 16])
+def test_sliced_16bit_allreduce_matches_oracle(N, dtype, op):
+    """bf16 / fp16: fp32 partial sums in scratch, rounded once into the
+    receive buffers; every launch shape (1, 2 and 4 groups a thread)."""
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    counts = (1, 7, 8, 13, 1023, 4096 + 5, 65536 + 37) + ((300_001, 1_500_003) if op == "sum" else ())
+    for count in counts:
+        xs = _inputs(dtype, 8700 + N + count, N, count)
+        for algo in SLICED_ALGOS:
+            want = cxx.allreduce(xs, algo, dtype, op=op, want_log=False).outputs
+            got, recs = _run(xs, algo, dtype, op)
+            assert len(recs) == 1 and recs[0]["kernel"].endswith("_sliced"), (algo, N, count, recs)
+            for r in range(N):
+                assert same_bits(got[r], want[r]), (algo, N, dtype, op, count, r, first_diff(got[r], want[r]))
+
+
 @pytest.mark.parametrize("N", [4, 8])
 def test_sliced_in_place(N):
     vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
     for count in (777, 100_000):
-        xs = _inputs("f32", 8200 + N + count, N, count)
-        for algo in SLICED_ALGOS:
-            want = cxx.allreduce(xs, algo, "f32", want_log=False).outputs
-            got, recs = _run(xs, algo, "f32", inplace=True)
-            assert recs[0]["kernel"].endswith("_sliced"), (algo, recs)
-            for r in range(N):
-                assert same_bits(got[r], want[r]), (algo, N, count, r)
+        for dtype in ("f32", "bf16"):
+            xs = _inputs(dtype, 8200 + N + count, N, count)
+            for algo in SLICED_ALGOS:
+                want = cxx.allreduce(xs, algo, dtype, want_log=False).outputs
+                got, recs = _run(xs, algo, dtype, inplace=True)
+                assert recs[0]["kernel"].endswith("_sliced"), (algo, recs)
+                for r in range(N):
+                    assert same_bits(got[r], want[r]), (algo, N, dtype, count, r)
 
 
 def test_sliced_large_messages():
@@ -108,16 +131,38 @@ def test_sliced_large_messages():
         assert same_bits(got, want), (algo, first_diff(got, want))
 
 
+def test_sliced_16bit_at_8_mib():
+    """bf16 at 8 MiB per rank, 8 ranks (16 MiB of fp32 partials: the largest
+    flat Ring): every element of rank 0 equal to the oracle's, every rank equal."""
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    N, count = 8, (8 << 20) // 2
+    xs = _inputs("bf16", 8310, N, count)
+    sends = [to_dev(x) for x in xs]
+    recvs = [torch.empty_like(s) for s in sends]
+    for algo in ("ring", "rhd", "dbt"):
+        recs = _traced(lambda: vc.vc_allreduce(sends, recvs, algo=algo))
+        assert recs[0]["kernel"].endswith("_sliced"), recs
+        for r in range(1, N):
+            assert torch.equal(recvs[r], recvs[0]), (algo, r)
+        want = cxx.allreduce(xs, algo, "bf16", want_log=False, keep=(0,)).outputs[0]
+        got = to_host(recvs[0])
+        assert same_bits(got, want), (algo, first_diff(got, want))
+
+
 def test_calls_that_do_not_qualify_take_other_forms():
     vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
-    N, count = 8, 4096 + 3
-    # 16-bit data (fp32 partials in scratch), unaligned pointers, a single-step plan
+    # a 16-bit Ring with more than 16 MiB of fp32 partials per rank: they
+    # alternate between two chunk slots (at 8 ranks six steps write partials,
+    # so each slot holds three chunks in turn; at 4 ranks or fewer each slot
+    # holds one and stays positional)
+    N, count = 8, (16 << 20) // 4 + 8 * 3 + 5
     xb = _inputs("bf16", 8400, N, count)
-    for algo in ("ring", "rhd", "dbt"):
-        want = cxx.allreduce(xb, algo, "bf16", want_log=False).outputs
-        got, recs = _run(xb, algo, "bf16")
-        assert not any(r["kernel"].endswith("_sliced") for r in recs), (algo, recs)
-        assert all(same_bits(got[r], want[r]) for r in range(N)), algo
+    want = cxx.allreduce(xb, "ring", "bf16", want_log=False).outputs
+    got, recs = _run(xb, "ring", "bf16")
+    assert not any(r["kernel"].endswith("_sliced") for r in recs), recs
+    assert all(same_bits(got[r], want[r]) for r in range(N))
+    # unaligned pointers, a single-step plan
+    N, count = 8, 4096 + 3
     xs = _inputs("f32", 8401, N, count)
     for algo in ("ring", "fused"):
         want = cxx.allreduce(xs, algo, "f32", want_log=False).outputs
@@ -147,6 +192,17 @@ def test_default_limit():
             want = sliced
             assert any(r["kernel"].endswith("_sliced") for r in recs) == want, (algo, nbytes, recs)
             assert torch.allclose(y[0], s, atol=1e-5), (algo, nbytes)
+        del x, y
+    # 16-bit data: the limit counts the fp32 partial sums, 4 bytes per element
+    for nbytes, sliced in ((1 << 20, True), (vc.VC_SLICE_DEFAULT // 2, True), (vc.VC_SLICE_DEFAULT, False)):
+        count = nbytes // 2
+        x = [torch.randn(count, device="cuda").to(torch.bfloat16) for _ in range(N)]
+        y = [torch.empty_like(t) for t in x]
+        s = torch.stack(x).float().sum(0)
+        for algo in ("ring", "dbt", "mesh", "rhd"):
+            recs = _traced(lambda: vc.vc_allreduce(x, y, algo=algo))
+            assert any(r["kernel"].endswith("_sliced") for r in recs) == sliced, (algo, nbytes, recs)
+            assert torch.allclose(y[0].float(), s, rtol=1e-2, atol=1e-2), (algo, nbytes)
         del x, y
 
 

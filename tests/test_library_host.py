@@ -233,8 +233,10 @@ def test_scratch_sizes():
     # fp32 ring / rhd / dbt AllReduce keep partial sums in the receive buffers
     for algo in ("ring", "rhd", "dbt", "fused"):
         assert get_plan("allreduce", algo, 8, 1 << 20, "f32")[1] == 0
-    # bf16 ring: two fp32 chunk slots per rank
-    assert get_plan("allreduce", "ring", 8, 1 << 20, "bf16")[1] == 8 * 2 * (1 << 17) * 4
+    # bf16 ring: one fp32 partial per element and rank while they take at most
+    # 16 MiB per rank, above that two fp32 chunk slots per rank
+    assert get_plan("allreduce", "ring", 8, 1 << 20, "bf16")[1] == 8 * (1 << 20) * 4
+    assert get_plan("allreduce", "ring", 8, 1 << 24, "bf16")[1] == 8 * 2 * (1 << 21) * 4
     # Bruck at N = 8 (3 rounds) uses two working buffers of N blocks per rank
     assert get_plan("alltoall", "bruck", 8, 1024, "bf16")[1] == 2 * 8 * 8 * 1024 * 2
 
