@@ -27,7 +27,6 @@ namespace dev {
 // address is ordered before them).  Steps, operations, operands and every
 // element's association are the plan's; only positions far apart run out of
 // step with each other, as when a ring is pipelined in slices.  The host
-// lists each operation's element range [e0, e1) after the operand table and
 // checks that every position has one place in each buffer; the positions
 // after an operation's last whole group are handled, one by one, by the
 // owner of that group.
@@ -47,65 +46,15 @@ __device__ __forceinline__ uint4 cmb4(uint4 a, uint4 w) {
   return a;
 }
 
-// Shared memory of a block: the plan description (16-byte words, ending with
-// the operations' element ranges), the call's buffer bases, then each
-// operand's address (base + offset), which the block derives once.  Every
-// buffer of a sliced call holds fewer than 2^29 elements (checked on the
-// host), so element and byte offsets within it fit 32 bits.
-__host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t nbases, uint32_t nrefs) {
-  return size_t(words) * 16 + size_t(nbases) * 8 + size_t(nrefs) * 8;
-}
-
-// The block's copy of the description and the operand addresses.
-struct SliceTables {
-  PlanHeader h;
-  const PlanStep* steps;
-  const OpDesc* ops;
-  const int2* rng;   // per operation: e0, e1
-  char* const* addr;  // per operand: its address
-};
-template <int BT>
-__device__ __forceinline__ SliceTables slice_prologue(const PlanParams& p, uint4* sm) {
-  for (uint32_t i = threadIdx.x; i < p.words; i += BT) sm[i] = ld16(p.plan + i);
-  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
-  for (uint32_t i = threadIdx.x; i < p.nbases; i += BT) sbase[i] = p.base[i];
-  __syncthreads();
-  SliceTables t;
-  t.h = *reinterpret_cast<const PlanHeader*>(sm);
-  t.steps = reinterpret_cast<const PlanStep*>(sm + 1);
-  t.ops = reinterpret_cast<const OpDesc*>(sm + 1 + t.h.nsteps);
-  const OperandRef* refs = reinterpret_cast<const OperandRef*>(t.ops + t.h.nops);
-  t.rng = reinterpret_cast<const int2*>(refs + t.h.nrefs);
-  char** addr = reinterpret_cast<char**>(const_cast<void**>(sbase + p.nbases));
-  for (uint32_t i = threadIdx.x; i < t.h.nrefs; i += BT)
-    addr[i] = static_cast<char*>(const_cast<void*>(sbase[refs[i].base])) + refs[i].off;
-  t.addr = addr;
-  __syncthreads();
-  return t;
-}
-
-// Each thread looks for the next operation of the step that covers one of
-// its groups (elements [ea, eb) span them), then applies it.  Threads of a
-// warp can be in different operations (small chunks); searching first and
-// applying after keeps the warp together, so their loads go out at once
-// instead of one operation's chain after another.
-// The step's operations are listed by position (ascending first element), so
-// none after one that starts past this thread's groups can cover them.
-// Stopping there measured faster where a thread carries 4 or more groups (4
-// MiB per rank fp32: ring 24.5 -> 20.4 us) and slower where it carries 1 or 2
-// (up to 2 MiB: ring 10.7 -> 13.4 us at 4 KiB), so only the former stop
-// early.  Returns the operation's index, or kend.
-template <int U>
-__device__ __forceinline__ uint32_t slice_next_op(const int2* rng, uint32_t k, uint32_t kend, int ea, int eb,
-                                                  int2* r) {
-  for (; k < kend; ++k) {
-    *r = rng[k];
-    if constexpr (U >= 4) {
-      if (r->x >= eb) return kend;
-    }
-    if (ea < r->y && eb > r->x) return k;  // covers one of the groups
-  }
-  return kend;
+// Shared memory of a block: the plan description (16-byte words), the call's
+// buffer bases, then two tables: each operation's element range [e0, e1)
+// and each operand's address (base + offset).  (16-bit plans take the ranges
+// as part of the description: the same size, up to 8 bytes.)  Every buffer
+// of a sliced call holds fewer than 2^29 elements (checked on the host), so
+// element and byte offsets within it fit 32 bits.
+__host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t nbases, uint32_t nops,
+                                                      uint32_t nrefs) {
+  return size_t(words) * 16 + size_t(nbases) * 8 + size_t(nops) * 8 + size_t(nrefs) * 8;
 }
 
 // BT threads a block; U groups a thread, BT apart (slices of U * BT groups);
@@ -115,7 +64,24 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
   static_assert(RMODE == kF32 || RMODE == kI32, "4-byte sliced plans are fp32 or int32");
   extern __shared__ uint4 sm[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const SliceTables t = slice_prologue<BT>(p, sm);
+  for (uint32_t i = threadIdx.x; i < p.words; i += BT) sm[i] = ld16(p.plan + i);
+  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
+  for (uint32_t i = threadIdx.x; i < p.nbases; i += BT) sbase[i] = p.base[i];
+  __syncthreads();
+  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
+  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
+  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
+  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
+  int2* rng = reinterpret_cast<int2*>(sbase + p.nbases);             // per operation: e0, e1
+  char** addr = reinterpret_cast<char**>(rng + h.nops);              // per operand: its address
+  // 4-byte plans keep every operand in a send or receive buffer at byte 4 e0
+  for (uint32_t i = threadIdx.x; i < h.nops; i += BT) {
+    const int e0 = static_cast<int>(refs[ops[i].p0].off >> 2);
+    rng[i] = make_int2(e0, e0 + static_cast<int>(ops[i].n));
+  }
+  for (uint32_t i = threadIdx.x; i < h.nrefs; i += BT)
+    addr[i] = static_cast<char*>(const_cast<void*>(sbase[refs[i].base])) + refs[i].off;
+  __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kSlice = U * BT;
   const int groups = static_cast<int>(p.groups);
@@ -124,14 +90,36 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
     const int g0 = sl * kSlice + static_cast<int>(threadIdx.x);  // this thread's groups: g0 + u * BT
     if (g0 >= groups) break;
     const int ea = g0 * 4, eb = (g0 + (U - 1) * BT) * 4 + 4;     // elements its groups span
-    for (uint32_t s = 0; s < t.h.nsteps; ++s) {
-      const PlanStep st = t.steps[s];
+    for (uint32_t s = 0; s < h.nsteps; ++s) {
+      const PlanStep st = steps[s];
+      // Each thread looks for the next operation of the step that covers one
+      // of its groups, then applies it.  Threads of a warp can be in different
+      // operations (small chunks); searching first and applying after keeps
+      // the warp together, so their loads go out at once instead of one
+      // operation's chain after another.
+      // The step's operations are listed by position (ascending first
+      // element), so none after one that starts past this thread's groups
+      // can cover them.  Stopping there measured faster where a thread
+      // carries 4 or more groups (4 MiB per rank: ring 24.5 -> 20.4 us) and
+      // slower where it carries 1 or 2 (up to 2 MiB: ring 10.7 -> 13.4 us at
+      // 4 KiB), so only the former stop early.
+      uint32_t k = st.op0;
       const uint32_t kend = st.op0 + st.nops;
-      int2 r = make_int2(0, 0);
-      for (uint32_t k = slice_next_op<U>(t.rng, st.op0, kend, ea, eb, &r); k < kend;
-           k = slice_next_op<U>(t.rng, k + 1, kend, ea, eb, &r)) {
-        const OpDesc& o = t.ops[k];
-        char* const* P = t.addr + o.p0;  // sources, then destinations
+      for (;;) {
+        int2 r = make_int2(0, 0);
+        for (; k < kend; ++k) {
+          r = rng[k];
+          if constexpr (U >= 4) {
+            if (r.x >= eb) {
+              k = kend;
+              break;
+            }
+          }
+          if (ea < r.y && eb > r.x) break;  // covers one of the groups
+        }
+        if (k >= kend) break;
+        const OpDesc& o = ops[k++];
+        char* const* P = addr + o.p0;  // sources, then destinations
         const int ns = o.ns, nd = o.nd;
         bool whole[U];
         int off[U];  // bytes into every operand
@@ -183,16 +171,60 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
   }
 }
 
+// 16-bit plans: copies the description -- here with the operations' element
+// ranges after the operand table, which the host lists because fp32 partials
+// in scratch sit at other offsets than the data -- and the bases to shared
+// memory, and derives each operand's address (after the bases).
+template <int BT>
+__device__ __forceinline__ void slice_prologue(const PlanParams& p, uint4* sm) {
+  for (uint32_t i = threadIdx.x; i < p.words; i += BT) sm[i] = ld16(p.plan + i);
+  const void** sbase = reinterpret_cast<const void**>(sm + p.words);
+  for (uint32_t i = threadIdx.x; i < p.nbases; i += BT) sbase[i] = p.base[i];
+  __syncthreads();
+  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
+  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
+  const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
+  char** addr = reinterpret_cast<char**>(const_cast<void**>(sbase + p.nbases));
+  for (uint32_t i = threadIdx.x; i < h.nrefs; i += BT)
+    addr[i] = static_cast<char*>(const_cast<void*>(sbase[refs[i].base])) + refs[i].off;
+  __syncthreads();
+}
+
+// The search of slice_kernel as a function: the next operation of the step,
+// from k on, that covers one of the groups spanning elements [ea, eb);
+// returns its index, or kend.
+template <int U>
+__device__ __forceinline__ uint32_t slice_next_op(const int2* rng, uint32_t k, uint32_t kend, int ea, int eb,
+                                                  int2* r) {
+  for (; k < kend; ++k) {
+    *r = rng[k];
+    if constexpr (U >= 4) {
+      if (r->x >= eb) return kend;
+    }
+    if (ea < r->y && eb > r->x) return k;  // covers one of the groups
+  }
+  return kend;
+}
+
 // bf16 / fp16 plans: a group is 8 elements, 16 bytes of a buffer in the data
 // type or 32 of an fp32 partial-sum buffer (smask / dmask bit set).  Every
 // source is widened to fp32 (exact) and combined in the plan's order; a
 // destination in the data type takes the fp32 result rounded to nearest even,
 // once, exactly as the per-step kernels do.  Copies move the data type.
+// Against the form of slice_kernel (ranges derived in the block, the search
+// inline), this one measured 0.2-1 us faster on 16-bit plans (8 ranks, 4 KiB
+// to 4 MiB per rank); on 4-byte plans it measured up to 0.5 us slower at up
+// to 256 KiB, so each keeps the form that measured faster for it.
 template <bool F16, int OP, int U, int BT>
 __global__ void __launch_bounds__(BT) slice16_kernel(const __grid_constant__ PlanParams p) {
   extern __shared__ uint4 sm[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const SliceTables t = slice_prologue<BT>(p, sm);
+  slice_prologue<BT>(p, sm);
+  const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
+  const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
+  const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
+  const int2* rng = reinterpret_cast<const int2*>(reinterpret_cast<const OperandRef*>(ops + h.nops) + h.nrefs);
+  char* const* addr = reinterpret_cast<char* const*>(reinterpret_cast<void* const*>(sm + p.words) + p.nbases);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kSlice = U * BT;
   const int groups = static_cast<int>(p.groups);
@@ -201,14 +233,14 @@ __global__ void __launch_bounds__(BT) slice16_kernel(const __grid_constant__ Pla
     const int g0 = sl * kSlice + static_cast<int>(threadIdx.x);  // this thread's groups: g0 + u * BT
     if (g0 >= groups) break;
     const int ea = g0 * 8, eb = (g0 + (U - 1) * BT) * 8 + 8;     // elements its groups span
-    for (uint32_t s = 0; s < t.h.nsteps; ++s) {
-      const PlanStep st = t.steps[s];
+    for (uint32_t s = 0; s < h.nsteps; ++s) {
+      const PlanStep st = steps[s];
       const uint32_t kend = st.op0 + st.nops;
       int2 r = make_int2(0, 0);
-      for (uint32_t k = slice_next_op<U>(t.rng, st.op0, kend, ea, eb, &r); k < kend;
-           k = slice_next_op<U>(t.rng, k + 1, kend, ea, eb, &r)) {
-        const OpDesc& o = t.ops[k];
-        char* const* P = t.addr + o.p0;  // sources, then destinations
+      for (uint32_t k = slice_next_op<U>(rng, st.op0, kend, ea, eb, &r); k < kend;
+           k = slice_next_op<U>(rng, k + 1, kend, ea, eb, &r)) {
+        const OpDesc& o = ops[k];
+        char* const* P = addr + o.p0;  // sources, then destinations
         const int ns = o.ns, nd = o.nd;
         bool whole[U];
         int rel[U];  // elements into every operand

@@ -790,7 +790,7 @@ struct DevPlan {
   int nops = 0;
   bool sliced = false;           // every operation keeps element positions: the sliced form applies
   uint32_t nrefs = 0;
-  uint32_t slice_words = 0;      // sliced form: the description with the operations' element ranges
+  uint32_t slice_words = 0;      // the description with the operations' element ranges (16-bit sliced form)
 };
 struct PlanStore {
   std::unordered_map<PlanKey, DevPlan, PlanKeyHash> plans;
@@ -990,9 +990,9 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
   dp->nrefs = static_cast<uint32_t>(nrefs);
   dp->eligible = true;
   dp->sliced = sliceable(plan, dp->rmode) &&
-               dev::slice_smem_bytes(dp->words + static_cast<uint32_t>((nops + 1) / 2), 2 * N + 1,
-                                     static_cast<uint32_t>(nrefs)) <= static_cast<size_t>(kPlanSmemMax);
-  if (dp->sliced) {  // the operations' element ranges [e0, e1), in listed order, after the operand table
+               dev::slice_smem_bytes(dp->words, 2 * N + 1, static_cast<uint32_t>(nops + 1), static_cast<uint32_t>(nrefs)) <=
+                   static_cast<size_t>(kPlanSmemMax);
+  if (dp->sliced) {  // after the description: the operations' element ranges [e0, e1), in listed order
     dp->slice_words = dp->words + static_cast<uint32_t>((nops + 1) / 2);
     img->resize(dp->slice_words, make_uint4(0, 0, 0, 0));
     auto* rng = reinterpret_cast<int2*>(img->data() + dp->words);
@@ -1113,7 +1113,8 @@ vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanPar
                            : U == 4 ? slice_kernel_for<4, kSliceBlock>(dp.rmode, dp.red)
                                     : slice_kernel_for<8, kSliceBlock>(dp.rmode, dp.red);
   if (!kernel) return fail(VC_ERR_UNSUPPORTED, "no sliced kernel for this launch shape");
-  const size_t smem = dev::slice_smem_bytes(dp.slice_words, prm.nbases, dp.nrefs);
+  // (16-bit: the ranges within the description, up to 8 bytes more than the table)
+  const size_t smem = dev::slice_smem_bytes(dp.words, prm.nbases, dp.nops + 1, dp.nrefs);
   int per_sm = 0;
   {
     static std::mutex mu;
@@ -1178,7 +1179,7 @@ vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<con
   prm.words = dp.words;
   prm.nbases = static_cast<uint32_t>(2 * N + 1);
   prm.groups = slice_groups;
-  if (slice_groups > 0) prm.words = dp.slice_words;
+  if (slice_groups > 0 && (dp.rmode == dev::kBF16 || dp.rmode == dev::kF16)) prm.words = dp.slice_words;
   for (int r = 0; r < N; ++r) {
     prm.base[r] = sends[r];
     prm.base[N + r] = recvs[r];
