@@ -859,15 +859,41 @@ int plan_cluster(PlanStore& ps) {
   return best;
 }
 
+// Byte ranges of one buffer written so far (start -> end, disjoint).
+struct Written {
+  std::map<int64_t, int64_t> runs;
+  void add(int64_t lo, int64_t hi) {
+    auto it = runs.upper_bound(lo);
+    if (it != runs.begin() && std::prev(it)->second >= lo) {
+      --it;
+      lo = it->first;
+      hi = std::max(hi, it->second);
+      it = runs.erase(it);
+    }
+    while (it != runs.end() && it->first <= hi) {
+      hi = std::max(hi, it->second);
+      it = runs.erase(it);
+    }
+    runs.emplace(lo, hi);
+  }
+  bool covers(int64_t lo, int64_t hi) const {
+    auto it = runs.upper_bound(lo);
+    return it != runs.begin() && std::prev(it)->second >= hi;
+  }
+};
+
 // The sliced form (slice_kernel, slice16_kernel) applies to a plan whose
 // every operation keeps element positions: operation element i is position
 // pos0 + i of the collective's buffers, one run, a copy from one source.
 // Position e lives at byte e * size of a send or receive buffer (of the data
 // type), and at byte origin + 4 e of an fp32 partial-sum region of scratch
-// (16-bit data), where the regions whose bytes overlap share one origin.
-// Then each byte any operation touches belongs to one position, and with
-// groups and operations starting on 16-byte boundaries a thread that owns a
-// group of positions owns every byte of them.  Positions stay below 2^29
+// (16-bit data, 32-byte aligned), where the regions whose bytes overlap
+// share one origin.  Then each byte any operation touches belongs to one
+// position, and with groups and operations starting on 16-byte boundaries a
+// thread that owns a group of positions owns every byte of them.  Send
+// buffers are only read, and every byte of a receive buffer or of scratch
+// that a step reads was written by an earlier step -- by the thread that
+// owns it, which therefore reads it through L1.  Positions stay below 2^29
 // (checked per call), so the kernels' 32-bit element offsets hold.
 bool sliceable(const Plan& plan, int rmode) {
   int es;
@@ -887,15 +913,30 @@ bool sliceable(const Plan& plan, int rmode) {
         if (o.buf != Buf::Scratch) return esize(o.dt) == es && o.byte_off == op.pos0 * es;
         if (es != 2 || o.dt != DT::F32 || st.mode == Mode::Copy) return false;
         const int64_t origin = o.byte_off - op.pos0 * 4;
-        if (origin % 16 != 0) return false;
+        if (origin % 32 != 0) return false;
         regions.push_back({o.byte_off, o.byte_off + op.n * 4, origin});
         return true;
       };
       for (const Operand& o : op.src)
         if (!fits(o)) return false;
       for (const Operand& o : op.dst)
-        if (!fits(o)) return false;
+        if (o.buf == Buf::Send || !fits(o)) return false;
     }
+  // receive buffers and scratch: written before read, step by step
+  std::map<std::pair<int, int>, Written> written;  // (buffer kind, owner)
+  auto key = [](const Operand& o) {
+    return std::make_pair(static_cast<int>(o.buf), o.buf == Buf::Scratch ? 0 : o.owner);
+  };
+  for (const Step& st : plan.steps) {
+    for (const Op& op : st.ops)
+      for (const Operand& o : op.src) {
+        if (o.buf == Buf::Send) continue;
+        const auto it = written.find(key(o));
+        if (it == written.end() || !it->second.covers(o.byte_off, o.byte_off + op.n * esize(o.dt))) return false;
+      }
+    for (const Op& op : st.ops)
+      for (const Operand& o : op.dst) written[key(o)].add(o.byte_off, o.byte_off + op.n * esize(o.dt));
+  }
   std::sort(regions.begin(), regions.end(), [](const Region& a, const Region& b) { return a.lo < b.lo; });
   int64_t reach = INT64_MIN, origin = 0;  // furthest byte of the regions so far, and their origin
   for (const Region& g : regions) {
@@ -1092,8 +1133,8 @@ SliceKernel slice_kernel_for(int rmode, RedOp r) {
 // of a step a thread issues together) that take at most two blocks per SM.
 // Grids of more than 64 blocks of one group a thread were up to twice as
 // slow, and 512- or 1024-thread blocks slower at small sizes.  16-bit plans
-// stop at 4 groups a thread (8 elements each, fp32 sums: 128 registers, two
-// blocks per SM; 8 groups take 240).
+// stop at 4 groups a thread (8 elements each, fp32 sums: 128 registers for
+// bf16, two blocks per SM, 144 for fp16; 8 groups take 240).
 constexpr int kSliceBlock = 256;
 constexpr int kSliceSmallGrid = 64;
 
@@ -1386,7 +1427,9 @@ vc_status_t run(const Call& c) {
   const size_t slim = slice_limit();
   // the sliced form's size: the 4 bytes a thread carries through the steps
   // per element (fp32 / int32 data, or the fp32 partial sums of 16-bit data)
+  // (16-bit sliced plans access their fp32 partials 32 bytes at a time)
   if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 &&
+      (es == 4 || (reinterpret_cast<uintptr_t>(scratch) & 31) == 0) &&
       c.count < (int64_t(1) << 29) && static_cast<uint64_t>(c.count * 4) <= std::min<uint64_t>(slim, INT64_MAX)) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;

@@ -158,6 +158,37 @@ def position_places(plan, mem: Memory, group: int) -> list:
     return bad
 
 
+def reads_before_writes(plan, mem: Memory) -> list:
+    """Reads of a receive buffer or of scratch whose bytes no earlier step
+    wrote (the sliced form reads those through L1 and needs none: what it
+    reads there, the reading thread stored earlier in the launch).  Send
+    buffers are inputs and may be read at any step; nothing may write them.
+    Returns the violations."""
+    bad = []
+    written = defaultdict(list)  # buffer -> [(lo, hi)] written by earlier steps
+    for si, ops in enumerate(plan):
+        for oi, op in enumerate(ops):
+            for (k, o, dt, off, stride) in op["dst"]:
+                if k == SEND:
+                    bad.append((si, oi, "writes a send buffer", o))
+            for (k, o, dt, off, stride) in op["src"]:
+                if k == SEND:
+                    continue
+                lo, hi = off, off + op["n"] * ESZ[dt]
+                key = ("X", 0) if k == SCRATCH else ("R", o)
+                cov = lo
+                for (a, b) in sorted(written[key]):
+                    if a <= cov < b:
+                        cov = b
+                if cov < hi:
+                    bad.append((si, oi, key, lo, hi, cov))
+        for op in ops:
+            for (k, o, dt, off, stride) in op["dst"]:
+                key = ("X", 0) if k == SCRATCH else ("R", o)
+                written[key].append((off, off + op["n"] * ESZ[dt]))
+    return bad
+
+
 def run_plan_sliced(plan, mem: Memory, count: int, group: int, schedule) -> None:
     """The sliced form's execution with its owners interleaved as given: each
     group of `group` element positions walks the steps in order, applying the

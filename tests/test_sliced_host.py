@@ -9,7 +9,9 @@ the plan the library describes (no GPU):
 
 - every AllReduce schedule in every data type and op meets that condition
   while the partial sums take at most 16 MiB per rank (the 16-bit Ring keeps
-  one fp32 partial per position);
+  one fp32 partial per position), writes no send buffer, and reads a receive
+  buffer or scratch only where an earlier step wrote (the sliced kernels
+  read those through L1: the reading thread stored them itself);
 - running the plan group by group -- each group to the end before the next,
   and the groups' steps randomly interleaved -- gives the oracle's result bit
   for bit;
@@ -28,7 +30,7 @@ from oracle import schedules
 from synthetic_inputs import rank_buffers
 
 from .plan_replay import (DT, ESZ, NPT, SCRATCH, Memory, get_plan, hazards, one_after_another, position_places,
-                          run_plan, run_plan_sliced, shuffled)
+                          reads_before_writes, run_plan, run_plan_sliced, shuffled)
 
 ALGOS = tuple(a for a in schedules.ALGOS["allreduce"] if a != "fused")  # multi-step schedules
 
@@ -67,6 +69,10 @@ def test_allreduce_plans_keep_positions(N, dtype):
                 mem = Memory([None] * N, [0] * N, scratch)
                 bad = position_places(plan, mem, _group(dtype))
                 assert not bad, (algo, N, count, dtype, op, bad[:3])
+                for inplace in (False, True):
+                    plan_i = get_plan("allreduce", algo, N, count, dtype, op=op, inplace=inplace)[0]
+                    bad = reads_before_writes(plan_i, mem)
+                    assert not bad, (algo, N, count, dtype, op, inplace, bad[:3])
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "i32"])
@@ -118,6 +124,18 @@ def _alternating_slots(plan, N, count):
             new_ops.append(op)
         out.append(new_ops)
     return out
+
+
+def test_reads_before_writes_catches_a_planted_early_read():
+    """A read of a receive buffer moved one step before the write it needs:
+    in the bf16 Ring (partials in scratch) AllGather step 2 copies the chunk
+    that step 1 stored, and nothing wrote those bytes before."""
+    N, count = 4, 4 * 64
+    plan, scratch = get_plan("allreduce", "ring", N, count, "bf16")
+    mem = Memory([None] * N, [0] * N, scratch)
+    assert not reads_before_writes(plan, mem)
+    planted = plan[:N] + [plan[-1]] + plan[N:-1]  # AllGather steps 0, 2, 1
+    assert reads_before_writes(planted, mem)
 
 
 def test_planted_slot_reuse_fails_both_checks():
