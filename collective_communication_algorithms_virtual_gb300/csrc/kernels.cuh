@@ -74,7 +74,7 @@ struct __align__(16) LaunchParams {
   uint32_t nops;    // operations in use
   uint32_t ntiles;  // tiles of the launch
   uint32_t rev;     // walk the launch's tiles last to first (the previous step's latest writes first)
-  uint32_t pad;
+  uint32_t late;    // 1: the grid leaves room on the GPU; let the next grid in only after the wait
   OpDesc op[OPS];
   const void* ptr[PTRS];
 };
@@ -742,15 +742,22 @@ __device__ __forceinline__ int find_op(const OpDesc* op, int nops, uint32_t t) {
 // the previous step's grid drains; it lets the next step be scheduled the
 // same way, then waits until the previous grid has completed and its writes
 // are visible before touching the buffers.  Without the launch attribute
-// both are no-ops and stream order applies.
+// both are no-ops and stream order applies.  A grid that covers the GPU
+// keeps the next one from running ahead of it.  One that leaves room (late:
+// fewer tiles than resident blocks) lets the next grid in only after its wait,
+// as the one-launch kernels do (see plan_kernel).  After the wait for every
+// grid, the 256 MiB per rank Ring and RHD measured 4% and 2% slower; for none,
+// per-step Rings of 512 KiB - 1 MiB per rank 12-28% slower.
 template <int MODE, int OP, class P, int SB, bool ELEM, bool FAN>
 __global__ void __launch_bounds__(kThreads) step_kernel(const __grid_constant__ P p) {
   __shared__ uint32_t s_tile0[sizeof(P::op) / sizeof(OpDesc)];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const bool late = p.late != 0;
+  if (!late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int nops = static_cast<int>(p.nops);
   for (int i = threadIdx.x; i < nops; i += kThreads) s_tile0[i] = p.op[i].tile0;
   __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // (kernels with the bulk-store path, which serve fused and fan-out
   // operations, keep the forward walk: their code stays as it was, and the
   // fused AllReduce measured 2% slower with the direction select in it)
@@ -814,7 +821,8 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
   extern __shared__ __align__(128) unsigned char stage[];  // kCopyStages * kCopyTileBytes, then the mbarriers
   __shared__ uint32_t s_tile0[sizeof(P::op) / sizeof(OpDesc)];
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kCopyStages * kCopyTileBytes);
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const bool late = p.late != 0;  // as in step_kernel
+  if (!late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int nops = static_cast<int>(p.nops);
   for (int i = threadIdx.x; i < nops; i += kCopyThreads) s_tile0[i] = p.op[i].tile0;
   if (threadIdx.x == 0) {
@@ -824,6 +832,7 @@ __global__ void __launch_bounds__(kCopyThreads) tma_copy_kernel(const __grid_con
   }
   __syncwarp();
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x != 0) return;
   // tile i of this block is global tile blockIdx.x + i * gridDim.x
   const int64_t n = p.ntiles > blockIdx.x ? (p.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -951,12 +960,19 @@ constexpr int kPlanThreads = kThreads * kPlanSubs;
 template <int RMODE, int OP>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
   extern __shared__ uint4 sm[];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (uint32_t i = threadIdx.x; i < p.words; i += kPlanThreads) sm[i] = ld16(p.plan + i);
   const void** sbase = reinterpret_cast<const void**>(sm + p.words);
   for (uint32_t i = threadIdx.x; i < p.nbases; i += kPlanThreads) sbase[i] = p.base[i];
   __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The next grid may be scheduled once every block of this one is past its
+  // wait: at most one grid ahead.  Triggered as the first instruction (as a
+  // step grid does), each waiting grid admitted the next, a run of small
+  // back-to-back launches filled the SMs with waiting blocks, and the time
+  // per launch grew with the run.  The sliced form, 8 ranks, fp32 Ring at 1
+  // MiB per rank: 12.2 us a call at 10 calls in a graph, 19.7 at 400; with the
+  // trigger here, 11.1 at both.  This form: 28.8 -> 22.7 us at 1 MiB.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
   const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
   const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);

@@ -121,7 +121,6 @@ template <int RMODE, int OP, int U, int BT>
 __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanParams p) {
   static_assert(RMODE == kF32 || RMODE == kI32, "4-byte sliced plans are fp32 or int32");
   extern __shared__ uint4 sm[];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (uint32_t i = threadIdx.x; i < p.words; i += BT) sm[i] = ld16(p.plan + i);
   const void** sbase = reinterpret_cast<const void**>(sm + p.words);
   for (uint32_t i = threadIdx.x; i < p.nbases; i += BT) sbase[i] = p.base[i];
@@ -141,6 +140,7 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
     addr[i] = slice_addr(refs[i], sbase, (p.nbases - 1) / 2);
   __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // at most one grid ahead (plan_kernel)
   constexpr int kSlice = U * BT;
   const int groups = static_cast<int>(p.groups);
   const int nslices = (groups + kSlice - 1) / kSlice;
@@ -278,7 +278,6 @@ __device__ __forceinline__ uint32_t slice_next_op(const int2* rng, uint32_t k, u
 template <bool F16, int OP, int U, int BT>
 __global__ void __launch_bounds__(BT) slice16_kernel(const __grid_constant__ PlanParams p) {
   extern __shared__ uint4 sm[];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   slice_prologue<BT>(p, sm);
   const PlanHeader h = *reinterpret_cast<const PlanHeader*>(sm);
   const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
@@ -286,6 +285,7 @@ __global__ void __launch_bounds__(BT) slice16_kernel(const __grid_constant__ Pla
   const int2* rng = reinterpret_cast<const int2*>(reinterpret_cast<const OperandRef*>(ops + h.nops) + h.nrefs);
   char* const* addr = reinterpret_cast<char* const*>(reinterpret_cast<void* const*>(sm + p.words) + p.nbases);
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // at most one grid ahead (plan_kernel)
   constexpr int kSlice = U * BT;
   const int groups = static_cast<int>(p.groups);
   const int nslices = (groups + kSlice - 1) / kSlice;

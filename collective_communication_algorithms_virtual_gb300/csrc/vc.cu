@@ -302,6 +302,7 @@ bool fill_params(P& p, const Step& st, size_t i, size_t j, const Bases& b, int64
   if (tiles < 0) return false;
   p.nops = static_cast<uint32_t>(j - i);
   p.rev = st.reverse ? 1 : 0;
+  p.late = 0;
   p.ntiles = static_cast<uint32_t>(tiles);
   *tiles_out = tiles;
   return true;
@@ -376,6 +377,7 @@ vc_status_t launch_typed(DeviceState* st, const Step& s, size_t i, size_t j, con
     }
   }
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, cap));
+  p.late = tiles < cap ? 1 : 0;  // the grid leaves room: the next grid only after this one's wait
   std::unique_lock<std::mutex> lk(g_trace_mu);
   const bool trace = trace_slot();
   if (!trace) lk.unlock();
