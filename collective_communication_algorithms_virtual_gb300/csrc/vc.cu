@@ -1131,14 +1131,17 @@ SliceKernel slice_kernel_for(int rmode, RedOp r) {
 }
 // The sliced form's launch shape, measured on 8 ranks (ring / DBT / RHD, 256 KiB
 // to 8 MiB per rank): 256-thread blocks; one group a thread while that takes
-// at most 64 blocks, else the fewest groups a thread (2, 4 or 8, whose loads
+// at most 256 blocks, else the fewest groups a thread (2, 4 or 8, whose loads
 // of a step a thread issues together) that take at most two blocks per SM.
-// Grids of more than 64 blocks of one group a thread were up to twice as
-// slow, and 512- or 1024-thread blocks slower at small sizes.  16-bit plans
-// stop at 4 groups a thread (8 elements each, fp32 sums: 128 registers for
-// bf16, two blocks per SM, 144 for fp16; 8 groups take 240).
+// One group a thread up to 256 blocks against up to 64: 512 KiB - 1 MiB per
+// rank 0.3-1 us faster, fp32 and bf16.  (Before a grid let the next one in
+// only after its wait, grids of more than 64 blocks of one group a thread
+// measured up to twice as slow.)  512- or 1024-thread blocks were slower at
+// small sizes.  16-bit plans stop at 4 groups a thread (8 elements each,
+// fp32 sums: 128 registers for bf16, two blocks per SM, 144 for fp16; 8
+// groups take 240).
 constexpr int kSliceBlock = 256;
-constexpr int kSliceSmallGrid = 64;
+constexpr int kSliceSmallGrid = 256;
 
 // A sliced plan (slice_kernel): one launch over the whole GPU, each thread
 // carrying its 16-byte group of every buffer through every step.
