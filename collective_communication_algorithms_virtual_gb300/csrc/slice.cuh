@@ -23,8 +23,9 @@ namespace dev {
 // the plan's order, the result stored to every destination.  Whatever a step
 // reads at a position was written there by an earlier step, by this same
 // thread, so program order is the step barrier and no thread reads what
-// another wrote (loads go to L2 with .cg; a thread's own earlier store to the
-// address is ordered before them).  Steps, operations, operands and every
+// another wrote (a thread's own earlier store to an address is ordered before
+// its later loads of it, whatever the cache path; see the loads below).
+// Steps, operations, operands and every
 // element's association are the plan's; only positions far apart run out of
 // step with each other, as when a ring is pipelined in slices.  The host
 // checks that every position has one place in each buffer; the positions
