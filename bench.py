@@ -396,6 +396,7 @@ def run_ours(args) -> int:
             out["sweep"] = sweep(vc, send, recv, stream)
             out["alpha_beta"] = alpha_beta_fit(
                 out["sweep"], auto=lambda M: vc.vc_select_algo("allreduce", N, M // 4, "f32")[0])
+            out["sweep_collectives"] = sweep_collectives(vc, send, recv, stream)
         if not args.no_configs:
             out["configs"] = other_configs(vc, dev, peaks)
 
@@ -411,7 +412,7 @@ def run_ours(args) -> int:
     return 0
 
 
-DETAIL_KEYS = ("per_algo", "sweep", "alpha_beta", "configs")
+DETAIL_KEYS = ("per_algo", "sweep", "alpha_beta", "sweep_collectives", "configs")
 FINAL_LINE_MAX = 2048
 
 
@@ -567,6 +568,62 @@ def sweep(vc, send, recv, stream):
                            "busbw_eager": nbytes * busbw_factor(N) / (ms_eager * 1e-3) / 1e9,
                            "steps": steps, "algorithmic_bytes": hbm,
                            "l2_resident": 2 * N * nbytes <= (129 << 20)})
+    return res
+
+
+# the other collectives' algorithms, and the busbw factor of the pages' table
+# tbl-model-algo-busbw-coef for each (latency-formula page): M is the bytes per
+# rank the table counts -- ReduceScatter's input, AllGather's output,
+# Broadcast's message, AllToAll's buffer
+COLL_SWEEP = {"reduce_scatter": ("ring", "fused"), "allgather": ("ring", "fused"),
+              "broadcast": ("binomial", "scatter_allgather", "pipe_chain", "pipe_tree", "fused"),
+              "alltoall": ("pairwise", "bruck", "ring", "fused")}
+COLL_SWEEP_SIZES = (4 << 10, 64 << 10, 1 << 20, 16 << 20, 256 << 20)
+
+
+def coll_busbw_factor(coll: str, N: int) -> float:
+    return 1.0 if coll == "broadcast" else (N - 1) / N
+
+
+def sweep_collectives(vc, send, recv, stream, sizes=COLL_SWEEP_SIZES):
+    """busbw versus message size for ReduceScatter, AllGather, Broadcast and
+    AllToAll, every algorithm, 8 ranks, fp32, graph-timed, on the bench's
+    buffers (sends, and the first output set)."""
+    N = len(send)
+    outs = recv[ALGOS[0]]
+    res = {}
+    for coll, algos in COLL_SWEEP.items():
+        for a in algos:
+            rows = []
+            for nbytes in sizes:
+                cnt = nbytes // 4
+                if cnt * 4 > send[0].numel() * 4 or cnt % N:
+                    continue
+                blk = cnt // N
+                if coll == "reduce_scatter":
+                    ins, o = [x[:cnt] for x in send], [y[:blk] for y in outs]
+                    fn = lambda: vc.vc_reduce_scatter(ins, o, algo=a)
+                    shape = plan_shape(vc, coll, a, N, blk)
+                elif coll == "allgather":
+                    ins, o = [x[:blk] for x in send], [y[:cnt] for y in outs]
+                    fn = lambda: vc.vc_allgather(ins, o, algo=a)
+                    shape = plan_shape(vc, coll, a, N, blk)
+                elif coll == "broadcast":
+                    src, o = send[0][:cnt], [y[:cnt] for y in outs]
+                    if a.startswith("pipe_"):
+                        fn = lambda: vc.vc_broadcast_pipelined(src, o, root=0, algo=a)
+                    else:
+                        fn = lambda: vc.vc_broadcast(src, o, root=0, algo=a)
+                    shape = plan_shape(vc, coll, a, N, cnt)
+                else:
+                    ins, o = [x[:cnt] for x in send], [y[:cnt] for y in outs]
+                    fn = lambda: vc.vc_alltoall(ins, o, algo=a)
+                    shape = plan_shape(vc, coll, a, N, blk)
+                ms = time_graph(fn, stream)
+                rows.append({"bytes_per_rank": nbytes, "us": ms * 1e3,
+                             "busbw": nbytes * coll_busbw_factor(coll, N) / (ms * 1e-3) / 1e9,
+                             "algorithmic_bytes": shape[0], "steps": shape[1]})
+            res[f"{coll}_{a}"] = rows
     return res
 
 

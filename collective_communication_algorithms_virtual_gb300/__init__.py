@@ -34,6 +34,7 @@ from .binding import (  # noqa: F401
     vc_device_errors,
     vc_copy_selftest,
     SINGLE_LAUNCH_ALWAYS,
+    VC_SINGLE_LAUNCH_DEFAULT,
     vc_set_slice_limit,
     vc_set_merge_steps,
     vc_get_merge_steps,

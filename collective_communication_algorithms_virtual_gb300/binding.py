@@ -323,6 +323,7 @@ def vc_get_single_launch() -> int:
 
 
 SINGLE_LAUNCH_ALWAYS = (1 << 64) - 1
+VC_SINGLE_LAUNCH_DEFAULT = 768 << 10  # VC_SINGLE_LAUNCH_DEFAULT
 
 
 def vc_set_slice_limit(max_bytes_per_rank: int) -> None:

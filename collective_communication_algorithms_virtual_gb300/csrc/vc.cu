@@ -1440,8 +1440,13 @@ vc_status_t run(const Call& c) {
     if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;
     else dp = nullptr;
   }
+  // a plan whose steps all share one launch (step merging: Pairwise
+  // AllToAll's rounds) runs that launch, not a cluster with a barrier per step
+  // (8 ranks, 64 KiB per rank: 10.4 us as a cluster, 2-3 us as one launch)
+  const bool one_launch = !plan.launch_end.empty() && plan.launch_end[0] == plan.steps.size();
   const size_t limit = single_launch_limit();
-  if (!dp && aligned && limit > 0 && plan.steps.size() >= 2 && plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
+  if (!dp && !one_launch && aligned && limit > 0 && plan.steps.size() >= 2 &&
+      plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > limit)) dp = nullptr;
   }

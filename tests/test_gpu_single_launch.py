@@ -37,11 +37,15 @@ def _lib():
 
 @pytest.fixture(autouse=True)
 def _restore_limit():
-    old, old_slice = vc.vc_get_single_launch(), vc.vc_get_slice_limit()
-    vc.vc_set_slice_limit(0)  # the cluster form is the one under test here (the sliced form: test_gpu_sliced.py)
+    old, old_slice, old_merge = vc.vc_get_single_launch(), vc.vc_get_slice_limit(), vc.vc_get_merge_steps()
+    # the cluster form is the one under test here: not the sliced form (test_gpu_sliced.py), and not
+    # the one launch that a plan whose steps all merge takes instead (test_gpu_merge_steps.py)
+    vc.vc_set_slice_limit(0)
+    vc.vc_set_merge_steps(False)
     yield
     vc.vc_set_single_launch(old)
     vc.vc_set_slice_limit(old_slice)
+    vc.vc_set_merge_steps(old_merge)
 
 
 def _inputs(dtype, seed, N, n):
