@@ -43,8 +43,9 @@ int heap_depth(int i) {
 }
 int lowbit(int v) { return v & -v; }
 
-// 16-bit Ring AllReduce: while its fp32 partial sums take at most this many
-// bytes per rank, they keep one place per element (see allreduce_ring).
+// Ring AllReduce of 16-bit data and ring ReduceScatter: while their partial
+// sums take at most this many bytes per rank, they keep one place per element
+// (see allreduce_ring, reduce_scatter).
 constexpr int64_t kFlatPartialBytes = int64_t(16) << 20;
 int md(int a, int n) { return ((a % n) + n) % n; }
 bool is_pow2(int n) { return n >= 1 && (n & (n - 1)) == 0; }
@@ -366,18 +367,24 @@ class Builder {
     // Ring: the AllReduce ReduceScatter shifted by one block so that rank r
     // ends with block r (block ownership is left open by the pages): at step s
     // rank r adds block (r-s-2) mod N from rank r-1.  Partials travel through
-    // two scratch slots per rank (step s writes slot s%2).
+    // scratch: while they take at most kFlatPartialBytes per rank, one buffer
+    // of N blocks per rank, block c at its own place (every scratch byte then
+    // belongs to one element of the input, which the sliced form needs);
+    // above that two block slots per rank (step s writes slot s%2).
     std::vector<int64_t> slot0(N_);
     const DT adt = acc_dt();
-    for (int r = 0; r < N_; ++r) slot0[r] = alloc(2 * rc * esize(adt));
-    auto part = [&](int r, int s) { return Sc(r, slot0[r] + (s & 1) * rc * esize(adt), adt); };
+    const bool flat = !a_.compact_partials && int64_t(N_) * rc * esize(adt) <= kFlatPartialBytes;
+    for (int r = 0; r < N_; ++r) slot0[r] = alloc((flat ? N_ : 2) * rc * esize(adt));
+    auto part = [&](int r, int s, int c) {
+      return Sc(r, slot0[r] + (flat ? c : (s & 1)) * rc * esize(adt), adt);
+    };
     for (int s = 0; s < N_ - 1; ++s) {
       const size_t st = new_step(reduce_mode());
       for (int r = 0; r < N_; ++r) {
         const int c = md(r - s - 2, N_), left = md(r - 1, N_);
-        const Operand in = s == 0 ? S(left, c * rc) : part(left, s - 1);
-        const Operand out = s == N_ - 2 ? R(r, 0) : part(r, s);
-        add(st, {S(r, c * rc), in}, {out}, rc);
+        const Operand in = s == 0 ? S(left, c * rc) : part(left, s - 1, c);
+        const Operand out = s == N_ - 2 ? R(r, 0) : part(r, s, c);
+        add(st, {S(r, c * rc), in}, {out}, rc, c * rc);  // positions: the input's elements
       }
     }
   }
@@ -400,10 +407,10 @@ class Builder {
     for (int s = 0; s < N_ - 1; ++s) {
       const size_t st = new_step(Mode::Copy);
       if (s == 0)
-        for (int r = 0; r < N_; ++r) copy(st, S(r, 0), R(r, r * sc), sc);
+        for (int r = 0; r < N_; ++r) copy(st, S(r, 0), R(r, r * sc), sc, r * sc);
       for (int r = 0; r < N_; ++r) {
         const int c = md(r - s - 1, N_), left = md(r - 1, N_);
-        copy(st, s == 0 ? S(left, 0) : R(left, c * sc), R(r, c * sc), sc);
+        copy(st, s == 0 ? S(left, 0) : R(left, c * sc), R(r, c * sc), sc, c * sc);  // positions: the output's elements
       }
     }
   }
@@ -433,9 +440,9 @@ class Builder {
       for (int s = 0; s < L; ++s) {
         const int d = 1 << (L - 1 - s);
         const size_t st = new_step(Mode::Copy);
-        if (s == 0 && !a_.inplace) copy(st, S(root, 0), R(root, 0), count);
+        if (s == 0 && !a_.inplace) copy(st, S(root, 0), R(root, 0), count, 0);
         for (int v = 0; v + d < N_; v += 2 * d)
-          copy(st, v == 0 ? S(root, 0) : R(absr(v), 0), R(absr(v + d), 0), count);
+          copy(st, v == 0 ? S(root, 0) : R(absr(v), 0), R(absr(v + d), 0), count, 0);
       }
       return;
     }
@@ -475,18 +482,19 @@ class Builder {
     const int nsteps = chain ? N_ + k - 2 : L + k - 1;
     for (int t = 0; t < nsteps; ++t) {
       const size_t st = new_step(Mode::Copy);
-      if (t == 0 && !a_.inplace) copy(st, S(root, 0), R(root, 0), count_all());
+      if (t == 0 && !a_.inplace) copy(st, S(root, 0), R(root, 0), count_all(), 0);
       for (int j = 0; j < k; ++j) {
         const int s = t - j;
         if (chain) {
           if (s < 0 || s >= N_ - 1) continue;
           const int v = s;
-          copy(st, v == 0 ? S(root, ch.lo(j)) : R(absr(v), ch.lo(j)), R(absr(v + 1), ch.lo(j)), ch.len(j));
+          copy(st, v == 0 ? S(root, ch.lo(j)) : R(absr(v), ch.lo(j)), R(absr(v + 1), ch.lo(j)), ch.len(j), ch.lo(j));
         } else {
           if (s < 0 || s >= L) continue;
           const int d = 1 << (L - 1 - s);
           for (int v = 0; v + d < N_; v += 2 * d)
-            copy(st, v == 0 ? S(root, ch.lo(j)) : R(absr(v), ch.lo(j)), R(absr(v + d), ch.lo(j)), ch.len(j));
+            copy(st, v == 0 ? S(root, ch.lo(j)) : R(absr(v), ch.lo(j)), R(absr(v + d), ch.lo(j)), ch.len(j),
+                 ch.lo(j));
         }
       }
     }

@@ -44,9 +44,12 @@ struct Op {
   int64_t dstride = 0;  // bytes between runs, every destination
   bool keep = false;    // execution only: the next step reads the results (keep them in L2)
   uint32_t built = 0;   // introspection: the operation's index in its step as built
-  // Element position of the operation's first element, when every operand
-  // holds position i of the operation at element pos0 + i of the collective's
-  // buffers (the AllReduce schedules set it); -1 otherwise.
+  // Element position of the operation's first element: element i of the
+  // operation is position pos0 + i, and each operand holds the positions of
+  // its region of a buffer in order.  Positions are the elements of the
+  // message: AllReduce's buffer, ring ReduceScatter's input, ring
+  // AllGather's output, the binomial and pipelined Broadcasts' message.  -1:
+  // the operation does not keep positions.
   int64_t pos0 = -1;
 };
 
@@ -76,6 +79,9 @@ struct PlanArgs {
   bool inplace = false;
   int nchunks = 1;  // pipelined Broadcasts: chunks of the message (>= 1)
   RedOp op = RedOp::Sum;
+  // ring ReduceScatter: partial sums in two block slots per rank even where
+  // one slot per block would fit (the entry point without allocation)
+  bool compact_partials = false;
 };
 
 enum class PlanStatus { Ok, Invalid, Unsupported };

@@ -107,8 +107,9 @@ __device__ __forceinline__ char* slice_addr(const OperandRef& r, const void* con
 
 // Shared memory of a block: the plan description (16-byte words), the call's
 // buffer bases, then two tables: each operation's element range [e0, e1)
-// and each operand's address (base + offset).  (16-bit plans take the ranges
-// as part of the description: the same size, up to 8 bytes.)  Every buffer
+// and each operand's address (base + offset).  (Kernels that take the ranges
+// the host lists read them as part of the description: the same size, up to
+// 8 bytes.)  Every buffer
 // of a sliced call holds fewer than 2^29 elements (checked on the host), so
 // element and byte offsets within it fit 32 bits.
 __host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t nbases, uint32_t nops,
@@ -117,8 +118,12 @@ __host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t n
 }
 
 // BT threads a block; U groups a thread, BT apart (slices of U * BT groups);
-// the loads of a thread's groups in a step are issued together.
-template <int RMODE, int OP, int U, int BT>
+// the loads of a thread's groups in a step are issued together.  HR: the
+// operations' element ranges are the ones the host lists after the
+// description (positions counted within a block: ring ReduceScatter and
+// AllGather); otherwise each is derived from its first operand's offset
+// (absolute positions: AllReduce, Broadcast).
+template <int RMODE, int OP, int U, int BT, bool HR>
 __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanParams p) {
   static_assert(RMODE == kF32 || RMODE == kI32, "4-byte sliced plans are fp32 or int32");
   extern __shared__ uint4 sm[];
@@ -130,12 +135,19 @@ __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanP
   const PlanStep* steps = reinterpret_cast<const PlanStep*>(sm + 1);
   const OpDesc* ops = reinterpret_cast<const OpDesc*>(sm + 1 + h.nsteps);
   const OperandRef* refs = reinterpret_cast<const OperandRef*>(ops + h.nops);
-  int2* rng = reinterpret_cast<int2*>(sbase + p.nbases);             // per operation: e0, e1
-  char** addr = reinterpret_cast<char**>(rng + h.nops);              // per operand: its address
-  // 4-byte plans keep every operand in a send or receive buffer at byte 4 e0
-  for (uint32_t i = threadIdx.x; i < h.nops; i += BT) {
-    const int e0 = static_cast<int>(refs[ops[i].p0].off >> 2);
-    rng[i] = make_int2(e0, e0 + static_cast<int>(ops[i].n));
+  int2* rng;    // per operation: e0, e1
+  char** addr;  // per operand: its address
+  if constexpr (HR) {
+    rng = const_cast<int2*>(reinterpret_cast<const int2*>(refs + h.nrefs));
+    addr = reinterpret_cast<char**>(const_cast<void**>(sbase + p.nbases));
+  } else {
+    rng = reinterpret_cast<int2*>(sbase + p.nbases);
+    addr = reinterpret_cast<char**>(rng + h.nops);
+    // absolute positions: every operand in a send or receive buffer at byte 4 e0
+    for (uint32_t i = threadIdx.x; i < h.nops; i += BT) {
+      const int e0 = static_cast<int>(refs[ops[i].p0].off >> 2);
+      rng[i] = make_int2(e0, e0 + static_cast<int>(ops[i].n));
+    }
   }
   for (uint32_t i = threadIdx.x; i < h.nrefs; i += BT)
     addr[i] = slice_addr(refs[i], sbase, (p.nbases - 1) / 2);

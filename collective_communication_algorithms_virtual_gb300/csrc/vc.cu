@@ -576,16 +576,17 @@ vc_status_t resolve_auto(PlanArgs* pa) {
 struct PlanKey {
   int coll, algo, nranks, dt, root, inplace, nchunks, op;
   int64_t count;
+  int compact;
   bool operator==(const PlanKey& o) const {
     return coll == o.coll && algo == o.algo && nranks == o.nranks && dt == o.dt && root == o.root &&
-           inplace == o.inplace && nchunks == o.nchunks && op == o.op && count == o.count;
+           inplace == o.inplace && nchunks == o.nchunks && op == o.op && count == o.count && compact == o.compact;
   }
 };
 struct PlanKeyHash {
   size_t operator()(const PlanKey& k) const {
     uint64_t h = 1469598103934665603ull;
     for (int64_t v : {int64_t(k.coll), int64_t(k.algo), int64_t(k.nranks), int64_t(k.dt), int64_t(k.root),
-                      int64_t(k.inplace), int64_t(k.nchunks), int64_t(k.op), k.count})
+                      int64_t(k.inplace), int64_t(k.nchunks), int64_t(k.op), k.count, int64_t(k.compact)})
       h = (h ^ static_cast<uint64_t>(v)) * 1099511628211ull;
     return static_cast<size_t>(h);
   }
@@ -595,7 +596,8 @@ std::unordered_map<PlanKey, std::shared_ptr<const Plan>, PlanKeyHash> g_plans;
 
 PlanKey plan_key(const PlanArgs& pa) {
   return PlanKey{static_cast<int>(pa.coll), static_cast<int>(pa.algo), pa.nranks, static_cast<int>(pa.dt),
-                 pa.root, pa.inplace ? 1 : 0, pa.nchunks, static_cast<int>(pa.op), pa.count};
+                 pa.root, pa.inplace ? 1 : 0, pa.nchunks, static_cast<int>(pa.op), pa.count,
+                 pa.compact_partials ? 1 : 0};
 }
 
 // Orders each step for reuse of what the previous step wrote while it is
@@ -792,7 +794,10 @@ struct DevPlan {
   int nops = 0;
   bool sliced = false;           // every operation keeps element positions: the sliced form applies
   uint32_t nrefs = 0;
-  uint32_t slice_words = 0;      // the description with the operations' element ranges (16-bit sliced form)
+  uint32_t slice_words = 0;      // the description with the operations' element ranges
+  int slice_es = 0;              // sliced form: bytes of the data type
+  bool slice_host_ranges = false;  // the kernel takes the ranges the host lists (else derives them)
+  int64_t slice_positions = 0;   // element positions the sliced plan covers
 };
 struct PlanStore {
   std::unordered_map<PlanKey, DevPlan, PlanKeyHash> plans;
@@ -886,37 +891,58 @@ struct Written {
 
 // The sliced form (slice_kernel, slice16_kernel) applies to a plan whose
 // every operation keeps element positions: operation element i is position
-// pos0 + i of the collective's buffers, one run, a copy from one source.
-// Position e lives at byte e * size of a send or receive buffer (of the data
-// type), and at byte origin + 4 e of an fp32 partial-sum region of scratch
-// (16-bit data, 32-byte aligned), where the regions whose bytes overlap
-// share one origin.  Then each byte any operation touches belongs to one
-// position, and with groups and operations starting on 16-byte boundaries a
-// thread that owns a group of positions owns every byte of them.  Send
-// buffers are only read, and every byte of a receive buffer or of scratch
-// that a step reads was written by an earlier step -- by the thread that
-// owns it, which therefore reads it through L1.  Positions stay below 2^29
-// (checked per call), so the kernels' 32-bit element offsets hold.
-bool sliceable(const Plan& plan, int rmode) {
-  int es;
+// pos0 + i, one run, a copy from one source.  Each operand holds the
+// positions of its region of a buffer in order: position e at byte
+// origin + e * size, where origin = offset - pos0 * size.  Regions of one
+// buffer whose bytes overlap share one origin and size, so each byte any
+// operation touches belongs to one position; with groups and origins on
+// 16-byte boundaries (32 for the fp32 partial sums of 16-bit data, accessed
+// 32 bytes at a time) a thread that owns a group of positions owns every byte
+// of them.  Send and receive buffers hold the data type; scratch holds it too,
+// or fp32 partial sums of 16-bit reductions.  Send buffers are only read, and
+// every byte of a receive buffer or of scratch that a step reads was written
+// by an earlier step -- by the thread that owns it, which therefore reads it
+// through L1.  Positions stay below 2^29, so the kernels' 32-bit element
+// offsets hold.  AllReduce and Broadcast positions are absolute (every send
+// and receive region has origin 0, so a 4-byte kernel can derive each
+// operation's range from its first operand); the ring ReduceScatter and
+// AllGather count them within a block.
+struct SliceShape {
+  int es = 0;              // bytes of the data type
+  bool absolute = true;    // every send / receive region has origin 0
+  int64_t positions = 0;   // positions the plan covers
+};
+bool sliceable(const Plan& plan, int rmode, SliceShape* sh) {
+  int es = 0;
   if (rmode == dev::kF32 || rmode == dev::kI32) es = 4;
   else if (rmode == dev::kBF16 || rmode == dev::kF16) es = 2;
-  else return false;
+  else if (rmode == dev::kCopy && !plan.steps.empty() && !plan.steps[0].ops.empty())
+    es = esize(plan.steps[0].ops[0].src[0].dt);  // copies only: the data type of any operand
+  if (es != 2 && es != 4) return false;
   const int64_t gelems = 16 / es;
   struct Region {
     int64_t lo, hi, origin;
+    int size;
   };
-  std::vector<Region> regions;
+  std::map<std::pair<int, int>, std::vector<Region>> regions;  // (buffer kind, owner) -> regions
+  auto key = [](const Operand& o) {
+    return std::make_pair(static_cast<int>(o.buf), o.buf == Buf::Scratch ? 0 : o.owner);
+  };
+  bool absolute = true;
+  int64_t positions = 0;
   for (const Step& st : plan.steps)
     for (const Op& op : st.ops) {
       if (op.pos0 < 0 || op.nb != 1 || op.pos0 % gelems != 0 || op.pos0 + op.n > (int64_t(1) << 29)) return false;
       if (st.mode == Mode::Copy && op.src.size() != 1) return false;
+      positions = std::max(positions, op.pos0 + op.n);
       auto fits = [&](const Operand& o) {
-        if (o.buf != Buf::Scratch) return esize(o.dt) == es && o.byte_off == op.pos0 * es;
-        if (es != 2 || o.dt != DT::F32 || st.mode == Mode::Copy) return false;
-        const int64_t origin = o.byte_off - op.pos0 * 4;
-        if (origin % 32 != 0) return false;
-        regions.push_back({o.byte_off, o.byte_off + op.n * 4, origin});
+        const int z = esize(o.dt);
+        const bool partial = es == 2 && o.dt == DT::F32 && o.buf == Buf::Scratch && st.mode != Mode::Copy;
+        if (z != es && !partial) return false;
+        const int64_t origin = o.byte_off - op.pos0 * z;
+        if (origin % (partial ? 32 : 16) != 0) return false;
+        if (o.buf != Buf::Scratch) absolute = absolute && origin == 0;
+        regions[key(o)].push_back({o.byte_off, o.byte_off + op.n * z, origin, z});
         return true;
       };
       for (const Operand& o : op.src)
@@ -925,10 +951,7 @@ bool sliceable(const Plan& plan, int rmode) {
         if (o.buf == Buf::Send || !fits(o)) return false;
     }
   // receive buffers and scratch: written before read, step by step
-  std::map<std::pair<int, int>, Written> written;  // (buffer kind, owner)
-  auto key = [](const Operand& o) {
-    return std::make_pair(static_cast<int>(o.buf), o.buf == Buf::Scratch ? 0 : o.owner);
-  };
+  std::map<std::pair<int, int>, Written> written;
   for (const Step& st : plan.steps) {
     for (const Op& op : st.ops)
       for (const Operand& o : op.src) {
@@ -939,13 +962,23 @@ bool sliceable(const Plan& plan, int rmode) {
     for (const Op& op : st.ops)
       for (const Operand& o : op.dst) written[key(o)].add(o.byte_off, o.byte_off + op.n * esize(o.dt));
   }
-  std::sort(regions.begin(), regions.end(), [](const Region& a, const Region& b) { return a.lo < b.lo; });
-  int64_t reach = INT64_MIN, origin = 0;  // furthest byte of the regions so far, and their origin
-  for (const Region& g : regions) {
-    if (g.lo < reach && g.origin != origin) return false;
-    if (g.lo >= reach) origin = g.origin;
-    reach = std::max(reach, g.hi);
+  for (auto& kv : regions) {
+    std::vector<Region>& rs = kv.second;
+    std::sort(rs.begin(), rs.end(), [](const Region& x, const Region& y) { return x.lo < y.lo; });
+    int64_t reach = INT64_MIN, origin = 0;  // furthest byte of the regions so far, and their origin and size
+    int size = 0;
+    for (const Region& g : rs) {
+      if (g.lo < reach && (g.origin != origin || g.size != size)) return false;
+      if (g.lo >= reach) {
+        origin = g.origin;
+        size = g.size;
+      }
+      reach = std::max(reach, g.hi);
+    }
   }
+  sh->es = es;
+  sh->absolute = absolute;
+  sh->positions = positions;
   return true;
 }
 
@@ -1032,9 +1065,13 @@ void build_image(const Plan& plan, int N, int workers, std::vector<uint4>* img, 
   dp->nops = static_cast<int>(nops);
   dp->nrefs = static_cast<uint32_t>(nrefs);
   dp->eligible = true;
-  dp->sliced = sliceable(plan, dp->rmode) &&
+  SliceShape sh;
+  dp->sliced = sliceable(plan, dp->rmode, &sh) &&
                dev::slice_smem_bytes(dp->words, 2 * N + 1, static_cast<uint32_t>(nops + 1), static_cast<uint32_t>(nrefs)) <=
                    static_cast<size_t>(kPlanSmemMax);
+  dp->slice_es = sh.es;
+  dp->slice_host_ranges = sh.es == 2 || !sh.absolute;
+  dp->slice_positions = sh.positions;
   if (dp->sliced) {  // after the description: the operations' element ranges [e0, e1), in listed order
     dp->slice_words = dp->words + static_cast<uint32_t>((nops + 1) / 2);
     img->resize(dp->slice_words, make_uint4(0, 0, 0, 0));
@@ -1100,12 +1137,12 @@ const DevPlan* resident_plan(int dev, const PlanKey& key, const Plan& plan, int 
 }
 
 using SliceKernel = void (*)(dev::PlanParams);
-template <int RMODE, int U, int BT>
+template <int RMODE, int U, int BT, bool HR>
 SliceKernel slice_kernel_op(RedOp r) {
   switch (r) {
-    case RedOp::Max: return dev::slice_kernel<RMODE, dev::kMax, U, BT>;
-    case RedOp::Min: return dev::slice_kernel<RMODE, dev::kMin, U, BT>;
-    default: return dev::slice_kernel<RMODE, dev::kSum, U, BT>;
+    case RedOp::Max: return dev::slice_kernel<RMODE, dev::kMax, U, BT, HR>;
+    case RedOp::Min: return dev::slice_kernel<RMODE, dev::kMin, U, BT, HR>;
+    default: return dev::slice_kernel<RMODE, dev::kSum, U, BT, HR>;
   }
 }
 template <bool F16, int U, int BT>
@@ -1116,18 +1153,22 @@ SliceKernel slice16_kernel_op(RedOp r) {
     default: return dev::slice16_kernel<F16, dev::kSum, U, BT>;
   }
 }
+// The kernel for a sliced plan: 16-bit data (reductions, or copies alone) the
+// 16-bit kernel; 4-byte data the 4-byte one, taking the host's ranges where
+// positions are not absolute.  Copy-only plans never combine, so any
+// reduction variant serves.
 template <int U, int BT>
-SliceKernel slice_kernel_for(int rmode, RedOp r) {
-  switch (rmode) {
-    case dev::kI32: return slice_kernel_op<dev::kI32, U, BT>(r);
-    case dev::kBF16:
-      if constexpr (U <= 4) return slice16_kernel_op<false, U, BT>(r);
-      return nullptr;
-    case dev::kF16:
-      if constexpr (U <= 4) return slice16_kernel_op<true, U, BT>(r);
-      return nullptr;
-    default: return slice_kernel_op<dev::kF32, U, BT>(r);
+SliceKernel slice_kernel_for(const DevPlan& dp) {
+  if (dp.slice_es == 2) {
+    if constexpr (U <= 4) return dp.rmode == dev::kF16 ? slice16_kernel_op<true, U, BT>(dp.red)
+                                                      : slice16_kernel_op<false, U, BT>(dp.red);
+    return nullptr;
   }
+  if (dp.rmode == dev::kI32)
+    return dp.slice_host_ranges ? slice_kernel_op<dev::kI32, U, BT, true>(dp.red)
+                                : slice_kernel_op<dev::kI32, U, BT, false>(dp.red);
+  return dp.slice_host_ranges ? slice_kernel_op<dev::kF32, U, BT, true>(dp.red)
+                              : slice_kernel_op<dev::kF32, U, BT, false>(dp.red);
 }
 // The sliced form's launch shape, measured on 8 ranks (ring / DBT / RHD, 256 KiB
 // to 8 MiB per rank): 256-thread blocks; one group a thread while that takes
@@ -1148,16 +1189,16 @@ constexpr int kSliceSmallGrid = 256;
 vc_status_t launch_sliced(const DevPlan& dp, DeviceState* st, const dev::PlanParams& prm, cudaStream_t stream,
                           const LaunchCtx& tc) {
   const int64_t g = prm.groups, per_block = kSliceBlock;
-  const int umax = (dp.rmode == dev::kBF16 || dp.rmode == dev::kF16) ? 4 : 8;
+  const int umax = dp.slice_es == 2 ? 4 : 8;
   int U = 1;
   if (g > int64_t(kSliceSmallGrid) * per_block) {
     U = 2;
     while (U < umax && g > int64_t(2) * st->nsm * per_block * U) U *= 2;
   }
-  const SliceKernel kernel = U == 1 ? slice_kernel_for<1, kSliceBlock>(dp.rmode, dp.red)
-                           : U == 2 ? slice_kernel_for<2, kSliceBlock>(dp.rmode, dp.red)
-                           : U == 4 ? slice_kernel_for<4, kSliceBlock>(dp.rmode, dp.red)
-                                    : slice_kernel_for<8, kSliceBlock>(dp.rmode, dp.red);
+  const SliceKernel kernel = U == 1 ? slice_kernel_for<1, kSliceBlock>(dp)
+                           : U == 2 ? slice_kernel_for<2, kSliceBlock>(dp)
+                           : U == 4 ? slice_kernel_for<4, kSliceBlock>(dp)
+                                    : slice_kernel_for<8, kSliceBlock>(dp);
   if (!kernel) return fail(VC_ERR_UNSUPPORTED, "no sliced kernel for this launch shape");
   // (16-bit: the ranges within the description, up to 8 bytes more than the table)
   const size_t smem = dev::slice_smem_bytes(dp.words, prm.nbases, dp.nops + 1, dp.nrefs);
@@ -1225,7 +1266,7 @@ vc_status_t launch_plan(const DevPlan& dp, int dev, int N, const std::vector<con
   prm.words = dp.words;
   prm.nbases = static_cast<uint32_t>(2 * N + 1);
   prm.groups = slice_groups;
-  if (slice_groups > 0 && (dp.rmode == dev::kBF16 || dp.rmode == dev::kF16)) prm.words = dp.slice_words;
+  if (slice_groups > 0 && dp.slice_host_ranges) prm.words = dp.slice_words;
   for (int r = 0; r < N; ++r) {
     prm.base[r] = sends[r];
     prm.base[N + r] = recvs[r];
@@ -1430,14 +1471,26 @@ vc_status_t run(const Call& c) {
     aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
                (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
   const size_t slim = slice_limit();
-  // the sliced form's size: the 4 bytes a thread carries through the steps
-  // per element (fp32 / int32 data, or the fp32 partial sums of 16-bit data)
-  // (16-bit sliced plans access their fp32 partials 32 bytes at a time)
-  if (aligned && slim > 0 && c.coll == Coll::AllReduce && plan.steps.size() >= 2 &&
+  // the sliced form's size per rank: AllReduce the 4 bytes a thread carries
+  // through the steps per element (fp32 / int32 data, or the fp32 partial
+  // sums of 16-bit data), ReduceScatter its input likewise, AllGather its
+  // output, Broadcast its message.  Not for in-place calls of the other
+  // collectives, whose send and receive buffers would hold positions at two
+  // places.  (16-bit sliced plans access their fp32 partials 32 bytes at a
+  // time.)
+  int64_t slice_bytes = -1;
+  switch (c.coll) {
+    case Coll::AllReduce: slice_bytes = c.count * 4; break;
+    case Coll::ReduceScatter: slice_bytes = pa.inplace ? -1 : c.count * N * 4; break;
+    case Coll::AllGather: slice_bytes = pa.inplace ? -1 : c.count * N * es; break;
+    case Coll::Broadcast: slice_bytes = pa.inplace ? -1 : c.count * es; break;
+    default: break;
+  }
+  if (aligned && slim > 0 && slice_bytes >= 0 && plan.steps.size() >= 2 &&
       (es == 4 || (reinterpret_cast<uintptr_t>(scratch) & 31) == 0) &&
-      c.count < (int64_t(1) << 29) && static_cast<uint64_t>(c.count * 4) <= std::min<uint64_t>(slim, INT64_MAX)) {
+      c.count < (int64_t(1) << 29) && static_cast<uint64_t>(slice_bytes) <= std::min<uint64_t>(slim, INT64_MAX)) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
-    if (dp && dp->eligible && dp->sliced) slice_groups = (c.count * es + 15) / 16;
+    if (dp && dp->eligible && dp->sliced) slice_groups = (dp->slice_positions * es + 15) / 16;
     else dp = nullptr;
   }
   // a plan whose steps all share one launch (step merging: Pairwise
@@ -1934,8 +1987,11 @@ vc_status_t run_reduce_scatter_noalloc(const void* const* send, void* const* rec
       if (overlap(recv[i], rbytes, send[q], sbytes))
         return fail(VC_ERR_INVALID_ARG, "a receive buffer overlaps a send buffer");
   }
-  // the same cached plan, in the same execution order, as the allocating call
+  // the allocating call's steps, operations and execution order, with the
+  // partial sums in two block slots per rank (the allocating call keeps one
+  // slot per block while they take at most 16 MiB per rank)
   PlanArgs pa{Coll::ReduceScatter, Algo::Ring, N, rc, dt, 0, false};
+  pa.compact_partials = true;
   std::shared_ptr<const Plan> plan_ptr;
   std::string why;
   const PlanStatus ps = cached_plan(pa, &plan_ptr, &why);

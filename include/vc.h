@@ -283,10 +283,12 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
  * run in one launch; steps run in order.
  *   buf: 0 send, 1 recv, 2 library scratch; owner: the rank that holds it;
  *   byte_off: from the start of that rank's buffer (scratch: of the scratch
- *   block); dtype: storage type of the operand; elem0: for AllReduce, the
- *   element position (index into the collective's buffers) of the
- *   operation's first element -- its element i combines position elem0 + i
- *   of every rank -- else -1.
+ *   block); dtype: storage type of the operand; elem0: the element position
+ *   of the operation's first element, where the schedule keeps positions --
+ *   its element i is position elem0 + i, held in order by each operand's
+ *   region.  Positions are the elements of the message: AllReduce's buffer,
+ *   ring ReduceScatter's input, ring AllGather's output, the binomial and
+ *   pipelined Broadcasts' message.  Else -1.
  * Returns VC_ERR_INVALID_ARG if `capacity` is too small (with *n_entries set
  * to the size needed).  *scratch_bytes receives the scratch the call needs,
  * *n_steps the number of steps.
@@ -304,7 +306,7 @@ typedef struct {
   int64_t n;
   int64_t nb;
   int64_t stride_bytes;
-  int64_t elem0;  /* AllReduce: element position of the first element; else -1 */
+  int64_t elem0;  /* element position of the first element, or -1 (above) */
 } vc_plan_entry_t;
 
 vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count,
@@ -522,7 +524,8 @@ vc_status_t vc_copy_selftest(vc_stream_t stream, uint32_t* flags);
  * computes (same schedule and execution order, same results bit for bit),
  * but its partial sums live in one fixed array that the library places in
  * each GPU's memory when its device code is loaded there, instead of in the
- * library's pool.
+ * library's pool, in two block slots per rank (the allocating call keeps one
+ * slot per block while they take at most 16 MiB per rank).
  *
  *   op: VC_SUM only; VC_MAX and VC_MIN return VC_ERR_UNSUPPORTED.
  *   dtype: VC_FLOAT32, VC_BFLOAT16, VC_FLOAT16 or VC_INT32.

@@ -1,4 +1,5 @@
-"""The sliced form of AllReduce schedules, against the oracle.
+"""The sliced form of AllReduce, ReduceScatter, AllGather and Broadcast
+schedules, against the oracle.
 
 In the sliced form (vc_set_slice_limit) one launch over the whole GPU runs
 every step of the plan, each thread carrying its 16-byte group of every rank
@@ -149,6 +150,75 @@ def test_sliced_16bit_at_8_mib():
         assert same_bits(got, want), (algo, first_diff(got, want))
 
 
+def _rs_ag_counts(dtype):
+    G = 16 // {"f32": 4, "i32": 4, "bf16": 2, "f16": 2}[dtype]
+    # whole groups a block (sliced), and a block of 5 elements, whose blocks are
+    # not 16-byte aligned in the send buffer (the other forms)
+    return ((G, True), (64 * G + G, True), (4096, True), (5, False))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
+@pytest.mark.parametrize("N", [2, 3, 5, 8, 16])
+def test_sliced_reduce_scatter_allgather(N, dtype):
+    """Ring ReduceScatter and AllGather: positions counted within a block."""
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    for rc, aligned in _rs_ag_counts(dtype):
+        sliced = aligned and N > 2  # at 2 ranks the ring is one step
+        xs = _inputs(dtype, 8800 + N + rc, N, N * rc)
+        want = cxx.reduce_scatter(xs, "ring", dtype, want_log=False).outputs
+        sends = [Guarded(N * rc, dtype, fill=x) for x in xs]
+        recvs = [Guarded(rc, dtype) for _ in range(N)]
+        recs = _traced(lambda: vc.vc_reduce_scatter([g.t for g in sends], [g.t for g in recvs], algo="ring"))
+        assert (len(recs) == 1 and recs[0]["kernel"].endswith("_sliced")) == sliced, ("rs", N, rc, recs)
+        assert all(g.guards_intact() for g in sends + recvs)
+        for r in range(N):
+            got = recvs[r].host()
+            assert same_bits(got, want[r]), ("rs", N, dtype, rc, r, first_diff(got, want[r]))
+        ins = _inputs(dtype, 8900 + N + rc, N, rc)
+        want = cxx.allgather(ins, "ring", dtype, want_log=False).outputs
+        sends = [Guarded(rc, dtype, fill=x) for x in ins]
+        recvs = [Guarded(N * rc, dtype) for _ in range(N)]
+        recs = _traced(lambda: vc.vc_allgather([g.t for g in sends], [g.t for g in recvs], algo="ring"))
+        assert (len(recs) == 1 and recs[0]["kernel"].endswith("_sliced")) == sliced, ("ag", N, rc, recs)
+        assert all(g.guards_intact() for g in sends + recvs)
+        for r in range(N):
+            got = recvs[r].host()
+            assert same_bits(got, want[r]), ("ag", N, dtype, rc, r, first_diff(got, want[r]))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [2, 3, 5, 8, 16])
+def test_sliced_broadcast(N, dtype):
+    """Binomial and pipelined Broadcasts (absolute positions), every root:
+    every rank ends with the root's message, bit for bit; in place at the
+    root takes the other forms."""
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    for count in (1, 1000 + 3, 65536 + 5):
+        A = _inputs(dtype, 9000 + N + count, 1, count)[0]
+        for root in sorted({0, N // 2, N - 1}):
+            for algo, k in (("binomial", 0), ("pipe_chain", 4), ("pipe_tree", 3), ("pipe_chain", 0)):
+                for inplace in (False, True):
+                    recvs = [Guarded(count, dtype) for _ in range(N)]
+                    if inplace:
+                        recvs[root].t.copy_(to_dev(A))
+                        src = recvs[root].t
+                    else:
+                        src = to_dev(A)
+                    if algo.startswith("pipe"):
+                        fn = lambda: vc.vc_broadcast_pipelined(src, [g.t for g in recvs], root=root, algo=algo,
+                                                               nchunks=k)
+                    else:
+                        fn = lambda: vc.vc_broadcast(src, [g.t for g in recvs], root=root, algo=algo)
+                    recs = _traced(fn)
+                    steps = vc.vc_plan_describe("broadcast", algo, N, count, dtype, root, inplace, k)[2]
+                    sliced = steps >= 2 and not inplace
+                    assert (len(recs) == 1 and recs[0]["kernel"].endswith("_sliced")) == sliced, (
+                        algo, k, N, count, root, inplace, recs)
+                    assert all(g.guards_intact() for g in recvs)
+                    for r in range(N):
+                        assert same_bits(recvs[r].host(), A), (algo, k, N, count, root, inplace, r)
+
+
 def test_calls_that_do_not_qualify_take_other_forms():
     vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
     # a 16-bit Ring with more than 16 MiB of fp32 partials per rank: they
@@ -169,12 +239,17 @@ def test_calls_that_do_not_qualify_take_other_forms():
         got, recs = _run(xs, algo, "f32", shift=1 if algo == "ring" else 0)
         assert not any(r["kernel"].endswith("_sliced") for r in recs), (algo, recs)
         assert all(same_bits(got[r], want[r]) for r in range(N)), algo
-    # another collective with 4-byte data: a binomial Broadcast
+    # a Broadcast whose Scatter stages subtrees in scratch, and a binomial Scatter
     A = np.arange(count, dtype=np.int32)
     outs = [torch.empty(count, dtype=torch.int32, device="cuda") for _ in range(N)]
-    recs = _traced(lambda: vc.vc_broadcast(to_dev(A), outs, root=0, algo="binomial"))
+    recs = _traced(lambda: vc.vc_broadcast(to_dev(A), outs, root=0, algo="scatter_allgather"))
     assert not any(r["kernel"].endswith("_sliced") for r in recs), recs
     assert all(np.array_equal(to_host(o), A) for o in outs)
+    B = np.arange(N * 1024, dtype=np.int32)
+    outs = [torch.empty(1024, dtype=torch.int32, device="cuda") for _ in range(N)]
+    recs = _traced(lambda: vc.vc_scatter(to_dev(B), outs, root=0, algo="binomial"))
+    assert not any(r["kernel"].endswith("_sliced") for r in recs), recs
+    assert all(np.array_equal(to_host(outs[r]), B[r * 1024:(r + 1) * 1024]) for r in range(N))
 
 
 def test_default_limit():

@@ -173,3 +173,72 @@ def test_ring_partials_above_16_mib_alternate(dtype):
         ce = ((count + N - 1) // N + 7) // 8 * 8
         per_rank = count * 4 if count <= limit else 2 * ce * 4
         assert scratch == N * ((per_rank + 255) // 256 * 256), (N, count, scratch)
+
+
+# ---- the other collectives whose schedules keep positions ---------------------------------
+# Positions are the elements of the message: the ring ReduceScatter's input
+# (its partial sums keep one slot per block while they take at most 16 MiB per
+# rank), the ring AllGather's output, the binomial and pipelined Broadcasts'
+# message.
+
+def _rs_ag_bcast_cases(N, dtype):
+    G = _group(dtype)
+    rc = 8 * G + (G if dtype != "bf16" else 0)  # whole groups a block; every block 16-byte aligned
+    xs = _inputs(dtype, 1300 + N, N, N * rc)
+    yield ("reduce_scatter", "ring", rc, 0, 0,
+           lambda: schedules.reduce_scatter(xs, "ring", dtype).outputs, xs, [rc * ESZ[DT[dtype]]] * N, N * rc)
+    ins = _inputs(dtype, 1400 + N, N, rc)
+    yield ("allgather", "ring", rc, 0, 0,
+           lambda: schedules.allgather(ins, "ring", dtype).outputs, ins, [N * rc * ESZ[DT[dtype]]] * N, N * rc)
+    count = 1000 + 3
+    A = _inputs(dtype, 1500 + N, 1, count)[0]
+    for root in (0, N - 1):
+        send = [None] * N
+        send[root] = A
+        for algo, k in (("binomial", 0), ("pipe_chain", 5), ("pipe_tree", 3)):
+            if k:
+                want = lambda root=root, algo=algo, k=k: schedules.broadcast_pipelined(A, N, root, algo, dtype, k).outputs
+            else:
+                want = lambda root=root, algo=algo: schedules.broadcast(A, N, root, algo, dtype).outputs
+            yield ("broadcast", algo, count, root, k, want, send, [count * ESZ[DT[dtype]]] * N, count)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("N", [2, 3, 5, 8])
+def test_other_collective_plans_keep_positions_and_run_group_by_group(N, dtype):
+    G = _group(dtype)
+    rng = np.random.default_rng(31 + N)
+    for coll, algo, count, root, k, want_fn, send, recv_bytes, positions in _rs_ag_bcast_cases(N, dtype):
+        plan, scratch = get_plan(coll, algo, N, count, dtype, root=root, nchunks=k)
+        mem = Memory(send, recv_bytes, scratch)
+        assert not position_places(plan, mem, G), (coll, algo, N, dtype, position_places(plan, mem, G)[:3])
+        assert not reads_before_writes(plan, mem), (coll, algo, N, dtype)
+        want = want_fn()
+        groups = (positions + G - 1) // G
+        for sched in (one_after_another(groups, len(plan)), shuffled(groups, len(plan), rng)):
+            mem = Memory(send, recv_bytes, scratch)
+            run_plan_sliced(plan, mem, positions, G, sched)
+            for r in range(N):
+                got = mem.recv[r].view(NPT[DT[dtype]])
+                assert _same(got, want[r]), (coll, algo, N, dtype, root, r)
+
+
+def test_scatter_allgather_broadcast_does_not_keep_positions():
+    """Its binomial Scatter stages subtrees in scratch: the library leaves it
+    to the other forms (an operation without elem0)."""
+    plan, _ = get_plan("broadcast", "scatter_allgather", 8, 4096, "f32")
+    assert any(op["elem0"] < 0 for ops in plan for op in ops)
+
+
+def test_reduce_scatter_partials_flat_up_to_16_mib():
+    """One partial slot per block and rank while the partials take at most
+    16 MiB per rank (positional), two above (not); the scratch sizes say so."""
+    N = 8
+    for dtype, acc in (("f32", 4), ("bf16", 4)):
+        limit = (16 << 20) // (N * acc)  # block size at which N blocks of partials take 16 MiB
+        for rc, flat in ((limit, True), (limit + 8, False)):
+            plan, scratch = get_plan("reduce_scatter", "ring", N, rc, dtype)
+            mem = Memory([None] * N, [0] * N, scratch)
+            assert (not position_places(plan, mem, _group(dtype))) == flat, (dtype, rc)
+            per_rank = (N if flat else 2) * rc * acc
+            assert scratch == N * ((per_rank + 255) // 256 * 256), (dtype, rc, scratch)
