@@ -412,32 +412,39 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * Sliced execution (a form of single-launch execution, tried before the
  * cluster form).
  *
- * In the AllReduce schedules (Ring, RHD, DBT, Mesh, RING_HOP) every
- * operation maps element position e of each source to position e of each
- * destination, and each buffer holds position e at one place: element e of
- * every rank's send and receive buffer and, for bf16 / fp16 data, element e
- * of the fp32 partial sums the schedule keeps in scratch.  An AllReduce call
- * of such a schedule whose fp32 / int32 data, or fp32 partial sums of 16-bit
- * data, take at most `max_bytes_per_rank` per rank (4 bytes per element in
- * either case) runs all its steps in one launch over the whole GPU: each
- * thread owns one group of positions (16 bytes of the data type) of every
- * buffer and carries it through every step of the plan in order, applying
- * each operation that covers it.  What a step reads at a position was written
- * there by an earlier step, by the same thread, so the thread's program order
- * is the step barrier and no thread reads what another wrote.  The steps,
- * operations, operands and every element's association (16-bit data:
- * widened, combined in fp32, rounded once) are unchanged, so results are
- * identical bit for bit; different positions merely run out of step with
- * each other, as when a ring is pipelined in slices.  The 16-bit Ring keeps
- * one fp32 partial per element while they take at most 16 MiB per rank;
- * above that it alternates two chunk-sized slots per rank, which several
- * positions share, and does not run sliced at 5 ranks or more.  The
+ * In the AllReduce schedules (Ring, RHD, DBT, Mesh, RING_HOP), the ring
+ * ReduceScatter and AllGather and the binomial and pipelined Broadcasts,
+ * every operation maps element position e of each source to position e of
+ * each destination, where positions are the elements of the message
+ * (AllReduce's buffer, ReduceScatter's input, AllGather's output, the
+ * Broadcast message), and each buffer region holds its positions in order at
+ * one place: the send and receive buffers and the partial sums the schedule
+ * keeps in scratch (fp32 for bf16 / fp16 data).  A call of such a schedule
+ * runs all its steps in one launch over the whole GPU when, per rank, it
+ * carries at most `max_bytes_per_rank`: AllReduce 4 bytes per element (the
+ * fp32 / int32 data, or the fp32 partials of 16-bit data), ReduceScatter 4
+ * bytes per input element likewise, AllGather its output, Broadcast its
+ * message.  Each thread owns one group of positions (16 bytes of the data
+ * type) of every buffer and carries it through every step of the plan in
+ * order, applying each operation that covers it.  What a step reads at a
+ * position was written there by an earlier step, by the same thread, so the
+ * thread's program order is the step barrier and no thread reads what
+ * another wrote.  The steps, operations, operands and every element's
+ * association (16-bit data: widened, combined in fp32, rounded once) are
+ * unchanged, so results are identical bit for bit; different positions
+ * merely run out of step with each other, as when a ring is pipelined in
+ * slices.  The 16-bit AllReduce Ring and the ReduceScatter ring keep one
+ * partial per element while the partials take at most 16 MiB per rank;
+ * above that they alternate two chunk-sized slots per rank, which several
+ * positions share, and do not run sliced at 5 ranks or more.  In-place
+ * ReduceScatter, AllGather and Broadcast calls, Scatter+AllGather
+ * Broadcasts and the other collectives take the other forms.  The
  * conditions of single-launch execution on alignment and the resident
  * description apply as well.  max_bytes_per_rank: 0 disables it, SIZE_MAX
  * applies it to every eligible call.  Default VC_SLICE_LIMIT_DEFAULT: up to
  * 16 MiB per rank the form measured faster than the cluster form and than
  * per-step launches (8 ranks, fp32 and bf16, GB300; above, the whole GPU's
- * bandwidth per step wins).  Process-wide.
+ * bandwidth per step wins for AllReduce).  Process-wide.
  */
 #define VC_SLICE_LIMIT_DEFAULT ((size_t)16 << 20)
 vc_status_t vc_set_slice_limit(size_t max_bytes_per_rank);
