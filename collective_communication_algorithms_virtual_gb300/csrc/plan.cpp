@@ -455,12 +455,12 @@ class Builder {
     auto clen = [&](int c) { return ch.len(c); };
     size_t first = plan_.steps.size();
     binomial_scatter(clo, clen, ch.ce, [&](int r) { return R(r, ch.lo(r)); });
-    if (!a_.inplace) copy(first, S(root, ch.lo(root)), R(root, ch.lo(root)), ch.len(root));
+    if (!a_.inplace) copy(first, S(root, ch.lo(root)), R(root, ch.lo(root)), ch.len(root), ch.lo(root));
     for (int s = 0; s < N_ - 1; ++s) {
       const size_t st = new_step(Mode::Copy);
       for (int r = 0; r < N_; ++r) {
         const int c = md(r - s - 1, N_);
-        copy(st, R(md(r - 1, N_), ch.lo(c)), R(r, ch.lo(c)), ch.len(c));
+        copy(st, R(md(r - 1, N_), ch.lo(c)), R(r, ch.lo(c)), ch.len(c), ch.lo(c));
       }
     }
   }
@@ -525,16 +525,16 @@ class Builder {
     for (int s = 0; s < L; ++s) {
       const int d = 1 << s;
       const size_t st = new_step(Mode::Copy);
-      if (s == 0) copy(st, S(root, 0), R(root, root * rc), rc);
+      if (s == 0) copy(st, S(root, 0), R(root, root * rc), rc, root * rc);  // positions: the root's output
       for (int u = 0; u + d < N_; u += 2 * d) {
         const int v = u + d, end = std::min(v + d, N_);
         auto dst = [&](int q) { return u == 0 ? R(root, absr(q) * rc) : stage_op(u, q); };
-        copy(st, S(absr(v), 0), dst(v), rc);
+        copy(st, S(absr(v), 0), dst(v), rc, absr(v) * rc);
         int q = v + 1;
         while (q < end) {  // runs contiguous at both ends (the root's buffer wraps past rank N-1)
           int q2 = q + 1;
           while (q2 < end && !(u == 0 && absr(q2) == 0)) ++q2;
-          copy(st, stage_op(v, q), dst(q), int64_t(q2 - q) * rc);
+          copy(st, stage_op(v, q), dst(q), int64_t(q2 - q) * rc, absr(q) * rc);
           q = q2;
         }
       }
@@ -576,7 +576,7 @@ class Builder {
         const Operand own = partial[u] ? P(u) : S(absr(u), 0);
         const Operand other = partial[v] ? P(v) : S(absr(v), 0);
         const bool last = u == 0 && s == L - 1;
-        add(st, {own, other}, {last ? R(root, 0) : P(u)}, count);
+        add(st, {own, other}, {last ? R(root, 0) : P(u)}, count, 0);
         partial[u] = true;
       }
     }
@@ -593,7 +593,7 @@ class Builder {
     }
     size_t first = plan_.steps.size();
     binomial_scatter([&](int c) { return c * rc; }, [&](int) { return rc; }, rc, [&](int r) { return R(r, 0); });
-    copy(first, S(root, root * rc), R(root, 0), rc);
+    copy(first, S(root, root * rc), R(root, 0), rc, root * rc);
   }
 
   // Binomial Scatter over absolute chunks [clo(c), clo(c)+clen(c)) of the
@@ -617,7 +617,7 @@ class Builder {
       const size_t st = new_step(Mode::Copy);
       for (int v = 0; v + d < N_; v += 2 * d) {
         const int w = v + d, end = std::min(v + 2 * d, N_);
-        copy(st, held(v, w), own_dst(absr(w)), clen(absr(w)));
+        copy(st, held(v, w), own_dst(absr(w)), clen(absr(w)), clo(absr(w)));  // positions: the root's buffer
         // the rest, in runs that stay contiguous in the root's buffer (split
         // where absolute chunk numbers wrap past N-1)
         int q = w + 1;
@@ -626,7 +626,7 @@ class Builder {
           while (q2 < end && absr(q2) != 0) ++q2;
           int64_t n = 0;
           for (int k = q; k < q2; ++k) n += clen(absr(k));
-          copy(st, held(v, q), stage_op(w, q), n);
+          copy(st, held(v, q), stage_op(w, q), n, clo(absr(q)));
           q = q2;
         }
       }

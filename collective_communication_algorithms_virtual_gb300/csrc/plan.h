@@ -47,9 +47,10 @@ struct Op {
   // Element position of the operation's first element: element i of the
   // operation is position pos0 + i, and each operand holds the positions of
   // its region of a buffer in order.  Positions are the elements of the
-  // message: AllReduce's buffer, ring ReduceScatter's input, ring
-  // AllGather's output, the binomial and pipelined Broadcasts' message.  -1:
-  // the operation does not keep positions.
+  // message: AllReduce's and the tree Reduce's buffer, ring ReduceScatter's
+  // input, ring AllGather's output, the Broadcasts' message (binomial,
+  // Scatter+AllGather, pipelined), the binomial Scatter's input and Gather's
+  // output at the root.  -1: the operation does not keep positions.
   int64_t pos0 = -1;
 };
 

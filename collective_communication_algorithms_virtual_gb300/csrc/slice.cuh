@@ -120,9 +120,9 @@ __host__ __device__ constexpr size_t slice_smem_bytes(uint32_t words, uint32_t n
 // BT threads a block; U groups a thread, BT apart (slices of U * BT groups);
 // the loads of a thread's groups in a step are issued together.  HR: the
 // operations' element ranges are the ones the host lists after the
-// description (positions counted within a block: ring ReduceScatter and
-// AllGather); otherwise each is derived from its first operand's offset
-// (absolute positions: AllReduce, Broadcast).
+// description; otherwise each is derived from its first operand's offset,
+// which the host allows only where every operand region has origin 0 (the
+// AllReduce schedules, the Broadcasts).
 template <int RMODE, int OP, int U, int BT, bool HR>
 __global__ void __launch_bounds__(BT) slice_kernel(const __grid_constant__ PlanParams p) {
   static_assert(RMODE == kF32 || RMODE == kI32, "4-byte sliced plans are fp32 or int32");

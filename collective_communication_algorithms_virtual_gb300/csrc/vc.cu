@@ -903,21 +903,26 @@ struct Written {
 // every byte of a receive buffer or of scratch that a step reads was written
 // by an earlier step -- by the thread that owns it, which therefore reads it
 // through L1.  Positions stay below 2^29, so the kernels' 32-bit element
-// offsets hold.  AllReduce and Broadcast positions are absolute (every send
-// and receive region has origin 0, so a 4-byte kernel can derive each
-// operation's range from its first operand); the ring ReduceScatter and
-// AllGather count them within a block.
+// offsets hold.  Where every region, scratch included, has origin 0 (the
+// 4-byte AllReduce schedules, the Broadcasts), a 4-byte kernel derives each
+// operation's range from its first operand's offset; otherwise it takes the
+// ranges the host lists (a Reduce's first operand can be a partial sum in
+// scratch, whose origin is its slot).
 struct SliceShape {
   int es = 0;              // bytes of the data type
-  bool absolute = true;    // every send / receive region has origin 0
+  bool absolute = true;    // every region has origin 0 (an operation's range follows from any operand)
   int64_t positions = 0;   // positions the plan covers
 };
 bool sliceable(const Plan& plan, int rmode, SliceShape* sh) {
   int es = 0;
   if (rmode == dev::kF32 || rmode == dev::kI32) es = 4;
   else if (rmode == dev::kBF16 || rmode == dev::kF16) es = 2;
-  else if (rmode == dev::kCopy && !plan.steps.empty() && !plan.steps[0].ops.empty())
-    es = esize(plan.steps[0].ops[0].src[0].dt);  // copies only: the data type of any operand
+  else if (rmode == dev::kCopy)  // copies only: the data type of any operand (a step may have none)
+    for (const Step& st : plan.steps)
+      if (!st.ops.empty()) {
+        es = esize(st.ops[0].src[0].dt);
+        break;
+      }
   if (es != 2 && es != 4) return false;
   const int64_t gelems = 16 / es;
   struct Region {
@@ -941,7 +946,7 @@ bool sliceable(const Plan& plan, int rmode, SliceShape* sh) {
         if (z != es && !partial) return false;
         const int64_t origin = o.byte_off - op.pos0 * z;
         if (origin % (partial ? 32 : 16) != 0) return false;
-        if (o.buf != Buf::Scratch) absolute = absolute && origin == 0;
+        absolute = absolute && origin == 0;
         regions[key(o)].push_back({o.byte_off, o.byte_off + op.n * z, origin, z});
         return true;
       };
@@ -1471,21 +1476,25 @@ vc_status_t run(const Call& c) {
     aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
                (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
   const size_t slim = slice_limit();
-  // the sliced form's size per rank: AllReduce the 4 bytes a thread carries
-  // through the steps per element (fp32 / int32 data, or the fp32 partial
-  // sums of 16-bit data), ReduceScatter its input likewise, AllGather its
-  // output, Broadcast its message.  Not for in-place calls of the other
-  // collectives, whose send and receive buffers would hold positions at two
-  // places.  (16-bit sliced plans access their fp32 partials 32 bytes at a
-  // time.)
+  // the sliced form's size per rank: AllReduce and Reduce the 4 bytes a
+  // thread carries through the steps per element (fp32 / int32 data, or the
+  // fp32 partial sums of 16-bit data), ReduceScatter its input likewise,
+  // AllGather and Gather their output, Broadcast and Scatter their message.
+  // Not for in-place calls of the other collectives, whose send and receive
+  // buffers would hold positions at two places.  (16-bit sliced plans access
+  // their fp32 partials 32 bytes at a time.)
   int64_t slice_bytes = -1;
   switch (c.coll) {
     case Coll::AllReduce: slice_bytes = c.count * 4; break;
-    case Coll::ReduceScatter: slice_bytes = pa.inplace ? -1 : c.count * N * 4; break;
-    case Coll::AllGather: slice_bytes = pa.inplace ? -1 : c.count * N * es; break;
-    case Coll::Broadcast: slice_bytes = pa.inplace ? -1 : c.count * es; break;
+    case Coll::Reduce: slice_bytes = c.count * 4; break;
+    case Coll::ReduceScatter: slice_bytes = c.count * N * 4; break;
+    case Coll::AllGather:
+    case Coll::Gather:
+    case Coll::Scatter: slice_bytes = c.count * N * es; break;
+    case Coll::Broadcast: slice_bytes = c.count * es; break;
     default: break;
   }
+  if (pa.inplace && c.coll != Coll::AllReduce) slice_bytes = -1;
   if (aligned && slim > 0 && slice_bytes >= 0 && plan.steps.size() >= 2 &&
       (es == 4 || (reinterpret_cast<uintptr_t>(scratch) & 31) == 0) &&
       c.count < (int64_t(1) << 29) && static_cast<uint64_t>(slice_bytes) <= std::min<uint64_t>(slim, INT64_MAX)) {

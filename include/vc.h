@@ -286,9 +286,10 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
  *   block); dtype: storage type of the operand; elem0: the element position
  *   of the operation's first element, where the schedule keeps positions --
  *   its element i is position elem0 + i, held in order by each operand's
- *   region.  Positions are the elements of the message: AllReduce's buffer,
- *   ring ReduceScatter's input, ring AllGather's output, the binomial and
- *   pipelined Broadcasts' message.  Else -1.
+ *   region.  Positions are the elements of the message: AllReduce's and the
+ *   tree Reduce's buffer, ring ReduceScatter's input, ring AllGather's
+ *   output, the Broadcasts' message, the binomial Scatter's input and
+ *   Gather's output at the root.  Else -1.
  * Returns VC_ERR_INVALID_ARG if `capacity` is too small (with *n_entries set
  * to the size needed).  *scratch_bytes receives the scratch the call needs,
  * *n_steps the number of steps.
@@ -413,18 +414,21 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * cluster form).
  *
  * In the AllReduce schedules (Ring, RHD, DBT, Mesh, RING_HOP), the ring
- * ReduceScatter and AllGather and the binomial and pipelined Broadcasts,
- * every operation maps element position e of each source to position e of
- * each destination, where positions are the elements of the message
- * (AllReduce's buffer, ReduceScatter's input, AllGather's output, the
- * Broadcast message), and each buffer region holds its positions in order at
+ * ReduceScatter and AllGather, the Broadcasts (binomial, Scatter+AllGather,
+ * pipelined), the binomial Scatter and Gather and the tree Reduce, every
+ * operation maps element position e of each source to position e of each
+ * destination, where positions are the elements of the message (AllReduce's
+ * and Reduce's buffer, ReduceScatter's input, AllGather's output, the
+ * Broadcast message, Scatter's input and Gather's output at the root), and
+ * each buffer region holds its positions in order at
  * one place: the send and receive buffers and the partial sums the schedule
  * keeps in scratch (fp32 for bf16 / fp16 data).  A call of such a schedule
  * runs all its steps in one launch over the whole GPU when, per rank, it
  * carries at most `max_bytes_per_rank`: AllReduce 4 bytes per element (the
  * fp32 / int32 data, or the fp32 partials of 16-bit data), ReduceScatter 4
  * bytes per input element likewise, AllGather its output, Broadcast its
- * message.  Each thread owns one group of positions (16 bytes of the data
+ * message (Reduce, Scatter and Gather likewise).  Each thread owns one group
+ * of positions (16 bytes of the data
  * type) of every buffer and carries it through every step of the plan in
  * order, applying each operation that covers it.  What a step reads at a
  * position was written there by an earlier step, by the same thread, so the
@@ -437,8 +441,7 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * partial per element while the partials take at most 16 MiB per rank;
  * above that they alternate two chunk-sized slots per rank, which several
  * positions share, and do not run sliced at 5 ranks or more.  In-place
- * ReduceScatter, AllGather and Broadcast calls, Scatter+AllGather
- * Broadcasts and the other collectives take the other forms.  The
+ * calls other than AllReduce, and the AllToAlls, take the other forms.  The
  * conditions of single-launch execution on alignment and the resident
  * description apply as well.  max_bytes_per_rank: 0 disables it, SIZE_MAX
  * applies it to every eligible call.  Default VC_SLICE_LIMIT_DEFAULT: up to

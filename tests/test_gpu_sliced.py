@@ -219,6 +219,41 @@ def test_sliced_broadcast(N, dtype):
                         assert same_bits(recvs[r].host(), A), (algo, k, N, count, root, inplace, r)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [3, 5, 8, 16])
+def test_sliced_scatter_gather_reduce_and_scatter_allgather(N, dtype):
+    """Binomial Scatter and Gather (positions: the root's buffer), tree
+    Reduce, Scatter+AllGather Broadcast: every root, against the oracle."""
+    vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
+    G = 16 // (4 if dtype == "f32" else 2)
+    for rc in (G, 64 * G + G):
+        for root in sorted({0, N // 2, N - 1}):
+            B = _inputs(dtype, 9100 + N + rc + root, 1, N * rc)[0]
+            recvs = [Guarded(rc, dtype) for _ in range(N)]
+            recs = _traced(lambda: vc.vc_scatter(to_dev(B), [g.t for g in recvs], root=root, algo="binomial"))
+            assert len(recs) == 1 and recs[0]["kernel"].endswith("_sliced"), ("scatter", N, rc, root, recs)
+            for r in range(N):
+                assert same_bits(recvs[r].host(), B[r * rc:(r + 1) * rc]), ("scatter", N, rc, root, r)
+            xs = _inputs(dtype, 9200 + N + rc + root, N, rc)
+            out = Guarded(N * rc, dtype)
+            recs = _traced(lambda: vc.vc_gather([to_dev(x) for x in xs], out.t, root=root, algo="binomial"))
+            assert len(recs) == 1 and recs[0]["kernel"].endswith("_sliced"), ("gather", N, rc, root, recs)
+            assert same_bits(out.host(), np.concatenate(xs)), ("gather", N, rc, root)
+            want = cxx.reduce(xs, root, "binomial", dtype, want_log=False).outputs[0]
+            out = Guarded(rc, dtype)
+            recs = _traced(lambda: vc.vc_reduce([to_dev(x) for x in xs], out.t, root=root, algo="binomial"))
+            assert len(recs) == 1 and recs[0]["kernel"].endswith("_sliced"), ("reduce", N, rc, root, recs)
+            got = out.host()
+            assert same_bits(got, want), ("reduce", N, rc, root, first_diff(got, want))
+            A = _inputs(dtype, 9300 + N + rc + root, 1, N * rc + 3)[0]
+            bout = [Guarded(len(A), dtype) for _ in range(N)]
+            recs = _traced(lambda: vc.vc_broadcast(to_dev(A), [g.t for g in bout], root=root, algo="scatter_allgather"))
+            assert len(recs) == 1 and recs[0]["kernel"].endswith("_sliced"), ("sag", N, rc, root, recs)
+            assert all(g.guards_intact() for g in recvs + bout + [out])
+            for r in range(N):
+                assert same_bits(bout[r].host(), A), ("sag", N, rc, root, r)
+
+
 def test_calls_that_do_not_qualify_take_other_forms():
     vc.vc_set_slice_limit(vc.SLICE_ALWAYS)
     # a 16-bit Ring with more than 16 MiB of fp32 partials per rank: they
@@ -239,17 +274,16 @@ def test_calls_that_do_not_qualify_take_other_forms():
         got, recs = _run(xs, algo, "f32", shift=1 if algo == "ring" else 0)
         assert not any(r["kernel"].endswith("_sliced") for r in recs), (algo, recs)
         assert all(same_bits(got[r], want[r]) for r in range(N)), algo
-    # a Broadcast whose Scatter stages subtrees in scratch, and a binomial Scatter
-    A = np.arange(count, dtype=np.int32)
-    outs = [torch.empty(count, dtype=torch.int32, device="cuda") for _ in range(N)]
-    recs = _traced(lambda: vc.vc_broadcast(to_dev(A), outs, root=0, algo="scatter_allgather"))
-    assert not any(r["kernel"].endswith("_sliced") for r in recs), recs
-    assert all(np.array_equal(to_host(o), A) for o in outs)
-    B = np.arange(N * 1024, dtype=np.int32)
-    outs = [torch.empty(1024, dtype=torch.int32, device="cuda") for _ in range(N)]
-    recs = _traced(lambda: vc.vc_scatter(to_dev(B), outs, root=0, algo="binomial"))
-    assert not any(r["kernel"].endswith("_sliced") for r in recs), recs
-    assert all(np.array_equal(to_host(outs[r]), B[r * 1024:(r + 1) * 1024]) for r in range(N))
+    # AllToAll (blocks move between offsets that differ by rank)
+    B = np.arange(N * N * 1024, dtype=np.int32).reshape(N, N * 1024)
+    ins = [to_dev(B[r]) for r in range(N)]
+    outs = [torch.empty(N * 1024, dtype=torch.int32, device="cuda") for _ in range(N)]
+    for algo in ("bruck", "ring"):
+        recs = _traced(lambda: vc.vc_alltoall(ins, outs, algo=algo))
+        assert not any(r["kernel"].endswith("_sliced") for r in recs), (algo, recs)
+        for j in range(N):
+            got = to_host(outs[j]).reshape(N, 1024)
+            assert all(np.array_equal(got[i], B[i, j * 1024:(j + 1) * 1024]) for i in range(N)), (algo, j)
 
 
 def test_default_limit():

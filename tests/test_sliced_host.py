@@ -178,8 +178,8 @@ def test_ring_partials_above_16_mib_alternate(dtype):
 # ---- the other collectives whose schedules keep positions ---------------------------------
 # Positions are the elements of the message: the ring ReduceScatter's input
 # (its partial sums keep one slot per block while they take at most 16 MiB per
-# rank), the ring AllGather's output, the binomial and pipelined Broadcasts'
-# message.
+# rank), the ring AllGather's output, the Broadcasts' message, the binomial
+# Scatter's input and Gather's output at the root, the tree Reduce's buffer.
 
 def _rs_ag_bcast_cases(N, dtype):
     G = _group(dtype)
@@ -195,12 +195,31 @@ def _rs_ag_bcast_cases(N, dtype):
     for root in (0, N - 1):
         send = [None] * N
         send[root] = A
-        for algo, k in (("binomial", 0), ("pipe_chain", 5), ("pipe_tree", 3)):
+        for algo, k in (("binomial", 0), ("scatter_allgather", 0), ("pipe_chain", 5), ("pipe_tree", 3)):
             if k:
                 want = lambda root=root, algo=algo, k=k: schedules.broadcast_pipelined(A, N, root, algo, dtype, k).outputs
             else:
                 want = lambda root=root, algo=algo: schedules.broadcast(A, N, root, algo, dtype).outputs
             yield ("broadcast", algo, count, root, k, want, send, [count * ESZ[DT[dtype]]] * N, count)
+        # binomial Scatter / Gather (blocks of rc) and tree Reduce, at the root only
+        B = _inputs(dtype, 1600 + N + root, 1, N * rc)[0]
+        sendB = [None] * N
+        sendB[root] = B
+        yield ("scatter", "binomial", rc, root, 0, lambda root=root: schedules.scatter(B, N, root, "binomial", dtype).outputs,
+               sendB, [rc * ESZ[DT[dtype]]] * N, N * rc)
+        root_only = lambda nbytes, root=root: [nbytes if r == root else 0 for r in range(N)]
+        yield ("gather", "binomial", rc, root, 0,
+               lambda root=root: _at_root(schedules.gather(ins, root, "binomial", dtype).outputs[0], root, N),
+               ins, root_only(N * rc * ESZ[DT[dtype]]), N * rc)
+        if dtype != "i32":
+            yield ("reduce", "binomial", rc, root, 0,
+                   lambda root=root: _at_root(schedules.reduce(ins, root, "binomial", dtype).outputs[0], root, N),
+                   ins, root_only(rc * ESZ[DT[dtype]]), rc)
+
+
+def _at_root(out, root, N):
+    """A root-only output as a per-rank list (other ranks: empty)."""
+    return [out if r == root else np.zeros(0, out.dtype) for r in range(N)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
@@ -223,11 +242,12 @@ def test_other_collective_plans_keep_positions_and_run_group_by_group(N, dtype):
                 assert _same(got, want[r]), (coll, algo, N, dtype, root, r)
 
 
-def test_scatter_allgather_broadcast_does_not_keep_positions():
-    """Its binomial Scatter stages subtrees in scratch: the library leaves it
-    to the other forms (an operation without elem0)."""
-    plan, _ = get_plan("broadcast", "scatter_allgather", 8, 4096, "f32")
-    assert any(op["elem0"] < 0 for ops in plan for op in ops)
+def test_alltoall_plans_do_not_keep_positions():
+    """AllToAll's rounds move blocks between offsets that differ by rank: the
+    library leaves them to the other forms (operations without elem0)."""
+    for algo in ("pairwise", "bruck", "ring"):
+        plan, _ = get_plan("alltoall", algo, 8, 1024, "f32")
+        assert any(op["elem0"] < 0 for ops in plan for op in ops), algo
 
 
 def test_reduce_scatter_partials_flat_up_to_16_mib():
