@@ -1,5 +1,7 @@
-"""bench.py's host logic on the CPU: the reference arm's JSON line and the
-replica timing reductions over two gloo ranks (world size 2)."""
+"""bench.py's host logic on the CPU: the reference arm's JSON line, the
+replica timing reductions over two gloo ranks (world size 2), the final
+line's size, the alpha-beta fit and the collectives sweep's slices and busbw
+(with the library calls and the timing stubbed)."""
 import io
 import json
 import os
@@ -154,3 +156,60 @@ def test_alpha_beta_fit_predicts_every_pair():
     assert r["crossovers"]["ring/dbt"]["measured"]["never"] == "dbt faster at every swept size"
     assert r["auto_vs_measured"]["differs_at"] == []
     assert "schedule_model_vs_measured" not in r
+
+
+class _FakeVC:
+    """Records the library calls the collectives sweep makes (no GPU)."""
+
+    def __init__(self):
+        self.calls = []
+
+    def _rec(self, name, *args, **kw):
+        self.calls.append((name, args, kw))
+
+    def vc_reduce_scatter(self, ins, outs, algo):
+        self._rec("reduce_scatter", len(ins[0]), len(outs[0]), algo=algo)
+
+    def vc_allgather(self, ins, outs, algo):
+        self._rec("allgather", len(ins[0]), len(outs[0]), algo=algo)
+
+    def vc_broadcast(self, src, outs, root, algo):
+        self._rec("broadcast", len(src), len(outs[0]), algo=algo)
+
+    def vc_broadcast_pipelined(self, src, outs, root, algo):
+        self._rec("broadcast", len(src), len(outs[0]), algo=algo)
+
+    def vc_alltoall(self, ins, outs, algo):
+        self._rec("alltoall", len(ins[0]), len(outs[0]), algo=algo)
+
+    def vc_plan_describe(self, coll, algo, N, count, dtype, root=0):
+        return [], 0, 1
+
+
+def test_sweep_collectives_sizes_and_busbw(monkeypatch):
+    """Every collective and algorithm at every size, with the buffer slices
+    the pages' busbw convention implies and busbw = M x factor / time."""
+    N = 8
+    import torch
+
+    send = [torch.empty((1 << 20) // 4) for _ in range(N)]  # 1 MiB per rank, host tensors
+    recv = {bench.ALGOS[0]: [torch.empty((1 << 20) // 4) for _ in range(N)]}
+    vc = _FakeVC()
+    monkeypatch.setattr(bench, "time_graph", lambda fn, stream: (fn(), 0.01)[1])  # 10 us a call
+    sizes = (4 << 10, 1 << 20, 4 << 20)  # the last exceeds the buffers and is skipped
+    res = bench.sweep_collectives(vc, send, recv, None, sizes)
+    assert set(res) == {f"{c}_{a}" for c, algos in bench.COLL_SWEEP.items() for a in algos}
+    for key, rows in res.items():
+        assert [r["bytes_per_rank"] for r in rows] == [4 << 10, 1 << 20], key
+        for r in rows:
+            f = 1.0 if key.startswith("broadcast") else (N - 1) / N
+            assert r["busbw"] == pytest.approx(r["bytes_per_rank"] * f / 10e-6 / 1e9), key
+    # the slices: RS input M / output M/N, AG input M/N / output M, Bcast M, A2A M
+    for name, args, kw in vc.calls:
+        n_in, n_out = args
+        if name == "reduce_scatter":
+            assert n_in == N * n_out
+        elif name == "allgather":
+            assert n_out == N * n_in
+        else:
+            assert n_in == n_out
