@@ -572,23 +572,25 @@ def sweep(vc, send, recv, stream):
 
 
 # the other collectives' algorithms, and the busbw factor of the pages' table
-# tbl-model-algo-busbw-coef for each (latency-formula page): M is the bytes per
-# rank the table counts -- ReduceScatter's input, AllGather's output,
-# Broadcast's message, AllToAll's buffer
+# tbl-model-algo-busbw-coef for each (latency-formula page; Scatter and Gather,
+# not in it, take (N-1)/N): M is the bytes per rank the table counts --
+# ReduceScatter's input, AllGather's output, Broadcast's and Reduce's
+# message, AllToAll's buffer, Scatter's input and Gather's output at the root
 COLL_SWEEP = {"reduce_scatter": ("ring", "fused"), "allgather": ("ring", "fused"),
               "broadcast": ("binomial", "scatter_allgather", "pipe_chain", "pipe_tree", "fused"),
-              "alltoall": ("pairwise", "bruck", "ring", "fused")}
+              "alltoall": ("pairwise", "bruck", "ring", "fused"),
+              "scatter": ("binomial", "fused"), "gather": ("binomial", "fused"), "reduce": ("binomial", "fused")}
 COLL_SWEEP_SIZES = (4 << 10, 64 << 10, 1 << 20, 16 << 20, 256 << 20)
 
 
 def coll_busbw_factor(coll: str, N: int) -> float:
-    return 1.0 if coll == "broadcast" else (N - 1) / N
+    return 1.0 if coll in ("broadcast", "reduce") else (N - 1) / N
 
 
 def sweep_collectives(vc, send, recv, stream, sizes=COLL_SWEEP_SIZES):
-    """busbw versus message size for ReduceScatter, AllGather, Broadcast and
-    AllToAll, every algorithm, 8 ranks, fp32, graph-timed, on the bench's
-    buffers (sends, and the first output set)."""
+    """busbw versus message size for ReduceScatter, AllGather, Broadcast,
+    AllToAll, Scatter, Gather and Reduce, every algorithm, 8 ranks, fp32,
+    graph-timed, on the bench's buffers (sends, and the first output set)."""
     N = len(send)
     outs = recv[ALGOS[0]]
     res = {}
@@ -615,10 +617,22 @@ def sweep_collectives(vc, send, recv, stream, sizes=COLL_SWEEP_SIZES):
                     else:
                         fn = lambda: vc.vc_broadcast(src, o, root=0, algo=a)
                     shape = plan_shape(vc, coll, a, N, cnt)
-                else:
+                elif coll == "alltoall":
                     ins, o = [x[:cnt] for x in send], [y[:cnt] for y in outs]
                     fn = lambda: vc.vc_alltoall(ins, o, algo=a)
                     shape = plan_shape(vc, coll, a, N, blk)
+                elif coll == "scatter":
+                    src, o = send[0][:cnt], [y[:blk] for y in outs]
+                    fn = lambda: vc.vc_scatter(src, o, root=0, algo=a)
+                    shape = plan_shape(vc, coll, a, N, blk)
+                elif coll == "gather":
+                    ins, o = [x[:blk] for x in send], outs[0][:cnt]
+                    fn = lambda: vc.vc_gather(ins, o, root=0, algo=a)
+                    shape = plan_shape(vc, coll, a, N, blk)
+                else:
+                    ins, o = [x[:cnt] for x in send], outs[0][:cnt]
+                    fn = lambda: vc.vc_reduce(ins, o, root=0, algo=a)
+                    shape = plan_shape(vc, coll, a, N, cnt)
                 ms = time_graph(fn, stream)
                 rows.append({"bytes_per_rank": nbytes, "us": ms * 1e3,
                              "busbw": nbytes * coll_busbw_factor(coll, N) / (ms * 1e-3) / 1e9,

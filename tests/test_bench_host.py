@@ -182,6 +182,15 @@ class _FakeVC:
     def vc_alltoall(self, ins, outs, algo):
         self._rec("alltoall", len(ins[0]), len(outs[0]), algo=algo)
 
+    def vc_scatter(self, src, outs, root, algo):
+        self._rec("scatter", len(src), len(outs[0]), algo=algo)
+
+    def vc_gather(self, ins, out, root, algo):
+        self._rec("gather", len(ins[0]), len(out), algo=algo)
+
+    def vc_reduce(self, ins, out, root, algo):
+        self._rec("reduce", len(ins[0]), len(out), algo=algo)
+
     def vc_plan_describe(self, coll, algo, N, count, dtype, root=0):
         return [], 0, 1
 
@@ -192,6 +201,8 @@ def test_sweep_collectives_sizes_and_busbw(monkeypatch):
     N = 8
     import torch
 
+    import collective_communication_algorithms_virtual_gb300 as vc_lib
+
     send = [torch.empty((1 << 20) // 4) for _ in range(N)]  # 1 MiB per rank, host tensors
     recv = {bench.ALGOS[0]: [torch.empty((1 << 20) // 4) for _ in range(N)]}
     vc = _FakeVC()
@@ -201,15 +212,18 @@ def test_sweep_collectives_sizes_and_busbw(monkeypatch):
     assert set(res) == {f"{c}_{a}" for c, algos in bench.COLL_SWEEP.items() for a in algos}
     for key, rows in res.items():
         assert [r["bytes_per_rank"] for r in rows] == [4 << 10, 1 << 20], key
+        coll = next(c for c in bench.COLL_SWEEP if key.startswith(c + "_"))
+        f = vc_lib.vc_busbw_factor(coll, N)  # the library's table
+        assert bench.coll_busbw_factor(coll, N) == f, coll
         for r in rows:
-            f = 1.0 if key.startswith("broadcast") else (N - 1) / N
             assert r["busbw"] == pytest.approx(r["bytes_per_rank"] * f / 10e-6 / 1e9), key
-    # the slices: RS input M / output M/N, AG input M/N / output M, Bcast M, A2A M
+    # the slices: RS and Scatter input M / output M/N, AG and Gather input M/N /
+    # output M, Bcast, Reduce and A2A M
     for name, args, kw in vc.calls:
         n_in, n_out = args
-        if name == "reduce_scatter":
-            assert n_in == N * n_out
-        elif name == "allgather":
-            assert n_out == N * n_in
+        if name in ("reduce_scatter", "scatter"):
+            assert n_in == N * n_out, name
+        elif name in ("allgather", "gather"):
+            assert n_out == N * n_in, name
         else:
-            assert n_in == n_out
+            assert n_in == n_out, name
