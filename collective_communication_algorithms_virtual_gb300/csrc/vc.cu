@@ -1504,10 +1504,14 @@ vc_status_t run(const Call& c) {
   }
   // a plan whose steps all share one launch (step merging: Pairwise
   // AllToAll's rounds) runs that launch, not a cluster with a barrier per step
-  // (8 ranks, 64 KiB per rank: 10.4 us as a cluster, 2-3 us as one launch)
+  // (8 ranks, 64 KiB per rank: 10.4 us as a cluster, 2-3 us as one launch).
+  // AllToAll plans run per step: their steps are many small block copies, and
+  // one launch a step measured faster than one cluster (8 ranks, 1-16 KiB per
+  // rank: Bruck 7.3-7.5 against 10.1-10.6 us, Ring 12.0-12.3 against
+  // 14.2-14.9).
   const bool one_launch = !plan.launch_end.empty() && plan.launch_end[0] == plan.steps.size();
   const size_t limit = single_launch_limit();
-  if (!dp && !one_launch && aligned && limit > 0 && plan.steps.size() >= 2 &&
+  if (!dp && !one_launch && c.coll != Coll::AllToAll && aligned && limit > 0 && plan.steps.size() >= 2 &&
       plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > limit)) dp = nullptr;

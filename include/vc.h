@@ -391,8 +391,9 @@ vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n
  *   - its description fits the kernel's shared memory (96 KB; e.g. the ring
  *     AllReduce up to about 24 ranks),
  *   - every buffer pointer of the call is 16-byte aligned,
- *   - its steps do not all share one launch under vc_set_merge_steps (a
- *     Pairwise AllToAll's independent rounds run as that one launch), and
+ *   - it is not an AllToAll (their steps of many small block copies measured
+ *     faster as one launch a step; a Pairwise AllToAll's independent rounds
+ *     share one launch under vc_set_merge_steps), and
  *   - the description is resident on the device.  It is uploaded once per
  *     call shape (collective, algorithm, ranks, count, type, op, root, in
  *     place), at the first call that is not being captured into a CUDA graph

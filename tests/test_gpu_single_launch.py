@@ -147,7 +147,8 @@ def test_reduce_scatter_allgather_alltoall_single_launch(N, dtype):
                 assert all(g.guards_intact() for g in sends + recvs)
                 for r in range(N):
                     assert same_bits(recvs[r].host(), want[r]), ("a2a", algo, N, rc, limit, r)
-                _check_launches(recs, limit, _nsteps("alltoall", algo, N, rc, dtype), ("a2a", algo))
+                # AllToAll runs per step whatever the limit (faster than one cluster)
+                _check_launches(recs, 0, _nsteps("alltoall", algo, N, rc, dtype), ("a2a", algo))
 
 
 @pytest.mark.parametrize("N", [2, 3, 8, 16])
