@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     vc_last_error,
     vc_plan_describe,
     vc_plan_exec_order,
+    vc_plan_form,
     vc_reduce_scatter,
     vc_scatter,
     vc_select_algo,

@@ -99,6 +99,9 @@ def lib() -> ctypes.CDLL:
         L.vc_plan_exec_order.argtypes = [I, I, I, Z, I, I, I, I, I, U32P, U8P, Z, U8P, Z, ctypes.POINTER(Z),
                                          ctypes.POINTER(I)]
         L.vc_plan_exec_order.restype = I
+        L.vc_plan_form.argtypes = [I, I, I, Z, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I),
+                                   ctypes.POINTER(I)]
+        L.vc_plan_form.restype = I
         L.vc_trace_enable.argtypes = [I]
         L.vc_trace_enable.restype = I
         L.vc_trace_read.argtypes = [ctypes.POINTER(TraceRecord), Z, ctypes.POINTER(Z)]
@@ -432,6 +435,22 @@ def vc_plan_describe(coll, algo, nranks: int, count: int, dtype="f32", root: int
     check(L.vc_plan_describe(*args, buf, need.value, ctypes.byref(need), ctypes.byref(scratch),
                              ctypes.byref(steps)))
     return list(buf[:need.value]), scratch.value, steps.value
+
+
+FORMS = {0: "steps", 1: "cluster", 2: "sliced"}
+
+
+def vc_plan_form(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,
+                 nchunks: int = 0, op="sum"):
+    """The execution form a call takes under the current settings, on aligned
+    buffers: ("sliced" | "cluster" | "steps", launches, host_ranges); host
+    only, needs no GPU."""
+    L = lib()
+    form, launches, hr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    check(L.vc_plan_form(_code(COLLS, coll), _code(ALGOS, algo), int(nranks), int(count), _code(DTYPES, dtype),
+                         _code(OPS, op), int(root), int(bool(inplace)), int(nchunks), ctypes.byref(form),
+                         ctypes.byref(launches), ctypes.byref(hr)))
+    return FORMS[form.value], launches.value, bool(hr.value)
 
 
 def vc_plan_exec_order(coll, algo, nranks: int, count: int, dtype="f32", root: int = 0, inplace: bool = False,

@@ -1358,6 +1358,55 @@ PlanStatus supported(const PlanArgs& zero, std::string* why) {
   return ps;
 }
 
+// Which one-launch forms a call may take, before its device description
+// says whether the plan qualifies.  `aligned`: every buffer pointer and the
+// scratch block 16-byte aligned; `scratch32`: the scratch block 32-byte
+// aligned (16-bit sliced plans access their fp32 partials 32 bytes at a time).
+struct FormGate {
+  bool sliced = false;   // try the sliced form
+  bool cluster = false;  // else try one cluster
+  size_t cluster_limit = 0;
+};
+FormGate form_gate(const PlanArgs& pa, const Plan& plan, int64_t es, bool aligned, bool scratch32) {
+  FormGate g;
+  const int64_t N = pa.nranks, count = pa.count;
+  if (!aligned || plan.steps.size() < 2) return g;
+  // the sliced form's size per rank: AllReduce and Reduce the 4 bytes a
+  // thread carries through the steps per element (fp32 / int32 data, or the
+  // fp32 partial sums of 16-bit data), ReduceScatter its input likewise,
+  // AllGather and Gather their output, Broadcast and Scatter their message.
+  // Not for in-place calls of the other collectives, whose send and receive
+  // buffers would hold positions at two places.
+  int64_t slice_bytes = -1;
+  switch (pa.coll) {
+    case Coll::AllReduce:
+    case Coll::Reduce: slice_bytes = count * 4; break;
+    case Coll::ReduceScatter: slice_bytes = count * N * 4; break;
+    case Coll::AllGather:
+    case Coll::Gather:
+    case Coll::Scatter: slice_bytes = count * N * es; break;
+    case Coll::Broadcast: slice_bytes = count * es; break;
+    default: break;
+  }
+  if (pa.inplace && pa.coll != Coll::AllReduce) slice_bytes = -1;
+  const size_t slim = slice_limit();
+  g.sliced = slim > 0 && slice_bytes >= 0 && (es == 4 || scratch32) && count < (int64_t(1) << 29) &&
+             static_cast<uint64_t>(slice_bytes) <= std::min<uint64_t>(slim, INT64_MAX);
+  // a plan whose steps all share one launch (step merging: Pairwise
+  // AllToAll's rounds) runs that launch, not a cluster with a barrier per step
+  // (8 ranks, 64 KiB per rank: 10.4 us as a cluster, 2-3 us as one launch).
+  // AllToAll plans run per step: their steps are many small block copies, and
+  // one launch a step measured faster than one cluster (8 ranks, 1-16 KiB per
+  // rank: Bruck 7.3-7.5 against 10.1-10.6 us, Ring 12.0-12.3 against
+  // 14.2-14.9).
+  const bool one_launch = !plan.launch_end.empty() && plan.launch_end[0] == plan.steps.size();
+  g.cluster_limit = single_launch_limit();
+  g.cluster = !one_launch && pa.coll != Coll::AllToAll && g.cluster_limit > 0 &&
+              plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <=
+                  static_cast<int64_t>(std::min<size_t>(g.cluster_limit, INT64_MAX));
+  return g;
+}
+
 vc_status_t run(const Call& c) {
   const int N = c.nranks;
   if (N < 1 || N > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
@@ -1475,46 +1524,15 @@ vc_status_t run(const Call& c) {
   for (int r = 0; r < N; ++r)
     aligned &= (!sends[r] || (reinterpret_cast<uintptr_t>(sends[r]) & 15) == 0) &&
                (!recvs[r] || (reinterpret_cast<uintptr_t>(recvs[r]) & 15) == 0);
-  const size_t slim = slice_limit();
-  // the sliced form's size per rank: AllReduce and Reduce the 4 bytes a
-  // thread carries through the steps per element (fp32 / int32 data, or the
-  // fp32 partial sums of 16-bit data), ReduceScatter its input likewise,
-  // AllGather and Gather their output, Broadcast and Scatter their message.
-  // Not for in-place calls of the other collectives, whose send and receive
-  // buffers would hold positions at two places.  (16-bit sliced plans access
-  // their fp32 partials 32 bytes at a time.)
-  int64_t slice_bytes = -1;
-  switch (c.coll) {
-    case Coll::AllReduce: slice_bytes = c.count * 4; break;
-    case Coll::Reduce: slice_bytes = c.count * 4; break;
-    case Coll::ReduceScatter: slice_bytes = c.count * N * 4; break;
-    case Coll::AllGather:
-    case Coll::Gather:
-    case Coll::Scatter: slice_bytes = c.count * N * es; break;
-    case Coll::Broadcast: slice_bytes = c.count * es; break;
-    default: break;
-  }
-  if (pa.inplace && c.coll != Coll::AllReduce) slice_bytes = -1;
-  if (aligned && slim > 0 && slice_bytes >= 0 && plan.steps.size() >= 2 &&
-      (es == 4 || (reinterpret_cast<uintptr_t>(scratch) & 31) == 0) &&
-      c.count < (int64_t(1) << 29) && static_cast<uint64_t>(slice_bytes) <= std::min<uint64_t>(slim, INT64_MAX)) {
+  const FormGate gate = form_gate(pa, plan, es, aligned, (reinterpret_cast<uintptr_t>(scratch) & 31) == 0);
+  if (gate.sliced) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
     if (dp && dp->eligible && dp->sliced) slice_groups = (dp->slice_positions * es + 15) / 16;
     else dp = nullptr;
   }
-  // a plan whose steps all share one launch (step merging: Pairwise
-  // AllToAll's rounds) runs that launch, not a cluster with a barrier per step
-  // (8 ranks, 64 KiB per rank: 10.4 us as a cluster, 2-3 us as one launch).
-  // AllToAll plans run per step: their steps are many small block copies, and
-  // one launch a step measured faster than one cluster (8 ranks, 1-16 KiB per
-  // rank: Bruck 7.3-7.5 against 10.1-10.6 us, Ring 12.0-12.3 against
-  // 14.2-14.9).
-  const bool one_launch = !plan.launch_end.empty() && plan.launch_end[0] == plan.steps.size();
-  const size_t limit = single_launch_limit();
-  if (!dp && !one_launch && c.coll != Coll::AllToAll && aligned && limit > 0 && plan.steps.size() >= 2 &&
-      plan_bytes(plan) / static_cast<int64_t>(plan.steps.size()) <= static_cast<int64_t>(std::min<size_t>(limit, INT64_MAX))) {
+  if (!dp && gate.cluster) {
     dp = resident_plan(dev, plan_key(pa), plan, N, c.stream);
-    if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > limit)) dp = nullptr;
+    if (dp && (!dp->eligible || static_cast<uint64_t>(dp->max_step_bytes) > gate.cluster_limit)) dp = nullptr;
   }
   if (dp) {
     tc.step = -1;
@@ -1813,7 +1831,7 @@ VC_EXPORT double vc_busbw_factor(vc_coll_t coll, int nranks) {
 
 // The plan of a host-only description call (vc_plan_describe, vc_plan_exec_order).
 vc_status_t describe_plan(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype, vc_op_t op,
-                          int root, int inplace, int nchunks, Plan* plan) {
+                          int root, int inplace, int nchunks, Plan* plan, PlanArgs* args = nullptr) {
   if (static_cast<int>(coll) < 0 || static_cast<int>(coll) > 7) return fail(VC_ERR_INVALID_ARG, "unknown collective");
   PlanArgs pa;
   pa.coll = static_cast<Coll>(static_cast<int>(coll));
@@ -1835,6 +1853,7 @@ vc_status_t describe_plan(vc_coll_t coll, vc_algo_t algo, int nranks, size_t cou
   std::string why;
   const PlanStatus ps = build_plan(pa, plan, &why);
   if (ps != PlanStatus::Ok) return plan_status(ps, why);
+  if (args) *args = pa;
   return VC_SUCCESS;
 }
 
@@ -1908,6 +1927,43 @@ VC_EXPORT vc_status_t vc_plan_exec_order(vc_coll_t coll, vc_algo_t algo, int nra
         keep[k] = o.keep ? 1 : 0;
         ++k;
       }
+    }
+    return VC_SUCCESS;
+  });
+}
+
+VC_EXPORT vc_status_t vc_plan_form(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype,
+                                   vc_op_t op, int root, int inplace, int nchunks, int* form, int* launches,
+                                   int* host_ranges) {
+  return entry([&]() -> vc_status_t {
+    if (!form || !launches || !host_ranges) return fail(VC_ERR_INVALID_ARG, "null output");
+    if (nranks < 1 || nranks > VC_MAX_RANKS) return fail(VC_ERR_INVALID_ARG, "nranks must be in [1, 64]");
+    Plan plan;
+    PlanArgs pa;
+    const vc_status_t rc = describe_plan(coll, algo, nranks, count, dtype, op, root, inplace, nchunks, &plan, &pa);
+    if (rc != VC_SUCCESS) return rc;
+    // as a call builds it (cached_plan), and an AllReduce in place as a call runs it
+    order_for_reuse(&plan);
+    mark_independent_steps(&plan);
+    if (pa.coll == Coll::AllReduce) pa.inplace = nranks == 1 && pa.inplace;
+    const FormGate gate = form_gate(pa, plan, esize(pa.dt), true, true);
+    DevPlan dp;
+    std::vector<uint4> img;
+    if (gate.sliced || gate.cluster) build_image(plan, nranks, 16 * dev::kPlanSubs, &img, &dp);
+    *host_ranges = 0;
+    if (gate.sliced && dp.eligible && dp.sliced) {
+      *form = VC_FORM_SLICED;
+      *launches = 1;
+      *host_ranges = dp.slice_host_ranges ? 1 : 0;
+    } else if (gate.cluster && dp.eligible && static_cast<uint64_t>(dp.max_step_bytes) <= gate.cluster_limit) {
+      *form = VC_FORM_CLUSTER;
+      *launches = 1;
+    } else {
+      *form = VC_FORM_STEPS;
+      int n = 0;
+      for (size_t si = 0; si < plan.steps.size(); ++n)
+        si = plan.launch_end.empty() ? si + 1 : plan.launch_end[si];
+      *launches = n;
     }
     return VC_SUCCESS;
   });

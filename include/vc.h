@@ -317,6 +317,28 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
                              int* n_steps);
 
 /*
+ * Host-only: the execution form a call with these arguments takes under the
+ * current settings (vc_set_slice_limit, vc_set_single_launch,
+ * vc_set_merge_steps), on 16-byte aligned buffers with a resident plan
+ * description (a call whose buffers are not aligned, or whose shape is first
+ * seen while its stream is captured, runs its steps one launch each).
+ *   *form: VC_FORM_SLICED (one launch over the GPU, each thread carrying its
+ *     group of positions through every step), VC_FORM_CLUSTER (one launch of
+ *     one thread-block cluster with a barrier between steps) or VC_FORM_STEPS
+ *     (one launch per step, or per run of independent steps);
+ *   *launches: the launches the call makes (1 for the one-launch forms; 0 for
+ *     a call with nothing to do);
+ *   *host_ranges: for the sliced form, 1 if its kernel reads the operation
+ *     ranges the host lists (16-bit data, or a region not at origin 0), 0 if
+ *     it derives them from each operation's first operand.
+ * VC_ERR_INVALID_ARG for a null output; other errors as vc_plan_describe.
+ * Needs no GPU.
+ */
+typedef enum { VC_FORM_STEPS = 0, VC_FORM_CLUSTER = 1, VC_FORM_SLICED = 2 } vc_form_t;
+vc_status_t vc_plan_form(vc_coll_t coll, vc_algo_t algo, int nranks, size_t count, vc_dtype_t dtype, vc_op_t op,
+                         int root, int inplace, int nchunks, int* form, int* launches, int* host_ranges);
+
+/*
  * Host-only introspection of the L2 reuse order (vc_set_reuse_order, read at
  * the call): the plan vc_plan_describe returns, in the order the library
  * executes it (no counterpart on the source pages).  For the k-th operation

@@ -158,6 +158,20 @@ def position_places(plan, mem: Memory, group: int) -> list:
     return bad
 
 
+def origins(plan, es: int) -> list:
+    """Every operand's (origin, alignment it needs): origin = byte offset -
+    elem0 x its element size; 16 bytes, or 32 for the fp32 partial sums of
+    16-bit data in scratch (accessed 32 bytes at a time)."""
+    out = []
+    for ops in plan:
+        for op in ops:
+            for (k, o, dt, off, stride) in op["src"] + op["dst"]:
+                z = ESZ[dt]
+                need = 32 if (k == SCRATCH and es == 2 and z == 4) else 16
+                out.append((off - op["elem0"] * z, need))
+    return out
+
+
 def reads_before_writes(plan, mem: Memory) -> list:
     """Reads of a receive buffer or of scratch whose bytes no earlier step
     wrote (the sliced form reads those through L1 and needs none: what it

@@ -29,8 +29,8 @@ from collective_communication_algorithms_virtual_gb300 import build
 from oracle import schedules
 from synthetic_inputs import rank_buffers
 
-from .plan_replay import (DT, ESZ, NPT, SCRATCH, Memory, get_plan, hazards, one_after_another, position_places,
-                          reads_before_writes, run_plan, run_plan_sliced, shuffled)
+from .plan_replay import (DT, ESZ, NPT, SCRATCH, Memory, get_plan, hazards, one_after_another, origins,
+                          position_places, reads_before_writes, run_plan, run_plan_sliced, shuffled)
 
 ALGOS = tuple(a for a in schedules.ALGOS["allreduce"] if a != "fused")  # multi-step schedules
 
@@ -262,3 +262,81 @@ def test_reduce_scatter_partials_flat_up_to_16_mib():
             assert (not position_places(plan, mem, _group(dtype))) == flat, (dtype, rc)
             per_rank = (N if flat else 2) * rc * acc
             assert scratch == N * ((per_rank + 255) // 256 * 256), (dtype, rc, scratch)
+
+
+# ---- the library's choice of form, against these checks ------------------------------------
+# vc_plan_form reports the form a call takes (host only).  The sliced form is
+# predicted here from the plan alone, with the checks above: two or more
+# steps, every operation keeping positions (one run; a copy from one source),
+# each byte at one position, origins aligned, write-before-read, within the
+# size limit and not in place (AllReduce excepted).  Its kernel derives
+# operation ranges only where every origin is 0 (else "host ranges").
+
+def _slice_bytes(coll, N, count, es):
+    return {"allreduce": count * 4, "reduce": count * 4, "reduce_scatter": count * N * 4,
+            "allgather": count * N * es, "gather": count * N * es, "scatter": count * N * es,
+            "broadcast": count * es}.get(coll)
+
+
+def _predict(coll, algo, N, count, dtype, root, inplace, k):
+    plan, scratch = get_plan(coll, algo, N, count, dtype, root=root, inplace=inplace, nchunks=k)
+    es = ESZ[DT[dtype]]
+    G = 16 // es
+    mem = Memory([None] * N, [0] * N, scratch)
+    sb = _slice_bytes(coll, N, count, es)
+    ok = len(plan) >= 2 and sb is not None and sb <= (16 << 20) and count < (1 << 29)
+    ok = ok and not (inplace and coll != "allreduce")
+    ok = ok and all(op["elem0"] >= 0 and op["nb"] == 1 and (op["reduce"] or len(op["src"]) == 1)
+                    for ops in plan for op in ops)
+    ok = ok and not position_places(plan, mem, G) and not reads_before_writes(plan, mem)
+    orig = origins(plan, es) if ok else []
+    ok = ok and all(o % need == 0 for o, need in orig)
+    host_ranges = ok and (es == 2 or any(o != 0 for o, _ in orig))
+    return ok, host_ranges, len(plan)
+
+
+FORM_CASES = [("allreduce", a, 0) for a in ("ring", "rhd", "dbt", "mesh", "ring_hop", "fused")] + \
+    [("reduce_scatter", a, 0) for a in ("ring", "fused")] + [("allgather", a, 0) for a in ("ring", "fused")] + \
+    [("broadcast", a, 0) for a in ("binomial", "scatter_allgather", "fused")] + \
+    [("broadcast", "pipe_chain", 3), ("broadcast", "pipe_tree", 3)] + \
+    [("scatter", a, 0) for a in ("binomial", "fused")] + [("gather", a, 0) for a in ("binomial", "fused")] + \
+    [("reduce", a, 0) for a in ("binomial", "fused")] + \
+    [("alltoall", a, 0) for a in ("pairwise", "bruck", "ring", "fused")]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("N", [2, 3, 5, 8])
+def test_library_form_matches_the_independent_checks(N, dtype):
+    import collective_communication_algorithms_virtual_gb300 as vc
+
+    for coll, algo, k in FORM_CASES:
+        for count in (1, 5, 64, 1000 + 3):
+            for root in sorted({0, N - 1}):
+                for inplace in (False, True):
+                    if inplace and coll not in ("allreduce", "broadcast", "reduce"):
+                        continue
+                    sliced, hr, steps = _predict(coll, algo, N, count, dtype, root, inplace, k)
+                    form, launches, got_hr = vc.vc_plan_form(coll, algo, N, count, dtype, root, inplace, k)
+                    what = (coll, algo, N, count, dtype, root, inplace)
+                    assert (form == "sliced") == sliced, (what, form)
+                    if sliced:
+                        assert launches == 1 and got_hr == hr, (what, launches, got_hr, hr)
+                    elif coll == "alltoall":
+                        assert form == "steps", (what, form)
+
+
+def test_library_form_above_the_limit_and_for_merged_rounds():
+    import collective_communication_algorithms_virtual_gb300 as vc
+
+    # 8 Mi fp32 elements: 32 MiB carried per rank, above the 16 MiB default
+    assert vc.vc_plan_form("allreduce", "ring", 8, 8 << 20, "f32") == ("steps", 14, False)
+    assert vc.vc_plan_form("allreduce", "ring", 8, 4 << 20, "f32")[0] == "sliced"
+    # Pairwise AllToAll: its rounds share one launch; Bruck runs a launch per step
+    assert vc.vc_plan_form("alltoall", "pairwise", 8, 1024, "f32") == ("steps", 1, False)
+    assert vc.vc_plan_form("alltoall", "bruck", 8, 128, "f32") == ("steps", 3, False)
+    old = vc.vc_get_slice_limit()
+    try:
+        vc.vc_set_slice_limit(0)
+        assert vc.vc_plan_form("allreduce", "ring", 8, 1024, "f32")[0] == "cluster"
+    finally:
+        vc.vc_set_slice_limit(old)
