@@ -340,3 +340,31 @@ def test_library_form_above_the_limit_and_for_merged_rounds():
         assert vc.vc_plan_form("allreduce", "ring", 8, 1024, "f32")[0] == "cluster"
     finally:
         vc.vc_set_slice_limit(old)
+
+
+def test_library_form_of_degenerate_calls_and_bad_arguments():
+    import ctypes
+
+    import collective_communication_algorithms_virtual_gb300 as vc
+    from collective_communication_algorithms_virtual_gb300.binding import (VC_ERR_INVALID_ARG, VC_ERR_UNSUPPORTED,
+                                                                           VCError)
+
+    # nothing to do: no launch (an empty message; one rank in place)
+    assert vc.vc_plan_form("allreduce", "ring", 8, 0, "f32") == ("steps", 0, False)
+    assert vc.vc_plan_form("allreduce", "ring", 1, 1000, "f32", inplace=True) == ("steps", 0, False)
+    # one rank out of place: its copy, one launch
+    assert vc.vc_plan_form("allreduce", "ring", 1, 1000, "f32") == ("steps", 1, False)
+    # RHD folds 6 ranks into 4 and still keeps positions; DBT at 16 ranks, bf16: host ranges
+    assert vc.vc_plan_form("allreduce", "rhd", 6, 1000, "f32") == ("sliced", 1, False)
+    assert vc.vc_plan_form("allreduce", "dbt", 16, 1 << 20, "bf16") == ("sliced", 1, True)
+    for args in (("allreduce", "ring", 0, 10), ("allreduce", "ring", 65, 10), ("broadcast", "binomial", 4, 10, "f32", 4)):
+        with pytest.raises(VCError) as e:
+            vc.vc_plan_form(*args)
+        assert e.value.status == VC_ERR_INVALID_ARG, args
+    with pytest.raises(VCError) as e:
+        vc.vc_plan_form("reduce_scatter", "rhd", 4, 10, "f32")
+    assert e.value.status == VC_ERR_UNSUPPORTED
+    # a null output through the C ABI itself
+    L = vc.lib()
+    i = ctypes.c_int()
+    assert L.vc_plan_form(0, 1, 8, 1024, 0, 0, 0, 0, 0, None, ctypes.byref(i), ctypes.byref(i)) == VC_ERR_INVALID_ARG
