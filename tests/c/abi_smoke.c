@@ -48,6 +48,20 @@ int main(void) {
     vc_set_merge_steps(1);
     if (vc_get_merge_steps(NULL) != VC_ERR_INVALID_ARG) return 19;
   }
+  {
+    /* 8 ranks, 1 MiB of fp32 per rank: the 14-step ring in one sliced launch;
+       at 32 MiB per rank, above the slice limit, 14 launches */
+    int form = -1, launches = -1, hr = -1;
+    if (vc_plan_form(VC_COLL_ALLREDUCE, VC_ALGO_RING, 8, 1 << 18, VC_FLOAT32, VC_SUM, 0, 0, 0, &form, &launches,
+                     &hr) != VC_SUCCESS || form != VC_FORM_SLICED || launches != 1 || hr != 0)
+      return 20;
+    if (vc_plan_form(VC_COLL_ALLREDUCE, VC_ALGO_RING, 8, (size_t)1 << 23, VC_FLOAT32, VC_SUM, 0, 0, 0, &form,
+                     &launches, &hr) != VC_SUCCESS || form != VC_FORM_STEPS || launches != 14)
+      return 21;
+    if (vc_plan_form(VC_COLL_ALLREDUCE, VC_ALGO_RING, 8, 16, VC_FLOAT32, VC_SUM, 0, 0, 0, NULL, &launches, &hr) !=
+        VC_ERR_INVALID_ARG)
+      return 22;
+  }
   printf("ok %d\n", vc_version());
   return 0;
 }
