@@ -368,3 +368,24 @@ def test_library_form_of_degenerate_calls_and_bad_arguments():
     L = vc.lib()
     i = ctypes.c_int()
     assert L.vc_plan_form(0, 1, 8, 1024, 0, 0, 0, 0, 0, None, ctypes.byref(i), ctypes.byref(i)) == VC_ERR_INVALID_ARG
+
+
+def test_library_form_keeps_positions_below_2_pow_29():
+    """The sliced kernels keep element and byte offsets in 32 bits: with no
+    size limit, a call runs sliced only while its positions stay below 2^29
+    (AllGather, Gather and Scatter: N x count of them)."""
+    import collective_communication_algorithms_virtual_gb300 as vc
+
+    old = vc.vc_get_slice_limit()
+    try:
+        vc.vc_set_slice_limit((1 << 64) - 1)
+        assert vc.vc_plan_form("allgather", "ring", 8, 1 << 26, "f32")[0] == "sliced"  # last position 2^29 - 1
+        assert vc.vc_plan_form("allgather", "ring", 8, (1 << 26) + 4, "f32") == ("steps", 7, False)
+        assert vc.vc_plan_form("gather", "binomial", 8, (1 << 26) + 4, "f32")[0] == "steps"
+        assert vc.vc_plan_form("allreduce", "ring", 8, (1 << 29) - 8, "f32")[0] == "sliced"
+        assert vc.vc_plan_form("allreduce", "ring", 8, 1 << 29, "f32") == ("steps", 14, False)
+        # ReduceScatter partials above 16 MiB per rank: two slots a rank, positional at 4 ranks, not at 8
+        assert vc.vc_plan_form("reduce_scatter", "ring", 4, (1 << 27) - 4, "f32")[0] == "sliced"
+        assert vc.vc_plan_form("reduce_scatter", "ring", 8, 1 << 26, "f32")[0] == "steps"
+    finally:
+        vc.vc_set_slice_limit(old)
