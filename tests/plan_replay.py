@@ -282,3 +282,35 @@ def oracle_transfers(log) -> Counter:
         if t.n:
             tot[(t.step, t.src, t.dst, t.reduce)] += t.n
     return tot
+
+
+def slice_bytes(coll, N, count, es):
+    """What a sliced call carries per rank, against the size limit: AllReduce
+    and Reduce 4 bytes per element (fp32 / int32 data, or fp32 partials of
+    16-bit data), ReduceScatter likewise per input element, AllGather, Gather
+    and Scatter their N x count message, Broadcast its message; None for the
+    AllToAlls."""
+    return {"allreduce": count * 4, "reduce": count * 4, "reduce_scatter": count * N * 4,
+            "allgather": count * N * es, "gather": count * N * es, "scatter": count * N * es,
+            "broadcast": count * es}.get(coll)
+
+
+def predict_sliced(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0, op="sum", limit=16 << 20):
+    """The sliced form predicted from the described plan alone, with the checks
+    above: two or more steps, every operation keeping positions (one run; a
+    copy from one source), each byte at one position, origins aligned,
+    write-before-read, within the size limit and not in place (AllReduce
+    excepted).  Returns (sliced, host_ranges): the kernel derives operation
+    ranges itself only where every origin is 0 and the data is 4 bytes wide."""
+    plan, scratch = get_plan(coll, algo, N, count, dtype, root=root, inplace=inplace, nchunks=nchunks, op=op)
+    es = ESZ[DT[dtype]]
+    mem = Memory([None] * N, [0] * N, scratch)
+    sb = slice_bytes(coll, N, count, es)
+    ok = len(plan) >= 2 and sb is not None and sb <= limit and count < (1 << 29)
+    ok = ok and not (inplace and coll != "allreduce")
+    ok = ok and all(o["elem0"] >= 0 and o["nb"] == 1 and (o["reduce"] or len(o["src"]) == 1)
+                    for ops in plan for o in ops)
+    ok = ok and not position_places(plan, mem, 16 // es) and not reads_before_writes(plan, mem)
+    orig = origins(plan, es) if ok else []
+    ok = ok and all(o % need == 0 for o, need in orig)
+    return ok, ok and (es == 2 or any(o != 0 for o, _ in orig))

@@ -3,7 +3,8 @@ collective and algorithm, N in 1..16, ragged counts, roots, dtypes, ops,
 in-place and chunk counts.  Each plan the library would launch is replayed
 and must match the oracle bit for bit, move data between the same ranks in
 the same steps, read and write the oracle's algorithmic bytes, and have no
-intra-step hazards."""
+intra-step hazards.  The execution form the library reports for it
+(vc_plan_form) must be the one predicted from the plan's positions."""
 import random
 
 import numpy as np
@@ -12,7 +13,8 @@ import pytest
 from oracle import numerics, schedules
 from synthetic_inputs import rank_buffers
 
-from .plan_replay import DT, ESZ, NPT, Memory, get_plan, hazards, oracle_transfers, run_plan, transfers
+from .plan_replay import (DT, ESZ, NPT, Memory, get_plan, hazards, oracle_transfers, predict_sliced, run_plan,
+                          transfers)
 
 import collective_communication_algorithms_virtual_gb300 as vc
 
@@ -80,7 +82,6 @@ def _oracle(coll, algo, N, dtype, op, root, count, inplace, k, seed):
 @pytest.mark.parametrize("batch", range(8))
 def test_random_calls_replay_to_oracle(batch):
     rng = random.Random(1000 + batch)
-    es_of = ESZ[0]
     for i in range(50):
         coll, algo, N, dtype, op, root, count, inplace, k = _case(rng)
         es = ESZ[DT[dtype]]
@@ -110,7 +111,12 @@ def test_random_calls_replay_to_oracle(batch):
         assert transfers(plan) == oracle_transfers(res.log), ctx
         entries = vc.vc_plan_describe(coll, algo, N, count, dtype, root, inplace, k, op)[0]
         assert sum(e.n * e.nb * ESZ[e.dtype] for e in entries) == res.hbm_bytes, ctx
-    del es_of
+        # the library's form against the prediction from the plan's positions
+        form, launches, host_ranges = vc.vc_plan_form(coll, algo, N, count, dtype, root, inplace, k, op)
+        sliced, want_hr = predict_sliced(coll, algo, N, count, dtype, root, inplace, k, op)
+        assert (form == "sliced") == sliced, (ctx, form)
+        assert not sliced or (launches, host_ranges) == (1, want_hr), (ctx, launches, host_ranges)
+        assert coll != "alltoall" or form == "steps", (ctx, form)
 
 
 def test_corner_cases_replay_to_oracle():

@@ -29,8 +29,8 @@ from collective_communication_algorithms_virtual_gb300 import build
 from oracle import schedules
 from synthetic_inputs import rank_buffers
 
-from .plan_replay import (DT, ESZ, NPT, SCRATCH, Memory, get_plan, hazards, one_after_another, origins,
-                          position_places, reads_before_writes, run_plan, run_plan_sliced, shuffled)
+from .plan_replay import (DT, ESZ, NPT, SCRATCH, Memory, get_plan, hazards, one_after_another, position_places,
+                          predict_sliced, reads_before_writes, run_plan, run_plan_sliced, shuffled)
 
 ALGOS = tuple(a for a in schedules.ALGOS["allreduce"] if a != "fused")  # multi-step schedules
 
@@ -272,29 +272,6 @@ def test_reduce_scatter_partials_flat_up_to_16_mib():
 # size limit and not in place (AllReduce excepted).  Its kernel derives
 # operation ranges only where every origin is 0 (else "host ranges").
 
-def _slice_bytes(coll, N, count, es):
-    return {"allreduce": count * 4, "reduce": count * 4, "reduce_scatter": count * N * 4,
-            "allgather": count * N * es, "gather": count * N * es, "scatter": count * N * es,
-            "broadcast": count * es}.get(coll)
-
-
-def _predict(coll, algo, N, count, dtype, root, inplace, k):
-    plan, scratch = get_plan(coll, algo, N, count, dtype, root=root, inplace=inplace, nchunks=k)
-    es = ESZ[DT[dtype]]
-    G = 16 // es
-    mem = Memory([None] * N, [0] * N, scratch)
-    sb = _slice_bytes(coll, N, count, es)
-    ok = len(plan) >= 2 and sb is not None and sb <= (16 << 20) and count < (1 << 29)
-    ok = ok and not (inplace and coll != "allreduce")
-    ok = ok and all(op["elem0"] >= 0 and op["nb"] == 1 and (op["reduce"] or len(op["src"]) == 1)
-                    for ops in plan for op in ops)
-    ok = ok and not position_places(plan, mem, G) and not reads_before_writes(plan, mem)
-    orig = origins(plan, es) if ok else []
-    ok = ok and all(o % need == 0 for o, need in orig)
-    host_ranges = ok and (es == 2 or any(o != 0 for o, _ in orig))
-    return ok, host_ranges, len(plan)
-
-
 FORM_CASES = [("allreduce", a, 0) for a in ("ring", "rhd", "dbt", "mesh", "ring_hop", "fused")] + \
     [("reduce_scatter", a, 0) for a in ("ring", "fused")] + [("allgather", a, 0) for a in ("ring", "fused")] + \
     [("broadcast", a, 0) for a in ("binomial", "scatter_allgather", "fused")] + \
@@ -315,7 +292,7 @@ def test_library_form_matches_the_independent_checks(N, dtype):
                 for inplace in (False, True):
                     if inplace and coll not in ("allreduce", "broadcast", "reduce"):
                         continue
-                    sliced, hr, steps = _predict(coll, algo, N, count, dtype, root, inplace, k)
+                    sliced, hr = predict_sliced(coll, algo, N, count, dtype, root, inplace, k)
                     form, launches, got_hr = vc.vc_plan_form(coll, algo, N, count, dtype, root, inplace, k)
                     what = (coll, algo, N, count, dtype, root, inplace)
                     assert (form == "sliced") == sliced, (what, form)
