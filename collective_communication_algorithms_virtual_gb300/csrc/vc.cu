@@ -450,27 +450,56 @@ vc_status_t launch_mode(DeviceState* st, const Step& s, size_t i, size_t j, cons
 
 int op_ptrs(const Op& op) { return static_cast<int>(op.src.size() + op.dst.size()); }
 
+// The launch of step `s` that starts at operation i: all the remaining
+// operations if they fit the small parameter block (16 operations, 64
+// operand pointers), else the largest prefix that fits the large one (128,
+// 512; *large set).  Returns the end of its operations; i itself when one
+// operation alone has too many operands.
+size_t launch_span(const Step& s, size_t i, bool* large) {
+  size_t j = i;
+  int ptrs = 0;
+  while (j < s.ops.size() && j - i < 16 && ptrs + op_ptrs(s.ops[j]) <= 64) ptrs += op_ptrs(s.ops[j++]);
+  *large = j != s.ops.size();
+  if (!*large) return j;
+  j = i;
+  ptrs = 0;
+  while (j < s.ops.size() && j - i < 128 && ptrs + op_ptrs(s.ops[j]) <= 512) ptrs += op_ptrs(s.ops[j++]);
+  return j;
+}
+
 vc_status_t launch_step(DeviceState* st, const Step& s, const Bases& b, cudaStream_t stream, int* launches,
                         const LaunchCtx& tc) {
-  size_t i = 0;
-  while (i < s.ops.size()) {
-    // the largest prefix that fits the small parameter block, else the large one
-    size_t j = i;
-    int ptrs = 0;
-    while (j < s.ops.size() && j - i < 16 && ptrs + op_ptrs(s.ops[j]) <= 64) ptrs += op_ptrs(s.ops[j++]);
-    vc_status_t rc;
-    if (j == s.ops.size()) {
-      rc = launch_mode<dev::SmallParams>(st, s, i, j, b, stream, tc);
-    } else {
-      j = i;
-      ptrs = 0;
-      while (j < s.ops.size() && j - i < 128 && ptrs + op_ptrs(s.ops[j]) <= 512) ptrs += op_ptrs(s.ops[j++]);
-      if (j == i) return fail(VC_ERR_INVALID_ARG, "operation has too many operands");
-      rc = launch_mode<dev::LargeParams>(st, s, i, j, b, stream, tc);
-    }
+  for (size_t i = 0; i < s.ops.size();) {
+    bool large = false;
+    const size_t j = launch_span(s, i, &large);
+    if (j == i) return fail(VC_ERR_INVALID_ARG, "operation has too many operands");
+    const vc_status_t rc = large ? launch_mode<dev::LargeParams>(st, s, i, j, b, stream, tc)
+                                 : launch_mode<dev::SmallParams>(st, s, i, j, b, stream, tc);
     if (rc != VC_SUCCESS) return rc;
     ++*launches;
     i = j;
+  }
+  return VC_SUCCESS;
+}
+
+// Per-step execution of a plan: f(first step, step) for each step, where a
+// run of independent steps (Plan::launch_end) is one step holding their
+// operations in step order.  Stops at the first status other than success.
+template <class F>
+vc_status_t for_each_launch_group(const Plan& plan, F&& f) {
+  for (size_t si = 0; si < plan.steps.size();) {
+    const size_t se = plan.launch_end.empty() ? si + 1 : plan.launch_end[si];
+    vc_status_t rc;
+    if (se == si + 1) {
+      rc = f(si, plan.steps[si]);
+    } else {
+      Step merged = plan.steps[si];
+      for (size_t k = si + 1; k < se; ++k)
+        merged.ops.insert(merged.ops.end(), plan.steps[k].ops.begin(), plan.steps[k].ops.end());
+      rc = f(si, static_cast<const Step&>(merged));
+    }
+    if (rc != VC_SUCCESS) return rc;
+    si = se;
   }
   return VC_SUCCESS;
 }
@@ -683,11 +712,14 @@ void order_for_reuse(Plan* plan) {
 // barrier, and a barrier is needed only where a step reads what an earlier
 // one wrote or writes what an earlier one read or wrote.  A run of
 // consecutive steps of one kernel mode in which no step does either with
-// respect to the earlier steps of the run (Pairwise AllToAll's rounds: each
-// reads only the send buffers and writes its own output blocks) runs as one
-// launch: its steps' operations in step order, so each block still takes the
-// rounds in order, without a barrier between them.  Every operation's
-// operands and bytes are unchanged.
+// respect to the earlier steps of the run runs as one launch: its steps'
+// operations in step order, so each block still takes the steps in order,
+// without a barrier between them.  Every operation's operands and bytes are
+// unchanged.  Such runs: Pairwise AllToAll's rounds (each reads only the send
+// buffers and writes its own output blocks), the Ring AllToAll's local copy
+// with its first round, the Mesh AllReduce's copies of the result to each
+// rank, and binomial steps at rank counts that are not powers of 2, where a
+// rank reached in one step forwards nothing in the next.
 std::atomic<int> g_merge_steps{1};
 void mark_independent_steps(Plan* plan) {
   plan->launch_end.clear();
@@ -1539,20 +1571,10 @@ vc_status_t run(const Call& c) {
     rc = launch_plan(*dp, dev, N, sends, recvs, scratch, c.stream, tc, st, slice_groups);
     if (rc == VC_SUCCESS) launches = 1;
   } else {
-    for (size_t si = 0; si < plan.steps.size();) {
+    rc = for_each_launch_group(plan, [&](size_t si, const Step& s) {
       tc.step = static_cast<int>(si);
-      const size_t se = plan.launch_end.empty() ? si + 1 : plan.launch_end[si];
-      if (se == si + 1) {
-        rc = launch_step(st, plan.steps[si], b, c.stream, &launches, tc);
-      } else {  // independent steps: one launch, their operations in step order
-        Step merged = plan.steps[si];
-        for (size_t k = si + 1; k < se; ++k)
-          merged.ops.insert(merged.ops.end(), plan.steps[k].ops.begin(), plan.steps[k].ops.end());
-        rc = launch_step(st, merged, b, c.stream, &launches, tc);
-      }
-      if (rc != VC_SUCCESS) break;
-      si = se;
-    }
+      return launch_step(st, s, b, c.stream, &launches, tc);
+    });
   }
   if (scratch) {
     cudaError_t e = cudaFreeAsync(scratch, c.stream);
@@ -1958,11 +1980,19 @@ VC_EXPORT vc_status_t vc_plan_form(vc_coll_t coll, vc_algo_t algo, int nranks, s
     } else if (gate.cluster && dp.eligible && static_cast<uint64_t>(dp.max_step_bytes) <= gate.cluster_limit) {
       *form = VC_FORM_CLUSTER;
       *launches = 1;
-    } else {
+    } else {  // as run() launches it: empty steps launch nothing, large ones split
       *form = VC_FORM_STEPS;
       int n = 0;
-      for (size_t si = 0; si < plan.steps.size(); ++n)
-        si = plan.launch_end.empty() ? si + 1 : plan.launch_end[si];
+      const vc_status_t rs = for_each_launch_group(plan, [&](size_t, const Step& s) -> vc_status_t {
+        for (size_t i = 0; i < s.ops.size(); ++n) {
+          bool large = false;
+          const size_t j = launch_span(s, i, &large);
+          if (j == i) return fail(VC_ERR_INVALID_ARG, "operation has too many operands");
+          i = j;
+        }
+        return VC_SUCCESS;
+      });
+      if (rs != VC_SUCCESS) return rs;
       *launches = n;
     }
     return VC_SUCCESS;

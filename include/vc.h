@@ -483,12 +483,16 @@ vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank);
  * barrier is needed only where a step reads what an earlier one wrote, or
  * writes what an earlier one read or wrote.  When `on` (the default), a run of
  * consecutive steps of one kind in which no step does either with respect to
- * the earlier steps of the run -- Pairwise AllToAll's rounds, each reading
- * only the send buffers and writing its own output blocks, and the Ring
- * AllToAll's local copy with its first round -- runs as one launch, the steps'
- * operations in step order (each block takes them in that order), without a
- * barrier between them.  Every operation, operand and byte is unchanged;
- * vc_plan_describe still reports the schedule's steps.  Process-wide.
+ * the earlier steps of the run runs as one launch, the steps' operations in
+ * step order (each block takes them in that order), without a barrier
+ * between them.  Such runs: Pairwise AllToAll's rounds, each reading only the
+ * send buffers and writing its own output blocks; the Ring AllToAll's local
+ * copy with its first round; the Mesh AllReduce's copies of the result to
+ * each rank; binomial steps (Broadcast, Scatter, Gather, the pipelined
+ * tree) at rank counts that are not powers of 2, where a rank reached in one
+ * step forwards nothing in the next.  Every operation, operand and byte is
+ * unchanged; vc_plan_describe still reports the schedule's steps, and
+ * vc_plan_form the launches.  Process-wide.
  */
 vc_status_t vc_set_merge_steps(int on);
 vc_status_t vc_get_merge_steps(int* on);

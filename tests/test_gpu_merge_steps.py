@@ -2,7 +2,9 @@
 
 Pairwise AllToAll's rounds read only the send buffers and write their own
 output blocks, and the Ring AllToAll's local copy touches nothing its first
-round does, so those steps share a launch by default.  With the setting on
+round does, so those steps share a launch by default (as do the Mesh
+AllReduce's result copies and some binomial steps at rank counts that are not
+powers of 2, which the randomised sweep covers).  With the setting on
 and off, every result must equal the C++ oracle's simulation bit for bit, the
 launch trace must show the shared launch (or one launch per round), and canary
 bands catch stray writes.  Schedules whose every step depends on the one

@@ -311,6 +311,15 @@ def test_library_form_above_the_limit_and_for_merged_rounds():
     # Pairwise AllToAll: its rounds share one launch; Bruck runs a launch per step
     assert vc.vc_plan_form("alltoall", "pairwise", 8, 1024, "f32") == ("steps", 1, False)
     assert vc.vc_plan_form("alltoall", "bruck", 8, 128, "f32") == ("steps", 3, False)
+    # 16 ranks: 16 rounds of 16 two-operand copies, over the 128 operations of
+    # the large parameter block: two launches
+    assert vc.vc_plan_form("alltoall", "pairwise", 16, 1024, "f32") == ("steps", 2, False)
+    # Mesh AllReduce, 16 ranks, 20 MiB per rank: 15 reduce steps into the root,
+    # then its 15 copies of the result, independent, in one launch
+    assert vc.vc_plan_form("allreduce", "mesh", 16, 5 << 20, "f32") == ("steps", 16, False)
+    # binomial Broadcast of 64 MiB over 5 ranks (above the slice limit): 0 -> 4
+    # and 0 -> 2 touch different ranks (rank 4 forwards nothing), then 0 -> 1, 2 -> 3
+    assert vc.vc_plan_form("broadcast", "binomial", 5, 16 << 20, "f32") == ("steps", 2, False)
     old = vc.vc_get_slice_limit()
     try:
         vc.vc_set_slice_limit(0)
