@@ -314,3 +314,62 @@ def predict_sliced(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0
     orig = origins(plan, es) if ok else []
     ok = ok and all(o % need == 0 for o, need in orig)
     return ok, ok and (es == 2 or any(o != 0 for o, _ in orig))
+
+
+def step_kind(ops):
+    """A step's kernel kind as the plan description gives it: 0 for a copy
+    step, 1 + op for a reduction step (one data type per plan).  None for a
+    step without operations."""
+    return ops[0]["red"] if ops else None
+
+
+def launch_groups(plan, ident) -> list:
+    """Runs of consecutive steps of one kind in which no step reads bytes an
+    earlier step of the run wrote, or writes bytes an earlier one read or
+    wrote: each (first, end) range may run as one launch.  `ident(kind,
+    owner)` names the buffer an operand lies in, so that buffers that are one
+    (an in-place call's send and receive buffers of a rank) compare equal.  An
+    operand's bytes are the hull of its nb runs."""
+
+    def spans(ops, role):
+        out = []
+        for op in ops:
+            for (k, o, dt, off, stride) in op[role]:
+                last = off + (op["nb"] - 1) * stride
+                out.append((ident(k, o), min(off, last), max(off, last) + op["n"] * ESZ[dt]))
+        return out
+
+    def hit(a, b):
+        return any(x[0] == y[0] and x[1] < y[2] and y[1] < x[2] for x in a for y in b)
+
+    groups, s = [], 0
+    while s < len(plan):
+        reads, writes = spans(plan[s], "src"), spans(plan[s], "dst")
+        e = s + 1
+        while e < len(plan) and step_kind(plan[e]) == step_kind(plan[s]):
+            r, w = spans(plan[e], "src"), spans(plan[e], "dst")
+            if hit(writes, r) or hit(writes, w) or hit(reads, w):
+                break
+            reads, writes, e = reads + r, writes + w, e + 1
+        groups.append((s, e))
+        s = e
+    return groups
+
+
+def launches_of(ops) -> int:
+    """Launches one (merged) step takes: all remaining operations at once if
+    they fit the small kernel parameter block (16 operations, 64 operand
+    pointers), else the largest prefix that fits the large one (128, 512)."""
+    n, i = 0, 0
+    ptrs = [len(op["src"]) + len(op["dst"]) for op in ops]
+    while i < len(ops):
+        j, p = i, 0
+        while j < len(ops) and j - i < 16 and p + ptrs[j] <= 64:
+            p, j = p + ptrs[j], j + 1
+        if j < len(ops):
+            j, p = i, 0
+            while j < len(ops) and j - i < 128 and p + ptrs[j] <= 512:
+                p, j = p + ptrs[j], j + 1
+            assert j > i, "an operation with more operand pointers than the large block holds"
+        n, i = n + 1, j
+    return n
