@@ -411,7 +411,7 @@ vc_status_t vc_trace_read(vc_trace_record_t* records, size_t capacity, size_t* n
  *   - the schedule's reduction steps share one data type and op (true of
  *     every schedule of this library),
  *   - its description fits the kernel's shared memory (96 KB; e.g. the ring
- *     AllReduce up to about 24 ranks),
+ *     AllReduce up to 21 ranks),
  *   - every buffer pointer of the call is 16-byte aligned,
  *   - it is not an AllToAll (their steps of many small block copies measured
  *     faster as one launch a step; a Pairwise AllToAll's independent rounds
@@ -466,7 +466,10 @@ vc_status_t vc_get_single_launch(size_t* max_step_bytes);
  * positions share, and do not run sliced at 5 ranks or more.  In-place
  * calls other than AllReduce, and the AllToAlls, take the other forms.  The
  * conditions of single-launch execution on alignment and the resident
- * description apply as well.  max_bytes_per_rank: 0 disables it, SIZE_MAX
+ * description apply as well, and the description with each operation's
+ * element range and each operand's address must fit the kernel's 96 KB of
+ * shared memory (the ring AllReduce up to 18 ranks, the ring ReduceScatter
+ * and AllGather up to 25 and 26, the tree schedules up to 64).  max_bytes_per_rank: 0 disables it, SIZE_MAX
  * applies it to every eligible call.  Default VC_SLICE_LIMIT_DEFAULT: up to
  * 16 MiB per rank the form measured faster than the cluster form and than
  * per-step launches (8 ranks, fp32 and bf16, GB300; above, the whole GPU's

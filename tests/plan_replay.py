@@ -301,7 +301,10 @@ def predict_sliced(coll, algo, N, count, dtype, root=0, inplace=False, nchunks=0
     copy from one source), each byte at one position, origins aligned,
     write-before-read, within the size limit and not in place (AllReduce
     excepted).  Returns (sliced, host_ranges): the kernel derives operation
-    ranges itself only where every origin is 0 and the data is 4 bytes wide."""
+    ranges itself only where every origin is 0 and the data is 4 bytes wide.
+    Left out: the library also needs the plan's description to fit a block's
+    shared memory, which holds at the rank counts the tests use (16 or
+    fewer; the ring AllReduce's is the first to outgrow it, at 19)."""
     plan, scratch = get_plan(coll, algo, N, count, dtype, root=root, inplace=inplace, nchunks=nchunks, op=op)
     es = ESZ[DT[dtype]]
     mem = Memory([None] * N, [0] * N, scratch)

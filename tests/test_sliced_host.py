@@ -375,3 +375,20 @@ def test_library_form_keeps_positions_below_2_pow_29():
         assert vc.vc_plan_form("reduce_scatter", "ring", 8, 1 << 26, "f32")[0] == "steps"
     finally:
         vc.vc_set_slice_limit(old)
+
+
+def test_library_form_needs_the_description_in_shared_memory():
+    """Past 18 ranks the Ring AllReduce's description (2(N-1) steps of N
+    operations) with the sliced kernel's range and address tables outgrows a
+    block's 96 KB of shared memory: the call keeps positions, but runs as one
+    cluster, whose kernel holds the description alone, up to 21 ranks, and per
+    step beyond."""
+    import collective_communication_algorithms_virtual_gb300 as vc
+
+    assert vc.vc_plan_form("allreduce", "ring", 18, 1024, "f32")[0] == "sliced"
+    assert predict_sliced("allreduce", "ring", 19, 1024, "f32")[0]
+    assert vc.vc_plan_form("allreduce", "ring", 19, 1024, "f32")[0] == "cluster"
+    assert vc.vc_plan_form("allreduce", "ring", 21, 1024, "f32")[0] == "cluster"
+    assert vc.vc_plan_form("allreduce", "ring", 22, 1024, "f32") == ("steps", 42, False)
+    # the tree schedules' descriptions stay small up to 64 ranks
+    assert vc.vc_plan_form("allreduce", "dbt", 64, 1024, "f32")[0] == "sliced"
