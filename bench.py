@@ -305,6 +305,8 @@ def run_ours(args) -> int:
     import collective_communication_algorithms_virtual_gb300 as vc
     from synthetic_inputs import uniform_pm1_f32
 
+    if args.slice_limit is not None:  # e.g. 0: small calls take the cluster form, for profiling it
+        vc.vc_set_slice_limit(args.slice_limit)
     global ALGOS
     ALGOS = [a for a in args.algos.split(",") if a]
     N, M = NVR, int(args.mib_per_rank * (1 << 20)) // 16 * 16
@@ -940,6 +942,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-per-algo", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other workload configurations")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--slice-limit", type=int, default=None,
+                    help="bytes per rank up to which calls take the sliced form (default: the library's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--e2e-steps", type=int, default=8)
