@@ -170,11 +170,6 @@ def t_pipe_tree_bcast(N, M, alpha, beta, k):  # eq. pipe-tree-bcast
     return (ceil_log2(N) + k - 1) * (alpha + M / (k * beta))
 
 
-def bcast_switch_point(N, alpha, beta):
-    """M* ~ 2 N alpha beta, below the algorithm comparison table."""
-    return 2 * N * alpha * beta
-
-
 def scatter_latency_lower_bound(N, alpha):  # eq. onetoall-scatter-delay-lb
     return ceil_log2(N) * alpha
 

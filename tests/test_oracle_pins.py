@@ -137,7 +137,38 @@ def test_bcast_lower_bounds():
     assert cm.t_binomial_bcast(N, M, a, b) >= lb
     assert cm.t_chain_bcast(N, M, a, b) >= cm.t_binomial_bcast(N, M, a, b)
     assert cm.t_bcast_tree(N, M, a, b) == pytest.approx(cm.t_binomial_bcast(N, M, a, b))
-    assert cm.bcast_switch_point(N, a, b) == pytest.approx(2 * N * a * b)
+
+
+@pytest.mark.parametrize("N", [3, 4, 8, 16, 64])
+def test_binomial_and_scatter_allgather_broadcast_cross_where_derived(N):
+    """The binomial Broadcast (eq. binomial-bcast) and Scatter + AllGather
+    (eq. binomial-scatter plus eq. model-algo-ring-allgather) cost the same at
+    M* = (N-1) alpha beta / (ceil(log2 N) - 2(N-1)/N), derived by hand from
+    L(alpha + M/beta) = (L + N - 1) alpha + 2 (N-1) M / (N beta): 5.6 alpha
+    beta at N = 8.  (The Bcast/Scatter page's rule of thumb below its
+    comparison table, M* ~ 2 N alpha beta, is context only: 16 alpha beta at
+    N = 8.)  Below it the tree is cheaper, above it Scatter + AllGather."""
+    a, b = 5e-6, 450e9
+    L = (N - 1).bit_length()
+    Ms = (N - 1) * a * b / (L - 2 * (N - 1) / N)
+
+    def sag(M):
+        return cm.t_binomial_scatter(N, M, a, b) + cm.t_ring_allgather(N, M, a, b)
+
+    assert cm.t_binomial_bcast(N, Ms, a, b) == pytest.approx(sag(Ms), rel=1e-12)
+    assert cm.t_binomial_bcast(N, Ms / 2, a, b) < sag(Ms / 2)
+    assert cm.t_binomial_bcast(N, Ms * 2, a, b) > sag(Ms * 2)
+    if N == 8:
+        assert Ms / (a * b) == pytest.approx(5.6)
+
+
+def test_two_rank_broadcast_never_prefers_scatter_allgather():
+    """At N = 2 the denominator above is 0: Scatter + AllGather costs one
+    more alpha than the tree's single step at every size."""
+    a, b = 5e-6, 450e9
+    for M in (1.0, 1e4, 1e8, 1e12):
+        sag = cm.t_binomial_scatter(2, M, a, b) + cm.t_ring_allgather(2, M, a, b)
+        assert sag - cm.t_binomial_bcast(2, M, a, b) == pytest.approx(a)
 
 
 # ----------------------------------------------------------------------------
