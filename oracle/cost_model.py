@@ -90,11 +90,6 @@ def t_a2a_pairwise(N, M, alpha, beta):  # eq. model-algo-a2a-pairwise
     return (N - 1) * (alpha + M / (N * beta))
 
 
-def t_a2a_pairwise_full_mesh(N, M, alpha, beta):
-    """All N-1 rounds in parallel on a fully connected fabric."""
-    return alpha + M / (N * beta)
-
-
 def t_a2a_bruck(N, M, alpha, beta):  # eq. model-algo-a2a-bruck (as printed)
     return ceil_log2(N) * alpha + (N - 1) / N * M / beta
 

@@ -162,6 +162,22 @@ def test_binomial_and_scatter_allgather_broadcast_cross_where_derived(N):
         assert Ms / (a * b) == pytest.approx(5.6)
 
 
+@pytest.mark.parametrize("N", [2, 4, 8, 64])
+def test_naive_scatter_meets_the_bandwidth_bound_not_the_latency_bound(N):
+    """The root sending each rank its piece in turn (eq. onetoall-scatter-
+    naive): the Bcast/Scatter page notes that its bandwidth term reaches the
+    lower bound (eq. onetoall-scatter-bw-lb) while its latency term grows as
+    O(N), above the ceil(log2 N) alpha of eq. onetoall-scatter-delay-lb from
+    N = 3 on; the binomial Scatter meets both."""
+    a, b = 5e-6, 450e9
+    for M in (1e3, 1e9):
+        assert cm.t_scatter_naive(N, M, 0.0, b) == pytest.approx(cm.scatter_bandwidth_lower_bound(N, M, b))
+        latency = cm.t_scatter_naive(N, M, a, b) - cm.t_scatter_naive(N, M, 0.0, b)
+        assert latency == pytest.approx((N - 1) * a)
+        assert (latency > cm.scatter_latency_lower_bound(N, a) * (1 + 1e-9)) == (N > 2)
+        assert cm.t_binomial_scatter(N, M, a, b) <= cm.t_scatter_naive(N, M, a, b) * (1 + 1e-12)
+
+
 def test_two_rank_broadcast_never_prefers_scatter_allgather():
     """At N = 2 the denominator above is 0: Scatter + AllGather costs one
     more alpha than the tree's single step at every size."""
@@ -252,6 +268,43 @@ def test_binomial_bcast_bandwidth(sim):
         res = sim.broadcast(A, N, 0, "binomial", "i32")
         assert res.nsteps == cm.ceil_log2(N)
         assert res.log.bandwidth_bytes() == cm.ceil_log2(N) * 160
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16])
+def test_printed_times_equal_the_simulated_steps(N, sim):
+    """Each schedule's printed time is the alpha-beta model summed over its
+    steps: every step costs alpha plus its largest message over beta.  Summed
+    over the simulated transfer log that gives the printed formula exactly, for
+    the ring AllReduce, ReduceScatter and AllGather (eqs. model-algo-ring-ar,
+    -ring-reducescatter, -ring-allgather), RHD and DBT (eqs. model-algo-rhd-ar,
+    -dbt-ar), Pairwise AllToAll (eq. model-algo-a2a-pairwise), the binomial
+    Broadcast, Scatter and Gather (eqs. binomial-bcast, binomial-scatter,
+    onetoall-gather-scatter-duality) and the tree Reduce (eq.
+    model-algo-reduce-tree), at powers of 2, where log2 N is whole."""
+    a, b = 5e-6, 450e9
+    count = N * 64
+    M = count * 4
+
+    def logged(res):
+        per = res.log.max_message_bytes_per_step()
+        return sum(a + per[s] / b for s in per)
+
+    xs = rank_buffers("small_ints_f32", 7, N, count)
+    blocks = [x[: count // N] for x in xs]
+    cases = [
+        (sim.allreduce(xs, "ring", "f32"), cm.t_ring_ar(N, M, a, b)),
+        (sim.allreduce(xs, "rhd", "f32"), cm.t_rhd_ar(N, M, a, b)),
+        (sim.allreduce(xs, "dbt", "f32"), cm.t_dbt_ar(N, M, a, b)),
+        (sim.reduce_scatter(xs, "ring", "f32"), cm.t_ring_reducescatter(N, M, a, b)),
+        (sim.allgather(blocks, "ring", "f32"), cm.t_ring_allgather(N, M, a, b)),
+        (sim.alltoall(xs, "pairwise", "f32"), cm.t_a2a_pairwise(N, M, a, b)),
+        (sim.broadcast(xs[0], N, 0, "binomial", "f32"), cm.t_binomial_bcast(N, M, a, b)),
+        (sim.scatter(xs[0], N, 0, "binomial", "f32"), cm.t_binomial_scatter(N, M, a, b)),
+        (sim.gather(blocks, 0, "binomial", "f32"), cm.t_gather(N, M, a, b)),
+        (sim.reduce(xs, 0, "binomial", "f32"), cm.t_reduce_tree(N, M, a, b)),
+    ]
+    for i, (res, printed) in enumerate(cases):
+        assert logged(res) == pytest.approx(printed, rel=1e-12), (i, logged(res), printed)
 
 
 @pytest.mark.parametrize("N", [8])
