@@ -302,13 +302,13 @@ struct Sim {
     return m;
   }
 
-  void deliver(const Msg& m, const std::vector<std::vector<uint8_t>>& pb, const std::vector<std::vector<Lane>>& pl,
-               size_t mi) {
+  void deliver(const Msg& m, const std::vector<std::vector<uint8_t>>& sent_bytes,
+               const std::vector<std::vector<Lane>>& sent_lanes, size_t mi) {
     int64_t at = 0;
     for (const Piece& p : m.pieces) {
       if (p.dst->lanes) {
         Lane* d = p.dst->l.data() + p.doff;
-        const Lane* s = pl[mi].data() + at;
+        const Lane* s = sent_lanes[mi].data() + at;
         if (m.rec.reduce)
           combine_into(d, s, p.n, op, lanes_are_float(dt));
         else
@@ -320,7 +320,7 @@ struct Sim {
             d[i] = widen_elem(tmp, dt);
           }
       } else {
-        std::memcpy(p.dst->b.data() + p.doff * p.dst->es, pb[mi].data() + at * p.dst->es,
+        std::memcpy(p.dst->b.data() + p.doff * p.dst->es, sent_bytes[mi].data() + at * p.dst->es,
                     static_cast<size_t>(p.n * p.dst->es));
       }
       at += p.n;
