@@ -6,7 +6,6 @@ import io
 import json
 import os
 import socket
-import sys
 from contextlib import redirect_stdout
 
 import pytest

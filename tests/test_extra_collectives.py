@@ -7,7 +7,6 @@ from oracle import cost_model as cm
 from oracle import numerics, schedules, selection
 from synthetic_inputs import int32_bits, rank_buffers, small_ints_f32
 
-from .conftest import read_golden
 from .plan_replay import ESZ, Memory, get_plan, hazards, oracle_transfers, run_plan, transfers
 
 import collective_communication_algorithms_virtual_gb300 as vc

@@ -1,6 +1,5 @@
 """Pipelined Broadcasts, Gather and Tree Reduce on the GPU against the oracle
 (bit for bit; canary bands around every buffer)."""
-import numpy as np
 import pytest
 import torch
 

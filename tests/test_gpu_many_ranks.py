@@ -7,7 +7,6 @@ Pairwise with 64 rounds merged into launches of at most 128 operations.
 Bit for bit against the C++ oracle's simulation of the same schedule, with
 canary bands around every buffer.
 """
-import numpy as np
 import pytest
 import torch
 

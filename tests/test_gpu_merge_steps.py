@@ -10,7 +10,6 @@ launch trace must show the shared launch (or one launch per round), and canary
 bands catch stray writes.  Schedules whose every step depends on the one
 before (Ring AllReduce) keep one launch per step either way.
 """
-import numpy as np
 import pytest
 import torch
 

@@ -6,7 +6,7 @@ import pytest
 
 from oracle import cost_model as cm
 from oracle import numerics, orders, schedules
-from synthetic_inputs import int32_bits, rank_buffers
+from synthetic_inputs import rank_buffers
 
 from .plan_replay import DT, ESZ, NPT, Memory, get_plan, hazards, oracle_transfers, run_plan, transfers
 

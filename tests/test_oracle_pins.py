@@ -18,7 +18,7 @@ import torch
 from oracle import cost_model as cm
 from oracle import cxx, numerics, orders, schedules
 from oracle.partition import chunk_elems, chunk_range
-from synthetic_inputs import int32_bits, rank_buffers, small_ints_f32, uniform_pm1_f32
+from synthetic_inputs import int32_bits, rank_buffers, small_ints_f32
 
 from . import witness
 

@@ -7,7 +7,6 @@ Binary Tree, with Recursive Halving-Doubling preferred whenever N is a power
 of 2 (it has Ring's bandwidth term and DBT's latency term); the HBM model
 picks the fused one-pass schedule, which has the fewest steps and bytes.
 """
-import numpy as np
 import pytest
 
 import collective_communication_algorithms_virtual_gb300 as vc
