@@ -124,10 +124,6 @@ class _Bytes:
         self.total += n * sum(sizes)
 
 
-def _is_pow2(n: int) -> bool:
-    return n >= 1 and (n & (n - 1)) == 0
-
-
 def _ceil_log2(n: int) -> int:
     return (n - 1).bit_length()
 
