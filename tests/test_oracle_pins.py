@@ -307,6 +307,29 @@ def test_printed_times_equal_the_simulated_steps(N, sim):
         assert logged(res) == pytest.approx(printed, rel=1e-12), (i, logged(res), printed)
 
 
+def test_ring_and_mesh_toy_example(golden, sim):
+    """The hccl article's toy example (100 GB over 100 GB/s links, 32 nodes:
+    Ring about 2 s, Mesh about 32 s, the root the bottleneck), against the
+    simulated transfer logs scaled to that size: the busiest Ring rank sends
+    2 (N-1)/N of the data (1.94 s); the Mesh root takes in the other N-1
+    ranks' data (31 s), within N/(N-1) of the page's N x data / bandwidth."""
+    rows = {algo: (int(n), float(t)) for algo, n, t in golden("ring_mesh_toy_n32.txt")}
+    N = rows["ring"][0]
+    count = N * 16
+    xs = rank_buffers("small_ints_f32", 9, N, count)
+    scale = 1.0 / (count * 4)  # seconds per simulated byte: the page's data takes 1 s at its bandwidth
+    ring = sim.allreduce(xs, "ring", "f32").log
+    t_ring = max(ring.bytes_sent_by(r) for r in range(N)) * scale
+    assert t_ring == pytest.approx(2 * (N - 1) / N)
+    assert t_ring == pytest.approx(rows["ring"][1], rel=1.0 / N)
+    mesh = sim.allreduce(xs, "mesh", "f32").log
+    t_root = max(mesh.bytes_received_by(r) for r in range(N)) * scale
+    assert t_root == pytest.approx(N - 1)
+    assert t_root == pytest.approx(rows["mesh"][1], rel=1.0 / N)
+    # every other Mesh rank takes in one copy of the result: the root is the bottleneck
+    assert sorted(mesh.bytes_received_by(r) for r in range(N))[-2] * scale == pytest.approx(1.0)
+
+
 @pytest.mark.parametrize("N", [8])
 def test_hbm_bytes_closed_forms(N, sim):
     """Algorithmic bytes at N = 8, fp32, M per rank."""
