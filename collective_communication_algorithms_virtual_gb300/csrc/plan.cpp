@@ -825,8 +825,9 @@ namespace {
 
 // The pages' alpha-beta formulas with M the per-rank message in bytes
 // (latency-formula page: eqs. model-algo-ring-ar, -rhd-ar, -dbt-ar,
-// -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck;
-// Broadcast/Scatter page: eqs. binomial-bcast, binomial-scatter).
+// -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck, -a2a-ring,
+// -reduce-tree; Broadcast/Scatter page: eqs. binomial-bcast, binomial-scatter,
+// onetoall-gather-scatter-duality, pipe-chain-bcast, pipe-tree-bcast).
 double link_time(Coll c, Algo a, int N, double M, double al, double be, double k) {
   const double n = N, lg = std::log2(n), cl = ceil_log2(N);
   switch (c) {

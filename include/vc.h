@@ -80,10 +80,10 @@ typedef enum { VC_SUM = 0, VC_MAX = 1, VC_MIN = 2 } vc_op_t;
 
 typedef enum {
   VC_ALGO_FUSED = 0,             /* one pass over all ranks: every collective          */
-  VC_ALGO_RING = 1,              /* AllReduce, ReduceScatter, AllGather                */
-  VC_ALGO_RHD = 2,               /* AllReduce, nranks a power of 2                     */
+  VC_ALGO_RING = 1,              /* AllReduce, ReduceScatter, AllGather, AllToAll      */
+  VC_ALGO_RHD = 2,               /* AllReduce; fold-in when nranks is not 2^k          */
   VC_ALGO_DBT = 3,               /* AllReduce                                          */
-  VC_ALGO_BINOMIAL = 4,          /* Broadcast, Scatter                                 */
+  VC_ALGO_BINOMIAL = 4,          /* Broadcast, Scatter, Gather, Reduce                 */
   VC_ALGO_SCATTER_ALLGATHER = 5, /* Broadcast                                          */
   VC_ALGO_PAIRWISE = 6,          /* AllToAll                                           */
   VC_ALGO_BRUCK = 7,             /* AllToAll                                           */
@@ -153,7 +153,8 @@ vc_status_t vc_allgather(const void* const* send, void* const* recv, int nranks,
  * sections.
  *   send_root, recv[r]: `count` elements.  send_root == recv[root] is allowed.
  *   algo: FUSED (one read, N writes), BINOMIAL (ceil(log2 N) steps),
- *   SCATTER_ALLGATHER (binomial Scatter of N chunks, then a Ring AllGather).
+ *   SCATTER_ALLGATHER (binomial Scatter of N chunks, then a Ring AllGather),
+ *   PIPE_CHAIN or PIPE_TREE (as vc_broadcast_pipelined with nchunks = 0).
  */
 vc_status_t vc_broadcast(const void* send_root, void* const* recv, int nranks, size_t count,
                          vc_dtype_t dtype, int root, vc_algo_t algo, vc_stream_t stream);
@@ -194,8 +195,10 @@ vc_status_t vc_alltoall(const void* const* send, void* const* recv, int nranks, 
  *     sweep), beta = 6.6e12 B/s (measured HBM copy rate).
  *   VC_COST_LINK: the pages' own formulas with M the per-rank message and
  *     beta a link bandwidth (eqs. model-algo-ring-ar, -rhd-ar, -dbt-ar,
- *     -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck;
- *     Broadcast/Scatter page eqs. binomial-bcast, binomial-scatter).
+ *     -ring-reducescatter, -ring-allgather, -a2a-pairwise, -a2a-bruck,
+ *     -a2a-ring, -reduce-tree; Broadcast/Scatter page eqs. binomial-bcast,
+ *     binomial-scatter, onetoall-gather-scatter-duality, pipe-chain-bcast,
+ *     pipe-tree-bcast).
  *     Candidates: the pages' algorithms only (no fused).  Defaults: alpha =
  *     5e-6 s, beta = 450e9 B/s, the page's NVLink example.
  *
@@ -210,7 +213,8 @@ vc_status_t vc_get_cost_model(vc_cost_policy_t* policy, double* alpha_s, double*
 /*
  * The algorithm VC_ALGO_AUTO would run for these arguments and the time the
  * model predicts for it (host only, no CUDA call).  `count` follows the
- * collective's convention; `root` is used by Broadcast and Scatter.
+ * collective's convention; `root` is used by the rooted collectives
+ * (Broadcast, Scatter, Gather, Reduce).
  */
 vc_status_t vc_select_algo(vc_coll_t coll, int nranks, size_t count, vc_dtype_t dtype, int root,
                            vc_algo_t* algo, double* predicted_s);
