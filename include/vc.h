@@ -283,8 +283,8 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
  * op (reduction steps) or copies its single source (copy steps), and writes
  * the result to each of its
  * destinations; it covers `nb` runs of `n` elements, run b starting
- * b*stride_bytes after run 0.  All operations of one step are independent and
- * run in one launch; steps run in order.
+ * b*stride_bytes after run 0.  All operations of one step are independent;
+ * steps run in order (vc_plan_form reports how they are launched).
  *   buf: 0 send, 1 recv, 2 library scratch; owner: the rank that holds it;
  *   byte_off: from the start of that rank's buffer (scratch: of the scratch
  *   block); dtype: storage type of the operand; elem0: the element position
