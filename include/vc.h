@@ -325,11 +325,12 @@ vc_status_t vc_plan_describe(vc_coll_t coll, vc_algo_t algo, int nranks, size_t 
  * current settings (vc_set_slice_limit, vc_set_single_launch,
  * vc_set_merge_steps), on 16-byte aligned buffers with a resident plan
  * description (a call whose buffers are not aligned, or whose shape is first
- * seen while its stream is captured, runs its steps one launch each).
+ * seen while its stream is captured, runs per step).
  *   *form: VC_FORM_SLICED (one launch over the GPU, each thread carrying its
  *     group of positions through every step), VC_FORM_CLUSTER (one launch of
  *     one thread-block cluster with a barrier between steps) or VC_FORM_STEPS
- *     (one launch per step, or per run of independent steps);
+ *     (one launch per step, or per run of independent steps, and more than
+ *     one for a step whose operations outgrow the kernel parameter block);
  *   *launches: the launches the call makes (1 for the one-launch forms; 0 for
  *     a call with nothing to do);
  *   *host_ranges: for the sliced form, 1 if its kernel reads the operation
