@@ -500,7 +500,8 @@ vc_status_t vc_get_slice_limit(size_t* max_bytes_per_rank);
  * tree) at rank counts that are not powers of 2, where a rank reached in one
  * step forwards nothing in the next.  Every operation, operand and byte is
  * unchanged; vc_plan_describe still reports the schedule's steps, and
- * vc_plan_form the launches.  Process-wide.
+ * vc_plan_form the launches.  Process-wide; applies to plans built after the
+ * call (the plan cache is cleared).
  */
 vc_status_t vc_set_merge_steps(int on);
 vc_status_t vc_get_merge_steps(int* on);
