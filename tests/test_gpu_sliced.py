@@ -1,5 +1,5 @@
-"""The sliced form of AllReduce, ReduceScatter, AllGather and Broadcast
-schedules, against the oracle.
+"""The sliced form of the AllReduce, ReduceScatter, AllGather, Broadcast,
+Scatter, Gather and Reduce schedules, against the oracle.
 
 In the sliced form (vc_set_slice_limit) one launch over the whole GPU runs
 every step of the plan, each thread carrying its 16-byte group of every rank
@@ -12,8 +12,9 @@ the C++ oracle's simulation of the same schedule bit for bit, and the launch
 trace must show one sliced launch for the call.  Also: calls that do not
 qualify (an 8-rank 16-bit Ring whose fp32 partial sums take more than 16
 MiB per rank and alternate between two chunk slots, unaligned pointers,
-single-step plans, other collectives) take the other forms and stay exact;
-the default size limit; canary bands around every buffer.
+single-step plans, the AllToAlls) take the other forms and stay exact; the
+default size limit; a sliced call captured in a CUDA graph; canary bands
+around every buffer.
 """
 import numpy as np
 import pytest
