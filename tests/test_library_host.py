@@ -114,6 +114,20 @@ def test_invalid_arguments_rejected_on_host():
     assert L.vc_allgather(good, ag_inplace, 4, 16, F32, RING, None) == vc.binding.VC_ERR_INVALID_ARG
     # zero count is a no-op success
     assert L.vc_allreduce(good, outs, 4, 0, F32, SUM, RING, None) == vc.binding.VC_SUCCESS
+    # counts whose byte sizes overflow: refused by the calls and by every host-side description of them
+    huge = 1 << 62
+    assert L.vc_allgather(good, outs, 4, huge, F32, RING, None) == vc.binding.VC_ERR_INVALID_ARG
+    for fn in (lambda: vc.vc_plan_describe("allgather", "ring", 4, huge, "f32"),
+               lambda: vc.vc_plan_form("allgather", "ring", 4, huge, "f32"),
+               lambda: vc.vc_select_algo("allgather", 4, huge, "f32")):
+        with pytest.raises(vc.VCError) as e:
+            fn()
+        assert e.value.status == vc.binding.VC_ERR_INVALID_ARG and "too large" in str(e.value)
+    # an algorithm the collective does not define is reported first, at any size
+    with pytest.raises(vc.VCError) as e:
+        vc.vc_plan_form("allgather", "bruck", 4, huge, "f32")
+    assert e.value.status == vc.binding.VC_ERR_UNSUPPORTED
+    assert vc.vc_plan_form("allgather", "ring", 4, 1 << 40, "f32") == ("steps", 3, False)
 
 
 # ----------------------------------------------------------------------------
