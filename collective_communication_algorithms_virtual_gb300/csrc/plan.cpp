@@ -766,6 +766,8 @@ class Builder {
 
 }  // namespace
 
+int64_t count_limit(int nranks) { return INT64_MAX / 16 / (int64_t(nranks) * nranks); }
+
 PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   auto bad = [&](PlanStatus s, const char* msg) {
     if (why) *why = msg;
@@ -797,9 +799,7 @@ PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why) {
   }
   if (a.coll == Coll::Broadcast && (a.algo == Algo::PipeChain || a.algo == Algo::PipeTree)) ok = true;
   if (!ok) return bad(PlanStatus::Unsupported, "algorithm not defined for this collective");
-  // every byte offset and size of the plan (N x count elements of up to 8
-  // bytes at most) fits int64, as the calls check before building
-  if (a.count > (INT64_MAX / 8) / a.nranks) return bad(PlanStatus::Invalid, "count too large");
+  if (a.count > count_limit(a.nranks)) return bad(PlanStatus::Invalid, "count too large");
   Builder b(a);
   b.build();
   *out = b.take();

@@ -87,7 +87,13 @@ struct PlanArgs {
 
 enum class PlanStatus { Ok, Invalid, Unsupported };
 
-// Builds the plan; on failure `why` says what is wrong.
+// The largest count a plan for `nranks` ranks takes: every byte offset and
+// size in it then fits int64 (an AllToAll's working buffers, the largest,
+// hold 2 N x N x count elements of 4 bytes).
+int64_t count_limit(int nranks);
+
+// Builds the plan; on failure `why` says what is wrong (counts above
+// count_limit are Invalid).
 PlanStatus build_plan(const PlanArgs& a, Plan* out, std::string* why);
 
 // Algorithmic bytes of a plan (every operand read or written once) and the

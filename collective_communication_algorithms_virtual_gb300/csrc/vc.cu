@@ -1476,7 +1476,7 @@ vc_status_t run(const Call& c) {
   if (c.coll == Coll::ReduceScatter || c.coll == Coll::Scatter) send_elems = c.count * N;
   if (c.coll == Coll::AllGather || c.coll == Coll::Gather) recv_elems = c.count * N;
   if (c.coll == Coll::AllToAll) send_elems = recv_elems = c.count * N;
-  if (c.count > (INT64_MAX / 8) / N) return fail(VC_ERR_INVALID_ARG, "count too large");
+  if (c.count > count_limit(N)) return fail(VC_ERR_INVALID_ARG, "count too large");
   const int64_t sbytes = send_elems * es, rbytes = recv_elems * es;
 
   std::vector<const void*> sends;

@@ -29,8 +29,9 @@
  *    aligned the vector path runs; otherwise a slower element-wise path.
  *  - Errors are returned, never raised: VC_ERR_INVALID_ARG (null pointer,
  *    nranks outside [1, VC_MAX_RANKS], root outside [0, nranks), overlapping
- *    buffers, size overflow), VC_ERR_UNSUPPORTED (an algorithm that is not
- *    defined for the collective or the rank count),
+ *    buffers, a count above INT64_MAX / (16 nranks^2), beyond which some
+ *    schedule's sizes would overflow), VC_ERR_UNSUPPORTED (an algorithm
+ *    that is not defined for the collective or the rank count),
  *    VC_ERR_NOMEM (scratch allocation failed), VC_ERR_CUDA (a CUDA call or
  *    launch failed; vc_last_error() has the text).  On any error nothing has
  *    been enqueued, except for VC_ERR_CUDA from a launch after earlier steps.

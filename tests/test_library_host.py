@@ -299,3 +299,30 @@ def test_step_merging_keeps_the_described_steps():
                 assert vc.vc_plan_describe("alltoall", "pairwise", N, 64, "bf16")[2] == N
     finally:
         vc.vc_set_merge_steps(old)
+
+
+@pytest.mark.parametrize("N", [2, 5, 8, 64])
+def test_plans_at_the_count_limit_stay_in_their_buffers(N):
+    """At the largest count a plan takes (2 N x N x count x 4 bytes within
+    int64) every operand of every schedule lies inside its buffer, scratch
+    included, with no offset or size wrapped; one more element is refused."""
+    limit = (2 ** 63 - 1) // 16 // (N * N)
+    colls = {"allreduce": ("fused", "ring", "rhd", "dbt", "mesh", "ring_hop"),
+             "reduce_scatter": ("fused", "ring"), "allgather": ("fused", "ring"),
+             "broadcast": ("fused", "binomial", "scatter_allgather", "pipe_chain", "pipe_tree"),
+             "scatter": ("fused", "binomial"), "gather": ("fused", "binomial"),
+             "reduce": ("fused", "binomial"), "alltoall": ("fused", "pairwise", "bruck", "ring")}
+    for coll, algos in colls.items():
+        for algo in algos:
+            for dtype, es in (("f32", 4), ("bf16", 2)):
+                entries, scratch, _ = vc.vc_plan_describe(coll, algo, N, limit, dtype, 0, False, 3)
+                send = limit * (N if coll in ("reduce_scatter", "scatter", "alltoall") else 1) * es
+                recv = limit * (N if coll in ("allgather", "gather", "alltoall") else 1) * es
+                size = {0: send, 1: recv, 2: scratch}
+                for e in entries:
+                    z = {0: 4, 1: 2, 2: 4, 3: 2}[e.dtype]
+                    last = e.byte_off + (e.nb - 1) * e.stride_bytes
+                    assert 0 <= min(e.byte_off, last) and e.n >= 0 and e.nb >= 1, (coll, algo, dtype, e.byte_off)
+                    assert max(e.byte_off, last) + e.n * z <= size[e.buf] < 2 ** 63, (coll, algo, dtype, e.buf)
+                with pytest.raises(vc.VCError):
+                    vc.vc_plan_describe(coll, algo, N, limit + 1, dtype, 0, False, 3)
