@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <cstdio>
@@ -1795,6 +1796,8 @@ VC_EXPORT const char* vc_last_error(void) { return g_last_error.c_str(); }
 VC_EXPORT vc_status_t vc_set_cost_model(vc_cost_policy_t policy, double alpha_s, double beta_bytes_per_s) {
   return entry([&]() -> vc_status_t {
     if (policy != VC_COST_HBM && policy != VC_COST_LINK) return fail(VC_ERR_INVALID_ARG, "unknown cost policy");
+    if (!std::isfinite(alpha_s) || !std::isfinite(beta_bytes_per_s))
+      return fail(VC_ERR_INVALID_ARG, "alpha and beta must be finite");
     CostModel m = default_cost(static_cast<CostPolicy>(static_cast<int>(policy)));
     if (alpha_s > 0) m.alpha = alpha_s;
     if (beta_bytes_per_s > 0) m.beta = beta_bytes_per_s;

@@ -203,8 +203,9 @@ vc_status_t vc_alltoall(const void* const* send, void* const* recv, int nranks, 
  *     Candidates: the pages' algorithms only (no fused).  Defaults: alpha =
  *     5e-6 s, beta = 450e9 B/s, the page's NVLink example.
  *
- * alpha <= 0 or beta <= 0 selects the policy's default.  Ties go to the
- * first candidate in enum order.
+ * alpha <= 0 or beta <= 0 selects the policy's default; a NaN or infinite
+ * alpha or beta returns VC_ERR_INVALID_ARG and leaves the model unchanged.
+ * Ties go to the first candidate in enum order.
  */
 typedef enum { VC_COST_HBM = 0, VC_COST_LINK = 1 } vc_cost_policy_t;
 

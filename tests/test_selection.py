@@ -77,3 +77,16 @@ def test_auto_is_accepted_by_plan_describe():
     vc.vc_set_cost_model("hbm")
     entries, _, nsteps = vc.vc_plan_describe("allreduce", "auto", 8, 1 << 20, "f32")
     assert nsteps == 1  # fused
+
+
+def test_cost_model_refuses_non_finite_constants():
+    """alpha or beta at or below 0 takes the policy's default; NaN or an
+    infinite value is refused and leaves the model as it was."""
+    vc.vc_set_cost_model("link", 2e-6, 300e9)
+    before = vc.vc_get_cost_model()
+    for a, b in ((float("nan"), 1e9), (1e-6, float("nan")), (float("inf"), 1e9), (1e-6, float("-inf"))):
+        with pytest.raises(vc.VCError):
+            vc.vc_set_cost_model("link", a, b)
+        assert vc.vc_get_cost_model() == before
+    vc.vc_set_cost_model("link", 0.0, -1.0)
+    assert vc.vc_get_cost_model() == ("link", 5e-6, 450e9)
