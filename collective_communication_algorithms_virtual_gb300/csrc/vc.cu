@@ -1873,8 +1873,11 @@ vc_status_t describe_plan(vc_coll_t coll, vc_algo_t algo, int nranks, size_t cou
     rc = resolve_auto(&pa);
     if (rc != VC_SUCCESS) return rc;
   }
-  if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree)
+  if (pa.algo == Algo::PipeChain || pa.algo == Algo::PipeTree) {
+    // as vc_broadcast_pipelined takes it
+    if (nchunks < 0 || nchunks > 1024) return fail(VC_ERR_INVALID_ARG, "nchunks must be in [0, 1024]");
     pa.nchunks = nchunks > 0 ? nchunks : default_chunks(pa.algo, nranks, pa.count, pa.dt, current_cost());
+  }
   std::string why;
   const PlanStatus ps = build_plan(pa, plan, &why);
   if (ps != PlanStatus::Ok) return plan_status(ps, why);

@@ -350,6 +350,12 @@ def test_library_form_of_degenerate_calls_and_bad_arguments():
     with pytest.raises(VCError) as e:
         vc.vc_plan_form("reduce_scatter", "rhd", 4, 10, "f32")
     assert e.value.status == VC_ERR_UNSUPPORTED
+    # chunk counts as vc_broadcast_pipelined takes them: 0 (the optimum) to 1024; ignored by other algorithms
+    for k in (-1, 1025):
+        with pytest.raises(VCError) as e:
+            vc.vc_plan_form("broadcast", "pipe_tree", 8, 4096, "f32", 0, False, k)
+        assert e.value.status == VC_ERR_INVALID_ARG
+    assert vc.vc_plan_form("broadcast", "binomial", 8, 4096, "f32", 0, False, -1)[0] == "sliced"
     # a null output through the C ABI itself
     L = vc.lib()
     i = ctypes.c_int()
