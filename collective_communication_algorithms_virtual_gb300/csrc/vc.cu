@@ -1869,6 +1869,9 @@ vc_status_t describe_plan(vc_coll_t coll, vc_algo_t algo, int nranks, size_t cou
   pa.count = static_cast<int64_t>(count);
   pa.root = root;
   pa.inplace = inplace != 0;
+  // as the calls allow it: AllReduce, and a Broadcast or Reduce at its root
+  if (pa.inplace && pa.coll != Coll::AllReduce && pa.coll != Coll::Broadcast && pa.coll != Coll::Reduce)
+    return fail(VC_ERR_INVALID_ARG, "in place only for AllReduce, Broadcast and Reduce");
   if (is_auto) {
     rc = resolve_auto(&pa);
     if (rc != VC_SUCCESS) return rc;

@@ -279,7 +279,11 @@ double vc_busbw_factor(vc_coll_t coll, int nranks);
  * Schedule introspection (host only; no CUDA call, usable without a GPU).
  *
  * Builds the step plan a call with these arguments would execute (nchunks:
- * as vc_broadcast_pipelined; ignored by other algorithms) and writes
+ * as vc_broadcast_pipelined, ignored by other algorithms; inplace: 1 for an
+ * AllReduce with send[r] == recv[r], a Broadcast with send_root ==
+ * recv[root] or a Reduce with recv_root == send[root], and
+ * VC_ERR_INVALID_ARG for the other collectives, which do not run in place)
+ * and writes
  * one entry per operand of every operation.  An operation reads its sources
  * in the listed order (`pos`), combines them left to right with the step's
  * op (reduction steps) or copies its single source (copy steps), and writes

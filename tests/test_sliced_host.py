@@ -356,6 +356,13 @@ def test_library_form_of_degenerate_calls_and_bad_arguments():
             vc.vc_plan_form("broadcast", "pipe_tree", 8, 4096, "f32", 0, False, k)
         assert e.value.status == VC_ERR_INVALID_ARG
     assert vc.vc_plan_form("broadcast", "binomial", 8, 4096, "f32", 0, False, -1)[0] == "sliced"
+    # in place as the calls allow it: AllReduce, Broadcast and Reduce only
+    for coll, algo in (("allgather", "ring"), ("reduce_scatter", "ring"), ("scatter", "binomial"),
+                       ("gather", "binomial"), ("alltoall", "pairwise")):
+        with pytest.raises(VCError) as e:
+            vc.vc_plan_form(coll, algo, 8, 64, "f32", 0, True)
+        assert e.value.status == VC_ERR_INVALID_ARG, coll
+    assert vc.vc_plan_form("reduce", "binomial", 8, 1000, "f32", 3, True)[0] == "cluster"
     # a null output through the C ABI itself
     L = vc.lib()
     i = ctypes.c_int()
