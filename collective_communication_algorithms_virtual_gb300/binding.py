@@ -4,6 +4,13 @@ Argument marshalling only: tensors become device pointers, counts and enum
 codes; every step of every collective runs in libvcoll.so.  The functions
 keep the C names.  There is no fallback: if the library is not built, or a
 call fails, an exception is raised.
+
+The C ABI takes bare pointers and counts and cannot see a buffer's size, so
+before each call every tensor is checked to hold at least the elements the
+call reads or writes there, contiguous, of the call's dtype, on one CUDA
+device; anything else raises VCError(VC_ERR_INVALID_ARG) before the library
+is called.  The checks cost about 5 us of host time for 16 tensors;
+VC_CHECK_TENSORS=0 in the environment skips them.
 """
 from __future__ import annotations
 
@@ -197,8 +204,32 @@ def _stream_handle(stream, like) -> int:
     return int(stream.cuda_stream)
 
 
-def _ptrs(ts) -> list[int]:
-    return [t.data_ptr() for t in ts]
+CHECK_TENSORS = os.environ.get("VC_CHECK_TENSORS", "1") != "0"
+
+
+def _checked(ts, need: int, like) -> list[int]:
+    """Pointers of `ts`, each tensor checked to hold at least `need`
+    contiguous elements of `like`'s dtype on `like`'s CUDA device."""
+    if not CHECK_TENSORS:
+        return [t.data_ptr() for t in ts]
+    dt, dev = like.dtype, like.get_device()
+    if dev < 0:
+        raise VCError(VC_ERR_INVALID_ARG, f"tensors must be on a CUDA device, not {like.device}")
+    out = []
+    for t in ts:
+        if t.numel() < need or t.dtype is not dt or t.get_device() != dev or not t.is_contiguous():
+            raise VCError(VC_ERR_INVALID_ARG,
+                          f"each tensor must be contiguous {dt} on cuda:{dev} with at least {need} elements, "
+                          f"not {tuple(t.shape)} {t.dtype} on {t.device}"
+                          + ("" if t.is_contiguous() else " (not contiguous)"))
+        out.append(t.data_ptr())
+    return out
+
+
+def _ranks(ts, N: int, what: str):
+    if len(ts) != N:
+        raise VCError(VC_ERR_INVALID_ARG, f"{what}: {len(ts)} tensors for {N} ranks")
+    return ts
 
 
 def _code(table: dict, key) -> int:
@@ -212,70 +243,83 @@ def _code(table: dict, key) -> int:
 def vc_allreduce(send, recv, algo="fused", op="sum", stream=None) -> None:
     """recv[r] = sum over ranks of send[q]; ``send[r] is recv[r]`` allowed."""
     N = len(send)
-    check(lib().vc_allreduce(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, send[0].numel(),
-                             _dtype_code(send[0]), _code(OPS, op), _code(ALGOS, algo),
-                             _stream_handle(stream, send[0])))
+    n = send[0].numel()
+    sp, rp = _checked(send, n, send[0]), _checked(_ranks(recv, N, "recv"), n, send[0])
+    check(lib().vc_allreduce(_ptr_array(sp), _ptr_array(rp), N, n, _dtype_code(send[0]), _code(OPS, op),
+                             _code(ALGOS, algo), _stream_handle(stream, send[0])))
 
 
 def vc_reduce_scatter(send, recv, algo="fused", op="sum", stream=None) -> None:
     """recv[r] = block r of the sum; send[q] holds N blocks of recv[r].numel()."""
     N = len(send)
-    check(lib().vc_reduce_scatter(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, recv[0].numel(),
-                                  _dtype_code(send[0]), _code(OPS, op), _code(ALGOS, algo),
-                                  _stream_handle(stream, send[0])))
+    rc = recv[0].numel()
+    sp, rp = _checked(send, N * rc, send[0]), _checked(_ranks(recv, N, "recv"), rc, send[0])
+    check(lib().vc_reduce_scatter(_ptr_array(sp), _ptr_array(rp), N, rc, _dtype_code(send[0]), _code(OPS, op),
+                                  _code(ALGOS, algo), _stream_handle(stream, send[0])))
 
 
 def vc_allgather(send, recv, algo="fused", stream=None) -> None:
     """recv[r] = concatenation of send[0..N-1]."""
     N = len(send)
-    check(lib().vc_allgather(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, send[0].numel(),
-                             _dtype_code(send[0]), _code(ALGOS, algo), _stream_handle(stream, send[0])))
+    sc = send[0].numel()
+    sp, rp = _checked(send, sc, send[0]), _checked(_ranks(recv, N, "recv"), N * sc, send[0])
+    check(lib().vc_allgather(_ptr_array(sp), _ptr_array(rp), N, sc, _dtype_code(send[0]), _code(ALGOS, algo),
+                             _stream_handle(stream, send[0])))
 
 
 def vc_broadcast(send_root, recv, root=0, algo="fused", stream=None) -> None:
     """recv[r] = send_root for every rank; ``send_root is recv[root]`` allowed."""
     N = len(recv)
-    check(lib().vc_broadcast(ctypes.c_void_p(send_root.data_ptr()), _ptr_array(_ptrs(recv)), N,
-                             recv[0].numel(), _dtype_code(send_root), int(root), _code(ALGOS, algo),
-                             _stream_handle(stream, send_root)))
+    n = recv[0].numel()
+    (sp,), rp = _checked([send_root], n, send_root), _checked(recv, n, send_root)
+    check(lib().vc_broadcast(ctypes.c_void_p(sp), _ptr_array(rp), N, n, _dtype_code(send_root), int(root),
+                             _code(ALGOS, algo), _stream_handle(stream, send_root)))
 
 
 def vc_scatter(send_root, recv, root=0, algo="fused", stream=None) -> None:
     """recv[r] = block r of send_root."""
     N = len(recv)
-    check(lib().vc_scatter(ctypes.c_void_p(send_root.data_ptr()), _ptr_array(_ptrs(recv)), N,
-                           recv[0].numel(), _dtype_code(send_root), int(root), _code(ALGOS, algo),
-                           _stream_handle(stream, send_root)))
+    rc = recv[0].numel()
+    (sp,), rp = _checked([send_root], N * rc, send_root), _checked(recv, rc, send_root)
+    check(lib().vc_scatter(ctypes.c_void_p(sp), _ptr_array(rp), N, rc, _dtype_code(send_root), int(root),
+                           _code(ALGOS, algo), _stream_handle(stream, send_root)))
 
 
 def vc_alltoall(send, recv, algo="fused", stream=None) -> None:
     """recv[j] block i = send[i] block j; every buffer holds N blocks."""
     N = len(send)
-    check(lib().vc_alltoall(_ptr_array(_ptrs(send)), _ptr_array(_ptrs(recv)), N, send[0].numel() // N,
-                            _dtype_code(send[0]), _code(ALGOS, algo), _stream_handle(stream, send[0])))
+    blk = send[0].numel() // N
+    sp, rp = _checked(send, N * blk, send[0]), _checked(_ranks(recv, N, "recv"), N * blk, send[0])
+    check(lib().vc_alltoall(_ptr_array(sp), _ptr_array(rp), N, blk, _dtype_code(send[0]), _code(ALGOS, algo),
+                            _stream_handle(stream, send[0])))
 
 
 def vc_broadcast_pipelined(send_root, recv, root=0, algo="pipe_tree", nchunks=0, stream=None) -> None:
     """Chunked Broadcast; nchunks=0 takes the cost model's optimum."""
     N = len(recv)
-    check(lib().vc_broadcast_pipelined(ctypes.c_void_p(send_root.data_ptr()), _ptr_array(_ptrs(recv)), N,
-                                       recv[0].numel(), _dtype_code(send_root), int(root), _code(ALGOS, algo),
-                                       int(nchunks), _stream_handle(stream, send_root)))
+    n = recv[0].numel()
+    (sp,), rp = _checked([send_root], n, send_root), _checked(recv, n, send_root)
+    check(lib().vc_broadcast_pipelined(ctypes.c_void_p(sp), _ptr_array(rp), N, n, _dtype_code(send_root),
+                                       int(root), _code(ALGOS, algo), int(nchunks),
+                                       _stream_handle(stream, send_root)))
 
 
 def vc_gather(send, recv_root, root=0, algo="fused", stream=None) -> None:
     """recv_root = concatenation of send[0..N-1] (on the root only)."""
     N = len(send)
-    check(lib().vc_gather(_ptr_array(_ptrs(send)), ctypes.c_void_p(recv_root.data_ptr()), N, send[0].numel(),
-                          _dtype_code(send[0]), int(root), _code(ALGOS, algo), _stream_handle(stream, send[0])))
+    sc = send[0].numel()
+    sp, (rp,) = _checked(send, sc, send[0]), _checked([recv_root], N * sc, send[0])
+    check(lib().vc_gather(_ptr_array(sp), ctypes.c_void_p(rp), N, sc, _dtype_code(send[0]), int(root),
+                          _code(ALGOS, algo), _stream_handle(stream, send[0])))
 
 
 def vc_reduce(send, recv_root, root=0, algo="fused", op="sum", stream=None) -> None:
     """recv_root = sum over ranks of send[q]; ``recv_root is send[root]`` allowed."""
     N = len(send)
-    check(lib().vc_reduce(_ptr_array(_ptrs(send)), ctypes.c_void_p(recv_root.data_ptr()), N, send[0].numel(),
-                          _dtype_code(send[0]), _code(OPS, op), int(root), _code(ALGOS, algo),
-                          _stream_handle(stream, send[0])))
+    n = send[0].numel()
+    sp, (rp,) = _checked(send, n, send[0]), _checked([recv_root], n, send[0])
+    check(lib().vc_reduce(_ptr_array(sp), ctypes.c_void_p(rp), N, n, _dtype_code(send[0]), _code(OPS, op),
+                          int(root), _code(ALGOS, algo), _stream_handle(stream, send[0])))
 
 
 def vc_busbw_factor(coll, nranks: int) -> float:
