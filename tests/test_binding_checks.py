@@ -114,3 +114,14 @@ def test_checks_can_be_switched_off(rec, monkeypatch):
     monkeypatch.setattr(b, "CHECK_TENSORS", False)
     b.vc_allreduce(ts(100), ts(99), stream=1)
     assert rec.calls[-1][0] == "vc_allreduce"
+
+
+def test_real_host_tensors_are_refused(rec):
+    """torch's own host tensors (get_device() == -1): refused before the
+    library, which would otherwise hand host pointers to a kernel."""
+    xs = [torch.ones(16) for _ in range(N)]
+    for fn in (lambda: b.vc_allreduce(xs, xs), lambda: b.vc_broadcast(xs[0], xs), lambda: b.vc_alltoall(xs, xs)):
+        with pytest.raises(b.VCError) as e:
+            fn()
+        assert e.value.status == b.VC_ERR_INVALID_ARG and "CUDA" in str(e.value)
+    assert rec.calls == []
